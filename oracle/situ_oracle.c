@@ -1,0 +1,262 @@
+/*
+ * situ_oracle.c -- FP64 CPU oracle for the SiTU-GLU expert feed-forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously-correct statement
+ * of what the GPU library computes.  It is built into its own shared object and
+ * may be loaded only by the test suite, by the package's smoke check and by the
+ * benchmark's CPU-baseline leg.  The GPU library never links, loads or calls it,
+ * and it shares no code, header, table or helper with the GPU library.
+ *
+ * Sources (web pages on SiTU-GLU, cited by title and section):
+ *   [problem]  "SiTU-GLU" problem page (ai-engineer-exhaustive.pages.dev, Kimi K3):
+ *              "Theory" formula, "Implementation order", "A scalar example",
+ *              "Requirements", "Constraints".
+ *   [bound]    "Kimi K3 - Bound the up branch" (atlas.klimoza.dev): the up-branch
+ *              formula, and its code excerpts of the activation module
+ *              (SituAndMul) and the expert MLP (KimiBlockSparseMLP).
+ *   [dense]    "DenseFFN and SituGLU - Docs - Kimi K3 from Scratch": "SiTU-GLU: one
+ *              split, two softly bounded branches" and "Two linear maps and a
+ *              guarded compiled branch".
+ *   [chapter]  "SiTU-GLU" architecture chapter (mkdocs.reaper.mx, in French): the
+ *              boxed SiTU-GLU equation of "La construction de SiTU-GLU", "Les
+ *              valeurs chez Kimi K3", "La borne de sortie".
+ *
+ * Every value is carried in IEEE double.  Inputs may be given as double, float or
+ * bfloat16 bit patterns; all three convert to double exactly.  Nothing is fused,
+ * blocked or reordered beyond what the definitions state: each projection is a
+ * plain dot product over the input features in ascending order.
+ *
+ * Parity pins: every function here is pinned by the CPU test suite against values
+ * the pages print and against closed forms (worked example, the beta1*beta2 bound,
+ * first-order agreement with SwiGLU, the SwiGLU limit, basis-vector projections,
+ * brute-force recounts of the expert index).  None is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Input element types accepted by the oracle (its own enum; unrelated to the
+ * GPU library's dtype codes). */
+enum { ORACLE_F64 = 0, ORACLE_BF16 = 1, ORACLE_F32 = 2 };
+
+/* Status codes returned by the oracle. */
+enum { ORACLE_OK = 0, ORACLE_BAD_ARG = 1, ORACLE_BAD_INDEX = 2 };
+
+/* bfloat16 is the upper half of an IEEE binary32 pattern. */
+static double oracle_bf16_to_double(uint16_t v) {
+  uint32_t bits = ((uint32_t)v) << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+static double oracle_load(const void* p, int dt, int64_t i) {
+  if (dt == ORACLE_F64) return ((const double*)p)[i];
+  if (dt == ORACLE_F32) return (double)((const float*)p)[i];
+  return oracle_bf16_to_double(((const uint16_t*)p)[i]);
+}
+
+static int oracle_dtype_ok(int dt) {
+  return dt == ORACLE_F64 || dt == ORACLE_BF16 || dt == ORACLE_F32;
+}
+
+/* Soft cap beta * tanh(x / beta): divide by the cap, take tanh, multiply back
+ * ([problem] "Implementation order", second bullet; "Why scaled tanh is
+ * useful").  A cap of zero or below stands for "no cap" and returns x unchanged,
+ * the behaviour of the activation module when its linear_beta is unset ([bound]
+ * code excerpt of SituAndMul). */
+double oracle_softcap(double x, double beta) {
+  if (!(beta > 0.0)) return x;
+  return beta * tanh(x / beta);
+}
+
+/* Logistic sigmoid 1 / (1 + exp(-g)).  For g < 0 the same value is written as
+ * exp(g) / (1 + exp(g)) so that exp never overflows. */
+double oracle_sigmoid(double g) {
+  if (g >= 0.0) return 1.0 / (1.0 + exp(-g));
+  double e = exp(g);
+  return e / (1.0 + e);
+}
+
+/* Gate branch a = beta1 * tanh(g / beta1) * sigmoid(g).  The sigmoid takes the
+ * UNCAPPED gate projection ([problem] "Implementation order", third bullet). */
+double oracle_gate_branch(double g, double beta) {
+  return oracle_softcap(g, beta) * oracle_sigmoid(g);
+}
+
+/* Up branch b = beta2 * tanh(u / beta2) ([bound] page formula; [problem]
+ * "Implementation order", fourth bullet). */
+double oracle_up_branch(double u, double linear_beta) {
+  return oracle_softcap(u, linear_beta);
+}
+
+/* One output coordinate h = a(g) * b(u) ([chapter] boxed SiTU-GLU equation;
+ * [problem] "Implementation order", last bullet). */
+double oracle_situ_pair(double g, double u, double beta, double linear_beta) {
+  return oracle_gate_branch(g, beta) * oracle_up_branch(u, linear_beta);
+}
+
+/* Standalone activation over rows of a packed [rows, 2I] tensor: the first I
+ * columns are the gate projection g, the last I the up projection u ([dense]
+ * "one split, two softly bounded branches": chunk(2) along the last dimension;
+ * [bound] SituAndMul slices at d = width / 2).  out is [rows, I], row-major. */
+int oracle_situ_glu_act(const void* gate_up, int in_dt, double* out, int64_t rows,
+                        int64_t I, double beta, double linear_beta) {
+  if (!oracle_dtype_ok(in_dt) || rows < 0 || I < 0) return ORACLE_BAD_ARG;
+  if (rows > 0 && I > 0 && (gate_up == 0 || out == 0)) return ORACLE_BAD_ARG;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t j = 0; j < I; ++j) {
+      double g = oracle_load(gate_up, in_dt, r * 2 * I + j);
+      double u = oracle_load(gate_up, in_dt, r * 2 * I + I + j);
+      out[r * I + j] = oracle_situ_pair(g, u, beta, linear_beta);
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* The SiTU-GLU feed-forward of one row.  x_row holds M doubles; w_gate_up is
+ * [2I, M] (rows 0..I-1 gate, rows I..2I-1 up), w_down is [M, I]; both use the
+ * [out, in] orientation of a bias-free linear map ([dense] "Two linear maps":
+ * gate_up_proj M -> 2I, down_proj I -> M).  gu is scratch of 2I doubles. */
+static void oracle_ffn_row(const double* x_row, const void* w_gate_up,
+                           const void* w_down, int w_dt, int64_t M, int64_t I,
+                           double beta, double linear_beta, double* gu,
+                           double* h_row, double* y_row) {
+  for (int64_t n = 0; n < 2 * I; ++n) {
+    double s = 0.0;
+    for (int64_t k = 0; k < M; ++k) s += x_row[k] * oracle_load(w_gate_up, w_dt, n * M + k);
+    gu[n] = s;
+  }
+  for (int64_t j = 0; j < I; ++j) h_row[j] = oracle_situ_pair(gu[j], gu[I + j], beta, linear_beta);
+  for (int64_t m = 0; m < M; ++m) {
+    double s = 0.0;
+    for (int64_t j = 0; j < I; ++j) s += h_row[j] * oracle_load(w_down, w_dt, m * I + j);
+    y_row[m] = s;
+  }
+}
+
+/* Dense expert FFN over R rows: gu = x W_gate_up^T, h = SiTU-GLU(gu),
+ * y = h W_down^T, all in FP64 with no rounding of gu or h ([dense] forward:
+ * packed projection, activation, down projection; [bound] KimiBlockSparseMLP
+ * forward, where concatenating the separate gate and up outputs gives the same
+ * packed tensor).  x is [R, M]; h_out ([R, I]) may be NULL; y is [R, M]. */
+int oracle_ffn_forward(const void* x, int x_dt, const void* w_gate_up,
+                       const void* w_down, int w_dt, double* h_out, double* y,
+                       int64_t R, int64_t M, int64_t I, double beta,
+                       double linear_beta) {
+  if (!oracle_dtype_ok(x_dt) || !oracle_dtype_ok(w_dt)) return ORACLE_BAD_ARG;
+  if (R < 0 || M <= 0 || I <= 0) return ORACLE_BAD_ARG;
+  if (R == 0) return ORACLE_OK;
+  if (!x || !w_gate_up || !w_down || !y) return ORACLE_BAD_ARG;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < R; ++r) {
+    double* xr = (double*)malloc(sizeof(double) * (size_t)(M + 3 * I));
+    if (!xr) {
+#pragma omp atomic write
+      bad = 1;
+      continue;
+    }
+    double* gu = xr + M;
+    double* hr = gu + 2 * I;
+    for (int64_t k = 0; k < M; ++k) xr[k] = oracle_load(x, x_dt, r * M + k);
+    oracle_ffn_row(xr, w_gate_up, w_down, w_dt, M, I, beta, linear_beta, gu, hr, y + r * M);
+    if (h_out) memcpy(h_out + r * I, hr, sizeof(double) * (size_t)I);
+    free(xr);
+  }
+  return bad ? ORACLE_BAD_ARG : ORACLE_OK;
+}
+
+/* Expert index: a stable counting sort of the n = T * k_eff flat (token, slot)
+ * routes by expert id.  offsets[e] .. offsets[e+1]-1 are the positions of expert
+ * e's routes in token_index, and within one expert the flat indices ascend.
+ * The pages show no router; variable per-expert row counts are what the expert
+ * FFN is called on ([dense] "a varying number of expert-token rows"). */
+int oracle_moe_build_index(const int32_t* expert_ids, int64_t n, int32_t E,
+                           int32_t* offsets, int32_t* token_index) {
+  if (n < 0 || E <= 0 || !offsets || (n > 0 && (!expert_ids || !token_index)))
+    return ORACLE_BAD_ARG;
+  if (n > INT32_MAX) return ORACLE_BAD_ARG;
+  for (int32_t e = 0; e <= E; ++e) offsets[e] = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    int32_t e = expert_ids[i];
+    if (e < 0 || e >= E) return ORACLE_BAD_INDEX;
+    offsets[e + 1] += 1;
+  }
+  for (int32_t e = 0; e < E; ++e) offsets[e + 1] += offsets[e];
+  int32_t* cursor = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
+  if (!cursor) return ORACLE_BAD_ARG;
+  for (int32_t e = 0; e < E; ++e) cursor[e] = offsets[e];
+  for (int64_t i = 0; i < n; ++i) token_index[cursor[expert_ids[i]]++] = (int32_t)i;
+  free(cursor);
+  return ORACLE_OK;
+}
+
+/* Grouped routed experts: build the expert index, then for every expert e and
+ * every route r in its group, gather the token row x[token_index[r] / k_eff],
+ * run expert e's SiTU-GLU FFN on it and write the result to flat slot
+ * token_index[r] of y ([T * k_eff, M], no combine weights).  Expert weights are
+ * stacked: w_gate_up is [E, 2I, M], w_down is [E, M, I]. */
+int oracle_moe_grouped_forward(const void* x, int x_dt, const int32_t* expert_ids,
+                               const void* w_gate_up, const void* w_down, int w_dt,
+                               double* y, int64_t T, int32_t k_eff, int32_t E,
+                               int64_t M, int64_t I, double beta, double linear_beta) {
+  if (!oracle_dtype_ok(x_dt) || !oracle_dtype_ok(w_dt)) return ORACLE_BAD_ARG;
+  if (T < 0 || k_eff <= 0 || E <= 0 || M <= 0 || I <= 0) return ORACLE_BAD_ARG;
+  int64_t n = T * (int64_t)k_eff;
+  if (n == 0) return ORACLE_OK;
+  if (!x || !expert_ids || !w_gate_up || !w_down || !y) return ORACLE_BAD_ARG;
+  int32_t* offsets = (int32_t*)malloc(sizeof(int32_t) * (size_t)(E + 1));
+  int32_t* token_index = (int32_t*)malloc(sizeof(int32_t) * (size_t)n);
+  if (!offsets || !token_index) {
+    free(offsets);
+    free(token_index);
+    return ORACLE_BAD_ARG;
+  }
+  int st = oracle_moe_build_index(expert_ids, n, E, offsets, token_index);
+  if (st != ORACLE_OK) {
+    free(offsets);
+    free(token_index);
+    return st;
+  }
+  size_t wgu_elems = (size_t)(2 * I * M), wd_elems = (size_t)(M * I);
+  size_t esz = w_dt == ORACLE_F64 ? 8 : (w_dt == ORACLE_F32 ? 4 : 2);
+  int bad = 0;
+  for (int32_t e = 0; e < E; ++e) {
+    const char* wgu_e = (const char*)w_gate_up + (size_t)e * wgu_elems * esz;
+    const char* wd_e = (const char*)w_down + (size_t)e * wd_elems * esz;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = offsets[e]; r < offsets[e + 1]; ++r) {
+      int64_t flat = token_index[r];
+      int64_t t = flat / k_eff;
+      double* xr = (double*)malloc(sizeof(double) * (size_t)(M + 3 * I));
+      if (!xr) {
+#pragma omp atomic write
+        bad = 1;
+        continue;
+      }
+      double* gu = xr + M;
+      double* hr = gu + 2 * I;
+      for (int64_t k = 0; k < M; ++k) xr[k] = oracle_load(x, x_dt, t * M + k);
+      oracle_ffn_row(xr, wgu_e, wd_e, w_dt, M, I, beta, linear_beta, gu, hr, y + flat * M);
+      free(xr);
+    }
+  }
+  free(offsets);
+  free(token_index);
+  return bad ? ORACLE_BAD_ARG : ORACLE_OK;
+}
+
+/* Number of threads the oracle's parallel loops use. */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,339 @@
+"""Pins for the FP64 oracle: checks that tie it to what the SiTU-GLU pages print and
+to closed forms of the mathematics, never to a second copy of its own formula.
+
+Each pin is a function ``pin(o)`` taking an ``oracle.Oracle`` and raising
+AssertionError when the oracle disagrees.  ``test_oracle_pins.py`` runs them on
+the real oracle; ``test_oracle_mutants.py`` runs them on deliberately broken
+builds of the oracle and requires every mistake to be caught by at least one.
+
+Page titles cited below:
+  problem page  "SiTU-GLU" (ai-engineer-exhaustive.pages.dev)
+  chapter       "SiTU-GLU" architecture chapter (mkdocs.reaper.mx, French)
+  docs page     "DenseFFN and SituGLU - Docs - Kimi K3 from Scratch"
+  bound page    "Kimi K3 - Bound the up branch" (atlas.klimoza.dev)
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+B1, B2 = 4.0, 25.0  # chapter, "Les valeurs chez Kimi K3"
+
+
+def load_golden(name: str) -> dict:
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, value, half = line.split()
+            vals[key] = (float(value), float(half))
+    return vals
+
+
+def _close(got, want, half, what):
+    assert abs(got - want) <= half, f"{what}: oracle {got!r}, page prints {want} (+-{half})"
+
+
+# ---------------------------------------------------------------------------
+# Scalar pins
+# ---------------------------------------------------------------------------
+def pin_worked_example(o):
+    """problem page "A scalar example" and chapter "Verification de comprehension"."""
+    gv = load_golden("worked_example.txt")
+    g, u = gv["g"][0], gv["u"][0]
+    b1, b2 = gv["beta"][0], gv["linear_beta"][0]
+    _close(o.softcap(g, b1) / b1, *gv["tanh_half"], "tanh(2/4)")
+    _close(o.sigmoid(g), *gv["sigmoid_two"], "sigmoid(2)")
+    _close(o.gate(g, b1), *gv["gate_branch"], "gate branch at g=2")
+    _close(o.up(u, b2), *gv["up_branch"], "up branch at u=2")
+    _close(o.pair(g, u, b1, b2), *gv["product"], "SiTU-GLU at g=u=2")
+
+
+def pin_swiglu_gate_and_gaps(o):
+    """chapter: SwiGLU's gate at x=2 is 1.762; the caps cost about 8 % on the gate
+    and 0.2 % on the up branch.  A cap of 1e12 reaches the SwiGLU gate."""
+    gv = load_golden("worked_example.txt")
+    _close(o.gate(2.0, 1e12), *gv["swiglu_gate"], "uncapped gate (SwiGLU) at 2")
+    gap_gate = 1.0 - o.gate(2.0, B1) / o.gate(2.0, 1e12)
+    gap_up = 1.0 - o.up(2.0, B2) / 2.0
+    _close(gap_gate, *gv["gate_gap_vs_swiglu"], "relative gate gap")
+    _close(gap_up, *gv["up_gap_vs_linear"], "relative up gap")
+
+
+def pin_bound(o):
+    """chapter "La borne de sortie": |SiTU-GLU| <= beta1*beta2 = 100 for every input;
+    reached at saturation (g -> +inf, |u| -> inf)."""
+    gv = load_golden("worked_example.txt")
+    bound = gv["bound"][0]
+    assert B1 * B2 == bound
+    rng = np.random.default_rng(1234)
+    samples = np.concatenate([
+        rng.normal(0, 3, 2000), rng.normal(0, 1000, 2000),
+        rng.choice([-1, 1], 2000) * 10.0 ** rng.uniform(-30, 30, 2000),
+        np.array([1e4, -1e4, 1e30, -1e30, 0.0, 88.0, -88.0, 1e-30]),
+    ])
+    gs = rng.permutation(samples)
+    us = rng.permutation(samples)
+    for g, u in zip(gs, us):
+        h = o.pair(g, u, B1, B2)
+        assert abs(h) <= bound, f"|h({g}, {u})| = {abs(h)} > {bound}"
+    assert o.pair(1e4, 1e4, B1, B2) == bound
+    assert o.pair(1e4, -1e4, B1, B2) == -bound
+    assert o.pair(-1e4, 1e4, B1, B2) == 0.0
+
+
+def pin_saturation_limits(o):
+    """problem page "Why scaled tanh is useful": beta*tanh(x/beta) -> +-beta for large
+    |x|; the gate cap is beta1 and the up cap is beta2 ("The two caps are
+    independent"); for large positive g the sigmoid goes to one."""
+    assert o.gate(1e4, B1) == B1
+    assert o.up(1e4, B2) == B2 and o.up(-1e4, B2) == -B2
+    assert o.softcap(1e6, 7.0) == 7.0 and o.softcap(-1e6, 7.0) == -7.0
+    # just short of saturation the soft cap is strictly inside (unlike a clamp)
+    assert 0 < o.gate(10.0, B1) < B1 and 0 < o.up(40.0, B2) < B2
+
+
+def pin_negative_tail(o):
+    """problem page: for a large negative gate the sigmoid moves toward zero (Swish's
+    vanishing negative side); chapter "Les proprietes": negative tail kept.
+    Closed form: for g << 0, tanh(g/4) -> -1 and sigmoid(g) = e^g/(1+e^g), so
+    a(g) = -4 e^g (1 + O(e^{g/2}))."""
+    for g, rel in [(-80.0, 1e-12), (-40.0, 1e-7), (-200.0, 1e-12)]:
+        a = o.gate(g, B1)
+        ref = -B1 * math.exp(g)
+        assert a < 0, f"a({g}) = {a} should be negative"
+        assert abs(a / ref - 1) <= rel, f"a({g}) = {a}, closed form {ref}"
+    assert o.sigmoid(-800.0) == 0.0 and o.gate(-1e4, B1) == 0.0
+
+
+def pin_odd_in_up(o):
+    """h is odd in u (the up branch is a scaled tanh, with no sigmoid -- problem page
+    "Common mistakes": sigmoid belongs only to the gate)."""
+    rng = np.random.default_rng(7)
+    for g, u in rng.normal(0, 20, (200, 2)):
+        assert o.pair(g, -u, B1, B2) == -o.pair(g, u, B1, B2)
+        assert o.up(-u, B2) == -o.up(u, B2)
+    assert o.up(-30.0, B2) < -20.0
+
+
+def pin_first_order(o):
+    """chapter: beta*tanh(z/beta) = z + O(z^3/beta^2); SiTU-GLU agrees with SwiGLU to
+    first order at the origin.  Closed form of the ratio to SwiGLU:
+      h / (g sigmoid(g) u) = [1 - g^2/(3 beta1^2) + ...][1 - u^2/(3 beta2^2) + ...]
+                           = 1 - g^2/48 - u^2/1875 + O(4th order)."""
+    rng = np.random.default_rng(11)
+    for g, u in rng.uniform(1e-3, 2e-2, (200, 2)) * rng.choice([-1, 1], (200, 2)):
+        swish = g / (1.0 + math.exp(-g))
+        ratio = o.pair(g, u, B1, B2) / (swish * u)
+        resid = ratio - (1.0 - g * g / 48.0 - u * u / 1875.0)
+        assert abs(resid) <= 1e-9, f"second-order term wrong at g={g}, u={u}: {resid}"
+
+
+def pin_swiglu_limit(o):
+    """chapter "Les proprietes": exactly SwiGLU as beta1, beta2 -> infinity."""
+    rng = np.random.default_rng(3)
+    for g, u in rng.normal(0, 5, (300, 2)):
+        swiglu = g / (1.0 + math.exp(-g)) * u
+        h = o.pair(g, u, 1e8, 1e8)
+        assert abs(h - swiglu) <= 1e-12 * (abs(swiglu) + 1e-300), (g, u, h, swiglu)
+
+
+def pin_caps_independent(o):
+    """problem page "The two caps are independent": swapping or sharing caps must
+    change the result.  At g = u the product is symmetric in the two caps whenever
+    sigmoid(g) factors out, so the check uses g = 2, u = 30."""
+    h = o.pair(2.0, 30.0, B1, B2)
+    assert abs(o.pair(2.0, 30.0, B2, B1) - h) > 1.0
+    assert abs(o.pair(2.0, 30.0, B1, B1) - h) > 1.0
+    assert abs(o.pair(2.0, 30.0, B2, B2) - h) > 1.0
+
+
+def pin_bf16_decode(o):
+    """Input decoding: bfloat16 bit patterns are the top half of binary32."""
+    bits = np.array([[0x4000, 0x4000],  # g = 2, u = 2
+                     [0x3F80, 0xC000],  # 1, -2
+                     [0x0001, 0x3F80],  # 2^-133 (subnormal), 1
+                     [0x4049, 0x7F7F],  # 3.140625, max finite
+                     [0xC2B4, 0x4000]],  # -90, 2
+                    dtype=np.uint16)
+    vals = np.array([[2.0, 2.0], [1.0, -2.0], [2.0 ** -133, 1.0],
+                     [3.140625, 3.3895313892515355e38], [-90.0, 2.0]])
+    got = o.situ_glu_act(bits.reshape(5, 2))
+    want = o.situ_glu_act(vals)
+    assert np.array_equal(got, want), (got, want)
+    gv = load_golden("worked_example.txt")
+    _close(got[0, 0], *gv["product"], "bf16 worked example")
+
+
+def pin_act_split_order(o):
+    """docs page "one split, two softly bounded branches": the first half of the
+    last dimension is the gate, the second half the up projection."""
+    gate_up = np.array([[2.0, 30.0, 30.0, 2.0],
+                        [-5.0, 0.5, 1.0, -7.0]])
+    out = o.situ_glu_act(gate_up)
+    assert out.shape == (2, 2)
+    for r in range(2):
+        for j in range(2):
+            g, u = gate_up[r, j], gate_up[r, 2 + j]
+            assert out[r, j] == o.pair(g, u, B1, B2)
+    # pair(2, 30) and pair(30, 2) differ: the halves are not interchangeable
+    assert abs(out[0, 0] - o.pair(30.0, 2.0)) > 1.0
+    # empty inputs are a no-op
+    assert o.situ_glu_act(np.zeros((0, 8))).shape == (0, 4)
+
+
+# ---------------------------------------------------------------------------
+# FFN pins
+# ---------------------------------------------------------------------------
+def pin_ffn_basis(o):
+    """docs page "Two linear maps": gate_up_proj M -> 2I (rows 0..I-1 gate, I..2I-1
+    up), down_proj I -> M, [out, in] orientation, no bias.  With a one-hot input and
+    a weight that routes the input to gate column c and up column c with value 2,
+    h is zero except h[c] = the worked example (about 3.25), and y = h[c] W_down[:, c]."""
+    gv = load_golden("worked_example.txt")
+    M, I = 6, 4
+    rng = np.random.default_rng(5)
+    wd = rng.normal(size=(M, I))
+    for k in range(M):
+        for c in range(I):
+            x = np.zeros(M)
+            x[k] = 1.0
+            wgu = np.zeros((2 * I, M))
+            wgu[c, k] = 2.0
+            wgu[I + c, k] = 2.0
+            y, h = o.ffn_forward(x[None], wgu, wd, want_h=True)
+            assert np.count_nonzero(h) == 1 and h[0, c] != 0, h
+            _close(h[0, c], *gv["product"], "h at the routed column")
+            assert np.array_equal(y[0], h[0, c] * wd[:, c]), (y, h[0, c] * wd[:, c])
+    # gate 2 / up 30 at column 1: split order decides the value
+    x = np.zeros(M)
+    x[0] = 1.0
+    wgu = np.zeros((2 * I, M))
+    wgu[1, 0] = 2.0
+    wgu[I + 1, 0] = 30.0
+    _, h = o.ffn_forward(x[None], wgu, wd, want_h=True)
+    assert h[0, 1] == o.pair(2.0, 30.0)
+
+
+def pin_ffn_packed_equals_separate(o):
+    """docs page: the packed gate_up_proj is a storage layout, not a coupling of the
+    two projections; bound page, KimiBlockSparseMLP: separate gate (w1) and up (w3)
+    outputs concatenated.  On small-integer data every FP64 sum is exact, so the
+    packed oracle's h must equal the activation of the two separate products
+    exactly, and y must equal h W_down^T to rounding."""
+    rng = np.random.default_rng(9)
+    for (R, M, I) in [(3, 5, 4), (4, 7, 3), (1, 2, 6)]:
+        x = rng.integers(-3, 4, (R, M)).astype(np.float64)
+        wg = rng.integers(-2, 3, (I, M)).astype(np.float64)
+        wu = rng.integers(-2, 3, (I, M)).astype(np.float64)
+        wd = rng.normal(size=(M, I))
+        y, h = o.ffn_forward(x, np.concatenate([wg, wu]), wd, want_h=True)
+        gate_up = np.concatenate([x @ wg.T, x @ wu.T], axis=1)
+        assert np.array_equal(h, o.situ_glu_act(gate_up))
+        np.testing.assert_allclose(y, h @ wd.T, rtol=1e-13, atol=1e-13)
+        assert y.shape == (R, M)
+
+
+def pin_ffn_dtypes(o):
+    """Inputs of any accepted precision decode exactly: float32 and bf16 inputs give
+    the same FFN output as their float64 values."""
+    rng = np.random.default_rng(2)
+    M, I, R = 8, 4, 3
+    x32 = rng.normal(size=(R, M)).astype(np.float32)
+    wgu32 = rng.normal(size=(2 * I, M)).astype(np.float32)
+    wd32 = rng.normal(size=(M, I)).astype(np.float32)
+    y32 = o.ffn_forward(x32, wgu32, wd32)
+    y64 = o.ffn_forward(x32.astype(np.float64), wgu32.astype(np.float64),
+                        wd32.astype(np.float64))
+    assert np.array_equal(y32, y64)
+    # bf16: truncate float32 bits to their upper half
+    tob = lambda a: (a.view(np.uint32) >> 16).astype(np.uint16)
+    frm = lambda b: (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    xb, wgb, wdb = tob(x32), tob(wgu32), tob(wd32)
+    assert np.array_equal(o.ffn_forward(xb, wgb, wdb), o.ffn_forward(frm(xb), frm(wgb), frm(wdb)))
+
+
+# ---------------------------------------------------------------------------
+# Expert index and grouped pins
+# ---------------------------------------------------------------------------
+def pin_build_index(o):
+    """Stable counting sort, checked by brute-force recount: group sizes are the
+    per-expert counts, each group lists exactly that expert's flat routes in
+    ascending order, and empty experts give empty groups."""
+    rng = np.random.default_rng(4)
+    for (n, E) in [(0, 3), (1, 1), (17, 5), (200, 9), (64, 64)]:
+        ids = rng.integers(0, E, n).astype(np.int32)
+        if n > 10:
+            ids[ids == 2] = 3  # force expert 2 empty
+        off, tix = o.moe_build_index(ids, E)
+        assert off[0] == 0 and off[-1] == n
+        for e in range(E):
+            want = np.flatnonzero(ids == e)
+            assert off[e + 1] - off[e] == want.size
+            assert np.array_equal(tix[off[e]:off[e + 1]], want)
+
+
+def pin_grouped_equals_naive(o):
+    """Grouped over experts = one dense FFN per (token, slot) with that slot's expert
+    ("grouped vs naive", docs page "Verification"); the y row of (t, s) is flat
+    index t*k_eff + s; no combine weights."""
+    rng = np.random.default_rng(6)
+    T, k_eff, E, M, I = 5, 3, 4, 6, 4
+    x = rng.normal(size=(T, M))
+    wgu = rng.normal(size=(E, 2 * I, M)) / math.sqrt(M)
+    wd = rng.normal(size=(E, M, I)) / math.sqrt(I)
+    ids = np.stack([rng.choice([0, 1, 3], k_eff, replace=False) for _ in range(T)]).astype(np.int32)
+    y = o.moe_grouped_forward(x, ids, wgu, wd)
+    assert y.shape == (T, k_eff, M)
+    for t in range(T):
+        for s in range(k_eff):
+            want = o.ffn_forward(x[t:t + 1], wgu[ids[t, s]], wd[ids[t, s]])[0]
+            assert np.array_equal(y[t, s], want), (t, s)
+
+
+ALL_PINS = [
+    pin_worked_example,
+    pin_swiglu_gate_and_gaps,
+    pin_bound,
+    pin_saturation_limits,
+    pin_negative_tail,
+    pin_odd_in_up,
+    pin_first_order,
+    pin_swiglu_limit,
+    pin_caps_independent,
+    pin_bf16_decode,
+    pin_act_split_order,
+    pin_ffn_basis,
+    pin_ffn_packed_equals_separate,
+    pin_ffn_dtypes,
+    pin_build_index,
+    pin_grouped_equals_naive,
+]
+
+
+def run_all(o) -> list:
+    """Run every pin; return the names of those that fail (any exception)."""
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin(o)
+        except Exception:
+            failed.append(pin.__name__)
+    return failed
+
+
+if __name__ == "__main__":
+    # Child-process entry used by the mutation tests: a planted mistake may
+    # corrupt memory, so each broken build runs in a process of its own.
+    import json
+    import sys
+
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    from oracle import Oracle, load
+
+    print("PINS_FAILED " + json.dumps(run_all(Oracle(load(sys.argv[1])))), flush=True)
