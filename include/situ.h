@@ -1,0 +1,250 @@
+/*
+ * situ.h -- C ABI of libsitu, the GB300 (sm_103a) SiTU-GLU expert feed-forward.
+ *
+ * SiTU-GLU (Sigmoid-Tanh-Unit GLU) is the activation of every feed-forward
+ * network of Kimi K3.  For a gate projection g and an up projection u,
+ *
+ *     h = [beta1 * tanh(g / beta1) * sigmoid(g)] * [beta2 * tanh(u / beta2)],
+ *
+ * with beta1 = 4 and beta2 = 25 in Kimi K3, so that |h| <= beta1 * beta2 = 100.
+ * Sources, by page title and section:
+ *   - "SiTU-GLU" problem page (ai-engineer-exhaustive.pages.dev): "Theory",
+ *     "Implementation order", "Requirements", "Constraints", "Starter Code";
+ *   - "Kimi K3 - Bound the up branch" (atlas.klimoza.dev): the up-branch formula
+ *     and the expert MLP / activation-module code excerpts;
+ *   - "DenseFFN and SituGLU - Docs - Kimi K3 from Scratch": the packed
+ *     gate_up_proj (M -> 2I) and down_proj (I -> M), FP32 activation math, cast
+ *     back to the input dtype;
+ *   - "SiTU-GLU" architecture chapter (mkdocs.reaper.mx): the boxed equation, the
+ *     beta values and the bound.
+ *
+ * Conventions shared by every call:
+ *   - Every pointer named as device memory must be a CUDA device pointer on the
+ *     current device.  The caller allocates and owns every buffer; the library
+ *     keeps only a per-device status word.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t, NULL for the legacy
+ *     default stream).  A non-OK return means nothing was launched.  Device-side
+ *     failures (a bounded wait that gave up, a route index out of range) are
+ *     recorded in the per-device status word: read them with
+ *     situ_device_status() after synchronising the stream.
+ *   - Inputs are never written ("Do not mutate any input tensor", problem page,
+ *     "Requirements").  An output that overlaps an input returns SITU_ERR_ALIAS.
+ *   - Both caps must be finite and > 0 ("Both cap values are positive", problem
+ *     page, "Constraints"); otherwise SITU_ERR_ARG.
+ *   - The output dtype equals the input dtype ("Preserve the floating-point dtype",
+ *     problem page, "Requirements").  Activation math is FP32 in every path.
+ *   - Matrices are row-major.  Weights use the [out, in] orientation of a
+ *     bias-free linear layer: W_gate_up is [2I, M] with rows 0..I-1 the gate
+ *     projection and rows I..2I-1 the up projection; W_down is [M, I].
+ *   - Zero rows is a valid no-op.
+ */
+#ifndef SITU_H
+#define SITU_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SITU_ABI_VERSION 1
+
+typedef enum {
+  SITU_BF16 = 0, /* bfloat16 storage, FP32 accumulation and activation math */
+  SITU_F32 = 1   /* float32 storage (small-shape SIMT path) */
+} situ_dtype;
+
+typedef enum {
+  SITU_OK = 0,
+  SITU_ERR_ARG = 1,         /* bad size, NULL pointer, bad cap, bad dtype */
+  SITU_ERR_ALIGN = 2,       /* a pointer lacks the alignment the kernel requires */
+  SITU_ERR_ALIAS = 3,       /* an output overlaps an input */
+  SITU_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
+  SITU_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (device status) */
+  SITU_ERR_UNSUPPORTED = 6, /* shape/dtype combination the kernels do not cover */
+  SITU_ERR_INDEX = 7,       /* expert id, route index or expert offsets invalid */
+  SITU_ERR_WORKSPACE = 8    /* workspace NULL, too small or misaligned */
+} situ_status;
+
+/* ABI version of the loaded library (SITU_ABI_VERSION). */
+int situ_abi_version(void);
+
+/* Static, NUL-terminated name of a status code. */
+const char* situ_status_string(situ_status s);
+
+/* Text of the last CUDA error seen by this host thread inside the library
+ * ("" if none).  Static storage per thread; valid until the next call. */
+const char* situ_last_cuda_error(void);
+
+/* Device-side status of the current device: SITU_OK, or the first failure a
+ * kernel recorded since the last clear (SITU_ERR_TIMEOUT, SITU_ERR_INDEX).
+ * Synchronous: call it after synchronising the streams the kernels ran on.
+ * clear != 0 resets the word to SITU_OK. */
+situ_status situ_device_status(int clear);
+
+/* -------------------------------------------------------------------------
+ * situ_glu_act -- standalone SiTU-GLU activation.
+ *
+ * Operation (problem page "Implementation order"; docs page "SiTU-GLU: one split,
+ * two softly bounded branches"; bound page, SituAndMul excerpt): for every row r
+ * and column j < I, with g = gate_up[r, j] and u = gate_up[r, I + j],
+ *   out[r, j] = dtype( beta * tanh(g / beta) * sigmoid(g)
+ *                      * linear_beta * tanh(u / linear_beta) ).
+ *
+ *   gate_up  device, [rows, 2I] of `dt`, row-major, read only.
+ *   out      device, [rows, I] of `dt`, row-major, written; must not overlap
+ *            gate_up.
+ *   rows     >= 0; leading dimensions flattened by the caller.
+ *   I        >= 1 (half the width of gate_up).
+ *   beta, linear_beta   gate and up caps, finite and > 0.
+ * Rows whose start is 16-byte aligned (bf16: I % 8 == 0, f32: I % 4 == 0, and
+ * 16-byte aligned base pointers) take the 128-bit vector path; other shapes take
+ * a scalar path, never an error.  |out| <= beta * linear_beta holds exactly.
+ * Errors: SITU_ERR_ARG, SITU_ERR_ALIAS, SITU_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+situ_status situ_glu_act(const void* gate_up, void* out, int64_t rows, int64_t I,
+                         float beta, float linear_beta, situ_dtype dt, void* stream);
+
+/* -------------------------------------------------------------------------
+ * situ_ffn_forward -- dense SiTU-GLU feed-forward (one expert, or a dense layer).
+ *
+ * Operation (docs page "Two linear maps and a guarded compiled branch": packed
+ * gate_up_proj M -> 2I, activation, down_proj I -> M; bound page,
+ * KimiBlockSparseMLP forward):
+ *   gu = x W_gate_up^T            (FP32 accumulation, kept on chip for bf16)
+ *   h  = dtype(SiTU-GLU(gu[:, :I], gu[:, I:]))   (FP32 math, as situ_glu_act)
+ *   y  = dtype(h W_down^T)        (FP32 accumulation)
+ * For bf16 the gate_up product and the activation run in one tcgen05 GEMM whose
+ * epilogue applies SiTU-GLU to the FP32 accumulators, so the [R, 2I] tensor never
+ * reaches memory; h ([R, I], bf16) is written to the workspace and read back by a
+ * second tcgen05 GEMM.
+ *
+ *   x          device, [R, M] of `dt`.
+ *   W_gate_up  device, [2I, M] of `dt`.
+ *   W_down     device, [M, I] of `dt`.
+ *   y          device, [R, M] of `dt`, written; must not overlap any input or the
+ *              workspace.
+ *   workspace  device, >= situ_ffn_workspace_size(R, M, I, dt) bytes, 256-byte
+ *              aligned; its contents are overwritten (h lives there).
+ *   R >= 0, M >= 1, I >= 1.  bf16 requires M % 8 == 0, I % 8 == 0 and 16-byte
+ *   aligned x, W_gate_up, W_down and y (tensor-memory-access rules); otherwise
+ *   SITU_ERR_UNSUPPORTED / SITU_ERR_ALIGN.  f32 accepts any shape.
+ * Errors: SITU_ERR_ARG, SITU_ERR_ALIGN, SITU_ERR_ALIAS, SITU_ERR_WORKSPACE,
+ *         SITU_ERR_UNSUPPORTED, SITU_ERR_CUDA; SITU_ERR_TIMEOUT on the device.
+ * ------------------------------------------------------------------------- */
+size_t situ_ffn_workspace_size(int64_t R, int64_t M, int64_t I, situ_dtype dt);
+
+situ_status situ_ffn_forward(const void* x, const void* W_gate_up, const void* W_down,
+                             void* y, void* workspace, size_t workspace_bytes,
+                             int64_t R, int64_t M, int64_t I, float beta,
+                             float linear_beta, situ_dtype dt, void* stream);
+
+/* -------------------------------------------------------------------------
+ * situ_ffn_gate_up -- the first half of situ_ffn_forward on its own:
+ *   h = dtype(SiTU-GLU(x W_gate_up^T))          h: device, [R, I] of `dt`
+ * (docs page "Two linear maps": packed gate_up_proj followed by the activation;
+ * for bf16 one tcgen05 GEMM with the activation in its epilogue).  Arguments,
+ * shape and alignment rules as situ_ffn_forward; h must not overlap the inputs.
+ * Errors: SITU_ERR_ARG, SITU_ERR_ALIGN, SITU_ERR_ALIAS, SITU_ERR_UNSUPPORTED,
+ *         SITU_ERR_CUDA; SITU_ERR_TIMEOUT on the device.
+ * ------------------------------------------------------------------------- */
+situ_status situ_ffn_gate_up(const void* x, const void* W_gate_up, void* h, int64_t R,
+                             int64_t M, int64_t I, float beta, float linear_beta,
+                             situ_dtype dt, void* stream);
+
+/* -------------------------------------------------------------------------
+ * situ_ffn_down -- the second half of situ_ffn_forward on its own:
+ *   y = dtype(h W_down^T)                        y: device, [R, M] of `dt`
+ * (docs page "Two linear maps": down_proj I -> M, no bias).  h is [R, I], W_down
+ * [M, I]; bf16 needs M % 8 == 0, I % 8 == 0 and 16-byte aligned pointers.
+ * Errors: SITU_ERR_ARG, SITU_ERR_ALIGN, SITU_ERR_ALIAS, SITU_ERR_UNSUPPORTED,
+ *         SITU_ERR_CUDA; SITU_ERR_TIMEOUT on the device.
+ * ------------------------------------------------------------------------- */
+situ_status situ_ffn_down(const void* h, const void* W_down, void* y, int64_t R, int64_t M,
+                          int64_t I, situ_dtype dt, void* stream);
+
+/* -------------------------------------------------------------------------
+ * situ_moe_build_index -- expert index of a routed batch.
+ *
+ * Operation: a stable counting sort of the n_routes = T * k_eff flat routes
+ * (route t*k_eff + s is slot s of token t) by expert id.  After the call,
+ * expert_offsets[e] .. expert_offsets[e+1]-1 are the positions in token_index of
+ * expert e's routes, listed in ascending flat order.  The pages call the expert
+ * FFN on a varying number of expert-token rows (docs page, "Two linear maps and
+ * a guarded compiled branch"); this builds those row groups.
+ *
+ *   expert_ids      device, [n_routes] int32, each in [0, E).
+ *   expert_offsets  device, [E + 1] int32, written.
+ *   token_index     device, [n_routes] int32, written.
+ *   workspace       device, >= situ_moe_index_workspace_size(n_routes, E) bytes.
+ *   0 <= n_routes < 2^31, 1 <= E <= 16384.
+ * An id outside [0, E) records SITU_ERR_INDEX in the device status and that route
+ * is dropped (expert_offsets[E] is then < n_routes).
+ * Errors: SITU_ERR_ARG, SITU_ERR_ALIAS, SITU_ERR_WORKSPACE, SITU_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+size_t situ_moe_index_workspace_size(int64_t n_routes, int32_t E);
+
+situ_status situ_moe_build_index(const int32_t* expert_ids, int32_t* expert_offsets,
+                                 int32_t* token_index, void* workspace,
+                                 size_t workspace_bytes, int64_t n_routes, int32_t E,
+                                 void* stream);
+
+/* -------------------------------------------------------------------------
+ * situ_moe_grouped_forward -- SiTU-GLU experts over variable row groups.
+ *
+ * Operation: for every expert e and every position r in
+ * [expert_offsets[e], expert_offsets[e+1]), with flat = token_index[r] and token
+ * t = flat / k_eff,
+ *   y[flat, :] = SiTU-GLU FFN of expert e applied to x[t, :]
+ * (the dense operation of situ_ffn_forward with expert e's weights).  Each routed
+ * and shared expert of Kimi K3 is such an FFN ("SiTU-GLU" chapter, "Ou SiTU-GLU
+ * est utilise"; bound page, "Direct evidence": each routed expert is its own
+ * gated MLP).  There are no combine weights: the output has one row per
+ * (token, slot), shape [T, k_eff, M].  Shared experts are extra experts whose
+ * groups hold every token.
+ *
+ *   x               device, [T, M] of `dt` (bf16 only).
+ *   expert_offsets  device, [E + 1] int32: offsets[0] = 0, non-decreasing,
+ *                   offsets[E] = R = T * k_eff.
+ *   token_index     device, [R] int32, a permutation of 0..R-1 (as written by
+ *                   situ_moe_build_index).
+ *   W_gate_up       device, [E, 2I, M] of `dt`: the experts' packed gate_up
+ *                   weights stacked in one allocation.
+ *   W_down          device, [E, M, I] of `dt`, stacked likewise.
+ *   y               device, [T * k_eff, M] of `dt`; every row listed in
+ *                   token_index is written.
+ *   workspace       device, >= situ_moe_workspace_size(T * k_eff, E, M, I, dt)
+ *                   bytes, 256-byte aligned.
+ *   M % 8 == 0, I % 8 == 0, 16-byte aligned pointers.
+ * Offsets that are not monotone or do not end at R record SITU_ERR_INDEX in the
+ * device status and the call writes nothing.
+ * Errors: SITU_ERR_ARG, SITU_ERR_ALIGN, SITU_ERR_ALIAS, SITU_ERR_WORKSPACE,
+ *         SITU_ERR_UNSUPPORTED, SITU_ERR_CUDA; SITU_ERR_TIMEOUT / SITU_ERR_INDEX
+ *         on the device.
+ * ------------------------------------------------------------------------- */
+size_t situ_moe_workspace_size(int64_t R, int32_t E, int64_t M, int64_t I, situ_dtype dt);
+
+situ_status situ_moe_grouped_forward(const void* x, const int32_t* expert_offsets,
+                                     const int32_t* token_index, const void* W_gate_up,
+                                     const void* W_down, void* y, void* workspace,
+                                     size_t workspace_bytes, int64_t T, int32_t k_eff,
+                                     int32_t E, int64_t M, int64_t I, float beta,
+                                     float linear_beta, situ_dtype dt, void* stream);
+
+/* -------------------------------------------------------------------------
+ * situ_selftest_bounded_wait -- failure-detection self test (no counterpart on
+ * the pages).  Launches one block that waits on a shared-memory barrier nothing
+ * ever completes, with a wait limit of `limit_us` microseconds (1..1000000).
+ * The wait gives up, records SITU_ERR_TIMEOUT in the device status and the
+ * kernel returns normally, leaving the context usable.  This is the same bounded
+ * wait every pipelined kernel of the library uses.
+ * Errors: SITU_ERR_ARG, SITU_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+situ_status situ_selftest_bounded_wait(uint32_t limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SITU_H */

@@ -1,0 +1,21 @@
+"""SiTU-GLU expert feed-forward on GB300 (sm_103a).
+
+Hand-written CUDA kernels behind a C ABI (``include/situ.h``, ``libsitu.so``):
+  * ``situ_glu_act``              standalone activation (memory bound)
+  * ``situ_ffn_forward``          dense FFN: tcgen05 gate_up GEMM with the
+                                  activation in its epilogue, tcgen05 down GEMM
+  * ``situ_moe_build_index``      stable expert index of routed tokens
+  * ``situ_moe_grouped_forward``  the FFN grouped over experts
+This package is the thin PyTorch binding over that ABI.
+"""
+from .api import (SituError, device_status, ffn_workspace_bytes, moe_workspace_bytes,
+                  selftest_bounded_wait, situ_ffn_down, situ_ffn_forward, situ_ffn_gate_up,
+                  situ_glu_act,
+                  situ_moe_build_index, situ_moe_grouped_forward)
+
+__all__ = [
+    "SituError", "situ_glu_act", "situ_ffn_forward", "situ_ffn_gate_up", "situ_ffn_down",
+    "situ_moe_build_index",
+    "situ_moe_grouped_forward", "ffn_workspace_bytes", "moe_workspace_bytes",
+    "device_status", "selftest_bounded_wait",
+]

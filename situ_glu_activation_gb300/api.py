@@ -1,0 +1,236 @@
+"""Python front end of libsitu over PyTorch tensors.
+
+Argument marshalling only: shapes are checked, leading dimensions flattened,
+outputs and workspaces allocated with PyTorch on the input's device, and the
+matching C entry point (include/situ.h) launched on PyTorch's current stream.
+Every step of the computation runs in the library's CUDA kernels; there is no
+CPU or PyTorch fallback, and a missing library raises.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _native
+from ._native import SITU_BF16, SITU_F32, SituError, check
+
+_DTYPES = {torch.bfloat16: SITU_BF16, torch.float32: SITU_F32}
+
+
+def _dt(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}: bfloat16 or float32 expected") from None
+
+
+def _cuda_contig(name: str, t: torch.Tensor) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def situ_glu_act(gate_up: torch.Tensor, beta: float = 4.0, linear_beta: float = 25.0,
+                 out: torch.Tensor | None = None) -> torch.Tensor:
+    """SiTU-GLU of a packed [..., 2I] tensor -> [..., I], same dtype.
+
+    The first half of the last dimension is the gate projection g, the second
+    half the up projection u; out = beta*tanh(g/beta)*sigmoid(g) *
+    linear_beta*tanh(u/linear_beta), computed in FP32 and rounded once.
+    """
+    _cuda_contig("gate_up", gate_up)
+    if gate_up.shape[-1] % 2:
+        raise ValueError("the last dimension of gate_up must be even")
+    I = gate_up.shape[-1] // 2
+    rows = gate_up.numel() // max(gate_up.shape[-1], 1)
+    if out is None:
+        out = torch.empty(*gate_up.shape[:-1], I, dtype=gate_up.dtype, device=gate_up.device)
+    else:
+        _cuda_contig("out", out)
+        if out.shape != (*gate_up.shape[:-1], I) or out.dtype != gate_up.dtype:
+            raise ValueError("out has the wrong shape or dtype")
+    if rows == 0 or I == 0:
+        return out
+    lib = _native.lib()
+    check("situ_glu_act", lib.situ_glu_act(gate_up.data_ptr(), out.data_ptr(), rows, I,
+                                           float(beta), float(linear_beta), _dt(gate_up),
+                                           _stream(gate_up.device)))
+    return out
+
+
+def ffn_workspace_bytes(R: int, M: int, I: int, dtype=torch.bfloat16) -> int:
+    return int(_native.lib().situ_ffn_workspace_size(R, M, I, _DTYPES[dtype]))
+
+
+def situ_ffn_forward(x: torch.Tensor, W_gate_up: torch.Tensor, W_down: torch.Tensor,
+                     beta: float = 4.0, linear_beta: float = 25.0,
+                     y: torch.Tensor | None = None,
+                     workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Dense SiTU-GLU feed-forward: y = (SiTU-GLU(x W_gate_up^T)) W_down^T.
+
+    x [..., M]; W_gate_up [2I, M] (gate rows then up rows); W_down [M, I].
+    """
+    for n, t in (("x", x), ("W_gate_up", W_gate_up), ("W_down", W_down)):
+        _cuda_contig(n, t)
+        if t.dtype != x.dtype:
+            raise TypeError("x and the weights must share a dtype")
+    M = x.shape[-1]
+    I = W_gate_up.shape[0] // 2
+    if W_gate_up.shape != (2 * I, M) or W_down.shape != (M, I):
+        raise ValueError(f"weights {tuple(W_gate_up.shape)}, {tuple(W_down.shape)} do not "
+                         f"match M={M}")
+    R = x.numel() // M if M else 0
+    if y is None:
+        y = torch.empty_like(x)
+    else:
+        _cuda_contig("y", y)
+        if y.shape != x.shape or y.dtype != x.dtype:
+            raise ValueError("y has the wrong shape or dtype")
+    if R == 0:
+        return y
+    lib = _native.lib()
+    need = int(lib.situ_ffn_workspace_size(R, M, I, _dt(x)))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    check("situ_ffn_forward",
+          lib.situ_ffn_forward(x.data_ptr(), W_gate_up.data_ptr(), W_down.data_ptr(),
+                               y.data_ptr(), workspace.data_ptr(),
+                               workspace.numel() * workspace.element_size(), R, M, I,
+                               float(beta), float(linear_beta), _dt(x), _stream(x.device)))
+    return y
+
+
+def situ_ffn_gate_up(x: torch.Tensor, W_gate_up: torch.Tensor, beta: float = 4.0,
+                     linear_beta: float = 25.0, h: torch.Tensor | None = None) -> torch.Tensor:
+    """h = SiTU-GLU(x W_gate_up^T) [..., I], bf16: one tcgen05 GEMM, activation fused."""
+    _cuda_contig("x", x)
+    _cuda_contig("W_gate_up", W_gate_up)
+    M = x.shape[-1]
+    I = W_gate_up.shape[0] // 2
+    if W_gate_up.shape != (2 * I, M) or W_gate_up.dtype != x.dtype:
+        raise ValueError("W_gate_up must be [2I, M] of x's dtype")
+    R = x.numel() // M if M else 0
+    if h is None:
+        h = torch.empty(*x.shape[:-1], I, dtype=x.dtype, device=x.device)
+    if R == 0:
+        return h
+    check("situ_ffn_gate_up",
+          _native.lib().situ_ffn_gate_up(x.data_ptr(), W_gate_up.data_ptr(), h.data_ptr(), R, M,
+                                         I, float(beta), float(linear_beta), _dt(x),
+                                         _stream(x.device)))
+    return h
+
+
+def situ_ffn_down(h: torch.Tensor, W_down: torch.Tensor,
+                  y: torch.Tensor | None = None) -> torch.Tensor:
+    """y = h W_down^T [..., M], bf16 tcgen05 GEMM."""
+    _cuda_contig("h", h)
+    _cuda_contig("W_down", W_down)
+    I = h.shape[-1]
+    M = W_down.shape[0]
+    if W_down.shape != (M, I) or W_down.dtype != h.dtype:
+        raise ValueError("W_down must be [M, I] of h's dtype")
+    R = h.numel() // I if I else 0
+    if y is None:
+        y = torch.empty(*h.shape[:-1], M, dtype=h.dtype, device=h.device)
+    if R == 0:
+        return y
+    check("situ_ffn_down",
+          _native.lib().situ_ffn_down(h.data_ptr(), W_down.data_ptr(), y.data_ptr(), R, M, I,
+                                      _dt(h), _stream(h.device)))
+    return y
+
+
+def situ_moe_build_index(expert_ids: torch.Tensor, num_experts: int,
+                         expert_offsets: torch.Tensor | None = None,
+                         token_index: torch.Tensor | None = None):
+    """Stable counting sort of flat routes by expert.
+
+    expert_ids [T, k_eff] (or flat) int32 on the GPU ->
+    (expert_offsets [E+1] int32, token_index [T*k_eff] int32).
+    """
+    _cuda_contig("expert_ids", expert_ids)
+    if expert_ids.dtype != torch.int32:
+        raise TypeError("expert_ids must be int32")
+    n = expert_ids.numel()
+    dev = expert_ids.device
+    if expert_offsets is None:
+        expert_offsets = torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+    if token_index is None:
+        token_index = torch.empty(n, dtype=torch.int32, device=dev)
+    lib = _native.lib()
+    need = int(lib.situ_moe_index_workspace_size(n, num_experts))
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    check("situ_moe_build_index",
+          lib.situ_moe_build_index(expert_ids.data_ptr(), expert_offsets.data_ptr(),
+                                   token_index.data_ptr(), ws.data_ptr(), ws.numel(), n,
+                                   num_experts, _stream(dev)))
+    return expert_offsets, token_index
+
+
+def moe_workspace_bytes(R: int, E: int, M: int, I: int) -> int:
+    return int(_native.lib().situ_moe_workspace_size(R, E, M, I, SITU_BF16))
+
+
+def situ_moe_grouped_forward(x: torch.Tensor, expert_offsets: torch.Tensor,
+                             token_index: torch.Tensor, W_gate_up: torch.Tensor,
+                             W_down: torch.Tensor, k_eff: int, beta: float = 4.0,
+                             linear_beta: float = 25.0, y: torch.Tensor | None = None,
+                             workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Grouped SiTU-GLU experts: y[t, s] = FFN_{expert of (t, s)}(x[t]).
+
+    x [T, M] bf16; expert_offsets [E+1], token_index [T*k_eff] int32 (from
+    situ_moe_build_index); W_gate_up [E, 2I, M], W_down [E, M, I] bf16, stacked.
+    Returns y [T, k_eff, M].
+    """
+    for n, t in (("x", x), ("expert_offsets", expert_offsets), ("token_index", token_index),
+                 ("W_gate_up", W_gate_up), ("W_down", W_down)):
+        _cuda_contig(n, t)
+    T, M = x.shape
+    E, twoI, _ = W_gate_up.shape
+    I = twoI // 2
+    if W_gate_up.shape != (E, 2 * I, M) or W_down.shape != (E, M, I):
+        raise ValueError("stacked weight shapes do not match x")
+    if expert_offsets.numel() != E + 1 or token_index.numel() != T * k_eff:
+        raise ValueError("index arrays do not match E and T*k_eff")
+    if y is None:
+        y = torch.empty(T, k_eff, M, dtype=x.dtype, device=x.device)
+    R = T * k_eff
+    if R == 0:
+        return y
+    lib = _native.lib()
+    need = int(lib.situ_moe_workspace_size(R, E, M, I, _dt(x)))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    check("situ_moe_grouped_forward",
+          lib.situ_moe_grouped_forward(x.data_ptr(), expert_offsets.data_ptr(),
+                                       token_index.data_ptr(), W_gate_up.data_ptr(),
+                                       W_down.data_ptr(), y.data_ptr(), workspace.data_ptr(),
+                                       workspace.numel() * workspace.element_size(), T,
+                                       k_eff, E, M, I, float(beta), float(linear_beta),
+                                       _dt(x), _stream(x.device)))
+    return y
+
+
+def device_status(clear: bool = True) -> int:
+    """First device-side failure recorded since the last clear (0 = SITU_OK)."""
+    return int(_native.lib().situ_device_status(1 if clear else 0))
+
+
+def selftest_bounded_wait(limit_us: int = 2000) -> None:
+    """Launch the bounded-wait self test on the current stream."""
+    check("situ_selftest_bounded_wait",
+          _native.lib().situ_selftest_bounded_wait(int(limit_us),
+                                                   _stream(torch.device("cuda"))))
+
+
+__all__ = [
+    "SituError", "situ_glu_act", "situ_ffn_forward", "situ_ffn_gate_up", "situ_ffn_down",
+    "situ_moe_build_index",
+    "situ_moe_grouped_forward", "ffn_workspace_bytes", "moe_workspace_bytes",
+    "device_status", "selftest_bounded_wait",
+]

@@ -1,0 +1,407 @@
+// abi.cu -- the extern "C" entry points of libsitu (declared and documented in
+// include/situ.h): argument validation, workspace carving and kernel launches.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "situ.h"
+#include "situ_internal.h"
+#include "situ_math.cuh"
+
+namespace {
+
+using namespace situ;
+
+constexpr int kMaxDevices = 64;
+
+// Per-device status word: the first device-side failure since the last clear.
+__device__ uint32_t g_device_status;
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  uint32_t* status = nullptr;  // device address of g_device_status
+};
+
+DeviceState g_devices[kMaxDevices];
+std::mutex g_mutex;
+thread_local char t_last_cuda_error[256] = "";
+
+situ_status cuda_fail(cudaError_t e) {
+  std::snprintf(t_last_cuda_error, sizeof t_last_cuda_error, "%s: %s", cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return SITU_ERR_CUDA;
+}
+
+// Set-up of the current device (once): SM count and the status word's address.
+situ_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return SITU_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_devices[dev];
+  if (!st.ready) {
+    int major = 0;
+    if ((e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev)) !=
+        cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+        cudaSuccess)
+      return cuda_fail(e);
+    if (major < 10) return SITU_ERR_UNSUPPORTED;
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess) return cuda_fail(e);
+    st.status = static_cast<uint32_t*>(p);
+    st.ready = true;
+  }
+  *out = &st;
+  return SITU_OK;
+}
+
+bool caps_ok(float beta, float linear_beta) {
+  if (!(std::isfinite(beta) && std::isfinite(linear_beta))) return false;
+  if (!(beta > 0.0f && linear_beta > 0.0f)) return false;
+  // beta1 * beta2 * 2^64 must stay finite in FP32 (the scaled product).
+  const double prod = static_cast<double>(beta) * linear_beta;
+  return prod < 1.0e19;
+}
+
+bool dtype_ok(situ_dtype dt) { return dt == SITU_BF16 || dt == SITU_F32; }
+
+bool overlap(const void* a, size_t an, const void* b, size_t bn) {
+  if (!a || !b || an == 0 || bn == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bn && b0 < a0 + an;
+}
+
+bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+situ_status finish(cudaError_t e) { return e == cudaSuccess ? SITU_OK : cuda_fail(e); }
+
+}  // namespace
+
+extern "C" {
+
+int situ_abi_version(void) { return SITU_ABI_VERSION; }
+
+const char* situ_status_string(situ_status s) {
+  switch (s) {
+    case SITU_OK: return "SITU_OK";
+    case SITU_ERR_ARG: return "SITU_ERR_ARG";
+    case SITU_ERR_ALIGN: return "SITU_ERR_ALIGN";
+    case SITU_ERR_ALIAS: return "SITU_ERR_ALIAS";
+    case SITU_ERR_CUDA: return "SITU_ERR_CUDA";
+    case SITU_ERR_TIMEOUT: return "SITU_ERR_TIMEOUT";
+    case SITU_ERR_UNSUPPORTED: return "SITU_ERR_UNSUPPORTED";
+    case SITU_ERR_INDEX: return "SITU_ERR_INDEX";
+    case SITU_ERR_WORKSPACE: return "SITU_ERR_WORKSPACE";
+  }
+  return "SITU_ERR_UNKNOWN";
+}
+
+const char* situ_last_cuda_error(void) { return t_last_cuda_error; }
+
+situ_status situ_device_status(int clear) {
+  DeviceState* st = nullptr;
+  situ_status s = device_state(&st);
+  if (s != SITU_OK) return s;
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpy(&v, st->status, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (clear) {
+    const uint32_t zero = 0;
+    e = cudaMemcpy(st->status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return static_cast<situ_status>(v);
+}
+
+situ_status situ_glu_act(const void* gate_up, void* out, int64_t rows, int64_t I, float beta,
+                         float linear_beta, situ_dtype dt, void* stream) {
+  if (!dtype_ok(dt) || rows < 0 || I < 1 || !caps_ok(beta, linear_beta)) return SITU_ERR_ARG;
+  if (rows == 0) return SITU_OK;
+  if (!gate_up || !out) return SITU_ERR_ARG;
+  const size_t esz = dtype_size(dt);
+  if (overlap(gate_up, static_cast<size_t>(rows) * 2 * I * esz, out,
+              static_cast<size_t>(rows) * I * esz))
+    return SITU_ERR_ALIAS;
+  if (reinterpret_cast<uintptr_t>(gate_up) % esz || reinterpret_cast<uintptr_t>(out) % esz)
+    return SITU_ERR_ALIGN;
+  DeviceState* st = nullptr;
+  situ_status s = device_state(&st);
+  if (s != SITU_OK) return s;
+  return finish(launch_situ_act(gate_up, out, rows, I, make_situ_params(beta, linear_beta), dt,
+                                st->num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+size_t situ_ffn_workspace_size(int64_t R, int64_t M, int64_t I, situ_dtype dt) {
+  (void)M;
+  if (R <= 0 || I <= 0 || !dtype_ok(dt)) return 0;
+  return round_up(static_cast<size_t>(R) * I * dtype_size(dt), 256);
+}
+
+namespace {
+
+// Shared argument checks of the dense FFN calls.
+situ_status ffn_common_checks(situ_dtype dt, int64_t R, int64_t M, int64_t I, float beta,
+                              float linear_beta) {
+  if (!dtype_ok(dt) || R < 0 || M < 1 || I < 1 || !caps_ok(beta, linear_beta))
+    return SITU_ERR_ARG;
+  if (R >= (int64_t(1) << 31) || 2 * I >= (int64_t(1) << 31) || M >= (int64_t(1) << 31))
+    return SITU_ERR_UNSUPPORTED;
+  return SITU_OK;
+}
+
+situ_status bf16_gemm_checks(const void* a, const void* b, const void* c, int64_t M, int64_t I) {
+  if (M % 8 || I % 8) return SITU_ERR_UNSUPPORTED;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(c)) return SITU_ERR_ALIGN;
+  return SITU_OK;
+}
+
+cudaError_t run_gate_up(const DeviceState* st, const void* x, const void* W_gate_up, void* h,
+                        int64_t R, int64_t M, int64_t I, const SituParams& p, cudaStream_t cs) {
+  GemmShape g{};
+  g.a = x;
+  g.a_rows = R;
+  g.b = W_gate_up;
+  g.b_rows = 2 * I;
+  g.K = M;
+  g.num_groups = 1;
+  g.b_group_rows = 2 * I;
+  g.b_up_offset = I;
+  g.n_out = I;
+  g.out = h;
+  g.ldo = I;
+  g.out_rows = R;
+  return launch_gemm_situ(g, p, st->status, st->num_sms, cs);
+}
+
+cudaError_t run_down(const DeviceState* st, const void* h, const void* W_down, void* y,
+                     int64_t R, int64_t M, int64_t I, cudaStream_t cs) {
+  GemmShape d{};
+  d.a = h;
+  d.a_rows = R;
+  d.b = W_down;
+  d.b_rows = M;
+  d.K = I;
+  d.num_groups = 1;
+  d.b_group_rows = M;
+  d.n_out = M;
+  d.out = y;
+  d.ldo = M;
+  d.out_rows = R;
+  return launch_gemm_plain(d, st->status, st->num_sms, cs);
+}
+
+}  // namespace
+
+situ_status situ_ffn_forward(const void* x, const void* W_gate_up, const void* W_down, void* y,
+                             void* workspace, size_t workspace_bytes, int64_t R, int64_t M,
+                             int64_t I, float beta, float linear_beta, situ_dtype dt,
+                             void* stream) {
+  situ_status s = ffn_common_checks(dt, R, M, I, beta, linear_beta);
+  if (s != SITU_OK || R == 0) return s;
+  if (!x || !W_gate_up || !W_down || !y) return SITU_ERR_ARG;
+  const size_t esz = dtype_size(dt);
+  const size_t need = situ_ffn_workspace_size(R, M, I, dt);
+  if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return SITU_ERR_WORKSPACE;
+  const size_t y_bytes = static_cast<size_t>(R) * M * esz;
+  if (overlap(y, y_bytes, x, static_cast<size_t>(R) * M * esz) ||
+      overlap(y, y_bytes, W_gate_up, static_cast<size_t>(2 * I) * M * esz) ||
+      overlap(y, y_bytes, W_down, static_cast<size_t>(M) * I * esz) ||
+      overlap(y, y_bytes, workspace, need) ||
+      overlap(workspace, need, x, static_cast<size_t>(R) * M * esz) ||
+      overlap(workspace, need, W_gate_up, static_cast<size_t>(2 * I) * M * esz) ||
+      overlap(workspace, need, W_down, static_cast<size_t>(M) * I * esz))
+    return SITU_ERR_ALIAS;
+  DeviceState* st = nullptr;
+  if ((s = device_state(&st)) != SITU_OK) return s;
+  const SituParams p = make_situ_params(beta, linear_beta);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (dt == SITU_F32) {
+    if (reinterpret_cast<uintptr_t>(x) % 4 || reinterpret_cast<uintptr_t>(W_gate_up) % 4 ||
+        reinterpret_cast<uintptr_t>(W_down) % 4 || reinterpret_cast<uintptr_t>(y) % 4)
+      return SITU_ERR_ALIGN;
+    return finish(launch_ffn_f32(static_cast<const float*>(x),
+                                 static_cast<const float*>(W_gate_up),
+                                 static_cast<const float*>(W_down),
+                                 static_cast<float*>(workspace), static_cast<float*>(y), R, M,
+                                 I, p, cs));
+  }
+  if ((s = bf16_gemm_checks(x, W_gate_up, W_down, M, I)) != SITU_OK) return s;
+  if (!aligned16(y)) return SITU_ERR_ALIGN;
+  cudaError_t e = run_gate_up(st, x, W_gate_up, workspace, R, M, I, p, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return finish(run_down(st, workspace, W_down, y, R, M, I, cs));
+}
+
+situ_status situ_ffn_gate_up(const void* x, const void* W_gate_up, void* h, int64_t R,
+                             int64_t M, int64_t I, float beta, float linear_beta,
+                             situ_dtype dt, void* stream) {
+  situ_status s = ffn_common_checks(dt, R, M, I, beta, linear_beta);
+  if (s != SITU_OK || R == 0) return s;
+  if (!x || !W_gate_up || !h) return SITU_ERR_ARG;
+  const size_t esz = dtype_size(dt);
+  const size_t h_bytes = static_cast<size_t>(R) * I * esz;
+  if (overlap(h, h_bytes, x, static_cast<size_t>(R) * M * esz) ||
+      overlap(h, h_bytes, W_gate_up, static_cast<size_t>(2 * I) * M * esz))
+    return SITU_ERR_ALIAS;
+  if (dt == SITU_F32) return SITU_ERR_UNSUPPORTED;
+  if ((s = bf16_gemm_checks(x, W_gate_up, h, M, I)) != SITU_OK) return s;
+  DeviceState* st = nullptr;
+  if ((s = device_state(&st)) != SITU_OK) return s;
+  return finish(run_gate_up(st, x, W_gate_up, h, R, M, I, make_situ_params(beta, linear_beta),
+                            static_cast<cudaStream_t>(stream)));
+}
+
+situ_status situ_ffn_down(const void* h, const void* W_down, void* y, int64_t R, int64_t M,
+                          int64_t I, situ_dtype dt, void* stream) {
+  situ_status s = ffn_common_checks(dt, R, M, I, 1.0f, 1.0f);
+  if (s != SITU_OK || R == 0) return s;
+  if (!h || !W_down || !y) return SITU_ERR_ARG;
+  const size_t esz = dtype_size(dt);
+  const size_t y_bytes = static_cast<size_t>(R) * M * esz;
+  if (overlap(y, y_bytes, h, static_cast<size_t>(R) * I * esz) ||
+      overlap(y, y_bytes, W_down, static_cast<size_t>(M) * I * esz))
+    return SITU_ERR_ALIAS;
+  if (dt == SITU_F32) return SITU_ERR_UNSUPPORTED;
+  if ((s = bf16_gemm_checks(h, W_down, y, M, I)) != SITU_OK) return s;
+  DeviceState* st = nullptr;
+  if ((s = device_state(&st)) != SITU_OK) return s;
+  return finish(run_down(st, h, W_down, y, R, M, I, static_cast<cudaStream_t>(stream)));
+}
+
+size_t situ_moe_index_workspace_size(int64_t n_routes, int32_t E) {
+  if (n_routes < 0 || E < 1) return 0;
+  return round_up(index_workspace_bytes(n_routes, E), 256);
+}
+
+situ_status situ_moe_build_index(const int32_t* expert_ids, int32_t* expert_offsets,
+                                 int32_t* token_index, void* workspace, size_t workspace_bytes,
+                                 int64_t n_routes, int32_t E, void* stream) {
+  if (n_routes < 0 || n_routes >= (int64_t(1) << 31) || E < 1 || E > 16384) return SITU_ERR_ARG;
+  if (!expert_offsets || (n_routes > 0 && (!expert_ids || !token_index))) return SITU_ERR_ARG;
+  const size_t need = situ_moe_index_workspace_size(n_routes, E);
+  if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 16)
+    return SITU_ERR_WORKSPACE;
+  const size_t ids_b = static_cast<size_t>(n_routes) * 4, off_b = static_cast<size_t>(E + 1) * 4;
+  if (overlap(expert_offsets, off_b, expert_ids, ids_b) ||
+      overlap(token_index, ids_b, expert_ids, ids_b) ||
+      overlap(token_index, ids_b, expert_offsets, off_b) ||
+      overlap(workspace, need, expert_ids, ids_b) ||
+      overlap(workspace, need, expert_offsets, off_b) ||
+      overlap(workspace, need, token_index, ids_b))
+    return SITU_ERR_ALIAS;
+  DeviceState* st = nullptr;
+  situ_status s = device_state(&st);
+  if (s != SITU_OK) return s;
+  return finish(launch_build_index(expert_ids, expert_offsets, token_index, workspace, n_routes,
+                                   E, st->status, static_cast<cudaStream_t>(stream)));
+}
+
+size_t situ_moe_workspace_size(int64_t R, int32_t E, int64_t M, int64_t I, situ_dtype dt) {
+  if (R < 0 || E < 1 || M < 1 || I < 1 || dt != SITU_BF16) return 0;
+  const size_t tiles = round_up(static_cast<size_t>(E + 1) * 4, 256);
+  const size_t xperm = round_up(static_cast<size_t>(R) * M * 2, 256);
+  const size_t h = round_up(static_cast<size_t>(R) * I * 2, 256);
+  return tiles + xperm + h;
+}
+
+situ_status situ_moe_grouped_forward(const void* x, const int32_t* expert_offsets,
+                                     const int32_t* token_index, const void* W_gate_up,
+                                     const void* W_down, void* y, void* workspace,
+                                     size_t workspace_bytes, int64_t T, int32_t k_eff,
+                                     int32_t E, int64_t M, int64_t I, float beta,
+                                     float linear_beta, situ_dtype dt, void* stream) {
+  if (dt != SITU_BF16) return dt == SITU_F32 ? SITU_ERR_UNSUPPORTED : SITU_ERR_ARG;
+  if (T < 0 || k_eff < 1 || E < 1 || E > 65536 || M < 1 || I < 1 || !caps_ok(beta, linear_beta))
+    return SITU_ERR_ARG;
+  const int64_t R = T * k_eff;
+  if (R == 0) return SITU_OK;
+  if (!x || !expert_offsets || !token_index || !W_gate_up || !W_down || !y) return SITU_ERR_ARG;
+  if (R >= (int64_t(1) << 31) || static_cast<int64_t>(E) * 2 * I >= (int64_t(1) << 31) ||
+      static_cast<int64_t>(E) * M >= (int64_t(1) << 31))
+    return SITU_ERR_UNSUPPORTED;
+  if (M % 8 || I % 8) return SITU_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(W_gate_up) || !aligned16(W_down) || !aligned16(y))
+    return SITU_ERR_ALIGN;
+  const size_t need = situ_moe_workspace_size(R, E, M, I, dt);
+  if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return SITU_ERR_WORKSPACE;
+  const size_t x_b = static_cast<size_t>(T) * M * 2, y_b = static_cast<size_t>(R) * M * 2;
+  const size_t wgu_b = static_cast<size_t>(E) * 2 * I * M * 2, wd_b = static_cast<size_t>(E) * M * I * 2;
+  const size_t off_b = static_cast<size_t>(E + 1) * 4, tix_b = static_cast<size_t>(R) * 4;
+  const void* ins[] = {x, W_gate_up, W_down, expert_offsets, token_index};
+  const size_t in_b[] = {x_b, wgu_b, wd_b, off_b, tix_b};
+  for (int i = 0; i < 5; ++i) {
+    if (overlap(y, y_b, ins[i], in_b[i]) || overlap(workspace, need, ins[i], in_b[i]))
+      return SITU_ERR_ALIAS;
+  }
+  if (overlap(y, y_b, workspace, need)) return SITU_ERR_ALIAS;
+  DeviceState* st = nullptr;
+  situ_status s = device_state(&st);
+  if (s != SITU_OK) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* tile_offsets = reinterpret_cast<int32_t*>(ws);
+  void* x_perm = ws + round_up(static_cast<size_t>(E + 1) * 4, 256);
+  void* h_perm = static_cast<uint8_t*>(x_perm) + round_up(static_cast<size_t>(R) * M * 2, 256);
+
+  cudaError_t e = launch_group_tiles(expert_offsets, E, R, tile_offsets, st->status, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = launch_gather_rows(x, token_index, x_perm, R, k_eff, M, st->status, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const SituParams p = make_situ_params(beta, linear_beta);
+  GemmShape g{};
+  g.a = x_perm;
+  g.a_rows = R;
+  g.b = W_gate_up;
+  g.b_rows = static_cast<int64_t>(E) * 2 * I;
+  g.K = M;
+  g.num_groups = E;
+  g.group_offsets = expert_offsets;
+  g.tile_offsets = tile_offsets;
+  g.b_group_rows = 2 * I;
+  g.b_up_offset = I;
+  g.n_out = I;
+  g.out = h_perm;
+  g.ldo = I;
+  g.out_rows = R;
+  e = launch_gemm_situ(g, p, st->status, st->num_sms, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  GemmShape d{};
+  d.a = h_perm;
+  d.a_rows = R;
+  d.b = W_down;
+  d.b_rows = static_cast<int64_t>(E) * M;
+  d.K = I;
+  d.num_groups = E;
+  d.group_offsets = expert_offsets;
+  d.tile_offsets = tile_offsets;
+  d.b_group_rows = M;
+  d.n_out = M;
+  d.out = y;
+  d.ldo = M;
+  d.out_rows = R;
+  d.out_row_index = token_index;
+  return finish(launch_gemm_plain(d, st->status, st->num_sms, cs));
+}
+
+situ_status situ_selftest_bounded_wait(uint32_t limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return SITU_ERR_ARG;
+  DeviceState* st = nullptr;
+  situ_status s = device_state(&st);
+  if (s != SITU_OK) return s;
+  return finish(launch_bounded_wait_selftest(static_cast<uint64_t>(limit_us) * 1000, st->status,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,546 @@
+// gemm.cu -- persistent, warp-specialised tcgen05 GEMMs for the SiTU-GLU
+// feed-forward on sm_103a, dense or grouped over experts.
+//
+//   gate_up + SiTU-GLU:  h[r, j] = SiTU-GLU(x[r] . Wgu[j], x[r] . Wgu[I + j])
+//   down:                y[r, m] = h[r] . Wd[m]
+// ("DenseFFN and SituGLU - Docs - Kimi K3 from Scratch", "Two linear maps and a
+// guarded compiled branch": packed gate_up_proj M -> 2I, down_proj I -> M; the
+// activation of "SiTU-GLU: one split, two softly bounded branches" applied to the
+// FP32 accumulators so the [R, 2I] product never reaches memory.)
+//
+// Design (one CTA per SM, 192 threads):
+//   warp 0      TMA producer: per k-block, one 128x64 A box and two 128x64 B
+//               boxes (gate rows and the matching up rows for the SiTU GEMM; two
+//               adjacent 128-row halves for the plain GEMM) into a 4-stage ring of
+//               128-byte-swizzled shared-memory buffers.
+//   warp 1      MMA issuer: tcgen05.mma kind::f16, M=128 N=256 K=16, accumulating
+//               in tensor memory; tcgen05.commit frees each stage and publishes each
+//               finished accumulator.  Two 256-column accumulators (all 512 TMEM
+//               columns) let the epilogue of tile i overlap the MMAs of tile i+1.
+//   warps 2..5  epilogue: tcgen05.ld of the FP32 accumulator (thread = tile row),
+//               SiTU-GLU on (gate column j, up column 128 + j) or plain conversion,
+//               bf16 round-to-nearest-even, 16-byte stores of each row's segment.
+// Tiles are walked in (m-tile, n-tile) order with a grid-wide stride, so the
+// n-tiles of one m-tile run side by side and share the A rows in L2.
+// Every wait is bounded (mbar_wait); on a timeout the CTA records
+// SITU_ERR_TIMEOUT, drains its in-flight copies and MMAs with bounded waits,
+// frees its tensor memory and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "situ_internal.h"
+#include "situ_math.cuh"
+#include "situ_ptx.cuh"
+
+namespace situ {
+namespace {
+
+constexpr int kBM = 128;  // tile rows (UMMA M)
+constexpr int kBN = 256;  // accumulator columns per tile (UMMA N)
+constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
+constexpr int kUK = 16;   // K per tcgen05.mma for 16-bit inputs
+constexpr int kStages = 4;
+constexpr int kAccBufs = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr uint32_t kABytes = kBM * kBK * 2;  // 16 KiB
+constexpr uint32_t kBHalfBytes = 128 * kBK * 2;
+constexpr uint32_t kBBytes = kBN * kBK * 2;  // 32 KiB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint64_t kWaitLimitNs = 10ull * 1000 * 1000 * 1000;  // 10 s
+constexpr uint64_t kDrainLimitNs = 100ull * 1000 * 1000;       // 100 ms
+constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
+
+enum class Epi { kSitu, kPlain };
+
+struct Args {
+  int32_t num_groups;
+  const int32_t* group_offsets;  // [G+1] device or null (dense)
+  const int32_t* tile_offsets;   // [G+1] device or null (dense)
+  int32_t dense_rows;
+  int32_t n_tiles;
+  int32_t k_blocks;
+  int64_t b_group_rows;
+  int64_t b_up_offset;
+  int64_t n_out;
+  __nv_bfloat16* out;
+  int64_t ldo;
+  int64_t out_rows;
+  const int32_t* out_row_index;
+  SituParams sp;
+  uint32_t* status;
+};
+
+struct SharedCtl {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full[kAccBufs];
+  uint64_t acc_empty[kAccBufs];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort;
+};
+
+struct TileCoord {
+  int32_t a_row0;   // first A row of the tile
+  int32_t row_end;  // one past the last valid A row (group end)
+  int32_t group;
+  int32_t n_tile;
+};
+
+__device__ __forceinline__ int32_t total_tiles(const Args& a) {
+  const int32_t m_tiles = a.tile_offsets ? __ldg(a.tile_offsets + a.num_groups)
+                                         : (a.dense_rows + kBM - 1) / kBM;
+  return m_tiles * a.n_tiles;
+}
+
+__device__ __forceinline__ TileCoord decode_tile(const Args& a, int32_t t) {
+  TileCoord c;
+  const int32_t mt = t / a.n_tiles;
+  c.n_tile = t - mt * a.n_tiles;
+  if (!a.tile_offsets) {
+    c.group = 0;
+    c.a_row0 = mt * kBM;
+    c.row_end = a.dense_rows;
+    return c;
+  }
+  // Largest g with tile_offsets[g] <= mt (empty groups repeat an offset; the
+  // last of a run of equal offsets is the group that owns the tile).
+  int32_t lo = 0, hi = a.num_groups - 1;
+  while (lo < hi) {
+    const int32_t mid = (lo + hi + 1) >> 1;
+    if (__ldg(a.tile_offsets + mid) <= mt) lo = mid; else hi = mid - 1;
+  }
+  c.group = lo;
+  c.a_row0 = __ldg(a.group_offsets + lo) + (mt - __ldg(a.tile_offsets + lo)) * kBM;
+  c.row_end = __ldg(a.group_offsets + lo + 1);
+  return c;
+}
+
+__device__ __forceinline__ bool ctl_wait(SharedCtl* ctl, uint64_t* bar, uint32_t parity,
+                                         uint32_t* status) {
+  const uint32_t b = smem_u32(bar);
+  if (mbar_try_wait(b, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t polls = 0;
+  while (true) {
+    if (mbar_try_wait(b, parity)) return true;
+    if ((++polls & 63u) == 0u) {
+      if (ctl->abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        record_status(status, SITU_ERR_TIMEOUT);
+        ctl->abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Store up to 32 bf16 (16 packed words) of one row; columns >= n_valid are not
+// written (n_valid is a multiple of 8, so a 16-byte piece is all in or all out).
+__device__ __forceinline__ void store_row_chunk(__nv_bfloat16* dst, const uint32_t (&w)[16],
+                                                int64_t col0, int64_t n_valid) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    if (col0 + 8 * v + 8 <= n_valid) {
+      st_global_v4(dst + 8 * v, w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+    }
+  }
+}
+
+template <Epi kEpi>
+__global__ void __launch_bounds__(kThreads, 1)
+    ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                    const __grid_constant__ CUtensorMap map_b, const Args args) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled operand buffers.
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + kStages * kStageBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int b = 0; b < kAccBufs; ++b) {
+      mbar_init(smem_u32(&ctl->acc_full[b]), 1);
+      mbar_init(smem_u32(&ctl->acc_empty[b]), kEpiThreads);
+    }
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+    tma_prefetch_map(&map_a);
+    tma_prefetch_map(&map_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+    tmem_relinquish();
+    tc_fence_before_sync();
+  }
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = ctl->tmem_base;
+  const int32_t n_total = total_tiles(args);
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued = 0;
+      bool ok = true;
+      for (int32_t t = blockIdx.x; t < n_total && ok; t += gridDim.x) {
+        const TileCoord tc = decode_tile(args, t);
+        const int64_t gbase = static_cast<int64_t>(tc.group) * args.b_group_rows;
+        int32_t b_row0, b_row1;
+        if (kEpi == Epi::kSitu) {
+          b_row0 = static_cast<int32_t>(gbase + static_cast<int64_t>(tc.n_tile) * 128);
+          b_row1 = static_cast<int32_t>(gbase + args.b_up_offset +
+                                        static_cast<int64_t>(tc.n_tile) * 128);
+        } else {
+          b_row0 = static_cast<int32_t>(gbase + static_cast<int64_t>(tc.n_tile) * kBN);
+          b_row1 = b_row0 + 128;
+        }
+        for (int32_t kb = 0; kb < args.k_blocks; ++kb) {
+          if (!ctl_wait(ctl, &ctl->empty[stage], phase ^ 1u, args.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_u32(&ctl->full[stage]);
+          const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+          mbar_arrive_expect_tx(full, kStageBytes);
+          tma_load_2d(sa, &map_a, kb * kBK, tc.a_row0, full);
+          tma_load_2d(sb, &map_b, kb * kBK, b_row0, full);
+          tma_load_2d(sb + kBHalfBytes, &map_b, kb * kBK, b_row1, full);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Drain: wait (bounded) for the copies of the last stages issued.
+        const uint32_t n = issued < kStages ? issued : kStages;
+        for (uint32_t i = 0; i < n; ++i) {
+          stage = (stage + kStages - 1) % kStages;
+          if (stage == kStages - 1) phase ^= 1u;
+          mbar_wait(smem_u32(&ctl->full[stage]), phase, nullptr, kDrainLimitNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t local = 0;
+      bool ok = true;
+      for (int32_t t = blockIdx.x; t < n_total && ok; t += gridDim.x, ++local) {
+        const uint32_t acc = local & 1u;
+        const uint32_t acc_phase = (local >> 1) & 1u;
+        if (!ctl_wait(ctl, &ctl->acc_empty[acc], acc_phase ^ 1u, args.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * kBN;
+        for (int32_t kb = 0; kb < args.k_blocks; ++kb) {
+          if (!ctl_wait(ctl, &ctl->full[stage], phase, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / kUK; ++k) {
+            umma_bf16(d_tmem, sw128_kmajor_desc(sa + k * kUK * 2),
+                      sw128_kmajor_desc(sb + k * kUK * 2), kIdesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&ctl->empty[stage]));
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&ctl->acc_full[acc]));
+      }
+      if (!ok) {
+        // Drain the MMAs already issued before the tensor memory is freed.
+        umma_commit(smem_u32(&ctl->drain));
+        mbar_wait(smem_u32(&ctl->drain), 0, nullptr, kDrainLimitNs);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int row_in_tile = quarter * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t local = 0;
+    for (int32_t t = blockIdx.x; t < n_total; t += gridDim.x, ++local) {
+      const uint32_t acc = local & 1u;
+      const uint32_t acc_phase = (local >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = ctl_wait(ctl, &ctl->acc_full[acc], acc_phase, args.status) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const TileCoord tc = decode_tile(args, t);
+      const int32_t row = tc.a_row0 + row_in_tile;
+      bool valid = row < tc.row_end;
+      int64_t out_row = row;
+      if (valid && args.out_row_index) {
+        out_row = __ldg(args.out_row_index + row);
+        valid = out_row >= 0 && out_row < args.out_rows;
+      }
+      const uint32_t t_acc = tmem_base + lane_addr + acc * kBN;
+      if (kEpi == Epi::kSitu) {
+        __nv_bfloat16* dst_row = args.out + out_row * args.ldo;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          __syncwarp();  // tcgen05.ld is warp-collective (.sync.aligned)
+          uint32_t g[32], u[32];
+          tmem_ld32(t_acc + c * 32, g);
+          tmem_ld32(t_acc + 128 + c * 32, u);
+          tmem_ld_wait2(g, u);
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            w[i] = pack_bf16x2(
+                situ_glu_f32(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), args.sp),
+                situ_glu_f32(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]),
+                             args.sp));
+          }
+          const int64_t col0 = static_cast<int64_t>(tc.n_tile) * 128 + c * 32;
+          if (valid) store_row_chunk(dst_row + col0, w, col0, args.n_out);
+        }
+      } else {
+        __nv_bfloat16* dst_row = args.out + out_row * args.ldo;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          __syncwarp();
+          uint32_t a[32];
+          tmem_ld32(t_acc + c * 32, a);
+          tmem_ld_wait(a);
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            w[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+          }
+          const int64_t col0 = static_cast<int64_t>(tc.n_tile) * kBN + c * 32;
+          if (valid) store_row_chunk(dst_row + col0, w, col0, args.n_out);
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&ctl->acc_empty[acc]));
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Small helper kernels of the grouped path
+// ---------------------------------------------------------------------------
+
+// tile_offsets[g] = sum over g' < g of ceil(rows_g' / 128); validates offsets.
+__global__ void group_tiles_kernel(const int32_t* __restrict__ off, int32_t G, int64_t R,
+                                   int32_t* __restrict__ tiles, uint32_t* status) {
+  __shared__ int32_t partial[1024];
+  __shared__ int bad;
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  const int per = (G + blockDim.x - 1) / blockDim.x;
+  const int g0 = threadIdx.x * per;
+  int32_t sum = 0;
+  for (int g = g0; g < g0 + per && g < G; ++g) {
+    const int32_t a = off[g], b = off[g + 1];
+    if (b < a) bad = 1;
+    sum += (b - a + kBM - 1) / kBM;
+  }
+  if (threadIdx.x == 0 && (off[0] != 0 || static_cast<int64_t>(off[G]) != R)) bad = 1;
+  partial[threadIdx.x] = sum;
+  __syncthreads();
+  // Inclusive scan of the per-thread sums (Hillis-Steele over one block).
+  for (int d = 1; d < static_cast<int>(blockDim.x); d <<= 1) {
+    const int32_t v = threadIdx.x >= static_cast<unsigned>(d) ? partial[threadIdx.x - d] : 0;
+    __syncthreads();
+    partial[threadIdx.x] += v;
+    __syncthreads();
+  }
+  if (bad) {
+    for (int g = threadIdx.x; g <= G; g += blockDim.x) tiles[g] = 0;
+    if (threadIdx.x == 0) record_status(status, SITU_ERR_INDEX);
+    return;
+  }
+  int32_t run = threadIdx.x == 0 ? 0 : partial[threadIdx.x - 1];
+  for (int g = g0; g < g0 + per && g < G; ++g) {
+    tiles[g] = run;
+    run += (off[g + 1] - off[g] + kBM - 1) / kBM;
+  }
+  if (threadIdx.x == blockDim.x - 1) tiles[G] = partial[threadIdx.x];
+}
+
+// One warp per gathered row: x_perm[r] = x[token_index[r] / k_eff] (16-byte copies).
+__global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ tix,
+                                   uint4* __restrict__ xp, int64_t R, int32_t k_eff,
+                                   int64_t vec_per_row, int64_t T, uint32_t* status) {
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       r < R; r += warps) {
+    const int32_t flat = __ldg(tix + r);
+    const int64_t t = flat / k_eff;
+    uint4* dst = xp + r * vec_per_row;
+    if (flat < 0 || t >= T) {
+      if ((threadIdx.x & 31) == 0) record_status(status, SITU_ERR_INDEX);
+      for (int64_t v = threadIdx.x & 31; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* src = x + t * vec_per_row;
+    for (int64_t v = threadIdx.x & 31; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+  }
+}
+
+__global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, uint32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    // Nothing ever arrives on this barrier: the wait must give up by itself.
+    mbar_wait(smem_u32(&bar), 0, status, limit_ns);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+  }
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, cols] matrix, 64 x 128 boxes, 128-byte
+// swizzle (the layout sw128_kmajor_desc describes), zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+constexpr size_t kSmemBytes = kStages * kStageBytes + sizeof(SharedCtl) + 1024;
+
+template <Epi kEpi>
+cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, int num_sms,
+                   cudaStream_t stream) {
+  if (s.a_rows == 0 && !s.tile_offsets) return cudaSuccess;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, s.a, s.a_rows, s.K) || !make_map(&mb, s.b, s.b_rows, s.K))
+    return cudaErrorInvalidValue;
+  Args a;
+  a.num_groups = s.num_groups;
+  a.group_offsets = s.group_offsets;
+  a.tile_offsets = s.tile_offsets;
+  a.dense_rows = static_cast<int32_t>(s.a_rows);
+  const int64_t out_cols_per_tile = kEpi == Epi::kSitu ? 128 : kBN;
+  a.n_tiles = static_cast<int32_t>((s.n_out + out_cols_per_tile - 1) / out_cols_per_tile);
+  a.k_blocks = static_cast<int32_t>((s.K + kBK - 1) / kBK);
+  a.b_group_rows = s.b_group_rows;
+  a.b_up_offset = s.b_up_offset;
+  a.n_out = s.n_out;
+  a.out = static_cast<__nv_bfloat16*>(s.out);
+  a.ldo = s.ldo;
+  a.out_rows = s.out_rows;
+  a.out_row_index = s.out_row_index;
+  a.sp = p;
+  a.status = status;
+  int grid = num_sms;
+  if (!s.tile_offsets) {
+    const int64_t tiles = ((s.a_rows + kBM - 1) / kBM) * a.n_tiles;
+    if (tiles < grid) grid = static_cast<int>(tiles);
+  }
+  cudaError_t e = cudaFuncSetAttribute(ffn_gemm_kernel<kEpi>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  ffn_gemm_kernel<kEpi><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_situ(const GemmShape& s, const SituParams& p, uint32_t* status,
+                             int num_sms, cudaStream_t stream) {
+  return launch<Epi::kSitu>(s, p, status, num_sms, stream);
+}
+
+cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
+                              cudaStream_t stream) {
+  return launch<Epi::kPlain>(s, SituParams{}, status, num_sms, stream);
+}
+
+cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,
+                               int32_t* tile_offsets, uint32_t* status, cudaStream_t stream) {
+  group_tiles_kernel<<<1, 1024, 0, stream>>>(group_offsets, G, R, tile_offsets, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* x, const int32_t* token_index, void* x_perm,
+                               int64_t R, int32_t k_eff, int64_t M, uint32_t* status,
+                               cudaStream_t stream) {
+  if (R == 0) return cudaSuccess;
+  const int64_t T = R / k_eff;
+  const int threads = 256;
+  int64_t blocks = (R + (threads / 32) - 1) / (threads / 32);
+  if (blocks > 65535) blocks = 65535;
+  gather_rows_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(
+      static_cast<const uint4*>(x), token_index, static_cast<uint4*>(x_perm), R, k_eff, M / 8,
+      T, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, uint32_t* status,
+                                         cudaStream_t stream) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(limit_ns, status);
+  return cudaGetLastError();
+}
+
+}  // namespace situ

@@ -1,0 +1,79 @@
+// situ_internal.h -- host-side launchers shared between the library's
+// translation units (not part of the public ABI; see include/situ.h).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "situ.h"
+#include "situ_math.cuh"
+
+namespace situ {
+
+// Bytes of one element of a library dtype.
+inline size_t dtype_size(situ_dtype dt) { return dt == SITU_F32 ? 4 : 2; }
+
+// ----- standalone activation (act.cu) --------------------------------------
+// gate_up [rows, 2I] -> out [rows, I]; picks the 128-bit path when rows start
+// 16-byte aligned, else the scalar path.
+cudaError_t launch_situ_act(const void* gate_up, void* out, int64_t rows, int64_t I,
+                            const SituParams& p, situ_dtype dt, int num_sms,
+                            cudaStream_t stream);
+
+// ----- FP32 small-shape FFN (act.cu) ----------------------------------------
+// h [R, I] = SiTU-GLU(x W_gate_up^T) then y [R, M] = h W_down^T, all float32.
+cudaError_t launch_ffn_f32(const float* x, const float* w_gate_up, const float* w_down,
+                           float* h, float* y, int64_t R, int64_t M, int64_t I,
+                           const SituParams& p, cudaStream_t stream);
+
+// ----- tcgen05 GEMMs (gemm.cu) ------------------------------------------------
+struct GemmShape {
+  // A operand: [a_rows, K] bf16 row-major (dense x / gathered rows / h).
+  const void* a;
+  int64_t a_rows;
+  // B operand: [b_rows, K] bf16 row-major (one or E stacked weight matrices).
+  const void* b;
+  int64_t b_rows;
+  int64_t K;
+  // Row groups (experts).  group_offsets / tile_offsets are device arrays of
+  // G + 1 int32 each, or NULL for a single dense group of a_rows rows.
+  int32_t num_groups;
+  const int32_t* group_offsets;
+  const int32_t* tile_offsets;
+  int64_t b_group_rows;  // B rows per group
+  int64_t b_up_offset;   // SiTU epilogue: row offset of the up half inside a group
+  int64_t n_out;         // valid output columns
+  // Output [out_rows, ldo] bf16; row of A-row r is out_row_index[r] if given.
+  void* out;
+  int64_t ldo;
+  int64_t out_rows;
+  const int32_t* out_row_index;
+};
+
+// gu = A B^T with the SiTU-GLU epilogue: output column j of group tile n pairs B
+// row n*128 + j (gate) with B row b_up_offset + n*128 + j (up).
+cudaError_t launch_gemm_situ(const GemmShape& s, const SituParams& p, uint32_t* status,
+                             int num_sms, cudaStream_t stream);
+// C = A B^T, bf16 output.
+cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
+                              cudaStream_t stream);
+// M-tile prefix over row groups + validation of the offsets.
+cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,
+                               int32_t* tile_offsets, uint32_t* status, cudaStream_t stream);
+// x_perm[r, :] = x[token_index[r] / k_eff, :]  (M bf16 columns).
+cudaError_t launch_gather_rows(const void* x, const int32_t* token_index, void* x_perm,
+                               int64_t R, int32_t k_eff, int64_t M, uint32_t* status,
+                               cudaStream_t stream);
+// One block waiting on a barrier nothing completes, bounded by limit_ns.
+cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, uint32_t* status,
+                                         cudaStream_t stream);
+
+// ----- expert index (moe_index.cu) -------------------------------------------
+size_t index_workspace_bytes(int64_t n, int32_t E);
+cudaError_t launch_build_index(const int32_t* expert_ids, int32_t* offsets,
+                               int32_t* token_index, void* workspace, int64_t n, int32_t E,
+                               uint32_t* status, cudaStream_t stream);
+
+}  // namespace situ

@@ -1,0 +1,91 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, and its host-side argument checks answer before any device work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from situ_glu_activation_gb300 import _native
+from situ_glu_activation_gb300.build import INCLUDE
+
+HEADER = os.path.join(INCLUDE, "situ.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(situ_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for must in ["situ_glu_act", "situ_ffn_forward", "situ_moe_grouped_forward",
+                 "situ_moe_build_index", "situ_device_status"]:
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(situ_lib):
+    names = declared_functions()
+    assert set(names) == set(_native.SIGNATURES), "binding and header disagree"
+    for n in names:
+        assert hasattr(situ_lib, n), f"libsitu.so does not export {n}"
+
+
+def test_version_and_status_strings(situ_lib):
+    assert situ_lib.situ_abi_version() == 1
+    for code, name in _native.STATUS_NAMES.items():
+        assert situ_lib.situ_status_string(code).decode() == name
+    assert situ_lib.situ_status_string(99).decode() == "SITU_ERR_UNKNOWN"
+
+
+def test_workspace_sizes(situ_lib):
+    assert situ_lib.situ_ffn_workspace_size(16384, 2048, 3072, 0) == 16384 * 3072 * 2
+    assert situ_lib.situ_ffn_workspace_size(3, 8, 5, 1) == 256  # fp32 h, rounded to 256 B
+    assert situ_lib.situ_ffn_workspace_size(0, 8, 8, 0) == 0
+    R, E, M, I = 1000, 7, 64, 96
+    expect = 256 + ((R * M * 2 + 255) // 256) * 256 + ((R * I * 2 + 255) // 256) * 256
+    assert situ_lib.situ_moe_workspace_size(R, E, M, I, 0) == expect
+    assert situ_lib.situ_moe_workspace_size(R, E, M, I, 1) == 0  # grouped path is bf16 only
+    assert situ_lib.situ_moe_index_workspace_size(1024, 10) == 256
+    assert situ_lib.situ_moe_index_workspace_size(1025, 10) == 256
+
+
+BAD, ALIAS, WS = 1, 3, 8
+
+
+@pytest.mark.parametrize("beta,lbeta", [(0.0, 25.0), (4.0, -1.0), (float("nan"), 25.0),
+                                        (4.0, float("inf")), (1e10, 1e10)])
+def test_caps_must_be_positive_and_finite(situ_lib, beta, lbeta):
+    # Rejected before any pointer is touched (the problem page: both caps positive).
+    assert situ_lib.situ_glu_act(16, 32, 4, 8, beta, lbeta, 0, None) == BAD
+    assert situ_lib.situ_ffn_forward(16, 16, 16, 16, 16, 0, 4, 8, 8, beta, lbeta, 0, None) == BAD
+
+
+def test_argument_checks(situ_lib):
+    f = situ_lib.situ_glu_act
+    assert f(None, None, 0, 8, 4.0, 25.0, 0, None) == 0          # zero rows: no-op
+    assert f(None, None, 4, 8, 4.0, 25.0, 0, None) == BAD        # null pointers
+    assert f(4096, 8192, 4, 0, 4.0, 25.0, 0, None) == BAD        # I < 1
+    assert f(4096, 8192, 4, 8, 4.0, 25.0, 7, None) == BAD        # bad dtype
+    # out overlapping gate_up: [4096, 4096 + 4*16*2) vs out at 4096 + 64
+    assert f(4096, 4096 + 64, 4, 8, 4.0, 25.0, 0, None) == ALIAS
+    g = situ_lib.situ_ffn_forward
+    # workspace too small / misaligned
+    assert g(1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20, 10, 4, 8, 8, 4.0, 25.0, 0, None) == WS
+    assert g(1 << 20, 2 << 20, 3 << 20, 4 << 20, (5 << 20) + 16, 1 << 20, 4, 8, 8, 4.0, 25.0, 0,
+             None) == WS
+    # y overlapping x
+    assert g(1 << 20, 2 << 20, 3 << 20, (1 << 20) + 32, 5 << 20, 1 << 20, 4, 8, 8, 4.0, 25.0, 0,
+             None) == ALIAS
+    m = situ_lib.situ_moe_grouped_forward
+    assert m(0, 0, 0, 0, 0, 0, 0, 0, 4, 2, 3, 8, 8, 4.0, 25.0, 1, None) == 6  # fp32: unsupported
+    assert m(0, 0, 0, 0, 0, 0, 0, 0, 0, 2, 3, 8, 8, 4.0, 25.0, 0, None) == 0  # no tokens
+    b = situ_lib.situ_moe_build_index
+    assert b(0, 0, 0, 0, 0, 10, 0, None) == BAD   # E = 0
+    assert b(1 << 20, 2 << 20, 3 << 20, 0, 0, 10, 4, None) == WS
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="not found"):
+        _native.lib(str(tmp_path / "libsitu.so"))

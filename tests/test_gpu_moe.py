@@ -1,0 +1,131 @@
+"""Expert index and grouped SiTU-GLU experts on the GPU against the FP64 oracle.
+
+Indices: bit-exact.  Outputs: |y - ref| <= 2e-2 (1 + |ref|)."""
+import numpy as np
+import pytest
+import torch
+
+import situ_glu_activation_gb300 as situ
+from situ_glu_activation_gb300 import workloads as wl
+from numerics import assert_ffn_close, oracle_input, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _index(ids_cpu, E, dev):
+    off, tix = situ.situ_moe_build_index(ids_cpu.to(dev).contiguous(), E)
+    torch.cuda.synchronize()
+    return off.cpu().numpy(), tix.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["grouped", "k3_decode", "k3_prefill"])
+def test_index_bit_exact_full_size(oracle, cuda_dev, name):
+    w = wl.WORKLOADS[name]
+    ids = wl.routes(w, seed=0)
+    off, tix = _index(ids, w.num_experts, cuda_dev)
+    ref_off, ref_tix = oracle.moe_build_index(ids.numpy(), w.num_experts)
+    assert np.array_equal(off, ref_off)
+    assert np.array_equal(tix, ref_tix)
+    if name == "grouped":
+        assert (np.diff(off) == 0).sum() >= 4  # the forced-empty experts
+
+
+@pytest.mark.parametrize("n,E", [(0, 5), (1, 1), (1000, 3), (1025, 17), (4097, 900), (3000, 16384)])
+def test_index_edge_sizes(oracle, cuda_dev, n, E):
+    g = torch.Generator().manual_seed(n + E)
+    ids = torch.randint(0, E, (n,), generator=g, dtype=torch.int32)
+    off, tix = _index(ids, E, cuda_dev)
+    ref_off, ref_tix = oracle.moe_build_index(ids.numpy(), E)
+    assert np.array_equal(off, ref_off) and np.array_equal(tix, ref_tix)
+
+
+def test_index_bad_id_reported(cuda_dev):
+    ids = torch.tensor([0, 1, 7, 1], dtype=torch.int32)
+    off, tix = _index(ids, 3, cuda_dev)
+    assert situ.device_status(clear=True) == 7  # SITU_ERR_INDEX
+    assert off[-1] == 3  # the bad route was dropped
+
+
+def _grouped(x, ids, wgu, wd, dev):
+    E = wgu.shape[0]
+    ids_d = ids.to(dev).contiguous()
+    off, tix = situ.situ_moe_build_index(ids_d, E)
+    y = situ.situ_moe_grouped_forward(x.to(dev), off, tix, wgu.to(dev), wd.to(dev), ids.shape[1])
+    torch.cuda.synchronize()
+    return y
+
+
+@pytest.mark.parametrize("T,k,E,M,I", [
+    (50, 3, 6, 256, 384),    # some experts with a single row
+    (300, 2, 3, 128, 256),   # groups spanning several 128-row tiles with tails
+    (40, 4, 9, 136, 200),    # ragged K and N
+])
+def test_grouped_small(oracle, cuda_dev, T, k, E, M, I):
+    g = torch.Generator().manual_seed(T * k + E)
+    ids = torch.stack([torch.randperm(E - 1, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    x = wl.normal((T, M), 1.0, seed=T)
+    wgu, wd = wl.expert_weights(E, M, I, seed=E)
+    y = _grouped(x, ids, wgu, wd, cuda_dev)
+    ref = oracle.moe_grouped_forward(oracle_input(x), ids.numpy(), oracle_input(wgu),
+                                     oracle_input(wd))
+    assert_ffn_close(to_f64(y), ref, f"grouped {T}x{k} E={E}")
+
+
+def test_grouped_equals_dense_per_expert(cuda_dev):
+    """Grouped vs naive on the GPU: each (token, slot) row equals the dense FFN of
+    that expert applied to the token (same kernels, same rounding of h)."""
+    T, k, E, M, I = 64, 2, 4, 256, 256
+    g = torch.Generator().manual_seed(1)
+    ids = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    x = wl.normal((T, M), 1.0, seed=2)
+    wgu, wd = wl.expert_weights(E, M, I, seed=3)
+    y = _grouped(x, ids, wgu, wd, cuda_dev).cpu()
+    for e in range(E):
+        ye = situ.situ_ffn_forward(x.to(cuda_dev), wgu[e].to(cuda_dev), wd[e].to(cuda_dev)).cpu()
+        t_idx, s_idx = (ids == e).nonzero(as_tuple=True)
+        assert torch.equal(y[t_idx, s_idx].view(torch.int16), ye[t_idx].view(torch.int16))
+
+
+def _sample_check(oracle, w, dev, n_sample, seed=0):
+    ids = wl.routes(w, seed=seed)
+    E = w.num_experts
+    x = wl.normal((w.T, w.M), 1.0, seed=seed, device=dev)
+    wgu, wd = wl.expert_weights(E, w.M, w.I, seed=seed, device=dev)
+    off, tix = situ.situ_moe_build_index(ids.to(dev), E)
+    y = situ.situ_moe_grouped_forward(x, off, tix, wgu, wd, w.k_eff)
+    torch.cuda.synchronize()
+    off_c = off.cpu().numpy()
+    tix_c = tix.cpu().numpy()
+    g = torch.Generator().manual_seed(seed + 99)
+    # first and last row of several groups, plus random rows
+    nonempty = np.flatnonzero(np.diff(off_c) > 0)
+    pick = list(off_c[nonempty[:8]]) + list(off_c[nonempty[-8:] + 1] - 1)
+    pick += torch.randint(0, w.T * w.k_eff, (n_sample - len(pick),), generator=g).tolist()
+    for r in pick:
+        flat = int(tix_c[r])
+        t, s = divmod(flat, w.k_eff)
+        e = int(ids[t, s])
+        ref = oracle.ffn_forward(oracle_input(x[t:t + 1].cpu()), oracle_input(wgu[e].cpu()),
+                                 oracle_input(wd[e].cpu()))
+        assert_ffn_close(to_f64(y[t, s:s + 1]), ref, f"{w.name}: row {r} (t={t}, s={s}, e={e})")
+
+
+def test_grouped_zipf_full_size_sampled(oracle, cuda_dev):
+    _sample_check(oracle, wl.WORKLOADS["grouped"], cuda_dev, 40)
+
+
+def test_k3_decode_full_size_sampled(oracle, cuda_dev):
+    _sample_check(oracle, wl.WORKLOADS["k3_decode"], cuda_dev, 40)
+
+
+def test_bad_offsets_write_nothing(cuda_dev):
+    T, k, E, M, I = 8, 2, 3, 64, 64
+    x = wl.normal((T, M), 1.0, seed=0, device=cuda_dev)
+    wgu, wd = wl.expert_weights(E, M, I, seed=0, device=cuda_dev)
+    off = torch.tensor([0, 10, 5, 16], dtype=torch.int32, device=cuda_dev)  # not monotone
+    tix = torch.arange(T * k, dtype=torch.int32, device=cuda_dev)
+    y = torch.full((T, k, M), 7.0, dtype=torch.bfloat16, device=cuda_dev)
+    situ.situ_moe_grouped_forward(x, off, tix, wgu, wd, k, y=y)
+    torch.cuda.synchronize()
+    assert situ.device_status(clear=True) == 7
+    assert bool((y == 7.0).all())
