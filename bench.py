@@ -1,0 +1,520 @@
+#!/usr/bin/env python
+"""Benchmark of the SiTU-GLU expert feed-forward on GB300.
+
+One step = one dense SiTU-GLU FFN forward over 16384 tokens (M=2048, I=3072,
+bf16): the tcgen05 gate_up GEMM with the activation fused into its epilogue,
+then the tcgen05 down GEMM.  ``value`` is tokens/s of that step, device-timed
+with CUDA events, L2 flushed between steps.  The same JSON line also carries:
+  * ``act``: the standalone activation on [65536, 2x3072] bf16 (GB/s, HBM roofline);
+  * ``moe``: the grouped expert paths (index build + grouped FFN) on the Zipf
+    top-8 64-expert workload and on the Kimi-K3-shaped layer (896 routed + 2
+    shared experts) at 512 and 32768 tokens;
+  * ``roofline`` of the dominant kernel (the fused gate_up GEMM);
+  * ``e2e``: the public ``situ_ffn_forward`` call with host (pinned) buffers,
+    host->device copy of x and device->host copy of y inside the timed region;
+  * ``cpu_baseline``: the FP64 CPU oracle on a bounded sample of the same rows.
+
+``--impl reference`` times the FP64 CPU oracle itself (the reference arm) on the
+same workload, a bounded sample of rows per step.
+
+Multi-GPU (torchrun): every rank runs the same per-GPU workload (replicas, weak
+scaling, no collective on the data path); the step time is the max over ranks
+and value the tokens of all ranks over that time.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "expert-FFN tokens/s + TFLOP/s (% bf16 TC peak); SiTU act GB/s (% HBM)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+FLOP_PER_ROW = 6  # x (2*M*2I + 2*I*M) = 6*M*I per row
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas; the only collectives are the timing barrier
+# and the max/sum reductions of the result)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_ms: float, local_units: float, world: int):
+    """Max of the step time and sum of the work over ranks (identity at world 1)."""
+    if world <= 1:
+        return local_ms, local_units
+    import torch
+    import torch.distributed as dist
+
+    backend = dist.get_backend()
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else None
+    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, L2
+# ---------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if self.proc is None or self.tmp is None:
+            return None
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            rows = [r for r in csv.reader(f) if len(r) >= 9]
+        os.unlink(self.tmp.name)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, smax, reasons = [], 0.0, set()
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax = max(smax, float(r[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_digest(*names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "situ_glu_activation_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, digest: str, units: float):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/traffic.txt), if it was captured on the current kernel source;
+    else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        with open(path) as f:
+            for line in f:
+                parts = line.split("#", 1)[0].split()
+                if len(parts) >= 3 and parts[0] == kernel and parts[1] == digest:
+                    return float(parts[2]) * units
+    except (OSError, ValueError):
+        return None
+    return None
+
+
+# ---------------------------------------------------------------------------
+# timing
+# ---------------------------------------------------------------------------
+def timed_steps(step, K: int, W: int, flush, world: int, inner: int = 0):
+    """W untimed warm-up steps, then K device-timed steps (CUDA events on the
+    current stream, L2 flushed before each).  `step(marks)` may record `inner`
+    extra events between its launches.  Returns (per-step ms, per-segment ms)."""
+    import torch
+
+    for _ in range(W):
+        flush()
+        step(None)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    per_step, segs = [], [[] for _ in range(inner + 1)]
+    for _ in range(K):
+        flush()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(inner + 2)]
+        ev[0].record()
+        step(ev[1:-1] if inner else None)
+        ev[-1].record()
+        ev[-1].synchronize()
+        per_step.append(ev[0].elapsed_time(ev[-1]))
+        for i in range(inner + 1):
+            segs[i].append(ev[i].elapsed_time(ev[i + 1]))
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    return per_step, segs
+
+
+def mean(v):
+    return sum(v) / len(v)
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+def bench_dense(args, dev, peaks, world, flush):
+    import torch
+
+    import situ_glu_activation_gb300 as situ
+    from situ_glu_activation_gb300 import workloads as wl
+
+    w = wl.WORKLOADS["dense"]
+    x, wgu, wd = wl.ffn_inputs(w.M, w.I, w.rows, seed=0, device=dev)
+    h = torch.empty(w.rows, w.I, dtype=torch.bfloat16, device=dev)
+    y = torch.empty_like(x)
+
+    def step(marks):
+        situ.situ_ffn_gate_up(x, wgu, wl.BETA, wl.LINEAR_BETA, h=h)
+        if marks:
+            marks[0].record()
+        situ.situ_ffn_down(h, wd, y=y)
+
+    per_step, (t_gu, t_down) = timed_steps(step, args.steps, args.warmup, flush, world, inner=1)
+    ms = mean(per_step)
+    flop_gu = 2.0 * w.rows * w.M * 2 * w.I
+    flop_down = 2.0 * w.rows * w.I * w.M
+    out = {
+        "ms": ms, "tokens": w.rows, "launches_per_step": 2,
+        "gate_up_ms": mean(t_gu), "down_ms": mean(t_down),
+        "tflops": (flop_gu + flop_down) / (ms * 1e-3) / 1e12,
+        "gate_up_tflops": flop_gu / (mean(t_gu) * 1e-3) / 1e12,
+        "down_tflops": flop_down / (mean(t_down) * 1e-3) / 1e12,
+        "flop_gate_up": flop_gu,
+    }
+
+    # End to end through the public call with host buffers.
+    x_h = x.cpu().pin_memory()
+    y_h = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    x_d = torch.empty_like(x)
+    ws = torch.empty(situ.ffn_workspace_bytes(w.rows, w.M, w.I), dtype=torch.uint8, device=dev)
+
+    def e2e_step(_):
+        x_d.copy_(x_h, non_blocking=True)
+        situ.situ_ffn_forward(x_d, wgu, wd, wl.BETA, wl.LINEAR_BETA, y=y_d, workspace=ws)
+        y_h.copy_(y_d, non_blocking=True)
+
+    y_d = torch.empty_like(x)
+    e2e_ms, _ = timed_steps(e2e_step, args.steps, args.warmup, flush, world)
+    out["e2e_ms"] = mean(e2e_ms)
+    out["h2d_bytes"] = x.numel() * x.element_size()
+    out["d2h_bytes"] = y.numel() * y.element_size()
+    return out, w
+
+
+def bench_act(args, dev, peaks, world, flush):
+    import torch
+
+    import situ_glu_activation_gb300 as situ
+    from situ_glu_activation_gb300 import workloads as wl
+
+    w = wl.WORKLOADS["act"]
+    g = wl.gate_up_input(w, seed=0, device=dev)
+    o = torch.empty(w.rows, w.I, dtype=torch.bfloat16, device=dev)
+    per_step, _ = timed_steps(lambda m: situ.situ_glu_act(g, wl.BETA, wl.LINEAR_BETA, out=o),
+                              args.steps, args.warmup, flush, world)
+    ms = mean(per_step)
+    nbytes = 3 * w.rows * w.I * 2  # read 2I, write I per row, bf16
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "ms": ms, "bytes": nbytes, "gbs": gbs,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}}
+
+
+def bench_moe(args, dev, peaks, world, flush, names):
+    import torch
+
+    import situ_glu_activation_gb300 as situ
+    from situ_glu_activation_gb300 import workloads as wl
+
+    results = {}
+    weights = {}
+    for name in names:
+        w = wl.WORKLOADS[name]
+        E = w.num_experts
+        key = (E, w.M, w.I)
+        if key not in weights:
+            weights.clear()
+            torch.cuda.empty_cache()
+            weights[key] = wl.expert_weights(E, w.M, w.I, seed=0, device=dev)
+        wgu, wd = weights[key]
+        ids_cpu = wl.routes(w, seed=0)
+        ids = ids_cpu.to(dev)
+        x = wl.normal((w.T, w.M), 1.0, seed=0, device=dev)
+        R = w.T * w.k_eff
+        off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        tix = torch.empty(R, dtype=torch.int32, device=dev)
+        y = torch.empty(w.T, w.k_eff, w.M, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(situ.moe_workspace_bytes(R, E, w.M, w.I), dtype=torch.uint8, device=dev)
+
+        def step(marks):
+            situ.situ_moe_build_index(ids, E, expert_offsets=off, token_index=tix)
+            if marks:
+                marks[0].record()
+            situ.situ_moe_grouped_forward(x, off, tix, wgu, wd, w.k_eff, wl.BETA, wl.LINEAR_BETA,
+                                          y=y, workspace=ws)
+
+        per_step, (t_idx, t_ffn) = timed_steps(step, args.steps, args.warmup, flush, world,
+                                               inner=1)
+        ms = mean(per_step)
+        counts = torch.bincount(ids_cpu.view(-1).long(), minlength=E)
+        touched = int((counts > 0).sum())
+        wbytes = touched * 3 * w.M * w.I * 2
+        flop = FLOP_PER_ROW * R * w.M * w.I
+        tflops = flop / (ms * 1e-3) / 1e12
+        weight_gbs = wbytes / (ms * 1e-3) / 1e9
+        results[name] = {
+            "workload": w.name, "ms": ms, "index_ms": mean(t_idx), "ffn_ms": mean(t_ffn),
+            "tokens": w.T, "routes": R, "experts_touched": touched,
+            "tokens_per_s": w.T / (ms * 1e-3), "tflops": tflops,
+            "tc_frac": tflops / peaks["bf16_tflops"],
+            "weight_gbs": weight_gbs, "hbm_frac": weight_gbs / peaks["hbm_gbs"],
+            "launches_per_step": 3 + 4,
+        }
+        del x, y, ws, off, tix, ids
+    weights.clear()
+    torch.cuda.empty_cache()
+    return results
+
+
+def cpu_baseline(seconds: float, rows_hint: int = 0):
+    """The FP64 oracle (as it stands) on a bounded sample of the dense workload's
+    rows: rows/s = tokens/s on the host cores."""
+    import numpy as np
+    import torch
+
+    from oracle import Oracle
+    from situ_glu_activation_gb300 import workloads as wl
+
+    o = Oracle()
+    w = wl.WORKLOADS["dense"]
+    x, wgu, wd = wl.ffn_inputs(w.M, w.I, w.rows, seed=0)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    xb, wgb, wdb = bits(x), bits(wgu), bits(wd)
+    threads = o.num_threads()
+    n = rows_hint or max(threads, 8)
+    t0 = time.perf_counter()
+    o.ffn_forward(xb[:n], wgb, wdb)
+    dt = time.perf_counter() - t0
+    if not rows_hint and dt < seconds:
+        n2 = min(w.rows, max(n, int(n * seconds / max(dt, 1e-3))))
+        t0 = time.perf_counter()
+        o.ffn_forward(xb[:n2], wgb, wdb)
+        dt = time.perf_counter() - t0
+        n = n2
+    return {"value": n / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {n} of the 16384 token rows of the dense workload "
+                      f"(FP64 gate_up, SiTU-GLU, down), {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import torch
+
+    from oracle import Oracle
+    from situ_glu_activation_gb300 import workloads as wl
+
+    o = Oracle()
+    w = wl.WORKLOADS["dense"]
+    x, wgu, wd = wl.ffn_inputs(w.M, w.I, w.rows, seed=0)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    xb, wgb, wdb = bits(x), bits(wgu), bits(wd)
+    rows = args.ref_rows or max(o.num_threads(), 4)
+    for i in range(args.warmup):
+        o.ffn_forward(xb[i * rows:(i + 1) * rows], wgb, wdb)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        r0 = (i * rows) % (w.rows - rows)
+        o.ffn_forward(xb[r0:r0 + rows], wgb, wdb)
+    dt = time.perf_counter() - t0
+    value = args.steps * rows / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.rows, "M": w.M, "I": w.I,
+                   "beta": wl.BETA, "linear_beta": wl.LINEAR_BETA,
+                   "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": o.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{rows} token rows per step of the dense workload"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_situ(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    import situ_glu_activation_gb300 as situ
+    from situ_glu_activation_gb300 import workloads as wl
+    from situ_glu_activation_gb300.build import build
+
+    build()
+    peaks, peak_src = load_peaks()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.fill_(1)
+
+    with ClockSampler(dev.index or 0) as clk:
+        dense, w = bench_dense(args, dev, peaks, world, flush)
+    clocks = clk.summary()
+    ms_max, tokens_all = aggregate(dense["ms"], float(dense["tokens"]), world)
+    value = tokens_all / (ms_max * 1e-3)
+    e2e_ms, _ = aggregate(dense["e2e_ms"], 0.0, world)
+
+    act = bench_act(args, dev, peaks, world, flush) if args.suite == "full" else None
+    moe = (bench_moe(args, dev, peaks, world, flush, ["grouped", "k3_decode", "k3_prefill"])
+           if args.suite == "full" else None)
+    status = situ.device_status(clear=True)
+
+    achieved = dense["gate_up_tflops"]
+    digest = source_digest("gemm.cu", "situ_math.cuh", "situ_ptx.cuh")
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic: seeded x ~ N(0,1), weights ~ N(0, 1/fan_in); no dataset",
+        "config": {"workload": w.name, "tokens": w.rows, "M": w.M, "I": w.I,
+                   "beta": wl.BETA, "linear_beta": wl.LINEAR_BETA,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)"},
+        "tflops": dense["tflops"],
+        "tc_frac": dense["tflops"] / peaks["bf16_tflops"],
+        "kernels": {"ffn_gate_up_situ": {"ms": dense["gate_up_ms"],
+                                         "tflops": dense["gate_up_tflops"]},
+                    "ffn_down": {"ms": dense["down_ms"], "tflops": dense["down_tflops"]}},
+        "roofline": {"bound": "tensor", "kernel": "ffn_gate_up_situ (fused gate_up GEMM + "
+                     "SiTU-GLU epilogue)", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                     "peak_source": f"{peak_src} (bf16 dense, burst)",
+                     "traffic": profiled_traffic("ffn_gate_up_situ", digest, w.rows)},
+        "e2e": {"value": tokens_all / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": dense["h2d_bytes"],
+                "d2h_bytes_per_step": dense["d2h_bytes"],
+                "call": "situ_ffn_forward with pinned host x, y"},
+        "gpu_launches": dense["launches_per_step"] * args.steps,
+        "clocks": clocks,
+        "device_status": status,
+    }
+    if act:
+        line["act"] = act
+    if moe:
+        line["moe"] = moe
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["situ", "reference"], default="situ")
+    ap.add_argument("--suite", choices=["full", "dense"], default="full")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-rows", type=int, default=0, help="oracle rows per reference step")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_situ(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
