@@ -165,6 +165,42 @@ situ_status situ_ffn_down(const void* h, const void* W_down, void* y, int64_t R,
                           int64_t I, situ_dtype dt, void* stream);
 
 /* -------------------------------------------------------------------------
+ * situ_ffn_forward_noalloc -- situ_ffn_forward for callers that cannot allocate
+ * device memory.  The pages have no counterpart: this is a library service.
+ *
+ * Some callers have no way to hand the library a workspace: a plugin whose
+ * enqueue hook runs inside another engine's execution phase, where every buffer
+ * was planned before execution began; a latency-bound serving loop that must not
+ * call cudaMalloc (it can synchronise the whole device); code with no allocator
+ * of its own.  For them this call keeps the intermediate h in a scratch array
+ * built into the library: a file-scope device array of SITU_NOALLOC_SCRATCH_BYTES
+ * bytes that every GPU which loads libsitu holds until the process exits.  The
+ * call itself allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.
+ *
+ *   x, W_gate_up, W_down, y, R, M, I, beta, linear_beta, dt, stream: exactly as
+ *   situ_ffn_forward (same shapes, alignment rules and result).
+ *   The caller still passes (and owns) every input and output.
+ *   Limit: R * I * sizeof(dt) <= SITU_NOALLOC_SCRATCH_BYTES (at I = 3072 and bf16,
+ *   up to 2730 rows); larger calls return SITU_ERR_WORKSPACE and launch nothing.
+ *
+ * Set-up: the first call on a device, with that device current, looks up the
+ * scratch array's device address once (cudaGetSymbolAddress) and caches it; make
+ * that first call before any stream capture on the device.
+ * Sharing: every call on a device uses the same scratch array, which keeps the
+ * previous call's h.  Nothing in it needs to start at zero (each call writes every
+ * h element it reads), but two calls whose kernels overlap on the GPU (different
+ * streams without ordering) race on it: order them on one stream or with events.
+ * Errors: those of situ_ffn_forward, with SITU_ERR_WORKSPACE for a size above
+ * the limit.
+ * ------------------------------------------------------------------------- */
+#define SITU_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB */
+
+situ_status situ_ffn_forward_noalloc(const void* x, const void* W_gate_up, const void* W_down,
+                                     void* y, int64_t R, int64_t M, int64_t I, float beta,
+                                     float linear_beta, situ_dtype dt, void* stream);
+
+/* -------------------------------------------------------------------------
  * situ_moe_build_index -- expert index of a routed batch.
  *
  * Operation: a stable counting sort of the n_routes = T * k_eff flat routes

@@ -35,6 +35,8 @@ SIGNATURES = {
                          _ci),
     "situ_ffn_gate_up": ([_vp, _vp, _vp, _i64, _i64, _i64, _f32, _f32, _ci, _vp], _ci),
     "situ_ffn_down": ([_vp, _vp, _vp, _i64, _i64, _i64, _ci, _vp], _ci),
+    "situ_ffn_forward_noalloc": ([_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _f32, _ci, _vp],
+                                 _ci),
     "situ_moe_index_workspace_size": ([_i64, _i32], _sz),
     "situ_moe_build_index": ([_vp, _vp, _vp, _vp, _sz, _i64, _i32, _vp], _ci),
     "situ_moe_workspace_size": ([_i64, _i32, _i64, _i64, _ci], _sz),

@@ -405,3 +405,21 @@ situ_status situ_selftest_bounded_wait(uint32_t limit_us, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Internal accessors for other translation units of the library.
+// ---------------------------------------------------------------------------
+namespace situ {
+
+situ_status current_device_context(int* num_sms, uint32_t** status) {
+  DeviceState* st = nullptr;
+  situ_status s = device_state(&st);
+  if (s != SITU_OK) return s;
+  *num_sms = st->num_sms;
+  *status = st->status;
+  return SITU_OK;
+}
+
+situ_status report_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
+}  // namespace situ

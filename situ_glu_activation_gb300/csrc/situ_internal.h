@@ -77,3 +77,14 @@ cudaError_t launch_build_index(const int32_t* expert_ids, int32_t* offsets,
                                uint32_t* status, cudaStream_t stream);
 
 }  // namespace situ
+
+namespace situ {
+
+// ----- shared with abi.cu ------------------------------------------------------
+// SM count and device address of the status word of the current device (the
+// library's one-time per-device set-up runs on first use; it allocates nothing).
+situ_status current_device_context(int* num_sms, uint32_t** status);
+// Record a CUDA error for situ_last_cuda_error() and return SITU_ERR_CUDA.
+situ_status report_cuda_error(cudaError_t e);
+
+}  // namespace situ
