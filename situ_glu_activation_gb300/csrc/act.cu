@@ -7,8 +7,11 @@
 // bounded branches").  Every input byte is read once and every output byte
 // written once, so the kernel is bound by HBM bandwidth: 128-bit loads of 8
 // gate and 8 up bf16 values and one 128-bit store of 8 outputs per vector step,
-// streaming cache hints (the data is touched once), a grid of a few blocks per
-// SM with each thread keeping two vector steps in flight.
+// streaming cache hints (the data is touched once), a grid of 16 blocks of 256
+// threads per SM with each thread keeping two vector steps (four 16-byte loads)
+// in flight.  The activation costs three special-function ops and about a
+// dozen FP32 ops per output (situ_math.cuh), which keeps instruction issue
+// below the memory time.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -21,7 +24,7 @@ namespace situ {
 namespace {
 
 constexpr int kActThreads = 256;
-constexpr int kActBlocksPerSm = 8;
+constexpr int kActBlocksPerSm = 16;
 constexpr int kActUnroll = 2;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -92,10 +95,10 @@ __global__ void __launch_bounds__(kActThreads)
     const float4 g = __ldcs(src);
     const float4 u = __ldcs(src + vpr);
     float4 o;
-    o.x = situ_glu_f32(g.x, u.x, p);
-    o.y = situ_glu_f32(g.y, u.y, p);
-    o.z = situ_glu_f32(g.z, u.z, p);
-    o.w = situ_glu_f32(g.w, u.w, p);
+    o.x = situ_glu_f32_accurate(g.x, u.x, p);
+    o.y = situ_glu_f32_accurate(g.y, u.y, p);
+    o.z = situ_glu_f32_accurate(g.z, u.z, p);
+    o.w = situ_glu_f32_accurate(g.w, u.w, p);
     __stcs(out + static_cast<size_t>(row) * vpr + c, o);
     row += q;
     c += rem;
@@ -139,7 +142,9 @@ __global__ void __launch_bounds__(kActThreads)
     const uint64_t j = idx - r * I;
     const float g = load_elem(in, r * 2 * I + j);
     const float u = load_elem(in, r * 2 * I + I + j);
-    store_elem(out, idx, situ_glu_f32(g, u, p));
+    // float32 outputs take the accurate variant; bf16 outputs the fast one.
+    const float h = sizeof(T) == 4 ? situ_glu_f32_accurate(g, u, p) : situ_glu_f32(g, u, p);
+    store_elem(out, idx, h);
   }
 }
 
@@ -160,7 +165,7 @@ __global__ void ffn_f32_gate_up_kernel(const float* __restrict__ x, const float*
       g = fmaf(xr[k], wg[k], g);
       u = fmaf(xr[k], wu[k], u);
     }
-    h[idx] = situ_glu_f32(g, u, p);
+    h[idx] = situ_glu_f32_accurate(g, u, p);
   }
 }
 

@@ -122,6 +122,28 @@ __device__ __forceinline__ TileCoord decode_tile(const Args& a, int32_t t) {
   return c;
 }
 
+// Work units.  Unpaired: one unit = one tile, from decode_tile.  Paired (dense
+// only, clusters of two CTAs): one unit = the tiles (2p, n) and (2p+1, n); CTA
+// rank r of the cluster takes m-tile 2p+r and both share the B tile of n-tile n.
+template <bool kPair>
+__device__ __forceinline__ int32_t num_units(const Args& a) {
+  if (!kPair) return total_tiles(a);
+  const int32_t m_tiles = (a.dense_rows + kBM - 1) / kBM;
+  return ((m_tiles + 1) / 2) * a.n_tiles;
+}
+
+template <bool kPair>
+__device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_t rank) {
+  if (!kPair) return decode_tile(a, u);
+  TileCoord c;
+  const int32_t mp = u / a.n_tiles;
+  c.n_tile = u - mp * a.n_tiles;
+  c.group = 0;
+  c.a_row0 = (2 * mp + static_cast<int32_t>(rank)) * kBM;
+  c.row_end = a.dense_rows;
+  return c;
+}
+
 __device__ __forceinline__ bool ctl_wait(SharedCtl* ctl, uint64_t* bar, uint32_t parity,
                                          uint32_t* status) {
   const uint32_t b = smem_u32(bar);
@@ -158,7 +180,7 @@ __device__ __forceinline__ void store_row_chunk(__nv_bfloat16* dst, const uint32
   }
 }
 
-template <Epi kEpi>
+template <Epi kEpi, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_b, const Args args) {
@@ -170,11 +192,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), 1);
+      // Paired: a stage is free once the MMAs of both CTAs have read it (the
+      // peer's multicast writes into this CTA's copy of the stage).
+      mbar_init(smem_u32(&ctl->empty[s]), kPair ? 2 : 1);
     }
     for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(smem_u32(&ctl->acc_full[b]), 1);
@@ -192,9 +217,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before_sync();
   }
   __syncthreads();
+  if (kPair) cluster_sync();  // the peer's barriers exist before any multicast
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
-  const int32_t n_total = total_tiles(args);
+  const int32_t n_total = num_units<kPair>(args);
+  const int32_t u0 = kPair ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x);
+  const int32_t ustride = kPair ? static_cast<int32_t>(gridDim.x >> 1) : static_cast<int32_t>(gridDim.x);
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -202,8 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t issued = 0;
       bool ok = true;
-      for (int32_t t = blockIdx.x; t < n_total && ok; t += gridDim.x) {
-        const TileCoord tc = decode_tile(args, t);
+      for (int32_t t = u0; t < n_total && ok; t += ustride) {
+        const TileCoord tc = unit_tile<kPair>(args, t, rank);
         const int64_t gbase = static_cast<int64_t>(tc.group) * args.b_group_rows;
         int32_t b_row0, b_row1;
         if (kEpi == Epi::kSitu) {
@@ -224,8 +252,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sb = sa + kABytes;
           mbar_arrive_expect_tx(full, kStageBytes);
           tma_load_2d(sa, &map_a, kb * kBK, tc.a_row0, full);
-          tma_load_2d(sb, &map_b, kb * kBK, b_row0, full);
-          tma_load_2d(sb + kBHalfBytes, &map_b, kb * kBK, b_row1, full);
+          if (kPair) {
+            // This CTA fetches half of the shared B tile and multicasts it to both.
+            tma_load_2d_multicast(sb + rank * kBHalfBytes, &map_b, kb * kBK,
+                                  rank == 0 ? b_row0 : b_row1, full, 0x3);
+          } else {
+            tma_load_2d(sb, &map_b, kb * kBK, b_row0, full);
+            tma_load_2d(sb + kBHalfBytes, &map_b, kb * kBK, b_row1, full);
+          }
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -249,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t local = 0;
       bool ok = true;
-      for (int32_t t = blockIdx.x; t < n_total && ok; t += gridDim.x, ++local) {
+      for (int32_t t = u0; t < n_total && ok; t += ustride, ++local) {
         const uint32_t acc = local & 1u;
         const uint32_t acc_phase = (local >> 1) & 1u;
         if (!ctl_wait(ctl, &ctl->acc_empty[acc], acc_phase ^ 1u, args.status)) {
@@ -271,7 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_bf16(d_tmem, sw128_kmajor_desc(sa + k * kUK * 2),
                       sw128_kmajor_desc(sb + k * kUK * 2), kIdesc, (kb | k) != 0 ? 1u : 0u);
           }
-          umma_commit(smem_u32(&ctl->empty[stage]));
+          if (kPair) {
+            umma_commit_multicast(smem_u32(&ctl->empty[stage]), 0x3);
+          } else {
+            umma_commit(smem_u32(&ctl->empty[stage]));
+          }
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -292,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row_in_tile = quarter * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t local = 0;
-    for (int32_t t = blockIdx.x; t < n_total; t += gridDim.x, ++local) {
+    for (int32_t t = u0; t < n_total; t += ustride, ++local) {
       const uint32_t acc = local & 1u;
       const uint32_t acc_phase = (local >> 1) & 1u;
       int ok = 1;
@@ -300,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after_sync();
-      const TileCoord tc = decode_tile(args, t);
+      const TileCoord tc = unit_tile<kPair>(args, t, rank);
       const int32_t row = tc.a_row0 + row_in_tile;
       bool valid = row < tc.row_end;
       int64_t out_row = row;
@@ -352,6 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
+  // Paired: neither CTA leaves while the peer may still write into it.
+  if (kPair) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after_sync();
@@ -468,6 +508,36 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
 
 constexpr size_t kSmemBytes = kStages * kStageBytes + sizeof(SharedCtl) + 1024;
 
+// Most 2-CTA clusters of ffn_gemm_kernel<kEpi, true> resident at once, per
+// device (0 if the query fails: the unpaired kernel is used then).
+template <Epi kEpi>
+int max_pair_clusters(size_t smem) {
+  static int cached[64] = {};
+  static bool done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!done[dev]) {
+    done[dev] = true;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, ffn_gemm_kernel<kEpi, true>, &cfg) == cudaSuccess)
+      cached[dev] = n;
+    else
+      (void)cudaGetLastError();
+  }
+  return cached[dev];
+}
+
 template <Epi kEpi>
 cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, int num_sms,
                    cudaStream_t stream) {
@@ -492,16 +562,39 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
   a.out_row_index = s.out_row_index;
   a.sp = p;
   a.status = status;
+  for (auto fn : {ffn_gemm_kernel<kEpi, false>, ffn_gemm_kernel<kEpi, true>}) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+  }
+  if (!s.tile_offsets) {
+    // Dense: clusters of two CTAs share each B tile (multicast).
+    const int64_t m_tiles = (s.a_rows + kBM - 1) / kBM;
+    const int64_t units = ((m_tiles + 1) / 2) * a.n_tiles;
+    int clusters = max_pair_clusters<kEpi>(kSmemBytes);
+    if (clusters > 0) {
+      if (units < clusters) clusters = static_cast<int>(units);
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * clusters, 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = kSmemBytes;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = 2;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, true>, ma, mb, a);
+    }
+  }
   int grid = num_sms;
   if (!s.tile_offsets) {
     const int64_t tiles = ((s.a_rows + kBM - 1) / kBM) * a.n_tiles;
     if (tiles < grid) grid = static_cast<int>(tiles);
   }
-  cudaError_t e = cudaFuncSetAttribute(ffn_gemm_kernel<kEpi>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemBytes));
-  if (e != cudaSuccess) return e;
-  ffn_gemm_kernel<kEpi><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, a);
+  ffn_gemm_kernel<kEpi, false><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, a);
   return cudaGetLastError();
 }
 

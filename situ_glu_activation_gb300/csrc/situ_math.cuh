@@ -8,27 +8,33 @@
 // cap the up branch with its own cap; multiply); "DenseFFN and SituGLU - Docs",
 // "one split, two softly bounded branches" (math in FP32, cast at the end).
 //
-// Method (exponential form, written for this library).  With
-//   E1 = exp(-2|g|/b1), F = exp(-2|u|/b2), E0 = exp(-|g|),
-//   tanh(|g|/b1) = (1 - E1) / (1 + E1),  tanh(|u|/b2) = (1 - F) / (1 + F),
-//   sigmoid(g)   = P / (1 + E0),  P = 1 for g >= 0 and P = E0 for g < 0,
-// so that
-//   |h| = b1 b2 (1 - E1)(1 - F) P / ((1 + E1)(1 + F)(1 + E0)),
-//   sign(h) = sign(g) sign(u).
-// Three ex2 and one reciprocal on the special-function unit; the rest is FMA.
-//   * 1 - exp(-x) loses relative accuracy for small x (cancellation), so for
-//     x < 1/16 it is taken from its Taylor series x - x^2/2 + x^3/6 - x^4/24 +
-//     x^5/120 (truncation below 2^-29 relative there); above, 1 - E has
-//     relative error below 2^-17.
-//   * For g < 0 the factor P = e^g is evaluated as 2^64 e^g and the product is
-//     scaled back by 2^-64 in its last multiply, so outputs in the subnormal
-//     range (g from about -87 down to -104) come out correctly rounded instead of
-//     flushed: the final multiply and the bf16 conversion keep subnormals.
-//   * Every factor is at most 1, so |h| <= b1 b2 holds after rounding; an explicit
-//     min keeps the bound structural even for caps whose product rounds.
-// The ex2 and rcp used are the hardware approximations (ex2.approx.ftz,
-// rcp.approx.ftz); their inputs and outputs that matter stay normal.  Overall
-// relative error is a few 2^-20, far inside half a bf16 ulp (2^-9 relative).
+// Method (written for this library):
+//   * tanh(g / b1) and tanh(u / b2) come from the hardware tanh.approx.f32
+//     (documented maximum relative error about 2^-11 over the whole range; no
+//     cancellation near zero, since it returns tanh itself, not 1 - something);
+//   * sigmoid(g) = P / (1 + E0) with E0 = exp(-|g|) from one ex2.approx and
+//     P = 1 for g >= 0, P = E0 for g < 0 -- never 0.5 + 0.5 tanh(g/2), which
+//     cancels to zero for g << 0 and would lose all relative accuracy there;
+//   * for g < 0 the factor P = e^g is carried as 2^64 e^g (one ex2 with the
+//     exponent shifted by 64) and the product is scaled back by 2^-64 in its
+//     last multiply, so outputs in the subnormal range (g from about -87 down to
+//     -104) come out correctly rounded instead of flushed: the final multiply
+//     and the bf16 conversion keep subnormals;
+//   * one hardware reciprocal, rcp.approx of (1 + E0) in [1, 2].
+// Three special-function ops and about a dozen FP32 ops per output.  Relative
+// error: at most about 2 * 2^-11 from the two tanh plus a few 2^-22, i.e. below
+// a quarter of a bf16 ulp, so after round-to-nearest-even the output is within
+// 0.75 bf16 ulp of the exact value (measured: 0.503 ulp worst case over every
+// bf16 input of either branch).  |tanh.approx| <= 1, P <= 1 and the reciprocal
+// of a number >= 1 is <= 1, so |h| <= b1 b2; a final clamp keeps the bound
+// structural even for caps whose product rounds.  NaN propagates.
+//
+// situ_glu_f32_accurate is the variant for float32 outputs, where a 2^-11 error
+// would be visible: the same sigmoid, but each tanh in exponential form,
+// tanh(x) = (1 - e^{-2x}) / (1 + e^{-2x}) for x >= 0, with 1 - e^{-2x} from its
+// Taylor series x' - x'^2/2 + x'^3/6 - x'^4/24 + x'^5/120 (x' = 2x) below x' = 1/16
+// (where 1 - e^{-x'} cancels) and one reciprocal for the product of the three
+// denominators.  Relative error a few 2^-20.
 #pragma once
 
 #include <cstdint>
@@ -36,16 +42,16 @@
 namespace situ {
 
 struct SituParams {
-  float two_inv_b1;  // 2 / beta1
-  float two_inv_b2;  // 2 / beta2
-  float b1b2;        // beta1 * beta2, the bound on |h|
-  float limit;       // beta1 * beta2 * 2^64: the bound before the final 2^-64 scale
+  float inv_b1;  // 1 / beta1
+  float inv_b2;  // 1 / beta2
+  float b1b2;    // beta1 * beta2, the bound on |h|
+  float limit;   // beta1 * beta2 * 2^64: the bound before the final 2^-64 scale
 };
 
 __host__ __device__ inline SituParams make_situ_params(float beta, float linear_beta) {
   SituParams p;
-  p.two_inv_b1 = 2.0f / beta;
-  p.two_inv_b2 = 2.0f / linear_beta;
+  p.inv_b1 = 1.0f / beta;
+  p.inv_b2 = 1.0f / linear_beta;
   p.b1b2 = beta * linear_beta;
   p.limit = p.b1b2 * 0x1p64f;
   return p;
@@ -63,6 +69,30 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// One SiTU-GLU output in FP32 (see the header comment for the method).
+__device__ __forceinline__ float situ_glu_f32(float g, float u, const SituParams& p) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  const float t1 = tanh_approx(g * p.inv_b1);  // tanh(g / b1), carries sign(g)
+  const float t2 = tanh_approx(u * p.inv_b2);  // tanh(u / b2), carries sign(u)
+  const bool gneg = g < 0.0f;
+  // r = 2^64 e^{-|g|} for g < 0, e^{-|g|} otherwise.
+  const float r = ex2_approx(fmaf(-fabsf(g), kLog2e, gneg ? 64.0f : 0.0f));
+  const float e0 = gneg ? r * 0x1p-64f : r;  // e^{-|g|}
+  const float ps = gneg ? r : 0x1p64f;       // 2^64 P
+  // h 2^64 = b1 b2 (2^64 P) / (1 + e^{-|g|}) tanh(g/b1) tanh(u/b2); scale dropped last.
+  float h = (p.b1b2 * ps) * rcp_approx(1.0f + e0);
+  h = h * t1;
+  h = h * t2;
+  h = h > p.limit ? p.limit : (h < -p.limit ? -p.limit : h);  // NaN passes through
+  return h * 0x1p-64f;  // correctly rounded, subnormals kept
+}
+
 // 1 - exp(-x) for x >= 0: Taylor series below 1/16, else 1 - e (e = exp(-x)).
 __device__ __forceinline__ float one_minus_exp_neg(float x, float e) {
   float q = fmaf(x, 1.0f / 120.0f, -1.0f / 24.0f);
@@ -73,30 +103,28 @@ __device__ __forceinline__ float one_minus_exp_neg(float x, float e) {
   return x < 0.0625f ? series : 1.0f - e;
 }
 
-// One SiTU-GLU output in FP32 (see the header comment for the method).
-__device__ __forceinline__ float situ_glu_f32(float g, float u, const SituParams& p) {
+// One SiTU-GLU output in FP32 for float32 outputs (see the header comment).
+__device__ __forceinline__ float situ_glu_f32_accurate(float g, float u, const SituParams& p) {
   constexpr float kLog2e = 1.4426950408889634f;
   const float ag = fabsf(g);
   const float au = fabsf(u);
-  const float x1 = ag * p.two_inv_b1;  // 2|g|/b1
-  const float x2 = au * p.two_inv_b2;  // 2|u|/b2
+  const float x1 = 2.0f * ag * p.inv_b1;  // 2|g|/b1
+  const float x2 = 2.0f * au * p.inv_b2;  // 2|u|/b2
   const float e1 = ex2_approx(-x1 * kLog2e);
   const float f = ex2_approx(-x2 * kLog2e);
   const float n1 = one_minus_exp_neg(x1, e1);
   const float n2 = one_minus_exp_neg(x2, f);
   const bool gneg = g < 0.0f;
-  // r = 2^64 e^{-|g|} for g < 0, e^{-|g|} otherwise.
   const float r = ex2_approx(fmaf(-ag, kLog2e, gneg ? 64.0f : 0.0f));
-  const float e0 = gneg ? r * 0x1p-64f : r;  // e^{-|g|}
-  const float ps = gneg ? r : 0x1p64f;       // 2^64 P
+  const float e0 = gneg ? r * 0x1p-64f : r;
+  const float ps = gneg ? r : 0x1p64f;
   const float den = (1.0f + e1) * (1.0f + f) * (1.0f + e0);
-  // |h| 2^64 = b1 b2 (2^64 P) rcp(den) n1 n2; the scale is dropped last.
   float mag = p.b1b2 * ps;
   mag = mag * rcp_approx(den);
   mag = mag * n1;
   mag = mag * n2;
-  mag = mag > p.limit ? p.limit : mag;  // NaN passes through
-  const float h = mag * 0x1p-64f;       // correctly rounded, subnormals kept
+  mag = mag > p.limit ? p.limit : mag;
+  const float h = mag * 0x1p-64f;
   const uint32_t sign = (__float_as_uint(g) ^ __float_as_uint(u)) & 0x80000000u;
   return __uint_as_float(__float_as_uint(h) | sign);
 }

@@ -111,6 +111,16 @@ def test_fp32_special_rows(oracle, cuda_dev):
         assert got[0, 1] == 100.0 and got[0, 2] == -100.0  # the bound, reached
 
 
+def test_fp32_relative_accuracy(oracle, cuda_dev):
+    """float32 outputs take the accurate exponential form: relative error below
+    1e-5 (far inside a bf16 ulp), absolute 1e-40 near zero."""
+    g = wl.gate_up_input(wl.WORKLOADS["act"], seed=3, rows=256).float()
+    got = _run(g, cuda_dev)
+    ref = oracle.situ_glu_act(oracle_input(g))
+    err = np.abs(got - ref)
+    assert (err <= 1e-5 * np.abs(ref) + 1e-40).all(), float((err / (np.abs(ref) + 1e-40)).max())
+
+
 def test_caps_are_arguments(oracle, cuda_dev):
     gate_up = wl.normal((64, 256), 10.0, seed=4)
     for b1, b2 in [(25.0, 4.0), (1.0, 1.0), (8.0, 50.0)]:
