@@ -1,0 +1,83 @@
+"""bench.py host logic without a GPU: the max/sum aggregation over ranks (gloo,
+world size 2), the reference arm's JSON line, peaks and traffic bookkeeping."""
+import json
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        q.put((rank, bench.aggregate(float(rank + 1), 100.0 * (rank + 1), world)))
+        bench.barrier(world)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_aggregate_two_ranks_gloo():
+    """Replicas: the step time is the max over ranks, the work the sum."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    results = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert results[0] == (2.0, 300.0) and results[1] == (2.0, 300.0)
+
+
+def test_aggregate_single_rank_is_identity():
+    assert bench.aggregate(3.5, 7.0, 1) == (3.5, 7.0)
+
+
+def test_reference_arm_json(capsys, monkeypatch):
+    monkeypatch.delenv("RANK", raising=False)
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3",
+                       "--ref-rows", "1"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["value"] > 0
+    assert line["metric"] == bench.METRIC
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["config"]["workload"].startswith("dense SiTU-GLU FFN")
+
+
+def test_reference_arm_other_ranks_do_nothing(capsys, monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"]) == 0
+    assert capsys.readouterr().out == ""
+
+
+def test_warmup_floor():
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2"])
+
+
+def test_peaks_and_traffic(tmp_path, monkeypatch):
+    peaks, src = bench.load_peaks()
+    assert src in ("measured", "fallback") and peaks["hbm_gbs"] > 0
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_peaks() == (bench.FALLBACK_PEAKS, "fallback")
+    assert bench.profiled_traffic("ffn_gate_up_situ", "x", 10) is None
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.txt").write_text("# c\nk abc 2.5 row f.md\n")
+    assert bench.profiled_traffic("k", "abc", 4) == 10.0
+    assert bench.profiled_traffic("k", "old", 4) is None  # kernel changed since the capture
