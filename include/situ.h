@@ -165,6 +165,35 @@ situ_status situ_ffn_down(const void* h, const void* W_down, void* y, int64_t R,
                           int64_t I, situ_dtype dt, void* stream);
 
 /* -------------------------------------------------------------------------
+ * situ_ffn_forward_host -- situ_ffn_forward with x and y in host memory.
+ *
+ * Same operation as situ_ffn_forward (docs page "Two linear maps"), for callers
+ * whose activations live on the host.  The rows are processed in chunks of
+ * `chunk_rows`: while chunk c runs on the GPU, chunk c+1 is copied in and chunk
+ * c-1 copied out on two library-owned copy streams, ordered with events, so the
+ * host<->device traffic overlaps the GEMMs.  The call returns once everything is
+ * enqueued; `stream` completes only after the last result row has reached y_host.
+ *
+ *   x_host     host, [R, M] of `dt`, read only.  Use page-locked (pinned) memory:
+ *              pageable memory works but its copies do not overlap.
+ *   y_host     host, [R, M] of `dt`, written.
+ *   W_gate_up, W_down   device, as situ_ffn_forward.
+ *   workspace  device, >= situ_ffn_host_workspace_size(R, M, I, dt, chunk_rows)
+ *              bytes, 256-byte aligned (two x chunks, two y chunks, one h chunk).
+ *   chunk_rows rows per chunk, >= 1; 0 picks 4096.
+ * The copy streams and events are created once per device on first use.
+ * Errors: those of situ_ffn_forward.
+ * ------------------------------------------------------------------------- */
+size_t situ_ffn_host_workspace_size(int64_t R, int64_t M, int64_t I, situ_dtype dt,
+                                    int64_t chunk_rows);
+
+situ_status situ_ffn_forward_host(const void* x_host, const void* W_gate_up,
+                                  const void* W_down, void* y_host, void* workspace,
+                                  size_t workspace_bytes, int64_t R, int64_t M, int64_t I,
+                                  int64_t chunk_rows, float beta, float linear_beta,
+                                  situ_dtype dt, void* stream);
+
+/* -------------------------------------------------------------------------
  * situ_ffn_forward_noalloc -- situ_ffn_forward for callers that cannot allocate
  * device memory.  The pages have no counterpart: this is a library service.
  *

@@ -8,14 +8,17 @@ Hand-written CUDA kernels behind a C ABI (``include/situ.h``, ``libsitu.so``):
   * ``situ_moe_grouped_forward``  the FFN grouped over experts
 This package is the thin PyTorch binding over that ABI.
 """
-from .api import (SituError, device_status, ffn_workspace_bytes, moe_workspace_bytes,
-                  selftest_bounded_wait, situ_ffn_down, situ_ffn_forward, situ_ffn_gate_up,
+from .api import (SituError, device_status, ffn_host_workspace_bytes, ffn_workspace_bytes,
+                  moe_workspace_bytes,
+                  selftest_bounded_wait, situ_ffn_down, situ_ffn_forward, situ_ffn_forward_host,
+                  situ_ffn_gate_up,
                   situ_glu_act,
                   situ_moe_build_index, situ_moe_grouped_forward)
 
 __all__ = [
-    "SituError", "situ_glu_act", "situ_ffn_forward", "situ_ffn_gate_up", "situ_ffn_down",
+    "SituError", "situ_glu_act", "situ_ffn_forward", "situ_ffn_forward_host", "situ_ffn_gate_up",
+    "situ_ffn_down",
     "situ_moe_build_index",
     "situ_moe_grouped_forward", "ffn_workspace_bytes", "moe_workspace_bytes",
-    "device_status", "selftest_bounded_wait",
+    "device_status", "selftest_bounded_wait", "ffn_host_workspace_bytes",
 ]

@@ -104,6 +104,51 @@ def situ_ffn_forward(x: torch.Tensor, W_gate_up: torch.Tensor, W_down: torch.Ten
     return y
 
 
+def situ_ffn_forward_host(x_host: torch.Tensor, W_gate_up: torch.Tensor, W_down: torch.Tensor,
+                          beta: float = 4.0, linear_beta: float = 25.0,
+                          y_host: torch.Tensor | None = None, chunk_rows: int = 0,
+                          workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Dense SiTU-GLU FFN with x and y in (pinned) host memory.
+
+    Row chunks are pipelined so host->device copies, the GEMMs and device->host
+    copies overlap; returns y_host, complete once the current stream is synchronised.
+    """
+    if x_host.is_cuda or not x_host.is_contiguous():
+        raise ValueError("x_host must be a contiguous host tensor")
+    for n, t in (("W_gate_up", W_gate_up), ("W_down", W_down)):
+        _cuda_contig(n, t)
+        if t.dtype != x_host.dtype:
+            raise TypeError("x_host and the weights must share a dtype")
+    M = x_host.shape[-1]
+    I = W_gate_up.shape[0] // 2
+    if W_gate_up.shape != (2 * I, M) or W_down.shape != (M, I):
+        raise ValueError("weight shapes do not match x_host")
+    R = x_host.numel() // M if M else 0
+    if y_host is None:
+        y_host = torch.empty(x_host.shape, dtype=x_host.dtype, pin_memory=True)
+    elif y_host.is_cuda or y_host.shape != x_host.shape or not y_host.is_contiguous():
+        raise ValueError("y_host must be a contiguous host tensor shaped like x_host")
+    if R == 0:
+        return y_host
+    lib = _native.lib()
+    need = int(lib.situ_ffn_host_workspace_size(R, M, I, _dt(x_host), chunk_rows))
+    dev = W_gate_up.device
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    check("situ_ffn_forward_host",
+          lib.situ_ffn_forward_host(x_host.data_ptr(), W_gate_up.data_ptr(), W_down.data_ptr(),
+                                    y_host.data_ptr(), workspace.data_ptr(),
+                                    workspace.numel() * workspace.element_size(), R, M, I,
+                                    chunk_rows, float(beta), float(linear_beta), _dt(x_host),
+                                    _stream(dev)))
+    return y_host
+
+
+def ffn_host_workspace_bytes(R: int, M: int, I: int, chunk_rows: int = 0,
+                             dtype=torch.bfloat16) -> int:
+    return int(_native.lib().situ_ffn_host_workspace_size(R, M, I, _DTYPES[dtype], chunk_rows))
+
+
 def situ_ffn_gate_up(x: torch.Tensor, W_gate_up: torch.Tensor, beta: float = 4.0,
                      linear_beta: float = 25.0, h: torch.Tensor | None = None) -> torch.Tensor:
     """h = SiTU-GLU(x W_gate_up^T) [..., I], bf16: one tcgen05 GEMM, activation fused."""
@@ -229,8 +274,9 @@ def selftest_bounded_wait(limit_us: int = 2000) -> None:
 
 
 __all__ = [
-    "SituError", "situ_glu_act", "situ_ffn_forward", "situ_ffn_gate_up", "situ_ffn_down",
+    "SituError", "situ_glu_act", "situ_ffn_forward", "situ_ffn_forward_host", "situ_ffn_gate_up",
+    "situ_ffn_down",
     "situ_moe_build_index",
     "situ_moe_grouped_forward", "ffn_workspace_bytes", "moe_workspace_bytes",
-    "device_status", "selftest_bounded_wait",
+    "device_status", "selftest_bounded_wait", "ffn_host_workspace_bytes",
 ]

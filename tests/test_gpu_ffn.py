@@ -84,6 +84,25 @@ def test_dense_full_size_sampled(oracle, cuda_dev):
     assert_ffn_close(to_f64(y[rd]), ref, "dense full size")
 
 
+@pytest.mark.parametrize("R,chunk,pinned", [(10000, 4096, True), (3000, 1000, True),
+                                             (777, 0, False), (5, 2, True)])
+def test_host_io_pipeline(oracle, cuda_dev, R, chunk, pinned):
+    """x and y in host memory, rows pipelined in chunks: same bits as the device
+    call (each row's arithmetic does not depend on the chunking), and the oracle
+    on sampled rows."""
+    M, I = 512, 384
+    x, wgu, wd = wl.ffn_inputs(M, I, R, seed=R)
+    x_h = x.pin_memory() if pinned else x.clone()
+    wgu_d, wd_d = wgu.to(cuda_dev), wd.to(cuda_dev)
+    y_h = situ.situ_ffn_forward_host(x_h, wgu_d, wd_d, chunk_rows=chunk)
+    torch.cuda.synchronize()
+    y_d = situ.situ_ffn_forward(x.to(cuda_dev), wgu_d, wd_d).cpu()
+    assert torch.equal(y_h.view(torch.int16), y_d.view(torch.int16))
+    rows = sorted({0, R - 1, R // 2, min(R - 1, max(chunk, 1))})
+    ref = oracle.ffn_forward(oracle_input(x[rows]), oracle_input(wgu), oracle_input(wd))
+    assert_ffn_close(to_f64(y_h[rows]), ref, f"host io R={R}")
+
+
 def test_tiny_fp32(oracle, cuda_dev):
     """The tiny fp32 configuration: x [2, 8, 128], W_gate_up [512, 128], W_down [128, 256]."""
     w = wl.WORKLOADS["tiny_fp32"]
