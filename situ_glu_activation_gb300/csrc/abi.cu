@@ -309,7 +309,8 @@ situ_status situ_moe_build_index(const int32_t* expert_ids, int32_t* expert_offs
 
 size_t situ_moe_workspace_size(int64_t R, int32_t E, int64_t M, int64_t I, situ_dtype dt) {
   if (R < 0 || E < 1 || M < 1 || I < 1 || dt != SITU_BF16) return 0;
-  const size_t tiles = round_up(static_cast<size_t>(E + 1) * 4, 256);
+  // m-tile prefix + paired-unit prefixes of the two GEMMs
+  const size_t tiles = 3 * round_up(static_cast<size_t>(E + 1) * 4, 256);
   const size_t xperm = round_up(static_cast<size_t>(R) * M * 2, 256);
   const size_t h = round_up(static_cast<size_t>(R) * I * 2, 256);
   return tiles + xperm + h;
@@ -351,11 +352,15 @@ situ_status situ_moe_grouped_forward(const void* x, const int32_t* expert_offset
   if (s != SITU_OK) return s;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t prefix_bytes = round_up(static_cast<size_t>(E + 1) * 4, 256);
   int32_t* tile_offsets = reinterpret_cast<int32_t*>(ws);
-  void* x_perm = ws + round_up(static_cast<size_t>(E + 1) * 4, 256);
+  int32_t* units_gu = reinterpret_cast<int32_t*>(ws + prefix_bytes);
+  int32_t* units_dn = reinterpret_cast<int32_t*>(ws + 2 * prefix_bytes);
+  void* x_perm = ws + 3 * prefix_bytes;
   void* h_perm = static_cast<uint8_t*>(x_perm) + round_up(static_cast<size_t>(R) * M * 2, 256);
 
-  cudaError_t e = launch_group_tiles(expert_offsets, E, R, tile_offsets, st->status, cs);
+  cudaError_t e = launch_group_tiles(expert_offsets, E, R, I, M, tile_offsets, units_gu,
+                                     units_dn, st->status, cs);
   if (e != cudaSuccess) return cuda_fail(e);
   e = launch_gather_rows(x, token_index, x_perm, R, k_eff, M, st->status, cs);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -369,6 +374,7 @@ situ_status situ_moe_grouped_forward(const void* x, const int32_t* expert_offset
   g.num_groups = E;
   g.group_offsets = expert_offsets;
   g.tile_offsets = tile_offsets;
+  g.unit_offsets = units_gu;
   g.b_group_rows = 2 * I;
   g.b_up_offset = I;
   g.n_out = I;
@@ -386,6 +392,7 @@ situ_status situ_moe_grouped_forward(const void* x, const int32_t* expert_offset
   d.num_groups = E;
   d.group_offsets = expert_offsets;
   d.tile_offsets = tile_offsets;
+  d.unit_offsets = units_dn;
   d.b_group_rows = M;
   d.n_out = M;
   d.out = y;

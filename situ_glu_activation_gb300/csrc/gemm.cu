@@ -61,7 +61,8 @@ enum class Epi { kSitu, kPlain };
 struct Args {
   int32_t num_groups;
   const int32_t* group_offsets;  // [G+1] device or null (dense)
-  const int32_t* tile_offsets;   // [G+1] device or null (dense)
+  const int32_t* tile_offsets;   // [G+1] device or null (dense): m-tile prefix
+  const int32_t* unit_offsets;   // [G+1] device or null (dense): paired-unit prefix
   int32_t dense_rows;
   int32_t n_tiles;
   int32_t k_blocks;
@@ -91,6 +92,7 @@ struct TileCoord {
   int32_t row_end;  // one past the last valid A row (group end)
   int32_t group;
   int32_t n_tile;
+  int32_t share_a;  // paired unit of one m-tile and two n-tiles (A multicast)
 };
 
 __device__ __forceinline__ int32_t total_tiles(const Args& a) {
@@ -107,6 +109,7 @@ __device__ __forceinline__ TileCoord decode_tile(const Args& a, int32_t t) {
     c.group = 0;
     c.a_row0 = mt * kBM;
     c.row_end = a.dense_rows;
+    c.share_a = 0;
     return c;
   }
   // Largest g with tile_offsets[g] <= mt (empty groups repeat an offset; the
@@ -119,28 +122,62 @@ __device__ __forceinline__ TileCoord decode_tile(const Args& a, int32_t t) {
   c.group = lo;
   c.a_row0 = __ldg(a.group_offsets + lo) + (mt - __ldg(a.tile_offsets + lo)) * kBM;
   c.row_end = __ldg(a.group_offsets + lo + 1);
+  c.share_a = 0;
   return c;
 }
 
-// Work units.  Unpaired: one unit = one tile, from decode_tile.  Paired (dense
-// only, clusters of two CTAs): one unit = the tiles (2p, n) and (2p+1, n); CTA
-// rank r of the cluster takes m-tile 2p+r and both share the B tile of n-tile n.
+// Work units.  Unpaired: one unit = one tile, from decode_tile.  Paired
+// (clusters of two CTAs, CTA rank r):
+//   * a group (expert) with m m-tiles has floor(m/2) * n_tiles "shared-B" units:
+//     unit (p, n) gives rank r the tile (m-tile 2p + r, n-tile n); the two CTAs
+//     share the B tile of n-tile n, each fetching one half and multicasting it;
+//   * when m is odd, its last m-tile forms ceil(n_tiles/2) "shared-A" units:
+//     unit q gives rank r the tile (m-tile m-1, n-tile 2q + r); the two CTAs share
+//     the A tile, each fetching 64 of its 128 rows and multicasting them.
+// Dense calls are one group of all rows; grouped calls read the per-group unit
+// prefix from unit_offsets.
+__device__ __forceinline__ int32_t units_of(int32_t m, int32_t n_tiles) {
+  return (m >> 1) * n_tiles + (m & 1) * ((n_tiles + 1) >> 1);
+}
+
 template <bool kPair>
 __device__ __forceinline__ int32_t num_units(const Args& a) {
   if (!kPair) return total_tiles(a);
-  const int32_t m_tiles = (a.dense_rows + kBM - 1) / kBM;
-  return ((m_tiles + 1) / 2) * a.n_tiles;
+  if (a.unit_offsets) return __ldg(a.unit_offsets + a.num_groups);
+  return units_of((a.dense_rows + kBM - 1) / kBM, a.n_tiles);
 }
 
 template <bool kPair>
 __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_t rank) {
   if (!kPair) return decode_tile(a, u);
+  int32_t g = 0, row0 = 0, row_end = a.dense_rows, local = u;
+  if (a.unit_offsets) {
+    int32_t lo = 0, hi = a.num_groups - 1;
+    while (lo < hi) {
+      const int32_t mid = (lo + hi + 1) >> 1;
+      if (__ldg(a.unit_offsets + mid) <= u) lo = mid; else hi = mid - 1;
+    }
+    g = lo;
+    row0 = __ldg(a.group_offsets + g);
+    row_end = __ldg(a.group_offsets + g + 1);
+    local = u - __ldg(a.unit_offsets + g);
+  }
+  const int32_t m = (row_end - row0 + kBM - 1) / kBM;
+  const int32_t shared_b_units = (m >> 1) * a.n_tiles;
   TileCoord c;
-  const int32_t mp = u / a.n_tiles;
-  c.n_tile = u - mp * a.n_tiles;
-  c.group = 0;
-  c.a_row0 = (2 * mp + static_cast<int32_t>(rank)) * kBM;
-  c.row_end = a.dense_rows;
+  c.group = g;
+  c.row_end = row_end;
+  if (local < shared_b_units) {
+    const int32_t p = local / a.n_tiles;
+    c.n_tile = local - p * a.n_tiles;
+    c.a_row0 = row0 + (2 * p + static_cast<int32_t>(rank)) * kBM;
+    c.share_a = 0;
+  } else {
+    const int32_t q = local - shared_b_units;
+    c.n_tile = 2 * q + static_cast<int32_t>(rank);
+    c.a_row0 = row0 + (m - 1) * kBM;
+    c.share_a = 1;
+  }
   return c;
 }
 
@@ -183,6 +220,7 @@ __device__ __forceinline__ void store_row_chunk(__nv_bfloat16* dst, const uint32
 template <Epi kEpi, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                    const __grid_constant__ CUtensorMap map_a64,
                     const __grid_constant__ CUtensorMap map_b, const Args args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled operand buffers.
@@ -209,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ctl->abort = 0;
     fence_mbar_init();
     tma_prefetch_map(&map_a);
+    if (kPair) tma_prefetch_map(&map_a64);
     tma_prefetch_map(&map_b);
   }
   if (warp == 1) {
@@ -251,12 +290,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = smem_u32(smem + stage * kStageBytes);
           const uint32_t sb = sa + kABytes;
           mbar_arrive_expect_tx(full, kStageBytes);
-          tma_load_2d(sa, &map_a, kb * kBK, tc.a_row0, full);
-          if (kPair) {
-            // This CTA fetches half of the shared B tile and multicasts it to both.
+          if (!kPair) {
+            tma_load_2d(sa, &map_a, kb * kBK, tc.a_row0, full);
+            tma_load_2d(sb, &map_b, kb * kBK, b_row0, full);
+            tma_load_2d(sb + kBHalfBytes, &map_b, kb * kBK, b_row1, full);
+          } else if (!tc.share_a) {
+            // Shared B: this CTA fetches one half of the B tile for both CTAs.
+            tma_load_2d(sa, &map_a, kb * kBK, tc.a_row0, full);
             tma_load_2d_multicast(sb + rank * kBHalfBytes, &map_b, kb * kBK,
                                   rank == 0 ? b_row0 : b_row1, full, 0x3);
           } else {
+            // Shared A: this CTA fetches 64 of the 128 A rows for both CTAs.
+            tma_load_2d_multicast(sa + rank * (kABytes / 2), &map_a64, kb * kBK,
+                                  tc.a_row0 + static_cast<int32_t>(rank) * 64, full, 0x3);
             tma_load_2d(sb, &map_b, kb * kBK, b_row0, full);
             tma_load_2d(sb + kBHalfBytes, &map_b, kb * kBK, b_row1, full);
           }
@@ -403,42 +449,64 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Small helper kernels of the grouped path
 // ---------------------------------------------------------------------------
 
-// tile_offsets[g] = sum over g' < g of ceil(rows_g' / 128); validates offsets.
+// Per-group work prefixes of the grouped GEMMs, and validation of the offsets:
+//   tiles[g]    = sum over g' < g of m_g'            (m_g = ceil(rows_g / 128))
+//   units_gu[g] = sum over g' < g of units(m_g', n_gu) (paired units, gate_up GEMM)
+//   units_dn[g] = sum over g' < g of units(m_g', n_dn) (paired units, down GEMM)
+// Invalid offsets (not starting at 0, decreasing, not ending at R) zero all three
+// so the GEMMs do nothing, and record SITU_ERR_INDEX.  One block of 1024 threads.
 __global__ void group_tiles_kernel(const int32_t* __restrict__ off, int32_t G, int64_t R,
-                                   int32_t* __restrict__ tiles, uint32_t* status) {
-  __shared__ int32_t partial[1024];
+                                   int32_t n_gu, int32_t n_dn, int32_t* __restrict__ tiles,
+                                   int32_t* __restrict__ units_gu,
+                                   int32_t* __restrict__ units_dn, uint32_t* status) {
+  __shared__ int32_t partial[3][1024];
   __shared__ int bad;
   if (threadIdx.x == 0) bad = 0;
   __syncthreads();
   const int per = (G + blockDim.x - 1) / blockDim.x;
   const int g0 = threadIdx.x * per;
-  int32_t sum = 0;
+  int32_t sum[3] = {0, 0, 0};
   for (int g = g0; g < g0 + per && g < G; ++g) {
     const int32_t a = off[g], b = off[g + 1];
     if (b < a) bad = 1;
-    sum += (b - a + kBM - 1) / kBM;
+    const int32_t m = (b - a + kBM - 1) / kBM;
+    sum[0] += m;
+    sum[1] += units_of(m, n_gu);
+    sum[2] += units_of(m, n_dn);
   }
   if (threadIdx.x == 0 && (off[0] != 0 || static_cast<int64_t>(off[G]) != R)) bad = 1;
-  partial[threadIdx.x] = sum;
+  for (int k = 0; k < 3; ++k) partial[k][threadIdx.x] = sum[k];
   __syncthreads();
-  // Inclusive scan of the per-thread sums (Hillis-Steele over one block).
+  // Inclusive scans of the per-thread sums (Hillis-Steele over one block).
   for (int d = 1; d < static_cast<int>(blockDim.x); d <<= 1) {
-    const int32_t v = threadIdx.x >= static_cast<unsigned>(d) ? partial[threadIdx.x - d] : 0;
+    int32_t v[3];
+    for (int k = 0; k < 3; ++k)
+      v[k] = threadIdx.x >= static_cast<unsigned>(d) ? partial[k][threadIdx.x - d] : 0;
     __syncthreads();
-    partial[threadIdx.x] += v;
+    for (int k = 0; k < 3; ++k) partial[k][threadIdx.x] += v[k];
     __syncthreads();
   }
   if (bad) {
-    for (int g = threadIdx.x; g <= G; g += blockDim.x) tiles[g] = 0;
+    for (int g = threadIdx.x; g <= G; g += blockDim.x) tiles[g] = units_gu[g] = units_dn[g] = 0;
     if (threadIdx.x == 0) record_status(status, SITU_ERR_INDEX);
     return;
   }
-  int32_t run = threadIdx.x == 0 ? 0 : partial[threadIdx.x - 1];
+  int32_t run[3];
+  for (int k = 0; k < 3; ++k) run[k] = threadIdx.x == 0 ? 0 : partial[k][threadIdx.x - 1];
   for (int g = g0; g < g0 + per && g < G; ++g) {
-    tiles[g] = run;
-    run += (off[g + 1] - off[g] + kBM - 1) / kBM;
+    tiles[g] = run[0];
+    units_gu[g] = run[1];
+    units_dn[g] = run[2];
+    const int32_t m = (off[g + 1] - off[g] + kBM - 1) / kBM;
+    run[0] += m;
+    run[1] += units_of(m, n_gu);
+    run[2] += units_of(m, n_dn);
   }
-  if (threadIdx.x == blockDim.x - 1) tiles[G] = partial[threadIdx.x];
+  if (threadIdx.x == blockDim.x - 1) {
+    tiles[G] = partial[0][threadIdx.x];
+    units_gu[G] = partial[1][threadIdx.x];
+    units_dn[G] = partial[2][threadIdx.x];
+  }
 }
 
 // One warp per gathered row: x_perm[r] = x[token_index[r] / k_eff] (16-byte copies).
@@ -490,14 +558,15 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// 2-D bf16 map over a row-major [rows, cols] matrix, 64 x 128 boxes, 128-byte
+// 2-D bf16 map over a row-major [rows, cols] matrix, 64 x box_rows boxes, 128-byte
 // swizzle (the layout sw128_kmajor_desc describes), zero fill out of bounds.
-bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
+              uint32_t box_rows = 128) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), 128};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -542,13 +611,15 @@ template <Epi kEpi>
 cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, int num_sms,
                    cudaStream_t stream) {
   if (s.a_rows == 0 && !s.tile_offsets) return cudaSuccess;
-  CUtensorMap ma, mb;
-  if (!make_map(&ma, s.a, s.a_rows, s.K) || !make_map(&mb, s.b, s.b_rows, s.K))
+  CUtensorMap ma, ma64, mb;
+  if (!make_map(&ma, s.a, s.a_rows, s.K) || !make_map(&ma64, s.a, s.a_rows, s.K, 64) ||
+      !make_map(&mb, s.b, s.b_rows, s.K))
     return cudaErrorInvalidValue;
   Args a;
   a.num_groups = s.num_groups;
   a.group_offsets = s.group_offsets;
   a.tile_offsets = s.tile_offsets;
+  a.unit_offsets = nullptr;
   a.dense_rows = static_cast<int32_t>(s.a_rows);
   const int64_t out_cols_per_tile = kEpi == Epi::kSitu ? 128 : kBN;
   a.n_tiles = static_cast<int32_t>((s.n_out + out_cols_per_tile - 1) / out_cols_per_tile);
@@ -567,34 +638,35 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
   }
-  if (!s.tile_offsets) {
-    // Dense: clusters of two CTAs share each B tile (multicast).
-    const int64_t m_tiles = (s.a_rows + kBM - 1) / kBM;
-    const int64_t units = ((m_tiles + 1) / 2) * a.n_tiles;
-    int clusters = max_pair_clusters<kEpi>(kSmemBytes);
-    if (clusters > 0) {
+  int clusters = max_pair_clusters<kEpi>(kSmemBytes);
+  if (clusters > 0 && (!s.tile_offsets || s.unit_offsets)) {
+    // Clusters of two CTAs sharing a B or an A tile by multicast.
+    a.unit_offsets = s.unit_offsets;
+    if (!s.tile_offsets) {
+      const int64_t m = (s.a_rows + kBM - 1) / kBM;
+      const int64_t units = (m / 2) * a.n_tiles + (m % 2) * ((a.n_tiles + 1) / 2);
       if (units < clusters) clusters = static_cast<int>(units);
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(2 * clusters, 1, 1);
-      cfg.blockDim = dim3(kThreads, 1, 1);
-      cfg.dynamicSmemBytes = kSmemBytes;
-      cfg.stream = stream;
-      cudaLaunchAttribute attr;
-      attr.id = cudaLaunchAttributeClusterDimension;
-      attr.val.clusterDim.x = 2;
-      attr.val.clusterDim.y = 1;
-      attr.val.clusterDim.z = 1;
-      cfg.attrs = &attr;
-      cfg.numAttrs = 1;
-      return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, true>, ma, mb, a);
     }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, true>, ma, ma64, mb, a);
   }
   int grid = num_sms;
   if (!s.tile_offsets) {
     const int64_t tiles = ((s.a_rows + kBM - 1) / kBM) * a.n_tiles;
     if (tiles < grid) grid = static_cast<int>(tiles);
   }
-  ffn_gemm_kernel<kEpi, false><<<grid, kThreads, kSmemBytes, stream>>>(ma, mb, a);
+  ffn_gemm_kernel<kEpi, false><<<grid, kThreads, kSmemBytes, stream>>>(ma, ma64, mb, a);
   return cudaGetLastError();
 }
 
@@ -611,8 +683,13 @@ cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
 }
 
 cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,
-                               int32_t* tile_offsets, uint32_t* status, cudaStream_t stream) {
-  group_tiles_kernel<<<1, 1024, 0, stream>>>(group_offsets, G, R, tile_offsets, status);
+                               int64_t n_out_gate_up, int64_t n_out_down, int32_t* tile_offsets,
+                               int32_t* units_gate_up, int32_t* units_down, uint32_t* status,
+                               cudaStream_t stream) {
+  const int32_t n_gu = static_cast<int32_t>((n_out_gate_up + 127) / 128);
+  const int32_t n_dn = static_cast<int32_t>((n_out_down + kBN - 1) / kBN);
+  group_tiles_kernel<<<1, 1024, 0, stream>>>(group_offsets, G, R, n_gu, n_dn, tile_offsets,
+                                             units_gate_up, units_down, status);
   return cudaGetLastError();
 }
 

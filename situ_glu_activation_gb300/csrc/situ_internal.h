@@ -42,6 +42,8 @@ struct GemmShape {
   int32_t num_groups;
   const int32_t* group_offsets;
   const int32_t* tile_offsets;
+  // Paired-unit prefix per group for this GEMM (from launch_group_tiles), or NULL.
+  const int32_t* unit_offsets;
   int64_t b_group_rows;  // B rows per group
   int64_t b_up_offset;   // SiTU epilogue: row offset of the up half inside a group
   int64_t n_out;         // valid output columns
@@ -59,9 +61,12 @@ cudaError_t launch_gemm_situ(const GemmShape& s, const SituParams& p, uint32_t* 
 // C = A B^T, bf16 output.
 cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
                               cudaStream_t stream);
-// M-tile prefix over row groups + validation of the offsets.
+// Per-group prefixes of m-tiles and of paired units of the gate_up (n_out_gate_up =
+// I output columns) and down (n_out_down = M) GEMMs, plus validation of the offsets.
 cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,
-                               int32_t* tile_offsets, uint32_t* status, cudaStream_t stream);
+                               int64_t n_out_gate_up, int64_t n_out_down, int32_t* tile_offsets,
+                               int32_t* units_gate_up, int32_t* units_down, uint32_t* status,
+                               cudaStream_t stream);
 // x_perm[r, :] = x[token_index[r] / k_eff, :]  (M bf16 columns).
 cudaError_t launch_gather_rows(const void* x, const int32_t* token_index, void* x_perm,
                                int64_t R, int32_t k_eff, int64_t M, uint32_t* status,

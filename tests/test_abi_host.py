@@ -44,7 +44,7 @@ def test_workspace_sizes(situ_lib):
     assert situ_lib.situ_ffn_workspace_size(3, 8, 5, 1) == 256  # fp32 h, rounded to 256 B
     assert situ_lib.situ_ffn_workspace_size(0, 8, 8, 0) == 0
     R, E, M, I = 1000, 7, 64, 96
-    expect = 256 + ((R * M * 2 + 255) // 256) * 256 + ((R * I * 2 + 255) // 256) * 256
+    expect = 3 * 256 + ((R * M * 2 + 255) // 256) * 256 + ((R * I * 2 + 255) // 256) * 256
     assert situ_lib.situ_moe_workspace_size(R, E, M, I, 0) == expect
     assert situ_lib.situ_moe_workspace_size(R, E, M, I, 1) == 0  # grouped path is bf16 only
     assert situ_lib.situ_moe_index_workspace_size(1024, 10) == 256
