@@ -432,6 +432,17 @@ def run_situ(args):
     peaks, peak_src = load_peaks()
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush = lambda: flush_buf.fill_(1)
+    if args.suite not in ("full", "dense"):
+        # One workload alone (profiling runs): a reduced line with that result.
+        if args.suite == "act":
+            res = bench_act(args, dev, peaks, world, flush)
+        else:
+            res = bench_moe(args, dev, peaks, world, flush, [args.suite])[args.suite]
+        if rank == 0:
+            print(json.dumps({"suite": args.suite, "steps": args.steps, "warmup": args.warmup,
+                              "result": res, "device_status": situ.device_status(clear=True)}),
+                  flush=True)
+        return 0
 
     with ClockSampler(dev.index or 0) as clk:
         dense, w = bench_dense(args, dev, peaks, world, flush)
@@ -505,7 +516,11 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["situ", "reference"], default="situ")
-    ap.add_argument("--suite", choices=["full", "dense"], default="full")
+    ap.add_argument("--suite", default="full",
+                    choices=["full", "dense", "act", "grouped", "k3_decode", "k3_prefill",
+                             "k3_prefill_slice"],
+                    help="full: the headline line with every sub-result; dense: the headline "
+                         "only; any other name: that workload alone (for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=0, help="oracle rows per reference step")

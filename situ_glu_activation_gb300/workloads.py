@@ -80,6 +80,11 @@ WORKLOADS = {
     "k3_prefill": Workload("Kimi-K3-shaped MoE layer, 896 routed + 2 shared experts, "
                            "32768 tokens", "moe", T=32768, E=896, k=8, shared=(896, 897),
                            routing="uniform"),
+    # A 64-expert slice with the prefill's rows per expert (about 293): the same
+    # per-expert GEMM shapes with 2.4 GB of weights, for profiling.
+    "k3_prefill_slice": Workload("64 routed experts, 2344 tokens top-8 uniform (about 293 rows "
+                                 "per expert, the K3 prefill shape)", "moe", T=2344, E=64, k=8,
+                                 routing="uniform"),
 }
 
 
