@@ -7,11 +7,11 @@
 // bounded branches").  Every input byte is read once and every output byte
 // written once, so the kernel is bound by HBM bandwidth: 128-bit loads of 8
 // gate and 8 up bf16 values and one 128-bit store of 8 outputs per vector step,
-// streaming cache hints (the data is touched once), a grid of 16 blocks of 256
-// threads per SM with each thread keeping two vector steps (four 16-byte loads)
-// in flight.  The activation costs three special-function ops and about a
-// dozen FP32 ops per output (situ_math.cuh), which keeps instruction issue
-// below the memory time.
+// streaming cache hints (the data is touched once), a grid of up to 32 blocks of
+// 256 threads per SM with each thread keeping two vector steps (four 16-byte
+// loads) in flight.  The activation costs four special-function ops and eight
+// FP32 ops per output, with no select (situ_math.cuh), which keeps instruction
+// issue below the memory time.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -24,7 +24,7 @@ namespace situ {
 namespace {
 
 constexpr int kActThreads = 256;
-constexpr int kActBlocksPerSm = 16;
+constexpr int kActBlocksPerSm = 32;
 constexpr int kActUnroll = 2;
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

@@ -12,25 +12,29 @@
 //   * tanh(g / b1) and tanh(u / b2) come from the hardware tanh.approx.f32
 //     (documented maximum relative error about 2^-11 over the whole range; no
 //     cancellation near zero, since it returns tanh itself, not 1 - something);
-//   * sigmoid(g) = P / (1 + E0) with E0 = exp(-|g|) from one ex2.approx and
-//     P = 1 for g >= 0, P = E0 for g < 0 -- never 0.5 + 0.5 tanh(g/2), which
-//     cancels to zero for g << 0 and would lose all relative accuracy there;
-//   * for g < 0 the factor P = e^g is carried as 2^64 e^g (one ex2 with the
-//     exponent shifted by 64) and the product is scaled back by 2^-64 in its
-//     last multiply, so outputs in the subnormal range (g from about -87 down to
-//     -104) come out correctly rounded instead of flushed: the final multiply
-//     and the bf16 conversion keep subnormals;
-//   * one hardware reciprocal, rcp.approx of (1 + E0) in [1, 2].
-// Three special-function ops and about a dozen FP32 ops per output.  Relative
-// error: at most about 2 * 2^-11 from the two tanh plus a few 2^-22, i.e. below
-// a quarter of a bf16 ulp, so after round-to-nearest-even the output is within
-// 0.75 bf16 ulp of the exact value (measured: 0.503 ulp worst case over every
-// bf16 input of either branch).  |tanh.approx| <= 1, P <= 1 and the reciprocal
-// of a number >= 1 is <= 1, so |h| <= b1 b2; a final clamp keeps the bound
-// structural even for caps whose product rounds.  NaN propagates.
+//   * the sigmoid is carried scaled by 2^64, in a form with no branch or select:
+//         2^64 sigmoid(g) = 1 / (2^-64 + 2^(-g log2(e) - 64)),
+//     one FMA, one ex2.approx, one add, one rcp.approx.  It is exact in the
+//     negative tail, where 0.5 + 0.5 tanh(g/2) would cancel to zero, and the
+//     2^64 scale keeps outputs in the subnormal range (g from about -87 down to
+//     -104) correctly rounded instead of flushed: the 2^-64 is applied by the
+//     last multiply, and that multiply and the bf16 conversion keep subnormals.
+//     For g below about -133 the exponential overflows to +inf and the sigmoid
+//     to 0, below any representable output; for g above about 44 the sum is
+//     2^-64 and the sigmoid exactly 1.
+// Four special-function ops and eight FP32 ops per output.  Relative error: at
+// most about 2 * 2^-11 from the two tanh plus about 2^-17 from the sigmoid's
+// exponent argument, below a quarter of a bf16 ulp, so after round-to-nearest-
+// even the output is within 0.75 bf16 ulp of the exact value (measured: 0.503
+// ulp worst case over every bf16 input of either branch).
+// Bound: |tanh.approx| <= 1 (it saturates at +-1), the reciprocal is at most
+// 2^64 (its argument is at least 2^-64 and its error is under one ulp), and a
+// round-to-nearest multiply by a factor of magnitude <= 1 never increases a
+// magnitude, so |h| <= b1 b2 holds structurally, with no clamp.  NaN propagates.
 //
 // situ_glu_f32_accurate is the variant for float32 outputs, where a 2^-11 error
-// would be visible: the same sigmoid, but each tanh in exponential form,
+// would be visible: the sigmoid as P / (1 + e^{-|g|}) (P = 1 or e^{-|g|}, the
+// latter carried as 2^64 e^{-|g|}), each tanh in exponential form,
 // tanh(x) = (1 - e^{-2x}) / (1 + e^{-2x}) for x >= 0, with 1 - e^{-2x} from its
 // Taylor series x' - x'^2/2 + x'^3/6 - x'^4/24 + x'^5/120 (x' = 2x) below x' = 1/16
 // (where 1 - e^{-x'} cancels) and one reciprocal for the product of the three
@@ -80,16 +84,11 @@ __device__ __forceinline__ float situ_glu_f32(float g, float u, const SituParams
   constexpr float kLog2e = 1.4426950408889634f;
   const float t1 = tanh_approx(g * p.inv_b1);  // tanh(g / b1), carries sign(g)
   const float t2 = tanh_approx(u * p.inv_b2);  // tanh(u / b2), carries sign(u)
-  const bool gneg = g < 0.0f;
-  // r = 2^64 e^{-|g|} for g < 0, e^{-|g|} otherwise.
-  const float r = ex2_approx(fmaf(-fabsf(g), kLog2e, gneg ? 64.0f : 0.0f));
-  const float e0 = gneg ? r * 0x1p-64f : r;  // e^{-|g|}
-  const float ps = gneg ? r : 0x1p64f;       // 2^64 P
-  // h 2^64 = b1 b2 (2^64 P) / (1 + e^{-|g|}) tanh(g/b1) tanh(u/b2); scale dropped last.
-  float h = (p.b1b2 * ps) * rcp_approx(1.0f + e0);
+  // 2^64 sigmoid(g) = 1 / (2^-64 + e^{-g} 2^-64)
+  const float s = rcp_approx(0x1p-64f + ex2_approx(fmaf(-g, kLog2e, -64.0f)));
+  float h = p.b1b2 * s;
   h = h * t1;
   h = h * t2;
-  h = h > p.limit ? p.limit : (h < -p.limit ? -p.limit : h);  // NaN passes through
   return h * 0x1p-64f;  // correctly rounded, subnormals kept
 }
 
