@@ -233,6 +233,10 @@ def bench_dense(args, dev, peaks, world, flush):
 
     per_step, (t_gu, t_down) = timed_steps(step, args.steps, args.warmup, flush, world, inner=1)
     ms = mean(per_step)
+    # The same fused GEMM with both caps removed (SwiGLU): the cost of the caps.
+    inf = float("inf")
+    sw_ms, _ = timed_steps(lambda m: situ.situ_ffn_gate_up(x, wgu, inf, inf, h=h), args.steps,
+                           args.warmup, flush, world)
     flop_gu = 2.0 * w.rows * w.M * 2 * w.I
     flop_down = 2.0 * w.rows * w.I * w.M
     out = {
@@ -242,6 +246,7 @@ def bench_dense(args, dev, peaks, world, flush):
         "gate_up_tflops": flop_gu / (mean(t_gu) * 1e-3) / 1e12,
         "down_tflops": flop_down / (mean(t_down) * 1e-3) / 1e12,
         "flop_gate_up": flop_gu,
+        "swiglu_gate_up_ms": mean(sw_ms),
     }
 
     # End to end through the public host-buffer call: x is copied in from pinned host
@@ -274,9 +279,12 @@ def bench_act(args, dev, peaks, world, flush):
     per_step, _ = timed_steps(lambda m: situ.situ_glu_act(g, wl.BETA, wl.LINEAR_BETA, out=o),
                               args.steps, args.warmup, flush, world)
     ms = mean(per_step)
+    inf = float("inf")
+    sw_ms, _ = timed_steps(lambda m: situ.situ_glu_act(g, inf, inf, out=o), args.steps,
+                           args.warmup, flush, world)
     nbytes = 3 * w.rows * w.I * 2  # read 2I, write I per row, bf16
     gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"workload": w.name, "ms": ms, "bytes": nbytes, "gbs": gbs,
+    return {"workload": w.name, "ms": ms, "bytes": nbytes, "gbs": gbs, "swiglu_ms": mean(sw_ms),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}}
 
@@ -494,8 +502,18 @@ def run_situ(args):
         "clocks": clocks,
         "device_status": status,
     }
+    cost = {"page_remark": "two extra tanh per element, on the order of a percent of the FFN "
+                           "(unmeasured remark on the SiTU-GLU chapter page)",
+            "fused_gate_up_situ_ms": dense["gate_up_ms"],
+            "fused_gate_up_swiglu_ms": dense["swiglu_gate_up_ms"],
+            "fused_gate_up_overhead_pct": 100.0 * (dense["gate_up_ms"] / dense["swiglu_gate_up_ms"]
+                                                   - 1.0)}
     if act:
         line["act"] = act
+        cost["act_situ_ms"] = act["ms"]
+        cost["act_swiglu_ms"] = act["swiglu_ms"]
+        cost["act_overhead_pct"] = 100.0 * (act["ms"] / act["swiglu_ms"] - 1.0)
+    line["situ_cost_vs_swiglu"] = cost
     if moe:
         line["moe"] = moe
     if rank == 0 and not args.no_cpu_baseline:

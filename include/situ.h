@@ -29,8 +29,13 @@
  *     situ_device_status() after synchronising the stream.
  *   - Inputs are never written ("Do not mutate any input tensor", problem page,
  *     "Requirements").  An output that overlaps an input returns SITU_ERR_ALIAS.
- *   - Both caps must be finite and > 0 ("Both cap values are positive", problem
- *     page, "Constraints"); otherwise SITU_ERR_ARG.
+ *   - Each cap (beta, linear_beta) is either finite in (0, 2^20] ("Both cap
+ *     values are positive", problem page, "Constraints") or +infinity, which
+ *     leaves that branch uncapped: beta tanh(x / beta) -> x as beta -> infinity.
+ *     An infinite up cap is the activation module's linear_beta = None ("Kimi K3 -
+ *     Bound the up branch", SituAndMul excerpt); both caps infinite is SwiGLU
+ *     ("SiTU-GLU" chapter, "Les proprietes").  Anything else returns SITU_ERR_ARG.
+ *     The bound |h| <= beta * linear_beta holds when both caps are finite.
  *   - The output dtype equals the input dtype ("Preserve the floating-point dtype",
  *     problem page, "Requirements").  Activation math is FP32 in every path.
  *   - Matrices are row-major.  Weights use the [out, in] orientation of a
@@ -97,7 +102,7 @@ situ_status situ_device_status(int clear);
  *            gate_up.
  *   rows     >= 0; leading dimensions flattened by the caller.
  *   I        >= 1 (half the width of gate_up).
- *   beta, linear_beta   gate and up caps, finite and > 0.
+ *   beta, linear_beta   gate and up caps (see the conventions above).
  * Rows whose start is 16-byte aligned (bf16: I % 8 == 0, f32: I % 4 == 0, and
  * 16-byte aligned base pointers) take the 128-bit vector path; other shapes take
  * a scalar path, never an error.  |out| <= beta * linear_beta holds exactly.

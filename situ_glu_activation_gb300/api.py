@@ -34,6 +34,19 @@ def _stream(device: torch.device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
 
+def caps(beta, linear_beta):
+    """The caps as the C ABI takes them.
+
+    Follows the activation module of "Kimi K3 - Bound the up branch": a gate cap
+    of None (or 0) becomes 1.0 (its ``beta or 1.0``), an up cap of None leaves the
+    up branch uncapped, passed as +infinity (the limit beta -> infinity of
+    beta tanh(x/beta) is x).  +infinity for both caps is SwiGLU.
+    """
+    b1 = 1.0 if not beta else float(beta)
+    b2 = float("inf") if linear_beta is None else float(linear_beta)
+    return b1, b2
+
+
 def situ_glu_act(gate_up: torch.Tensor, beta: float = 4.0, linear_beta: float = 25.0,
                  out: torch.Tensor | None = None) -> torch.Tensor:
     """SiTU-GLU of a packed [..., 2I] tensor -> [..., I], same dtype.
@@ -57,7 +70,7 @@ def situ_glu_act(gate_up: torch.Tensor, beta: float = 4.0, linear_beta: float = 
         return out
     lib = _native.lib()
     check("situ_glu_act", lib.situ_glu_act(gate_up.data_ptr(), out.data_ptr(), rows, I,
-                                           float(beta), float(linear_beta), _dt(gate_up),
+                                           *caps(beta, linear_beta), _dt(gate_up),
                                            _stream(gate_up.device)))
     return out
 
@@ -100,7 +113,7 @@ def situ_ffn_forward(x: torch.Tensor, W_gate_up: torch.Tensor, W_down: torch.Ten
           lib.situ_ffn_forward(x.data_ptr(), W_gate_up.data_ptr(), W_down.data_ptr(),
                                y.data_ptr(), workspace.data_ptr(),
                                workspace.numel() * workspace.element_size(), R, M, I,
-                               float(beta), float(linear_beta), _dt(x), _stream(x.device)))
+                               *caps(beta, linear_beta), _dt(x), _stream(x.device)))
     return y
 
 
@@ -139,7 +152,7 @@ def situ_ffn_forward_host(x_host: torch.Tensor, W_gate_up: torch.Tensor, W_down:
           lib.situ_ffn_forward_host(x_host.data_ptr(), W_gate_up.data_ptr(), W_down.data_ptr(),
                                     y_host.data_ptr(), workspace.data_ptr(),
                                     workspace.numel() * workspace.element_size(), R, M, I,
-                                    chunk_rows, float(beta), float(linear_beta), _dt(x_host),
+                                    chunk_rows, *caps(beta, linear_beta), _dt(x_host),
                                     _stream(dev)))
     return y_host
 
@@ -165,7 +178,7 @@ def situ_ffn_gate_up(x: torch.Tensor, W_gate_up: torch.Tensor, beta: float = 4.0
         return h
     check("situ_ffn_gate_up",
           _native.lib().situ_ffn_gate_up(x.data_ptr(), W_gate_up.data_ptr(), h.data_ptr(), R, M,
-                                         I, float(beta), float(linear_beta), _dt(x),
+                                         I, *caps(beta, linear_beta), _dt(x),
                                          _stream(x.device)))
     return h
 
@@ -256,7 +269,7 @@ def situ_moe_grouped_forward(x: torch.Tensor, expert_offsets: torch.Tensor,
                                        token_index.data_ptr(), W_gate_up.data_ptr(),
                                        W_down.data_ptr(), y.data_ptr(), workspace.data_ptr(),
                                        workspace.numel() * workspace.element_size(), T,
-                                       k_eff, E, M, I, float(beta), float(linear_beta),
+                                       k_eff, E, M, I, *caps(beta, linear_beta),
                                        _dt(x), _stream(x.device)))
     return y
 

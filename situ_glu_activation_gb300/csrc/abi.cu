@@ -63,12 +63,10 @@ situ_status device_state(DeviceState** out) {
   return SITU_OK;
 }
 
+// Each cap is either finite in (0, 2^20] or +infinity (that branch uncapped).
 bool caps_ok(float beta, float linear_beta) {
-  if (!(std::isfinite(beta) && std::isfinite(linear_beta))) return false;
-  if (!(beta > 0.0f && linear_beta > 0.0f)) return false;
-  // beta1 * beta2 * 2^64 must stay finite in FP32 (the scaled product).
-  const double prod = static_cast<double>(beta) * linear_beta;
-  return prod < 1.0e19;
+  auto one = [](float b) { return b == INFINITY || (b > 0.0f && b <= kMaxFiniteCap); };
+  return one(beta) && one(linear_beta);
 }
 
 bool dtype_ok(situ_dtype dt) { return dt == SITU_BF16 || dt == SITU_F32; }
@@ -137,8 +135,9 @@ situ_status situ_glu_act(const void* gate_up, void* out, int64_t rows, int64_t I
   DeviceState* st = nullptr;
   situ_status s = device_state(&st);
   if (s != SITU_OK) return s;
-  return finish(launch_situ_act(gate_up, out, rows, I, make_situ_params(beta, linear_beta), dt,
-                                st->num_sms, static_cast<cudaStream_t>(stream)));
+  return finish(launch_situ_act(gate_up, out, rows, I, make_situ_params(beta, linear_beta),
+                                caps_of(beta, linear_beta), dt, st->num_sms,
+                                static_cast<cudaStream_t>(stream)));
 }
 
 size_t situ_ffn_workspace_size(int64_t R, int64_t M, int64_t I, situ_dtype dt) {
@@ -166,7 +165,8 @@ situ_status bf16_gemm_checks(const void* a, const void* b, const void* c, int64_
 }
 
 cudaError_t run_gate_up(const DeviceState* st, const void* x, const void* W_gate_up, void* h,
-                        int64_t R, int64_t M, int64_t I, const SituParams& p, cudaStream_t cs) {
+                        int64_t R, int64_t M, int64_t I, float beta, float linear_beta,
+                        cudaStream_t cs) {
   GemmShape g{};
   g.a = x;
   g.a_rows = R;
@@ -180,7 +180,8 @@ cudaError_t run_gate_up(const DeviceState* st, const void* x, const void* W_gate
   g.out = h;
   g.ldo = I;
   g.out_rows = R;
-  return launch_gemm_situ(g, p, st->status, st->num_sms, cs);
+  return launch_gemm_situ(g, make_situ_params(beta, linear_beta), caps_of(beta, linear_beta),
+                          st->status, st->num_sms, cs);
 }
 
 cudaError_t run_down(const DeviceState* st, const void* h, const void* W_down, void* y,
@@ -234,11 +235,11 @@ situ_status situ_ffn_forward(const void* x, const void* W_gate_up, const void* W
                                  static_cast<const float*>(W_gate_up),
                                  static_cast<const float*>(W_down),
                                  static_cast<float*>(workspace), static_cast<float*>(y), R, M,
-                                 I, p, cs));
+                                 I, p, caps_of(beta, linear_beta), cs));
   }
   if ((s = bf16_gemm_checks(x, W_gate_up, W_down, M, I)) != SITU_OK) return s;
   if (!aligned16(y)) return SITU_ERR_ALIGN;
-  cudaError_t e = run_gate_up(st, x, W_gate_up, workspace, R, M, I, p, cs);
+  cudaError_t e = run_gate_up(st, x, W_gate_up, workspace, R, M, I, beta, linear_beta, cs);
   if (e != cudaSuccess) return cuda_fail(e);
   return finish(run_down(st, workspace, W_down, y, R, M, I, cs));
 }
@@ -258,7 +259,7 @@ situ_status situ_ffn_gate_up(const void* x, const void* W_gate_up, void* h, int6
   if ((s = bf16_gemm_checks(x, W_gate_up, h, M, I)) != SITU_OK) return s;
   DeviceState* st = nullptr;
   if ((s = device_state(&st)) != SITU_OK) return s;
-  return finish(run_gate_up(st, x, W_gate_up, h, R, M, I, make_situ_params(beta, linear_beta),
+  return finish(run_gate_up(st, x, W_gate_up, h, R, M, I, beta, linear_beta,
                             static_cast<cudaStream_t>(stream)));
 }
 
@@ -381,7 +382,7 @@ situ_status situ_moe_grouped_forward(const void* x, const int32_t* expert_offset
   g.out = h_perm;
   g.ldo = I;
   g.out_rows = R;
-  e = launch_gemm_situ(g, p, st->status, st->num_sms, cs);
+  e = launch_gemm_situ(g, p, caps_of(beta, linear_beta), st->status, st->num_sms, cs);
   if (e != cudaSuccess) return cuda_fail(e);
   GemmShape d{};
   d.a = h_perm;

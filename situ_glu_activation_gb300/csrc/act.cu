@@ -35,15 +35,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+template <Caps kC>
 __device__ __forceinline__ uint32_t situ_word(uint32_t gw, uint32_t uw, const SituParams& p) {
-  return pack_bf16x2(situ_glu_f32(bf16_lo(gw), bf16_lo(uw), p),
-                     situ_glu_f32(bf16_hi(gw), bf16_hi(uw), p));
+  return pack_bf16x2(situ_act<kC>(bf16_lo(gw), bf16_lo(uw), p),
+                     situ_act<kC>(bf16_hi(gw), bf16_hi(uw), p));
 }
 
 // Vector path, bf16: one step = 8 consecutive outputs of one row.  vpr = I / 8
 // steps per row; (row, c) walks the flattened [rows, vpr] space with a
 // grid-wide stride split as stride = q * vpr + rem so no division is needed
 // inside the loop.
+template <Caps kC>
 __global__ void __launch_bounds__(kActThreads)
     act_bf16_vec_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, uint32_t rows,
                         uint32_t vpr, uint32_t q, uint32_t rem, SituParams p) {
@@ -73,10 +75,10 @@ __global__ void __launch_bounds__(kActThreads)
     for (int k = 0; k < kActUnroll; ++k) {
       if (rr[k] < rows) {
         uint4 o;
-        o.x = situ_word(gv[k].x, uv[k].x, p);
-        o.y = situ_word(gv[k].y, uv[k].y, p);
-        o.z = situ_word(gv[k].z, uv[k].z, p);
-        o.w = situ_word(gv[k].w, uv[k].w, p);
+        o.x = situ_word<kC>(gv[k].x, uv[k].x, p);
+        o.y = situ_word<kC>(gv[k].y, uv[k].y, p);
+        o.z = situ_word<kC>(gv[k].z, uv[k].z, p);
+        o.w = situ_word<kC>(gv[k].w, uv[k].w, p);
         __stcs(out + static_cast<size_t>(rr[k]) * vpr + cc[k], o);
       }
     }
@@ -84,6 +86,7 @@ __global__ void __launch_bounds__(kActThreads)
 }
 
 // Vector path, float32: one step = 4 consecutive outputs.
+template <Caps kC>
 __global__ void __launch_bounds__(kActThreads)
     act_f32_vec_kernel(const float4* __restrict__ in, float4* __restrict__ out, uint32_t rows,
                        uint32_t vpr, uint32_t q, uint32_t rem, SituParams p) {
@@ -95,10 +98,10 @@ __global__ void __launch_bounds__(kActThreads)
     const float4 g = __ldcs(src);
     const float4 u = __ldcs(src + vpr);
     float4 o;
-    o.x = situ_glu_f32_accurate(g.x, u.x, p);
-    o.y = situ_glu_f32_accurate(g.y, u.y, p);
-    o.z = situ_glu_f32_accurate(g.z, u.z, p);
-    o.w = situ_glu_f32_accurate(g.w, u.w, p);
+    o.x = situ_act_accurate<kC>(g.x, u.x, p);
+    o.y = situ_act_accurate<kC>(g.y, u.y, p);
+    o.z = situ_act_accurate<kC>(g.z, u.z, p);
+    o.w = situ_act_accurate<kC>(g.w, u.w, p);
     __stcs(out + static_cast<size_t>(row) * vpr + c, o);
     row += q;
     c += rem;
@@ -131,7 +134,7 @@ __device__ __forceinline__ void store_elem<__nv_bfloat16>(__nv_bfloat16* p, size
   p[i] = __float2bfloat16_rn(v);
 }
 
-template <typename T>
+template <typename T, Caps kC>
 __global__ void __launch_bounds__(kActThreads)
     act_scalar_kernel(const T* __restrict__ in, T* __restrict__ out, uint64_t rows, uint64_t I,
                       SituParams p) {
@@ -143,12 +146,13 @@ __global__ void __launch_bounds__(kActThreads)
     const float g = load_elem(in, r * 2 * I + j);
     const float u = load_elem(in, r * 2 * I + I + j);
     // float32 outputs take the accurate variant; bf16 outputs the fast one.
-    const float h = sizeof(T) == 4 ? situ_glu_f32_accurate(g, u, p) : situ_glu_f32(g, u, p);
+    const float h = sizeof(T) == 4 ? situ_act_accurate<kC>(g, u, p) : situ_act<kC>(g, u, p);
     store_elem(out, idx, h);
   }
 }
 
 // FP32 small-shape FFN, first half: h[r, j] = SiTU-GLU(x[r] . Wgu[j], x[r] . Wgu[I + j]).
+template <Caps kC>
 __global__ void ffn_f32_gate_up_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                        float* __restrict__ h, int64_t R, int64_t M, int64_t I,
                                        SituParams p) {
@@ -165,7 +169,7 @@ __global__ void ffn_f32_gate_up_kernel(const float* __restrict__ x, const float*
       g = fmaf(xr[k], wg[k], g);
       u = fmaf(xr[k], wu[k], u);
     }
-    h[idx] = situ_glu_f32_accurate(g, u, p);
+    h[idx] = situ_act_accurate<kC>(g, u, p);
   }
 }
 
@@ -191,12 +195,10 @@ inline int grid_for(int64_t work_items, int threads, int max_blocks) {
   return b < 1 ? 1 : static_cast<int>(b);
 }
 
-}  // namespace
-
-cudaError_t launch_situ_act(const void* gate_up, void* out, int64_t rows, int64_t I,
-                            const SituParams& p, situ_dtype dt, int num_sms,
-                            cudaStream_t stream) {
-  if (rows == 0 || I == 0) return cudaSuccess;
+template <Caps kC>
+cudaError_t launch_situ_act_caps(const void* gate_up, void* out, int64_t rows, int64_t I,
+                                 const SituParams& p, situ_dtype dt, int num_sms,
+                                 cudaStream_t stream) {
   const int max_blocks = num_sms * kActBlocksPerSm;
   const size_t esz = dtype_size(dt);
   const int elems_per_vec = static_cast<int>(16 / esz);
@@ -210,22 +212,22 @@ cudaError_t launch_situ_act(const void* gate_up, void* out, int64_t rows, int64_
     const uint32_t q = stride / static_cast<uint32_t>(vpr);
     const uint32_t rem = stride - q * static_cast<uint32_t>(vpr);
     if (dt == SITU_BF16) {
-      act_bf16_vec_kernel<<<grid, kActThreads, 0, stream>>>(
+      act_bf16_vec_kernel<kC><<<grid, kActThreads, 0, stream>>>(
           static_cast<const uint4*>(gate_up), static_cast<uint4*>(out),
           static_cast<uint32_t>(rows), static_cast<uint32_t>(vpr), q, rem, p);
     } else {
-      act_f32_vec_kernel<<<grid, kActThreads, 0, stream>>>(
+      act_f32_vec_kernel<kC><<<grid, kActThreads, 0, stream>>>(
           static_cast<const float4*>(gate_up), static_cast<float4*>(out),
           static_cast<uint32_t>(rows), static_cast<uint32_t>(vpr), q, rem, p);
     }
   } else {
     const int grid = grid_for(rows * I, kActThreads, max_blocks);
     if (dt == SITU_BF16) {
-      act_scalar_kernel<__nv_bfloat16><<<grid, kActThreads, 0, stream>>>(
+      act_scalar_kernel<__nv_bfloat16, kC><<<grid, kActThreads, 0, stream>>>(
           static_cast<const __nv_bfloat16*>(gate_up), static_cast<__nv_bfloat16*>(out),
           static_cast<uint64_t>(rows), static_cast<uint64_t>(I), p);
     } else {
-      act_scalar_kernel<float><<<grid, kActThreads, 0, stream>>>(
+      act_scalar_kernel<float, kC><<<grid, kActThreads, 0, stream>>>(
           static_cast<const float*>(gate_up), static_cast<float*>(out),
           static_cast<uint64_t>(rows), static_cast<uint64_t>(I), p);
     }
@@ -233,18 +235,54 @@ cudaError_t launch_situ_act(const void* gate_up, void* out, int64_t rows, int64_
   return cudaGetLastError();
 }
 
-cudaError_t launch_ffn_f32(const float* x, const float* w_gate_up, const float* w_down,
-                           float* h, float* y, int64_t R, int64_t M, int64_t I,
-                           const SituParams& p, cudaStream_t stream) {
-  if (R == 0) return cudaSuccess;
+template <Caps kC>
+cudaError_t launch_ffn_f32_caps(const float* x, const float* w_gate_up, const float* w_down,
+                                float* h, float* y, int64_t R, int64_t M, int64_t I,
+                                const SituParams& p, cudaStream_t stream) {
   constexpr int threads = 128;
-  ffn_f32_gate_up_kernel<<<grid_for(R * I, threads, 4096), threads, 0, stream>>>(
+  ffn_f32_gate_up_kernel<kC><<<grid_for(R * I, threads, 4096), threads, 0, stream>>>(
       x, w_gate_up, h, R, M, I, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ffn_f32_down_kernel<<<grid_for(R * M, threads, 4096), threads, 0, stream>>>(h, w_down, y, R,
                                                                               M, I);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_situ_act(const void* gate_up, void* out, int64_t rows, int64_t I,
+                            const SituParams& p, Caps caps, situ_dtype dt, int num_sms,
+                            cudaStream_t stream) {
+  if (rows == 0 || I == 0) return cudaSuccess;
+  switch (caps) {
+    case Caps::kBoth:
+      return launch_situ_act_caps<Caps::kBoth>(gate_up, out, rows, I, p, dt, num_sms, stream);
+    case Caps::kGateOnly:
+      return launch_situ_act_caps<Caps::kGateOnly>(gate_up, out, rows, I, p, dt, num_sms, stream);
+    case Caps::kUpOnly:
+      return launch_situ_act_caps<Caps::kUpOnly>(gate_up, out, rows, I, p, dt, num_sms, stream);
+    case Caps::kNone:
+      return launch_situ_act_caps<Caps::kNone>(gate_up, out, rows, I, p, dt, num_sms, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_ffn_f32(const float* x, const float* w_gate_up, const float* w_down,
+                           float* h, float* y, int64_t R, int64_t M, int64_t I,
+                           const SituParams& p, Caps caps, cudaStream_t stream) {
+  if (R == 0) return cudaSuccess;
+  switch (caps) {
+    case Caps::kBoth:
+      return launch_ffn_f32_caps<Caps::kBoth>(x, w_gate_up, w_down, h, y, R, M, I, p, stream);
+    case Caps::kGateOnly:
+      return launch_ffn_f32_caps<Caps::kGateOnly>(x, w_gate_up, w_down, h, y, R, M, I, p, stream);
+    case Caps::kUpOnly:
+      return launch_ffn_f32_caps<Caps::kUpOnly>(x, w_gate_up, w_down, h, y, R, M, I, p, stream);
+    case Caps::kNone:
+      return launch_ffn_f32_caps<Caps::kNone>(x, w_gate_up, w_down, h, y, R, M, I, p, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace situ

@@ -217,7 +217,7 @@ __device__ __forceinline__ void store_row_chunk(__nv_bfloat16* dst, const uint32
   }
 }
 
-template <Epi kEpi, bool kPair>
+template <Epi kEpi, Caps kC, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_a64,
@@ -406,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             w[i] = pack_bf16x2(
-                situ_glu_f32(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), args.sp),
-                situ_glu_f32(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]),
+                situ_act<kC>(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), args.sp),
+                situ_act<kC>(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]),
                              args.sp));
           }
           const int64_t col0 = static_cast<int64_t>(tc.n_tile) * 128 + c * 32;
@@ -577,9 +577,9 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
 
 constexpr size_t kSmemBytes = kStages * kStageBytes + sizeof(SharedCtl) + 1024;
 
-// Most 2-CTA clusters of ffn_gemm_kernel<kEpi, true> resident at once, per
+// Most 2-CTA clusters of ffn_gemm_kernel<kEpi, kC, true> resident at once, per
 // device (0 if the query fails: the unpaired kernel is used then).
-template <Epi kEpi>
+template <Epi kEpi, Caps kC>
 int max_pair_clusters(size_t smem) {
   static int cached[64] = {};
   static bool done[64] = {};
@@ -599,7 +599,7 @@ int max_pair_clusters(size_t smem) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, ffn_gemm_kernel<kEpi, true>, &cfg) == cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&n, ffn_gemm_kernel<kEpi, kC, true>, &cfg) == cudaSuccess)
       cached[dev] = n;
     else
       (void)cudaGetLastError();
@@ -607,7 +607,7 @@ int max_pair_clusters(size_t smem) {
   return cached[dev];
 }
 
-template <Epi kEpi>
+template <Epi kEpi, Caps kC>
 cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, int num_sms,
                    cudaStream_t stream) {
   if (s.a_rows == 0 && !s.tile_offsets) return cudaSuccess;
@@ -633,12 +633,12 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
   a.out_row_index = s.out_row_index;
   a.sp = p;
   a.status = status;
-  for (auto fn : {ffn_gemm_kernel<kEpi, false>, ffn_gemm_kernel<kEpi, true>}) {
+  for (auto fn : {ffn_gemm_kernel<kEpi, kC, false>, ffn_gemm_kernel<kEpi, kC, true>}) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
   }
-  int clusters = max_pair_clusters<kEpi>(kSmemBytes);
+  int clusters = max_pair_clusters<kEpi, kC>(kSmemBytes);
   if (clusters > 0 && (!s.tile_offsets || s.unit_offsets)) {
     // Clusters of two CTAs sharing a B or an A tile by multicast.
     a.unit_offsets = s.unit_offsets;
@@ -659,27 +659,34 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, true>, ma, ma64, mb, a);
+    return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, kC, true>, ma, ma64, mb, a);
   }
   int grid = num_sms;
   if (!s.tile_offsets) {
     const int64_t tiles = ((s.a_rows + kBM - 1) / kBM) * a.n_tiles;
     if (tiles < grid) grid = static_cast<int>(tiles);
   }
-  ffn_gemm_kernel<kEpi, false><<<grid, kThreads, kSmemBytes, stream>>>(ma, ma64, mb, a);
+  ffn_gemm_kernel<kEpi, kC, false><<<grid, kThreads, kSmemBytes, stream>>>(ma, ma64, mb, a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_situ(const GemmShape& s, const SituParams& p, uint32_t* status,
-                             int num_sms, cudaStream_t stream) {
-  return launch<Epi::kSitu>(s, p, status, num_sms, stream);
+cudaError_t launch_gemm_situ(const GemmShape& s, const SituParams& p, Caps caps,
+                             uint32_t* status, int num_sms, cudaStream_t stream) {
+  switch (caps) {
+    case Caps::kBoth: return launch<Epi::kSitu, Caps::kBoth>(s, p, status, num_sms, stream);
+    case Caps::kGateOnly:
+      return launch<Epi::kSitu, Caps::kGateOnly>(s, p, status, num_sms, stream);
+    case Caps::kUpOnly: return launch<Epi::kSitu, Caps::kUpOnly>(s, p, status, num_sms, stream);
+    case Caps::kNone: return launch<Epi::kSitu, Caps::kNone>(s, p, status, num_sms, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
                               cudaStream_t stream) {
-  return launch<Epi::kPlain>(s, SituParams{}, status, num_sms, stream);
+  return launch<Epi::kPlain, Caps::kBoth>(s, SituParams{}, status, num_sms, stream);
 }
 
 cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,

@@ -60,9 +60,8 @@ extern "C" situ_status situ_ffn_forward_noalloc(const void* x, const void* W_gat
                                                 float linear_beta, situ_dtype dt,
                                                 void* stream) {
   if ((dt != SITU_BF16 && dt != SITU_F32) || R < 0 || M < 1 || I < 1) return SITU_ERR_ARG;
-  if (!(beta > 0.0f && linear_beta > 0.0f && beta < 3.0e38f && linear_beta < 3.0e38f) ||
-      static_cast<double>(beta) * linear_beta >= 1.0e19)
-    return SITU_ERR_ARG;
+  auto cap_ok = [](float b) { return b == INFINITY || (b > 0.0f && b <= kMaxFiniteCap); };
+  if (!cap_ok(beta) || !cap_ok(linear_beta)) return SITU_ERR_ARG;
   if (R == 0) return SITU_OK;
   if (!x || !W_gate_up || !W_down || !y) return SITU_ERR_ARG;
   const size_t esz = dtype_size(dt);
@@ -89,7 +88,7 @@ extern "C" situ_status situ_ffn_forward_noalloc(const void* x, const void* W_gat
       return SITU_ERR_ALIGN;
     e = launch_ffn_f32(static_cast<const float*>(x), static_cast<const float*>(W_gate_up),
                        static_cast<const float*>(W_down), static_cast<float*>(scratch),
-                       static_cast<float*>(y), R, M, I, p, cs);
+                       static_cast<float*>(y), R, M, I, p, caps_of(beta, linear_beta), cs);
     return e == cudaSuccess ? SITU_OK : report_cuda_error(e);
   }
   if (M % 8 || I % 8) return SITU_ERR_UNSUPPORTED;
@@ -109,7 +108,8 @@ extern "C" situ_status situ_ffn_forward_noalloc(const void* x, const void* W_gat
   g.out = scratch;  // h [R, I]
   g.ldo = I;
   g.out_rows = R;
-  if ((e = launch_gemm_situ(g, p, status, num_sms, cs)) != cudaSuccess)
+  if ((e = launch_gemm_situ(g, p, caps_of(beta, linear_beta), status, num_sms, cs)) !=
+      cudaSuccess)
     return report_cuda_error(e);
   GemmShape d{};
   d.a = scratch;

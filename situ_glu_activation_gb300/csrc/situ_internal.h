@@ -15,18 +15,27 @@ namespace situ {
 // Bytes of one element of a library dtype.
 inline size_t dtype_size(situ_dtype dt) { return dt == SITU_F32 ? 4 : 2; }
 
+// Largest finite cap the kernels accept (2^20); +infinity means "no cap".
+constexpr float kMaxFiniteCap = 1048576.0f;
+
+// Cap configuration from the two cap arguments (+infinity = uncapped branch).
+inline Caps caps_of(float beta, float linear_beta) {
+  const bool gi = beta > kMaxFiniteCap, ui = linear_beta > kMaxFiniteCap;
+  return gi ? (ui ? Caps::kNone : Caps::kUpOnly) : (ui ? Caps::kGateOnly : Caps::kBoth);
+}
+
 // ----- standalone activation (act.cu) --------------------------------------
 // gate_up [rows, 2I] -> out [rows, I]; picks the 128-bit path when rows start
 // 16-byte aligned, else the scalar path.
 cudaError_t launch_situ_act(const void* gate_up, void* out, int64_t rows, int64_t I,
-                            const SituParams& p, situ_dtype dt, int num_sms,
+                            const SituParams& p, Caps caps, situ_dtype dt, int num_sms,
                             cudaStream_t stream);
 
 // ----- FP32 small-shape FFN (act.cu) ----------------------------------------
 // h [R, I] = SiTU-GLU(x W_gate_up^T) then y [R, M] = h W_down^T, all float32.
 cudaError_t launch_ffn_f32(const float* x, const float* w_gate_up, const float* w_down,
                            float* h, float* y, int64_t R, int64_t M, int64_t I,
-                           const SituParams& p, cudaStream_t stream);
+                           const SituParams& p, Caps caps, cudaStream_t stream);
 
 // ----- tcgen05 GEMMs (gemm.cu) ------------------------------------------------
 struct GemmShape {
@@ -56,8 +65,8 @@ struct GemmShape {
 
 // gu = A B^T with the SiTU-GLU epilogue: output column j of group tile n pairs B
 // row n*128 + j (gate) with B row b_up_offset + n*128 + j (up).
-cudaError_t launch_gemm_situ(const GemmShape& s, const SituParams& p, uint32_t* status,
-                             int num_sms, cudaStream_t stream);
+cudaError_t launch_gemm_situ(const GemmShape& s, const SituParams& p, Caps caps,
+                             uint32_t* status, int num_sms, cudaStream_t stream);
 // C = A B^T, bf16 output.
 cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
                               cudaStream_t stream);

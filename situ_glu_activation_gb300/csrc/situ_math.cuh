@@ -32,32 +32,44 @@
 // round-to-nearest multiply by a factor of magnitude <= 1 never increases a
 // magnitude, so |h| <= b1 b2 holds structurally, with no clamp.  NaN propagates.
 //
-// situ_glu_f32_accurate is the variant for float32 outputs, where a 2^-11 error
-// would be visible: the sigmoid as P / (1 + e^{-|g|}) (P = 1 or e^{-|g|}, the
-// latter carried as 2^64 e^{-|g|}), each tanh in exponential form,
+// situ_act_accurate is the variant for float32 outputs, where a 2^-11 error would
+// be visible: the sigmoid as P / (1 + e^{-|g|}) (P = 1 or e^{-|g|}, the latter
+// carried as 2^64 e^{-|g|}), each tanh in exponential form,
 // tanh(x) = (1 - e^{-2x}) / (1 + e^{-2x}) for x >= 0, with 1 - e^{-2x} from its
 // Taylor series x' - x'^2/2 + x'^3/6 - x'^4/24 + x'^5/120 (x' = 2x) below x' = 1/16
-// (where 1 - e^{-x'} cancels) and one reciprocal for the product of the three
-// denominators.  Relative error a few 2^-20.
+// (where 1 - e^{-x'} cancels).  Relative error a few 2^-18 (the exponent
+// argument's rounding dominates in the negative tail).
 #pragma once
 
 #include <cstdint>
 
 namespace situ {
 
+// Which branches carry a soft cap.  A cap of +infinity stands for "no cap":
+// beta tanh(x / beta) -> x as beta -> infinity, so the uncapped up branch is the
+// activation module's linear_beta = None ("Kimi K3 - Bound the up branch", code
+// excerpt of SituAndMul) and both caps infinite give SwiGLU exactly (the
+// "SiTU-GLU" chapter, "Les proprietes": SwiGLU again as beta1, beta2 -> infinity).
+enum class Caps : int {
+  kBoth = 0,      // SiTU-GLU: beta1 on the gate, beta2 on the up branch
+  kGateOnly = 1,  // up branch uncapped (linear_beta unset)
+  kUpOnly = 2,    // gate branch uncapped (Swish gate), up branch capped
+  kNone = 3       // SwiGLU
+};
+
 struct SituParams {
-  float inv_b1;  // 1 / beta1
-  float inv_b2;  // 1 / beta2
-  float b1b2;    // beta1 * beta2, the bound on |h|
-  float limit;   // beta1 * beta2 * 2^64: the bound before the final 2^-64 scale
+  float b1, b2;          // the caps (finite ones only are used)
+  float inv_b1, inv_b2;  // 1 / beta1, 1 / beta2
+  float b1b2;            // beta1 * beta2, the bound on |h| when both are finite
 };
 
 __host__ __device__ inline SituParams make_situ_params(float beta, float linear_beta) {
   SituParams p;
+  p.b1 = beta;
+  p.b2 = linear_beta;
   p.inv_b1 = 1.0f / beta;
   p.inv_b2 = 1.0f / linear_beta;
   p.b1b2 = beta * linear_beta;
-  p.limit = p.b1b2 * 0x1p64f;
   return p;
 }
 
@@ -79,17 +91,11 @@ __device__ __forceinline__ float tanh_approx(float x) {
   return y;
 }
 
-// One SiTU-GLU output in FP32 (see the header comment for the method).
-__device__ __forceinline__ float situ_glu_f32(float g, float u, const SituParams& p) {
-  constexpr float kLog2e = 1.4426950408889634f;
-  const float t1 = tanh_approx(g * p.inv_b1);  // tanh(g / b1), carries sign(g)
-  const float t2 = tanh_approx(u * p.inv_b2);  // tanh(u / b2), carries sign(u)
-  // 2^64 sigmoid(g) = 1 / (2^-64 + e^{-g} 2^-64)
-  const float s = rcp_approx(0x1p-64f + ex2_approx(fmaf(-g, kLog2e, -64.0f)));
-  float h = p.b1b2 * s;
-  h = h * t1;
-  h = h * t2;
-  return h * 0x1p-64f;  // correctly rounded, subnormals kept
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^64 sigmoid(g) = 1 / (2^-64 + e^{-g} 2^-64), select-free (see the header).
+__device__ __forceinline__ float sigmoid_x2p64(float g) {
+  return rcp_approx(0x1p-64f + ex2_approx(fmaf(-g, kLog2e, -64.0f)));
 }
 
 // 1 - exp(-x) for x >= 0: Taylor series below 1/16, else 1 - e (e = exp(-x)).
@@ -102,30 +108,79 @@ __device__ __forceinline__ float one_minus_exp_neg(float x, float e) {
   return x < 0.0625f ? series : 1.0f - e;
 }
 
-// One SiTU-GLU output in FP32 for float32 outputs (see the header comment).
-__device__ __forceinline__ float situ_glu_f32_accurate(float g, float u, const SituParams& p) {
-  constexpr float kLog2e = 1.4426950408889634f;
-  const float ag = fabsf(g);
-  const float au = fabsf(u);
-  const float x1 = 2.0f * ag * p.inv_b1;  // 2|g|/b1
-  const float x2 = 2.0f * au * p.inv_b2;  // 2|u|/b2
-  const float e1 = ex2_approx(-x1 * kLog2e);
-  const float f = ex2_approx(-x2 * kLog2e);
-  const float n1 = one_minus_exp_neg(x1, e1);
-  const float n2 = one_minus_exp_neg(x2, f);
+// tanh(x) in exponential form, for float32 outputs: sign(x) (1 - e)/(1 + e),
+// e = exp(-2|x|), with 1 - e from the series where it cancels.
+__device__ __forceinline__ float tanh_accurate(float x) {
+  const float x2 = 2.0f * fabsf(x);
+  const float e = ex2_approx(-x2 * kLog2e);
+  const float t = one_minus_exp_neg(x2, e) * rcp_approx(1.0f + e);
+  return __uint_as_float(__float_as_uint(t) | (__float_as_uint(x) & 0x80000000u));
+}
+
+// 2^64 sigmoid(g) as P / (1 + e^{-|g|}), P = 1 or e^{-|g|} (carried as
+// 2^64 e^{-|g|}), for float32 outputs.
+__device__ __forceinline__ float sigmoid_x2p64_accurate(float g) {
   const bool gneg = g < 0.0f;
-  const float r = ex2_approx(fmaf(-ag, kLog2e, gneg ? 64.0f : 0.0f));
+  const float r = ex2_approx(fmaf(-fabsf(g), kLog2e, gneg ? 64.0f : 0.0f));
   const float e0 = gneg ? r * 0x1p-64f : r;
-  const float ps = gneg ? r : 0x1p64f;
-  const float den = (1.0f + e1) * (1.0f + f) * (1.0f + e0);
-  float mag = p.b1b2 * ps;
-  mag = mag * rcp_approx(den);
-  mag = mag * n1;
-  mag = mag * n2;
-  mag = mag > p.limit ? p.limit : mag;
-  const float h = mag * 0x1p-64f;
-  const uint32_t sign = (__float_as_uint(g) ^ __float_as_uint(u)) & 0x80000000u;
-  return __uint_as_float(__float_as_uint(h) | sign);
+  return (gneg ? r : 0x1p64f) * rcp_approx(1.0f + e0);
+}
+
+// Combine tanh values t1 = tanh(g/b1), t2 = tanh(u/b2) and s = 2^64 sigmoid(g)
+// into h for the cap configuration kC.  The 2^64 scale is dropped by the last
+// multiply, so subnormal outputs are correctly rounded.  For the uncapped
+// branches the scale is applied where no intermediate can overflow: a gate value
+// above 2^40 is used unscaled (its sigmoid is exactly 1), and an up value above
+// 2^20 in magnitude is scaled down instead of the product.
+template <Caps kC>
+__device__ __forceinline__ float situ_combine(float g, float u, float t1, float t2, float s,
+                                              const SituParams& p) {
+  if constexpr (kC == Caps::kBoth) {
+    float h = p.b1b2 * s;
+    h = h * t1;
+    h = h * t2;
+    return h * 0x1p-64f;
+  } else {
+    constexpr bool kCapGate = kC == Caps::kGateOnly;
+    constexpr bool kCapUp = kC == Caps::kUpOnly;
+    float a_s, scale;
+    if constexpr (kCapGate) {
+      a_s = (p.b1 * s) * t1;  // 2^64 * b1 tanh(g/b1) sigmoid(g)
+      scale = 0x1p-64f;
+    } else {
+      const bool big = g > 0x1p40f;
+      a_s = big ? g : g * s;  // 2^64 * g sigmoid(g), or g itself when sigmoid(g) = 1
+      scale = big ? 1.0f : 0x1p-64f;
+    }
+    const float b = kCapUp ? p.b2 * t2 : u;
+    return fabsf(b) <= 0x1p20f ? (a_s * b) * scale : a_s * (b * scale);
+  }
+}
+
+// One activation output in FP32, fast form (bf16 outputs): hardware tanh.approx
+// for the caps (see the header comment for the method and its error).
+template <Caps kC>
+__device__ __forceinline__ float situ_act(float g, float u, const SituParams& p) {
+  const bool cap_g = kC == Caps::kBoth || kC == Caps::kGateOnly;
+  const bool cap_u = kC == Caps::kBoth || kC == Caps::kUpOnly;
+  const float t1 = cap_g ? tanh_approx(g * p.inv_b1) : 0.0f;
+  const float t2 = cap_u ? tanh_approx(u * p.inv_b2) : 0.0f;
+  return situ_combine<kC>(g, u, t1, t2, sigmoid_x2p64(g), p);
+}
+
+// Same, accurate form (float32 outputs): exponential-form tanh and sigmoid.
+template <Caps kC>
+__device__ __forceinline__ float situ_act_accurate(float g, float u, const SituParams& p) {
+  const bool cap_g = kC == Caps::kBoth || kC == Caps::kGateOnly;
+  const bool cap_u = kC == Caps::kBoth || kC == Caps::kUpOnly;
+  const float t1 = cap_g ? tanh_accurate(g * p.inv_b1) : 0.0f;
+  const float t2 = cap_u ? tanh_accurate(u * p.inv_b2) : 0.0f;
+  return situ_combine<kC>(g, u, t1, t2, sigmoid_x2p64_accurate(g), p);
+}
+
+// SiTU-GLU with both caps (the hot path).
+__device__ __forceinline__ float situ_glu_f32(float g, float u, const SituParams& p) {
+  return situ_act<Caps::kBoth>(g, u, p);
 }
 
 }  // namespace situ

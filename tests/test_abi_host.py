@@ -7,6 +7,8 @@ import re
 import pytest
 
 from situ_glu_activation_gb300 import _native
+
+BAD, ALIAS, WS = 1, 3, 8
 from situ_glu_activation_gb300.build import INCLUDE
 
 HEADER = os.path.join(INCLUDE, "situ.h")
@@ -51,15 +53,29 @@ def test_workspace_sizes(situ_lib):
     assert situ_lib.situ_moe_index_workspace_size(1025, 10) == 256
 
 
-BAD, ALIAS, WS = 1, 3, 8
-
-
 @pytest.mark.parametrize("beta,lbeta", [(0.0, 25.0), (4.0, -1.0), (float("nan"), 25.0),
-                                        (4.0, float("inf")), (1e10, 1e10)])
-def test_caps_must_be_positive_and_finite(situ_lib, beta, lbeta):
-    # Rejected before any pointer is touched (the problem page: both caps positive).
+                                        (4.0, -float("inf")), (2.0e6, 25.0), (4.0, 1e10)])
+def test_caps_must_be_positive(situ_lib, beta, lbeta):
+    # Rejected before any pointer is touched (the problem page: both caps positive;
+    # finite caps up to 2^20, +inf = uncapped).
     assert situ_lib.situ_glu_act(16, 32, 4, 8, beta, lbeta, 0, None) == BAD
     assert situ_lib.situ_ffn_forward(16, 16, 16, 16, 16, 0, 4, 8, 8, beta, lbeta, 0, None) == BAD
+
+
+@pytest.mark.parametrize("beta,lbeta", [(4.0, float("inf")), (float("inf"), 25.0),
+                                        (float("inf"), float("inf")), (1048576.0, 1.0)])
+def test_infinite_cap_means_uncapped(situ_lib, beta, lbeta):
+    # Accepted caps: the call proceeds to the pointer checks (here: overlap).
+    assert situ_lib.situ_glu_act(4096, 4096 + 64, 4, 8, beta, lbeta, 0, None) == ALIAS
+
+
+def test_python_caps_follow_the_activation_module():
+    from situ_glu_activation_gb300.api import caps
+    inf = float("inf")
+    assert caps(4.0, 25.0) == (4.0, 25.0)
+    assert caps(None, 25.0) == (1.0, 25.0) and caps(0, 25.0) == (1.0, 25.0)  # beta or 1.0
+    assert caps(4.0, None) == (4.0, inf)                                       # no up cap
+    assert caps(inf, inf) == (inf, inf)
 
 
 def test_argument_checks(situ_lib):

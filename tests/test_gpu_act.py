@@ -24,6 +24,16 @@ OTHER = [2.0, -3.0, 0.5, 25.0, -1e4, 1e-3, -1e-30, 100.0, 7.5, -60.0,
          _bits(0x0001), _bits(0x8080), float("inf")]
 
 
+INF = float("inf")
+# The variants: up branch uncapped (linear_beta None), gate uncapped, SwiGLU.
+VARIANTS = [(4.0, INF), (INF, 25.0), (INF, INF)]
+
+
+def _oracle_caps(b1, b2):
+    """The oracle writes "no cap" as a cap of 0."""
+    return (0.0 if b1 == INF else b1), (0.0 if b2 == INF else b2)
+
+
 def _run(gate_up_cpu, dev, beta=4.0, lbeta=25.0):
     out = situ.situ_glu_act(gate_up_cpu.to(dev), beta, lbeta)
     torch.cuda.synchronize()
@@ -43,6 +53,31 @@ def test_exhaustive_bf16(oracle, cuda_dev, half):
     got = _run(gate_up, cuda_dev)
     ref = oracle.situ_glu_act(oracle_input(gate_up))
     assert_within_ulp(got, ref, f"exhaustive {half}")
+
+
+@pytest.mark.parametrize("caps", VARIANTS, ids=["up_uncapped", "gate_uncapped", "swiglu"])
+@pytest.mark.parametrize("half", ["gate", "up"])
+def test_exhaustive_bf16_variants(oracle, cuda_dev, caps, half):
+    """The uncapped variants on every bf16 value of one branch (no bound applies)."""
+    allv = _all_bf16()
+    n = allv.numel()
+    rows = []
+    for v in OTHER:
+        fixed = torch.full((n,), v, dtype=torch.bfloat16)
+        rows.append(torch.cat([allv, fixed]) if half == "gate" else torch.cat([fixed, allv]))
+    gate_up = torch.stack(rows)
+    got = _run(gate_up, cuda_dev, *caps)
+    ref = oracle.situ_glu_act(oracle_input(gate_up), *_oracle_caps(*caps))
+    assert_within_ulp(got, ref, f"exhaustive {half} {caps}", bound=INF)
+
+
+@pytest.mark.parametrize("caps", VARIANTS, ids=["up_uncapped", "gate_uncapped", "swiglu"])
+def test_fp32_variants(oracle, cuda_dev, caps):
+    g = wl.gate_up_input(wl.WORKLOADS["act"], seed=8, rows=64).float()
+    got = _run(g, cuda_dev, *caps)
+    ref = oracle.situ_glu_act(oracle_input(g), *_oracle_caps(*caps))
+    err = np.abs(got - ref)
+    assert (err <= 1e-5 * np.abs(ref) + 1e-40).all(), float((err / (np.abs(ref) + 1e-40)).max())
 
 
 def test_act_workload_slab(oracle, cuda_dev):

@@ -33,6 +33,21 @@ def test_dense_small(oracle, cuda_dev, R, M, I):
     assert_ffn_close(to_f64(y), ref, f"ffn {R}x{M}x{I}")
 
 
+INF = float("inf")
+
+
+@pytest.mark.parametrize("caps", [(4.0, INF), (INF, 25.0), (INF, INF), (1.0, 1.0)],
+                         ids=["up_uncapped", "gate_uncapped", "swiglu", "unit_caps"])
+def test_dense_variants(oracle, cuda_dev, caps):
+    """The fused epilogue with each cap configuration (+inf = uncapped branch)."""
+    R, M, I = 300, 512, 384
+    x, wgu, wd = wl.ffn_inputs(M, I, R, seed=21)
+    y = _ffn(x, wgu, wd, cuda_dev, beta=caps[0], linear_beta=caps[1])
+    oc = tuple(0.0 if c == INF else c for c in caps)
+    ref = oracle.ffn_forward(oracle_input(x), oracle_input(wgu), oracle_input(wd), *oc)
+    assert_ffn_close(to_f64(y), ref, f"ffn caps {caps}")
+
+
 def test_dense_h_in_workspace(oracle, cuda_dev):
     """The fused epilogue's output h (kept in the workspace) matches the oracle's h."""
     R, M, I = 200, 256, 384

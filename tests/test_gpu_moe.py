@@ -71,6 +71,24 @@ def test_grouped_small(oracle, cuda_dev, T, k, E, M, I):
     assert_ffn_close(to_f64(y), ref, f"grouped {T}x{k} E={E}")
 
 
+def test_grouped_swiglu_variant(oracle, cuda_dev):
+    """The grouped epilogue with both caps removed (SwiGLU)."""
+    T, k, E, M, I = 60, 2, 5, 256, 384
+    g = torch.Generator().manual_seed(3)
+    ids = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    x = wl.normal((T, M), 1.0, seed=4)
+    wgu, wd = wl.expert_weights(E, M, I, seed=5)
+    ids_d = ids.to(cuda_dev)
+    off, tix = situ.situ_moe_build_index(ids_d, E)
+    inf = float("inf")
+    y = situ.situ_moe_grouped_forward(x.to(cuda_dev), off, tix, wgu.to(cuda_dev), wd.to(cuda_dev),
+                                      k, inf, inf)
+    torch.cuda.synchronize()
+    ref = oracle.moe_grouped_forward(oracle_input(x), ids.numpy(), oracle_input(wgu),
+                                     oracle_input(wd), 0.0, 0.0)
+    assert_ffn_close(to_f64(y), ref, "grouped swiglu")
+
+
 def test_grouped_equals_dense_per_expert(cuda_dev):
     """Grouped vs naive on the GPU: each (token, slot) row equals the dense FFN of
     that expert applied to the token (same kernels, same rounding of h)."""
