@@ -35,7 +35,8 @@
  *     An infinite up cap is the activation module's linear_beta = None ("Kimi K3 -
  *     Bound the up branch", SituAndMul excerpt); both caps infinite is SwiGLU
  *     ("SiTU-GLU" chapter, "Les proprietes").  Anything else returns SITU_ERR_ARG.
- *     The bound |h| <= beta * linear_beta holds when both caps are finite.
+ *     The bound |h| <= beta * linear_beta holds when both caps are finite.  With
+ *     the up branch uncapped, outputs are within 1 bf16 ulp for |u| <= 2^50.
  *   - The output dtype equals the input dtype ("Preserve the floating-point dtype",
  *     problem page, "Requirements").  Activation math is FP32 in every path.
  *   - Matrices are row-major.  Weights use the [out, in] orientation of a
