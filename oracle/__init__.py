@@ -61,6 +61,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         ("oracle_moe_build_index", [vp, i64, i32, vp, vp], ci),
         ("oracle_moe_grouped_forward",
          [vp, ci, vp, vp, vp, ci, dp, i64, i32, i32, i64, i64, d, d], ci),
+        ("oracle_moe_combine", [dp, vp, ci, dp, i64, i32, i64], ci),
         ("oracle_num_threads", [], ci),
     ]:
         fn = getattr(lib, name)
@@ -176,6 +177,18 @@ class Oracle:
         _check(self.lib.oracle_moe_build_index(_ptr(ids), ids.size, E, _ptr(offsets),
                                                _ptr(token_index)), "moe_build_index")
         return offsets, token_index
+
+    def moe_combine(self, y: np.ndarray, w: np.ndarray) -> np.ndarray:
+        """y [T, k_eff, M] (float64), w [T, k_eff] -> out [T, M] = sum_s w[t,s] y[t,s]."""
+        ya = np.ascontiguousarray(y, dtype=np.float64)
+        wa, wdt = _as_input(w)
+        T, k_eff, M = ya.shape
+        if wa.shape != (T, k_eff):
+            raise ValueError("weights must be [T, k_eff]")
+        out = np.empty((T, M), dtype=np.float64)
+        _check(self.lib.oracle_moe_combine(_ptr(ya), _ptr(wa), wdt, _ptr(out), T, k_eff, M),
+               "moe_combine")
+        return out
 
     def moe_grouped_forward(self, x: np.ndarray, expert_ids: np.ndarray,
                             w_gate_up: np.ndarray, w_down: np.ndarray,

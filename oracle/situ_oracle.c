@@ -252,6 +252,30 @@ int oracle_moe_grouped_forward(const void* x, int x_dt, const int32_t* expert_id
   return bad ? ORACLE_BAD_ARG : ORACLE_OK;
 }
 
+/* Combine of a routed layer: out[t, :] = sum over slots s of w[t, s] * y[t, s, :]
+ * in slot order, FP64.  The pages' MoE calls each routed and shared expert on its
+ * token rows ("SiTU-GLU" chapter, "Ou SiTU-GLU est utilise": 896 routed plus 2
+ * shared experts per layer; docs page: DenseFFN is the expert network inside the
+ * MoE); the layer output is the router-weighted sum of a token's expert outputs,
+ * with the shared experts as extra slots.  y is [T, k_eff, M] (double), w is
+ * [T, k_eff] (any accepted input type), out is [T, M]. */
+int oracle_moe_combine(const double* y, const void* w, int w_dt, double* out, int64_t T,
+                       int32_t k_eff, int64_t M) {
+  if (!oracle_dtype_ok(w_dt) || T < 0 || k_eff <= 0 || M <= 0) return ORACLE_BAD_ARG;
+  if (T == 0) return ORACLE_OK;
+  if (!y || !w || !out) return ORACLE_BAD_ARG;
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t) {
+    for (int64_t m = 0; m < M; ++m) {
+      double s = 0.0;
+      for (int32_t k = 0; k < k_eff; ++k)
+        s += oracle_load(w, w_dt, t * k_eff + k) * y[(t * k_eff + k) * M + m];
+      out[t * M + m] = s;
+    }
+  }
+  return ORACLE_OK;
+}
+
 /* Number of threads the oracle's parallel loops use. */
 int oracle_num_threads(void) {
 #ifdef _OPENMP

@@ -296,6 +296,27 @@ def pin_grouped_equals_naive(o):
             assert np.array_equal(y[t, s], want), (t, s)
 
 
+def pin_combine(o):
+    """Combine of a routed layer, checked by brute force: one-hot weights pick a
+    slot exactly, unit weights give the plain sum over slots (exact on integer
+    data), and the result is linear in the weights."""
+    rng = np.random.default_rng(12)
+    T, k, M = 5, 4, 6
+    y = rng.integers(-5, 6, (T, k, M)).astype(np.float64)
+    for s in range(k):
+        w = np.zeros((T, k))
+        w[:, s] = 1.0
+        assert np.array_equal(o.moe_combine(y, w), y[:, s, :])
+    assert np.array_equal(o.moe_combine(y, np.ones((T, k))), y.sum(axis=1))
+    w = rng.integers(-3, 4, (T, k)).astype(np.float64)
+    want = np.array([[sum(w[t, s] * y[t, s, m] for s in range(k)) for m in range(M)]
+                     for t in range(T)])
+    assert np.array_equal(o.moe_combine(y, w), want)
+    assert np.array_equal(o.moe_combine(y, 2.0 * w), 2.0 * want)
+    w32 = w.astype(np.float32)
+    assert np.array_equal(o.moe_combine(y, w32), want)
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_swiglu_gate_and_gaps,
@@ -313,6 +334,7 @@ ALL_PINS = [
     pin_ffn_dtypes,
     pin_build_index,
     pin_grouped_equals_naive,
+    pin_combine,
 ]
 
 

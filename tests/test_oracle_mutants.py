@@ -51,6 +51,10 @@ MUTANTS = {
     "gather_sorted_position": ("int64_t t = flat / k_eff;", "int64_t t = r / k_eff;"),
     "scatter_sorted_position": ("y + flat * M);", "y + r * M);"),
     "bf16_decode_shift": ("((uint32_t)v) << 16", "((uint32_t)v) << 15"),
+    "combine_wrong_weight": ("oracle_load(w, w_dt, t * k_eff + k) * y[(t * k_eff + k) * M + m]",
+                             "oracle_load(w, w_dt, t * k_eff) * y[(t * k_eff + k) * M + m]"),
+    "combine_dropped_slot": ("for (int32_t k = 0; k < k_eff; ++k)\n        s +=",
+                             "for (int32_t k = 1; k < k_eff; ++k)\n        s +="),
 }
 
 
