@@ -6,7 +6,7 @@ bf16): the tcgen05 gate_up GEMM with the activation fused into its epilogue,
 then the tcgen05 down GEMM.  ``value`` is tokens/s of that step, device-timed
 with CUDA events, L2 flushed between steps.  The same JSON line also carries:
   * ``act``: the standalone activation on [65536, 2x3072] bf16 (GB/s, HBM roofline);
-  * ``moe``: the grouped expert paths (index build + grouped FFN) on the Zipf
+  * ``moe``: the routed layer (index build + grouped FFN + combine) on the Zipf
     top-8 64-expert workload and on the Kimi-K3-shaped layer (896 routed + 2
     shared experts) at 512 and 32768 tokens;
   * ``roofline`` of the dominant kernel (the fused gate_up GEMM);
@@ -313,6 +313,8 @@ def bench_moe(args, dev, peaks, world, flush, names):
         off = torch.empty(E + 1, dtype=torch.int32, device=dev)
         tix = torch.empty(R, dtype=torch.int32, device=dev)
         y = torch.empty(w.T, w.k_eff, w.M, dtype=torch.bfloat16, device=dev)
+        cw = wl.combine_weights(w.T, w.k, len(w.shared), seed=0).to(dev)
+        layer_out = torch.empty(w.T, w.M, dtype=torch.bfloat16, device=dev)
         ws = torch.empty(situ.moe_workspace_bytes(R, E, w.M, w.I), dtype=torch.uint8, device=dev)
 
         def step(marks):
@@ -321,9 +323,12 @@ def bench_moe(args, dev, peaks, world, flush, names):
                 marks[0].record()
             situ.situ_moe_grouped_forward(x, off, tix, wgu, wd, w.k_eff, wl.BETA, wl.LINEAR_BETA,
                                           y=y, workspace=ws)
+            if marks:
+                marks[1].record()
+            situ.situ_moe_combine(y, cw, out=layer_out)
 
-        per_step, (t_idx, t_ffn) = timed_steps(step, args.steps, args.warmup, flush, world,
-                                               inner=1)
+        per_step, (t_idx, t_ffn, t_comb) = timed_steps(step, args.steps, args.warmup, flush,
+                                                       world, inner=2)
         ms = mean(per_step)
         counts = torch.bincount(ids_cpu.view(-1).long(), minlength=E)
         touched = int((counts > 0).sum())
@@ -333,11 +338,13 @@ def bench_moe(args, dev, peaks, world, flush, names):
         weight_gbs = wbytes / (ms * 1e-3) / 1e9
         results[name] = {
             "workload": w.name, "ms": ms, "index_ms": mean(t_idx), "ffn_ms": mean(t_ffn),
+            "combine_ms": mean(t_comb),
             "tokens": w.T, "routes": R, "experts_touched": touched,
             "tokens_per_s": w.T / (ms * 1e-3), "tflops": tflops,
             "tc_frac": tflops / peaks["bf16_tflops"],
             "weight_gbs": weight_gbs, "hbm_frac": weight_gbs / peaks["hbm_gbs"],
-            "launches_per_step": 3 + 4,
+            "launches_per_step": 3 + 4 + 1,
+            "step": "expert index, grouped SiTU-GLU experts, router-weighted combine",
         }
         del x, y, ws, off, tix, ids
     weights.clear()

@@ -304,6 +304,24 @@ situ_status situ_moe_grouped_forward(const void* x, const int32_t* expert_offset
                                      float linear_beta, situ_dtype dt, void* stream);
 
 /* -------------------------------------------------------------------------
+ * situ_moe_combine -- the layer output of a routed batch: for every token t,
+ *   out[t, :] = dtype( sum over slots s = 0 .. k_eff-1 of w[t, s] * y[t, s, :] ),
+ * accumulated in FP32 in slot order (deterministic; no atomics).  Each routed and
+ * shared expert of Kimi K3 runs on its tokens ("SiTU-GLU" chapter, "Ou SiTU-GLU
+ * est utilise"); the layer output is the router-weighted sum of a token's expert
+ * outputs, with shared experts as extra slots (weight 1 for a plain sum).
+ *
+ *   y        device, [T, k_eff, M] of `dt` (as situ_moe_grouped_forward writes it).
+ *   weights  device, [T, k_eff] float32 combine weights.
+ *   out      device, [T, M] of `dt`; must not overlap y or weights.
+ *   T >= 0, k_eff >= 1, M >= 1.  Rows start 16-byte aligned (M % 8 == 0 for bf16,
+ *   M % 4 == 0 for f32, aligned pointers) use 128-bit accesses, others a scalar path.
+ * Errors: SITU_ERR_ARG, SITU_ERR_ALIAS, SITU_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+situ_status situ_moe_combine(const void* y, const float* weights, void* out, int64_t T,
+                             int32_t k_eff, int64_t M, situ_dtype dt, void* stream);
+
+/* -------------------------------------------------------------------------
  * situ_selftest_bounded_wait -- failure-detection self test (no counterpart on
  * the pages).  Launches one block that waits on a shared-memory barrier nothing
  * ever completes, with a wait limit of `limit_us` microseconds (1..1000000).

@@ -13,12 +13,12 @@ from .api import (SituError, device_status, ffn_host_workspace_bytes, ffn_worksp
                   selftest_bounded_wait, situ_ffn_down, situ_ffn_forward, situ_ffn_forward_host,
                   situ_ffn_gate_up,
                   situ_glu_act,
-                  situ_moe_build_index, situ_moe_grouped_forward)
+                  situ_moe_build_index, situ_moe_combine, situ_moe_grouped_forward)
 
 __all__ = [
     "SituError", "situ_glu_act", "situ_ffn_forward", "situ_ffn_forward_host", "situ_ffn_gate_up",
     "situ_ffn_down",
     "situ_moe_build_index",
     "situ_moe_grouped_forward", "ffn_workspace_bytes", "moe_workspace_bytes",
-    "device_status", "selftest_bounded_wait", "ffn_host_workspace_bytes",
+    "device_status", "selftest_bounded_wait", "ffn_host_workspace_bytes", "situ_moe_combine",
 ]

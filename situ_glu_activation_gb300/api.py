@@ -274,6 +274,25 @@ def situ_moe_grouped_forward(x: torch.Tensor, expert_offsets: torch.Tensor,
     return y
 
 
+def situ_moe_combine(y: torch.Tensor, weights: torch.Tensor,
+                     out: torch.Tensor | None = None) -> torch.Tensor:
+    """Layer output of a routed batch: out[t] = sum_s weights[t, s] * y[t, s] (FP32,
+    slot order).  y [T, k_eff, M]; weights [T, k_eff] float32 -> out [T, M]."""
+    _cuda_contig("y", y)
+    _cuda_contig("weights", weights)
+    T, k_eff, M = y.shape
+    if weights.shape != (T, k_eff) or weights.dtype != torch.float32:
+        raise ValueError("weights must be float32 [T, k_eff]")
+    if out is None:
+        out = torch.empty(T, M, dtype=y.dtype, device=y.device)
+    if T == 0:
+        return out
+    check("situ_moe_combine",
+          _native.lib().situ_moe_combine(y.data_ptr(), weights.data_ptr(), out.data_ptr(), T,
+                                         k_eff, M, _dt(y), _stream(y.device)))
+    return out
+
+
 def device_status(clear: bool = True) -> int:
     """First device-side failure recorded since the last clear (0 = SITU_OK)."""
     return int(_native.lib().situ_device_status(1 if clear else 0))
@@ -291,5 +310,5 @@ __all__ = [
     "situ_ffn_down",
     "situ_moe_build_index",
     "situ_moe_grouped_forward", "ffn_workspace_bytes", "moe_workspace_bytes",
-    "device_status", "selftest_bounded_wait", "ffn_host_workspace_bytes",
+    "device_status", "selftest_bounded_wait", "ffn_host_workspace_bytes", "situ_moe_combine",
 ]

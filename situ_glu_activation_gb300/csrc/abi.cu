@@ -403,6 +403,26 @@ situ_status situ_moe_grouped_forward(const void* x, const int32_t* expert_offset
   return finish(launch_gemm_plain(d, st->status, st->num_sms, cs));
 }
 
+situ_status situ_moe_combine(const void* y, const float* weights, void* out, int64_t T,
+                             int32_t k_eff, int64_t M, situ_dtype dt, void* stream) {
+  if (!dtype_ok(dt) || T < 0 || k_eff < 1 || M < 1) return SITU_ERR_ARG;
+  if (T == 0) return SITU_OK;
+  if (!y || !weights || !out) return SITU_ERR_ARG;
+  const size_t esz = dtype_size(dt);
+  const size_t out_b = static_cast<size_t>(T) * M * esz;
+  if (overlap(out, out_b, y, static_cast<size_t>(T) * k_eff * M * esz) ||
+      overlap(out, out_b, weights, static_cast<size_t>(T) * k_eff * 4))
+    return SITU_ERR_ALIAS;
+  if (reinterpret_cast<uintptr_t>(y) % esz || reinterpret_cast<uintptr_t>(out) % esz ||
+      reinterpret_cast<uintptr_t>(weights) % 4)
+    return SITU_ERR_ALIGN;
+  DeviceState* st = nullptr;
+  situ_status s = device_state(&st);
+  if (s != SITU_OK) return s;
+  return finish(launch_combine(y, weights, out, T, k_eff, M, dt, st->num_sms,
+                               static_cast<cudaStream_t>(stream)));
+}
+
 situ_status situ_selftest_bounded_wait(uint32_t limit_us, void* stream) {
   if (limit_us < 1 || limit_us > 1000000) return SITU_ERR_ARG;
   DeviceState* st = nullptr;

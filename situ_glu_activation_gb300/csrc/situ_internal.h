@@ -84,6 +84,11 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* token_index, void* 
 cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, uint32_t* status,
                                          cudaStream_t stream);
 
+// ----- routed-layer combine (combine.cu) --------------------------------------
+// out[t, :] = sum_s w[t, s] * y[t, s, :] in FP32, slot order.
+cudaError_t launch_combine(const void* y, const float* w, void* out, int64_t T, int32_t k_eff,
+                           int64_t M, situ_dtype dt, int num_sms, cudaStream_t stream);
+
 // ----- expert index (moe_index.cu) -------------------------------------------
 size_t index_workspace_bytes(int64_t n, int32_t E);
 cudaError_t launch_build_index(const int32_t* expert_ids, int32_t* offsets,

@@ -180,6 +180,17 @@ def uniform_routes(T: int, E: int, k: int, shared=(), seed: int = 0) -> torch.Te
     return ids.contiguous()
 
 
+def combine_weights(T: int, k: int, n_shared: int = 0, seed: int = 0) -> torch.Tensor:
+    """Router combine weights [T, k + n_shared] float32: for the k routed slots a
+    softmax of seeded N(0, 1) logits (positive, summing to 1 per token), then
+    weight 1 for every shared-expert slot."""
+    g = generator(seed)
+    w = torch.softmax(torch.randn(T, k, generator=g, dtype=torch.float32), dim=1)
+    if n_shared:
+        w = torch.cat([w, torch.ones(T, n_shared, dtype=torch.float32)], dim=1)
+    return w.contiguous()
+
+
 def routes(w: Workload, seed: int = 0, T: int | None = None) -> torch.Tensor:
     T = w.T if T is None else T
     if w.routing == "zipf":

@@ -147,3 +147,43 @@ def test_bad_offsets_write_nothing(cuda_dev):
     torch.cuda.synchronize()
     assert situ.device_status(clear=True) == 7
     assert bool((y == 7.0).all())
+
+
+# ---------------------------------------------------------------------------
+# Combine (router-weighted sum of a token's slot outputs)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("T,k,M,dtype", [(100, 10, 2048, torch.bfloat16), (7, 3, 12, torch.bfloat16),
+                                         (33, 4, 64, torch.float32), (5, 1, 6, torch.float32)])
+def test_combine_against_oracle(oracle, cuda_dev, T, k, M, dtype):
+    """FP32 accumulation in slot order, one rounding: within 1 bf16 ulp of the FP64
+    combine plus 1e-6 of sum |w y| (cancellation)."""
+    y = wl.normal((T, k, M), 1.0, seed=T + k, dtype=dtype)
+    w = wl.combine_weights(T, k - 1 if k > 1 else 1, 1 if k > 1 else 0, seed=k)
+    out = situ.situ_moe_combine(y.to(cuda_dev), w.to(cuda_dev))
+    torch.cuda.synchronize()
+    ref = oracle.moe_combine(to_f64(y), w.numpy())
+    slack = 1e-6 * np.einsum("tk,tkm->tm", np.abs(w.numpy().astype(np.float64)), np.abs(to_f64(y)))
+    err = np.abs(to_f64(out) - ref)
+    from numerics import bf16_ulp
+    assert (err <= bf16_ulp(ref) + slack).all(), float((err - bf16_ulp(ref)).max())
+
+
+def test_moe_layer_output(oracle, cuda_dev):
+    """Index, grouped experts and combine together (a routed layer's output)
+    against the oracle's grouped FFN and combine."""
+    T, k, E, M, I = 40, 3, 6, 256, 384
+    g = torch.Generator().manual_seed(31)
+    ids = torch.stack([torch.randperm(E - 1, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    ids = torch.cat([ids, torch.full((T, 1), E - 1, dtype=torch.int32)], dim=1)  # a shared expert
+    x = wl.normal((T, M), 1.0, seed=32)
+    wgu, wd = wl.expert_weights(E, M, I, seed=33)
+    w = wl.combine_weights(T, k, 1, seed=34)
+    off, tix = situ.situ_moe_build_index(ids.to(cuda_dev), E)
+    y = situ.situ_moe_grouped_forward(x.to(cuda_dev), off, tix, wgu.to(cuda_dev), wd.to(cuda_dev),
+                                      k + 1)
+    out = situ.situ_moe_combine(y, w.to(cuda_dev))
+    torch.cuda.synchronize()
+    yref = oracle.moe_grouped_forward(oracle_input(x), ids.numpy(), oracle_input(wgu),
+                                      oracle_input(wd))
+    ref = oracle.moe_combine(yref, w.numpy())
+    assert_ffn_close(to_f64(out), ref, "moe layer output")
