@@ -62,6 +62,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         ("oracle_moe_grouped_forward",
          [vp, ci, vp, vp, vp, ci, dp, i64, i32, i32, i64, i64, d, d], ci),
         ("oracle_moe_combine", [dp, vp, ci, dp, i64, i32, i64], ci),
+        ("oracle_situ_pair_grad", [d, d, d, d, dp, dp], None),
+        ("oracle_ffn_backward", [vp, ci, vp, vp, ci, vp, ci, dp, dp, dp, dp, i64, i64, i64, d, d],
+         ci),
         ("oracle_num_threads", [], ci),
     ]:
         fn = getattr(lib, name)
@@ -177,6 +180,39 @@ class Oracle:
         _check(self.lib.oracle_moe_build_index(_ptr(ids), ids.size, E, _ptr(offsets),
                                                _ptr(token_index)), "moe_build_index")
         return offsets, token_index
+
+    def pair_grad(self, g, u, beta=4.0, linear_beta=25.0):
+        """(dh/dg, dh/du) of one SiTU-GLU coordinate."""
+        dg, du = ctypes.c_double(), ctypes.c_double()
+        self.lib.oracle_situ_pair_grad(float(g), float(u), float(beta), float(linear_beta),
+                                       ctypes.byref(dg), ctypes.byref(du))
+        return dg.value, du.value
+
+    def ffn_backward(self, x, w_gate_up, w_down, dy, beta=4.0, linear_beta=25.0,
+                     want_dgu=False):
+        """Gradients of the dense FFN for upstream dy [R, M]:
+        (dx [R, M], dW_gate_up [2I, M], dW_down [M, I]) and optionally dgu [R, 2I]."""
+        xa, xdt = _as_input(x)
+        wg, wdt = _as_input(w_gate_up)
+        wd, wdt2 = _as_input(w_down)
+        dya, dydt = _as_input(dy)
+        if wdt != wdt2:
+            raise TypeError("w_gate_up and w_down must share a dtype")
+        M = xa.shape[-1]
+        I = wg.shape[0] // 2
+        R = int(np.prod(xa.shape[:-1], dtype=np.int64))
+        if wg.shape != (2 * I, M) or wd.shape != (M, I) or dya.size != R * M:
+            raise ValueError("bad shapes")
+        dx = np.empty((R, M))
+        dwg = np.empty((2 * I, M))
+        dwd = np.empty((M, I))
+        dgu = np.empty((R, 2 * I)) if want_dgu else None
+        _check(self.lib.oracle_ffn_backward(_ptr(xa), xdt, _ptr(wg), _ptr(wd), wdt, _ptr(dya),
+                                            dydt, _ptr(dx), _ptr(dwg), _ptr(dwd),
+                                            _ptr(dgu) if want_dgu else None, R, M, I,
+                                            float(beta), float(linear_beta)), "ffn_backward")
+        out = (dx.reshape(xa.shape), dwg, dwd)
+        return out + (dgu,) if want_dgu else out
 
     def moe_combine(self, y: np.ndarray, w: np.ndarray) -> np.ndarray:
         """y [T, k_eff, M] (float64), w [T, k_eff] -> out [T, M] = sum_s w[t,s] y[t,s]."""

@@ -252,6 +252,114 @@ int oracle_moe_grouped_forward(const void* x, int x_dt, const int32_t* expert_id
   return bad ? ORACLE_BAD_ARG : ORACLE_OK;
 }
 
+/* Partial derivatives of one output coordinate h = a(g) b(u):
+ *   dh/dg = b(u) a'(g),  a'(g) = sech^2(g/b1) sigmoid(g)
+ *                                + b1 tanh(g/b1) sigmoid(g) (1 - sigmoid(g)),
+ *   dh/du = a(g) b'(u),  b'(u) = sech^2(u/b2).
+ * (Differentiation of the "Implementation order" steps of the problem page; the
+ * chapter's "Pourquoi un plafond doux" section notes that the soft cap keeps these
+ * gradients nonzero where a hard clamp would zero them.)  sech^2 is written
+ * 1 / cosh^2 and 1 - sigmoid(g) as sigmoid(-g), so neither cancels.  A cap <= 0
+ * means no cap: a = g sigmoid(g), a' = sigmoid(g) + g sigmoid(g) sigmoid(-g);
+ * b = u, b' = 1. */
+void oracle_situ_pair_grad(double g, double u, double beta, double linear_beta, double* dh_dg,
+                           double* dh_du) {
+  const double sg = oracle_sigmoid(g), sgm = oracle_sigmoid(-g);
+  double da;
+  if (beta > 0.0) {
+    const double c = cosh(g / beta);
+    da = sg / (c * c) + beta * tanh(g / beta) * sg * sgm;
+  } else {
+    da = sg + g * sg * sgm;
+  }
+  double db = 1.0;
+  if (linear_beta > 0.0) {
+    const double c = cosh(u / linear_beta);
+    db = 1.0 / (c * c);
+  }
+  *dh_dg = oracle_up_branch(u, linear_beta) * da;
+  *dh_du = oracle_gate_branch(g, beta) * db;
+}
+
+/* Backward of the dense FFN y = h W_down^T, h = SiTU-GLU(x W_gate_up^T), for a
+ * given upstream gradient dy [R, M], in FP64 with no intermediate rounding:
+ *   dh    = dy W_down                        [R, I]
+ *   dg_j  = dh_j dh/dg(g_j, u_j), du_j = dh_j dh/du(g_j, u_j)   (dgu = [dg, du])
+ *   dx    = dgu W_gate_up                    [R, M]
+ *   dW_down    = dy^T h                      [M, I]
+ *   dW_gate_up = dgu^T x                     [2I, M]
+ * dgu_out ([R, 2I]) may be NULL.  Plain loops; the weight gradients sum over the
+ * rows in ascending order. */
+int oracle_ffn_backward(const void* x, int x_dt, const void* w_gate_up, const void* w_down,
+                        int w_dt, const void* dy, int dy_dt, double* dx, double* dw_gate_up,
+                        double* dw_down, double* dgu_out, int64_t R, int64_t M, int64_t I,
+                        double beta, double linear_beta) {
+  if (!oracle_dtype_ok(x_dt) || !oracle_dtype_ok(w_dt) || !oracle_dtype_ok(dy_dt))
+    return ORACLE_BAD_ARG;
+  if (R < 0 || M <= 0 || I <= 0) return ORACLE_BAD_ARG;
+  if (!x || !w_gate_up || !w_down || !dy || !dx || !dw_gate_up || !dw_down) return ORACLE_BAD_ARG;
+  double* h = (double*)malloc(sizeof(double) * (size_t)(R * I + 1));
+  double* dgu = (double*)malloc(sizeof(double) * (size_t)(R * 2 * I + 1));
+  if (!h || !dgu) {
+    free(h);
+    free(dgu);
+    return ORACLE_BAD_ARG;
+  }
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < R; ++r) {
+    double* gu = (double*)malloc(sizeof(double) * (size_t)(2 * I));
+    if (!gu) {
+#pragma omp atomic write
+      bad = 1;
+      continue;
+    }
+    for (int64_t n = 0; n < 2 * I; ++n) {
+      double s = 0.0;
+      for (int64_t k = 0; k < M; ++k)
+        s += oracle_load(x, x_dt, r * M + k) * oracle_load(w_gate_up, w_dt, n * M + k);
+      gu[n] = s;
+    }
+    for (int64_t j = 0; j < I; ++j) {
+      h[r * I + j] = oracle_situ_pair(gu[j], gu[I + j], beta, linear_beta);
+      double dhj = 0.0;
+      for (int64_t m = 0; m < M; ++m)
+        dhj += oracle_load(dy, dy_dt, r * M + m) * oracle_load(w_down, w_dt, m * I + j);
+      double pg, pu;
+      oracle_situ_pair_grad(gu[j], gu[I + j], beta, linear_beta, &pg, &pu);
+      dgu[r * 2 * I + j] = dhj * pg;
+      dgu[r * 2 * I + I + j] = dhj * pu;
+    }
+    for (int64_t k = 0; k < M; ++k) {
+      double s = 0.0;
+      for (int64_t n = 0; n < 2 * I; ++n)
+        s += dgu[r * 2 * I + n] * oracle_load(w_gate_up, w_dt, n * M + k);
+      dx[r * M + k] = s;
+    }
+    free(gu);
+  }
+#pragma omp parallel for schedule(static)
+  for (int64_t m = 0; m < M; ++m) {
+    for (int64_t j = 0; j < I; ++j) {
+      double s = 0.0;
+      for (int64_t r = 0; r < R; ++r) s += oracle_load(dy, dy_dt, r * M + m) * h[r * I + j];
+      dw_down[m * I + j] = s;
+    }
+  }
+#pragma omp parallel for schedule(static)
+  for (int64_t n = 0; n < 2 * I; ++n) {
+    for (int64_t k = 0; k < M; ++k) {
+      double s = 0.0;
+      for (int64_t r = 0; r < R; ++r) s += dgu[r * 2 * I + n] * oracle_load(x, x_dt, r * M + k);
+      dw_gate_up[n * M + k] = s;
+    }
+  }
+  if (dgu_out) memcpy(dgu_out, dgu, sizeof(double) * (size_t)(R * 2 * I));
+  free(h);
+  free(dgu);
+  return bad ? ORACLE_BAD_ARG : ORACLE_OK;
+}
+
 /* Combine of a routed layer: out[t, :] = sum over slots s of w[t, s] * y[t, s, :]
  * in slot order, FP64.  The pages' MoE calls each routed and shared expert on its
  * token rows ("SiTU-GLU" chapter, "Ou SiTU-GLU est utilise": 896 routed plus 2

@@ -317,6 +317,88 @@ def pin_combine(o):
     assert np.array_equal(o.moe_combine(y, w32), want)
 
 
+def pin_pair_grad_finite_differences(o):
+    """The derivatives against central differences of the (separately pinned)
+    forward: error O(eps^2), far below 1e-6 relative at eps = 1e-5."""
+    rng = np.random.default_rng(21)
+    pts = list(rng.normal(0, 5, (60, 2))) + [(2.0, 2.0), (0.3, -40.0), (-30.0, 7.0), (60.0, 60.0)]
+    for b1, b2 in [(B1, B2), (1.0, 3.0), (0.0, 0.0), (B1, 0.0)]:
+        for g, u in pts:
+            dg, du = o.pair_grad(g, u, b1, b2)
+            eps = 1e-5 * max(1.0, abs(g))
+            fg = (o.pair(g + eps, u, b1, b2) - o.pair(g - eps, u, b1, b2)) / (2 * eps)
+            eps = 1e-5 * max(1.0, abs(u))
+            fu = (o.pair(g, u + eps, b1, b2) - o.pair(g, u - eps, b1, b2)) / (2 * eps)
+            assert abs(dg - fg) <= 1e-6 * (1 + abs(fg)), (b1, b2, g, u, dg, fg)
+            assert abs(du - fu) <= 1e-6 * (1 + abs(fu)), (b1, b2, g, u, du, fu)
+
+
+def pin_pair_grad_closed_forms(o):
+    """At g = 0: a'(0) = sech^2(0) sigmoid(0) = 1/2, so dh/dg = b(u)/2 and dh/du = 0
+    (a(0) = 0).  At u = 0: b'(0) = 1, so dh/du = a(g).  As the caps grow, a'
+    becomes Swish's derivative sigmoid(g) (1 + g (1 - sigmoid(g))).  Far out, the
+    soft caps keep the gradient nonzero (chapter, soft cap vs hard clamp)."""
+    for u in [0.5, 2.0, -7.0, 100.0]:
+        dg, du = o.pair_grad(0.0, u)
+        assert dg == o.up(u) / 2 and du == 0.0
+    for g in [-3.0, 0.25, 2.0, 9.0]:
+        dg, du = o.pair_grad(g, 0.0)
+        assert du == o.gate(g) and dg == 0.0
+    for g in [-2.0, 0.7, 3.0]:
+        s = 1.0 / (1.0 + math.exp(-g))
+        swish_prime = s * (1 + g * (1 - s))
+        dg, _ = o.pair_grad(g, 1.0, 1e8, 1e8)
+        assert abs(dg - swish_prime) <= 1e-9, (g, dg, swish_prime)
+    dg, du = o.pair_grad(30.0, 60.0)
+    assert dg > 0 and du > 0
+
+
+def pin_ffn_backward_structure(o):
+    """The backward's linear algebra by brute force on integer-valued data (exact
+    sums): dx = dgu W_gate_up, dW_down = dy^T h, dW_gate_up = dgu^T x, with dgu from
+    the pair derivatives and h from the forward oracle."""
+    rng = np.random.default_rng(22)
+    R, M, I = 3, 5, 4
+    x = rng.integers(-2, 3, (R, M)).astype(np.float64)
+    wgu = rng.integers(-1, 2, (2 * I, M)).astype(np.float64)
+    wd = rng.integers(-2, 3, (M, I)).astype(np.float64)
+    dy = rng.integers(-3, 4, (R, M)).astype(np.float64)
+    dx, dwg, dwd, dgu = o.ffn_backward(x, wgu, wd, dy, want_dgu=True)
+    gu = x @ wgu.T
+    _, h = o.ffn_forward(x, wgu, wd, want_h=True)
+    dh = dy @ wd
+    for r in range(R):
+        for j in range(I):
+            pg, pu = o.pair_grad(gu[r, j], gu[r, I + j])
+            assert dgu[r, j] == dh[r, j] * pg and dgu[r, I + j] == dh[r, j] * pu
+    np.testing.assert_allclose(dx, dgu @ wgu, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(dwd, dy.T @ h, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(dwg, dgu.T @ x, rtol=1e-13, atol=1e-13)
+
+
+def pin_ffn_backward_finite_differences(o):
+    """The FFN gradients against central differences of the forward oracle's loss
+    L = sum(dy * y) on a tiny random problem."""
+    rng = np.random.default_rng(23)
+    R, M, I = 2, 3, 2
+    x = rng.normal(size=(R, M))
+    wgu = rng.normal(size=(2 * I, M))
+    wd = rng.normal(size=(M, I))
+    dy = rng.normal(size=(R, M))
+    dx, dwg, dwd = o.ffn_backward(x, wgu, wd, dy)
+    loss = lambda x_, g_, d_: float((dy * o.ffn_forward(x_, g_, d_)).sum())
+    eps = 1e-6
+    for arr, grad, idx in [(x, dx, 0), (wgu, dwg, 1), (wd, dwd, 2)]:
+        for pos in np.ndindex(arr.shape):
+            args = [x.copy(), wgu.copy(), wd.copy()]
+            args[idx][pos] += eps
+            lp = loss(*args)
+            args[idx][pos] -= 2 * eps
+            lm = loss(*args)
+            fd = (lp - lm) / (2 * eps)
+            assert abs(grad[pos] - fd) <= 1e-6 * (1 + abs(fd)), (idx, pos, grad[pos], fd)
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_swiglu_gate_and_gaps,
@@ -335,6 +417,10 @@ ALL_PINS = [
     pin_build_index,
     pin_grouped_equals_naive,
     pin_combine,
+    pin_pair_grad_finite_differences,
+    pin_pair_grad_closed_forms,
+    pin_ffn_backward_structure,
+    pin_ffn_backward_finite_differences,
 ]
 
 

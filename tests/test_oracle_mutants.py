@@ -51,6 +51,18 @@ MUTANTS = {
     "gather_sorted_position": ("int64_t t = flat / k_eff;", "int64_t t = r / k_eff;"),
     "scatter_sorted_position": ("y + flat * M);", "y + r * M);"),
     "bf16_decode_shift": ("((uint32_t)v) << 16", "((uint32_t)v) << 15"),
+    "grad_missing_sigmoid_term": ("da = sg / (c * c) + beta * tanh(g / beta) * sg * sgm;",
+                                  "da = sg / (c * c);"),
+    "grad_sign_flip": ("da = sg / (c * c) + beta * tanh(g / beta) * sg * sgm;",
+                       "da = sg / (c * c) - beta * tanh(g / beta) * sg * sgm;"),
+    "grad_up_cap_swapped": ("const double c = cosh(u / linear_beta);",
+                            "const double c = cosh(u / beta);"),
+    "grad_products_swapped": ("*dh_dg = oracle_up_branch(u, linear_beta) * da;",
+                              "*dh_dg = oracle_gate_branch(g, beta) * da;"),
+    "bwd_dh_transposed": ("oracle_load(w_down, w_dt, m * I + j);\n      double pg",
+                          "oracle_load(w_down, w_dt, j * M + m);\n      double pg"),
+    "bwd_dw_down_wrong_operand": ("s += oracle_load(dy, dy_dt, r * M + m) * h[r * I + j];",
+                                  "s += oracle_load(x, x_dt, r * M + m) * h[r * I + j];"),
     "combine_wrong_weight": ("oracle_load(w, w_dt, t * k_eff + k) * y[(t * k_eff + k) * M + m]",
                              "oracle_load(w, w_dt, t * k_eff) * y[(t * k_eff + k) * M + m]"),
     "combine_dropped_slot": ("for (int32_t k = 0; k < k_eff; ++k)\n        s +=",
