@@ -9,6 +9,7 @@ with CUDA events, L2 flushed between steps.  The same JSON line also carries:
   * ``moe``: the routed layer (index build + grouped FFN + combine) on the Zipf
     top-8 64-expert workload and on the Kimi-K3-shaped layer (896 routed + 2
     shared experts) at 512 and 32768 tokens;
+  * ``train``: a training step of the dense FFN (forward keeping gu and h, backward);
   * ``roofline`` of the dominant kernel (the fused gate_up GEMM);
   * ``e2e``: the public ``situ_ffn_forward`` call with host (pinned) buffers,
     host->device copy of x and device->host copy of y inside the timed region;
@@ -352,6 +353,41 @@ def bench_moe(args, dev, peaks, world, flush, names):
     return results
 
 
+def bench_train(args, dev, peaks, world, flush):
+    """Training step of the dense FFN: forward that keeps gu and h, then the
+    backward for a seeded upstream gradient (dx, dW_gate_up, dW_down)."""
+    import torch
+
+    import situ_glu_activation_gb300 as situ
+    from situ_glu_activation_gb300 import workloads as wl
+
+    w = wl.WORKLOADS["dense"]
+    x, wgu, wd = wl.ffn_inputs(w.M, w.I, w.rows, seed=0, device=dev)
+    dy = wl.normal((w.rows, w.M), 1.0, seed=7, device=dev)
+    ws = torch.empty(situ.ffn_backward_workspace_bytes(w.rows, w.M, w.I), dtype=torch.uint8,
+                     device=dev)
+    state = {}
+
+    def step(marks):
+        y, gu, h = situ.situ_ffn_forward_train(x, wgu, wd, wl.BETA, wl.LINEAR_BETA)
+        if marks:
+            marks[0].record()
+        state["g"] = situ.situ_ffn_backward(x, wgu, wd, gu, h, dy, wl.BETA, wl.LINEAR_BETA,
+                                            workspace=ws)
+
+    per_step, (t_fwd, t_bwd) = timed_steps(step, args.steps, args.warmup, flush, world, inner=1)
+    ms = mean(per_step)
+    flop_f = 6.0 * w.rows * w.M * w.I
+    flop_b = 12.0 * w.rows * w.M * w.I
+    return {"workload": w.name + ", training step (forward keeping gu and h, backward)",
+            "ms": ms, "forward_ms": mean(t_fwd), "backward_ms": mean(t_bwd),
+            "tokens_per_s": w.rows / (ms * 1e-3),
+            "tflops": (flop_f + flop_b) / (ms * 1e-3) / 1e12,
+            "backward_tflops": flop_b / (mean(t_bwd) * 1e-3) / 1e12,
+            "tc_frac": (flop_f + flop_b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+            "launches_per_step": 2 + 10}
+
+
 def cpu_baseline(seconds: float, rows_hint: int = 0):
     """The FP64 oracle (as it stands) on a bounded sample of the dense workload's
     rows: rows/s = tokens/s on the host cores."""
@@ -451,6 +487,8 @@ def run_situ(args):
         # One workload alone (profiling runs): a reduced line with that result.
         if args.suite == "act":
             res = bench_act(args, dev, peaks, world, flush)
+        elif args.suite == "train":
+            res = bench_train(args, dev, peaks, world, flush)
         else:
             res = bench_moe(args, dev, peaks, world, flush, [args.suite])[args.suite]
         if rank == 0:
@@ -469,6 +507,7 @@ def run_situ(args):
     act = bench_act(args, dev, peaks, world, flush) if args.suite == "full" else None
     moe = (bench_moe(args, dev, peaks, world, flush, ["grouped", "k3_decode", "k3_prefill"])
            if args.suite == "full" else None)
+    train = bench_train(args, dev, peaks, world, flush) if args.suite == "full" else None
     status = situ.device_status(clear=True)
 
     achieved = dense["gate_up_tflops"]
@@ -523,6 +562,8 @@ def run_situ(args):
     line["situ_cost_vs_swiglu"] = cost
     if moe:
         line["moe"] = moe
+    if train:
+        line["train"] = train
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
@@ -543,7 +584,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["situ", "reference"], default="situ")
     ap.add_argument("--suite", default="full",
                     choices=["full", "dense", "act", "grouped", "k3_decode", "k3_prefill",
-                             "k3_prefill_slice"],
+                             "k3_prefill_slice", "train"],
                     help="full: the headline line with every sub-result; dense: the headline "
                          "only; any other name: that workload alone (for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -171,6 +171,52 @@ situ_status situ_ffn_down(const void* h, const void* W_down, void* y, int64_t R,
                           int64_t I, situ_dtype dt, void* stream);
 
 /* -------------------------------------------------------------------------
+ * situ_ffn_forward_train / situ_ffn_backward -- training pair of the dense FFN.
+ *
+ * The forward also keeps what the backward needs: the pre-activation pair
+ * gu = x W_gate_up^T (bf16, [R, 2I]: gate columns then up columns) and the
+ * activation h ([R, I]); y as situ_ffn_forward.
+ *
+ * The backward, for an upstream gradient dy [R, M], computes (FP32 accumulation,
+ * bf16 outputs), by differentiating the steps of "Implementation order"
+ * (problem page) -- the soft caps keep the gradient nonzero where a hard clamp
+ * would not ("SiTU-GLU" chapter, "Pourquoi un plafond doux"):
+ *   dh   = dy W_down                                   [R, I]
+ *   dg   = dh * b(u) * a'(g),  a'(g) = sech^2(g/b1) sigmoid(g)
+ *                                    + b1 tanh(g/b1) sigmoid(g) sigmoid(-g)
+ *   du   = dh * a(g) * sech^2(u/b2)          (dgu = [dg, du], [R, 2I], bf16)
+ *   dx   = dgu W_gate_up                              [R, M]
+ *   dW_down    = dy^T h                                [M, I]
+ *   dW_gate_up = dgu^T x                               [2I, M]
+ * evaluated at the saved bf16 gu.  Caps as everywhere (+inf = uncapped).
+ * The activation derivative runs in the epilogue of the dy W_down GEMM; the
+ * weight gradients contract over the R rows after a re-layout of the operands
+ * in the workspace.
+ *
+ *   all tensors device, bf16, row-major; gu and h as written by
+ *   situ_ffn_forward_train.  dx, dW_gate_up, dW_down are written and must not
+ *   overlap the inputs or the workspace.
+ *   workspace  >= situ_ffn_backward_workspace_size(R, M, I, dt) bytes, 256-byte
+ *              aligned.
+ *   bf16 only; M % 8 == 0, I % 8 == 0, 1 <= R <= 4194240, 16-byte aligned
+ *   pointers.
+ * Errors: SITU_ERR_ARG, SITU_ERR_ALIGN, SITU_ERR_ALIAS, SITU_ERR_WORKSPACE,
+ *         SITU_ERR_UNSUPPORTED, SITU_ERR_CUDA; SITU_ERR_TIMEOUT on the device.
+ * ------------------------------------------------------------------------- */
+situ_status situ_ffn_forward_train(const void* x, const void* W_gate_up, const void* W_down,
+                                   void* y, void* gu, void* h, int64_t R, int64_t M,
+                                   int64_t I, float beta, float linear_beta, situ_dtype dt,
+                                   void* stream);
+
+size_t situ_ffn_backward_workspace_size(int64_t R, int64_t M, int64_t I, situ_dtype dt);
+
+situ_status situ_ffn_backward(const void* x, const void* W_gate_up, const void* W_down,
+                              const void* gu, const void* h, const void* dy, void* dx,
+                              void* dW_gate_up, void* dW_down, void* workspace,
+                              size_t workspace_bytes, int64_t R, int64_t M, int64_t I,
+                              float beta, float linear_beta, situ_dtype dt, void* stream);
+
+/* -------------------------------------------------------------------------
  * situ_ffn_forward_host -- situ_ffn_forward with x and y in host memory.
  *
  * Same operation as situ_ffn_forward (docs page "Two linear maps"), for callers

@@ -8,7 +8,9 @@ Hand-written CUDA kernels behind a C ABI (``include/situ.h``, ``libsitu.so``):
   * ``situ_moe_grouped_forward``  the FFN grouped over experts
 This package is the thin PyTorch binding over that ABI.
 """
-from .api import (SituError, device_status, ffn_host_workspace_bytes, ffn_workspace_bytes,
+from .api import (SituError, device_status, ffn_backward_workspace_bytes,
+                  ffn_host_workspace_bytes, ffn_workspace_bytes, situ_ffn_backward,
+                  situ_ffn_forward_train,
                   moe_workspace_bytes,
                   selftest_bounded_wait, situ_ffn_down, situ_ffn_forward, situ_ffn_forward_host,
                   situ_ffn_gate_up,
@@ -21,4 +23,5 @@ __all__ = [
     "situ_moe_build_index",
     "situ_moe_grouped_forward", "ffn_workspace_bytes", "moe_workspace_bytes",
     "device_status", "selftest_bounded_wait", "ffn_host_workspace_bytes", "situ_moe_combine",
+    "situ_ffn_forward_train", "situ_ffn_backward", "ffn_backward_workspace_bytes",
 ]

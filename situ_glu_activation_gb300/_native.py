@@ -35,6 +35,11 @@ SIGNATURES = {
                          _ci),
     "situ_ffn_gate_up": ([_vp, _vp, _vp, _i64, _i64, _i64, _f32, _f32, _ci, _vp], _ci),
     "situ_ffn_down": ([_vp, _vp, _vp, _i64, _i64, _i64, _ci, _vp], _ci),
+    "situ_ffn_forward_train": ([_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _f32, _ci,
+                                _vp], _ci),
+    "situ_ffn_backward_workspace_size": ([_i64, _i64, _i64, _ci], _sz),
+    "situ_ffn_backward": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64,
+                           _i64, _f32, _f32, _ci, _vp], _ci),
     "situ_ffn_host_workspace_size": ([_i64, _i64, _i64, _ci, _i64], _sz),
     "situ_ffn_forward_host": ([_vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _i64, _i64, _f32, _f32,
                                _ci, _vp], _ci),

@@ -203,6 +203,64 @@ def situ_ffn_down(h: torch.Tensor, W_down: torch.Tensor,
     return y
 
 
+def situ_ffn_forward_train(x: torch.Tensor, W_gate_up: torch.Tensor, W_down: torch.Tensor,
+                           beta: float = 4.0, linear_beta: float = 25.0):
+    """Training forward of the dense FFN (bf16): returns (y, gu, h) where gu [R, 2I]
+    is the pre-activation (gate then up columns) and h [R, I] the activation, both
+    kept for situ_ffn_backward."""
+    for n, t in (("x", x), ("W_gate_up", W_gate_up), ("W_down", W_down)):
+        _cuda_contig(n, t)
+    M = x.shape[-1]
+    I = W_gate_up.shape[0] // 2
+    if W_gate_up.shape != (2 * I, M) or W_down.shape != (M, I):
+        raise ValueError("weight shapes do not match x")
+    R = x.numel() // M
+    y = torch.empty_like(x)
+    gu = torch.empty(R, 2 * I, dtype=x.dtype, device=x.device)
+    h = torch.empty(R, I, dtype=x.dtype, device=x.device)
+    if R:
+        check("situ_ffn_forward_train",
+              _native.lib().situ_ffn_forward_train(x.data_ptr(), W_gate_up.data_ptr(),
+                                                   W_down.data_ptr(), y.data_ptr(), gu.data_ptr(),
+                                                   h.data_ptr(), R, M, I,
+                                                   *caps(beta, linear_beta), _dt(x),
+                                                   _stream(x.device)))
+    return y, gu, h
+
+
+def situ_ffn_backward(x: torch.Tensor, W_gate_up: torch.Tensor, W_down: torch.Tensor,
+                      gu: torch.Tensor, h: torch.Tensor, dy: torch.Tensor, beta: float = 4.0,
+                      linear_beta: float = 25.0, workspace: torch.Tensor | None = None):
+    """Backward of the dense FFN for upstream dy [R, M] (bf16): returns
+    (dx [R, M], dW_gate_up [2I, M], dW_down [M, I])."""
+    for n, t in (("x", x), ("W_gate_up", W_gate_up), ("W_down", W_down), ("gu", gu), ("h", h),
+                 ("dy", dy)):
+        _cuda_contig(n, t)
+    M = x.shape[-1]
+    I = W_gate_up.shape[0] // 2
+    R = x.numel() // M
+    if gu.shape != (R, 2 * I) or h.shape != (R, I) or dy.numel() != R * M:
+        raise ValueError("gu, h or dy do not match x and the weights")
+    dx = torch.empty_like(x)
+    dwg = torch.empty_like(W_gate_up)
+    dwd = torch.empty_like(W_down)
+    lib = _native.lib()
+    need = int(lib.situ_ffn_backward_workspace_size(R, M, I, _dt(x)))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    check("situ_ffn_backward",
+          lib.situ_ffn_backward(x.data_ptr(), W_gate_up.data_ptr(), W_down.data_ptr(),
+                                gu.data_ptr(), h.data_ptr(), dy.data_ptr(), dx.data_ptr(),
+                                dwg.data_ptr(), dwd.data_ptr(), workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(), R, M, I,
+                                *caps(beta, linear_beta), _dt(x), _stream(x.device)))
+    return dx, dwg, dwd
+
+
+def ffn_backward_workspace_bytes(R: int, M: int, I: int) -> int:
+    return int(_native.lib().situ_ffn_backward_workspace_size(R, M, I, SITU_BF16))
+
+
 def situ_moe_build_index(expert_ids: torch.Tensor, num_experts: int,
                          expert_offsets: torch.Tensor | None = None,
                          token_index: torch.Tensor | None = None):
@@ -311,4 +369,5 @@ __all__ = [
     "situ_moe_build_index",
     "situ_moe_grouped_forward", "ffn_workspace_bytes", "moe_workspace_bytes",
     "device_status", "selftest_bounded_wait", "ffn_host_workspace_bytes", "situ_moe_combine",
+    "situ_ffn_forward_train", "situ_ffn_backward", "ffn_backward_workspace_bytes",
 ]

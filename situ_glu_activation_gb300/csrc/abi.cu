@@ -280,6 +280,211 @@ situ_status situ_ffn_down(const void* h, const void* W_down, void* y, int64_t R,
   return finish(run_down(st, h, W_down, y, R, M, I, static_cast<cudaStream_t>(stream)));
 }
 
+situ_status situ_ffn_forward_train(const void* x, const void* W_gate_up, const void* W_down,
+                                   void* y, void* gu, void* h, int64_t R, int64_t M,
+                                   int64_t I, float beta, float linear_beta, situ_dtype dt,
+                                   void* stream) {
+  situ_status s = ffn_common_checks(dt, R, M, I, beta, linear_beta);
+  if (s != SITU_OK || R == 0) return s;
+  if (dt != SITU_BF16) return SITU_ERR_UNSUPPORTED;
+  if (!x || !W_gate_up || !W_down || !y || !gu || !h) return SITU_ERR_ARG;
+  if ((s = bf16_gemm_checks(x, W_gate_up, W_down, M, I)) != SITU_OK) return s;
+  if (!aligned16(y) || !aligned16(gu) || !aligned16(h)) return SITU_ERR_ALIGN;
+  const size_t xb = static_cast<size_t>(R) * M * 2, wgb = static_cast<size_t>(2 * I) * M * 2,
+               wdb = static_cast<size_t>(M) * I * 2, gub = static_cast<size_t>(R) * 2 * I * 2,
+               hb = static_cast<size_t>(R) * I * 2;
+  const void* ins[] = {x, W_gate_up, W_down};
+  const size_t inb[] = {xb, wgb, wdb};
+  void* outs[] = {y, gu, h};
+  const size_t outb[] = {xb, gub, hb};
+  for (int o = 0; o < 3; ++o) {
+    for (int i = 0; i < 3; ++i)
+      if (overlap(outs[o], outb[o], ins[i], inb[i])) return SITU_ERR_ALIAS;
+    for (int j = o + 1; j < 3; ++j)
+      if (overlap(outs[o], outb[o], outs[j], outb[j])) return SITU_ERR_ALIAS;
+  }
+  DeviceState* st = nullptr;
+  if ((s = device_state(&st)) != SITU_OK) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  GemmShape g{};
+  g.a = x;
+  g.a_rows = R;
+  g.b = W_gate_up;
+  g.b_rows = 2 * I;
+  g.K = M;
+  g.num_groups = 1;
+  g.b_group_rows = 2 * I;
+  g.b_up_offset = I;
+  g.n_out = I;
+  g.out = h;
+  g.ldo = I;
+  g.out_rows = R;
+  g.gu_store = gu;
+  g.split = I;
+  cudaError_t e = launch_gemm_situ(g, make_situ_params(beta, linear_beta),
+                                   caps_of(beta, linear_beta), st->status, st->num_sms, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return finish(run_down(st, h, W_down, y, R, M, I, cs));
+}
+
+namespace {
+
+struct BackwardLayout {
+  size_t wdT, wguT, dyT, hT, dgu, dguT, xT, total;
+  int64_t Rp;
+};
+
+BackwardLayout backward_layout(int64_t R, int64_t M, int64_t I) {
+  BackwardLayout L{};
+  L.Rp = (R + 7) / 8 * 8;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += round_up(bytes, 256);
+    return at;
+  };
+  L.wdT = take(static_cast<size_t>(I) * M * 2);
+  L.wguT = take(static_cast<size_t>(M) * 2 * I * 2);
+  L.dyT = take(static_cast<size_t>(M) * L.Rp * 2);
+  L.hT = take(static_cast<size_t>(I) * L.Rp * 2);
+  L.dgu = take(static_cast<size_t>(R) * 2 * I * 2);
+  L.dguT = take(static_cast<size_t>(2 * I) * L.Rp * 2);
+  L.xT = take(static_cast<size_t>(M) * L.Rp * 2);
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+size_t situ_ffn_backward_workspace_size(int64_t R, int64_t M, int64_t I, situ_dtype dt) {
+  if (R <= 0 || M <= 0 || I <= 0 || dt != SITU_BF16) return 0;
+  return backward_layout(R, M, I).total;
+}
+
+situ_status situ_ffn_backward(const void* x, const void* W_gate_up, const void* W_down,
+                              const void* gu, const void* h, const void* dy, void* dx,
+                              void* dW_gate_up, void* dW_down, void* workspace,
+                              size_t workspace_bytes, int64_t R, int64_t M, int64_t I,
+                              float beta, float linear_beta, situ_dtype dt, void* stream) {
+  situ_status s = ffn_common_checks(dt, R, M, I, beta, linear_beta);
+  if (s != SITU_OK) return s;
+  if (dt != SITU_BF16) return SITU_ERR_UNSUPPORTED;
+  if (R < 1 || R > 4194240) return R == 0 ? SITU_ERR_ARG : SITU_ERR_UNSUPPORTED;
+  if (!x || !W_gate_up || !W_down || !gu || !h || !dy || !dx || !dW_gate_up || !dW_down)
+    return SITU_ERR_ARG;
+  if (M % 8 || I % 8) return SITU_ERR_UNSUPPORTED;
+  const void* ptrs[] = {x, W_gate_up, W_down, gu, h, dy, dx, dW_gate_up, dW_down};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return SITU_ERR_ALIGN;
+  const BackwardLayout L = backward_layout(R, M, I);
+  if (!workspace || workspace_bytes < L.total || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return SITU_ERR_WORKSPACE;
+  const size_t xb = static_cast<size_t>(R) * M * 2, wgb = static_cast<size_t>(2 * I) * M * 2,
+               wdb = static_cast<size_t>(M) * I * 2, gub = static_cast<size_t>(R) * 2 * I * 2,
+               hb = static_cast<size_t>(R) * I * 2;
+  const void* ins[] = {x, W_gate_up, W_down, gu, h, dy, workspace};
+  const size_t inb[] = {xb, wgb, wdb, gub, hb, xb, L.total};
+  void* outs[] = {dx, dW_gate_up, dW_down};
+  const size_t outb[] = {xb, wgb, wdb};
+  for (int o = 0; o < 3; ++o) {
+    for (int i = 0; i < 7; ++i)
+      if (overlap(outs[o], outb[o], ins[i], inb[i])) return SITU_ERR_ALIAS;
+    for (int j = o + 1; j < 3; ++j)
+      if (overlap(outs[o], outb[o], outs[j], outb[j])) return SITU_ERR_ALIAS;
+  }
+  DeviceState* st = nullptr;
+  if ((s = device_state(&st)) != SITU_OK) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void *wdT = ws + L.wdT, *wguT = ws + L.wguT, *dyT = ws + L.dyT, *hT = ws + L.hT,
+       *dgu = ws + L.dgu, *dguT = ws + L.dguT, *xT = ws + L.xT;
+  const int64_t Rp = L.Rp;
+  cudaError_t e;
+#define SITU_TRY(call)                          \
+  do {                                          \
+    if ((e = (call)) != cudaSuccess) return cuda_fail(e); \
+  } while (0)
+  // dh = dy W_down -> d(g, u) in the epilogue.
+  SITU_TRY(launch_transpose(W_down, M, I, wdT, M, cs));
+  {
+    GemmShape g{};
+    g.a = dy;
+    g.a_rows = R;
+    g.b = wdT;
+    g.b_rows = I;
+    g.K = M;
+    g.num_groups = 1;
+    g.b_group_rows = I;
+    g.n_out = I;
+    g.out = dgu;
+    g.ldo = 2 * I;
+    g.out_rows = R;
+    g.gu_in = gu;
+    g.dgu_out = dgu;
+    g.split = I;
+    SITU_TRY(launch_gemm_situ_bwd(g, make_situ_params(beta, linear_beta),
+                                  caps_of(beta, linear_beta), st->status, st->num_sms, cs));
+  }
+  // dx = dgu W_gate_up.
+  SITU_TRY(launch_transpose(W_gate_up, 2 * I, M, wguT, 2 * I, cs));
+  {
+    GemmShape g{};
+    g.a = dgu;
+    g.a_rows = R;
+    g.b = wguT;
+    g.b_rows = M;
+    g.K = 2 * I;
+    g.num_groups = 1;
+    g.b_group_rows = M;
+    g.n_out = M;
+    g.out = dx;
+    g.ldo = M;
+    g.out_rows = R;
+    SITU_TRY(launch_gemm_plain(g, st->status, st->num_sms, cs));
+  }
+  // Weight gradients: contractions over the rows, operands [features, Rp].
+  SITU_TRY(launch_transpose(dy, R, M, dyT, Rp, cs));
+  SITU_TRY(launch_transpose(h, R, I, hT, Rp, cs));
+  SITU_TRY(launch_transpose(dgu, R, 2 * I, dguT, Rp, cs));
+  SITU_TRY(launch_transpose(x, R, M, xT, Rp, cs));
+  {
+    GemmShape g{};
+    g.a = dyT;
+    g.a_rows = M;
+    g.a_ld = Rp;
+    g.b = hT;
+    g.b_rows = I;
+    g.b_ld = Rp;
+    g.K = Rp;
+    g.num_groups = 1;
+    g.b_group_rows = I;
+    g.n_out = I;
+    g.out = dW_down;
+    g.ldo = I;
+    g.out_rows = M;
+    SITU_TRY(launch_gemm_plain(g, st->status, st->num_sms, cs));
+  }
+  {
+    GemmShape g{};
+    g.a = dguT;
+    g.a_rows = 2 * I;
+    g.a_ld = Rp;
+    g.b = xT;
+    g.b_rows = M;
+    g.b_ld = Rp;
+    g.K = Rp;
+    g.num_groups = 1;
+    g.b_group_rows = M;
+    g.n_out = M;
+    g.out = dW_gate_up;
+    g.ldo = M;
+    g.out_rows = 2 * I;
+    SITU_TRY(launch_gemm_plain(g, st->status, st->num_sms, cs));
+  }
+#undef SITU_TRY
+  return SITU_OK;
+}
+
 size_t situ_moe_index_workspace_size(int64_t n_routes, int32_t E) {
   if (n_routes < 0 || E < 1) return 0;
   return round_up(index_workspace_bytes(n_routes, E), 256);

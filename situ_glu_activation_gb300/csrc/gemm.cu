@@ -56,7 +56,11 @@ constexpr uint64_t kWaitLimitNs = 10ull * 1000 * 1000 * 1000;  // 10 s
 constexpr uint64_t kDrainLimitNs = 100ull * 1000 * 1000;       // 100 ms
 constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
 
-enum class Epi { kSitu, kPlain };
+// Epilogues: kSitu applies SiTU-GLU to (gate, up) accumulator pairs (and can
+// also store the pre-activation pair); kPlain converts to bf16; kSituBwd turns
+// dh accumulators into d(gate, up) through the activation's derivative, reading
+// the saved pre-activation pair.
+enum class Epi { kSitu, kPlain, kSituBwd };
 
 struct Args {
   int32_t num_groups;
@@ -75,6 +79,12 @@ struct Args {
   const int32_t* out_row_index;
   SituParams sp;
   uint32_t* status;
+  // kSitu: optional store of the pre-activation (g, u) as bf16 [rows, 2*split];
+  // kSituBwd: the saved (g, u) to read and d(g, u) to write, same layout.
+  __nv_bfloat16* gu_store;
+  const __nv_bfloat16* gu_in;
+  __nv_bfloat16* dgu_out;
+  int64_t split;
 };
 
 struct SharedCtl {
@@ -412,6 +422,54 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int64_t col0 = static_cast<int64_t>(tc.n_tile) * 128 + c * 32;
           if (valid) store_row_chunk(dst_row + col0, w, col0, args.n_out);
+          if (args.gu_store != nullptr && valid) {
+            // Pre-activation (g, u) for the backward pass, bf16.
+            uint32_t wg[16], wu[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              wg[i] = pack_bf16x2(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
+              wu[i] = pack_bf16x2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
+            }
+            __nv_bfloat16* gu_row = args.gu_store + out_row * 2 * args.split;
+            store_row_chunk(gu_row + col0, wg, col0, args.n_out);
+            store_row_chunk(gu_row + args.split + col0, wu, col0, args.n_out);
+          }
+        }
+      } else if (kEpi == Epi::kSituBwd) {
+        const __nv_bfloat16* gu_row = args.gu_in + static_cast<int64_t>(row) * 2 * args.split;
+        __nv_bfloat16* dgu_row = args.dgu_out + static_cast<int64_t>(row) * 2 * args.split;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          __syncwarp();
+          uint32_t a[32];
+          tmem_ld32(t_acc + c * 32, a);
+          tmem_ld_wait(a);
+          const int64_t col0 = static_cast<int64_t>(tc.n_tile) * kBN + c * 32;
+          if (!valid) continue;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int64_t cv = col0 + 8 * v;
+            if (cv + 8 > args.n_out) continue;
+            const uint4 gv = *reinterpret_cast<const uint4*>(gu_row + cv);
+            const uint4 uv = *reinterpret_cast<const uint4*>(gu_row + args.split + cv);
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+            const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+            uint32_t og[4], ou[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float pg0, pu0, pg1, pu1;
+              situ_act_grad<kC>(__uint_as_float(gw[i] << 16), __uint_as_float(uw[i] << 16),
+                                args.sp, pg0, pu0);
+              situ_act_grad<kC>(__uint_as_float(gw[i] & 0xFFFF0000u),
+                                __uint_as_float(uw[i] & 0xFFFF0000u), args.sp, pg1, pu1);
+              const float dh0 = __uint_as_float(a[8 * v + 2 * i]);
+              const float dh1 = __uint_as_float(a[8 * v + 2 * i + 1]);
+              og[i] = pack_bf16x2(dh0 * pg0, dh1 * pg1);
+              ou[i] = pack_bf16x2(dh0 * pu0, dh1 * pu1);
+            }
+            st_global_v4(dgu_row + cv, og[0], og[1], og[2], og[3]);
+            st_global_v4(dgu_row + args.split + cv, ou[0], ou[1], ou[2], ou[3]);
+          }
         }
       } else {
         __nv_bfloat16* dst_row = args.out + out_row * args.ldo;
@@ -561,11 +619,11 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 // 2-D bf16 map over a row-major [rows, cols] matrix, 64 x box_rows boxes, 128-byte
 // swizzle (the layout sw128_kmajor_desc describes), zero fill out of bounds.
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
-              uint32_t box_rows = 128) {
+              uint32_t box_rows = 128, int64_t ld = 0) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld > 0 ? ld : cols) * 2};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
@@ -612,8 +670,9 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
                    cudaStream_t stream) {
   if (s.a_rows == 0 && !s.tile_offsets) return cudaSuccess;
   CUtensorMap ma, ma64, mb;
-  if (!make_map(&ma, s.a, s.a_rows, s.K) || !make_map(&ma64, s.a, s.a_rows, s.K, 64) ||
-      !make_map(&mb, s.b, s.b_rows, s.K))
+  if (!make_map(&ma, s.a, s.a_rows, s.K, 128, s.a_ld) ||
+      !make_map(&ma64, s.a, s.a_rows, s.K, 64, s.a_ld) ||
+      !make_map(&mb, s.b, s.b_rows, s.K, 128, s.b_ld))
     return cudaErrorInvalidValue;
   Args a;
   a.num_groups = s.num_groups;
@@ -633,6 +692,10 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
   a.out_row_index = s.out_row_index;
   a.sp = p;
   a.status = status;
+  a.gu_store = static_cast<__nv_bfloat16*>(s.gu_store);
+  a.gu_in = static_cast<const __nv_bfloat16*>(s.gu_in);
+  a.dgu_out = static_cast<__nv_bfloat16*>(s.dgu_out);
+  a.split = s.split;
   for (auto fn : {ffn_gemm_kernel<kEpi, kC, false>, ffn_gemm_kernel<kEpi, kC, true>}) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
@@ -687,6 +750,19 @@ cudaError_t launch_gemm_situ(const GemmShape& s, const SituParams& p, Caps caps,
 cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
                               cudaStream_t stream) {
   return launch<Epi::kPlain, Caps::kBoth>(s, SituParams{}, status, num_sms, stream);
+}
+
+cudaError_t launch_gemm_situ_bwd(const GemmShape& s, const SituParams& p, Caps caps,
+                                 uint32_t* status, int num_sms, cudaStream_t stream) {
+  switch (caps) {
+    case Caps::kBoth: return launch<Epi::kSituBwd, Caps::kBoth>(s, p, status, num_sms, stream);
+    case Caps::kGateOnly:
+      return launch<Epi::kSituBwd, Caps::kGateOnly>(s, p, status, num_sms, stream);
+    case Caps::kUpOnly:
+      return launch<Epi::kSituBwd, Caps::kUpOnly>(s, p, status, num_sms, stream);
+    case Caps::kNone: return launch<Epi::kSituBwd, Caps::kNone>(s, p, status, num_sms, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,

@@ -61,6 +61,15 @@ struct GemmShape {
   int64_t ldo;
   int64_t out_rows;
   const int32_t* out_row_index;
+  // Row strides (elements) of A and B when they differ from K (0 = K).
+  int64_t a_ld;
+  int64_t b_ld;
+  // SiTU epilogue: optional bf16 store of the pre-activation (g, u), [rows, 2*split].
+  void* gu_store;
+  // Backward epilogue: saved (g, u) in, d(g, u) out, both [rows, 2*split] bf16.
+  const void* gu_in;
+  void* dgu_out;
+  int64_t split;
 };
 
 // gu = A B^T with the SiTU-GLU epilogue: output column j of group tile n pairs B
@@ -70,6 +79,13 @@ cudaError_t launch_gemm_situ(const GemmShape& s, const SituParams& p, Caps caps,
 // C = A B^T, bf16 output.
 cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
                               cudaStream_t stream);
+// dh = A B^T (B 256-wide tiles like the plain GEMM), epilogue: d(g, u) = dh * the
+// activation's partial derivatives at the saved (g, u).
+cudaError_t launch_gemm_situ_bwd(const GemmShape& s, const SituParams& p, Caps caps,
+                                 uint32_t* status, int num_sms, cudaStream_t stream);
+// out[c, r] = in[r, c] for r < rows, 0 for rows <= r < ld_out; bf16, cols % 8 == 0.
+cudaError_t launch_transpose(const void* in, int64_t rows, int64_t cols, void* out,
+                             int64_t ld_out, cudaStream_t stream);
 // Per-group prefixes of m-tiles and of paired units of the gate_up (n_out_gate_up =
 // I output columns) and down (n_out_down = M) GEMMs, plus validation of the offsets.
 cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,

@@ -178,6 +178,55 @@ __device__ __forceinline__ float situ_act_accurate(float g, float u, const SituP
   return situ_combine<kC>(g, u, t1, t2, sigmoid_x2p64_accurate(g), p);
 }
 
+// tanh(x) and sech^2(x) = 1 - tanh^2(x) without cancellation:
+// e = exp(-2|x|), tanh = sign(x) (1 - e)/(1 + e), sech^2 = 4 e / (1 + e)^2.
+__device__ __forceinline__ void tanh_sech2(float x, float& t, float& sech2) {
+  const float x2 = 2.0f * fabsf(x);
+  const float e = ex2_approx(-x2 * kLog2e);
+  const float r = rcp_approx(1.0f + e);
+  const float tm = one_minus_exp_neg(x2, e) * r;
+  t = __uint_as_float(__float_as_uint(tm) | (__float_as_uint(x) & 0x80000000u));
+  sech2 = 4.0f * e * r * r;
+}
+
+// Partial derivatives of one output h = a(g) b(u) for the backward pass:
+//   dh/dg = b(u) a'(g),  a'(g) = sech^2(g/b1) sigmoid(g) + b1 tanh(g/b1) sigmoid(g) sigmoid(-g)
+//   dh/du = a(g) b'(u),  b'(u) = sech^2(u/b2)
+// (uncapped: a = g sigmoid(g), a' = sigmoid(g) + g sigmoid(g) sigmoid(-g); b = u, b' = 1).
+// sigmoid(g) and sigmoid(-g) come from one e^{-|g|} as 1/(1+e) and e/(1+e).
+template <Caps kC>
+__device__ __forceinline__ void situ_act_grad(float g, float u, const SituParams& p, float& pg,
+                                              float& pu) {
+  const float e0 = ex2_approx(-fabsf(g) * kLog2e);
+  const float r0 = rcp_approx(1.0f + e0);
+  const float s_hi = r0, s_lo = e0 * r0;  // sigmoid(|g|), sigmoid(-|g|)
+  const bool gpos = g >= 0.0f;
+  const float sg = gpos ? s_hi : s_lo;    // sigmoid(g)
+  const float sgm = gpos ? s_lo : s_hi;   // sigmoid(-g)
+  float a, da;
+  if constexpr (kC == Caps::kBoth || kC == Caps::kGateOnly) {
+    float t, sech2;
+    tanh_sech2(g * p.inv_b1, t, sech2);
+    a = p.b1 * t * sg;
+    da = sech2 * sg + p.b1 * t * sg * sgm;
+  } else {
+    a = g * sg;
+    da = sg + g * sg * sgm;
+  }
+  float b, db;
+  if constexpr (kC == Caps::kBoth || kC == Caps::kUpOnly) {
+    float t, sech2;
+    tanh_sech2(u * p.inv_b2, t, sech2);
+    b = p.b2 * t;
+    db = sech2;
+  } else {
+    b = u;
+    db = 1.0f;
+  }
+  pg = b * da;
+  pu = a * db;
+}
+
 // SiTU-GLU with both caps (the hot path).
 __device__ __forceinline__ float situ_glu_f32(float g, float u, const SituParams& p) {
   return situ_act<Caps::kBoth>(g, u, p);

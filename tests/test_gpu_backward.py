@@ -1,0 +1,103 @@
+"""Training pair of the dense FFN on the GPU (forward that keeps the
+pre-activation, and the backward) against the FP64 oracle.
+
+Tolerance, derived from the arithmetic (no tolerance is stated for the
+backward).  Like an autograd pass in bf16, the GPU keeps gu, h and dgu in bf16:
+each stored factor carries a relative rounding of 2^-9, and dgu is evaluated at
+the rounded gu.  A gradient entry is a sum of products (over the rows for the
+weight gradients, over 2I for dx) that can cancel to far below its terms, so the
+bound is the FFN tolerance plus 2^-8 times the sum of the absolute terms:
+    |err| <= 2e-2 (1 + |ref|) + 2^-8 sum_i |term_i|
+(measured worst case: about 2^-11 of the absolute sum)."""
+import numpy as np
+import pytest
+import torch
+
+import situ_glu_activation_gb300 as situ
+from situ_glu_activation_gb300 import workloads as wl
+from numerics import assert_ffn_close, oracle_input, to_f64
+
+pytestmark = pytest.mark.gpu
+INF = float("inf")
+
+
+def _close(got, ref, abs_terms, what):
+    err = np.abs(to_f64(got) - ref)
+    tol = 2e-2 * (1.0 + np.abs(ref)) + 2.0 ** -8 * abs_terms
+    assert np.isfinite(to_f64(got)).all(), what
+    assert (err <= tol).all(), f"{what}: worst err/tol {float((err / tol).max()):.3g}"
+
+
+def _check_backward(oracle, x, wgu, wd, dy, dx, dwg, dwd, caps=(4.0, 25.0), what=""):
+    rdx, rdwg, rdwd, rdgu = oracle.ffn_backward(oracle_input(x), oracle_input(wgu),
+                                               oracle_input(wd), oracle_input(dy), *caps,
+                                               want_dgu=True)
+    _, rh = oracle.ffn_forward(oracle_input(x), oracle_input(wgu), oracle_input(wd), *caps,
+                               want_h=True)
+    ax, awg, awd, ady = (np.abs(to_f64(t)) for t in (x, wgu, wd, dy))
+    _close(dx, rdx, np.abs(rdgu) @ awg, f"dx {what}")
+    _close(dwg, rdwg, np.abs(rdgu).T @ ax, f"dW_gate_up {what}")
+    _close(dwd, rdwd, ady.T @ np.abs(rh), f"dW_down {what}")
+
+
+def _inputs(R, M, I, seed, dev):
+    x, wgu, wd = wl.ffn_inputs(M, I, R, seed=seed)
+    dy = wl.normal((R, M), 1.0, seed=seed + 7)
+    return x, wgu, wd, dy, [t.to(dev) for t in (x, wgu, wd, dy)]
+
+
+def test_forward_train_matches_forward(oracle, cuda_dev):
+    R, M, I = 300, 512, 384
+    x, wgu, wd, _, (xd, wgud, wdd, _) = _inputs(R, M, I, 1, cuda_dev)
+    y, gu, h = situ.situ_ffn_forward_train(xd, wgud, wdd)
+    ws = torch.empty(situ.ffn_workspace_bytes(R, M, I), dtype=torch.uint8, device=cuda_dev)
+    y2 = situ.situ_ffn_forward(xd, wgud, wdd, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    h2 = ws[: R * I * 2].view(torch.bfloat16).view(R, I)
+    assert torch.equal(h.view(torch.int16), h2.view(torch.int16))
+    gu_ref = to_f64(x) @ to_f64(wgu).T  # library matmul of the exact bf16 values
+    assert_ffn_close(to_f64(gu), gu_ref, "saved pre-activation", tol=2 ** -8)
+
+
+@pytest.mark.parametrize("R,M,I", [(300, 512, 384), (77, 136, 200), (1, 128, 256),
+                                   (260, 1024, 520), (129, 256, 128)])
+def test_backward_small(oracle, cuda_dev, R, M, I):
+    x, wgu, wd, dy, (xd, wgud, wdd, dyd) = _inputs(R, M, I, R + M, cuda_dev)
+    _, gu, h = situ.situ_ffn_forward_train(xd, wgud, wdd)
+    dx, dwg, dwd = situ.situ_ffn_backward(xd, wgud, wdd, gu, h, dyd)
+    torch.cuda.synchronize()
+    _check_backward(oracle, x, wgu, wd, dy, dx, dwg, dwd, what=f"{R}x{M}x{I}")
+
+
+@pytest.mark.parametrize("caps", [(INF, INF), (4.0, INF)], ids=["swiglu", "up_uncapped"])
+def test_backward_variants(oracle, cuda_dev, caps):
+    R, M, I = 200, 256, 256
+    x, wgu, wd, dy, (xd, wgud, wdd, dyd) = _inputs(R, M, I, 5, cuda_dev)
+    _, gu, h = situ.situ_ffn_forward_train(xd, wgud, wdd, *caps)
+    dx, dwg, dwd = situ.situ_ffn_backward(xd, wgud, wdd, gu, h, dyd, *caps)
+    torch.cuda.synchronize()
+    oc = tuple(0.0 if c == INF else c for c in caps)
+    _check_backward(oracle, x, wgu, wd, dy, dx, dwg, dwd, caps=oc, what=str(caps))
+
+
+def test_backward_full_size_sparse_dy(oracle, cuda_dev):
+    """The 16384-token workload (M=2048, I=3072) at full size, with dy nonzero on 16
+    seeded rows only: every other row contributes exactly zero, so the oracle's
+    backward over those 16 rows gives the full dW_gate_up and dW_down, and dx must
+    be zero elsewhere."""
+    w = wl.WORKLOADS["dense"]
+    x, wgu, wd = wl.ffn_inputs(w.M, w.I, w.rows, seed=0, device=cuda_dev)
+    g = torch.Generator().manual_seed(17)
+    rows = torch.cat([torch.tensor([0, w.rows - 1]), torch.randperm(w.rows - 2, generator=g)[:14] + 1])
+    dy = torch.zeros(w.rows, w.M, dtype=torch.bfloat16, device=cuda_dev)
+    dy[rows.to(cuda_dev)] = wl.normal((16, w.M), 1.0, seed=9).to(cuda_dev)
+    _, gu, h = situ.situ_ffn_forward_train(x, wgu, wd)
+    dx, dwg, dwd = situ.situ_ffn_backward(x, wgu, wd, gu, h, dy)
+    torch.cuda.synchronize()
+    rd = rows.to(cuda_dev)
+    mask = torch.ones(w.rows, dtype=torch.bool, device=cuda_dev)
+    mask[rd] = False
+    assert int((dx[mask] != 0).sum()) == 0
+    _check_backward(oracle, x[rd].cpu(), wgu.cpu(), wd.cpu(), dy[rd].cpu(), dx[rd], dwg, dwd,
+                    what="full size, 16 rows of dy")
