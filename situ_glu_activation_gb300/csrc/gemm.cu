@@ -55,6 +55,10 @@ constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint64_t kWaitLimitNs = 10ull * 1000 * 1000 * 1000;  // 10 s
 constexpr uint64_t kDrainLimitNs = 100ull * 1000 * 1000;       // 100 ms
 constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
+// Tiles with at most 64 valid rows (an expert's tail, a small group) issue M=64
+// MMAs: half the tensor work.  Their accumulator rows 16q..16q+15 sit in TMEM lanes
+// 32q..32q+15 (the first 16 lanes of each warp's quarter), measured on GB300.
+constexpr uint32_t kIdescHalf = idesc_bf16_f32(64, kBN);
 
 // Epilogues: kSitu applies SiTU-GLU to (gate, up) accumulator pairs (and can
 // also store the pre-activation pair); kPlain converts to bf16; kSituBwd turns
@@ -348,6 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kBN;
+        const TileCoord tcm = unit_tile<kPair>(args, t, rank);
+        const uint32_t idesc = tcm.row_end - tcm.a_row0 <= 64 ? kIdescHalf : kIdesc;
         for (int32_t kb = 0; kb < args.k_blocks; ++kb) {
           if (!ctl_wait(ctl, &ctl->full[stage], phase, args.status)) {
             ok = false;
@@ -359,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kBK / kUK; ++k) {
             umma_bf16(d_tmem, sw128_kmajor_desc(sa + k * kUK * 2),
-                      sw128_kmajor_desc(sb + k * kUK * 2), kIdesc, (kb | k) != 0 ? 1u : 0u);
+                      sw128_kmajor_desc(sb + k * kUK * 2), idesc, (kb | k) != 0 ? 1u : 0u);
           }
           if (kPair) {
             umma_commit_multicast(smem_u32(&ctl->empty[stage]), 0x3);
@@ -395,8 +401,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after_sync();
       const TileCoord tc = unit_tile<kPair>(args, t, rank);
-      const int32_t row = tc.a_row0 + row_in_tile;
-      bool valid = row < tc.row_end;
+      // M=64 tiles: only the first 16 lanes of each quarter hold rows (16q + lane).
+      const bool half = tc.row_end - tc.a_row0 <= 64;
+      const int32_t row = tc.a_row0 + (half ? quarter * 16 + lane : row_in_tile);
+      bool valid = row < tc.row_end && (!half || lane < 16);
       int64_t out_row = row;
       if (valid && args.out_row_index) {
         out_row = __ldg(args.out_row_index + row);
