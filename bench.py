@@ -192,9 +192,10 @@ def timed_steps(step, K: int, W: int, flush, world: int, inner: int = 0):
     barrier(world)
     torch.cuda.synchronize()
     per_step, segs = [], [[] for _ in range(inner + 1)]
-    for _ in range(K):
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(inner + 2)] for _ in range(K)]
+    for i in range(K):
+        ev = events[i]
         flush()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(inner + 2)]
         ev[0].record()
         step(ev[1:-1] if inner else None)
         ev[-1].record()
@@ -285,9 +286,12 @@ def bench_act(args, dev, peaks, world, flush):
                            args.warmup, flush, world)
     nbytes = 3 * w.rows * w.I * 2  # read 2I, write I per row, bf16
     gbs = nbytes / (ms * 1e-3) / 1e9
+    digest = source_digest("act.cu", "situ_math.cuh")
     return {"workload": w.name, "ms": ms, "bytes": nbytes, "gbs": gbs, "swiglu_ms": mean(sw_ms),
-            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}}
+            "roofline": {"bound": "hbm", "kernel": "act_bf16_vec_kernel", "achieved": gbs,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"],
+                         "traffic": profiled_traffic("situ_act", digest, w.rows * w.I)}}
 
 
 def bench_moe(args, dev, peaks, world, flush, names):

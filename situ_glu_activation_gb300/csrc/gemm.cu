@@ -231,7 +231,7 @@ __device__ __forceinline__ void store_row_chunk(__nv_bfloat16* dst, const uint32
   }
 }
 
-template <Epi kEpi, Caps kC, bool kPair>
+template <Epi kEpi, Caps kC, bool kPair, bool kStoreGu>
 __global__ void __launch_bounds__(kThreads, 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_a64,
@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const int64_t col0 = static_cast<int64_t>(tc.n_tile) * 128 + c * 32;
           if (valid) store_row_chunk(dst_row + col0, w, col0, args.n_out);
-          if (args.gu_store != nullptr && valid) {
+          if (kStoreGu && valid) {
             // Pre-activation (g, u) for the backward pass, bf16.
             uint32_t wg[16], wu[16];
 #pragma unroll
@@ -643,9 +643,9 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
 
 constexpr size_t kSmemBytes = kStages * kStageBytes + sizeof(SharedCtl) + 1024;
 
-// Most 2-CTA clusters of ffn_gemm_kernel<kEpi, kC, true> resident at once, per
-// device (0 if the query fails: the unpaired kernel is used then).
-template <Epi kEpi, Caps kC>
+// Most 2-CTA clusters of ffn_gemm_kernel<kEpi, kC, true, kStoreGu> resident at
+// once, per device (0 if the query fails: the unpaired kernel is used then).
+template <Epi kEpi, Caps kC, bool kStoreGu>
 int max_pair_clusters(size_t smem) {
   static int cached[64] = {};
   static bool done[64] = {};
@@ -665,7 +665,8 @@ int max_pair_clusters(size_t smem) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, ffn_gemm_kernel<kEpi, kC, true>, &cfg) == cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&n, ffn_gemm_kernel<kEpi, kC, true, kStoreGu>, &cfg) ==
+        cudaSuccess)
       cached[dev] = n;
     else
       (void)cudaGetLastError();
@@ -673,7 +674,7 @@ int max_pair_clusters(size_t smem) {
   return cached[dev];
 }
 
-template <Epi kEpi, Caps kC>
+template <Epi kEpi, Caps kC, bool kStoreGu = false>
 cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, int num_sms,
                    cudaStream_t stream) {
   if (s.a_rows == 0 && !s.tile_offsets) return cudaSuccess;
@@ -704,12 +705,20 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
   a.gu_in = static_cast<const __nv_bfloat16*>(s.gu_in);
   a.dgu_out = static_cast<__nv_bfloat16*>(s.dgu_out);
   a.split = s.split;
-  for (auto fn : {ffn_gemm_kernel<kEpi, kC, false>, ffn_gemm_kernel<kEpi, kC, true>}) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
+  // The shared-memory opt-in is a per-device property of each kernel: set once.
+  static bool smem_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!smem_set[dev]) {
+    for (auto fn : {ffn_gemm_kernel<kEpi, kC, false, kStoreGu>,
+                    ffn_gemm_kernel<kEpi, kC, true, kStoreGu>}) {
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kSmemBytes));
+      if (e != cudaSuccess) return e;
+    }
+    smem_set[dev] = true;
   }
-  int clusters = max_pair_clusters<kEpi, kC>(kSmemBytes);
+  int clusters = max_pair_clusters<kEpi, kC, kStoreGu>(kSmemBytes);
   if (clusters > 0 && (!s.tile_offsets || s.unit_offsets)) {
     // Clusters of two CTAs sharing a B or an A tile by multicast.
     a.unit_offsets = s.unit_offsets;
@@ -730,14 +739,15 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, kC, true>, ma, ma64, mb, a);
+    return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, kC, true, kStoreGu>, ma, ma64, mb, a);
   }
   int grid = num_sms;
   if (!s.tile_offsets) {
     const int64_t tiles = ((s.a_rows + kBM - 1) / kBM) * a.n_tiles;
     if (tiles < grid) grid = static_cast<int>(tiles);
   }
-  ffn_gemm_kernel<kEpi, kC, false><<<grid, kThreads, kSmemBytes, stream>>>(ma, ma64, mb, a);
+  ffn_gemm_kernel<kEpi, kC, false, kStoreGu><<<grid, kThreads, kSmemBytes, stream>>>(ma, ma64,
+                                                                                      mb, a);
   return cudaGetLastError();
 }
 
@@ -745,6 +755,21 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
 
 cudaError_t launch_gemm_situ(const GemmShape& s, const SituParams& p, Caps caps,
                              uint32_t* status, int num_sms, cudaStream_t stream) {
+  // Storing the pre-activation (training forward) is a separate instantiation,
+  // so the inference epilogue carries none of it.
+  if (s.gu_store) {
+    switch (caps) {
+      case Caps::kBoth:
+        return launch<Epi::kSitu, Caps::kBoth, true>(s, p, status, num_sms, stream);
+      case Caps::kGateOnly:
+        return launch<Epi::kSitu, Caps::kGateOnly, true>(s, p, status, num_sms, stream);
+      case Caps::kUpOnly:
+        return launch<Epi::kSitu, Caps::kUpOnly, true>(s, p, status, num_sms, stream);
+      case Caps::kNone:
+        return launch<Epi::kSitu, Caps::kNone, true>(s, p, status, num_sms, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (caps) {
     case Caps::kBoth: return launch<Epi::kSitu, Caps::kBoth>(s, p, status, num_sms, stream);
     case Caps::kGateOnly:
