@@ -389,7 +389,7 @@ def bench_train(args, dev, peaks, world, flush):
             "tflops": (flop_f + flop_b) / (ms * 1e-3) / 1e12,
             "backward_tflops": flop_b / (mean(t_bwd) * 1e-3) / 1e12,
             "tc_frac": (flop_f + flop_b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
-            "launches_per_step": 2 + 10}
+            "launches_per_step": 2 + 4}
 
 
 def cpu_baseline(seconds: float, rows_hint: int = 0):

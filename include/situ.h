@@ -189,17 +189,17 @@ situ_status situ_ffn_down(const void* h, const void* W_down, void* y, int64_t R,
  *   dW_down    = dy^T h                                [M, I]
  *   dW_gate_up = dgu^T x                               [2I, M]
  * evaluated at the saved bf16 gu.  Caps as everywhere (+inf = uncapped).
- * The activation derivative runs in the epilogue of the dy W_down GEMM; the
- * weight gradients contract over the R rows after a re-layout of the operands
- * in the workspace.
+ * The activation derivative runs in the epilogue of the dy W_down GEMM (dgu
+ * lives in the workspace); every GEMM reads its operands in their stored layout
+ * (the weights and the row-contracted operands as MN-major tiles), so nothing is
+ * transposed.
  *
  *   all tensors device, bf16, row-major; gu and h as written by
  *   situ_ffn_forward_train.  dx, dW_gate_up, dW_down are written and must not
  *   overlap the inputs or the workspace.
  *   workspace  >= situ_ffn_backward_workspace_size(R, M, I, dt) bytes, 256-byte
  *              aligned.
- *   bf16 only; M % 8 == 0, I % 8 == 0, 1 <= R <= 4194240, 16-byte aligned
- *   pointers.
+ *   bf16 only; M % 8 == 0, I % 8 == 0, R >= 1, 16-byte aligned pointers.
  * Errors: SITU_ERR_ARG, SITU_ERR_ALIGN, SITU_ERR_ALIAS, SITU_ERR_WORKSPACE,
  *         SITU_ERR_UNSUPPORTED, SITU_ERR_CUDA; SITU_ERR_TIMEOUT on the device.
  * ------------------------------------------------------------------------- */

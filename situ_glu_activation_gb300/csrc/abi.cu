@@ -327,38 +327,10 @@ situ_status situ_ffn_forward_train(const void* x, const void* W_gate_up, const v
   return finish(run_down(st, h, W_down, y, R, M, I, cs));
 }
 
-namespace {
-
-struct BackwardLayout {
-  size_t wdT, wguT, dyT, hT, dgu, dguT, xT, total;
-  int64_t Rp;
-};
-
-BackwardLayout backward_layout(int64_t R, int64_t M, int64_t I) {
-  BackwardLayout L{};
-  L.Rp = (R + 7) / 8 * 8;
-  size_t off = 0;
-  auto take = [&](size_t bytes) {
-    const size_t at = off;
-    off += round_up(bytes, 256);
-    return at;
-  };
-  L.wdT = take(static_cast<size_t>(I) * M * 2);
-  L.wguT = take(static_cast<size_t>(M) * 2 * I * 2);
-  L.dyT = take(static_cast<size_t>(M) * L.Rp * 2);
-  L.hT = take(static_cast<size_t>(I) * L.Rp * 2);
-  L.dgu = take(static_cast<size_t>(R) * 2 * I * 2);
-  L.dguT = take(static_cast<size_t>(2 * I) * L.Rp * 2);
-  L.xT = take(static_cast<size_t>(M) * L.Rp * 2);
-  L.total = off;
-  return L;
-}
-
-}  // namespace
-
 size_t situ_ffn_backward_workspace_size(int64_t R, int64_t M, int64_t I, situ_dtype dt) {
-  if (R <= 0 || M <= 0 || I <= 0 || dt != SITU_BF16) return 0;
-  return backward_layout(R, M, I).total;
+  (void)M;
+  if (R <= 0 || I <= 0 || dt != SITU_BF16) return 0;
+  return round_up(static_cast<size_t>(R) * 2 * I * 2, 256);  // dgu [R, 2I]
 }
 
 situ_status situ_ffn_backward(const void* x, const void* W_gate_up, const void* W_down,
@@ -369,21 +341,21 @@ situ_status situ_ffn_backward(const void* x, const void* W_gate_up, const void* 
   situ_status s = ffn_common_checks(dt, R, M, I, beta, linear_beta);
   if (s != SITU_OK) return s;
   if (dt != SITU_BF16) return SITU_ERR_UNSUPPORTED;
-  if (R < 1 || R > 4194240) return R == 0 ? SITU_ERR_ARG : SITU_ERR_UNSUPPORTED;
+  if (R < 1) return SITU_ERR_ARG;
   if (!x || !W_gate_up || !W_down || !gu || !h || !dy || !dx || !dW_gate_up || !dW_down)
     return SITU_ERR_ARG;
   if (M % 8 || I % 8) return SITU_ERR_UNSUPPORTED;
   const void* ptrs[] = {x, W_gate_up, W_down, gu, h, dy, dx, dW_gate_up, dW_down};
   for (const void* q : ptrs)
     if (!aligned16(q)) return SITU_ERR_ALIGN;
-  const BackwardLayout L = backward_layout(R, M, I);
-  if (!workspace || workspace_bytes < L.total || reinterpret_cast<uintptr_t>(workspace) % 256)
+  const size_t need = situ_ffn_backward_workspace_size(R, M, I, dt);
+  if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
     return SITU_ERR_WORKSPACE;
   const size_t xb = static_cast<size_t>(R) * M * 2, wgb = static_cast<size_t>(2 * I) * M * 2,
                wdb = static_cast<size_t>(M) * I * 2, gub = static_cast<size_t>(R) * 2 * I * 2,
                hb = static_cast<size_t>(R) * I * 2;
   const void* ins[] = {x, W_gate_up, W_down, gu, h, dy, workspace};
-  const size_t inb[] = {xb, wgb, wdb, gub, hb, xb, L.total};
+  const size_t inb[] = {xb, wgb, wdb, gub, hb, xb, need};
   void* outs[] = {dx, dW_gate_up, dW_down};
   const size_t outb[] = {xb, wgb, wdb};
   for (int o = 0; o < 3; ++o) {
@@ -395,26 +367,19 @@ situ_status situ_ffn_backward(const void* x, const void* W_gate_up, const void* 
   DeviceState* st = nullptr;
   if ((s = device_state(&st)) != SITU_OK) return s;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void *wdT = ws + L.wdT, *wguT = ws + L.wguT, *dyT = ws + L.dyT, *hT = ws + L.hT,
-       *dgu = ws + L.dgu, *dguT = ws + L.dguT, *xT = ws + L.xT;
-  const int64_t Rp = L.Rp;
+  void* dgu = workspace;
   cudaError_t e;
-#define SITU_TRY(call)                          \
-  do {                                          \
-    if ((e = (call)) != cudaSuccess) return cuda_fail(e); \
-  } while (0)
-  // dh = dy W_down -> d(g, u) in the epilogue.
-  SITU_TRY(launch_transpose(W_down, M, I, wdT, M, cs));
+  // dh = dy W_down (W_down [M, I] read as an MN-major [K = M, N = I] operand);
+  // the epilogue turns dh into d(g, u) at the saved gu.
   {
     GemmShape g{};
     g.a = dy;
     g.a_rows = R;
-    g.b = wdT;
+    g.b = W_down;
     g.b_rows = I;
+    g.b_mn_major = true;
     g.K = M;
     g.num_groups = 1;
-    g.b_group_rows = I;
     g.n_out = I;
     g.out = dgu;
     g.ldo = 2 * I;
@@ -422,66 +387,63 @@ situ_status situ_ffn_backward(const void* x, const void* W_gate_up, const void* 
     g.gu_in = gu;
     g.dgu_out = dgu;
     g.split = I;
-    SITU_TRY(launch_gemm_situ_bwd(g, make_situ_params(beta, linear_beta),
-                                  caps_of(beta, linear_beta), st->status, st->num_sms, cs));
+    e = launch_gemm_situ_bwd(g, make_situ_params(beta, linear_beta), caps_of(beta, linear_beta),
+                             st->status, st->num_sms, cs);
+    if (e != cudaSuccess) return cuda_fail(e);
   }
-  // dx = dgu W_gate_up.
-  SITU_TRY(launch_transpose(W_gate_up, 2 * I, M, wguT, 2 * I, cs));
+  // dx = dgu W_gate_up (W_gate_up [2I, M] read as MN-major [K = 2I, N = M]).
   {
     GemmShape g{};
     g.a = dgu;
     g.a_rows = R;
-    g.b = wguT;
+    g.b = W_gate_up;
     g.b_rows = M;
+    g.b_mn_major = true;
     g.K = 2 * I;
     g.num_groups = 1;
-    g.b_group_rows = M;
     g.n_out = M;
     g.out = dx;
     g.ldo = M;
     g.out_rows = R;
-    SITU_TRY(launch_gemm_plain(g, st->status, st->num_sms, cs));
+    if ((e = launch_gemm_plain(g, st->status, st->num_sms, cs)) != cudaSuccess)
+      return cuda_fail(e);
   }
-  // Weight gradients: contractions over the rows, operands [features, Rp].
-  SITU_TRY(launch_transpose(dy, R, M, dyT, Rp, cs));
-  SITU_TRY(launch_transpose(h, R, I, hT, Rp, cs));
-  SITU_TRY(launch_transpose(dgu, R, 2 * I, dguT, Rp, cs));
-  SITU_TRY(launch_transpose(x, R, M, xT, Rp, cs));
+  // dW_down = dy^T h: both operands read MN-major, contracting over the R rows.
   {
     GemmShape g{};
-    g.a = dyT;
+    g.a = dy;
     g.a_rows = M;
-    g.a_ld = Rp;
-    g.b = hT;
+    g.a_mn_major = true;
+    g.b = h;
     g.b_rows = I;
-    g.b_ld = Rp;
-    g.K = Rp;
+    g.b_mn_major = true;
+    g.K = R;
     g.num_groups = 1;
-    g.b_group_rows = I;
     g.n_out = I;
     g.out = dW_down;
     g.ldo = I;
     g.out_rows = M;
-    SITU_TRY(launch_gemm_plain(g, st->status, st->num_sms, cs));
+    if ((e = launch_gemm_plain(g, st->status, st->num_sms, cs)) != cudaSuccess)
+      return cuda_fail(e);
   }
+  // dW_gate_up = dgu^T x.
   {
     GemmShape g{};
-    g.a = dguT;
+    g.a = dgu;
     g.a_rows = 2 * I;
-    g.a_ld = Rp;
-    g.b = xT;
+    g.a_mn_major = true;
+    g.b = x;
     g.b_rows = M;
-    g.b_ld = Rp;
-    g.K = Rp;
+    g.b_mn_major = true;
+    g.K = R;
     g.num_groups = 1;
-    g.b_group_rows = M;
     g.n_out = M;
     g.out = dW_gate_up;
     g.ldo = M;
     g.out_rows = 2 * I;
-    SITU_TRY(launch_gemm_plain(g, st->status, st->num_sms, cs));
+    if ((e = launch_gemm_plain(g, st->status, st->num_sms, cs)) != cudaSuccess)
+      return cuda_fail(e);
   }
-#undef SITU_TRY
   return SITU_OK;
 }
 

@@ -59,6 +59,14 @@ constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
 // MMAs: half the tensor work.  Their accumulator rows 16q..16q+15 sit in TMEM lanes
 // 32q..32q+15 (the first 16 lanes of each warp's quarter), measured on GB300.
 constexpr uint32_t kIdescHalf = idesc_bf16_f32(64, kBN);
+// Operand layouts: kKMajor -- A [rows, K] and B [N, K] with K contiguous (the
+// forward); kBMN -- B stored [K, N] (N contiguous), e.g. W_down when the
+// backward multiplies by it untransposed; kABMN -- A stored [K, rows] and B
+// stored [K, N], e.g. dy and h when the weight gradient contracts over tokens.
+// MN-major tiles arrive as {64, 64} boxes (8 KB): A takes two, B four.
+enum class Major { kKMajor = 0, kBMN = 1, kABMN = 2 };
+constexpr uint32_t kAMnBit = 1u << 15, kBMnBit = 1u << 16;
+constexpr uint32_t kMnAtomBytes = 64 * 64 * 2;
 
 // Epilogues: kSitu applies SiTU-GLU to (gate, up) accumulator pairs (and can
 // also store the pre-activation pair); kPlain converts to bf16; kSituBwd turns
@@ -231,7 +239,7 @@ __device__ __forceinline__ void store_row_chunk(__nv_bfloat16* dst, const uint32
   }
 }
 
-template <Epi kEpi, Caps kC, bool kPair, bool kStoreGu>
+template <Epi kEpi, Caps kC, bool kPair, bool kStoreGu, Major kMajor>
 __global__ void __launch_bounds__(kThreads, 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_a64,
@@ -304,21 +312,51 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = smem_u32(smem + stage * kStageBytes);
           const uint32_t sb = sa + kABytes;
           mbar_arrive_expect_tx(full, kStageBytes);
+          constexpr bool kAMN = kMajor == Major::kABMN;
+          constexpr bool kBMN = kMajor != Major::kKMajor;
+          const int32_t kx = kb * kBK;
+          // A (128 rows of the tile); `half` picks one 64-row half for a shared-A unit.
+          auto load_a = [&](uint32_t dst, int32_t row, int rows64, bool mcast) {
+            for (int j = 0; j < rows64; ++j) {
+              const uint32_t d = dst + j * (kAMN ? kMnAtomBytes : 0u);
+              if (kAMN) {
+                if (mcast) tma_load_2d_multicast(d, &map_a, row + 64 * j, kx, full, 0x3);
+                else tma_load_2d(d, &map_a, row + 64 * j, kx, full);
+              } else if (rows64 == 2) {
+                tma_load_2d(d, &map_a, kx, row, full);
+                break;
+              } else {
+                if (mcast) tma_load_2d_multicast(d, &map_a64, kx, row, full, 0x3);
+                else tma_load_2d(d, &map_a64, kx, row, full);
+              }
+            }
+          };
+          // B (128 rows = one half of the 256-row tile).
+          auto load_b = [&](uint32_t dst, int32_t row, bool mcast) {
+            if (kBMN) {
+              for (int j = 0; j < 2; ++j) {
+                if (mcast) tma_load_2d_multicast(dst + j * kMnAtomBytes, &map_b, row + 64 * j, kx, full, 0x3);
+                else tma_load_2d(dst + j * kMnAtomBytes, &map_b, row + 64 * j, kx, full);
+              }
+            } else {
+              if (mcast) tma_load_2d_multicast(dst, &map_b, kx, row, full, 0x3);
+              else tma_load_2d(dst, &map_b, kx, row, full);
+            }
+          };
           if (!kPair) {
-            tma_load_2d(sa, &map_a, kb * kBK, tc.a_row0, full);
-            tma_load_2d(sb, &map_b, kb * kBK, b_row0, full);
-            tma_load_2d(sb + kBHalfBytes, &map_b, kb * kBK, b_row1, full);
+            load_a(sa, tc.a_row0, 2, false);
+            load_b(sb, b_row0, false);
+            load_b(sb + kBHalfBytes, b_row1, false);
           } else if (!tc.share_a) {
             // Shared B: this CTA fetches one half of the B tile for both CTAs.
-            tma_load_2d(sa, &map_a, kb * kBK, tc.a_row0, full);
-            tma_load_2d_multicast(sb + rank * kBHalfBytes, &map_b, kb * kBK,
-                                  rank == 0 ? b_row0 : b_row1, full, 0x3);
+            load_a(sa, tc.a_row0, 2, false);
+            load_b(sb + rank * kBHalfBytes, rank == 0 ? b_row0 : b_row1, true);
           } else {
             // Shared A: this CTA fetches 64 of the 128 A rows for both CTAs.
-            tma_load_2d_multicast(sa + rank * (kABytes / 2), &map_a64, kb * kBK,
-                                  tc.a_row0 + static_cast<int32_t>(rank) * 64, full, 0x3);
-            tma_load_2d(sb, &map_b, kb * kBK, b_row0, full);
-            tma_load_2d(sb + kBHalfBytes, &map_b, kb * kBK, b_row1, full);
+            load_a(sa + rank * (kABytes / 2), tc.a_row0 + static_cast<int32_t>(rank) * 64, 1,
+                   true);
+            load_b(sb, b_row0, false);
+            load_b(sb + kBHalfBytes, b_row1, false);
           }
           ++issued;
           if (++stage == kStages) {
@@ -353,7 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kBN;
         const TileCoord tcm = unit_tile<kPair>(args, t, rank);
-        const uint32_t idesc = tcm.row_end - tcm.a_row0 <= 64 ? kIdescHalf : kIdesc;
+        const uint32_t idesc = (tcm.row_end - tcm.a_row0 <= 64 ? kIdescHalf : kIdesc) |
+                               (kMajor == Major::kABMN ? kAMnBit : 0u) |
+                               (kMajor != Major::kKMajor ? kBMnBit : 0u);
         for (int32_t kb = 0; kb < args.k_blocks; ++kb) {
           if (!ctl_wait(ctl, &ctl->full[stage], phase, args.status)) {
             ok = false;
@@ -364,8 +404,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sb = sa + kABytes;
 #pragma unroll
           for (int k = 0; k < kBK / kUK; ++k) {
-            umma_bf16(d_tmem, sw128_kmajor_desc(sa + k * kUK * 2),
-                      sw128_kmajor_desc(sb + k * kUK * 2), idesc, (kb | k) != 0 ? 1u : 0u);
+            // K-major: 16 K elements = 32 bytes along the row; MN-major: 16 K rows
+            // = 2048 bytes.
+            const uint64_t ad = kMajor == Major::kABMN
+                                    ? sw128_mnmajor_desc(sa + k * 2048, kMnAtomBytes)
+                                    : sw128_kmajor_desc(sa + k * kUK * 2);
+            const uint64_t bd = kMajor != Major::kKMajor
+                                    ? sw128_mnmajor_desc(sb + k * 2048, kMnAtomBytes)
+                                    : sw128_kmajor_desc(sb + k * kUK * 2);
+            umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           if (kPair) {
             umma_commit_multicast(smem_u32(&ctl->empty[stage]), 0x3);
@@ -643,9 +690,9 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
 
 constexpr size_t kSmemBytes = kStages * kStageBytes + sizeof(SharedCtl) + 1024;
 
-// Most 2-CTA clusters of ffn_gemm_kernel<kEpi, kC, true, kStoreGu> resident at
-// once, per device (0 if the query fails: the unpaired kernel is used then).
-template <Epi kEpi, Caps kC, bool kStoreGu>
+// Most 2-CTA clusters of ffn_gemm_kernel<kEpi, kC, true, ...> resident at once,
+// per device (0 if the query fails: the unpaired kernel is used then).
+template <Epi kEpi, Caps kC, bool kStoreGu, Major kMajor>
 int max_pair_clusters(size_t smem) {
   static int cached[64] = {};
   static bool done[64] = {};
@@ -665,8 +712,8 @@ int max_pair_clusters(size_t smem) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, ffn_gemm_kernel<kEpi, kC, true, kStoreGu>, &cfg) ==
-        cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&n, ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor>,
+                                       &cfg) == cudaSuccess)
       cached[dev] = n;
     else
       (void)cudaGetLastError();
@@ -674,15 +721,28 @@ int max_pair_clusters(size_t smem) {
   return cached[dev];
 }
 
-template <Epi kEpi, Caps kC, bool kStoreGu = false>
+template <Epi kEpi, Caps kC, bool kStoreGu = false, Major kMajor = Major::kKMajor>
 cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, int num_sms,
                    cudaStream_t stream) {
+  static_assert(kEpi != Epi::kSitu || kMajor == Major::kKMajor,
+                "the SiTU epilogue pairs gate and up rows of a K-major B");
   if (s.a_rows == 0 && !s.tile_offsets) return cudaSuccess;
   CUtensorMap ma, ma64, mb;
-  if (!make_map(&ma, s.a, s.a_rows, s.K, 128, s.a_ld) ||
-      !make_map(&ma64, s.a, s.a_rows, s.K, 64, s.a_ld) ||
-      !make_map(&mb, s.b, s.b_rows, s.K, 128, s.b_ld))
-    return cudaErrorInvalidValue;
+  bool ok;
+  if (kMajor == Major::kABMN) {
+    // A stored [K, rows]: {64 rows, 64 K} boxes.
+    ok = make_map(&ma, s.a, s.K, s.a_rows, 64, s.a_ld);
+    ma64 = ma;
+  } else {
+    ok = make_map(&ma, s.a, s.a_rows, s.K, 128, s.a_ld) &&
+         make_map(&ma64, s.a, s.a_rows, s.K, 64, s.a_ld);
+  }
+  if (kMajor != Major::kKMajor) {
+    ok = ok && make_map(&mb, s.b, s.K, s.b_rows, 64, s.b_ld);  // B stored [K, N]
+  } else {
+    ok = ok && make_map(&mb, s.b, s.b_rows, s.K, 128, s.b_ld);
+  }
+  if (!ok) return cudaErrorInvalidValue;
   Args a;
   a.num_groups = s.num_groups;
   a.group_offsets = s.group_offsets;
@@ -710,15 +770,15 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!smem_set[dev]) {
-    for (auto fn : {ffn_gemm_kernel<kEpi, kC, false, kStoreGu>,
-                    ffn_gemm_kernel<kEpi, kC, true, kStoreGu>}) {
+    for (auto fn : {ffn_gemm_kernel<kEpi, kC, false, kStoreGu, kMajor>,
+                    ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor>}) {
       cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(kSmemBytes));
       if (e != cudaSuccess) return e;
     }
     smem_set[dev] = true;
   }
-  int clusters = max_pair_clusters<kEpi, kC, kStoreGu>(kSmemBytes);
+  int clusters = max_pair_clusters<kEpi, kC, kStoreGu, kMajor>(kSmemBytes);
   if (clusters > 0 && (!s.tile_offsets || s.unit_offsets)) {
     // Clusters of two CTAs sharing a B or an A tile by multicast.
     a.unit_offsets = s.unit_offsets;
@@ -739,15 +799,16 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, kC, true, kStoreGu>, ma, ma64, mb, a);
+    return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor>, ma, ma64,
+                              mb, a);
   }
   int grid = num_sms;
   if (!s.tile_offsets) {
     const int64_t tiles = ((s.a_rows + kBM - 1) / kBM) * a.n_tiles;
     if (tiles < grid) grid = static_cast<int>(tiles);
   }
-  ffn_gemm_kernel<kEpi, kC, false, kStoreGu><<<grid, kThreads, kSmemBytes, stream>>>(ma, ma64,
-                                                                                      mb, a);
+  ffn_gemm_kernel<kEpi, kC, false, kStoreGu, kMajor>
+      <<<grid, kThreads, kSmemBytes, stream>>>(ma, ma64, mb, a);
   return cudaGetLastError();
 }
 
@@ -782,11 +843,34 @@ cudaError_t launch_gemm_situ(const GemmShape& s, const SituParams& p, Caps caps,
 
 cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
                               cudaStream_t stream) {
+  if (s.a_mn_major && s.b_mn_major)
+    return launch<Epi::kPlain, Caps::kBoth, false, Major::kABMN>(s, SituParams{}, status, num_sms,
+                                                                stream);
+  if (s.b_mn_major)
+    return launch<Epi::kPlain, Caps::kBoth, false, Major::kBMN>(s, SituParams{}, status, num_sms,
+                                                               stream);
+  if (s.a_mn_major) return cudaErrorInvalidValue;
   return launch<Epi::kPlain, Caps::kBoth>(s, SituParams{}, status, num_sms, stream);
 }
 
 cudaError_t launch_gemm_situ_bwd(const GemmShape& s, const SituParams& p, Caps caps,
                                  uint32_t* status, int num_sms, cudaStream_t stream) {
+  if (s.a_mn_major) return cudaErrorInvalidValue;
+  if (s.b_mn_major) {
+    switch (caps) {
+      case Caps::kBoth:
+        return launch<Epi::kSituBwd, Caps::kBoth, false, Major::kBMN>(s, p, status, num_sms, stream);
+      case Caps::kGateOnly:
+        return launch<Epi::kSituBwd, Caps::kGateOnly, false, Major::kBMN>(s, p, status, num_sms,
+                                                                         stream);
+      case Caps::kUpOnly:
+        return launch<Epi::kSituBwd, Caps::kUpOnly, false, Major::kBMN>(s, p, status, num_sms,
+                                                                       stream);
+      case Caps::kNone:
+        return launch<Epi::kSituBwd, Caps::kNone, false, Major::kBMN>(s, p, status, num_sms, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (caps) {
     case Caps::kBoth: return launch<Epi::kSituBwd, Caps::kBoth>(s, p, status, num_sms, stream);
     case Caps::kGateOnly:

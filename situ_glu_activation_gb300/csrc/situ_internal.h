@@ -61,9 +61,15 @@ struct GemmShape {
   int64_t ldo;
   int64_t out_rows;
   const int32_t* out_row_index;
-  // Row strides (elements) of A and B when they differ from K (0 = K).
+  // Row strides (elements) of A and B when they differ from K (0 = K), or, for
+  // MN-major operands, from their row / N extent.
   int64_t a_ld;
   int64_t b_ld;
+  // MN-major operands: A stored [K, a_rows], B stored [K, b_rows] (the row / N
+  // index contiguous).  Supported: B alone, or A and B; the SiTU epilogue needs a
+  // K-major B.
+  bool a_mn_major;
+  bool b_mn_major;
   // SiTU epilogue: optional bf16 store of the pre-activation (g, u), [rows, 2*split].
   void* gu_store;
   // Backward epilogue: saved (g, u) in, d(g, u) out, both [rows, 2*split] bf16.
@@ -83,9 +89,7 @@ cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
 // activation's partial derivatives at the saved (g, u).
 cudaError_t launch_gemm_situ_bwd(const GemmShape& s, const SituParams& p, Caps caps,
                                  uint32_t* status, int num_sms, cudaStream_t stream);
-// out[c, r] = in[r, c] for r < rows, 0 for rows <= r < ld_out; bf16, cols % 8 == 0.
-cudaError_t launch_transpose(const void* in, int64_t rows, int64_t cols, void* out,
-                             int64_t ld_out, cudaStream_t stream);
+
 // Per-group prefixes of m-tiles and of paired units of the gate_up (n_out_gate_up =
 // I output columns) and down (n_out_down = M) GEMMs, plus validation of the offsets.
 cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,

@@ -220,6 +220,20 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
          | (static_cast<uint64_t>(2) << 61);             // swizzle: 128 B
 }
 
+// Shared-memory matrix descriptor of an MN-major operand in the 128-byte swizzle
+// layout TMA writes for a {64 (MN, contiguous), 64 (K, rows)} box: each 128-byte
+// row holds 64 MN elements of one k, 8-row K groups are 1024 bytes apart (stride
+// byte offset) and successive 64-element MN atoms `mn_atom_bytes` apart (leading
+// byte offset).  Stepping K by 16 rows adds 2048 bytes to the start address.
+// (Field roles measured on GB300 with an in-bounds probe against a known product.)
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t mn_atom_bytes) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4)
+         | (static_cast<uint64_t>(mn_atom_bytes >> 4) << 16)  // leading byte offset: MN atoms
+         | (static_cast<uint64_t>(1024 >> 4) << 32)           // stride byte offset: 8 K rows
+         | (static_cast<uint64_t>(1) << 46)
+         | (static_cast<uint64_t>(2) << 61);
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives lane
 // (taddr.lane + i), columns taddr.col .. taddr.col + 31.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
