@@ -63,6 +63,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
          [vp, ci, vp, vp, vp, ci, dp, i64, i32, i32, i64, i64, d, d], ci),
         ("oracle_moe_combine", [dp, vp, ci, dp, i64, i32, i64], ci),
         ("oracle_situ_pair_grad", [d, d, d, d, dp, dp], None),
+        ("oracle_moe_grouped_backward", [vp, ci, vp, vp, vp, ci, vp, ci, dp, dp, dp, i64, i32,
+                                         i32, i64, i64, d, d], ci),
         ("oracle_ffn_backward", [vp, ci, vp, vp, ci, vp, ci, dp, dp, dp, dp, i64, i64, i64, d, d],
          ci),
         ("oracle_num_threads", [], ci),
@@ -213,6 +215,28 @@ class Oracle:
                                             float(beta), float(linear_beta)), "ffn_backward")
         out = (dx.reshape(xa.shape), dwg, dwd)
         return out + (dgu,) if want_dgu else out
+
+    def moe_grouped_backward(self, x, expert_ids, w_gate_up, w_down, dy, beta=4.0,
+                             linear_beta=25.0):
+        """Gradients of the grouped experts for dy [T, k_eff, M]:
+        (dx [T, M], dW_gate_up [E, 2I, M], dW_down [E, M, I])."""
+        xa, xdt = _as_input(x)
+        ids = np.ascontiguousarray(expert_ids, dtype=np.int32)
+        wg, wdt = _as_input(w_gate_up)
+        wd, _ = _as_input(w_down)
+        dya, dydt = _as_input(dy)
+        T, M = xa.shape
+        k_eff = ids.shape[1]
+        E, twoI, _ = wg.shape
+        I = twoI // 2
+        dx = np.empty((T, M))
+        dwg = np.empty((E, 2 * I, M))
+        dwd = np.empty((E, M, I))
+        _check(self.lib.oracle_moe_grouped_backward(_ptr(xa), xdt, _ptr(ids), _ptr(wg), _ptr(wd),
+                                                    wdt, _ptr(dya), dydt, _ptr(dx), _ptr(dwg),
+                                                    _ptr(dwd), T, k_eff, E, M, I, float(beta),
+                                                    float(linear_beta)), "moe_grouped_backward")
+        return dx, dwg, dwd
 
     def moe_combine(self, y: np.ndarray, w: np.ndarray) -> np.ndarray:
         """y [T, k_eff, M] (float64), w [T, k_eff] -> out [T, M] = sum_s w[t,s] y[t,s]."""

@@ -360,6 +360,81 @@ int oracle_ffn_backward(const void* x, int x_dt, const void* w_gate_up, const vo
   return bad ? ORACLE_BAD_ARG : ORACLE_OK;
 }
 
+/* Backward of the grouped experts, for upstream gradients dy [T, k_eff, M] of the
+ * per-(token, slot) outputs: every route (t, s) with expert e = expert_ids[t, s]
+ * is one row of expert e's dense FFN on x[t], so, routes taken in ascending flat
+ * order,
+ *   dx[t]         += the dense backward's dx for (x[t], dy[t, s], expert e)
+ *   dW_gate_up[e] += dgu^T x[t],   dW_down[e] += dy[t, s]^T h
+ * (the dense backward of oracle_ffn_backward, row by row).  dx is [T, M],
+ * dw_gate_up [E, 2I, M], dw_down [E, M, I]; all are overwritten. */
+int oracle_moe_grouped_backward(const void* x, int x_dt, const int32_t* expert_ids,
+                                const void* w_gate_up, const void* w_down, int w_dt,
+                                const void* dy, int dy_dt, double* dx, double* dw_gate_up,
+                                double* dw_down, int64_t T, int32_t k_eff, int32_t E, int64_t M,
+                                int64_t I, double beta, double linear_beta) {
+  if (!oracle_dtype_ok(x_dt) || !oracle_dtype_ok(w_dt) || !oracle_dtype_ok(dy_dt))
+    return ORACLE_BAD_ARG;
+  if (T < 0 || k_eff <= 0 || E <= 0 || M <= 0 || I <= 0) return ORACLE_BAD_ARG;
+  if (!x || !expert_ids || !w_gate_up || !w_down || !dy || !dx || !dw_gate_up || !dw_down)
+    return ORACLE_BAD_ARG;
+  memset(dx, 0, sizeof(double) * (size_t)(T * M));
+  memset(dw_gate_up, 0, sizeof(double) * (size_t)(E * 2 * I * M));
+  memset(dw_down, 0, sizeof(double) * (size_t)(E * M * I));
+  double* gu = (double*)malloc(sizeof(double) * (size_t)(2 * I));
+  double* h = (double*)malloc(sizeof(double) * (size_t)I);
+  double* dgu = (double*)malloc(sizeof(double) * (size_t)(2 * I));
+  if (!gu || !h || !dgu) {
+    free(gu);
+    free(h);
+    free(dgu);
+    return ORACLE_BAD_ARG;
+  }
+  const size_t esz = w_dt == ORACLE_F64 ? 8 : (w_dt == ORACLE_F32 ? 4 : 2);
+  int st = ORACLE_OK;
+  for (int64_t f = 0; f < T * k_eff && st == ORACLE_OK; ++f) {
+    const int64_t t = f / k_eff;
+    const int32_t e = expert_ids[f];
+    if (e < 0 || e >= E) {
+      st = ORACLE_BAD_INDEX;
+      break;
+    }
+    const char* wg = (const char*)w_gate_up + (size_t)e * (size_t)(2 * I * M) * esz;
+    const char* wd = (const char*)w_down + (size_t)e * (size_t)(M * I) * esz;
+    for (int64_t n = 0; n < 2 * I; ++n) {
+      double acc = 0.0;
+      for (int64_t k = 0; k < M; ++k)
+        acc += oracle_load(x, x_dt, t * M + k) * oracle_load(wg, w_dt, n * M + k);
+      gu[n] = acc;
+    }
+    for (int64_t j = 0; j < I; ++j) {
+      h[j] = oracle_situ_pair(gu[j], gu[I + j], beta, linear_beta);
+      double dhj = 0.0;
+      for (int64_t m = 0; m < M; ++m)
+        dhj += oracle_load(dy, dy_dt, f * M + m) * oracle_load(wd, w_dt, m * I + j);
+      double pg, pu;
+      oracle_situ_pair_grad(gu[j], gu[I + j], beta, linear_beta, &pg, &pu);
+      dgu[j] = dhj * pg;
+      dgu[I + j] = dhj * pu;
+    }
+    for (int64_t k = 0; k < M; ++k) {
+      double acc = 0.0;
+      for (int64_t n = 0; n < 2 * I; ++n) acc += dgu[n] * oracle_load(wg, w_dt, n * M + k);
+      dx[t * M + k] += acc;
+    }
+    double* dwd_e = dw_down + (size_t)e * (size_t)(M * I);
+    for (int64_t m = 0; m < M; ++m)
+      for (int64_t j = 0; j < I; ++j) dwd_e[m * I + j] += oracle_load(dy, dy_dt, f * M + m) * h[j];
+    double* dwg_e = dw_gate_up + (size_t)e * (size_t)(2 * I * M);
+    for (int64_t n = 0; n < 2 * I; ++n)
+      for (int64_t k = 0; k < M; ++k) dwg_e[n * M + k] += dgu[n] * oracle_load(x, x_dt, t * M + k);
+  }
+  free(gu);
+  free(h);
+  free(dgu);
+  return st;
+}
+
 /* Combine of a routed layer: out[t, :] = sum over slots s of w[t, s] * y[t, s, :]
  * in slot order, FP64.  The pages' MoE calls each routed and shared expert on its
  * token rows ("SiTU-GLU" chapter, "Ou SiTU-GLU est utilise": 896 routed plus 2

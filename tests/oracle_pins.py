@@ -399,6 +399,42 @@ def pin_ffn_backward_finite_differences(o):
             assert abs(grad[pos] - fd) <= 1e-6 * (1 + abs(fd)), (idx, pos, grad[pos], fd)
 
 
+def pin_grouped_backward(o):
+    """The grouped backward against the dense backward, brute force: one expert and
+    one slot reproduce the dense backward exactly (same sums in the same order); in
+    general dx[t] is the sum over the token's slots of the dense dx of its expert,
+    and dW[e] the sum over expert e's routes; unused experts get zero gradients."""
+    rng = np.random.default_rng(24)
+    T, M, I = 4, 5, 3
+    x = rng.normal(size=(T, M))
+    wgu = rng.normal(size=(1, 2 * I, M))
+    wd = rng.normal(size=(1, M, I))
+    dy = rng.normal(size=(T, 1, M))
+    gdx, gdwg, gdwd = o.moe_grouped_backward(x, np.zeros((T, 1), np.int32), wgu, wd, dy)
+    ddx, ddwg, ddwd = o.ffn_backward(x, wgu[0], wd[0], dy[:, 0, :])
+    assert np.array_equal(gdx, ddx) and np.array_equal(gdwg[0], ddwg) and np.array_equal(gdwd[0], ddwd)
+    E, k = 4, 2
+    ids = np.array([[0, 2], [2, 0], [2, 3], [3, 0]], dtype=np.int32)  # expert 1 unused
+    wgu = rng.normal(size=(E, 2 * I, M))
+    wd = rng.normal(size=(E, M, I))
+    dy = rng.normal(size=(T, k, M))
+    gdx, gdwg, gdwd = o.moe_grouped_backward(x, ids, wgu, wd, dy)
+    want_dx = np.zeros((T, M))
+    want_dwg = np.zeros((E, 2 * I, M))
+    want_dwd = np.zeros((E, M, I))
+    for t in range(T):
+        for s in range(k):
+            e = ids[t, s]
+            a, b, c = o.ffn_backward(x[t:t + 1], wgu[e], wd[e], dy[t:t + 1, s, :])
+            want_dx[t] += a[0]
+            want_dwg[e] += b
+            want_dwd[e] += c
+    np.testing.assert_allclose(gdx, want_dx, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(gdwg, want_dwg, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(gdwd, want_dwd, rtol=1e-12, atol=1e-12)
+    assert not gdwg[1].any() and not gdwd[1].any()
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_swiglu_gate_and_gaps,
@@ -421,6 +457,7 @@ ALL_PINS = [
     pin_pair_grad_closed_forms,
     pin_ffn_backward_structure,
     pin_ffn_backward_finite_differences,
+    pin_grouped_backward,
 ]
 
 

@@ -63,6 +63,12 @@ MUTANTS = {
                           "oracle_load(w_down, w_dt, j * M + m);\n      double pg"),
     "bwd_dw_down_wrong_operand": ("s += oracle_load(dy, dy_dt, r * M + m) * h[r * I + j];",
                                   "s += oracle_load(x, x_dt, r * M + m) * h[r * I + j];"),
+    "grouped_bwd_wrong_expert_slab": (
+        "const char* wd = (const char*)w_down + (size_t)e * (size_t)(M * I) * esz;",
+        "const char* wd = (const char*)w_down;"),
+    "grouped_bwd_dx_overwrites_slot": ("dx[t * M + k] += acc;", "dx[t * M + k] = acc;"),
+    "grouped_bwd_dw_token_row": ("dwg_e[n * M + k] += dgu[n] * oracle_load(x, x_dt, t * M + k);",
+                                "dwg_e[n * M + k] += dgu[n] * oracle_load(x, x_dt, k);"),
     "combine_wrong_weight": ("oracle_load(w, w_dt, t * k_eff + k) * y[(t * k_eff + k) * M + m]",
                              "oracle_load(w, w_dt, t * k_eff) * y[(t * k_eff + k) * M + m]"),
     "combine_dropped_slot": ("for (int32_t k = 0; k < k_eff; ++k)\n        s +=",
