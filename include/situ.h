@@ -350,6 +350,61 @@ situ_status situ_moe_grouped_forward(const void* x, const int32_t* expert_offset
                                      float linear_beta, situ_dtype dt, void* stream);
 
 /* -------------------------------------------------------------------------
+ * situ_moe_grouped_forward_train / situ_moe_grouped_backward -- training step of
+ * the grouped experts.
+ *
+ * The forward is situ_moe_grouped_forward (same arguments, same y) that also
+ * keeps, in expert order (row r belongs to route token_index[r]), what the
+ * backward needs: the pre-activation pair gu [R, 2I] (gate columns then up
+ * columns, bf16) and the activation h [R, I], R = T * k_eff.
+ *
+ * The backward takes dy [T, k_eff, M], the gradient of the per-route outputs y
+ * (apply the combine weights to dy first: the combine is linear), and computes,
+ * every route (t, s) of expert e being one row of expert e's dense FFN on x[t]
+ * (as situ_ffn_backward, whose derivative it uses: "SiTU-GLU" chapter, "Pourquoi
+ * un plafond doux"; docs page, "Two linear maps and a guarded compiled branch"):
+ *   dx[t]          = sum over the token's slots s of d(g, u)[t, s] W_gate_up[e]
+ *   dW_gate_up[e]  = sum over expert e's routes of d(g, u)^T x[t]     [2I, M]
+ *   dW_down[e]     = sum over expert e's routes of dy[t, s]^T h       [M, I]
+ * FP32 accumulation, bf16 results; an expert without routes gets zero weight
+ * gradients.  The per-expert weight gradients contract over each expert's own
+ * rows; the per-route dx rows are summed over slots in FP32, slot order
+ * (deterministic, no atomics).
+ *
+ *   x, expert_offsets, token_index, W_gate_up, W_down, T, k_eff, E, M, I, caps:
+ *               as situ_moe_grouped_forward.
+ *   gu, h       device, as written by situ_moe_grouped_forward_train with the same
+ *               expert_offsets and token_index.
+ *   dy          device, [T, k_eff, M] bf16.
+ *   dx          device, [T, M] bf16, written.
+ *   dW_gate_up  device, [E, 2I, M] bf16, written;  dW_down  [E, M, I] bf16, written.
+ *   workspace   forward: >= situ_moe_workspace_size(R, E, M, I, dt) bytes;
+ *               backward: >= situ_moe_backward_workspace_size(R, E, M, I, dt) bytes;
+ *               256-byte aligned.  Outputs must not overlap inputs or workspace.
+ * T = 0: the backward zeroes dW_gate_up and dW_down.  Invalid offsets record
+ * SITU_ERR_INDEX in the device status and the GEMMs write nothing.
+ * Errors: those of situ_moe_grouped_forward.
+ * ------------------------------------------------------------------------- */
+situ_status situ_moe_grouped_forward_train(const void* x, const int32_t* expert_offsets,
+                                           const int32_t* token_index, const void* W_gate_up,
+                                           const void* W_down, void* y, void* gu, void* h,
+                                           void* workspace, size_t workspace_bytes, int64_t T,
+                                           int32_t k_eff, int32_t E, int64_t M, int64_t I,
+                                           float beta, float linear_beta, situ_dtype dt,
+                                           void* stream);
+
+size_t situ_moe_backward_workspace_size(int64_t R, int32_t E, int64_t M, int64_t I,
+                                        situ_dtype dt);
+
+situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offsets,
+                                      const int32_t* token_index, const void* W_gate_up,
+                                      const void* W_down, const void* gu, const void* h,
+                                      const void* dy, void* dx, void* dW_gate_up, void* dW_down,
+                                      void* workspace, size_t workspace_bytes, int64_t T,
+                                      int32_t k_eff, int32_t E, int64_t M, int64_t I, float beta,
+                                      float linear_beta, situ_dtype dt, void* stream);
+
+/* -------------------------------------------------------------------------
  * situ_moe_combine -- the layer output of a routed batch: for every token t,
  *   out[t, :] = dtype( sum over slots s = 0 .. k_eff-1 of w[t, s] * y[t, s, :] ),
  * accumulated in FP32 in slot order (deterministic; no atomics).  Each routed and

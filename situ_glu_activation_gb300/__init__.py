@@ -4,18 +4,21 @@ Hand-written CUDA kernels behind a C ABI (``include/situ.h``, ``libsitu.so``):
   * ``situ_glu_act``              standalone activation (memory bound)
   * ``situ_ffn_forward``          dense FFN: tcgen05 gate_up GEMM with the
                                   activation in its epilogue, tcgen05 down GEMM
+  * ``situ_ffn_forward_train`` / ``situ_ffn_backward``   dense training step
   * ``situ_moe_build_index``      stable expert index of routed tokens
   * ``situ_moe_grouped_forward``  the FFN grouped over experts
+  * ``situ_moe_grouped_forward_train`` / ``situ_moe_grouped_backward``
+                                  grouped training step
+  * ``situ_moe_combine``          router-weighted combine
 This package is the thin PyTorch binding over that ABI.
 """
 from .api import (SituError, device_status, ffn_backward_workspace_bytes,
-                  ffn_host_workspace_bytes, ffn_workspace_bytes, situ_ffn_backward,
-                  situ_ffn_forward_train,
-                  moe_workspace_bytes,
-                  selftest_bounded_wait, situ_ffn_down, situ_ffn_forward, situ_ffn_forward_host,
-                  situ_ffn_gate_up,
-                  situ_glu_act,
-                  situ_moe_build_index, situ_moe_combine, situ_moe_grouped_forward)
+                  ffn_host_workspace_bytes, ffn_workspace_bytes, moe_backward_workspace_bytes,
+                  moe_workspace_bytes, selftest_bounded_wait, situ_ffn_backward, situ_ffn_down,
+                  situ_ffn_forward, situ_ffn_forward_host, situ_ffn_forward_train,
+                  situ_ffn_gate_up, situ_glu_act, situ_moe_build_index, situ_moe_combine,
+                  situ_moe_grouped_backward, situ_moe_grouped_forward,
+                  situ_moe_grouped_forward_train)
 
 __all__ = [
     "SituError", "situ_glu_act", "situ_ffn_forward", "situ_ffn_forward_host", "situ_ffn_gate_up",
@@ -24,4 +27,5 @@ __all__ = [
     "situ_moe_grouped_forward", "ffn_workspace_bytes", "moe_workspace_bytes",
     "device_status", "selftest_bounded_wait", "ffn_host_workspace_bytes", "situ_moe_combine",
     "situ_ffn_forward_train", "situ_ffn_backward", "ffn_backward_workspace_bytes",
+    "situ_moe_grouped_forward_train", "situ_moe_grouped_backward", "moe_backward_workspace_bytes",
 ]

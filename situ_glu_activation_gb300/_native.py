@@ -50,6 +50,11 @@ SIGNATURES = {
     "situ_moe_workspace_size": ([_i64, _i32, _i64, _i64, _ci], _sz),
     "situ_moe_grouped_forward": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i32, _i32,
                                   _i64, _i64, _f32, _f32, _ci, _vp], _ci),
+    "situ_moe_grouped_forward_train": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64,
+                                        _i32, _i32, _i64, _i64, _f32, _f32, _ci, _vp], _ci),
+    "situ_moe_backward_workspace_size": ([_i64, _i32, _i64, _i64, _ci], _sz),
+    "situ_moe_grouped_backward": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                   _sz, _i64, _i32, _i32, _i64, _i64, _f32, _f32, _ci, _vp], _ci),
     "situ_moe_combine": ([_vp, _vp, _vp, _i64, _i32, _i64, _ci, _vp], _ci),
     "situ_selftest_bounded_wait": ([_u32, _vp], _ci),
 }

@@ -332,6 +332,83 @@ def situ_moe_grouped_forward(x: torch.Tensor, expert_offsets: torch.Tensor,
     return y
 
 
+def _moe_shapes(x, expert_offsets, token_index, W_gate_up, W_down, k_eff):
+    for n, t in (("x", x), ("expert_offsets", expert_offsets), ("token_index", token_index),
+                 ("W_gate_up", W_gate_up), ("W_down", W_down)):
+        _cuda_contig(n, t)
+    T, M = x.shape
+    E, twoI, _ = W_gate_up.shape
+    I = twoI // 2
+    if W_gate_up.shape != (E, 2 * I, M) or W_down.shape != (E, M, I):
+        raise ValueError("stacked weight shapes do not match x")
+    if expert_offsets.numel() != E + 1 or token_index.numel() != T * k_eff:
+        raise ValueError("index arrays do not match E and T*k_eff")
+    return T, M, E, I
+
+
+def situ_moe_grouped_forward_train(x: torch.Tensor, expert_offsets: torch.Tensor,
+                                   token_index: torch.Tensor, W_gate_up: torch.Tensor,
+                                   W_down: torch.Tensor, k_eff: int, beta: float = 4.0,
+                                   linear_beta: float = 25.0,
+                                   workspace: torch.Tensor | None = None):
+    """Training forward of the grouped experts: returns (y [T, k_eff, M], gu [R, 2I],
+    h [R, I]) with gu and h in expert order (row r is route token_index[r]), kept
+    for situ_moe_grouped_backward."""
+    T, M, E, I = _moe_shapes(x, expert_offsets, token_index, W_gate_up, W_down, k_eff)
+    R = T * k_eff
+    y = torch.empty(T, k_eff, M, dtype=x.dtype, device=x.device)
+    gu = torch.empty(R, 2 * I, dtype=x.dtype, device=x.device)
+    h = torch.empty(R, I, dtype=x.dtype, device=x.device)
+    if R == 0:
+        return y, gu, h
+    lib = _native.lib()
+    need = int(lib.situ_moe_workspace_size(R, E, M, I, _dt(x)))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    check("situ_moe_grouped_forward_train",
+          lib.situ_moe_grouped_forward_train(
+              x.data_ptr(), expert_offsets.data_ptr(), token_index.data_ptr(),
+              W_gate_up.data_ptr(), W_down.data_ptr(), y.data_ptr(), gu.data_ptr(), h.data_ptr(),
+              workspace.data_ptr(), workspace.numel() * workspace.element_size(), T, k_eff, E, M,
+              I, *caps(beta, linear_beta), _dt(x), _stream(x.device)))
+    return y, gu, h
+
+
+def moe_backward_workspace_bytes(R: int, E: int, M: int, I: int) -> int:
+    return int(_native.lib().situ_moe_backward_workspace_size(R, E, M, I, SITU_BF16))
+
+
+def situ_moe_grouped_backward(x: torch.Tensor, expert_offsets: torch.Tensor,
+                              token_index: torch.Tensor, W_gate_up: torch.Tensor,
+                              W_down: torch.Tensor, gu: torch.Tensor, h: torch.Tensor,
+                              dy: torch.Tensor, beta: float = 4.0, linear_beta: float = 25.0,
+                              workspace: torch.Tensor | None = None):
+    """Backward of the grouped experts for dy [T, k_eff, M] (the gradient of the
+    per-route outputs): returns (dx [T, M], dW_gate_up [E, 2I, M], dW_down [E, M, I])."""
+    k_eff = dy.shape[1] if dy.dim() == 3 else token_index.numel() // max(x.shape[0], 1)
+    T, M, E, I = _moe_shapes(x, expert_offsets, token_index, W_gate_up, W_down, k_eff)
+    R = T * k_eff
+    for n, t in (("gu", gu), ("h", h), ("dy", dy)):
+        _cuda_contig(n, t)
+    if gu.shape != (R, 2 * I) or h.shape != (R, I) or dy.numel() != R * M:
+        raise ValueError("gu, h or dy do not match the routes")
+    dx = torch.empty_like(x)
+    dwg = torch.empty_like(W_gate_up)
+    dwd = torch.empty_like(W_down)
+    lib = _native.lib()
+    need = int(lib.situ_moe_backward_workspace_size(R, E, M, I, _dt(x)))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    check("situ_moe_grouped_backward",
+          lib.situ_moe_grouped_backward(
+              x.data_ptr(), expert_offsets.data_ptr(), token_index.data_ptr(),
+              W_gate_up.data_ptr(), W_down.data_ptr(), gu.data_ptr(), h.data_ptr(),
+              dy.data_ptr(), dx.data_ptr(), dwg.data_ptr(), dwd.data_ptr(), workspace.data_ptr(),
+              workspace.numel() * workspace.element_size(), T, k_eff, E, M, I,
+              *caps(beta, linear_beta), _dt(x), _stream(x.device)))
+    return dx, dwg, dwd
+
+
 def situ_moe_combine(y: torch.Tensor, weights: torch.Tensor,
                      out: torch.Tensor | None = None) -> torch.Tensor:
     """Layer output of a routed batch: out[t] = sum_s weights[t, s] * y[t, s] (FP32,
@@ -370,4 +447,5 @@ __all__ = [
     "situ_moe_grouped_forward", "ffn_workspace_bytes", "moe_workspace_bytes",
     "device_status", "selftest_bounded_wait", "ffn_host_workspace_bytes", "situ_moe_combine",
     "situ_ffn_forward_train", "situ_ffn_backward", "ffn_backward_workspace_bytes",
+    "situ_moe_grouped_forward_train", "situ_moe_grouped_backward", "moe_backward_workspace_bytes",
 ]

@@ -484,51 +484,45 @@ size_t situ_moe_workspace_size(int64_t R, int32_t E, int64_t M, int64_t I, situ_
   return tiles + xperm + h;
 }
 
-situ_status situ_moe_grouped_forward(const void* x, const int32_t* expert_offsets,
-                                     const int32_t* token_index, const void* W_gate_up,
-                                     const void* W_down, void* y, void* workspace,
-                                     size_t workspace_bytes, int64_t T, int32_t k_eff,
-                                     int32_t E, int64_t M, int64_t I, float beta,
-                                     float linear_beta, situ_dtype dt, void* stream) {
+// Shared argument checks of the grouped entry points.
+situ_status moe_common_checks(const void* x, const int32_t* expert_offsets,
+                              const int32_t* token_index, const void* W_gate_up,
+                              const void* W_down, int64_t T, int32_t k_eff, int32_t E, int64_t M,
+                              int64_t I, float beta, float linear_beta, situ_dtype dt) {
   if (dt != SITU_BF16) return dt == SITU_F32 ? SITU_ERR_UNSUPPORTED : SITU_ERR_ARG;
   if (T < 0 || k_eff < 1 || E < 1 || E > 65536 || M < 1 || I < 1 || !caps_ok(beta, linear_beta))
     return SITU_ERR_ARG;
   const int64_t R = T * k_eff;
   if (R == 0) return SITU_OK;
-  if (!x || !expert_offsets || !token_index || !W_gate_up || !W_down || !y) return SITU_ERR_ARG;
+  if (!x || !expert_offsets || !token_index || !W_gate_up || !W_down) return SITU_ERR_ARG;
   if (R >= (int64_t(1) << 31) || static_cast<int64_t>(E) * 2 * I >= (int64_t(1) << 31) ||
       static_cast<int64_t>(E) * M >= (int64_t(1) << 31))
     return SITU_ERR_UNSUPPORTED;
   if (M % 8 || I % 8) return SITU_ERR_UNSUPPORTED;
-  if (!aligned16(x) || !aligned16(W_gate_up) || !aligned16(W_down) || !aligned16(y))
-    return SITU_ERR_ALIGN;
-  const size_t need = situ_moe_workspace_size(R, E, M, I, dt);
-  if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
-    return SITU_ERR_WORKSPACE;
-  const size_t x_b = static_cast<size_t>(T) * M * 2, y_b = static_cast<size_t>(R) * M * 2;
-  const size_t wgu_b = static_cast<size_t>(E) * 2 * I * M * 2, wd_b = static_cast<size_t>(E) * M * I * 2;
-  const size_t off_b = static_cast<size_t>(E + 1) * 4, tix_b = static_cast<size_t>(R) * 4;
-  const void* ins[] = {x, W_gate_up, W_down, expert_offsets, token_index};
-  const size_t in_b[] = {x_b, wgu_b, wd_b, off_b, tix_b};
-  for (int i = 0; i < 5; ++i) {
-    if (overlap(y, y_b, ins[i], in_b[i]) || overlap(workspace, need, ins[i], in_b[i]))
-      return SITU_ERR_ALIAS;
-  }
-  if (overlap(y, y_b, workspace, need)) return SITU_ERR_ALIAS;
+  if (!aligned16(x) || !aligned16(W_gate_up) || !aligned16(W_down)) return SITU_ERR_ALIGN;
+  return SITU_OK;
+}
+
+// The grouped forward; gu_store (training) additionally keeps the pre-activation.
+situ_status moe_forward_impl(const void* x, const int32_t* expert_offsets,
+                             const int32_t* token_index, const void* W_gate_up,
+                             const void* W_down, void* y, void* h_perm, void* gu_store,
+                             void* workspace, int64_t T, int32_t k_eff, int32_t E, int64_t M,
+                             int64_t I, float beta, float linear_beta, cudaStream_t cs) {
+  const int64_t R = T * k_eff;
   DeviceState* st = nullptr;
   situ_status s = device_state(&st);
   if (s != SITU_OK) return s;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const size_t prefix_bytes = round_up(static_cast<size_t>(E + 1) * 4, 256);
   int32_t* tile_offsets = reinterpret_cast<int32_t*>(ws);
   int32_t* units_gu = reinterpret_cast<int32_t*>(ws + prefix_bytes);
   int32_t* units_dn = reinterpret_cast<int32_t*>(ws + 2 * prefix_bytes);
   void* x_perm = ws + 3 * prefix_bytes;
-  void* h_perm = static_cast<uint8_t*>(x_perm) + round_up(static_cast<size_t>(R) * M * 2, 256);
 
-  cudaError_t e = launch_group_tiles(expert_offsets, E, R, I, M, tile_offsets, units_gu,
-                                     units_dn, st->status, cs);
+  cudaError_t e = launch_group_tiles(expert_offsets, E, R, gemm_n_tiles_situ(I),
+                                     gemm_n_tiles_wide(M), tile_offsets, units_gu, units_dn,
+                                     st->status, cs);
   if (e != cudaSuccess) return cuda_fail(e);
   e = launch_gather_rows(x, token_index, x_perm, R, k_eff, M, st->status, cs);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -549,6 +543,8 @@ situ_status situ_moe_grouped_forward(const void* x, const int32_t* expert_offset
   g.out = h_perm;
   g.ldo = I;
   g.out_rows = R;
+  g.gu_store = gu_store;
+  g.split = I;
   e = launch_gemm_situ(g, p, caps_of(beta, linear_beta), st->status, st->num_sms, cs);
   if (e != cudaSuccess) return cuda_fail(e);
   GemmShape d{};
@@ -568,6 +564,246 @@ situ_status situ_moe_grouped_forward(const void* x, const int32_t* expert_offset
   d.out_rows = R;
   d.out_row_index = token_index;
   return finish(launch_gemm_plain(d, st->status, st->num_sms, cs));
+}
+
+situ_status situ_moe_grouped_forward(const void* x, const int32_t* expert_offsets,
+                                     const int32_t* token_index, const void* W_gate_up,
+                                     const void* W_down, void* y, void* workspace,
+                                     size_t workspace_bytes, int64_t T, int32_t k_eff,
+                                     int32_t E, int64_t M, int64_t I, float beta,
+                                     float linear_beta, situ_dtype dt, void* stream) {
+  situ_status s = moe_common_checks(x, expert_offsets, token_index, W_gate_up, W_down, T, k_eff,
+                                    E, M, I, beta, linear_beta, dt);
+  const int64_t R = T * k_eff;
+  if (s != SITU_OK || R == 0) return s;
+  if (!y) return SITU_ERR_ARG;
+  if (!aligned16(y)) return SITU_ERR_ALIGN;
+  const size_t need = situ_moe_workspace_size(R, E, M, I, dt);
+  if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return SITU_ERR_WORKSPACE;
+  const size_t x_b = static_cast<size_t>(T) * M * 2, y_b = static_cast<size_t>(R) * M * 2;
+  const size_t wgu_b = static_cast<size_t>(E) * 2 * I * M * 2, wd_b = static_cast<size_t>(E) * M * I * 2;
+  const size_t off_b = static_cast<size_t>(E + 1) * 4, tix_b = static_cast<size_t>(R) * 4;
+  const void* ins[] = {x, W_gate_up, W_down, expert_offsets, token_index};
+  const size_t in_b[] = {x_b, wgu_b, wd_b, off_b, tix_b};
+  for (int i = 0; i < 5; ++i) {
+    if (overlap(y, y_b, ins[i], in_b[i]) || overlap(workspace, need, ins[i], in_b[i]))
+      return SITU_ERR_ALIAS;
+  }
+  if (overlap(y, y_b, workspace, need)) return SITU_ERR_ALIAS;
+  const size_t prefix_bytes = round_up(static_cast<size_t>(E + 1) * 4, 256);
+  void* h_perm = static_cast<uint8_t*>(workspace) + 3 * prefix_bytes +
+                 round_up(static_cast<size_t>(R) * M * 2, 256);
+  return moe_forward_impl(x, expert_offsets, token_index, W_gate_up, W_down, y, h_perm, nullptr,
+                          workspace, T, k_eff, E, M, I, beta, linear_beta,
+                          static_cast<cudaStream_t>(stream));
+}
+
+situ_status situ_moe_grouped_forward_train(const void* x, const int32_t* expert_offsets,
+                                           const int32_t* token_index, const void* W_gate_up,
+                                           const void* W_down, void* y, void* gu, void* h,
+                                           void* workspace, size_t workspace_bytes, int64_t T,
+                                           int32_t k_eff, int32_t E, int64_t M, int64_t I,
+                                           float beta, float linear_beta, situ_dtype dt,
+                                           void* stream) {
+  situ_status s = moe_common_checks(x, expert_offsets, token_index, W_gate_up, W_down, T, k_eff,
+                                    E, M, I, beta, linear_beta, dt);
+  const int64_t R = T * k_eff;
+  if (s != SITU_OK || R == 0) return s;
+  if (!y || !gu || !h) return SITU_ERR_ARG;
+  if (!aligned16(y) || !aligned16(gu) || !aligned16(h)) return SITU_ERR_ALIGN;
+  const size_t need = situ_moe_workspace_size(R, E, M, I, dt);
+  if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return SITU_ERR_WORKSPACE;
+  const size_t x_b = static_cast<size_t>(T) * M * 2, y_b = static_cast<size_t>(R) * M * 2;
+  const size_t wgu_b = static_cast<size_t>(E) * 2 * I * M * 2, wd_b = static_cast<size_t>(E) * M * I * 2;
+  const size_t off_b = static_cast<size_t>(E + 1) * 4, tix_b = static_cast<size_t>(R) * 4;
+  const size_t gu_b = static_cast<size_t>(R) * 2 * I * 2, h_b = static_cast<size_t>(R) * I * 2;
+  const void* ins[] = {x, W_gate_up, W_down, expert_offsets, token_index};
+  const size_t in_b[] = {x_b, wgu_b, wd_b, off_b, tix_b};
+  void* outs[] = {y, gu, h, workspace};
+  const size_t out_b[] = {y_b, gu_b, h_b, need};
+  for (int o = 0; o < 4; ++o) {
+    for (int i = 0; i < 5; ++i)
+      if (overlap(outs[o], out_b[o], ins[i], in_b[i])) return SITU_ERR_ALIAS;
+    for (int j = o + 1; j < 4; ++j)
+      if (overlap(outs[o], out_b[o], outs[j], out_b[j])) return SITU_ERR_ALIAS;
+  }
+  return moe_forward_impl(x, expert_offsets, token_index, W_gate_up, W_down, y, h, gu, workspace,
+                          T, k_eff, E, M, I, beta, linear_beta,
+                          static_cast<cudaStream_t>(stream));
+}
+
+size_t situ_moe_backward_workspace_size(int64_t R, int32_t E, int64_t M, int64_t I,
+                                        situ_dtype dt) {
+  if (R < 0 || E < 1 || M < 1 || I < 1 || dt != SITU_BF16) return 0;
+  // m-tile prefix + paired-unit prefixes of the dh and dx GEMMs, one [R, M] buffer
+  // (dy in expert order, then the per-route dx, then x in expert order) and
+  // d(g, u) [R, 2I] in expert order.
+  const size_t tiles = 3 * round_up(static_cast<size_t>(E + 1) * 4, 256);
+  const size_t rows_m = round_up(static_cast<size_t>(R) * M * 2, 256);
+  const size_t dgu = round_up(static_cast<size_t>(R) * 2 * I * 2, 256);
+  return tiles + rows_m + dgu;
+}
+
+situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offsets,
+                                      const int32_t* token_index, const void* W_gate_up,
+                                      const void* W_down, const void* gu, const void* h,
+                                      const void* dy, void* dx, void* dW_gate_up, void* dW_down,
+                                      void* workspace, size_t workspace_bytes, int64_t T,
+                                      int32_t k_eff, int32_t E, int64_t M, int64_t I, float beta,
+                                      float linear_beta, situ_dtype dt, void* stream) {
+  situ_status s = moe_common_checks(x, expert_offsets, token_index, W_gate_up, W_down, T, k_eff,
+                                    E, M, I, beta, linear_beta, dt);
+  if (s != SITU_OK) return s;
+  const int64_t R = T * k_eff;
+  if (!dW_gate_up || !dW_down) return SITU_ERR_ARG;
+  if (!aligned16(dW_gate_up) || !aligned16(dW_down)) return SITU_ERR_ALIGN;
+  if (M % 8 || I % 8) return SITU_ERR_UNSUPPORTED;
+  const size_t wgu_b = static_cast<size_t>(E) * 2 * I * M * 2, wd_b = static_cast<size_t>(E) * M * I * 2;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (R == 0) {
+    // No routes: every expert's weight gradient is zero and dx is empty.
+    if (overlap(dW_gate_up, wgu_b, dW_down, wd_b)) return SITU_ERR_ALIAS;
+    DeviceState* st = nullptr;
+    if ((s = device_state(&st)) != SITU_OK) return s;
+    cudaError_t e = cudaMemsetAsync(dW_gate_up, 0, wgu_b, cs);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dW_down, 0, wd_b, cs);
+    return finish(e);
+  }
+  if (!gu || !h || !dy || !dx) return SITU_ERR_ARG;
+  if (!aligned16(gu) || !aligned16(h) || !aligned16(dy) || !aligned16(dx)) return SITU_ERR_ALIGN;
+  const size_t need = situ_moe_backward_workspace_size(R, E, M, I, dt);
+  if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return SITU_ERR_WORKSPACE;
+  const size_t x_b = static_cast<size_t>(T) * M * 2, dy_b = static_cast<size_t>(R) * M * 2;
+  const size_t off_b = static_cast<size_t>(E + 1) * 4, tix_b = static_cast<size_t>(R) * 4;
+  const size_t gu_b = static_cast<size_t>(R) * 2 * I * 2, h_b = static_cast<size_t>(R) * I * 2;
+  const void* ins[] = {x, W_gate_up, W_down, expert_offsets, token_index, gu, h, dy};
+  const size_t in_b[] = {x_b, wgu_b, wd_b, off_b, tix_b, gu_b, h_b, dy_b};
+  void* outs[] = {dx, dW_gate_up, dW_down, workspace};
+  const size_t out_b[] = {x_b, wgu_b, wd_b, need};
+  for (int o = 0; o < 4; ++o) {
+    for (int i = 0; i < 8; ++i)
+      if (overlap(outs[o], out_b[o], ins[i], in_b[i])) return SITU_ERR_ALIAS;
+    for (int j = o + 1; j < 4; ++j)
+      if (overlap(outs[o], out_b[o], outs[j], out_b[j])) return SITU_ERR_ALIAS;
+  }
+  DeviceState* st = nullptr;
+  if ((s = device_state(&st)) != SITU_OK) return s;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t prefix_bytes = round_up(static_cast<size_t>(E + 1) * 4, 256);
+  int32_t* tile_offsets = reinterpret_cast<int32_t*>(ws);
+  int32_t* units_dh = reinterpret_cast<int32_t*>(ws + prefix_bytes);
+  int32_t* units_dx = reinterpret_cast<int32_t*>(ws + 2 * prefix_bytes);
+  void* rows_m = ws + 3 * prefix_bytes;  // [R, M]: dy, then per-route dx, then x
+  void* dgu = static_cast<uint8_t*>(rows_m) + round_up(static_cast<size_t>(R) * M * 2, 256);
+  const SituParams p = make_situ_params(beta, linear_beta);
+  cudaError_t e = launch_group_tiles(expert_offsets, E, R, gemm_n_tiles_wide(I),
+                                     gemm_n_tiles_wide(M), tile_offsets, units_dh, units_dx,
+                                     st->status, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  // dy in expert order: dy_perm[r] = dy[token_index[r]] (one row per route).
+  e = launch_gather_rows(dy, token_index, rows_m, R, 1, M, st->status, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  // dh = dy W_down[e] per expert (W_down[e] [M, I] read as MN-major [K = M, N = I]);
+  // the epilogue turns dh into d(g, u) at the saved pre-activation.
+  {
+    GemmShape g{};
+    g.a = rows_m;
+    g.a_rows = R;
+    g.b = W_down;
+    g.b_rows = I;
+    g.b_mn_major = true;
+    g.K = M;
+    g.num_groups = E;
+    g.group_offsets = expert_offsets;
+    g.tile_offsets = tile_offsets;
+    g.unit_offsets = units_dh;
+    g.b_group_rows = M;
+    g.n_out = I;
+    g.out = dgu;
+    g.ldo = 2 * I;
+    g.out_rows = R;
+    g.gu_in = gu;
+    g.dgu_out = dgu;
+    g.split = I;
+    e = launch_gemm_situ_bwd(g, p, caps_of(beta, linear_beta), st->status, st->num_sms, cs);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  // dW_down[e] = dy_e^T h_e: contraction over each expert's own rows.
+  {
+    GemmShape g{};
+    g.a = rows_m;
+    g.a_rows = M;
+    g.a_mn_major = true;
+    g.b = h;
+    g.b_rows = I;
+    g.b_mn_major = true;
+    g.K = R;
+    g.num_groups = E;
+    g.tile_offsets = tile_offsets;
+    g.k_group_offsets = expert_offsets;
+    g.out_group_rows = M;
+    g.n_out = I;
+    g.out = dW_down;
+    g.ldo = I;
+    g.out_rows = static_cast<int64_t>(E) * M;
+    if ((e = launch_gemm_plain(g, st->status, st->num_sms, cs)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  // Per-route dx = d(g, u) W_gate_up[e] (W_gate_up[e] [2I, M] as MN-major
+  // [K = 2I, N = M]), written in (token, slot) order over the dy rows.
+  {
+    GemmShape g{};
+    g.a = dgu;
+    g.a_rows = R;
+    g.b = W_gate_up;
+    g.b_rows = M;
+    g.b_mn_major = true;
+    g.K = 2 * I;
+    g.num_groups = E;
+    g.group_offsets = expert_offsets;
+    g.tile_offsets = tile_offsets;
+    g.unit_offsets = units_dx;
+    g.b_group_rows = 2 * I;
+    g.n_out = M;
+    g.out = rows_m;
+    g.ldo = M;
+    g.out_rows = R;
+    g.out_row_index = token_index;
+    if ((e = launch_gemm_plain(g, st->status, st->num_sms, cs)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  // dx[t] = sum over the token's slots of the per-route dx (FP32, slot order).
+  if ((e = launch_combine(rows_m, nullptr, dx, T, k_eff, M, SITU_BF16, st->num_sms, cs)) !=
+      cudaSuccess)
+    return cuda_fail(e);
+  // x in expert order, then dW_gate_up[e] = d(g, u)_e^T x_e.
+  if ((e = launch_gather_rows(x, token_index, rows_m, R, k_eff, M, st->status, cs)) !=
+      cudaSuccess)
+    return cuda_fail(e);
+  {
+    GemmShape g{};
+    g.a = dgu;
+    g.a_rows = 2 * I;
+    g.a_mn_major = true;
+    g.b = rows_m;
+    g.b_rows = M;
+    g.b_mn_major = true;
+    g.K = R;
+    g.num_groups = E;
+    g.tile_offsets = tile_offsets;
+    g.k_group_offsets = expert_offsets;
+    g.out_group_rows = 2 * I;
+    g.n_out = M;
+    g.out = dW_gate_up;
+    g.ldo = M;
+    g.out_rows = static_cast<int64_t>(E) * 2 * I;
+    if ((e = launch_gemm_plain(g, st->status, st->num_sms, cs)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  return SITU_OK;
 }
 
 situ_status situ_moe_combine(const void* y, const float* weights, void* out, int64_t T,

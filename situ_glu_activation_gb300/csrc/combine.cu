@@ -1,5 +1,6 @@
 // combine.cu -- the router-weighted combine of a routed layer:
 //   out[t, :] = sum over slots s of w[t, s] * y[t, s, :]   (FP32, slot order)
+// A null w means weight 1 for every slot (the sum the grouped backward needs).
 // Memory bound: every y byte is read once, every out byte written once.  One
 // thread owns 16 bytes of one token's output row (8 bf16 / 4 float columns) and
 // walks that token's k_eff slot rows with 128-bit streaming loads.
@@ -39,7 +40,8 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t c = i - t * vpr;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     const uint4* row = y + t * k_eff * vpr + c;
-    for (int32_t s = 0; s < k_eff; ++s) add_bf16x8(acc, __ldcs(row + s * vpr), __ldg(w + t * k_eff + s));
+    for (int32_t s = 0; s < k_eff; ++s)
+      add_bf16x8(acc, __ldcs(row + s * vpr), w ? __ldg(w + t * k_eff + s) : 1.0f);
     __stcs(out + i, make_uint4(pack2(acc[0], acc[1]), pack2(acc[2], acc[3]),
                                pack2(acc[4], acc[5]), pack2(acc[6], acc[7])));
   }
@@ -56,7 +58,7 @@ __global__ void __launch_bounds__(kThreads)
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const float4* row = y + t * k_eff * vpr + c;
     for (int32_t s = 0; s < k_eff; ++s) {
-      const float ws = __ldg(w + t * k_eff + s);
+      const float ws = w ? __ldg(w + t * k_eff + s) : 1.0f;
       const float4 v = __ldcs(row + s * vpr);
       acc.x = fmaf(ws, v.x, acc.x);
       acc.y = fmaf(ws, v.y, acc.y);
@@ -91,7 +93,7 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t m = i - t * M;
     float acc = 0.0f;
     for (int32_t s = 0; s < k_eff; ++s)
-      acc = fmaf(__ldg(w + t * k_eff + s), ld(y, (t * k_eff + s) * M + m), acc);
+      acc = fmaf(w ? __ldg(w + t * k_eff + s) : 1.0f, ld(y, (t * k_eff + s) * M + m), acc);
     st(out, i, acc);
   }
 }

@@ -97,6 +97,14 @@ struct Args {
   const __nv_bfloat16* gu_in;
   __nv_bfloat16* dgu_out;
   int64_t split;
+  // K-grouped contraction (MN-major A and B only): group g contracts over the K
+  // rows k_group_offsets[g] .. k_group_offsets[g+1]-1 of both operands and writes
+  // its [dense_rows, n_out] result at output rows g * out_group_rows.  Every group
+  // has units_per_group work units.  A nonzero tile_offsets[num_groups] marks the
+  // offsets as validated (zero: nothing runs).
+  const int32_t* k_group_offsets;
+  int32_t units_per_group;
+  int64_t out_group_rows;
 };
 
 struct SharedCtl {
@@ -115,6 +123,9 @@ struct TileCoord {
   int32_t group;
   int32_t n_tile;
   int32_t share_a;  // paired unit of one m-tile and two n-tiles (A multicast)
+  int32_t k0;       // first K row of the contraction (K-grouped; 0 otherwise)
+  int32_t k_end;    // one past its last K row (K-grouped)
+  int32_t k_blocks; // k-blocks of this tile
 };
 
 __device__ __forceinline__ int32_t total_tiles(const Args& a) {
@@ -148,6 +159,19 @@ __device__ __forceinline__ TileCoord decode_tile(const Args& a, int32_t t) {
   return c;
 }
 
+// Tile `local` of one group's rows row0 .. row_end-1 (unpaired: m-tile-major).
+__device__ __forceinline__ TileCoord in_group_tile(const Args& a, int32_t local, int32_t row0,
+                                                   int32_t row_end) {
+  TileCoord c;
+  const int32_t mt = local / a.n_tiles;
+  c.n_tile = local - mt * a.n_tiles;
+  c.a_row0 = row0 + mt * kBM;
+  c.row_end = row_end;
+  c.group = 0;
+  c.share_a = 0;
+  return c;
+}
+
 // Work units.  Unpaired: one unit = one tile, from decode_tile.  Paired
 // (clusters of two CTAs, CTA rank r):
 //   * a group (expert) with m m-tiles has floor(m/2) * n_tiles "shared-B" units:
@@ -162,32 +186,13 @@ __device__ __forceinline__ int32_t units_of(int32_t m, int32_t n_tiles) {
   return (m >> 1) * n_tiles + (m & 1) * ((n_tiles + 1) >> 1);
 }
 
-template <bool kPair>
-__device__ __forceinline__ int32_t num_units(const Args& a) {
-  if (!kPair) return total_tiles(a);
-  if (a.unit_offsets) return __ldg(a.unit_offsets + a.num_groups);
-  return units_of((a.dense_rows + kBM - 1) / kBM, a.n_tiles);
-}
-
-template <bool kPair>
-__device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_t rank) {
-  if (!kPair) return decode_tile(a, u);
-  int32_t g = 0, row0 = 0, row_end = a.dense_rows, local = u;
-  if (a.unit_offsets) {
-    int32_t lo = 0, hi = a.num_groups - 1;
-    while (lo < hi) {
-      const int32_t mid = (lo + hi + 1) >> 1;
-      if (__ldg(a.unit_offsets + mid) <= u) lo = mid; else hi = mid - 1;
-    }
-    g = lo;
-    row0 = __ldg(a.group_offsets + g);
-    row_end = __ldg(a.group_offsets + g + 1);
-    local = u - __ldg(a.unit_offsets + g);
-  }
+// Paired unit `local` of one group's rows row0 .. row_end-1 (see above).
+__device__ __forceinline__ TileCoord in_group_unit(const Args& a, int32_t local, uint32_t rank,
+                                                   int32_t row0, int32_t row_end) {
   const int32_t m = (row_end - row0 + kBM - 1) / kBM;
   const int32_t shared_b_units = (m >> 1) * a.n_tiles;
   TileCoord c;
-  c.group = g;
+  c.group = 0;
   c.row_end = row_end;
   if (local < shared_b_units) {
     const int32_t p = local / a.n_tiles;
@@ -200,6 +205,56 @@ __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_
     c.a_row0 = row0 + (m - 1) * kBM;
     c.share_a = 1;
   }
+  return c;
+}
+
+template <bool kPair, bool kKG>
+__device__ __forceinline__ int32_t num_units(const Args& a) {
+  if (kKG && a.k_group_offsets) {
+    if (a.tile_offsets && __ldg(a.tile_offsets + a.num_groups) == 0) return 0;
+    return a.num_groups * a.units_per_group;
+  }
+  if (!kPair) return total_tiles(a);
+  if (a.unit_offsets) return __ldg(a.unit_offsets + a.num_groups);
+  return units_of((a.dense_rows + kBM - 1) / kBM, a.n_tiles);
+}
+
+template <bool kPair, bool kKG>
+__device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_t rank) {
+  TileCoord c;
+  if (kKG && a.k_group_offsets) {
+    // Every group has the same output tiles; its K range is its row range.
+    const int32_t g = u / a.units_per_group;
+    const int32_t local = u - g * a.units_per_group;
+    c = kPair ? in_group_unit(a, local, rank, 0, a.dense_rows)
+              : in_group_tile(a, local, 0, a.dense_rows);
+    c.group = g;
+    c.k0 = __ldg(a.k_group_offsets + g);
+    c.k_end = __ldg(a.k_group_offsets + g + 1);
+    c.k_blocks = c.k_end > c.k0 ? (c.k_end - c.k0 + kBK - 1) / kBK : 0;
+    return c;
+  }
+  if (!kPair) {
+    c = decode_tile(a, u);
+  } else {
+    int32_t g = 0, row0 = 0, row_end = a.dense_rows, local = u;
+    if (a.unit_offsets) {
+      int32_t lo = 0, hi = a.num_groups - 1;
+      while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (__ldg(a.unit_offsets + mid) <= u) lo = mid; else hi = mid - 1;
+      }
+      g = lo;
+      row0 = __ldg(a.group_offsets + g);
+      row_end = __ldg(a.group_offsets + g + 1);
+      local = u - __ldg(a.unit_offsets + g);
+    }
+    c = in_group_unit(a, local, rank, row0, row_end);
+    c.group = g;
+  }
+  c.k0 = 0;
+  c.k_end = 0;
+  c.k_blocks = a.k_blocks;
   return c;
 }
 
@@ -219,6 +274,20 @@ __device__ __forceinline__ bool ctl_wait(SharedCtl* ctl, uint64_t* bar, uint32_t
         return false;
       }
     }
+  }
+}
+
+// Zero K rows kv..63 of a stage's MN-major operand tiles (2 A atoms, 4 B
+// atoms): row k of a {64 MN, 64 K} 128-byte-swizzled atom is the 128 bytes at
+// k * 128 (the swizzle permutes 16-byte pieces within a row), so the tail is one
+// contiguous range per atom.  Warp-collective.
+__device__ __forceinline__ void zero_k_tail(uint32_t sa, uint32_t sb, int32_t kv, int lane) {
+  const uint32_t first = static_cast<uint32_t>(kv) * 128u;
+  const uint32_t n = (kMnAtomBytes - first) / 16u;
+#pragma unroll 1
+  for (int at = 0; at < 6; ++at) {
+    const uint32_t base = (at < 2 ? sa + at * kMnAtomBytes : sb + (at - 2) * kMnAtomBytes) + first;
+    for (uint32_t i = lane; i < n; i += 32) st_shared_zero16(base + 16u * i);
   }
 }
 
@@ -253,6 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  // Contractions over rows (both operands MN-major) may be K-grouped.
+  constexpr bool kKG = kMajor == Major::kABMN;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -281,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (kPair) cluster_sync();  // the peer's barriers exist before any multicast
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
-  const int32_t n_total = num_units<kPair>(args);
+  const int32_t n_total = num_units<kPair, kKG>(args);
   const int32_t u0 = kPair ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x);
   const int32_t ustride = kPair ? static_cast<int32_t>(gridDim.x >> 1) : static_cast<int32_t>(gridDim.x);
 
@@ -292,18 +363,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued = 0;
       bool ok = true;
       for (int32_t t = u0; t < n_total && ok; t += ustride) {
-        const TileCoord tc = unit_tile<kPair>(args, t, rank);
+        const TileCoord tc = unit_tile<kPair, kKG>(args, t, rank);
         const int64_t gbase = static_cast<int64_t>(tc.group) * args.b_group_rows;
-        int32_t b_row0, b_row1;
+        constexpr bool kBMNp = kMajor != Major::kKMajor;
+        // K-major B: a group's weights are b_group_rows further down the N rows.
+        // MN-major B: they are b_group_rows further down the K rows (grouped by
+        // rows), or the contraction itself starts at k0 (K-grouped).
+        int32_t b_row0, b_row1, kb_off = 0;
         if (kEpi == Epi::kSitu) {
           b_row0 = static_cast<int32_t>(gbase + static_cast<int64_t>(tc.n_tile) * 128);
           b_row1 = static_cast<int32_t>(gbase + args.b_up_offset +
                                         static_cast<int64_t>(tc.n_tile) * 128);
+        } else if (kBMNp) {
+          b_row0 = tc.n_tile * kBN;
+          b_row1 = b_row0 + 128;
+          kb_off = (kKG && args.k_group_offsets) ? tc.k0 : static_cast<int32_t>(gbase);
         } else {
           b_row0 = static_cast<int32_t>(gbase + static_cast<int64_t>(tc.n_tile) * kBN);
           b_row1 = b_row0 + 128;
         }
-        for (int32_t kb = 0; kb < args.k_blocks; ++kb) {
+        for (int32_t kb = 0; kb < tc.k_blocks; ++kb) {
           if (!ctl_wait(ctl, &ctl->empty[stage], phase ^ 1u, args.status)) {
             ok = false;
             break;
@@ -314,7 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(full, kStageBytes);
           constexpr bool kAMN = kMajor == Major::kABMN;
           constexpr bool kBMN = kMajor != Major::kKMajor;
-          const int32_t kx = kb * kBK;
+          const int32_t kx = kb * kBK + tc.k0;     // A's K coordinate
+          const int32_t kxb = kb * kBK + kb_off;   // B's K coordinate
           // A (128 rows of the tile); `half` picks one 64-row half for a shared-A unit.
           auto load_a = [&](uint32_t dst, int32_t row, int rows64, bool mcast) {
             for (int j = 0; j < rows64; ++j) {
@@ -335,12 +415,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           auto load_b = [&](uint32_t dst, int32_t row, bool mcast) {
             if (kBMN) {
               for (int j = 0; j < 2; ++j) {
-                if (mcast) tma_load_2d_multicast(dst + j * kMnAtomBytes, &map_b, row + 64 * j, kx, full, 0x3);
-                else tma_load_2d(dst + j * kMnAtomBytes, &map_b, row + 64 * j, kx, full);
+                if (mcast) tma_load_2d_multicast(dst + j * kMnAtomBytes, &map_b, row + 64 * j, kxb, full, 0x3);
+                else tma_load_2d(dst + j * kMnAtomBytes, &map_b, row + 64 * j, kxb, full);
               }
             } else {
-              if (mcast) tma_load_2d_multicast(dst, &map_b, kx, row, full, 0x3);
-              else tma_load_2d(dst, &map_b, kx, row, full);
+              if (mcast) tma_load_2d_multicast(dst, &map_b, kxb, row, full, 0x3);
+              else tma_load_2d(dst, &map_b, kxb, row, full);
             }
           };
           if (!kPair) {
@@ -377,47 +457,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+    // Lane 0 waits and issues.  K-grouped contractions run the whole warp: the
+    // last k-block of a group holds the next group's first rows (or fill) past
+    // k_end, and the warp zeroes those K rows of both operands before the MMAs.
+    if (kKG || lane == 0) {
       uint32_t stage = 0, phase = 0;
       uint32_t local = 0;
       bool ok = true;
+      auto wait = [&](uint64_t* bar, uint32_t par) {
+        int w = 1;
+        if (lane == 0) w = ctl_wait(ctl, bar, par, args.status) ? 1 : 0;
+        if (kKG) w = __shfl_sync(0xFFFFFFFFu, w, 0);
+        return w != 0;
+      };
       for (int32_t t = u0; t < n_total && ok; t += ustride, ++local) {
         const uint32_t acc = local & 1u;
         const uint32_t acc_phase = (local >> 1) & 1u;
-        if (!ctl_wait(ctl, &ctl->acc_empty[acc], acc_phase ^ 1u, args.status)) {
+        if (!wait(&ctl->acc_empty[acc], acc_phase ^ 1u)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kBN;
-        const TileCoord tcm = unit_tile<kPair>(args, t, rank);
+        const TileCoord tcm = unit_tile<kPair, kKG>(args, t, rank);
         const uint32_t idesc = (tcm.row_end - tcm.a_row0 <= 64 ? kIdescHalf : kIdesc) |
                                (kMajor == Major::kABMN ? kAMnBit : 0u) |
                                (kMajor != Major::kKMajor ? kBMnBit : 0u);
-        for (int32_t kb = 0; kb < args.k_blocks; ++kb) {
-          if (!ctl_wait(ctl, &ctl->full[stage], phase, args.status)) {
+        for (int32_t kb = 0; kb < tcm.k_blocks; ++kb) {
+          if (!wait(&ctl->full[stage], phase)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
           const uint32_t sa = smem_u32(smem + stage * kStageBytes);
           const uint32_t sb = sa + kABytes;
-#pragma unroll
-          for (int k = 0; k < kBK / kUK; ++k) {
-            // K-major: 16 K elements = 32 bytes along the row; MN-major: 16 K rows
-            // = 2048 bytes.
-            const uint64_t ad = kMajor == Major::kABMN
-                                    ? sw128_mnmajor_desc(sa + k * 2048, kMnAtomBytes)
-                                    : sw128_kmajor_desc(sa + k * kUK * 2);
-            const uint64_t bd = kMajor != Major::kKMajor
-                                    ? sw128_mnmajor_desc(sb + k * 2048, kMnAtomBytes)
-                                    : sw128_kmajor_desc(sb + k * kUK * 2);
-            umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          if (kKG && args.k_group_offsets) {
+            const int32_t kv = tcm.k_end - (tcm.k0 + kb * kBK);
+            if (kv < kBK) {
+              zero_k_tail(sa, sb, kv, lane);
+              fence_proxy_async_smem();
+            }
+            __syncwarp();
           }
-          if (kPair) {
-            umma_commit_multicast(smem_u32(&ctl->empty[stage]), 0x3);
-          } else {
-            umma_commit(smem_u32(&ctl->empty[stage]));
+          if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < kBK / kUK; ++k) {
+              // K-major: 16 K elements = 32 bytes along the row; MN-major: 16 K
+              // rows = 2048 bytes.
+              const uint64_t ad = kMajor == Major::kABMN
+                                      ? sw128_mnmajor_desc(sa + k * 2048, kMnAtomBytes)
+                                      : sw128_kmajor_desc(sa + k * kUK * 2);
+              const uint64_t bd = kMajor != Major::kKMajor
+                                      ? sw128_mnmajor_desc(sb + k * 2048, kMnAtomBytes)
+                                      : sw128_kmajor_desc(sb + k * kUK * 2);
+              umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            }
+            if (kPair) {
+              umma_commit_multicast(smem_u32(&ctl->empty[stage]), 0x3);
+            } else {
+              umma_commit(smem_u32(&ctl->empty[stage]));
+            }
           }
           if (++stage == kStages) {
             stage = 0;
@@ -425,9 +524,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        umma_commit(smem_u32(&ctl->acc_full[acc]));
+        // A group without rows issues no MMA: the commit arrives at once and the
+        // epilogue writes zeros.
+        if (lane == 0) umma_commit(smem_u32(&ctl->acc_full[acc]));
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         // Drain the MMAs already issued before the tensor memory is freed.
         umma_commit(smem_u32(&ctl->drain));
         mbar_wait(smem_u32(&ctl->drain), 0, nullptr, kDrainLimitNs);
@@ -447,12 +548,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after_sync();
-      const TileCoord tc = unit_tile<kPair>(args, t, rank);
+      const TileCoord tc = unit_tile<kPair, kKG>(args, t, rank);
       // M=64 tiles: only the first 16 lanes of each quarter hold rows (16q + lane).
       const bool half = tc.row_end - tc.a_row0 <= 64;
       const int32_t row = tc.a_row0 + (half ? quarter * 16 + lane : row_in_tile);
       bool valid = row < tc.row_end && (!half || lane < 16);
       int64_t out_row = row;
+      // K-grouped: group g's result starts at output row g * out_group_rows; a
+      // group without rows has a zero result.
+      bool zero = false;
+      if (kKG && args.k_group_offsets) {
+        out_row += static_cast<int64_t>(tc.group) * args.out_group_rows;
+        zero = tc.k_blocks == 0;
+      }
       if (valid && args.out_row_index) {
         out_row = __ldg(args.out_row_index + row);
         valid = out_row >= 0 && out_row < args.out_rows;
@@ -537,7 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t w[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            w[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+            w[i] = zero ? 0u
+                        : pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
           }
           const int64_t col0 = static_cast<int64_t>(tc.n_tile) * kBN + c * 32;
           if (valid) store_row_chunk(dst_row + col0, w, col0, args.n_out);
@@ -727,6 +836,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
   static_assert(kEpi != Epi::kSitu || kMajor == Major::kKMajor,
                 "the SiTU epilogue pairs gate and up rows of a K-major B");
   if (s.a_rows == 0 && !s.tile_offsets) return cudaSuccess;
+  if (s.k_group_offsets && kMajor != Major::kABMN) return cudaErrorInvalidValue;
   CUtensorMap ma, ma64, mb;
   bool ok;
   if (kMajor == Major::kABMN) {
@@ -738,7 +848,10 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
          make_map(&ma64, s.a, s.a_rows, s.K, 64, s.a_ld);
   }
   if (kMajor != Major::kKMajor) {
-    ok = ok && make_map(&mb, s.b, s.K, s.b_rows, 64, s.b_ld);  // B stored [K, N]
+    // B stored [K, N]; grouped by rows, the groups' K-row blocks are stacked.
+    const int64_t b_k_rows =
+        (s.group_offsets && !s.k_group_offsets) ? s.b_group_rows * s.num_groups : s.K;
+    ok = ok && make_map(&mb, s.b, b_k_rows, s.b_rows, 64, s.b_ld);
   } else {
     ok = ok && make_map(&mb, s.b, s.b_rows, s.K, 128, s.b_ld);
   }
@@ -765,6 +878,10 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
   a.gu_in = static_cast<const __nv_bfloat16*>(s.gu_in);
   a.dgu_out = static_cast<__nv_bfloat16*>(s.dgu_out);
   a.split = s.split;
+  a.k_group_offsets = s.k_group_offsets;
+  a.out_group_rows = s.out_group_rows;
+  a.units_per_group = 0;
+  const int64_t m_tiles = (s.a_rows + kBM - 1) / kBM;
   // The shared-memory opt-in is a per-device property of each kernel: set once.
   static bool smem_set[64] = {};
   int dev = 0;
@@ -779,13 +896,16 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     smem_set[dev] = true;
   }
   int clusters = max_pair_clusters<kEpi, kC, kStoreGu, kMajor>(kSmemBytes);
-  if (clusters > 0 && (!s.tile_offsets || s.unit_offsets)) {
+  const int64_t pair_units = (m_tiles / 2) * a.n_tiles + (m_tiles % 2) * ((a.n_tiles + 1) / 2);
+  if (clusters > 0 && (!s.tile_offsets || s.unit_offsets || s.k_group_offsets)) {
     // Clusters of two CTAs sharing a B or an A tile by multicast.
     a.unit_offsets = s.unit_offsets;
-    if (!s.tile_offsets) {
-      const int64_t m = (s.a_rows + kBM - 1) / kBM;
-      const int64_t units = (m / 2) * a.n_tiles + (m % 2) * ((a.n_tiles + 1) / 2);
-      if (units < clusters) clusters = static_cast<int>(units);
+    if (s.k_group_offsets) {
+      a.units_per_group = static_cast<int32_t>(pair_units);
+      const int64_t units = pair_units * s.num_groups;
+      if (units < clusters) clusters = static_cast<int>(units < 1 ? 1 : units);
+    } else if (!s.tile_offsets) {
+      if (pair_units < clusters) clusters = static_cast<int>(pair_units);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
@@ -803,8 +923,12 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
                               mb, a);
   }
   int grid = num_sms;
-  if (!s.tile_offsets) {
-    const int64_t tiles = ((s.a_rows + kBM - 1) / kBM) * a.n_tiles;
+  if (s.k_group_offsets) {
+    a.units_per_group = static_cast<int32_t>(m_tiles * a.n_tiles);
+    const int64_t units = m_tiles * a.n_tiles * s.num_groups;
+    if (units < grid) grid = static_cast<int>(units < 1 ? 1 : units);
+  } else if (!s.tile_offsets) {
+    const int64_t tiles = m_tiles * a.n_tiles;
     if (tiles < grid) grid = static_cast<int>(tiles);
   }
   ffn_gemm_kernel<kEpi, kC, false, kStoreGu, kMajor>
@@ -883,15 +1007,16 @@ cudaError_t launch_gemm_situ_bwd(const GemmShape& s, const SituParams& p, Caps c
 }
 
 cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,
-                               int64_t n_out_gate_up, int64_t n_out_down, int32_t* tile_offsets,
-                               int32_t* units_gate_up, int32_t* units_down, uint32_t* status,
+                               int32_t n_tiles_1, int32_t n_tiles_2, int32_t* tile_offsets,
+                               int32_t* units_1, int32_t* units_2, uint32_t* status,
                                cudaStream_t stream) {
-  const int32_t n_gu = static_cast<int32_t>((n_out_gate_up + 127) / 128);
-  const int32_t n_dn = static_cast<int32_t>((n_out_down + kBN - 1) / kBN);
-  group_tiles_kernel<<<1, 1024, 0, stream>>>(group_offsets, G, R, n_gu, n_dn, tile_offsets,
-                                             units_gate_up, units_down, status);
+  group_tiles_kernel<<<1, 1024, 0, stream>>>(group_offsets, G, R, n_tiles_1, n_tiles_2,
+                                             tile_offsets, units_1, units_2, status);
   return cudaGetLastError();
 }
+
+int32_t gemm_n_tiles_situ(int64_t n_out) { return static_cast<int32_t>((n_out + 127) / 128); }
+int32_t gemm_n_tiles_wide(int64_t n_out) { return static_cast<int32_t>((n_out + kBN - 1) / kBN); }
 
 cudaError_t launch_gather_rows(const void* x, const int32_t* token_index, void* x_perm,
                                int64_t R, int32_t k_eff, int64_t M, uint32_t* status,

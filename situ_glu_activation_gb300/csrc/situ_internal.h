@@ -70,6 +70,14 @@ struct GemmShape {
   // K-major B.
   bool a_mn_major;
   bool b_mn_major;
+  // K-grouped contraction (A and B both MN-major, grouped by K rows): group g
+  // contracts over the K rows k_group_offsets[g] .. k_group_offsets[g+1]-1 of both
+  // operands ([G+1] int32, device) and writes its [a_rows, n_out] result at output
+  // row g * out_group_rows.  K is then the operands' total row count.  With
+  // tile_offsets given, a zero tile_offsets[num_groups] (offsets that failed
+  // validation) makes the GEMM do nothing.
+  const int32_t* k_group_offsets;
+  int64_t out_group_rows;
   // SiTU epilogue: optional bf16 store of the pre-activation (g, u), [rows, 2*split].
   void* gu_store;
   // Backward epilogue: saved (g, u) in, d(g, u) out, both [rows, 2*split] bf16.
@@ -90,12 +98,16 @@ cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
 cudaError_t launch_gemm_situ_bwd(const GemmShape& s, const SituParams& p, Caps caps,
                                  uint32_t* status, int num_sms, cudaStream_t stream);
 
-// Per-group prefixes of m-tiles and of paired units of the gate_up (n_out_gate_up =
-// I output columns) and down (n_out_down = M) GEMMs, plus validation of the offsets.
+// Per-group prefixes of m-tiles and of the paired units of two grouped GEMMs with
+// n_tiles_1 and n_tiles_2 output tiles per m-tile, plus validation of the offsets.
 cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,
-                               int64_t n_out_gate_up, int64_t n_out_down, int32_t* tile_offsets,
-                               int32_t* units_gate_up, int32_t* units_down, uint32_t* status,
+                               int32_t n_tiles_1, int32_t n_tiles_2, int32_t* tile_offsets,
+                               int32_t* units_1, int32_t* units_2, uint32_t* status,
                                cudaStream_t stream);
+// Output tiles per m-tile: of the SiTU GEMM (128 activation columns per tile) and
+// of the plain / backward GEMMs (256 columns per tile), for n_out output columns.
+int32_t gemm_n_tiles_situ(int64_t n_out);
+int32_t gemm_n_tiles_wide(int64_t n_out);
 // x_perm[r, :] = x[token_index[r] / k_eff, :]  (M bf16 columns).
 cudaError_t launch_gather_rows(const void* x, const int32_t* token_index, void* x_perm,
                                int64_t R, int32_t k_eff, int64_t M, uint32_t* status,
@@ -105,7 +117,7 @@ cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, uint32_t* status,
                                          cudaStream_t stream);
 
 // ----- routed-layer combine (combine.cu) --------------------------------------
-// out[t, :] = sum_s w[t, s] * y[t, s, :] in FP32, slot order.
+// out[t, :] = sum_s w[t, s] * y[t, s, :] in FP32, slot order (w == NULL: all 1).
 cudaError_t launch_combine(const void* y, const float* w, void* out, int64_t T, int32_t k_eff,
                            int64_t M, situ_dtype dt, int num_sms, cudaStream_t stream);
 

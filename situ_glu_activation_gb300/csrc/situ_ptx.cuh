@@ -279,6 +279,17 @@ __device__ __forceinline__ void tmem_ld_wait2(uint32_t (&a)[32], uint32_t (&b)[3
                : "memory");
 }
 
+// 16 zero bytes into this CTA's shared memory (generic proxy).
+__device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy accesses (tcgen05.mma operand reads, TMA writes).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 16-byte global store with streaming (evict-first) cache hint.
 __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
