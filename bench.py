@@ -9,7 +9,8 @@ with CUDA events, L2 flushed between steps.  The same JSON line also carries:
   * ``moe``: the routed layer (index build + grouped FFN + combine) on the Zipf
     top-8 64-expert workload and on the Kimi-K3-shaped layer (896 routed + 2
     shared experts) at 512 and 32768 tokens;
-  * ``train``: a training step of the dense FFN (forward keeping gu and h, backward);
+  * ``train``: a training step of the dense FFN (forward keeping gu and h, backward),
+    and (``train.grouped``) of the grouped experts on the Zipf top-8 64-expert workload;
   * ``roofline`` of the dominant kernel (the fused gate_up GEMM);
   * ``e2e``: the public ``situ_ffn_forward`` call with host (pinned) buffers,
     host->device copy of x and device->host copy of y inside the timed region;
@@ -392,6 +393,55 @@ def bench_train(args, dev, peaks, world, flush):
             "launches_per_step": 2 + 4}
 
 
+def bench_moe_train(args, dev, peaks, world, flush):
+    """Training step of the grouped experts (E=64, 16384 tokens top-8 Zipf): expert
+    index, forward that keeps gu and h in expert order, backward for a seeded
+    upstream gradient of the per-route outputs (dx, per-expert dW)."""
+    import torch
+
+    import situ_glu_activation_gb300 as situ
+    from situ_glu_activation_gb300 import workloads as wl
+
+    w = wl.WORKLOADS["grouped"]
+    E = w.num_experts
+    R = w.T * w.k_eff
+    wgu, wd = wl.expert_weights(E, w.M, w.I, seed=0, device=dev)
+    ids = wl.routes(w, seed=0).to(dev)
+    x = wl.normal((w.T, w.M), 1.0, seed=0, device=dev)
+    dy = wl.normal((w.T, w.k_eff, w.M), 1.0, seed=7, device=dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    tix = torch.empty(R, dtype=torch.int32, device=dev)
+    ws_f = torch.empty(situ.moe_workspace_bytes(R, E, w.M, w.I), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(situ.moe_backward_workspace_bytes(R, E, w.M, w.I), dtype=torch.uint8,
+                       device=dev)
+    state = {}
+
+    def step(marks):
+        situ.situ_moe_build_index(ids, E, expert_offsets=off, token_index=tix)
+        y, gu, h = situ.situ_moe_grouped_forward_train(x, off, tix, wgu, wd, w.k_eff, wl.BETA,
+                                                       wl.LINEAR_BETA, workspace=ws_f)
+        if marks:
+            marks[0].record()
+        state["g"] = situ.situ_moe_grouped_backward(x, off, tix, wgu, wd, gu, h, dy, wl.BETA,
+                                                    wl.LINEAR_BETA, workspace=ws_b)
+
+    per_step, (t_fwd, t_bwd) = timed_steps(step, args.steps, args.warmup, flush, world, inner=1)
+    state.clear()
+    ms = mean(per_step)
+    flop_f = 6.0 * R * w.M * w.I
+    flop_b = 12.0 * R * w.M * w.I
+    out = {"workload": w.name + ", training step (index, forward keeping gu and h, backward)",
+           "ms": ms, "forward_ms": mean(t_fwd), "backward_ms": mean(t_bwd),
+           "tokens_per_s": w.T / (ms * 1e-3), "routes": R,
+           "tflops": (flop_f + flop_b) / (ms * 1e-3) / 1e12,
+           "backward_tflops": flop_b / (mean(t_bwd) * 1e-3) / 1e12,
+           "tc_frac": (flop_f + flop_b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+           "launches_per_step": 3 + 4 + 8}
+    del wgu, wd, ws_f, ws_b, dy, x
+    torch.cuda.empty_cache()
+    return out
+
+
 def cpu_baseline(seconds: float, rows_hint: int = 0):
     """The FP64 oracle (as it stands) on a bounded sample of the dense workload's
     rows: rows/s = tokens/s on the host cores."""
@@ -493,6 +543,8 @@ def run_situ(args):
             res = bench_act(args, dev, peaks, world, flush)
         elif args.suite == "train":
             res = bench_train(args, dev, peaks, world, flush)
+        elif args.suite == "grouped_train":
+            res = bench_moe_train(args, dev, peaks, world, flush)
         else:
             res = bench_moe(args, dev, peaks, world, flush, [args.suite])[args.suite]
         if rank == 0:
@@ -511,7 +563,10 @@ def run_situ(args):
     act = bench_act(args, dev, peaks, world, flush) if args.suite == "full" else None
     moe = (bench_moe(args, dev, peaks, world, flush, ["grouped", "k3_decode", "k3_prefill"])
            if args.suite == "full" else None)
-    train = bench_train(args, dev, peaks, world, flush) if args.suite == "full" else None
+    train = None
+    if args.suite == "full":
+        train = bench_train(args, dev, peaks, world, flush)
+        train["grouped"] = bench_moe_train(args, dev, peaks, world, flush)
     status = situ.device_status(clear=True)
 
     achieved = dense["gate_up_tflops"]
@@ -588,7 +643,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["situ", "reference"], default="situ")
     ap.add_argument("--suite", default="full",
                     choices=["full", "dense", "act", "grouped", "k3_decode", "k3_prefill",
-                             "k3_prefill_slice", "train"],
+                             "k3_prefill_slice", "train", "grouped_train"],
                     help="full: the headline line with every sub-result; dense: the headline "
                          "only; any other name: that workload alone (for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

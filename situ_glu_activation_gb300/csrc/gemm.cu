@@ -64,7 +64,10 @@ constexpr uint32_t kIdescHalf = idesc_bf16_f32(64, kBN);
 // backward multiplies by it untransposed; kABMN -- A stored [K, rows] and B
 // stored [K, N], e.g. dy and h when the weight gradient contracts over tokens.
 // MN-major tiles arrive as {64, 64} boxes (8 KB): A takes two, B four.
-enum class Major { kKMajor = 0, kBMN = 1, kABMN = 2 };
+// kABMNGrouped -- the kABMN layouts with a K-grouped schedule: each group (expert)
+// contracts over its own row range (per-expert weight gradients).
+enum class Major { kKMajor = 0, kBMN = 1, kABMN = 2, kABMNGrouped = 3 };
+__host__ __device__ constexpr bool a_mn_major(Major m) { return m == Major::kABMN || m == Major::kABMNGrouped; }
 constexpr uint32_t kAMnBit = 1u << 15, kBMnBit = 1u << 16;
 constexpr uint32_t kMnAtomBytes = 64 * 64 * 2;
 
@@ -210,7 +213,7 @@ __device__ __forceinline__ TileCoord in_group_unit(const Args& a, int32_t local,
 
 template <bool kPair, bool kKG>
 __device__ __forceinline__ int32_t num_units(const Args& a) {
-  if (kKG && a.k_group_offsets) {
+  if (kKG) {
     if (a.tile_offsets && __ldg(a.tile_offsets + a.num_groups) == 0) return 0;
     return a.num_groups * a.units_per_group;
   }
@@ -222,7 +225,7 @@ __device__ __forceinline__ int32_t num_units(const Args& a) {
 template <bool kPair, bool kKG>
 __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_t rank) {
   TileCoord c;
-  if (kKG && a.k_group_offsets) {
+  if (kKG) {
     // Every group has the same output tiles; its K range is its row range.
     const int32_t g = u / a.units_per_group;
     const int32_t local = u - g * a.units_per_group;
@@ -323,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
   // Contractions over rows (both operands MN-major) may be K-grouped.
-  constexpr bool kKG = kMajor == Major::kABMN;
+  constexpr bool kKG = kMajor == Major::kABMNGrouped;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -377,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (kBMNp) {
           b_row0 = tc.n_tile * kBN;
           b_row1 = b_row0 + 128;
-          kb_off = (kKG && args.k_group_offsets) ? tc.k0 : static_cast<int32_t>(gbase);
+          kb_off = kKG ? tc.k0 : static_cast<int32_t>(gbase);
         } else {
           b_row0 = static_cast<int32_t>(gbase + static_cast<int64_t>(tc.n_tile) * kBN);
           b_row1 = b_row0 + 128;
@@ -391,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = smem_u32(smem + stage * kStageBytes);
           const uint32_t sb = sa + kABytes;
           mbar_arrive_expect_tx(full, kStageBytes);
-          constexpr bool kAMN = kMajor == Major::kABMN;
+          constexpr bool kAMN = a_mn_major(kMajor);
           constexpr bool kBMN = kMajor != Major::kKMajor;
           const int32_t kx = kb * kBK + tc.k0;     // A's K coordinate
           const int32_t kxb = kb * kBK + kb_off;   // B's K coordinate
@@ -481,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem_base + acc * kBN;
         const TileCoord tcm = unit_tile<kPair, kKG>(args, t, rank);
         const uint32_t idesc = (tcm.row_end - tcm.a_row0 <= 64 ? kIdescHalf : kIdesc) |
-                               (kMajor == Major::kABMN ? kAMnBit : 0u) |
+                               (a_mn_major(kMajor) ? kAMnBit : 0u) |
                                (kMajor != Major::kKMajor ? kBMnBit : 0u);
         for (int32_t kb = 0; kb < tcm.k_blocks; ++kb) {
           if (!wait(&ctl->full[stage], phase)) {
@@ -491,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after_sync();
           const uint32_t sa = smem_u32(smem + stage * kStageBytes);
           const uint32_t sb = sa + kABytes;
-          if (kKG && args.k_group_offsets) {
+          if (kKG) {
             const int32_t kv = tcm.k_end - (tcm.k0 + kb * kBK);
             if (kv < kBK) {
               zero_k_tail(sa, sb, kv, lane);
@@ -504,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < kBK / kUK; ++k) {
               // K-major: 16 K elements = 32 bytes along the row; MN-major: 16 K
               // rows = 2048 bytes.
-              const uint64_t ad = kMajor == Major::kABMN
+              const uint64_t ad = a_mn_major(kMajor)
                                       ? sw128_mnmajor_desc(sa + k * 2048, kMnAtomBytes)
                                       : sw128_kmajor_desc(sa + k * kUK * 2);
               const uint64_t bd = kMajor != Major::kKMajor
@@ -557,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // K-grouped: group g's result starts at output row g * out_group_rows; a
       // group without rows has a zero result.
       bool zero = false;
-      if (kKG && args.k_group_offsets) {
+      if (kKG) {
         out_row += static_cast<int64_t>(tc.group) * args.out_group_rows;
         zero = tc.k_blocks == 0;
       }
@@ -836,10 +839,11 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
   static_assert(kEpi != Epi::kSitu || kMajor == Major::kKMajor,
                 "the SiTU epilogue pairs gate and up rows of a K-major B");
   if (s.a_rows == 0 && !s.tile_offsets) return cudaSuccess;
-  if (s.k_group_offsets && kMajor != Major::kABMN) return cudaErrorInvalidValue;
+  if ((s.k_group_offsets != nullptr) != (kMajor == Major::kABMNGrouped))
+    return cudaErrorInvalidValue;
   CUtensorMap ma, ma64, mb;
   bool ok;
-  if (kMajor == Major::kABMN) {
+  if (a_mn_major(kMajor)) {
     // A stored [K, rows]: {64 rows, 64 K} boxes.
     ok = make_map(&ma, s.a, s.K, s.a_rows, 64, s.a_ld);
     ma64 = ma;
@@ -967,6 +971,9 @@ cudaError_t launch_gemm_situ(const GemmShape& s, const SituParams& p, Caps caps,
 
 cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
                               cudaStream_t stream) {
+  if (s.a_mn_major && s.b_mn_major && s.k_group_offsets)
+    return launch<Epi::kPlain, Caps::kBoth, false, Major::kABMNGrouped>(s, SituParams{}, status,
+                                                                       num_sms, stream);
   if (s.a_mn_major && s.b_mn_major)
     return launch<Epi::kPlain, Caps::kBoth, false, Major::kABMN>(s, SituParams{}, status, num_sms,
                                                                 stream);
