@@ -68,6 +68,15 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         ("oracle_ffn_backward", [vp, ci, vp, vp, ci, vp, ci, dp, dp, dp, dp, i64, i64, i64, d, d],
          ci),
         ("oracle_num_threads", [], ci),
+        ("oracle_e4m3_decode", [ctypes.c_uint32], d),
+        ("oracle_e4m3_encode", [d], ctypes.c_uint32),
+        ("oracle_e8m0_decode", [ctypes.c_uint32], d),
+        ("oracle_mx_scale_code", [d], ctypes.c_uint32),
+        ("oracle_mx_quantize", [vp, ci, i64, i64, vp, vp], ci),
+        ("oracle_mx_dequantize", [vp, vp, i64, i64, dp], ci),
+        ("oracle_e4m3_encode_array", [dp, i64, vp], ci),
+        ("oracle_e4m3_decode_array", [vp, i64, dp], ci),
+        ("oracle_round_bf16_array", [dp, i64, vp], ci),
     ]:
         fn = getattr(lib, name)
         fn.argtypes = args
@@ -237,6 +246,66 @@ class Oracle:
                                                     _ptr(dwd), T, k_eff, E, M, I, float(beta),
                                                     float(linear_beta)), "moe_grouped_backward")
         return dx, dwg, dwd
+
+    # ----- MXFP8 (OCP MX v1.0: E4M3 elements, E8M0 scales per 32) -----------
+    def e4m3_decode(self, codes) -> np.ndarray:
+        c = np.ascontiguousarray(codes, dtype=np.uint8)
+        out = np.empty(c.shape)
+        _check(self.lib.oracle_e4m3_decode_array(_ptr(c), c.size, _ptr(out)), "e4m3_decode")
+        return out
+
+    def e4m3_encode(self, v) -> np.ndarray:
+        a = np.ascontiguousarray(v, dtype=np.float64)
+        out = np.empty(a.shape, dtype=np.uint8)
+        _check(self.lib.oracle_e4m3_encode_array(_ptr(a), a.size, _ptr(out)), "e4m3_encode")
+        return out
+
+    def e8m0_decode(self, c) -> float:
+        return self.lib.oracle_e8m0_decode(int(c))
+
+    def mx_scale_code(self, amax) -> int:
+        return int(self.lib.oracle_mx_scale_code(float(amax)))
+
+    def round_bf16(self, v) -> np.ndarray:
+        """Round doubles to bfloat16 (RNE); returns the bit patterns (uint16)."""
+        a = np.ascontiguousarray(v, dtype=np.float64)
+        out = np.empty(a.shape, dtype=np.uint16)
+        _check(self.lib.oracle_round_bf16_array(_ptr(a), a.size, _ptr(out)), "round_bf16")
+        return out
+
+    def mx_quantize(self, a):
+        """MX quantization of a [R, K] tensor: (codes uint8 [R, K], scales uint8
+        [R, K/32])."""
+        src, dt = _as_input(a)
+        R, K = src.shape
+        codes = np.empty((R, K), dtype=np.uint8)
+        scales = np.empty((R, K // 32), dtype=np.uint8)
+        _check(self.lib.oracle_mx_quantize(_ptr(src), dt, R, K, _ptr(codes), _ptr(scales)),
+               "mx_quantize")
+        return codes, scales
+
+    def mx_dequantize(self, codes, scales) -> np.ndarray:
+        c = np.ascontiguousarray(codes, dtype=np.uint8)
+        sc = np.ascontiguousarray(scales, dtype=np.uint8)
+        R, K = c.shape
+        out = np.empty((R, K))
+        _check(self.lib.oracle_mx_dequantize(_ptr(c), _ptr(sc), R, K, _ptr(out)), "mx_dequantize")
+        return out
+
+    def mx_ffn_forward(self, xq, wguq, wdq, beta=4.0, linear_beta=25.0):
+        """The SiTU-GLU FFN with MXFP8 operands: each argument is a (codes, scales)
+        pair.  gu and h in FP64 on the decoded x and W_gate_up; h cast to bf16 (the
+        pages' cast back to the input dtype), MX-quantized as the down projection's
+        input, and y = dequant(h) dequant(W_down)^T in FP64.  Returns
+        (y [R, M], h_bf16 bits [R, I], (h codes, h scales))."""
+        x = self.mx_dequantize(*xq)
+        wgu = self.mx_dequantize(*wguq)
+        wd = self.mx_dequantize(*wdq)
+        _, h = self.ffn_forward(x, wgu, wd, beta, linear_beta, want_h=True)
+        hb = self.round_bf16(h)
+        hq = self.mx_quantize(hb)
+        y = self.mx_dequantize(*hq) @ wd.T  # library matmul of the decoded values
+        return y, hb, hq
 
     def moe_combine(self, y: np.ndarray, w: np.ndarray) -> np.ndarray:
         """y [T, k_eff, M] (float64), w [T, k_eff] -> out [T, M] = sum_s w[t,s] y[t,s]."""

@@ -459,6 +459,156 @@ int oracle_moe_combine(const double* y, const void* w, int w_dt, double* out, in
   return ORACLE_OK;
 }
 
+/* ---------------------------------------------------------------------------
+ * MXFP8: the block-scaled 8-bit format of the OCP Microscaling Formats (MX) v1.0
+ * specification.  The SiTU-GLU chapter ("Pourquoi un plafond doux", "Ou SiTU-GLU
+ * est utilise") motivates the activation's bound by experts that run in MXFP8 /
+ * MXFP4; the format is the specification's:
+ *   element E4M3: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent field
+ *     0 holds the subnormals m/8 * 2^-6; there are no infinities, and exponent 15
+ *     with mantissa 7 is NaN, so the largest magnitude is 1.75 * 2^8 = 448;
+ *   scale E8M0: an exponent alone, code c standing for 2^(c - 127) (255 is NaN);
+ *   a block of 32 consecutive elements shares one scale X = 2^(floor(log2 amax) - 8),
+ *     amax the block's largest magnitude and 8 the largest exponent of E4M3; each
+ *     element is stored as v / X rounded to E4M3, magnitudes past 448 clamped to 448.
+ * Readings where the specification leaves a choice: rounding is to nearest with
+ * ties to the even mantissa; a block of zeros (log2 0 = -inf) and any scale
+ * exponent below -127 take the smallest scale 2^-127, exponents above 127 the
+ * largest; an element that rounds to zero keeps its sign bit.
+ * ------------------------------------------------------------------------- */
+double oracle_e4m3_decode(uint32_t code) {
+  const uint32_t c = code & 0xFFu;
+  const double sign = (c & 0x80u) ? -1.0 : 1.0;
+  const int e = (int)((c >> 3) & 0xFu), m = (int)(c & 7u);
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) return sign * ldexp((double)m, -9);  /* m/8 * 2^-6 */
+  return sign * ldexp(8.0 + m, e - 10);             /* (1 + m/8) * 2^(e-7) */
+}
+
+uint32_t oracle_e4m3_encode(double v) {
+  const uint32_t s = signbit(v) ? 0x80u : 0u;
+  const double a = fabs(v);
+  if (isnan(v)) return s | 0x7Fu;
+  if (a == 0.0) return s;
+  /* The quantum of a's binade (3 mantissa bits); below 2^-6 the subnormal
+   * quantum 2^-9.  a / q is exact, so the rounding is the only rounding. */
+  int ea;
+  frexp(a, &ea);
+  int fl = ea - 1; /* floor(log2 a) */
+  if (fl < -6) fl = -6;
+  const double r = nearbyint(a / ldexp(1.0, fl - 3)) * ldexp(1.0, fl - 3);
+  if (r == 0.0) return s;
+  if (r >= 448.0) return s | 0x7Eu; /* clamped to the largest magnitude */
+  int er;
+  frexp(r, &er);
+  const int flr = er - 1;
+  if (flr < -6) return s | (uint32_t)(r / ldexp(1.0, -9)); /* subnormal: m * 2^-9 */
+  const uint32_t mant = (uint32_t)(r / ldexp(1.0, flr - 3)) - 8u;
+  return s | ((uint32_t)(flr + 7) << 3) | mant;
+}
+
+double oracle_e8m0_decode(uint32_t code) {
+  const uint32_t c = code & 0xFFu;
+  return c == 255u ? NAN : ldexp(1.0, (int)c - 127);
+}
+
+/* Scale code of a block whose largest magnitude is amax. */
+uint32_t oracle_mx_scale_code(double amax) {
+  if (!(amax > 0.0)) return 0u;
+  int e;
+  frexp(amax, &e);
+  int x = (e - 1) - 8;
+  if (x < -127) x = -127;
+  if (x > 127) x = 127;
+  return (uint32_t)(x + 127);
+}
+
+/* MX quantization of a row-major [R, K] tensor (K a multiple of 32): codes
+ * [R, K] E4M3, scales [R, K/32] E8M0, block b of row r = columns 32b .. 32b+31. */
+int oracle_mx_quantize(const void* src, int dt, int64_t R, int64_t K, uint8_t* codes,
+                       uint8_t* scales) {
+  if (!oracle_dtype_ok(dt) || R < 0 || K <= 0 || K % 32 != 0) return ORACLE_BAD_ARG;
+  if (R == 0) return ORACLE_OK;
+  if (!src || !codes || !scales) return ORACLE_BAD_ARG;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < R; ++r) {
+    for (int64_t b = 0; b < K / 32; ++b) {
+      double amax = 0.0;
+      for (int64_t i = 0; i < 32; ++i) {
+        const double a = fabs(oracle_load(src, dt, r * K + 32 * b + i));
+        if (a > amax) amax = a;
+      }
+      const uint32_t c = oracle_mx_scale_code(amax);
+      const double X = oracle_e8m0_decode(c);
+      scales[r * (K / 32) + b] = (uint8_t)c;
+      for (int64_t i = 0; i < 32; ++i)
+        codes[r * K + 32 * b + i] = (uint8_t)oracle_e4m3_encode(oracle_load(src, dt, r * K + 32 * b + i) / X);
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* The values an MX tensor stands for: code * scale of its block, in FP64. */
+int oracle_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t R, int64_t K,
+                         double* out) {
+  if (R < 0 || K <= 0 || K % 32 != 0) return ORACLE_BAD_ARG;
+  if (R == 0) return ORACLE_OK;
+  if (!codes || !scales || !out) return ORACLE_BAD_ARG;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < R; ++r)
+    for (int64_t k = 0; k < K; ++k)
+      out[r * K + k] = oracle_e4m3_decode(codes[r * K + k]) * oracle_e8m0_decode(scales[r * (K / 32) + k / 32]);
+  return ORACLE_OK;
+}
+
+/* Elementwise E4M3 encode / decode of arrays (for the tests). */
+int oracle_e4m3_encode_array(const double* v, int64_t n, uint8_t* out) {
+  if (n < 0 || (n > 0 && (!v || !out))) return ORACLE_BAD_ARG;
+  for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)oracle_e4m3_encode(v[i]);
+  return ORACLE_OK;
+}
+
+int oracle_e4m3_decode_array(const uint8_t* c, int64_t n, double* out) {
+  if (n < 0 || (n > 0 && (!c || !out))) return ORACLE_BAD_ARG;
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_decode(c[i]);
+  return ORACLE_OK;
+}
+
+/* bfloat16 rounding of doubles, to nearest with ties to the even last bit: the
+ * cast of h back to the input dtype ([dense] "SiTU-GLU: one split, two softly
+ * bounded branches").  bf16 keeps 8 significant bits down to 2^-126 and the
+ * fixed quantum 2^-133 below; magnitudes that round past the largest finite value
+ * become infinities.  Returned as bit patterns. */
+int oracle_round_bf16_array(const double* v, int64_t n, uint16_t* out) {
+  if (n < 0 || (n > 0 && (!v || !out))) return ORACLE_BAD_ARG;
+  for (int64_t i = 0; i < n; ++i) {
+    const double a = fabs(v[i]);
+    const uint16_t s = signbit(v[i]) ? 0x8000u : 0u;
+    if (isnan(v[i])) {
+      out[i] = (uint16_t)(s | 0x7FC0u);
+      continue;
+    }
+    double r = a;
+    if (a != 0.0 && !isinf(a)) {
+      int e;
+      frexp(a, &e);
+      int fl = e - 1;
+      if (fl < -126) fl = -126;
+      const double q = ldexp(1.0, fl - 7);
+      r = nearbyint(a / q) * q;
+    }
+    if (r >= ldexp(1.0, 128)) {
+      out[i] = (uint16_t)(s | 0x7F80u);
+      continue;
+    }
+    const float f = (float)r; /* exact: r is a bf16 value */
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    out[i] = (uint16_t)(s | (uint16_t)((bits >> 16) & 0x7FFFu));
+  }
+  return ORACLE_OK;
+}
+
 /* Number of threads the oracle's parallel loops use. */
 int oracle_num_threads(void) {
 #ifdef _OPENMP

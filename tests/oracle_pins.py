@@ -435,6 +435,167 @@ def pin_grouped_backward(o):
     assert not gdwg[1].any() and not gdwd[1].any()
 
 
+def _e4m3_reference_grid():
+    """Every finite E4M3 value written out from its definition (sign, 4-bit biased
+    exponent, 3-bit mantissa, subnormals m/8 * 2^-6, the all-ones pattern NaN), by
+    enumeration rather than through the oracle."""
+    vals = {}
+    for code in range(256):
+        e, m = (code >> 3) & 15, code & 7
+        if e == 15 and m == 7:
+            continue
+        mag = (m / 8.0) * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+        vals[code] = -mag if code & 0x80 else mag
+    return vals
+
+
+def pin_e4m3_codes(o):
+    """E4M3 decoding against the format's definition for all 256 codes: the printed
+    landmarks (1.0 = 0x38, 448 the largest, 2^-6 the smallest normal, 2^-9 the
+    smallest subnormal), NaN only at S.1111.111, and encode(decode(c)) = c for every
+    finite code (no two codes share a value but +0 / -0)."""
+    grid = _e4m3_reference_grid()
+    dec = o.e4m3_decode(np.arange(256, dtype=np.uint8))
+    for c in range(256):
+        if c in grid:
+            assert dec[c] == grid[c], hex(c)
+        else:
+            assert np.isnan(dec[c]), hex(c)
+    assert dec[0x38] == 1.0 and dec[0x7E] == 448.0 and dec[0x08] == 2.0 ** -6
+    assert dec[0x01] == 2.0 ** -9 and dec[0xB8] == -1.0 and dec[0x3C] == 1.5
+    codes = np.array(sorted(grid), dtype=np.uint8)
+    assert np.array_equal(o.e4m3_encode(dec[codes]), codes)
+    pos = np.array([grid[c] for c in range(0x7F)])
+    assert (np.diff(pos) > 0).all()  # monotone in the code
+
+
+def _brute_e4m3(x, pos):
+    """Code of the nearest finite E4M3 value to x by brute force over the positive
+    grid `pos` (list of (value, code)): ties to the even mantissa, magnitudes from
+    448 up clamped to 448, the sign bit kept."""
+    a = abs(x)
+    if a >= 448.0:
+        want = 0x7E
+    else:
+        d = [abs(a - p[0]) for p in pos]
+        best = min(d)
+        cands = [pos[i][1] for i in range(len(pos)) if d[i] == best]
+        want = cands[0] if len(cands) == 1 else [k for k in cands if k % 2 == 0][0]
+    if x < 0 or (x == 0 and np.signbit(x)):
+        want |= 0x80
+    return want
+
+
+def pin_e4m3_rounding(o):
+    """Rounding to E4M3 by brute force: the nearest finite value of the enumerated
+    grid, ties to the even mantissa, magnitudes from 448 up clamped to 448, tiny
+    values to a signed zero."""
+    grid = _e4m3_reference_grid()
+    pos = sorted((v, c) for c, v in grid.items() if c < 0x80)
+    rng = np.random.default_rng(40)
+    v = np.concatenate([rng.uniform(-500, 500, 3000), rng.uniform(-0.05, 0.05, 3000),
+                        np.array([p[0] for p in pos]) * 1.0,
+                        [(pos[i][0] + pos[i + 1][0]) / 2 for i in range(len(pos) - 1)],
+                        [448.0, 449.0, 464.0, 1e9, -1e9, 2.0 ** -10, -(2.0 ** -10), 2.0 ** -11]])
+    got = o.e4m3_encode(v)
+    for x, c in zip(v, got):
+        assert int(c) == _brute_e4m3(x, pos), (x, hex(int(c)))
+
+
+def pin_mx_scale(o):
+    """The block scale 2^(floor(log2 amax) - 8): amax in [2^e, 2^(e+1)) gives code
+    e - 8 + 127, so the block's largest scaled magnitude lies in [256, 512); zero
+    blocks and exponents below -127 take code 0."""
+    for e in (-100, -9, -1, 0, 1, 6, 7, 8, 100):
+        for f in (1.0, 1.5, 1.999):
+            assert o.mx_scale_code(f * 2.0 ** e) == e - 8 + 127
+    assert o.mx_scale_code(0.0) == 0
+    assert o.mx_scale_code(2.0 ** -130) == 0
+    assert o.mx_scale_code(2.0 ** 200) == 254
+    assert o.e8m0_decode(127) == 1.0 and o.e8m0_decode(0) == 2.0 ** -127
+    assert np.isnan(o.e8m0_decode(255))
+
+
+def pin_mx_quantize(o):
+    """MX quantization of bf16 rows against its definition, recomputed here with the
+    enumerated E4M3 grid: per 32-column block the scale from the largest magnitude,
+    then each element's nearest grid value (clamped to 448) times the scale; plus
+    the error bound |dequant - v| <= max(2^-3 |v|, 2^-10 X) (clamping costs at most
+    an eighth, rounding a sixteenth, the subnormal quantum 2^-9 X)."""
+    rng = np.random.default_rng(41)
+    x = rng.normal(0, 3, (6, 96))
+    x[0, :32] = 0.0                     # a zero block
+    x[1, 32:64] *= 1e-38                # a block of subnormal bf16 values
+    x[2, 64:96] = 1.9 * 2.0 ** 5        # clamping: 1.9 * 256 > 448 after scaling
+    x[3, 5] = 5000.0                    # one outlier flattens the rest of its block
+    xb = o.round_bf16(x)
+    xf = (xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    codes, scales = o.mx_quantize(xb)
+    grid = _e4m3_reference_grid()
+    pos = sorted((v, c) for c, v in grid.items() if c < 0x80)
+    deq = o.mx_dequantize(codes, scales)
+    for r in range(6):
+        for b in range(3):
+            blk = xf[r, 32 * b:32 * b + 32]
+            amax = np.abs(blk).max()
+            e = int(np.floor(np.log2(amax))) - 8 if amax > 0 else -127
+            e = max(-127, min(127, e))
+            assert scales[r, b] == e + 127
+            X = 2.0 ** e
+            for i, v in enumerate(blk):
+                assert codes[r, 32 * b + i] == _brute_e4m3(v / X, pos), (r, b, i, v)
+                err = abs(deq[r, 32 * b + i] - v)
+                assert err <= max(2.0 ** -3 * abs(v), 2.0 ** -10 * X), (r, b, i, v)
+    assert (codes[0, :32] == 0).all() and scales[0, 0] == 0
+    assert scales[1, 1] == 0
+    assert (np.abs(deq[2, 64:96]) == 448.0 * 2.0 ** -3).all()   # clamped: 1.9 * 2^5 -> 448 * 2^-3
+
+
+def pin_round_bf16(o):
+    """bf16 rounding against the bit-level rule on float32 inputs (add 0x7FFF plus
+    the kept last bit, drop 16 bits), including ties; doubles between two bf16
+    values round to the nearer one (no double rounding through float32)."""
+    rng = np.random.default_rng(42)
+    f = rng.normal(0, 10, 5000).astype(np.float32)
+    bits = f.view(np.uint32).astype(np.uint64)
+    ties = ((rng.integers(0, 2 ** 15, 200, dtype=np.uint64) << 16) | 0x8000).astype(np.uint32)
+    allf = np.concatenate([f, ties.view(np.float32)]).astype(np.float32)
+    bits = allf.view(np.uint32).astype(np.uint64)
+    want = ((bits + 0x7FFF + ((bits >> 16) & 1)) >> 16).astype(np.uint16)
+    assert np.array_equal(o.round_bf16(allf.astype(np.float64)), want)
+    # 1 + 2^-8 + 2^-30 is above the tie between 1 and 1 + 2^-7: rounds up; through
+    # float32 it would first become the tie 1 + 2^-8 and then round down to 1.
+    assert o.round_bf16(np.array([1.0 + 2.0 ** -8 + 2.0 ** -30]))[0] == 0x3F81
+
+
+def pin_mx_ffn_exact_inputs(o):
+    """The MX FFN on operands whose MX quantization is exact (every block's values
+    on the E4M3 grid times a power of two, its largest magnitude in the top binade)
+    equals the plain FFN on those values up to the bf16 cast and MX quantization of
+    h, which are applied to the plain FFN's h here by the pinned functions."""
+    rng = np.random.default_rng(43)
+    grid = np.array(sorted(v for c, v in _e4m3_reference_grid().items() if c < 0x80))
+    def exact(shape, e):
+        v = rng.choice(grid[grid >= 2.0 ** -3], shape) * rng.choice([-1.0, 1.0], shape)
+        v = v.reshape(shape[0], -1, 32)
+        v[:, :, 0] = 448.0  # top binade: the block scale is 2^0 before the 2^e factor
+        return (v * 2.0 ** e).reshape(shape)
+    M, I, R = 64, 96, 5
+    x = exact((R, M), -8)
+    wgu = exact((2 * I, M), -10)
+    wd = exact((M, I), -11)
+    xq, wguq, wdq = o.mx_quantize(x), o.mx_quantize(wgu), o.mx_quantize(wd)
+    for a, q in ((x, xq), (wgu, wguq), (wd, wdq)):
+        assert np.array_equal(o.mx_dequantize(*q), a)
+    y, hb, (hc, hs) = o.mx_ffn_forward(xq, wguq, wdq)
+    _, h = o.ffn_forward(x, wgu, wd, want_h=True)
+    assert np.array_equal(hb, o.round_bf16(h))
+    hc2, hs2 = o.mx_quantize(hb)
+    assert np.array_equal(hc, hc2) and np.array_equal(hs, hs2)
+    ref = o.mx_dequantize(hc2, hs2) @ wd.T
+    np.testing.assert_allclose(y, ref, rtol=1e-13, atol=1e-13)
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_swiglu_gate_and_gaps,
@@ -458,6 +619,12 @@ ALL_PINS = [
     pin_ffn_backward_structure,
     pin_ffn_backward_finite_differences,
     pin_grouped_backward,
+    pin_e4m3_codes,
+    pin_e4m3_rounding,
+    pin_mx_scale,
+    pin_mx_quantize,
+    pin_round_bf16,
+    pin_mx_ffn_exact_inputs,
 ]
 
 

@@ -69,6 +69,15 @@ MUTANTS = {
     "grouped_bwd_dx_overwrites_slot": ("dx[t * M + k] += acc;", "dx[t * M + k] = acc;"),
     "grouped_bwd_dw_token_row": ("dwg_e[n * M + k] += dgu[n] * oracle_load(x, x_dt, t * M + k);",
                                 "dwg_e[n * M + k] += dgu[n] * oracle_load(x, x_dt, k);"),
+    "mx_scale_emax_7": ("int x = (e - 1) - 8;", "int x = (e - 1) - 7;"),
+    "mx_scale_ceil": ("int x = (e - 1) - 8;", "int x = e - 8;"),
+    "e4m3_truncates": ("const double r = nearbyint(a / ldexp(1.0, fl - 3)) * ldexp(1.0, fl - 3);",
+                       "const double r = floor(a / ldexp(1.0, fl - 3)) * ldexp(1.0, fl - 3);"),
+    "e4m3_no_clamp": ("if (r >= 448.0) return s | 0x7Eu; /* clamped", "if (r >= 1e300) return s | 0x7Eu; /* clamped"),
+    "e4m3_subnormal_quantum": ("if (fl < -6) fl = -6;", "if (fl < -7) fl = -7;"),
+    "e4m3_bias_8": ("return sign * ldexp(8.0 + m, e - 10);", "return sign * ldexp(8.0 + m, e - 11);"),
+    "mx_block_scale_of_wrong_block": ("scales[r * (K / 32) + k / 32]", "scales[r * (K / 32) + k / 64]"),
+    "bf16_round_truncates": ("r = nearbyint(a / q) * q;", "r = floor(a / q) * q;"),
     "combine_wrong_weight": ("oracle_load(w, w_dt, t * k_eff + k) * y[(t * k_eff + k) * M + m]",
                              "oracle_load(w, w_dt, t * k_eff) * y[(t * k_eff + k) * M + m]"),
     "combine_dropped_slot": ("for (int32_t k = 0; k < k_eff; ++k)\n        s +=",
