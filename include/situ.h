@@ -405,6 +405,93 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
                                       float linear_beta, situ_dtype dt, void* stream);
 
 /* -------------------------------------------------------------------------
+ * MXFP8 experts -- the SiTU-GLU FFN with block-scaled 8-bit operands.
+ *
+ * The "SiTU-GLU" chapter ("Pourquoi un plafond doux"; "Ou SiTU-GLU est utilise")
+ * motivates the activation's +/-100 bound by experts that run in MXFP8 / MXFP4.
+ * The format is the OCP Microscaling (MX) v1.0 MXFP8: E4M3 element codes (largest
+ * magnitude 448), one E8M0 scale 2^(floor(log2 amax) - 8) per 32 consecutive
+ * elements along K (amax the block's largest magnitude; zero blocks take 2^-127);
+ * each code is the element divided by its scale, rounded to nearest even, clamped
+ * to 448.  Quantization reads bf16 values, so every rounding decision is taken on
+ * the bf16 input.
+ *
+ * Codes keep the operand's row-major layout (K contiguous).  Scales are stored
+ * in the tiles the block-scaled MMA consumes:
+ *   activations (x, h): per 128-row tile and 128-wide K stage, 512 bytes, byte
+ *     l * 16 + g * 4 + k = scale of row 32 g + l of the tile, 32-wide block k of the
+ *     stage; tiles ordered (row tile, K stage); situ_mx_act_scales_size bytes.
+ *   weights: per (expert, n-tile, K stage) 1024 bytes holding the n-tile's 192
+ *     rows as rows 0..127 and 128..191 of two such 512-byte tiles.  SITU_MX_GATE_UP
+ *     (W_gate_up [E, 2I, M], K = M): n-tile t = gate rows 96t..96t+95 then up rows
+ *     I + 96t..; SITU_MX_DOWN (W_down [E, M, I], K = I): n-tile t = rows
+ *     192t..192t+191.  situ_mx_weight_scales_size bytes; positions no row maps to
+ *     hold code 0.
+ * All MXFP8 calls need M and I multiples of 128 (SITU_ERR_UNSUPPORTED otherwise)
+ * and 16-byte aligned code and scale pointers.
+ * ------------------------------------------------------------------------- */
+#define SITU_MX_GATE_UP 0
+#define SITU_MX_DOWN 1
+
+size_t situ_mx_act_scales_size(int64_t R, int64_t K);
+size_t situ_mx_weight_scales_size(int32_t E, int64_t M, int64_t I, int kind);
+
+/* x [R, K] bf16 (device) -> codes [R, K] uint8 and scales (activation tiles),
+ * both device, written.  K % 128 == 0.  Errors: SITU_ERR_ARG, SITU_ERR_ALIGN,
+ * SITU_ERR_ALIAS, SITU_ERR_UNSUPPORTED, SITU_ERR_CUDA. */
+situ_status situ_mx_quantize_act(const void* x, void* codes, void* scales, int64_t R, int64_t K,
+                                 void* stream);
+
+/* Stacked expert weights W [E, rows, K] bf16 (kind SITU_MX_GATE_UP: rows = 2I,
+ * K = M; SITU_MX_DOWN: rows = M, K = I) -> codes [E, rows, K] uint8 and scales
+ * (weight tiles), written.  A one-time conversion: the weights then stay
+ * resident as MXFP8.  Errors: as situ_mx_quantize_act. */
+situ_status situ_mx_quantize_weights(const void* W, void* codes, void* scales, int32_t E,
+                                     int64_t M, int64_t I, int kind, void* stream);
+
+/* The packed gate_up projection of MXFP8 x (codes [R, M] + activation scales) by
+ * MXFP8 W_gate_up (one expert, SITU_MX_GATE_UP layout), FP32 accumulation, with
+ * the SiTU-GLU activation on the accumulators; h [R, I] bf16 written.  Caps as
+ * situ_glu_act.  Errors: SITU_ERR_ARG, SITU_ERR_ALIGN, SITU_ERR_ALIAS,
+ * SITU_ERR_UNSUPPORTED, SITU_ERR_CUDA; SITU_ERR_TIMEOUT on the device. */
+situ_status situ_ffn_gate_up_mxfp8(const void* x_codes, const void* x_scales,
+                                   const void* wgu_codes, const void* wgu_scales, void* h,
+                                   int64_t R, int64_t M, int64_t I, float beta,
+                                   float linear_beta, void* stream);
+
+/* The dense FFN with MXFP8 experts: x [R, M] bf16 is quantized to MXFP8; the gate_up
+ * GEMM (block-scaled, FP32 accumulation) applies SiTU-GLU, rounds h to bf16 (the
+ * pages' cast back to the input dtype) and writes it as MXFP8 in its epilogue; the
+ * down GEMM (block-scaled) writes y [R, M] bf16.
+ *   wgu_*, wd_*   device, one expert's weights as situ_mx_quantize_weights wrote them.
+ *   workspace     device, >= situ_ffn_mxfp8_workspace_size(R, M, I) bytes, 256-byte
+ *                 aligned; regions (each starting 256-byte aligned, in order): x codes
+ *                 [R, M], x scales, h codes [R, I], h scales -- after the call they
+ *                 hold the quantized x and h.
+ * Errors: those of situ_ffn_gate_up_mxfp8, SITU_ERR_WORKSPACE. */
+size_t situ_ffn_mxfp8_workspace_size(int64_t R, int64_t M, int64_t I);
+situ_status situ_ffn_forward_mxfp8(const void* x, const void* wgu_codes, const void* wgu_scales,
+                                   const void* wd_codes, const void* wd_scales, void* y,
+                                   void* workspace, size_t workspace_bytes, int64_t R, int64_t M,
+                                   int64_t I, float beta, float linear_beta, void* stream);
+
+/* situ_moe_grouped_forward with MXFP8 experts: x is gathered into expert order and
+ * quantized (scale tiles following each expert's 128-row tiles), then the grouped
+ * block-scaled gate_up (h written as MXFP8) and down GEMMs; y [T, k_eff, M] bf16 per
+ * (token, slot) as situ_moe_grouped_forward.  Weights [E, ...] as
+ * situ_mx_quantize_weights wrote them.  workspace >= situ_moe_mxfp8_workspace_size
+ * (T * k_eff, E, M, I) bytes, 256-byte aligned.  Errors: those of
+ * situ_moe_grouped_forward. */
+size_t situ_moe_mxfp8_workspace_size(int64_t R, int32_t E, int64_t M, int64_t I);
+situ_status situ_moe_grouped_forward_mxfp8(const void* x, const int32_t* expert_offsets,
+                                           const int32_t* token_index, const void* wgu_codes,
+                                           const void* wgu_scales, const void* wd_codes,
+                                           const void* wd_scales, void* y, void* workspace,
+                                           size_t workspace_bytes, int64_t T, int32_t k_eff,
+                                           int32_t E, int64_t M, int64_t I, float beta,
+                                           float linear_beta, void* stream);
+
+/* -------------------------------------------------------------------------
  * situ_moe_combine -- the layer output of a routed batch: for every token t,
  *   out[t, :] = dtype( sum over slots s = 0 .. k_eff-1 of w[t, s] * y[t, s, :] ),
  * accumulated in FP32 in slot order (deterministic; no atomics).  Each routed and

@@ -409,6 +409,142 @@ def situ_moe_grouped_backward(x: torch.Tensor, expert_offsets: torch.Tensor,
     return dx, dwg, dwd
 
 
+# ---------------------------------------------------------------------------
+# MXFP8 experts
+# ---------------------------------------------------------------------------
+MX_GATE_UP, MX_DOWN = 0, 1
+
+
+def mx_act_scales_bytes(R: int, K: int) -> int:
+    return int(_native.lib().situ_mx_act_scales_size(R, K))
+
+
+def mx_weight_scales_bytes(E: int, M: int, I: int, kind: int) -> int:
+    return int(_native.lib().situ_mx_weight_scales_size(E, M, I, kind))
+
+
+def mx_quantize_act(x: torch.Tensor):
+    """MXFP8 quantization of bf16 rows x [R, K]: (codes uint8 [R, K], scales uint8 in
+    the activation tile layout)."""
+    _cuda_contig("x", x)
+    if x.dtype != torch.bfloat16:
+        raise TypeError("x must be bf16")
+    K = x.shape[-1]
+    R = x.numel() // K
+    codes = torch.empty(R, K, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(max(mx_act_scales_bytes(R, K), 1), dtype=torch.uint8, device=x.device)
+    check("situ_mx_quantize_act",
+          _native.lib().situ_mx_quantize_act(x.data_ptr(), codes.data_ptr(), scales.data_ptr(),
+                                             R, K, _stream(x.device)))
+    return codes, scales
+
+
+def mx_quantize_weights(W: torch.Tensor, kind: int):
+    """MXFP8 quantization of stacked expert weights: kind MX_GATE_UP takes W_gate_up
+    [E, 2I, M] (or [2I, M]), MX_DOWN takes W_down [E, M, I] (or [M, I]).  Returns
+    (codes uint8 of W's shape, scales uint8 in the weight tile layout)."""
+    _cuda_contig("W", W)
+    if W.dtype != torch.bfloat16:
+        raise TypeError("W must be bf16")
+    w3 = W.view(1, *W.shape) if W.dim() == 2 else W
+    E, rows, K = w3.shape
+    if kind == MX_GATE_UP:
+        M, I = K, rows // 2
+    elif kind == MX_DOWN:
+        M, I = rows, K
+    else:
+        raise ValueError("kind must be MX_GATE_UP or MX_DOWN")
+    codes = torch.empty(W.shape, dtype=torch.uint8, device=W.device)
+    scales = torch.empty(max(mx_weight_scales_bytes(E, M, I, kind), 1), dtype=torch.uint8,
+                         device=W.device)
+    check("situ_mx_quantize_weights",
+          _native.lib().situ_mx_quantize_weights(W.data_ptr(), codes.data_ptr(),
+                                                 scales.data_ptr(), E, M, I, kind,
+                                                 _stream(W.device)))
+    return codes, scales
+
+
+def situ_ffn_gate_up_mxfp8(xq, wguq, beta: float = 4.0, linear_beta: float = 25.0):
+    """MXFP8 gate_up GEMM + SiTU-GLU: xq = (codes [R, M], scales), wguq = one expert's
+    (codes [2I, M], scales) -> h [R, I] bf16."""
+    xc, xs = xq
+    wc, ws = wguq
+    for n, t in (("x codes", xc), ("x scales", xs), ("W codes", wc), ("W scales", ws)):
+        _cuda_contig(n, t)
+    R, M = xc.shape
+    I = wc.shape[-2] // 2
+    h = torch.empty(R, I, dtype=torch.bfloat16, device=xc.device)
+    check("situ_ffn_gate_up_mxfp8",
+          _native.lib().situ_ffn_gate_up_mxfp8(xc.data_ptr(), xs.data_ptr(), wc.data_ptr(),
+                                               ws.data_ptr(), h.data_ptr(), R, M, I,
+                                               *caps(beta, linear_beta), _stream(xc.device)))
+    return h
+
+
+def ffn_mxfp8_workspace_bytes(R: int, M: int, I: int) -> int:
+    return int(_native.lib().situ_ffn_mxfp8_workspace_size(R, M, I))
+
+
+def situ_ffn_forward_mxfp8(x: torch.Tensor, wguq, wdq, beta: float = 4.0,
+                           linear_beta: float = 25.0, y: torch.Tensor | None = None,
+                           workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Dense SiTU-GLU FFN with MXFP8 experts: x [R, M] bf16, wguq / wdq one expert's
+    quantized weights (from mx_quantize_weights) -> y [R, M] bf16."""
+    _cuda_contig("x", x)
+    M = x.shape[-1]
+    R = x.numel() // M
+    I = wguq[0].shape[-2] // 2
+    if y is None:
+        y = torch.empty_like(x)
+    if R == 0:
+        return y
+    lib = _native.lib()
+    need = int(lib.situ_ffn_mxfp8_workspace_size(R, M, I))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    check("situ_ffn_forward_mxfp8",
+          lib.situ_ffn_forward_mxfp8(x.data_ptr(), wguq[0].data_ptr(), wguq[1].data_ptr(),
+                                     wdq[0].data_ptr(), wdq[1].data_ptr(), y.data_ptr(),
+                                     workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(), R, M, I,
+                                     *caps(beta, linear_beta), _stream(x.device)))
+    return y
+
+
+def moe_mxfp8_workspace_bytes(R: int, E: int, M: int, I: int) -> int:
+    return int(_native.lib().situ_moe_mxfp8_workspace_size(R, E, M, I))
+
+
+def situ_moe_grouped_forward_mxfp8(x: torch.Tensor, expert_offsets: torch.Tensor,
+                                   token_index: torch.Tensor, wguq, wdq, k_eff: int,
+                                   beta: float = 4.0, linear_beta: float = 25.0,
+                                   y: torch.Tensor | None = None,
+                                   workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Grouped SiTU-GLU experts with MXFP8 weights (stacked, from
+    mx_quantize_weights): y[t, s] = FFN_{expert of (t, s)}(x[t]), [T, k_eff, M] bf16."""
+    for n, t in (("x", x), ("expert_offsets", expert_offsets), ("token_index", token_index)):
+        _cuda_contig(n, t)
+    T, M = x.shape
+    E, twoI, _ = wguq[0].shape
+    I = twoI // 2
+    if y is None:
+        y = torch.empty(T, k_eff, M, dtype=x.dtype, device=x.device)
+    R = T * k_eff
+    if R == 0:
+        return y
+    lib = _native.lib()
+    need = int(lib.situ_moe_mxfp8_workspace_size(R, E, M, I))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    check("situ_moe_grouped_forward_mxfp8",
+          lib.situ_moe_grouped_forward_mxfp8(
+              x.data_ptr(), expert_offsets.data_ptr(), token_index.data_ptr(),
+              wguq[0].data_ptr(), wguq[1].data_ptr(), wdq[0].data_ptr(), wdq[1].data_ptr(),
+              y.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+              T, k_eff, E, M, I, *caps(beta, linear_beta), _stream(x.device)))
+    return y
+
+
 def situ_moe_combine(y: torch.Tensor, weights: torch.Tensor,
                      out: torch.Tensor | None = None) -> torch.Tensor:
     """Layer output of a routed batch: out[t] = sum_s weights[t, s] * y[t, s] (FP32,
@@ -448,4 +584,7 @@ __all__ = [
     "device_status", "selftest_bounded_wait", "ffn_host_workspace_bytes", "situ_moe_combine",
     "situ_ffn_forward_train", "situ_ffn_backward", "ffn_backward_workspace_bytes",
     "situ_moe_grouped_forward_train", "situ_moe_grouped_backward", "moe_backward_workspace_bytes",
+    "MX_GATE_UP", "MX_DOWN", "mx_act_scales_bytes", "mx_weight_scales_bytes", "mx_quantize_act",
+    "mx_quantize_weights", "situ_ffn_gate_up_mxfp8", "situ_ffn_forward_mxfp8",
+    "ffn_mxfp8_workspace_bytes", "situ_moe_grouped_forward_mxfp8", "moe_mxfp8_workspace_bytes",
 ]

@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(LIB_DIR, "libsitu.so")
-SOURCES = ["abi.cu", "act.cu", "combine.cu", "gemm.cu", "hostio.cu", "moe_index.cu", "noalloc.cu"]
+SOURCES = ["abi.cu", "act.cu", "combine.cu", "gemm.cu", "hostio.cu", "moe_index.cu", "mx_gemm.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

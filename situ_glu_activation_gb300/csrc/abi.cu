@@ -806,6 +806,304 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
   return SITU_OK;
 }
 
+// ---------------------------------------------------------------------------
+// MXFP8
+// ---------------------------------------------------------------------------
+namespace {
+
+int64_t mx_weight_rows(int kind, int64_t M, int64_t I) { return kind == SITU_MX_GATE_UP ? 2 * I : M; }
+int64_t mx_weight_k(int kind, int64_t M, int64_t I) { return kind == SITU_MX_GATE_UP ? M : I; }
+int64_t mx_weight_split(int kind, int64_t I) { return kind == SITU_MX_GATE_UP ? I : 0; }
+
+bool mx_shape_ok(int64_t M, int64_t I) { return M >= 128 && I >= 128 && M % 128 == 0 && I % 128 == 0; }
+
+}  // namespace
+
+size_t situ_mx_act_scales_size(int64_t R, int64_t K) {
+  if (R < 0 || K <= 0 || K % 128 != 0) return 0;
+  return mx_act_scale_bytes(R, K);
+}
+
+size_t situ_mx_weight_scales_size(int32_t E, int64_t M, int64_t I, int kind) {
+  if (E < 1 || (kind != SITU_MX_GATE_UP && kind != SITU_MX_DOWN) || !mx_shape_ok(M, I)) return 0;
+  return mx_weight_scale_bytes(E, mx_weight_rows(kind, M, I), mx_weight_k(kind, M, I),
+                               mx_weight_split(kind, I));
+}
+
+situ_status situ_mx_quantize_act(const void* x, void* codes, void* scales, int64_t R, int64_t K,
+                                 void* stream) {
+  if (R < 0 || K <= 0) return SITU_ERR_ARG;
+  if (K % 128 != 0) return SITU_ERR_UNSUPPORTED;
+  if (R == 0) return SITU_OK;
+  if (!x || !codes || !scales) return SITU_ERR_ARG;
+  if (!aligned16(x) || !aligned16(codes)) return SITU_ERR_ALIGN;
+  const size_t xb = static_cast<size_t>(R) * K * 2, cb = static_cast<size_t>(R) * K,
+               sb = mx_act_scale_bytes(R, K);
+  if (overlap(codes, cb, x, xb) || overlap(scales, sb, x, xb) || overlap(codes, cb, scales, sb))
+    return SITU_ERR_ALIAS;
+  DeviceState* st = nullptr;
+  situ_status s = device_state(&st);
+  if (s != SITU_OK) return s;
+  return finish(launch_mx_quantize_act(x, nullptr, 1, R, codes, scales, (R + 127) / 128, R, K, 0,
+                                       nullptr, nullptr, st->status,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+situ_status situ_mx_quantize_weights(const void* W, void* codes, void* scales, int32_t E,
+                                     int64_t M, int64_t I, int kind, void* stream) {
+  if (E < 1 || M < 1 || I < 1 || (kind != SITU_MX_GATE_UP && kind != SITU_MX_DOWN))
+    return SITU_ERR_ARG;
+  if (!mx_shape_ok(M, I)) return SITU_ERR_UNSUPPORTED;
+  if (!W || !codes || !scales) return SITU_ERR_ARG;
+  if (!aligned16(W) || !aligned16(codes)) return SITU_ERR_ALIGN;
+  const int64_t rows = mx_weight_rows(kind, M, I), K = mx_weight_k(kind, M, I);
+  const size_t wb = static_cast<size_t>(E) * rows * K * 2, cb = static_cast<size_t>(E) * rows * K,
+               sb = situ_mx_weight_scales_size(E, M, I, kind);
+  if (overlap(codes, cb, W, wb) || overlap(scales, sb, W, wb) || overlap(codes, cb, scales, sb))
+    return SITU_ERR_ALIAS;
+  DeviceState* st = nullptr;
+  situ_status s = device_state(&st);
+  if (s != SITU_OK) return s;
+  return finish(launch_mx_quantize_weights(W, codes, scales, E, rows, K,
+                                           mx_weight_split(kind, I),
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+
+// The MXFP8 gate_up GEMM (+ SiTU-GLU): bf16 h into h, or MXFP8 h into h_codes / h_sf.
+cudaError_t run_mx_gate_up(const DeviceState* st, const void* x_codes, const void* x_scales,
+                           const void* wgu_codes, const void* wgu_scales, void* h, void* h_codes,
+                           void* h_sf, int64_t R, int64_t M, int64_t I, float beta,
+                           float linear_beta, int32_t E, const int32_t* offsets,
+                           const int32_t* tiles, const int32_t* units, cudaStream_t cs) {
+  GemmShape g{};
+  g.a = x_codes;
+  g.a_rows = R;
+  g.b = wgu_codes;
+  g.b_rows = static_cast<int64_t>(E) * 2 * I;
+  g.K = M;
+  g.num_groups = offsets ? E : 1;
+  g.group_offsets = offsets;
+  g.tile_offsets = tiles;
+  g.unit_offsets = units;
+  g.b_group_rows = 2 * I;
+  g.b_up_offset = I;
+  g.n_out = I;
+  g.out = h;
+  g.ldo = I;
+  g.out_rows = R;
+  g.sfa = x_scales;
+  g.sfb = wgu_scales;
+  g.h_codes = h_codes;
+  g.h_sf = h_sf;
+  return launch_mx_gemm_situ(g, make_situ_params(beta, linear_beta), caps_of(beta, linear_beta),
+                             st->status, st->num_sms, cs);
+}
+
+cudaError_t run_mx_down(const DeviceState* st, const void* h_codes, const void* h_sf,
+                        const void* wd_codes, const void* wd_scales, void* y, int64_t R,
+                        int64_t M, int64_t I, int32_t E, const int32_t* offsets,
+                        const int32_t* tiles, const int32_t* units, const int32_t* row_index,
+                        cudaStream_t cs) {
+  GemmShape d{};
+  d.a = h_codes;
+  d.a_rows = R;
+  d.b = wd_codes;
+  d.b_rows = static_cast<int64_t>(E) * M;
+  d.K = I;
+  d.num_groups = offsets ? E : 1;
+  d.group_offsets = offsets;
+  d.tile_offsets = tiles;
+  d.unit_offsets = units;
+  d.b_group_rows = M;
+  d.n_out = M;
+  d.out = y;
+  d.ldo = M;
+  d.out_rows = R;
+  d.out_row_index = row_index;
+  d.sfa = h_sf;
+  d.sfb = wd_scales;
+  return launch_mx_gemm_plain(d, st->status, st->num_sms, cs);
+}
+
+// Carving of the dense MXFP8 FFN workspace: x codes, x scales, h codes, h scales.
+struct MxFfnWs {
+  size_t x_codes, x_sf, h_codes, h_sf, total;
+};
+MxFfnWs mx_ffn_ws(int64_t R, int64_t M, int64_t I) {
+  MxFfnWs w;
+  w.x_codes = 0;
+  w.x_sf = round_up(static_cast<size_t>(R) * M, 256);
+  w.h_codes = w.x_sf + round_up(mx_act_scale_bytes(R, M), 256);
+  w.h_sf = w.h_codes + round_up(static_cast<size_t>(R) * I, 256);
+  w.total = w.h_sf + round_up(mx_act_scale_bytes(R, I), 256);
+  return w;
+}
+
+}  // namespace
+
+situ_status situ_ffn_gate_up_mxfp8(const void* x_codes, const void* x_scales,
+                                   const void* wgu_codes, const void* wgu_scales, void* h,
+                                   int64_t R, int64_t M, int64_t I, float beta,
+                                   float linear_beta, void* stream) {
+  if (R < 0 || M < 1 || I < 1 || !caps_ok(beta, linear_beta)) return SITU_ERR_ARG;
+  if (!mx_shape_ok(M, I)) return SITU_ERR_UNSUPPORTED;
+  if (R == 0) return SITU_OK;
+  if (!x_codes || !x_scales || !wgu_codes || !wgu_scales || !h) return SITU_ERR_ARG;
+  if (!aligned16(x_codes) || !aligned16(x_scales) || !aligned16(wgu_codes) ||
+      !aligned16(wgu_scales) || !aligned16(h))
+    return SITU_ERR_ALIGN;
+  if (R >= (int64_t(1) << 31)) return SITU_ERR_UNSUPPORTED;
+  const size_t hb = static_cast<size_t>(R) * I * 2;
+  if (overlap(h, hb, x_codes, static_cast<size_t>(R) * M) ||
+      overlap(h, hb, x_scales, mx_act_scale_bytes(R, M)) ||
+      overlap(h, hb, wgu_codes, static_cast<size_t>(2 * I) * M) ||
+      overlap(h, hb, wgu_scales, situ_mx_weight_scales_size(1, M, I, SITU_MX_GATE_UP)))
+    return SITU_ERR_ALIAS;
+  DeviceState* st = nullptr;
+  situ_status s = device_state(&st);
+  if (s != SITU_OK) return s;
+  return finish(run_mx_gate_up(st, x_codes, x_scales, wgu_codes, wgu_scales, h, nullptr, nullptr,
+                               R, M, I, beta, linear_beta, 1, nullptr, nullptr, nullptr,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+size_t situ_ffn_mxfp8_workspace_size(int64_t R, int64_t M, int64_t I) {
+  if (R < 0 || !mx_shape_ok(M, I)) return 0;
+  return mx_ffn_ws(R, M, I).total;
+}
+
+situ_status situ_ffn_forward_mxfp8(const void* x, const void* wgu_codes, const void* wgu_scales,
+                                   const void* wd_codes, const void* wd_scales, void* y,
+                                   void* workspace, size_t workspace_bytes, int64_t R, int64_t M,
+                                   int64_t I, float beta, float linear_beta, void* stream) {
+  if (R < 0 || M < 1 || I < 1 || !caps_ok(beta, linear_beta)) return SITU_ERR_ARG;
+  if (!mx_shape_ok(M, I)) return SITU_ERR_UNSUPPORTED;
+  if (R == 0) return SITU_OK;
+  if (!x || !wgu_codes || !wgu_scales || !wd_codes || !wd_scales || !y) return SITU_ERR_ARG;
+  const void* ptrs[] = {x, wgu_codes, wgu_scales, wd_codes, wd_scales, y};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return SITU_ERR_ALIGN;
+  if (R >= (int64_t(1) << 31)) return SITU_ERR_UNSUPPORTED;
+  const MxFfnWs w = mx_ffn_ws(R, M, I);
+  if (!workspace || workspace_bytes < w.total || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return SITU_ERR_WORKSPACE;
+  const size_t xb = static_cast<size_t>(R) * M * 2;
+  const void* ins[] = {x, wgu_codes, wgu_scales, wd_codes, wd_scales};
+  const size_t inb[] = {xb, static_cast<size_t>(2 * I) * M,
+                        situ_mx_weight_scales_size(1, M, I, SITU_MX_GATE_UP),
+                        static_cast<size_t>(M) * I, situ_mx_weight_scales_size(1, M, I, SITU_MX_DOWN)};
+  for (int i = 0; i < 5; ++i)
+    if (overlap(y, xb, ins[i], inb[i]) || overlap(workspace, w.total, ins[i], inb[i]))
+      return SITU_ERR_ALIAS;
+  if (overlap(y, xb, workspace, w.total)) return SITU_ERR_ALIAS;
+  DeviceState* st = nullptr;
+  situ_status s = device_state(&st);
+  if (s != SITU_OK) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = launch_mx_quantize_act(x, nullptr, 1, R, ws + w.x_codes, ws + w.x_sf,
+                                         (R + 127) / 128, R, M, 0, nullptr, nullptr, st->status,
+                                         cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = run_mx_gate_up(st, ws + w.x_codes, ws + w.x_sf, wgu_codes, wgu_scales, nullptr,
+                     ws + w.h_codes, ws + w.h_sf, R, M, I, beta, linear_beta, 1, nullptr, nullptr,
+                     nullptr, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return finish(run_mx_down(st, ws + w.h_codes, ws + w.h_sf, wd_codes, wd_scales, y, R, M, I, 1,
+                            nullptr, nullptr, nullptr, nullptr, cs));
+}
+
+namespace {
+
+// Carving of the grouped MXFP8 workspace: three prefixes, x codes (expert order),
+// x scales, h codes, h scales.  Grouped m-tiles number at most ceil(R/128) + E.
+struct MxMoeWs {
+  size_t tiles, units_gu, units_dn, x_codes, x_sf, h_codes, h_sf, total;
+};
+MxMoeWs mx_moe_ws(int64_t R, int32_t E, int64_t M, int64_t I) {
+  MxMoeWs w;
+  const size_t pre = round_up(static_cast<size_t>(E + 1) * 4, 256);
+  const int64_t tile_rows = ((R + 127) / 128 + E) * 128;
+  w.tiles = 0;
+  w.units_gu = pre;
+  w.units_dn = 2 * pre;
+  w.x_codes = 3 * pre;
+  w.x_sf = w.x_codes + round_up(static_cast<size_t>(R) * M, 256);
+  w.h_codes = w.x_sf + round_up(mx_act_scale_bytes(tile_rows, M), 256);
+  w.h_sf = w.h_codes + round_up(static_cast<size_t>(R) * I, 256);
+  w.total = w.h_sf + round_up(mx_act_scale_bytes(tile_rows, I), 256);
+  return w;
+}
+
+}  // namespace
+
+size_t situ_moe_mxfp8_workspace_size(int64_t R, int32_t E, int64_t M, int64_t I) {
+  if (R < 0 || E < 1 || !mx_shape_ok(M, I)) return 0;
+  return mx_moe_ws(R, E, M, I).total;
+}
+
+situ_status situ_moe_grouped_forward_mxfp8(const void* x, const int32_t* expert_offsets,
+                                           const int32_t* token_index, const void* wgu_codes,
+                                           const void* wgu_scales, const void* wd_codes,
+                                           const void* wd_scales, void* y, void* workspace,
+                                           size_t workspace_bytes, int64_t T, int32_t k_eff,
+                                           int32_t E, int64_t M, int64_t I, float beta,
+                                           float linear_beta, void* stream) {
+  if (T < 0 || k_eff < 1 || E < 1 || E > 65536 || M < 1 || I < 1 || !caps_ok(beta, linear_beta))
+    return SITU_ERR_ARG;
+  if (!mx_shape_ok(M, I)) return SITU_ERR_UNSUPPORTED;
+  const int64_t R = T * k_eff;
+  if (R == 0) return SITU_OK;
+  if (!x || !expert_offsets || !token_index || !wgu_codes || !wgu_scales || !wd_codes ||
+      !wd_scales || !y)
+    return SITU_ERR_ARG;
+  if (R >= (int64_t(1) << 31) || static_cast<int64_t>(E) * 2 * I >= (int64_t(1) << 31) ||
+      static_cast<int64_t>(E) * M >= (int64_t(1) << 31))
+    return SITU_ERR_UNSUPPORTED;
+  const void* ptrs[] = {x, wgu_codes, wgu_scales, wd_codes, wd_scales, y};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return SITU_ERR_ALIGN;
+  const MxMoeWs w = mx_moe_ws(R, E, M, I);
+  if (!workspace || workspace_bytes < w.total || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return SITU_ERR_WORKSPACE;
+  const size_t x_b = static_cast<size_t>(T) * M * 2, y_b = static_cast<size_t>(R) * M * 2;
+  const void* ins[] = {x, expert_offsets, token_index, wgu_codes, wgu_scales, wd_codes, wd_scales};
+  const size_t in_b[] = {x_b, static_cast<size_t>(E + 1) * 4, static_cast<size_t>(R) * 4,
+                         static_cast<size_t>(E) * 2 * I * M,
+                         situ_mx_weight_scales_size(E, M, I, SITU_MX_GATE_UP),
+                         static_cast<size_t>(E) * M * I,
+                         situ_mx_weight_scales_size(E, M, I, SITU_MX_DOWN)};
+  for (int i = 0; i < 7; ++i)
+    if (overlap(y, y_b, ins[i], in_b[i]) || overlap(workspace, w.total, ins[i], in_b[i]))
+      return SITU_ERR_ALIAS;
+  if (overlap(y, y_b, workspace, w.total)) return SITU_ERR_ALIAS;
+  DeviceState* st = nullptr;
+  situ_status s = device_state(&st);
+  if (s != SITU_OK) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* tiles = reinterpret_cast<int32_t*>(ws + w.tiles);
+  int32_t* units_gu = reinterpret_cast<int32_t*>(ws + w.units_gu);
+  int32_t* units_dn = reinterpret_cast<int32_t*>(ws + w.units_dn);
+  cudaError_t e = launch_group_tiles(expert_offsets, E, R,
+                                     static_cast<int32_t>((I + kMxSituCols - 1) / kMxSituCols),
+                                     static_cast<int32_t>((M + kMxPlainCols - 1) / kMxPlainCols),
+                                     tiles, units_gu, units_dn, st->status, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  // Gather x into expert order and quantize it, scales tiled by the experts' m-tiles.
+  e = launch_mx_quantize_act(x, token_index, k_eff, T, ws + w.x_codes, ws + w.x_sf,
+                             (R + 127) / 128 + E, R, M, E, expert_offsets, tiles, st->status, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = run_mx_gate_up(st, ws + w.x_codes, ws + w.x_sf, wgu_codes, wgu_scales, nullptr,
+                     ws + w.h_codes, ws + w.h_sf, R, M, I, beta, linear_beta, E, expert_offsets,
+                     tiles, units_gu, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return finish(run_mx_down(st, ws + w.h_codes, ws + w.h_sf, wd_codes, wd_scales, y, R, M, I, E,
+                            expert_offsets, tiles, units_dn, token_index, cs));
+}
+
 situ_status situ_moe_combine(const void* y, const float* weights, void* out, int64_t T,
                              int32_t k_eff, int64_t M, situ_dtype dt, void* stream) {
   if (!dtype_ok(dt) || T < 0 || k_eff < 1 || M < 1) return SITU_ERR_ARG;

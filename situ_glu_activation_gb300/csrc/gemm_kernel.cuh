@@ -1,0 +1,986 @@
+// gemm_kernel.cuh -- the persistent, warp-specialised tcgen05 GEMM kernel shared
+// by the bf16 GEMMs (gemm.cu) and the MXFP8 block-scaled GEMMs (mx_gemm.cu), with
+// its host-side launch.  Included by exactly those translation units; everything
+// is in an anonymous namespace, so each unit instantiates what it launches.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "situ_internal.h"
+#include "situ_math.cuh"
+#include "situ_ptx.cuh"
+
+namespace situ {
+namespace {
+
+constexpr int kBM = 128;  // tile rows (UMMA M)
+constexpr int kBN = 256;  // accumulator columns per tile (UMMA N)
+constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
+constexpr int kUK = 16;   // K per tcgen05.mma for 16-bit inputs
+constexpr int kAccBufs = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr uint64_t kWaitLimitNs = 10ull * 1000 * 1000 * 1000;  // 10 s
+constexpr uint64_t kDrainLimitNs = 100ull * 1000 * 1000;       // 100 ms
+constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
+// Tiles with at most 64 valid rows (an expert's tail, a small group) issue M=64
+// MMAs: half the tensor work.  Their accumulator rows 16q..16q+15 sit in TMEM lanes
+// 32q..32q+15 (the first 16 lanes of each warp's quarter), measured on GB300.
+constexpr uint32_t kIdescHalf = idesc_bf16_f32(64, kBN);
+// Operand layouts: kKMajor -- A [rows, K] and B [N, K] with K contiguous (the
+// forward); kBMN -- B stored [K, N] (N contiguous), e.g. W_down when the
+// backward multiplies by it untransposed; kABMN -- A stored [K, rows] and B
+// stored [K, N], e.g. dy and h when the weight gradient contracts over tokens.
+// MN-major tiles arrive as {64, 64} boxes (8 KB): A takes two, B four.
+// kABMNGrouped -- the kABMN layouts with a K-grouped schedule: each group (expert)
+// contracts over its own row range (per-expert weight gradients).
+enum class Major { kKMajor = 0, kBMN = 1, kABMN = 2, kABMNGrouped = 3 };
+__host__ __device__ constexpr bool a_mn_major(Major m) { return m == Major::kABMN || m == Major::kABMNGrouped; }
+constexpr uint32_t kAMnBit = 1u << 15, kBMnBit = 1u << 16;
+constexpr uint32_t kMnAtomBytes = 64 * 64 * 2;
+
+// Tile geometry per operand type.  Both stage 128-byte rows of K (one 128-byte
+// swizzle row): 64 bf16 or 128 MXFP8 codes.
+//   bf16: N = 256 accumulator columns, 4 stages of A 128x64 + B 256x64 (48 KB).
+//   MXFP8 (E4M3 codes, one E8M0 scale per 32 along K): N = 192 (two accumulators
+//     of 192 columns leave TMEM room for the scales), 5 stages of A 128x128 +
+//     B 192x128 codes + the A and B scale tiles of the stage (512 + 1024 bytes),
+//     K = 32 per MMA.  B arrives as two 96-row halves.
+template <bool kMx>
+struct Geo {
+  static constexpr int BN = 256, BK = 64, UK = 16, Stages = 4, BHalfRows = 128;
+  static constexpr uint32_t ABytes = 16384, BBytes = 32768, SfBytes = 0;
+  static constexpr uint32_t TxBytes = ABytes + BBytes;  // bytes the copies of a stage bring
+  static constexpr uint32_t StageBytes = TxBytes;
+};
+template <>
+struct Geo<true> {
+  static constexpr int BN = 192, BK = 128, UK = 32, Stages = 5, BHalfRows = 96;
+  static constexpr uint32_t ABytes = 16384, BBytes = 24576, SfBytes = 512 + 1024;
+  static constexpr uint32_t TxBytes = ABytes + BBytes + SfBytes;
+  static constexpr uint32_t StageBytes = 43008;  // TxBytes rounded up to 1 KB
+};
+constexpr int kMaxStages = 5;
+// MXFP8 scale tiles.  The block-scaled MMA reads the E8M0 scale of A row m for its
+// k-th 32-wide K block (k = 0..3 within a 128-K stage) from TMEM lane m, column
+// base + m / 32, byte k; that of B row n from column base + n / 32, byte k, in the
+// lane quadrant of the accumulator row it is producing (measured on GB300 with an
+// in-bounds probe).  tcgen05.cp.32x128b.warpx4 copies 32 rows x 16 bytes into all
+// four quadrants, so a 128-row scale tile is stored as 512 bytes, byte
+// l * 16 + g * 4 + k holding row 32 g + l, block k; B's 192 rows take two such tiles
+// (1024 bytes, groups 6 and 7 unused).
+constexpr uint32_t kSfTileBytes = 512;
+constexpr uint32_t kSfbStageBytes = 1024;
+constexpr uint32_t kSfTmemCols = 12;  // per stage: A 4 columns, B 8 columns
+
+// Epilogues: kSitu applies SiTU-GLU to (gate, up) accumulator pairs (and can
+// also store the pre-activation pair); kPlain converts to bf16; kSituBwd turns
+// dh accumulators into d(gate, up) through the activation's derivative, reading
+// the saved pre-activation pair.
+// kSituMx (MXFP8 only) applies SiTU-GLU, rounds h to bf16 and stores it as MXFP8
+// codes and scales, the input format of the next block-scaled GEMM.
+enum class Epi { kSitu, kPlain, kSituBwd, kSituMx };
+
+struct Args {
+  int32_t num_groups;
+  const int32_t* group_offsets;  // [G+1] device or null (dense)
+  const int32_t* tile_offsets;   // [G+1] device or null (dense): m-tile prefix
+  const int32_t* unit_offsets;   // [G+1] device or null (dense): paired-unit prefix
+  int32_t dense_rows;
+  int32_t n_tiles;
+  int32_t k_blocks;
+  int64_t b_group_rows;
+  int64_t b_up_offset;
+  int64_t n_out;
+  __nv_bfloat16* out;
+  int64_t ldo;
+  int64_t out_rows;
+  const int32_t* out_row_index;
+  SituParams sp;
+  uint32_t* status;
+  // kSitu: optional store of the pre-activation (g, u) as bf16 [rows, 2*split];
+  // kSituBwd: the saved (g, u) to read and d(g, u) to write, same layout.
+  __nv_bfloat16* gu_store;
+  const __nv_bfloat16* gu_in;
+  __nv_bfloat16* dgu_out;
+  int64_t split;
+  // K-grouped contraction (MN-major A and B only): group g contracts over the K
+  // rows k_group_offsets[g] .. k_group_offsets[g+1]-1 of both operands and writes
+  // its [dense_rows, n_out] result at output rows g * out_group_rows.  Every group
+  // has units_per_group work units.  A nonzero tile_offsets[num_groups] marks the
+  // offsets as validated (zero: nothing runs).
+  const int32_t* k_group_offsets;
+  int32_t units_per_group;
+  int64_t out_group_rows;
+  // MXFP8: the scale tiles of A (per global m-tile and k-block, 512 bytes) and of
+  // B (per (group, n-tile) and k-block, 1024 bytes); kSituMx output: h codes
+  // [rows, ldo] and h scale tiles (A layout, n_out / 128 k-blocks per m-tile).
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  uint8_t* h_codes;
+  uint8_t* h_sf;
+};
+
+struct SharedCtl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t acc_full[kAccBufs];
+  uint64_t acc_empty[kAccBufs];
+  uint64_t drain;
+  uint32_t tmem_base;
+  volatile int abort;
+};
+
+struct TileCoord {
+  int32_t a_row0;   // first A row of the tile
+  int32_t row_end;  // one past the last valid A row (group end)
+  int32_t group;
+  int32_t n_tile;
+  int32_t share_a;  // paired unit of one m-tile and two n-tiles (A multicast)
+  int32_t k0;       // first K row of the contraction (K-grouped; 0 otherwise)
+  int32_t k_end;    // one past its last K row (K-grouped)
+  int32_t k_blocks; // k-blocks of this tile
+};
+
+__device__ __forceinline__ int32_t total_tiles(const Args& a) {
+  const int32_t m_tiles = a.tile_offsets ? __ldg(a.tile_offsets + a.num_groups)
+                                         : (a.dense_rows + kBM - 1) / kBM;
+  return m_tiles * a.n_tiles;
+}
+
+__device__ __forceinline__ TileCoord decode_tile(const Args& a, int32_t t) {
+  TileCoord c;
+  const int32_t mt = t / a.n_tiles;
+  c.n_tile = t - mt * a.n_tiles;
+  if (!a.tile_offsets) {
+    c.group = 0;
+    c.a_row0 = mt * kBM;
+    c.row_end = a.dense_rows;
+    c.share_a = 0;
+    return c;
+  }
+  // Largest g with tile_offsets[g] <= mt (empty groups repeat an offset; the
+  // last of a run of equal offsets is the group that owns the tile).
+  int32_t lo = 0, hi = a.num_groups - 1;
+  while (lo < hi) {
+    const int32_t mid = (lo + hi + 1) >> 1;
+    if (__ldg(a.tile_offsets + mid) <= mt) lo = mid; else hi = mid - 1;
+  }
+  c.group = lo;
+  c.a_row0 = __ldg(a.group_offsets + lo) + (mt - __ldg(a.tile_offsets + lo)) * kBM;
+  c.row_end = __ldg(a.group_offsets + lo + 1);
+  c.share_a = 0;
+  return c;
+}
+
+// Tile `local` of one group's rows row0 .. row_end-1 (unpaired: m-tile-major).
+__device__ __forceinline__ TileCoord in_group_tile(const Args& a, int32_t local, int32_t row0,
+                                                   int32_t row_end) {
+  TileCoord c;
+  const int32_t mt = local / a.n_tiles;
+  c.n_tile = local - mt * a.n_tiles;
+  c.a_row0 = row0 + mt * kBM;
+  c.row_end = row_end;
+  c.group = 0;
+  c.share_a = 0;
+  return c;
+}
+
+// Work units.  Unpaired: one unit = one tile, from decode_tile.  Paired
+// (clusters of two CTAs, CTA rank r):
+//   * a group (expert) with m m-tiles has floor(m/2) * n_tiles "shared-B" units:
+//     unit (p, n) gives rank r the tile (m-tile 2p + r, n-tile n); the two CTAs
+//     share the B tile of n-tile n, each fetching one half and multicasting it;
+//   * when m is odd, its last m-tile forms ceil(n_tiles/2) "shared-A" units:
+//     unit q gives rank r the tile (m-tile m-1, n-tile 2q + r); the two CTAs share
+//     the A tile, each fetching 64 of its 128 rows and multicasting them.
+// Dense calls are one group of all rows; grouped calls read the per-group unit
+// prefix from unit_offsets.
+__device__ __forceinline__ int32_t units_of(int32_t m, int32_t n_tiles) {
+  return (m >> 1) * n_tiles + (m & 1) * ((n_tiles + 1) >> 1);
+}
+
+// Paired unit `local` of one group's rows row0 .. row_end-1 (see above).
+__device__ __forceinline__ TileCoord in_group_unit(const Args& a, int32_t local, uint32_t rank,
+                                                   int32_t row0, int32_t row_end) {
+  const int32_t m = (row_end - row0 + kBM - 1) / kBM;
+  const int32_t shared_b_units = (m >> 1) * a.n_tiles;
+  TileCoord c;
+  c.group = 0;
+  c.row_end = row_end;
+  if (local < shared_b_units) {
+    const int32_t p = local / a.n_tiles;
+    c.n_tile = local - p * a.n_tiles;
+    c.a_row0 = row0 + (2 * p + static_cast<int32_t>(rank)) * kBM;
+    c.share_a = 0;
+  } else {
+    const int32_t q = local - shared_b_units;
+    c.n_tile = 2 * q + static_cast<int32_t>(rank);
+    c.a_row0 = row0 + (m - 1) * kBM;
+    c.share_a = 1;
+  }
+  return c;
+}
+
+template <bool kPair, bool kKG>
+__device__ __forceinline__ int32_t num_units(const Args& a) {
+  if (kKG) {
+    if (a.tile_offsets && __ldg(a.tile_offsets + a.num_groups) == 0) return 0;
+    return a.num_groups * a.units_per_group;
+  }
+  if (!kPair) return total_tiles(a);
+  if (a.unit_offsets) return __ldg(a.unit_offsets + a.num_groups);
+  return units_of((a.dense_rows + kBM - 1) / kBM, a.n_tiles);
+}
+
+template <bool kPair, bool kKG>
+__device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_t rank) {
+  TileCoord c;
+  if (kKG) {
+    // Every group has the same output tiles; its K range is its row range.
+    const int32_t g = u / a.units_per_group;
+    const int32_t local = u - g * a.units_per_group;
+    c = kPair ? in_group_unit(a, local, rank, 0, a.dense_rows)
+              : in_group_tile(a, local, 0, a.dense_rows);
+    c.group = g;
+    c.k0 = __ldg(a.k_group_offsets + g);
+    c.k_end = __ldg(a.k_group_offsets + g + 1);
+    c.k_blocks = c.k_end > c.k0 ? (c.k_end - c.k0 + kBK - 1) / kBK : 0;
+    return c;
+  }
+  if (!kPair) {
+    c = decode_tile(a, u);
+  } else {
+    int32_t g = 0, row0 = 0, row_end = a.dense_rows, local = u;
+    if (a.unit_offsets) {
+      int32_t lo = 0, hi = a.num_groups - 1;
+      while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (__ldg(a.unit_offsets + mid) <= u) lo = mid; else hi = mid - 1;
+      }
+      g = lo;
+      row0 = __ldg(a.group_offsets + g);
+      row_end = __ldg(a.group_offsets + g + 1);
+      local = u - __ldg(a.unit_offsets + g);
+    }
+    c = in_group_unit(a, local, rank, row0, row_end);
+    c.group = g;
+  }
+  c.k0 = 0;
+  c.k_end = 0;
+  c.k_blocks = a.k_blocks;
+  return c;
+}
+
+__device__ __forceinline__ bool ctl_wait(SharedCtl* ctl, uint64_t* bar, uint32_t parity,
+                                         uint32_t* status) {
+  const uint32_t b = smem_u32(bar);
+  if (mbar_try_wait(b, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t polls = 0;
+  while (true) {
+    if (mbar_try_wait(b, parity)) return true;
+    if ((++polls & 63u) == 0u) {
+      if (ctl->abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        record_status(status, SITU_ERR_TIMEOUT);
+        ctl->abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Zero K rows kv..63 of a stage's MN-major operand tiles (2 A atoms, 4 B
+// atoms): row k of a {64 MN, 64 K} 128-byte-swizzled atom is the 128 bytes at
+// k * 128 (the swizzle permutes 16-byte pieces within a row), so the tail is one
+// contiguous range per atom.  Warp-collective.
+__device__ __forceinline__ void zero_k_tail(uint32_t sa, uint32_t sb, int32_t kv, int lane) {
+  const uint32_t first = static_cast<uint32_t>(kv) * 128u;
+  const uint32_t n = (kMnAtomBytes - first) / 16u;
+#pragma unroll 1
+  for (int at = 0; at < 6; ++at) {
+    const uint32_t base = (at < 2 ? sa + at * kMnAtomBytes : sb + (at - 2) * kMnAtomBytes) + first;
+    for (uint32_t i = lane; i < n; i += 32) st_shared_zero16(base + 16u * i);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Store up to 32 bf16 (16 packed words) of one row; columns >= n_valid are not
+// written (n_valid is a multiple of 8, so a 16-byte piece is all in or all out).
+__device__ __forceinline__ void store_row_chunk(__nv_bfloat16* dst, const uint32_t (&w)[16],
+                                                int64_t col0, int64_t n_valid) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    if (col0 + 8 * v + 8 <= n_valid) {
+      st_global_v4(dst + 8 * v, w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+    }
+  }
+}
+
+// MXFP8 quantization of one block of 32 values given as bf16 (16 packed words,
+// element 2i in the low half of word i), per the OCP MX conversion: scale
+// 2^(floor(log2 amax) - 8), i.e. E8M0 code max(E - 8, 0) with E the biased exponent
+// of the largest magnitude (zero and tiny blocks take the smallest scale 2^-127);
+// each code is E4M3(v * 2^(127 - code)), an exact power-of-two scaling followed by
+// one rounding to nearest even, clamped to 448.  Fills 8 words of codes (element
+// 4j + b in byte b of word j) and returns the scale code.
+__device__ __forceinline__ uint32_t mx_quantize32(const uint32_t (&w)[16], uint32_t (&q)[8]) {
+  uint32_t amax = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = max(amax, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+  const uint32_t e = amax >> 7;
+  const uint32_t code = e > 8u ? e - 8u : 0u;
+  const float inv = __uint_as_float((254u - code) << 23);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float v0 = __uint_as_float(w[2 * j] << 16) * inv;
+    const float v1 = __uint_as_float(w[2 * j] & 0xFFFF0000u) * inv;
+    const float v2 = __uint_as_float(w[2 * j + 1] << 16) * inv;
+    const float v3 = __uint_as_float(w[2 * j + 1] & 0xFFFF0000u) * inv;
+    q[j] = cvt_e4m3x2(v0, v1) | (cvt_e4m3x2(v2, v3) << 16);
+  }
+  return code;
+}
+
+// Byte offset of the scale of row r (r_in_tile = its row within its 128-row tile
+// m_tile) and 32-wide block b in a 128-row scale-tile array with k_stages 128-wide
+// K stages per tile.
+__host__ __device__ __forceinline__ int64_t sf_tile_offset(int64_t m_tile, int64_t k_stages,
+                                                           int32_t r_in_tile, int64_t b) {
+  return (m_tile * k_stages + b / 4) * kSfTileBytes + (r_in_tile % 32) * 16 +
+         (r_in_tile / 32) * 4 + (b % 4);
+}
+
+template <Epi kEpi, Caps kC, bool kPair, bool kStoreGu, Major kMajor, bool kMx = false>
+__global__ void __launch_bounds__(kThreads, 1)
+    ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                    const __grid_constant__ CUtensorMap map_a64,
+                    const __grid_constant__ CUtensorMap map_b, const Args args) {
+  using G = Geo<kMx>;
+  static_assert(!kMx || kMajor == Major::kKMajor, "MXFP8 operands are K-major");
+  static_assert(kMx || kEpi != Epi::kSituMx, "the MXFP8 epilogue needs MXFP8 GEMMs");
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled operand buffers.
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + G::Stages * G::StageBytes);
+  constexpr bool kSituEpi = kEpi == Epi::kSitu || kEpi == Epi::kSituMx;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  // Contractions over rows (both operands MN-major) may be K-grouped.
+  constexpr bool kKG = kMajor == Major::kABMNGrouped;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < G::Stages; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      // Paired: a stage is free once the MMAs of both CTAs have read it (the
+      // peer's multicast writes into this CTA's copy of the stage).
+      mbar_init(smem_u32(&ctl->empty[s]), kPair ? 2 : 1);
+    }
+    for (int b = 0; b < kAccBufs; ++b) {
+      mbar_init(smem_u32(&ctl->acc_full[b]), 1);
+      mbar_init(smem_u32(&ctl->acc_empty[b]), kEpiThreads);
+    }
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+    tma_prefetch_map(&map_a);
+    if (kPair) tma_prefetch_map(&map_a64);
+    tma_prefetch_map(&map_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+    tmem_relinquish();
+    tc_fence_before_sync();
+  }
+  __syncthreads();
+  if (kPair) cluster_sync();  // the peer's barriers exist before any multicast
+  tc_fence_after_sync();
+  const uint32_t tmem_base = ctl->tmem_base;
+  const int32_t n_total = num_units<kPair, kKG>(args);
+  const int32_t u0 = kPair ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x);
+  const int32_t ustride = kPair ? static_cast<int32_t>(gridDim.x >> 1) : static_cast<int32_t>(gridDim.x);
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued = 0;
+      bool ok = true;
+      for (int32_t t = u0; t < n_total && ok; t += ustride) {
+        const TileCoord tc = unit_tile<kPair, kKG>(args, t, rank);
+        const int64_t gbase = static_cast<int64_t>(tc.group) * args.b_group_rows;
+        constexpr bool kBMNp = kMajor != Major::kKMajor;
+        // K-major B: a group's weights are b_group_rows further down the N rows.
+        // MN-major B: they are b_group_rows further down the K rows (grouped by
+        // rows), or the contraction itself starts at k0 (K-grouped).
+        int32_t b_row0, b_row1, kb_off = 0;
+        if (kSituEpi) {
+          b_row0 = static_cast<int32_t>(gbase + static_cast<int64_t>(tc.n_tile) * (G::BN / 2));
+          b_row1 = static_cast<int32_t>(gbase + args.b_up_offset +
+                                        static_cast<int64_t>(tc.n_tile) * (G::BN / 2));
+        } else if (kBMNp) {
+          b_row0 = tc.n_tile * G::BN;
+          b_row1 = b_row0 + 128;
+          kb_off = kKG ? tc.k0 : static_cast<int32_t>(gbase);
+        } else {
+          b_row0 = static_cast<int32_t>(gbase + static_cast<int64_t>(tc.n_tile) * G::BN);
+          b_row1 = b_row0 + G::BHalfRows;
+        }
+        // MXFP8: the unit's scale tiles (A per global m-tile, B per (group, n-tile)).
+        const uint8_t* sfa_unit = nullptr;
+        const uint8_t* sfb_unit = nullptr;
+        if constexpr (kMx) {
+          const int32_t a_tile =
+              args.tile_offsets ? __ldg(args.tile_offsets + tc.group) +
+                                      (tc.a_row0 - __ldg(args.group_offsets + tc.group)) / kBM
+                                : tc.a_row0 / kBM;
+          sfa_unit = args.sfa + static_cast<int64_t>(a_tile) * args.k_blocks * kSfTileBytes;
+          sfb_unit = args.sfb + (static_cast<int64_t>(tc.group) * args.n_tiles + tc.n_tile) *
+                                    args.k_blocks * kSfbStageBytes;
+        }
+        for (int32_t kb = 0; kb < tc.k_blocks; ++kb) {
+          if (!ctl_wait(ctl, &ctl->empty[stage], phase ^ 1u, args.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_u32(&ctl->full[stage]);
+          const uint32_t sa = smem_u32(smem + stage * G::StageBytes);
+          const uint32_t sb = sa + G::ABytes;
+          mbar_arrive_expect_tx(full, G::TxBytes);
+          constexpr bool kAMN = a_mn_major(kMajor);
+          constexpr bool kBMN = kMajor != Major::kKMajor;
+          const int32_t kx = kb * G::BK + tc.k0;     // A's K coordinate
+          const int32_t kxb = kb * G::BK + kb_off;   // B's K coordinate
+          // A (128 rows of the tile); `half` picks one 64-row half for a shared-A unit.
+          auto load_a = [&](uint32_t dst, int32_t row, int rows64, bool mcast) {
+            for (int j = 0; j < rows64; ++j) {
+              const uint32_t d = dst + j * (kAMN ? kMnAtomBytes : 0u);
+              if (kAMN) {
+                if (mcast) tma_load_2d_multicast(d, &map_a, row + 64 * j, kx, full, 0x3);
+                else tma_load_2d(d, &map_a, row + 64 * j, kx, full);
+              } else if (rows64 == 2) {
+                tma_load_2d(d, &map_a, kx, row, full);
+                break;
+              } else {
+                if (mcast) tma_load_2d_multicast(d, &map_a64, kx, row, full, 0x3);
+                else tma_load_2d(d, &map_a64, kx, row, full);
+              }
+            }
+          };
+          // B (128 rows = one half of the 256-row tile).
+          auto load_b = [&](uint32_t dst, int32_t row, bool mcast) {
+            if (kBMN) {
+              for (int j = 0; j < 2; ++j) {
+                if (mcast) tma_load_2d_multicast(dst + j * kMnAtomBytes, &map_b, row + 64 * j, kxb, full, 0x3);
+                else tma_load_2d(dst + j * kMnAtomBytes, &map_b, row + 64 * j, kxb, full);
+              }
+            } else {
+              if (mcast) tma_load_2d_multicast(dst, &map_b, kxb, row, full, 0x3);
+              else tma_load_2d(dst, &map_b, kxb, row, full);
+            }
+          };
+          constexpr uint32_t kBHalf = G::BHalfRows * 128;  // bytes of one B half
+          if (!kPair) {
+            load_a(sa, tc.a_row0, 2, false);
+            load_b(sb, b_row0, false);
+            load_b(sb + kBHalf, b_row1, false);
+          } else if (!tc.share_a) {
+            // Shared B: this CTA fetches one half of the B tile for both CTAs.
+            load_a(sa, tc.a_row0, 2, false);
+            load_b(sb + rank * kBHalf, rank == 0 ? b_row0 : b_row1, true);
+          } else {
+            // Shared A: this CTA fetches 64 of the 128 A rows for both CTAs.
+            load_a(sa + rank * (G::ABytes / 2), tc.a_row0 + static_cast<int32_t>(rank) * 64, 1,
+                   true);
+            load_b(sb, b_row0, false);
+            load_b(sb + kBHalf, b_row1, false);
+          }
+          if constexpr (kMx) {
+            // This CTA's own scale tiles of the stage (not multicast).
+            const uint32_t ssf = sb + G::BBytes;
+            bulk_load(ssf, sfa_unit + static_cast<int64_t>(kb) * kSfTileBytes, kSfTileBytes, full);
+            bulk_load(ssf + kSfTileBytes, sfb_unit + static_cast<int64_t>(kb) * kSfbStageBytes,
+                      kSfbStageBytes, full);
+          }
+          ++issued;
+          if (++stage == G::Stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Drain: wait (bounded) for the copies of the last stages issued.
+        const uint32_t n = issued < G::Stages ? issued : G::Stages;
+        for (uint32_t i = 0; i < n; ++i) {
+          stage = (stage + G::Stages - 1) % G::Stages;
+          if (stage == G::Stages - 1) phase ^= 1u;
+          mbar_wait(smem_u32(&ctl->full[stage]), phase, nullptr, kDrainLimitNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    // Lane 0 waits and issues.  K-grouped contractions run the whole warp: the
+    // last k-block of a group holds the next group's first rows (or fill) past
+    // k_end, and the warp zeroes those K rows of both operands before the MMAs.
+    if (kKG || lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      uint32_t local = 0;
+      bool ok = true;
+      auto wait = [&](uint64_t* bar, uint32_t par) {
+        int w = 1;
+        if (lane == 0) w = ctl_wait(ctl, bar, par, args.status) ? 1 : 0;
+        if (kKG) w = __shfl_sync(0xFFFFFFFFu, w, 0);
+        return w != 0;
+      };
+      for (int32_t t = u0; t < n_total && ok; t += ustride, ++local) {
+        const uint32_t acc = local & 1u;
+        const uint32_t acc_phase = (local >> 1) & 1u;
+        if (!wait(&ctl->acc_empty[acc], acc_phase ^ 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * G::BN;
+        const TileCoord tcm = unit_tile<kPair, kKG>(args, t, rank);
+        const uint32_t idesc = kMx ? idesc_mxf8(kBM, G::BN)
+                                   : (tcm.row_end - tcm.a_row0 <= 64 ? kIdescHalf : kIdesc) |
+                                         (a_mn_major(kMajor) ? kAMnBit : 0u) |
+                                         (kMajor != Major::kKMajor ? kBMnBit : 0u);
+        for (int32_t kb = 0; kb < tcm.k_blocks; ++kb) {
+          if (!wait(&ctl->full[stage], phase)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t sa = smem_u32(smem + stage * G::StageBytes);
+          const uint32_t sb = sa + G::ABytes;
+          if (kKG) {
+            const int32_t kv = tcm.k_end - (tcm.k0 + kb * G::BK);
+            if (kv < G::BK) {
+              zero_k_tail(sa, sb, kv, lane);
+              fence_proxy_async_smem();
+            }
+            __syncwarp();
+          }
+          if (kMx && lane == 0) {
+            // Scales of the stage into this stage's TMEM slot (A: 4 columns, B: 8),
+            // then four K=32 block-scaled MMAs, the k-th reading scale byte k.
+            // tcgen05.cp and tcgen05.mma issued by one thread run in order.
+            const uint32_t sf_t = tmem_base + 2 * G::BN + kSfTmemCols * stage;
+            const uint32_t ssf = sb + G::BBytes;
+            tmem_cp_32x128b_x4(sf_t, ssf);
+            tmem_cp_32x128b_x4(sf_t + 4, ssf + kSfTileBytes);
+            tmem_cp_32x128b_x4(sf_t + 8, ssf + 2 * kSfTileBytes);
+#pragma unroll
+            for (int k = 0; k < G::BK / G::UK; ++k) {
+              umma_mxf8(d_tmem, sw128_kmajor_desc(sa + k * 32), sw128_kmajor_desc(sb + k * 32),
+                        idesc | idesc_mxf8_ids(k, k), sf_t, sf_t + 4, (kb | k) != 0 ? 1u : 0u);
+            }
+            if (kPair) {
+              umma_commit_multicast(smem_u32(&ctl->empty[stage]), 0x3);
+            } else {
+              umma_commit(smem_u32(&ctl->empty[stage]));
+            }
+          } else if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < kBK / kUK; ++k) {
+              // K-major: 16 K elements = 32 bytes along the row; MN-major: 16 K
+              // rows = 2048 bytes.
+              const uint64_t ad = a_mn_major(kMajor)
+                                      ? sw128_mnmajor_desc(sa + k * 2048, kMnAtomBytes)
+                                      : sw128_kmajor_desc(sa + k * kUK * 2);
+              const uint64_t bd = kMajor != Major::kKMajor
+                                      ? sw128_mnmajor_desc(sb + k * 2048, kMnAtomBytes)
+                                      : sw128_kmajor_desc(sb + k * kUK * 2);
+              umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            }
+            if (kPair) {
+              umma_commit_multicast(smem_u32(&ctl->empty[stage]), 0x3);
+            } else {
+              umma_commit(smem_u32(&ctl->empty[stage]));
+            }
+          }
+          if (++stage == G::Stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        // A group without rows issues no MMA: the commit arrives at once and the
+        // epilogue writes zeros.
+        if (lane == 0) umma_commit(smem_u32(&ctl->acc_full[acc]));
+      }
+      if (!ok && lane == 0) {
+        // Drain the MMAs already issued before the tensor memory is freed.
+        umma_commit(smem_u32(&ctl->drain));
+        mbar_wait(smem_u32(&ctl->drain), 0, nullptr, kDrainLimitNs);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int row_in_tile = quarter * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t local = 0;
+    for (int32_t t = u0; t < n_total; t += ustride, ++local) {
+      const uint32_t acc = local & 1u;
+      const uint32_t acc_phase = (local >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = ctl_wait(ctl, &ctl->acc_full[acc], acc_phase, args.status) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const TileCoord tc = unit_tile<kPair, kKG>(args, t, rank);
+      // M=64 tiles (bf16 only): only the first 16 lanes of each quarter hold rows
+      // (16q + lane).
+      const bool half = !kMx && tc.row_end - tc.a_row0 <= 64;
+      const int32_t row = tc.a_row0 + (half ? quarter * 16 + lane : row_in_tile);
+      bool valid = row < tc.row_end && (!half || lane < 16);
+      int64_t out_row = row;
+      // K-grouped: group g's result starts at output row g * out_group_rows; a
+      // group without rows has a zero result.
+      bool zero = false;
+      if (kKG) {
+        out_row += static_cast<int64_t>(tc.group) * args.out_group_rows;
+        zero = tc.k_blocks == 0;
+      }
+      if (valid && args.out_row_index) {
+        out_row = __ldg(args.out_row_index + row);
+        valid = out_row >= 0 && out_row < args.out_rows;
+      }
+      const uint32_t t_acc = tmem_base + lane_addr + acc * G::BN;
+      if (kSituEpi) {
+        // Gate column j of the tile pairs with up column BN/2 + j.
+        constexpr int kHalfN = G::BN / 2;
+        __nv_bfloat16* dst_row = args.out + out_row * args.ldo;
+        int64_t h_tile = 0;
+        if constexpr (kEpi == Epi::kSituMx) {
+          h_tile = args.tile_offsets
+                       ? __ldg(args.tile_offsets + tc.group) +
+                             (tc.a_row0 - __ldg(args.group_offsets + tc.group)) / kBM
+                       : tc.a_row0 / kBM;
+        }
+#pragma unroll 1
+        for (int c = 0; c < kHalfN / 32; ++c) {
+          __syncwarp();  // tcgen05.ld is warp-collective (.sync.aligned)
+          uint32_t g[32], u[32];
+          tmem_ld32(t_acc + c * 32, g);
+          tmem_ld32(t_acc + kHalfN + c * 32, u);
+          tmem_ld_wait2(g, u);
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            w[i] = pack_bf16x2(
+                situ_act<kC>(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]), args.sp),
+                situ_act<kC>(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]),
+                             args.sp));
+          }
+          const int64_t col0 = static_cast<int64_t>(tc.n_tile) * kHalfN + c * 32;
+          if constexpr (kEpi == Epi::kSituMx) {
+            // h rounded to bf16 (w), then one 32-wide MXFP8 block: 32 codes and the
+            // block's scale in the A-operand scale tiles of the next GEMM.
+            if (valid && col0 < args.n_out) {
+              uint32_t q[8];
+              const uint32_t sc = mx_quantize32(w, q);
+              uint8_t* dst = args.h_codes + out_row * args.ldo + col0;
+              st_global_v4(dst, q[0], q[1], q[2], q[3]);
+              st_global_v4(dst + 16, q[4], q[5], q[6], q[7]);
+              args.h_sf[sf_tile_offset(h_tile, args.n_out / 128, row - tc.a_row0, col0 / 32)] =
+                  static_cast<uint8_t>(sc);
+            }
+          } else {
+            if (valid) store_row_chunk(dst_row + col0, w, col0, args.n_out);
+          }
+          if (kStoreGu && valid) {
+            // Pre-activation (g, u) for the backward pass, bf16.
+            uint32_t wg[16], wu[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              wg[i] = pack_bf16x2(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
+              wu[i] = pack_bf16x2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
+            }
+            __nv_bfloat16* gu_row = args.gu_store + out_row * 2 * args.split;
+            store_row_chunk(gu_row + col0, wg, col0, args.n_out);
+            store_row_chunk(gu_row + args.split + col0, wu, col0, args.n_out);
+          }
+        }
+      } else if (kEpi == Epi::kSituBwd) {
+        const __nv_bfloat16* gu_row = args.gu_in + static_cast<int64_t>(row) * 2 * args.split;
+        __nv_bfloat16* dgu_row = args.dgu_out + static_cast<int64_t>(row) * 2 * args.split;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          __syncwarp();
+          uint32_t a[32];
+          tmem_ld32(t_acc + c * 32, a);
+          tmem_ld_wait(a);
+          const int64_t col0 = static_cast<int64_t>(tc.n_tile) * G::BN + c * 32;
+          if (!valid) continue;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int64_t cv = col0 + 8 * v;
+            if (cv + 8 > args.n_out) continue;
+            const uint4 gv = *reinterpret_cast<const uint4*>(gu_row + cv);
+            const uint4 uv = *reinterpret_cast<const uint4*>(gu_row + args.split + cv);
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+            const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+            uint32_t og[4], ou[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float pg0, pu0, pg1, pu1;
+              situ_act_grad<kC>(__uint_as_float(gw[i] << 16), __uint_as_float(uw[i] << 16),
+                                args.sp, pg0, pu0);
+              situ_act_grad<kC>(__uint_as_float(gw[i] & 0xFFFF0000u),
+                                __uint_as_float(uw[i] & 0xFFFF0000u), args.sp, pg1, pu1);
+              const float dh0 = __uint_as_float(a[8 * v + 2 * i]);
+              const float dh1 = __uint_as_float(a[8 * v + 2 * i + 1]);
+              og[i] = pack_bf16x2(dh0 * pg0, dh1 * pg1);
+              ou[i] = pack_bf16x2(dh0 * pu0, dh1 * pu1);
+            }
+            st_global_v4(dgu_row + cv, og[0], og[1], og[2], og[3]);
+            st_global_v4(dgu_row + args.split + cv, ou[0], ou[1], ou[2], ou[3]);
+          }
+        }
+      } else {
+        __nv_bfloat16* dst_row = args.out + out_row * args.ldo;
+#pragma unroll 1
+        for (int c = 0; c < G::BN / 32; ++c) {
+          __syncwarp();
+          uint32_t a[32];
+          tmem_ld32(t_acc + c * 32, a);
+          tmem_ld_wait(a);
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            w[i] = zero ? 0u
+                        : pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+          }
+          const int64_t col0 = static_cast<int64_t>(tc.n_tile) * G::BN + c * 32;
+          if (valid) store_row_chunk(dst_row + col0, w, col0, args.n_out);
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&ctl->acc_empty[acc]));
+    }
+  }
+
+  __syncthreads();
+  // Paired: neither CTA leaves while the peer may still write into it.
+  if (kPair) cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+  }
+  return fn;
+}
+
+// 2-D map over a row-major [rows, cols] matrix of bf16 (64 x box_rows boxes) or of
+// bytes (MXFP8 codes: 128 x box_rows boxes) -- 128 bytes a box row, 128-byte swizzle
+// (the layout sw128_kmajor_desc describes), zero fill out of bounds.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
+              uint32_t box_rows = 128, int64_t ld = 0, bool bytes = false) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+  if (!enc) return false;
+  const int64_t esz = bytes ? 1 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld > 0 ? ld : cols) * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                   2, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool kMx>
+constexpr size_t smem_bytes() {
+  return Geo<kMx>::Stages * Geo<kMx>::StageBytes + sizeof(SharedCtl) + 1024;
+}
+static_assert(smem_bytes<true>() <= 232448 && smem_bytes<false>() <= 232448,
+              "shared memory per CTA");
+
+// Most 2-CTA clusters of ffn_gemm_kernel<kEpi, kC, true, ...> resident at once,
+// per device (0 if the query fails: the unpaired kernel is used then).
+template <Epi kEpi, Caps kC, bool kStoreGu, Major kMajor, bool kMx>
+int max_pair_clusters(size_t smem) {
+  static int cached[64] = {};
+  static bool done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!done[dev]) {
+    done[dev] = true;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx>,
+                                       &cfg) == cudaSuccess)
+      cached[dev] = n;
+    else
+      (void)cudaGetLastError();
+  }
+  return cached[dev];
+}
+
+template <Epi kEpi, Caps kC, bool kStoreGu = false, Major kMajor = Major::kKMajor,
+          bool kMx = false>
+cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, int num_sms,
+                   cudaStream_t stream) {
+  using G = Geo<kMx>;
+  constexpr size_t kSmem = smem_bytes<kMx>();
+  static_assert(kEpi != Epi::kSitu || kMajor == Major::kKMajor,
+                "the SiTU epilogue pairs gate and up rows of a K-major B");
+  if (s.a_rows == 0 && !s.tile_offsets) return cudaSuccess;
+  if (kMx && (!s.sfa || !s.sfb || s.K % G::BK != 0)) return cudaErrorInvalidValue;
+  if ((s.k_group_offsets != nullptr) != (kMajor == Major::kABMNGrouped))
+    return cudaErrorInvalidValue;
+  CUtensorMap ma, ma64, mb;
+  bool ok;
+  if (a_mn_major(kMajor)) {
+    // A stored [K, rows]: {64 rows, 64 K} boxes.
+    ok = make_map(&ma, s.a, s.K, s.a_rows, 64, s.a_ld);
+    ma64 = ma;
+  } else {
+    ok = make_map(&ma, s.a, s.a_rows, s.K, 128, s.a_ld, kMx) &&
+         make_map(&ma64, s.a, s.a_rows, s.K, 64, s.a_ld, kMx);
+  }
+  if (kMajor != Major::kKMajor) {
+    // B stored [K, N]; grouped by rows, the groups' K-row blocks are stacked.
+    const int64_t b_k_rows =
+        (s.group_offsets && !s.k_group_offsets) ? s.b_group_rows * s.num_groups : s.K;
+    ok = ok && make_map(&mb, s.b, b_k_rows, s.b_rows, 64, s.b_ld);
+  } else {
+    ok = ok && make_map(&mb, s.b, s.b_rows, s.K, G::BHalfRows, s.b_ld, kMx);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  Args a;
+  a.num_groups = s.num_groups;
+  a.group_offsets = s.group_offsets;
+  a.tile_offsets = s.tile_offsets;
+  a.unit_offsets = nullptr;
+  a.dense_rows = static_cast<int32_t>(s.a_rows);
+  const int64_t out_cols_per_tile =
+      (kEpi == Epi::kSitu || kEpi == Epi::kSituMx) ? G::BN / 2 : G::BN;
+  a.n_tiles = static_cast<int32_t>((s.n_out + out_cols_per_tile - 1) / out_cols_per_tile);
+  a.k_blocks = static_cast<int32_t>((s.K + G::BK - 1) / G::BK);
+  a.b_group_rows = s.b_group_rows;
+  a.b_up_offset = s.b_up_offset;
+  a.n_out = s.n_out;
+  a.out = static_cast<__nv_bfloat16*>(s.out);
+  a.ldo = s.ldo;
+  a.out_rows = s.out_rows;
+  a.out_row_index = s.out_row_index;
+  a.sp = p;
+  a.status = status;
+  a.gu_store = static_cast<__nv_bfloat16*>(s.gu_store);
+  a.gu_in = static_cast<const __nv_bfloat16*>(s.gu_in);
+  a.dgu_out = static_cast<__nv_bfloat16*>(s.dgu_out);
+  a.split = s.split;
+  a.k_group_offsets = s.k_group_offsets;
+  a.out_group_rows = s.out_group_rows;
+  a.units_per_group = 0;
+  a.sfa = static_cast<const uint8_t*>(s.sfa);
+  a.sfb = static_cast<const uint8_t*>(s.sfb);
+  a.h_codes = static_cast<uint8_t*>(s.h_codes);
+  a.h_sf = static_cast<uint8_t*>(s.h_sf);
+  const int64_t m_tiles = (s.a_rows + kBM - 1) / kBM;
+  // The shared-memory opt-in is a per-device property of each kernel: set once.
+  static bool smem_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!smem_set[dev]) {
+    for (auto fn : {ffn_gemm_kernel<kEpi, kC, false, kStoreGu, kMajor, kMx>,
+                    ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx>}) {
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kSmem));
+      if (e != cudaSuccess) return e;
+    }
+    smem_set[dev] = true;
+  }
+  int clusters = max_pair_clusters<kEpi, kC, kStoreGu, kMajor, kMx>(kSmem);
+  const int64_t pair_units = (m_tiles / 2) * a.n_tiles + (m_tiles % 2) * ((a.n_tiles + 1) / 2);
+  if (clusters > 0 && (!s.tile_offsets || s.unit_offsets || s.k_group_offsets)) {
+    // Clusters of two CTAs sharing a B or an A tile by multicast.
+    a.unit_offsets = s.unit_offsets;
+    if (s.k_group_offsets) {
+      a.units_per_group = static_cast<int32_t>(pair_units);
+      const int64_t units = pair_units * s.num_groups;
+      if (units < clusters) clusters = static_cast<int>(units < 1 ? 1 : units);
+    } else if (!s.tile_offsets) {
+      if (pair_units < clusters) clusters = static_cast<int>(pair_units);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx>, ma,
+                              ma64, mb, a);
+  }
+  int grid = num_sms;
+  if (s.k_group_offsets) {
+    a.units_per_group = static_cast<int32_t>(m_tiles * a.n_tiles);
+    const int64_t units = m_tiles * a.n_tiles * s.num_groups;
+    if (units < grid) grid = static_cast<int>(units < 1 ? 1 : units);
+  } else if (!s.tile_offsets) {
+    const int64_t tiles = m_tiles * a.n_tiles;
+    if (tiles < grid) grid = static_cast<int>(tiles);
+  }
+  ffn_gemm_kernel<kEpi, kC, false, kStoreGu, kMajor, kMx>
+      <<<grid, kThreads, kSmem, stream>>>(ma, ma64, mb, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace situ

@@ -78,6 +78,15 @@ struct GemmShape {
   // validation) makes the GEMM do nothing.
   const int32_t* k_group_offsets;
   int64_t out_group_rows;
+  // MXFP8 operands (launch_mx_gemm_*): A and B are E4M3 codes (row-major, K
+  // contiguous, K a multiple of 128); sfa / sfb their E8M0 scale tiles (A: 512 bytes
+  // per 128-row m-tile and 128-wide K stage; B: 1024 bytes per (group, n-tile) and K
+  // stage).  h_codes / h_sf: the SiTU epilogue's MXFP8 output (codes [rows, ldo],
+  // scale tiles in the A layout with n_out / 128 K stages), or null for bf16 h.
+  const void* sfa;
+  const void* sfb;
+  void* h_codes;
+  void* h_sf;
   // SiTU epilogue: optional bf16 store of the pre-activation (g, u), [rows, 2*split].
   void* gu_store;
   // Backward epilogue: saved (g, u) in, d(g, u) out, both [rows, 2*split] bf16.
@@ -97,6 +106,38 @@ cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
 // activation's partial derivatives at the saved (g, u).
 cudaError_t launch_gemm_situ_bwd(const GemmShape& s, const SituParams& p, Caps caps,
                                  uint32_t* status, int num_sms, cudaStream_t stream);
+
+// ----- MXFP8 block-scaled GEMMs (mx_gemm.cu) ------------------------------------
+// Tile widths of the MXFP8 GEMMs: 96 activation columns per SiTU tile (gate rows
+// and up rows of B in two 96-row halves), 192 output columns per plain tile.
+constexpr int kMxSituCols = 96;
+constexpr int kMxPlainCols = 192;
+// gu = A B^T (MXFP8) with the SiTU-GLU epilogue: bf16 h into s.out, or MXFP8 h into
+// s.h_codes / s.h_sf when s.h_codes is set.
+cudaError_t launch_mx_gemm_situ(const GemmShape& s, const SituParams& p, Caps caps,
+                                uint32_t* status, int num_sms, cudaStream_t stream);
+// C = A B^T (MXFP8), bf16 output.
+cudaError_t launch_mx_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
+                                 cudaStream_t stream);
+// MXFP8 quantization of bf16 rows [R, K] (K % 128 == 0) into codes [R, K] and A-layout
+// scale tiles.  Row r is read from src row (row_index ? row_index[r] / k_eff : r);
+// with group offsets (and their m-tile prefix) the tiles follow the groups' m-tiles.
+// sf_tiles bounds the scale tiles written (a row mapping outside is recorded as
+// SITU_ERR_INDEX and skipped).
+cudaError_t launch_mx_quantize_act(const void* src, const int32_t* row_index, int32_t k_eff,
+                                   int64_t src_rows, void* codes, void* scales, int64_t sf_tiles,
+                                   int64_t R, int64_t K, int32_t num_groups,
+                                   const int32_t* group_offsets, const int32_t* tile_offsets,
+                                   uint32_t* status, cudaStream_t stream);
+// MXFP8 quantization of G stacked weight matrices [rows_per_group, K] into codes and
+// B-layout scale tiles: split > 0 pairs gate row j < split with up row split + j in
+// tiles of 96 + 96 rows (the SiTU GEMM's B); split == 0 cuts plain 192-row tiles.
+cudaError_t launch_mx_quantize_weights(const void* w, void* codes, void* scales, int32_t G,
+                                       int64_t rows_per_group, int64_t K, int64_t split,
+                                       cudaStream_t stream);
+// Scale bytes of those layouts.
+size_t mx_act_scale_bytes(int64_t R, int64_t K);
+size_t mx_weight_scale_bytes(int32_t G, int64_t rows_per_group, int64_t K, int64_t split);
 
 // Per-group prefixes of m-tiles and of the paired units of two grouped GEMMs with
 // n_tiles_1 and n_tiles_2 output tiles per m-tile, plus validation of the offsets.

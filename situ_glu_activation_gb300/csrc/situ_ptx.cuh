@@ -279,6 +279,62 @@ __device__ __forceinline__ void tmem_ld_wait2(uint32_t (&a)[32], uint32_t (&b)[3
                : "memory");
 }
 
+// Untiled bulk copy global -> this CTA's shared memory, completing on an mbarrier
+// (both addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Copy 32 rows x 16 bytes of shared memory (no swizzle, rows 16 bytes apart) into
+// 4 TMEM columns of every lane quadrant: lane 32 q + l receives row l.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint32_t saddr) {
+  const uint64_t desc = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4)
+                        | (static_cast<uint64_t>(128 >> 4) << 16)  // leading byte offset
+                        | (static_cast<uint64_t>(128 >> 4) << 32)  // 8-row groups 128 B apart
+                        | (static_cast<uint64_t>(1) << 46);        // descriptor version
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+               : "memory");
+}
+
+// D[tmem] (+)= (A * scale_A) (B * scale_B)^T with E4M3 A and B (K-major), E8M0
+// scales read from TMEM per 32 K, FP32 accumulator; shape and scale bytes from idesc.
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of tcgen05.mma kind::mxf8f6f4 block-scaled: E4M3 A and B
+// (both K-major), E8M0 scales, tile M x N; the scale byte k (0..3) of A and B is
+// selected by sf_a_id / sf_b_id (idesc_mxf8_ids).
+__host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t m, uint32_t n) {
+  return (0u << 7)            // A format: E4M3
+         | (0u << 10)         // B format: E4M3
+         | ((n >> 3) << 17)   // N / 8
+         | (1u << 23)         // scale format: E8M0
+         | ((m >> 4) << 24);  // M / 16
+}
+__host__ __device__ constexpr uint32_t idesc_mxf8_ids(uint32_t sf_a_id, uint32_t sf_b_id) {
+  return (sf_b_id << 4) | (sf_a_id << 29);
+}
+
+// Two floats -> two E4M3 bytes, round to nearest even, magnitudes past 448 clamped
+// to 448 (satfinite); lo lands in the low byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // 16 zero bytes into this CTA's shared memory (generic proxy).
 __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
