@@ -54,6 +54,7 @@ constexpr uint32_t kMnAtomBytes = 64 * 64 * 2;
 //     K = 32 per MMA.  B arrives as two 96-row halves.
 template <bool kMx>
 struct Geo {
+  static constexpr int Threads = kThreads;
   static constexpr int BN = 256, BK = 64, UK = 16, Stages = 4, BHalfRows = 128;
   static constexpr uint32_t ABytes = 16384, BBytes = 32768, SfBytes = 0;
   static constexpr uint32_t TxBytes = ABytes + BBytes;  // bytes the copies of a stage bring
@@ -61,6 +62,11 @@ struct Geo {
 };
 template <>
 struct Geo<true> {
+  // A seventh warp copies each stage's scale tiles into TMEM as soon as the stage
+  // lands, so the MMA warp never issues a tcgen05.cp in front of its own MMAs (a
+  // copy issued right before the MMAs that read it held the tensor pipe ~20 % idle,
+  // measured on GB300).
+  static constexpr int Threads = kThreads + 32;
   static constexpr int BN = 192, BK = 128, UK = 32, Stages = 5, BHalfRows = 96;
   static constexpr uint32_t ABytes = 16384, BBytes = 24576, SfBytes = 512 + 1024;
   static constexpr uint32_t TxBytes = ABytes + BBytes + SfBytes;
@@ -133,6 +139,8 @@ struct SharedCtl {
   uint64_t acc_full[kAccBufs];
   uint64_t acc_empty[kAccBufs];
   uint64_t drain;
+  uint64_t sf_ready[kMaxStages];  // MXFP8: the stage's scales are in TMEM
+  uint64_t sf_drain;
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -363,7 +371,7 @@ __host__ __device__ __forceinline__ int64_t sf_tile_offset(int64_t m_tile, int64
 }
 
 template <Epi kEpi, Caps kC, bool kPair, bool kStoreGu, Major kMajor, bool kMx = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_a64,
                     const __grid_constant__ CUtensorMap map_b, const Args args) {
@@ -395,6 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&ctl->acc_empty[b]), kEpiThreads);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
+    if (kMx) {
+      for (int s = 0; s < G::Stages; ++s) mbar_init(smem_u32(&ctl->sf_ready[s]), 1);
+      mbar_init(smem_u32(&ctl->sf_drain), 1);
+    }
     ctl->abort = 0;
     fence_mbar_init();
     tma_prefetch_map(&map_a);
@@ -563,7 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          (a_mn_major(kMajor) ? kAMnBit : 0u) |
                                          (kMajor != Major::kKMajor ? kBMnBit : 0u);
         for (int32_t kb = 0; kb < tcm.k_blocks; ++kb) {
-          if (!wait(&ctl->full[stage], phase)) {
+          // MXFP8: the scale warp signals once the stage's data and scales are in.
+          if (!wait(kMx ? &ctl->sf_ready[stage] : &ctl->full[stage], phase)) {
             ok = false;
             break;
           }
@@ -579,14 +592,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
           }
           if (kMx && lane == 0) {
-            // Scales of the stage into this stage's TMEM slot (A: 4 columns, B: 8),
-            // then four K=32 block-scaled MMAs, the k-th reading scale byte k.
-            // tcgen05.cp and tcgen05.mma issued by one thread run in order.
+            // Four K=32 block-scaled MMAs, the k-th reading byte k of the stage's
+            // scales in its TMEM slot (A: 4 columns, B: 8).
             const uint32_t sf_t = tmem_base + 2 * G::BN + kSfTmemCols * stage;
-            const uint32_t ssf = sb + G::BBytes;
-            tmem_cp_32x128b_x4(sf_t, ssf);
-            tmem_cp_32x128b_x4(sf_t + 4, ssf + kSfTileBytes);
-            tmem_cp_32x128b_x4(sf_t + 8, ssf + 2 * kSfTileBytes);
 #pragma unroll
             for (int k = 0; k < G::BK / G::UK; ++k) {
               umma_mxf8(d_tmem, sw128_kmajor_desc(sa + k * 32), sw128_kmajor_desc(sb + k * 32),
@@ -630,6 +638,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Drain the MMAs already issued before the tensor memory is freed.
         umma_commit(smem_u32(&ctl->drain));
         mbar_wait(smem_u32(&ctl->drain), 0, nullptr, kDrainLimitNs);
+      }
+    }
+  } else if (kMx && warp == 6) {
+    // ---------------- scale copier (MXFP8) ----------------
+    // Per stage, once its copies landed: the A and B scale tiles into the stage's
+    // TMEM slot, then a commit that tells the MMA warp.  A slot is rewritten only
+    // after its stage was refilled, i.e. after the MMAs that read it completed.
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int32_t t = u0; t < n_total && ok; t += ustride) {
+        const TileCoord tcs = unit_tile<kPair, kKG>(args, t, rank);
+        for (int32_t kb = 0; kb < tcs.k_blocks; ++kb) {
+          if (!ctl_wait(ctl, &ctl->full[stage], phase, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t ssf = smem_u32(smem + stage * G::StageBytes) + G::ABytes + G::BBytes;
+          const uint32_t sf_t = tmem_base + 2 * G::BN + kSfTmemCols * stage;
+          tmem_cp_32x128b_x4(sf_t, ssf);
+          tmem_cp_32x128b_x4(sf_t + 4, ssf + kSfTileBytes);
+          tmem_cp_32x128b_x4(sf_t + 8, ssf + 2 * kSfTileBytes);
+          umma_commit(smem_u32(&ctl->sf_ready[stage]));
+          if (++stage == G::Stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Drain the copies already issued before the tensor memory is freed.
+        umma_commit(smem_u32(&ctl->sf_drain));
+        mbar_wait(smem_u32(&ctl->sf_drain), 0, nullptr, kDrainLimitNs);
       }
     }
   } else {
@@ -847,7 +889,7 @@ int max_pair_clusters(size_t smem) {
     done[dev] = true;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(Geo<kMx>::Threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -955,7 +997,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(G::Threads, 1, 1);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr;
@@ -978,7 +1020,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     if (tiles < grid) grid = static_cast<int>(tiles);
   }
   ffn_gemm_kernel<kEpi, kC, false, kStoreGu, kMajor, kMx>
-      <<<grid, kThreads, kSmem, stream>>>(ma, ma64, mb, a);
+      <<<grid, G::Threads, kSmem, stream>>>(ma, ma64, mb, a);
   return cudaGetLastError();
 }
 
