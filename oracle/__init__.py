@@ -77,6 +77,11 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         ("oracle_e4m3_encode_array", [dp, i64, vp], ci),
         ("oracle_e4m3_decode_array", [vp, i64, dp], ci),
         ("oracle_round_bf16_array", [dp, i64, vp], ci),
+        ("oracle_e2m1_decode", [ctypes.c_uint32], d),
+        ("oracle_e2m1_encode", [d], ctypes.c_uint32),
+        ("oracle_e2m1_encode_array", [dp, i64, vp], ci),
+        ("oracle_mxfp4_quantize", [vp, ci, i64, i64, vp, vp], ci),
+        ("oracle_mxfp4_dequantize", [vp, vp, i64, i64, dp], ci),
     ]:
         fn = getattr(lib, name)
         fn.argtypes = args
@@ -292,15 +297,45 @@ class Oracle:
         _check(self.lib.oracle_mx_dequantize(_ptr(c), _ptr(sc), R, K, _ptr(out)), "mx_dequantize")
         return out
 
-    def mx_ffn_forward(self, xq, wguq, wdq, beta=4.0, linear_beta=25.0):
-        """The SiTU-GLU FFN with MXFP8 operands: each argument is a (codes, scales)
-        pair.  gu and h in FP64 on the decoded x and W_gate_up; h cast to bf16 (the
+    def e2m1_decode(self, c) -> float:
+        return self.lib.oracle_e2m1_decode(int(c))
+
+    def e2m1_encode(self, v) -> np.ndarray:
+        a = np.ascontiguousarray(v, dtype=np.float64)
+        out = np.empty(a.shape, dtype=np.uint8)
+        _check(self.lib.oracle_e2m1_encode_array(_ptr(a), a.size, _ptr(out)), "e2m1_encode")
+        return out
+
+    def mxfp4_quantize(self, a):
+        """MXFP4 quantization of a [R, K] tensor: (codes uint8 [R, K/2], two E2M1 per
+        byte with the even element in the low nibble; scales uint8 [R, K/32])."""
+        src, dt = _as_input(a)
+        R, K = src.shape
+        codes = np.empty((R, K // 2), dtype=np.uint8)
+        scales = np.empty((R, K // 32), dtype=np.uint8)
+        _check(self.lib.oracle_mxfp4_quantize(_ptr(src), dt, R, K, _ptr(codes), _ptr(scales)),
+               "mxfp4_quantize")
+        return codes, scales
+
+    def mxfp4_dequantize(self, codes, scales) -> np.ndarray:
+        c = np.ascontiguousarray(codes, dtype=np.uint8)
+        sc = np.ascontiguousarray(scales, dtype=np.uint8)
+        R, K = c.shape[0], c.shape[1] * 2
+        out = np.empty((R, K))
+        _check(self.lib.oracle_mxfp4_dequantize(_ptr(c), _ptr(sc), R, K, _ptr(out)),
+               "mxfp4_dequantize")
+        return out
+
+    def mx_ffn_forward(self, xq, wguq, wdq, beta=4.0, linear_beta=25.0, weights_fp4=False):
+        """The SiTU-GLU FFN with MXFP8 operands (weights MXFP4 with weights_fp4): each
+        argument is a (codes, scales) pair.  gu and h in FP64 on the decoded x and W_gate_up; h cast to bf16 (the
         pages' cast back to the input dtype), MX-quantized as the down projection's
         input, and y = dequant(h) dequant(W_down)^T in FP64.  Returns
         (y [R, M], h_bf16 bits [R, I], (h codes, h scales))."""
         x = self.mx_dequantize(*xq)
-        wgu = self.mx_dequantize(*wguq)
-        wd = self.mx_dequantize(*wdq)
+        wdeq = self.mxfp4_dequantize if weights_fp4 else self.mx_dequantize
+        wgu = wdeq(*wguq)
+        wd = wdeq(*wdq)
         _, h = self.ffn_forward(x, wgu, wd, beta, linear_beta, want_h=True)
         hb = self.round_bf16(h)
         hq = self.mx_quantize(hb)

@@ -561,6 +561,102 @@ int oracle_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t R,
   return ORACLE_OK;
 }
 
+/* MXFP4 (OCP MX v1.0): element E2M1 -- sign, 2 exponent bits (bias 1), 1 mantissa
+ * bit; exponent field 0 holds the subnormal 0.5 (m * 2^-1); magnitudes 0, 0.5, 1,
+ * 1.5, 2, 3, 4, 6; no infinities or NaN.  A block of 32 shares the E8M0 scale
+ * X = 2^(floor(log2 amax) - 2) (2 = the largest exponent of E2M1); each element is
+ * v / X rounded to E2M1 (ties to the even mantissa), magnitudes past 6 clamped.
+ * Codes are packed two to a byte, element 2j in the low nibble of byte j (the order
+ * the block-scaled MMA reads). */
+double oracle_e2m1_decode(uint32_t code) {
+  const uint32_t c = code & 0xFu;
+  const double sign = (c & 8u) ? -1.0 : 1.0;
+  const int e = (int)((c >> 1) & 3u), m = (int)(c & 1u);
+  if (e == 0) return sign * 0.5 * m;
+  return sign * ldexp(2.0 + m, e - 2); /* (1 + m/2) * 2^(e-1) */
+}
+
+uint32_t oracle_e2m1_encode(double v) {
+  const uint32_t s = signbit(v) ? 8u : 0u;
+  const double a = fabs(v);
+  if (isnan(v)) return s | 7u;
+  if (a == 0.0) return s;
+  int ea;
+  frexp(a, &ea);
+  int fl = ea - 1;
+  if (fl < 0) fl = 0; /* below 1 the subnormal quantum 0.5 */
+  const double q = ldexp(1.0, fl - 1);
+  const double r = nearbyint(a / q) * q;
+  if (r == 0.0) return s;
+  if (r >= 6.0) return s | 7u; /* clamped to the largest magnitude */
+  if (r < 1.0) return s | 1u;  /* 0.5 */
+  int er;
+  frexp(r, &er);
+  const int flr = er - 1;
+  const uint32_t mant = (uint32_t)(r / ldexp(1.0, flr - 1)) - 2u;
+  return s | ((uint32_t)(flr + 1) << 1) | mant;
+}
+
+/* Scale code of a block of elements whose largest exponent is emax_elem. */
+static uint32_t oracle_mx_scale_code_emax(double amax, int emax_elem) {
+  if (!(amax > 0.0)) return 0u;
+  int e;
+  frexp(amax, &e);
+  int x = (e - 1) - emax_elem;
+  if (x < -127) x = -127;
+  if (x > 127) x = 127;
+  return (uint32_t)(x + 127);
+}
+
+/* MXFP4 quantization of a row-major [R, K] tensor (K a multiple of 32): codes
+ * [R, K/2] bytes (two E2M1 codes each), scales [R, K/32] E8M0. */
+int oracle_mxfp4_quantize(const void* src, int dt, int64_t R, int64_t K, uint8_t* codes,
+                          uint8_t* scales) {
+  if (!oracle_dtype_ok(dt) || R < 0 || K <= 0 || K % 32 != 0) return ORACLE_BAD_ARG;
+  if (R == 0) return ORACLE_OK;
+  if (!src || !codes || !scales) return ORACLE_BAD_ARG;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < R; ++r) {
+    for (int64_t b = 0; b < K / 32; ++b) {
+      double amax = 0.0;
+      for (int64_t i = 0; i < 32; ++i) {
+        const double a = fabs(oracle_load(src, dt, r * K + 32 * b + i));
+        if (a > amax) amax = a;
+      }
+      const uint32_t c = oracle_mx_scale_code_emax(amax, 2);
+      const double X = oracle_e8m0_decode(c);
+      scales[r * (K / 32) + b] = (uint8_t)c;
+      for (int64_t i = 0; i < 32; i += 2) {
+        const uint32_t lo = oracle_e2m1_encode(oracle_load(src, dt, r * K + 32 * b + i) / X);
+        const uint32_t hi = oracle_e2m1_encode(oracle_load(src, dt, r * K + 32 * b + i + 1) / X);
+        codes[(r * K + 32 * b + i) / 2] = (uint8_t)(lo | (hi << 4));
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
+int oracle_mxfp4_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t R, int64_t K,
+                            double* out) {
+  if (R < 0 || K <= 0 || K % 32 != 0) return ORACLE_BAD_ARG;
+  if (R == 0) return ORACLE_OK;
+  if (!codes || !scales || !out) return ORACLE_BAD_ARG;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < R; ++r)
+    for (int64_t k = 0; k < K; ++k) {
+      const uint8_t byte = codes[(r * K + k) / 2];
+      const uint32_t c = (k % 2 == 0) ? (byte & 0xFu) : (uint32_t)(byte >> 4);
+      out[r * K + k] = oracle_e2m1_decode(c) * oracle_e8m0_decode(scales[r * (K / 32) + k / 32]);
+    }
+  return ORACLE_OK;
+}
+
+int oracle_e2m1_encode_array(const double* v, int64_t n, uint8_t* out) {
+  if (n < 0 || (n > 0 && (!v || !out))) return ORACLE_BAD_ARG;
+  for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)oracle_e2m1_encode(v[i]);
+  return ORACLE_OK;
+}
+
 /* Elementwise E4M3 encode / decode of arrays (for the tests). */
 int oracle_e4m3_encode_array(const double* v, int64_t n, uint8_t* out) {
   if (n < 0 || (n > 0 && (!v || !out))) return ORACLE_BAD_ARG;

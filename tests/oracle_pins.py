@@ -596,6 +596,58 @@ def pin_mx_ffn_exact_inputs(o):
     np.testing.assert_allclose(y, ref, rtol=1e-13, atol=1e-13)
 
 
+def pin_e2m1(o):
+    """E2M1 against its definition (sign, 2-bit exponent with bias 1, 1-bit mantissa,
+    exponent 0 the subnormal m * 0.5): the eight magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6;
+    rounding by brute force over them with ties to the even mantissa (0.25 -> 0,
+    0.75 -> 1, 2.5 -> 2, 5 -> 4) and magnitudes past 6 clamped."""
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for c in range(16):
+        want = mags[c & 7] * (-1.0 if c & 8 else 1.0)
+        assert o.e2m1_decode(c) == want, c
+    v = np.concatenate([np.linspace(-8, 8, 3201), [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 7.0, 1e9,
+                                                    -0.25, -5.0, -0.0, 0.0, 1e-30]])
+    got = o.e2m1_encode(v)
+    for x, c in zip(v, got):
+        a = min(abs(x), 6.0)
+        d = [abs(a - m) for m in mags]
+        best = min(d)
+        cands = [i for i in range(8) if d[i] == best]
+        want = cands[0] if len(cands) == 1 else [i for i in cands if i % 2 == 0][0]
+        if x < 0 or (x == 0 and np.signbit(x)):
+            want |= 8
+        assert int(c) == want, (x, int(c), want)
+
+
+def pin_mxfp4_quantize(o):
+    """MXFP4 quantization against its definition: scale 2^(floor(log2 amax) - 2) (the
+    block maximum lands in [4, 8) before clamping to 6), codes by brute force, packing
+    with the even element in the low nibble; dequantize inverts the packing."""
+    rng = np.random.default_rng(44)
+    x = rng.normal(0, 1, (5, 64))
+    x[0, :32] = 0.0
+    x[1, 0] = 7.9                      # clamps after scaling
+    xb = o.round_bf16(x)
+    xf = (xb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    codes, scales = o.mxfp4_quantize(xb)
+    assert codes.shape == (5, 32) and scales.shape == (5, 2)
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    deq = o.mxfp4_dequantize(codes, scales)
+    for r in range(5):
+        for b in range(2):
+            blk = xf[r, 32 * b:32 * b + 32]
+            amax = np.abs(blk).max()
+            e = max(-127, int(np.floor(np.log2(amax))) - 2) if amax > 0 else -127
+            assert scales[r, b] == e + 127
+            X = 2.0 ** e
+            for i, v in enumerate(blk):
+                byte = codes[r, (32 * b + i) // 2]
+                c = (byte & 15) if i % 2 == 0 else (byte >> 4)
+                assert c == o.e2m1_encode(np.array([v / X]))[0], (r, b, i)
+                assert deq[r, 32 * b + i] == mags[c & 7] * (-1 if c & 8 else 1) * X
+    assert (codes[0, :16] == 0).all() and scales[0, 0] == 0
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_swiglu_gate_and_gaps,
@@ -625,6 +677,8 @@ ALL_PINS = [
     pin_mx_quantize,
     pin_round_bf16,
     pin_mx_ffn_exact_inputs,
+    pin_e2m1,
+    pin_mxfp4_quantize,
 ]
 
 

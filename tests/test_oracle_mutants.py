@@ -78,6 +78,13 @@ MUTANTS = {
     "e4m3_bias_8": ("return sign * ldexp(8.0 + m, e - 10);", "return sign * ldexp(8.0 + m, e - 11);"),
     "mx_block_scale_of_wrong_block": ("scales[r * (K / 32) + k / 32]", "scales[r * (K / 32) + k / 64]"),
     "bf16_round_truncates": ("r = nearbyint(a / q) * q;", "r = floor(a / q) * q;"),
+    "e2m1_scale_emax_3": ("const uint32_t c = oracle_mx_scale_code_emax(amax, 2);",
+                          "const uint32_t c = oracle_mx_scale_code_emax(amax, 3);"),
+    "e2m1_nibbles_swapped": ("codes[(r * K + 32 * b + i) / 2] = (uint8_t)(lo | (hi << 4));",
+                             "codes[(r * K + 32 * b + i) / 2] = (uint8_t)(hi | (lo << 4));"),
+    "e2m1_truncates": ("const double r = nearbyint(a / q) * q;\n  if (r == 0.0) return s;\n  if (r >= 6.0)",
+                       "const double r = floor(a / q) * q;\n  if (r == 0.0) return s;\n  if (r >= 6.0)"),
+    "e2m1_decode_bias": ("return sign * ldexp(2.0 + m, e - 2);", "return sign * ldexp(2.0 + m, e - 1);"),
     "combine_wrong_weight": ("oracle_load(w, w_dt, t * k_eff + k) * y[(t * k_eff + k) * M + m]",
                              "oracle_load(w, w_dt, t * k_eff) * y[(t * k_eff + k) * M + m]"),
     "combine_dropped_slot": ("for (int32_t k = 0; k < k_eff; ++k)\n        s +=",
