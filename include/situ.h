@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define SITU_ABI_VERSION 1
+#define SITU_ABI_VERSION 2
 
 typedef enum {
   SITU_BF16 = 0, /* bfloat16 storage, FP32 accumulation and activation math */
@@ -405,7 +405,8 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
                                       float linear_beta, situ_dtype dt, void* stream);
 
 /* -------------------------------------------------------------------------
- * MXFP8 experts -- the SiTU-GLU FFN with block-scaled 8-bit operands.
+ * MX experts -- the SiTU-GLU FFN with block-scaled operands: MXFP8 activations
+ * and MXFP8 or MXFP4 expert weights.
  *
  * The "SiTU-GLU" chapter ("Pourquoi un plafond doux"; "Ou SiTU-GLU est utilise")
  * motivates the activation's +/-100 bound by experts that run in MXFP8 / MXFP4.
@@ -415,6 +416,12 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
  * each code is the element divided by its scale, rounded to nearest even, clamped
  * to 448.  Quantization reads bf16 values, so every rounding decision is taken on
  * the bf16 input.
+ *
+ * MXFP4 weights (weight_fmt SITU_MX_E2M1) are the specification's MXFP4: E2M1 codes
+ * (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), one E8M0 scale 2^(floor(log2 amax) - 2)
+ * per 32 elements, codes past 6 clamped, packed two a byte with element 2j in the
+ * low nibble of byte j; they run on the same block-scaled MMA (E4M3 x E2M1) with half
+ * the weight bytes to stream.
  *
  * Codes keep the operand's row-major layout (K contiguous).  Scales are stored
  * in the tiles the block-scaled MMA consumes:
@@ -432,6 +439,8 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
  * ------------------------------------------------------------------------- */
 #define SITU_MX_GATE_UP 0
 #define SITU_MX_DOWN 1
+#define SITU_MX_E4M3 0 /* MXFP8 weight codes, one a byte */
+#define SITU_MX_E2M1 1 /* MXFP4 weight codes, two a byte */
 
 size_t situ_mx_act_scales_size(int64_t R, int64_t K);
 size_t situ_mx_weight_scales_size(int32_t E, int64_t M, int64_t I, int kind);
@@ -443,27 +452,30 @@ situ_status situ_mx_quantize_act(const void* x, void* codes, void* scales, int64
                                  void* stream);
 
 /* Stacked expert weights W [E, rows, K] bf16 (kind SITU_MX_GATE_UP: rows = 2I,
- * K = M; SITU_MX_DOWN: rows = M, K = I) -> codes [E, rows, K] uint8 and scales
- * (weight tiles), written.  A one-time conversion: the weights then stay
- * resident as MXFP8.  Errors: as situ_mx_quantize_act. */
+ * K = M; SITU_MX_DOWN: rows = M, K = I) -> codes (fmt SITU_MX_E4M3: [E, rows, K]
+ * bytes; SITU_MX_E2M1: [E, rows, K / 2] bytes) and scales (weight tiles), written.
+ * A one-time conversion: the weights then stay resident as MXFP8 / MXFP4.
+ * Errors: as situ_mx_quantize_act. */
 situ_status situ_mx_quantize_weights(const void* W, void* codes, void* scales, int32_t E,
-                                     int64_t M, int64_t I, int kind, void* stream);
+                                     int64_t M, int64_t I, int kind, int fmt, void* stream);
 
 /* The packed gate_up projection of MXFP8 x (codes [R, M] + activation scales) by
- * MXFP8 W_gate_up (one expert, SITU_MX_GATE_UP layout), FP32 accumulation, with
- * the SiTU-GLU activation on the accumulators; h [R, I] bf16 written.  Caps as
- * situ_glu_act.  Errors: SITU_ERR_ARG, SITU_ERR_ALIGN, SITU_ERR_ALIAS,
- * SITU_ERR_UNSUPPORTED, SITU_ERR_CUDA; SITU_ERR_TIMEOUT on the device. */
+ * W_gate_up (one expert, SITU_MX_GATE_UP layout, weight_fmt SITU_MX_E4M3 or
+ * SITU_MX_E2M1), FP32 accumulation, with the SiTU-GLU activation on the
+ * accumulators; h [R, I] bf16 written.  Caps as situ_glu_act.  Errors: SITU_ERR_ARG,
+ * SITU_ERR_ALIGN, SITU_ERR_ALIAS, SITU_ERR_UNSUPPORTED, SITU_ERR_CUDA;
+ * SITU_ERR_TIMEOUT on the device. */
 situ_status situ_ffn_gate_up_mxfp8(const void* x_codes, const void* x_scales,
-                                   const void* wgu_codes, const void* wgu_scales, void* h,
-                                   int64_t R, int64_t M, int64_t I, float beta,
+                                   const void* wgu_codes, const void* wgu_scales, int weight_fmt,
+                                   void* h, int64_t R, int64_t M, int64_t I, float beta,
                                    float linear_beta, void* stream);
 
 /* The dense FFN with MXFP8 experts: x [R, M] bf16 is quantized to MXFP8; the gate_up
  * GEMM (block-scaled, FP32 accumulation) applies SiTU-GLU, rounds h to bf16 (the
  * pages' cast back to the input dtype) and writes it as MXFP8 in its epilogue; the
  * down GEMM (block-scaled) writes y [R, M] bf16.
- *   wgu_*, wd_*   device, one expert's weights as situ_mx_quantize_weights wrote them.
+ *   wgu_*, wd_*   device, one expert's weights as situ_mx_quantize_weights wrote them,
+ *                 in format weight_fmt.
  *   workspace     device, >= situ_ffn_mxfp8_workspace_size(R, M, I) bytes, 256-byte
  *                 aligned; regions (each starting 256-byte aligned, in order): x codes
  *                 [R, M], x scales, h codes [R, I], h scales -- after the call they
@@ -471,25 +483,26 @@ situ_status situ_ffn_gate_up_mxfp8(const void* x_codes, const void* x_scales,
  * Errors: those of situ_ffn_gate_up_mxfp8, SITU_ERR_WORKSPACE. */
 size_t situ_ffn_mxfp8_workspace_size(int64_t R, int64_t M, int64_t I);
 situ_status situ_ffn_forward_mxfp8(const void* x, const void* wgu_codes, const void* wgu_scales,
-                                   const void* wd_codes, const void* wd_scales, void* y,
-                                   void* workspace, size_t workspace_bytes, int64_t R, int64_t M,
-                                   int64_t I, float beta, float linear_beta, void* stream);
+                                   const void* wd_codes, const void* wd_scales, int weight_fmt,
+                                   void* y, void* workspace, size_t workspace_bytes, int64_t R,
+                                   int64_t M, int64_t I, float beta, float linear_beta,
+                                   void* stream);
 
 /* situ_moe_grouped_forward with MXFP8 experts: x is gathered into expert order and
  * quantized (scale tiles following each expert's 128-row tiles), then the grouped
  * block-scaled gate_up (h written as MXFP8) and down GEMMs; y [T, k_eff, M] bf16 per
  * (token, slot) as situ_moe_grouped_forward.  Weights [E, ...] as
- * situ_mx_quantize_weights wrote them.  workspace >= situ_moe_mxfp8_workspace_size
+ * situ_mx_quantize_weights wrote them, in format weight_fmt.  workspace >= situ_moe_mxfp8_workspace_size
  * (T * k_eff, E, M, I) bytes, 256-byte aligned.  Errors: those of
  * situ_moe_grouped_forward. */
 size_t situ_moe_mxfp8_workspace_size(int64_t R, int32_t E, int64_t M, int64_t I);
 situ_status situ_moe_grouped_forward_mxfp8(const void* x, const int32_t* expert_offsets,
                                            const int32_t* token_index, const void* wgu_codes,
                                            const void* wgu_scales, const void* wd_codes,
-                                           const void* wd_scales, void* y, void* workspace,
-                                           size_t workspace_bytes, int64_t T, int32_t k_eff,
-                                           int32_t E, int64_t M, int64_t I, float beta,
-                                           float linear_beta, void* stream);
+                                           const void* wd_scales, int weight_fmt, void* y,
+                                           void* workspace, size_t workspace_bytes, int64_t T,
+                                           int32_t k_eff, int32_t E, int64_t M, int64_t I,
+                                           float beta, float linear_beta, void* stream);
 
 /* -------------------------------------------------------------------------
  * situ_moe_combine -- the layer output of a routed batch: for every token t,

@@ -59,14 +59,15 @@ SIGNATURES = {
     "situ_mx_act_scales_size": ([_i64, _i64], _sz),
     "situ_mx_weight_scales_size": ([_i32, _i64, _i64, _ci], _sz),
     "situ_mx_quantize_act": ([_vp, _vp, _vp, _i64, _i64, _vp], _ci),
-    "situ_mx_quantize_weights": ([_vp, _vp, _vp, _i32, _i64, _i64, _ci, _vp], _ci),
-    "situ_ffn_gate_up_mxfp8": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _f32, _vp], _ci),
+    "situ_mx_quantize_weights": ([_vp, _vp, _vp, _i32, _i64, _i64, _ci, _ci, _vp], _ci),
+    "situ_ffn_gate_up_mxfp8": ([_vp, _vp, _vp, _vp, _ci, _vp, _i64, _i64, _i64, _f32, _f32, _vp],
+                               _ci),
     "situ_ffn_mxfp8_workspace_size": ([_i64, _i64, _i64], _sz),
-    "situ_ffn_forward_mxfp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _i64, _f32,
-                                _f32, _vp], _ci),
+    "situ_ffn_forward_mxfp8": ([_vp, _vp, _vp, _vp, _vp, _ci, _vp, _vp, _sz, _i64, _i64, _i64,
+                                _f32, _f32, _vp], _ci),
     "situ_moe_mxfp8_workspace_size": ([_i64, _i32, _i64, _i64], _sz),
-    "situ_moe_grouped_forward_mxfp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64,
-                                        _i32, _i32, _i64, _i64, _f32, _f32, _vp], _ci),
+    "situ_moe_grouped_forward_mxfp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _vp, _vp, _sz,
+                                        _i64, _i32, _i32, _i64, _i64, _f32, _f32, _vp], _ci),
     "situ_selftest_bounded_wait": ([_u32, _vp], _ci),
 }
 

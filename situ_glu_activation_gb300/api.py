@@ -413,6 +413,23 @@ def situ_moe_grouped_backward(x: torch.Tensor, expert_offsets: torch.Tensor,
 # MXFP8 experts
 # ---------------------------------------------------------------------------
 MX_GATE_UP, MX_DOWN = 0, 1
+MX_E4M3, MX_E2M1 = 0, 1  # weight formats: MXFP8, MXFP4
+
+
+class MxWeights(tuple):
+    """Quantized expert weights: (codes, scales, fmt) -- fmt MX_E4M3 (MXFP8, one code
+    a byte) or MX_E2M1 (MXFP4, two codes a byte)."""
+
+    def __new__(cls, codes, scales, fmt=MX_E4M3):
+        return super().__new__(cls, (codes, scales, fmt))
+
+    codes = property(lambda self: self[0])
+    scales = property(lambda self: self[1])
+    fmt = property(lambda self: self[2])
+
+
+def _wfmt(w) -> int:
+    return int(w[2]) if len(w) > 2 else MX_E4M3
 
 
 def mx_act_scales_bytes(R: int, K: int) -> int:
@@ -439,10 +456,11 @@ def mx_quantize_act(x: torch.Tensor):
     return codes, scales
 
 
-def mx_quantize_weights(W: torch.Tensor, kind: int):
-    """MXFP8 quantization of stacked expert weights: kind MX_GATE_UP takes W_gate_up
-    [E, 2I, M] (or [2I, M]), MX_DOWN takes W_down [E, M, I] (or [M, I]).  Returns
-    (codes uint8 of W's shape, scales uint8 in the weight tile layout)."""
+def mx_quantize_weights(W: torch.Tensor, kind: int, fmt: int = MX_E4M3) -> MxWeights:
+    """MX quantization of stacked expert weights: kind MX_GATE_UP takes W_gate_up
+    [E, 2I, M] (or [2I, M]), MX_DOWN takes W_down [E, M, I] (or [M, I]); fmt MX_E4M3
+    (MXFP8) or MX_E2M1 (MXFP4).  Returns MxWeights(codes uint8 of W's shape -- the last
+    dimension halved for MXFP4 --, scales uint8 in the weight tile layout, fmt)."""
     _cuda_contig("W", W)
     if W.dtype != torch.bfloat16:
         raise TypeError("W must be bf16")
@@ -454,21 +472,22 @@ def mx_quantize_weights(W: torch.Tensor, kind: int):
         M, I = rows, K
     else:
         raise ValueError("kind must be MX_GATE_UP or MX_DOWN")
-    codes = torch.empty(W.shape, dtype=torch.uint8, device=W.device)
+    cshape = tuple(W.shape[:-1]) + (K // 2 if fmt == MX_E2M1 else K,)
+    codes = torch.empty(cshape, dtype=torch.uint8, device=W.device)
     scales = torch.empty(max(mx_weight_scales_bytes(E, M, I, kind), 1), dtype=torch.uint8,
                          device=W.device)
     check("situ_mx_quantize_weights",
           _native.lib().situ_mx_quantize_weights(W.data_ptr(), codes.data_ptr(),
-                                                 scales.data_ptr(), E, M, I, kind,
+                                                 scales.data_ptr(), E, M, I, kind, fmt,
                                                  _stream(W.device)))
-    return codes, scales
+    return MxWeights(codes, scales, fmt)
 
 
 def situ_ffn_gate_up_mxfp8(xq, wguq, beta: float = 4.0, linear_beta: float = 25.0):
     """MXFP8 gate_up GEMM + SiTU-GLU: xq = (codes [R, M], scales), wguq = one expert's
     (codes [2I, M], scales) -> h [R, I] bf16."""
-    xc, xs = xq
-    wc, ws = wguq
+    xc, xs = xq[0], xq[1]
+    wc, ws = wguq[0], wguq[1]
     for n, t in (("x codes", xc), ("x scales", xs), ("W codes", wc), ("W scales", ws)):
         _cuda_contig(n, t)
     R, M = xc.shape
@@ -476,7 +495,7 @@ def situ_ffn_gate_up_mxfp8(xq, wguq, beta: float = 4.0, linear_beta: float = 25.
     h = torch.empty(R, I, dtype=torch.bfloat16, device=xc.device)
     check("situ_ffn_gate_up_mxfp8",
           _native.lib().situ_ffn_gate_up_mxfp8(xc.data_ptr(), xs.data_ptr(), wc.data_ptr(),
-                                               ws.data_ptr(), h.data_ptr(), R, M, I,
+                                               ws.data_ptr(), _wfmt(wguq), h.data_ptr(), R, M, I,
                                                *caps(beta, linear_beta), _stream(xc.device)))
     return h
 
@@ -488,8 +507,9 @@ def ffn_mxfp8_workspace_bytes(R: int, M: int, I: int) -> int:
 def situ_ffn_forward_mxfp8(x: torch.Tensor, wguq, wdq, beta: float = 4.0,
                            linear_beta: float = 25.0, y: torch.Tensor | None = None,
                            workspace: torch.Tensor | None = None) -> torch.Tensor:
-    """Dense SiTU-GLU FFN with MXFP8 experts: x [R, M] bf16, wguq / wdq one expert's
-    quantized weights (from mx_quantize_weights) -> y [R, M] bf16."""
+    """Dense SiTU-GLU FFN with MX experts: x [R, M] bf16 (quantized to MXFP8), wguq /
+    wdq one expert's quantized weights (MXFP8 or MXFP4, from mx_quantize_weights) ->
+    y [R, M] bf16."""
     _cuda_contig("x", x)
     M = x.shape[-1]
     R = x.numel() // M
@@ -504,7 +524,8 @@ def situ_ffn_forward_mxfp8(x: torch.Tensor, wguq, wdq, beta: float = 4.0,
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     check("situ_ffn_forward_mxfp8",
           lib.situ_ffn_forward_mxfp8(x.data_ptr(), wguq[0].data_ptr(), wguq[1].data_ptr(),
-                                     wdq[0].data_ptr(), wdq[1].data_ptr(), y.data_ptr(),
+                                     wdq[0].data_ptr(), wdq[1].data_ptr(), _wfmt(wguq),
+                                     y.data_ptr(),
                                      workspace.data_ptr(),
                                      workspace.numel() * workspace.element_size(), R, M, I,
                                      *caps(beta, linear_beta), _stream(x.device)))
@@ -527,6 +548,8 @@ def situ_moe_grouped_forward_mxfp8(x: torch.Tensor, expert_offsets: torch.Tensor
     T, M = x.shape
     E, twoI, _ = wguq[0].shape
     I = twoI // 2
+    if wguq[0].shape[-1] * (2 if _wfmt(wguq) == MX_E2M1 else 1) != M:
+        raise ValueError("gate_up codes do not match x")
     if y is None:
         y = torch.empty(T, k_eff, M, dtype=x.dtype, device=x.device)
     R = T * k_eff
@@ -540,7 +563,8 @@ def situ_moe_grouped_forward_mxfp8(x: torch.Tensor, expert_offsets: torch.Tensor
           lib.situ_moe_grouped_forward_mxfp8(
               x.data_ptr(), expert_offsets.data_ptr(), token_index.data_ptr(),
               wguq[0].data_ptr(), wguq[1].data_ptr(), wdq[0].data_ptr(), wdq[1].data_ptr(),
-              y.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+              _wfmt(wguq), y.data_ptr(), workspace.data_ptr(),
+              workspace.numel() * workspace.element_size(),
               T, k_eff, E, M, I, *caps(beta, linear_beta), _stream(x.device)))
     return y
 
@@ -584,7 +608,7 @@ __all__ = [
     "device_status", "selftest_bounded_wait", "ffn_host_workspace_bytes", "situ_moe_combine",
     "situ_ffn_forward_train", "situ_ffn_backward", "ffn_backward_workspace_bytes",
     "situ_moe_grouped_forward_train", "situ_moe_grouped_backward", "moe_backward_workspace_bytes",
-    "MX_GATE_UP", "MX_DOWN", "mx_act_scales_bytes", "mx_weight_scales_bytes", "mx_quantize_act",
+    "MX_GATE_UP", "MX_DOWN", "MX_E4M3", "MX_E2M1", "MxWeights", "mx_act_scales_bytes", "mx_weight_scales_bytes", "mx_quantize_act",
     "mx_quantize_weights", "situ_ffn_gate_up_mxfp8", "situ_ffn_forward_mxfp8",
     "ffn_mxfp8_workspace_bytes", "situ_moe_grouped_forward_mxfp8", "moe_mxfp8_workspace_bytes",
 ]

@@ -816,6 +816,11 @@ int64_t mx_weight_k(int kind, int64_t M, int64_t I) { return kind == SITU_MX_GAT
 int64_t mx_weight_split(int kind, int64_t I) { return kind == SITU_MX_GATE_UP ? I : 0; }
 
 bool mx_shape_ok(int64_t M, int64_t I) { return M >= 128 && I >= 128 && M % 128 == 0 && I % 128 == 0; }
+bool mx_fmt_ok(int fmt) { return fmt == SITU_MX_E4M3 || fmt == SITU_MX_E2M1; }
+// Bytes of the codes of E weight matrices [rows, K] in format fmt.
+size_t mx_weight_code_bytes(int32_t E, int64_t rows, int64_t K, int fmt) {
+  return static_cast<size_t>(E) * rows * (fmt == SITU_MX_E2M1 ? K / 2 : K);
+}
 
 }  // namespace
 
@@ -850,14 +855,16 @@ situ_status situ_mx_quantize_act(const void* x, void* codes, void* scales, int64
 }
 
 situ_status situ_mx_quantize_weights(const void* W, void* codes, void* scales, int32_t E,
-                                     int64_t M, int64_t I, int kind, void* stream) {
-  if (E < 1 || M < 1 || I < 1 || (kind != SITU_MX_GATE_UP && kind != SITU_MX_DOWN))
+                                     int64_t M, int64_t I, int kind, int fmt, void* stream) {
+  if (E < 1 || M < 1 || I < 1 || (kind != SITU_MX_GATE_UP && kind != SITU_MX_DOWN) ||
+      !mx_fmt_ok(fmt))
     return SITU_ERR_ARG;
   if (!mx_shape_ok(M, I)) return SITU_ERR_UNSUPPORTED;
   if (!W || !codes || !scales) return SITU_ERR_ARG;
   if (!aligned16(W) || !aligned16(codes)) return SITU_ERR_ALIGN;
   const int64_t rows = mx_weight_rows(kind, M, I), K = mx_weight_k(kind, M, I);
-  const size_t wb = static_cast<size_t>(E) * rows * K * 2, cb = static_cast<size_t>(E) * rows * K,
+  const size_t wb = static_cast<size_t>(E) * rows * K * 2,
+               cb = mx_weight_code_bytes(E, rows, K, fmt),
                sb = situ_mx_weight_scales_size(E, M, I, kind);
   if (overlap(codes, cb, W, wb) || overlap(scales, sb, W, wb) || overlap(codes, cb, scales, sb))
     return SITU_ERR_ALIAS;
@@ -865,7 +872,7 @@ situ_status situ_mx_quantize_weights(const void* W, void* codes, void* scales, i
   situ_status s = device_state(&st);
   if (s != SITU_OK) return s;
   return finish(launch_mx_quantize_weights(W, codes, scales, E, rows, K,
-                                           mx_weight_split(kind, I),
+                                           mx_weight_split(kind, I), fmt == SITU_MX_E2M1,
                                            static_cast<cudaStream_t>(stream)));
 }
 
@@ -876,8 +883,10 @@ cudaError_t run_mx_gate_up(const DeviceState* st, const void* x_codes, const voi
                            const void* wgu_codes, const void* wgu_scales, void* h, void* h_codes,
                            void* h_sf, int64_t R, int64_t M, int64_t I, float beta,
                            float linear_beta, int32_t E, const int32_t* offsets,
-                           const int32_t* tiles, const int32_t* units, cudaStream_t cs) {
+                           const int32_t* tiles, const int32_t* units, bool fp4,
+                           cudaStream_t cs) {
   GemmShape g{};
+  g.b_fp4 = fp4;
   g.a = x_codes;
   g.a_rows = R;
   g.b = wgu_codes;
@@ -905,8 +914,9 @@ cudaError_t run_mx_down(const DeviceState* st, const void* h_codes, const void* 
                         const void* wd_codes, const void* wd_scales, void* y, int64_t R,
                         int64_t M, int64_t I, int32_t E, const int32_t* offsets,
                         const int32_t* tiles, const int32_t* units, const int32_t* row_index,
-                        cudaStream_t cs) {
+                        bool fp4, cudaStream_t cs) {
   GemmShape d{};
+  d.b_fp4 = fp4;
   d.a = h_codes;
   d.a_rows = R;
   d.b = wd_codes;
@@ -944,10 +954,11 @@ MxFfnWs mx_ffn_ws(int64_t R, int64_t M, int64_t I) {
 }  // namespace
 
 situ_status situ_ffn_gate_up_mxfp8(const void* x_codes, const void* x_scales,
-                                   const void* wgu_codes, const void* wgu_scales, void* h,
-                                   int64_t R, int64_t M, int64_t I, float beta,
+                                   const void* wgu_codes, const void* wgu_scales, int weight_fmt,
+                                   void* h, int64_t R, int64_t M, int64_t I, float beta,
                                    float linear_beta, void* stream) {
-  if (R < 0 || M < 1 || I < 1 || !caps_ok(beta, linear_beta)) return SITU_ERR_ARG;
+  if (R < 0 || M < 1 || I < 1 || !caps_ok(beta, linear_beta) || !mx_fmt_ok(weight_fmt))
+    return SITU_ERR_ARG;
   if (!mx_shape_ok(M, I)) return SITU_ERR_UNSUPPORTED;
   if (R == 0) return SITU_OK;
   if (!x_codes || !x_scales || !wgu_codes || !wgu_scales || !h) return SITU_ERR_ARG;
@@ -958,7 +969,7 @@ situ_status situ_ffn_gate_up_mxfp8(const void* x_codes, const void* x_scales,
   const size_t hb = static_cast<size_t>(R) * I * 2;
   if (overlap(h, hb, x_codes, static_cast<size_t>(R) * M) ||
       overlap(h, hb, x_scales, mx_act_scale_bytes(R, M)) ||
-      overlap(h, hb, wgu_codes, static_cast<size_t>(2 * I) * M) ||
+      overlap(h, hb, wgu_codes, mx_weight_code_bytes(1, 2 * I, M, weight_fmt)) ||
       overlap(h, hb, wgu_scales, situ_mx_weight_scales_size(1, M, I, SITU_MX_GATE_UP)))
     return SITU_ERR_ALIAS;
   DeviceState* st = nullptr;
@@ -966,7 +977,7 @@ situ_status situ_ffn_gate_up_mxfp8(const void* x_codes, const void* x_scales,
   if (s != SITU_OK) return s;
   return finish(run_mx_gate_up(st, x_codes, x_scales, wgu_codes, wgu_scales, h, nullptr, nullptr,
                                R, M, I, beta, linear_beta, 1, nullptr, nullptr, nullptr,
-                               static_cast<cudaStream_t>(stream)));
+                               weight_fmt == SITU_MX_E2M1, static_cast<cudaStream_t>(stream)));
 }
 
 size_t situ_ffn_mxfp8_workspace_size(int64_t R, int64_t M, int64_t I) {
@@ -975,10 +986,12 @@ size_t situ_ffn_mxfp8_workspace_size(int64_t R, int64_t M, int64_t I) {
 }
 
 situ_status situ_ffn_forward_mxfp8(const void* x, const void* wgu_codes, const void* wgu_scales,
-                                   const void* wd_codes, const void* wd_scales, void* y,
-                                   void* workspace, size_t workspace_bytes, int64_t R, int64_t M,
-                                   int64_t I, float beta, float linear_beta, void* stream) {
-  if (R < 0 || M < 1 || I < 1 || !caps_ok(beta, linear_beta)) return SITU_ERR_ARG;
+                                   const void* wd_codes, const void* wd_scales, int weight_fmt,
+                                   void* y, void* workspace, size_t workspace_bytes, int64_t R,
+                                   int64_t M, int64_t I, float beta, float linear_beta,
+                                   void* stream) {
+  if (R < 0 || M < 1 || I < 1 || !caps_ok(beta, linear_beta) || !mx_fmt_ok(weight_fmt))
+    return SITU_ERR_ARG;
   if (!mx_shape_ok(M, I)) return SITU_ERR_UNSUPPORTED;
   if (R == 0) return SITU_OK;
   if (!x || !wgu_codes || !wgu_scales || !wd_codes || !wd_scales || !y) return SITU_ERR_ARG;
@@ -991,9 +1004,10 @@ situ_status situ_ffn_forward_mxfp8(const void* x, const void* wgu_codes, const v
     return SITU_ERR_WORKSPACE;
   const size_t xb = static_cast<size_t>(R) * M * 2;
   const void* ins[] = {x, wgu_codes, wgu_scales, wd_codes, wd_scales};
-  const size_t inb[] = {xb, static_cast<size_t>(2 * I) * M,
+  const size_t inb[] = {xb, mx_weight_code_bytes(1, 2 * I, M, weight_fmt),
                         situ_mx_weight_scales_size(1, M, I, SITU_MX_GATE_UP),
-                        static_cast<size_t>(M) * I, situ_mx_weight_scales_size(1, M, I, SITU_MX_DOWN)};
+                        mx_weight_code_bytes(1, M, I, weight_fmt),
+                        situ_mx_weight_scales_size(1, M, I, SITU_MX_DOWN)};
   for (int i = 0; i < 5; ++i)
     if (overlap(y, xb, ins[i], inb[i]) || overlap(workspace, w.total, ins[i], inb[i]))
       return SITU_ERR_ALIAS;
@@ -1007,12 +1021,13 @@ situ_status situ_ffn_forward_mxfp8(const void* x, const void* wgu_codes, const v
                                          (R + 127) / 128, R, M, 0, nullptr, nullptr, st->status,
                                          cs);
   if (e != cudaSuccess) return cuda_fail(e);
+  const bool fp4 = weight_fmt == SITU_MX_E2M1;
   e = run_mx_gate_up(st, ws + w.x_codes, ws + w.x_sf, wgu_codes, wgu_scales, nullptr,
                      ws + w.h_codes, ws + w.h_sf, R, M, I, beta, linear_beta, 1, nullptr, nullptr,
-                     nullptr, cs);
+                     nullptr, fp4, cs);
   if (e != cudaSuccess) return cuda_fail(e);
   return finish(run_mx_down(st, ws + w.h_codes, ws + w.h_sf, wd_codes, wd_scales, y, R, M, I, 1,
-                            nullptr, nullptr, nullptr, nullptr, cs));
+                            nullptr, nullptr, nullptr, nullptr, fp4, cs));
 }
 
 namespace {
@@ -1047,11 +1062,12 @@ size_t situ_moe_mxfp8_workspace_size(int64_t R, int32_t E, int64_t M, int64_t I)
 situ_status situ_moe_grouped_forward_mxfp8(const void* x, const int32_t* expert_offsets,
                                            const int32_t* token_index, const void* wgu_codes,
                                            const void* wgu_scales, const void* wd_codes,
-                                           const void* wd_scales, void* y, void* workspace,
-                                           size_t workspace_bytes, int64_t T, int32_t k_eff,
-                                           int32_t E, int64_t M, int64_t I, float beta,
-                                           float linear_beta, void* stream) {
-  if (T < 0 || k_eff < 1 || E < 1 || E > 65536 || M < 1 || I < 1 || !caps_ok(beta, linear_beta))
+                                           const void* wd_scales, int weight_fmt, void* y,
+                                           void* workspace, size_t workspace_bytes, int64_t T,
+                                           int32_t k_eff, int32_t E, int64_t M, int64_t I,
+                                           float beta, float linear_beta, void* stream) {
+  if (T < 0 || k_eff < 1 || E < 1 || E > 65536 || M < 1 || I < 1 || !caps_ok(beta, linear_beta) ||
+      !mx_fmt_ok(weight_fmt))
     return SITU_ERR_ARG;
   if (!mx_shape_ok(M, I)) return SITU_ERR_UNSUPPORTED;
   const int64_t R = T * k_eff;
@@ -1071,9 +1087,9 @@ situ_status situ_moe_grouped_forward_mxfp8(const void* x, const int32_t* expert_
   const size_t x_b = static_cast<size_t>(T) * M * 2, y_b = static_cast<size_t>(R) * M * 2;
   const void* ins[] = {x, expert_offsets, token_index, wgu_codes, wgu_scales, wd_codes, wd_scales};
   const size_t in_b[] = {x_b, static_cast<size_t>(E + 1) * 4, static_cast<size_t>(R) * 4,
-                         static_cast<size_t>(E) * 2 * I * M,
+                         mx_weight_code_bytes(E, 2 * I, M, weight_fmt),
                          situ_mx_weight_scales_size(E, M, I, SITU_MX_GATE_UP),
-                         static_cast<size_t>(E) * M * I,
+                         mx_weight_code_bytes(E, M, I, weight_fmt),
                          situ_mx_weight_scales_size(E, M, I, SITU_MX_DOWN)};
   for (int i = 0; i < 7; ++i)
     if (overlap(y, y_b, ins[i], in_b[i]) || overlap(workspace, w.total, ins[i], in_b[i]))
@@ -1096,12 +1112,13 @@ situ_status situ_moe_grouped_forward_mxfp8(const void* x, const int32_t* expert_
   e = launch_mx_quantize_act(x, token_index, k_eff, T, ws + w.x_codes, ws + w.x_sf,
                              (R + 127) / 128 + E, R, M, E, expert_offsets, tiles, st->status, cs);
   if (e != cudaSuccess) return cuda_fail(e);
+  const bool fp4 = weight_fmt == SITU_MX_E2M1;
   e = run_mx_gate_up(st, ws + w.x_codes, ws + w.x_sf, wgu_codes, wgu_scales, nullptr,
                      ws + w.h_codes, ws + w.h_sf, R, M, I, beta, linear_beta, E, expert_offsets,
-                     tiles, units_gu, cs);
+                     tiles, units_gu, fp4, cs);
   if (e != cudaSuccess) return cuda_fail(e);
   return finish(run_mx_down(st, ws + w.h_codes, ws + w.h_sf, wd_codes, wd_scales, y, R, M, I, E,
-                            expert_offsets, tiles, units_dn, token_index, cs));
+                            expert_offsets, tiles, units_dn, token_index, fp4, cs));
 }
 
 situ_status situ_moe_combine(const void* y, const float* weights, void* out, int64_t T,

@@ -52,7 +52,11 @@ constexpr uint32_t kMnAtomBytes = 64 * 64 * 2;
 //     of 192 columns leave TMEM room for the scales), 5 stages of A 128x128 +
 //     B 192x128 codes + the A and B scale tiles of the stage (512 + 1024 bytes),
 //     K = 32 per MMA.  B arrives as two 96-row halves.
-template <bool kMx>
+// kMx: 0 bf16; 1 MXFP8 A and B; 2 MXFP8 A and MXFP4 B (E2M1 weights, packed two a
+// byte in memory; TMA unpacks each 16 codes into a 16-byte chunk of shared memory --
+// 8 bytes of codes, 8 bytes of gap -- the layout the block-scaled MMA reads for 4-bit
+// operands, so the stage keeps the MXFP8 geometry and only half the B bytes travel).
+template <int kMx>
 struct Geo {
   static constexpr int Threads = kThreads;
   static constexpr int BN = 256, BK = 64, UK = 16, Stages = 4, BHalfRows = 128;
@@ -61,7 +65,7 @@ struct Geo {
   static constexpr uint32_t StageBytes = TxBytes;
 };
 template <>
-struct Geo<true> {
+struct Geo<1> {
   // A seventh warp copies each stage's scale tiles into TMEM as soon as the stage
   // lands, so the MMA warp never issues a tcgen05.cp in front of its own MMAs (a
   // copy issued right before the MMAs that read it held the tensor pipe ~20 % idle,
@@ -71,6 +75,10 @@ struct Geo<true> {
   static constexpr uint32_t ABytes = 16384, BBytes = 24576, SfBytes = 512 + 1024;
   static constexpr uint32_t TxBytes = ABytes + BBytes + SfBytes;
   static constexpr uint32_t StageBytes = 43008;  // TxBytes rounded up to 1 KB
+};
+template <>
+struct Geo<2> : Geo<1> {
+  static constexpr uint32_t TxBytes = ABytes + BBytes / 2 + SfBytes;  // B arrives packed
 };
 constexpr int kMaxStages = 5;
 // MXFP8 scale tiles.  The block-scaled MMA reads the E8M0 scale of A row m for its
@@ -370,7 +378,7 @@ __host__ __device__ __forceinline__ int64_t sf_tile_offset(int64_t m_tile, int64
          (r_in_tile / 32) * 4 + (b % 4);
 }
 
-template <Epi kEpi, Caps kC, bool kPair, bool kStoreGu, Major kMajor, bool kMx = false>
+template <Epi kEpi, Caps kC, bool kPair, bool kStoreGu, Major kMajor, int kMx = 0>
 __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_a64,
@@ -570,7 +578,7 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * G::BN;
         const TileCoord tcm = unit_tile<kPair, kKG>(args, t, rank);
-        const uint32_t idesc = kMx ? idesc_mxf8(kBM, G::BN)
+        const uint32_t idesc = kMx ? idesc_mxf8(kBM, G::BN, kMx == 2 ? kMxE2M1 : kMxE4M3)
                                    : (tcm.row_end - tcm.a_row0 <= 64 ? kIdescHalf : kIdesc) |
                                          (a_mn_major(kMajor) ? kAMnBit : 0u) |
                                          (kMajor != Major::kKMajor ? kBMnBit : 0u);
@@ -850,36 +858,41 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// 2-D map over a row-major [rows, cols] matrix of bf16 (64 x box_rows boxes) or of
-// bytes (MXFP8 codes: 128 x box_rows boxes) -- 128 bytes a box row, 128-byte swizzle
-// (the layout sw128_kmajor_desc describes), zero fill out of bounds.
+// 2-D map over a row-major [rows, cols] matrix -- elem 0: bf16 (64 x box_rows
+// boxes); 1: bytes (MXFP8 codes, 128 x box_rows); 2: packed 4-bit codes (128 x
+// box_rows, two a byte in memory, unpacked to 16-byte chunks) -- 128 bytes a box row in
+// shared memory, 128-byte swizzle (the layout sw128_kmajor_desc describes), zero fill
+// out of bounds.  ld: row stride in elements (0 = cols).
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
-              uint32_t box_rows = 128, int64_t ld = 0, bool bytes = false) {
+              uint32_t box_rows = 128, int64_t ld = 0, int elem = 0) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
   if (!enc) return false;
-  const int64_t esz = bytes ? 1 : 2;
+  const int64_t ldv = ld > 0 ? ld : cols;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld > 0 ? ld : cols) * esz};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), box_rows};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(elem == 0 ? ldv * 2 : elem == 1 ? ldv : ldv / 2)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(elem == 0 ? 64 : 128), box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                   2, const_cast<void*>(base), dims,
+  const CUtensorMapDataType type = elem == 0   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                               : CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
+  CUresult r = enc(m, type, 2, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <bool kMx>
+template <int kMx>
 constexpr size_t smem_bytes() {
   return Geo<kMx>::Stages * Geo<kMx>::StageBytes + sizeof(SharedCtl) + 1024;
 }
-static_assert(smem_bytes<true>() <= 232448 && smem_bytes<false>() <= 232448,
+static_assert(smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448 &&
+                  smem_bytes<0>() <= 232448,
               "shared memory per CTA");
 
 // Most 2-CTA clusters of ffn_gemm_kernel<kEpi, kC, true, ...> resident at once,
 // per device (0 if the query fails: the unpaired kernel is used then).
-template <Epi kEpi, Caps kC, bool kStoreGu, Major kMajor, bool kMx>
+template <Epi kEpi, Caps kC, bool kStoreGu, Major kMajor, int kMx>
 int max_pair_clusters(size_t smem) {
   static int cached[64] = {};
   static bool done[64] = {};
@@ -909,7 +922,7 @@ int max_pair_clusters(size_t smem) {
 }
 
 template <Epi kEpi, Caps kC, bool kStoreGu = false, Major kMajor = Major::kKMajor,
-          bool kMx = false>
+          int kMx = 0>
 cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, int num_sms,
                    cudaStream_t stream) {
   using G = Geo<kMx>;
@@ -927,8 +940,8 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     ok = make_map(&ma, s.a, s.K, s.a_rows, 64, s.a_ld);
     ma64 = ma;
   } else {
-    ok = make_map(&ma, s.a, s.a_rows, s.K, 128, s.a_ld, kMx) &&
-         make_map(&ma64, s.a, s.a_rows, s.K, 64, s.a_ld, kMx);
+    ok = make_map(&ma, s.a, s.a_rows, s.K, 128, s.a_ld, kMx ? 1 : 0) &&
+         make_map(&ma64, s.a, s.a_rows, s.K, 64, s.a_ld, kMx ? 1 : 0);
   }
   if (kMajor != Major::kKMajor) {
     // B stored [K, N]; grouped by rows, the groups' K-row blocks are stacked.

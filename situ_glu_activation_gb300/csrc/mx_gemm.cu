@@ -1,6 +1,7 @@
 // mx_gemm.cu -- MXFP8 (OCP Microscaling E4M3 codes, one E8M0 scale per 32 along
-// K) block-scaled GEMMs of the SiTU-GLU feed-forward on sm_103a, and the
-// quantization kernels that produce their operands.
+// K) block-scaled GEMMs of the SiTU-GLU feed-forward on sm_103a -- with MXFP8 or
+// MXFP4 (E2M1) expert weights -- and the quantization kernels that produce their
+// operands.
 //
 // The "SiTU-GLU" chapter ("Pourquoi un plafond doux") motivates the activation's
 // bound by experts that run in MXFP8 / MXFP4: a bounded h never drives a block
@@ -95,7 +96,32 @@ __global__ void __launch_bounds__(kQuantThreads)
   }
 }
 
-// Weight rows: codes keep the row-major layout; scales go to the B tiles.
+// MXFP4 quantization of one block of 32 bf16 values (as mx_quantize32, with E2M1
+// elements): scale 2^(floor(log2 amax) - 2), i.e. code max(E - 2, 0); 16 bytes of
+// packed codes, element 2i in the low nibble of byte i.
+__device__ __forceinline__ uint32_t mx_quantize32_e2m1(const uint32_t (&w)[16], uint32_t (&q)[4]) {
+  uint32_t amax = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = max(amax, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+  const uint32_t e = amax >> 7;
+  const uint32_t code = e > 2u ? e - 2u : 0u;
+  const float inv = __uint_as_float((254u - code) << 23);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[4 * j + i] << 16) * inv;
+      v[2 * i + 1] = __uint_as_float(w[4 * j + i] & 0xFFFF0000u) * inv;
+    }
+    q[j] = cvt_e2m1x8(v);
+  }
+  return code;
+}
+
+// Weight rows: codes keep the row-major layout (E4M3 one a byte, or E2M1 two a
+// byte); scales go to the B tiles.
+template <bool kFp4>
 __global__ void __launch_bounds__(kQuantThreads)
     mx_quant_weight_kernel(const uint4* __restrict__ w, uint8_t* __restrict__ codes,
                            uint8_t* __restrict__ scales, int64_t rows_total, int64_t rows_g,
@@ -116,11 +142,18 @@ __global__ void __launch_bounds__(kQuantThreads)
       v[4 * j + 2] = x.z;
       v[4 * j + 3] = x.w;
     }
-    uint32_t q[8];
-    const uint32_t sc = mx_quantize32(v, q);
-    uint4* d = reinterpret_cast<uint4*>(codes + row * K + b * 32);
-    d[0] = make_uint4(q[0], q[1], q[2], q[3]);
-    d[1] = make_uint4(q[4], q[5], q[6], q[7]);
+    uint32_t sc;
+    if (kFp4) {
+      uint32_t q[4];
+      sc = mx_quantize32_e2m1(v, q);
+      *reinterpret_cast<uint4*>(codes + row * (K / 2) + b * 16) = make_uint4(q[0], q[1], q[2], q[3]);
+    } else {
+      uint32_t q[8];
+      sc = mx_quantize32(v, q);
+      uint4* d = reinterpret_cast<uint4*>(codes + row * K + b * 32);
+      d[0] = make_uint4(q[0], q[1], q[2], q[3]);
+      d[1] = make_uint4(q[4], q[5], q[6], q[7]);
+    }
     const int64_t g = row / rows_g;
     const int64_t r = row - g * rows_g;
     int64_t t, n;
@@ -177,7 +210,7 @@ cudaError_t launch_mx_quantize_act(const void* src, const int32_t* row_index, in
 
 cudaError_t launch_mx_quantize_weights(const void* w, void* codes, void* scales, int32_t G,
                                        int64_t rows_per_group, int64_t K, int64_t split,
-                                       cudaStream_t stream) {
+                                       bool fp4, cudaStream_t stream) {
   if (K % 128 != 0) return cudaErrorInvalidValue;
   // Tile positions no weight row maps to (a partial last tile, the unused fourth
   // 32-row group of the second 512-byte tile) read as scale code 0.
@@ -185,52 +218,60 @@ cudaError_t launch_mx_quantize_weights(const void* w, void* codes, void* scales,
       cudaMemsetAsync(scales, 0, mx_weight_scale_bytes(G, rows_per_group, K, split), stream);
   if (e != cudaSuccess) return e;
   const int64_t rows = static_cast<int64_t>(G) * rows_per_group;
-  mx_quant_weight_kernel<<<quant_grid(rows * (K / 32)), kQuantThreads, 0, stream>>>(
+  auto kernel = fp4 ? mx_quant_weight_kernel<true> : mx_quant_weight_kernel<false>;
+  kernel<<<quant_grid(rows * (K / 32)), kQuantThreads, 0, stream>>>(
       static_cast<const uint4*>(w), static_cast<uint8_t*>(codes), static_cast<uint8_t*>(scales),
       rows, rows_per_group, K, split, weight_n_tiles(rows_per_group, split));
   return cudaGetLastError();
 }
 
-cudaError_t launch_mx_gemm_situ(const GemmShape& s, const SituParams& p, Caps caps,
-                                uint32_t* status, int num_sms, cudaStream_t stream) {
+namespace {
+
+template <int kMx>
+cudaError_t mx_situ(const GemmShape& s, const SituParams& p, Caps caps, uint32_t* status,
+                    int num_sms, cudaStream_t stream) {
+  constexpr Major K = Major::kKMajor;
   if (s.h_codes) {
     switch (caps) {
       case Caps::kBoth:
-        return launch<Epi::kSituMx, Caps::kBoth, false, Major::kKMajor, true>(s, p, status,
-                                                                            num_sms, stream);
+        return launch<Epi::kSituMx, Caps::kBoth, false, K, kMx>(s, p, status, num_sms, stream);
       case Caps::kGateOnly:
-        return launch<Epi::kSituMx, Caps::kGateOnly, false, Major::kKMajor, true>(s, p, status,
-                                                                                num_sms, stream);
+        return launch<Epi::kSituMx, Caps::kGateOnly, false, K, kMx>(s, p, status, num_sms, stream);
       case Caps::kUpOnly:
-        return launch<Epi::kSituMx, Caps::kUpOnly, false, Major::kKMajor, true>(s, p, status,
-                                                                              num_sms, stream);
+        return launch<Epi::kSituMx, Caps::kUpOnly, false, K, kMx>(s, p, status, num_sms, stream);
       case Caps::kNone:
-        return launch<Epi::kSituMx, Caps::kNone, false, Major::kKMajor, true>(s, p, status,
-                                                                            num_sms, stream);
+        return launch<Epi::kSituMx, Caps::kNone, false, K, kMx>(s, p, status, num_sms, stream);
     }
     return cudaErrorInvalidValue;
   }
   switch (caps) {
     case Caps::kBoth:
-      return launch<Epi::kSitu, Caps::kBoth, false, Major::kKMajor, true>(s, p, status, num_sms,
-                                                                        stream);
+      return launch<Epi::kSitu, Caps::kBoth, false, K, kMx>(s, p, status, num_sms, stream);
     case Caps::kGateOnly:
-      return launch<Epi::kSitu, Caps::kGateOnly, false, Major::kKMajor, true>(s, p, status,
-                                                                            num_sms, stream);
+      return launch<Epi::kSitu, Caps::kGateOnly, false, K, kMx>(s, p, status, num_sms, stream);
     case Caps::kUpOnly:
-      return launch<Epi::kSitu, Caps::kUpOnly, false, Major::kKMajor, true>(s, p, status,
-                                                                          num_sms, stream);
+      return launch<Epi::kSitu, Caps::kUpOnly, false, K, kMx>(s, p, status, num_sms, stream);
     case Caps::kNone:
-      return launch<Epi::kSitu, Caps::kNone, false, Major::kKMajor, true>(s, p, status, num_sms,
-                                                                        stream);
+      return launch<Epi::kSitu, Caps::kNone, false, K, kMx>(s, p, status, num_sms, stream);
   }
   return cudaErrorInvalidValue;
 }
 
+}  // namespace
+
+cudaError_t launch_mx_gemm_situ(const GemmShape& s, const SituParams& p, Caps caps,
+                                uint32_t* status, int num_sms, cudaStream_t stream) {
+  return s.b_fp4 ? mx_situ<2>(s, p, caps, status, num_sms, stream)
+                 : mx_situ<1>(s, p, caps, status, num_sms, stream);
+}
+
 cudaError_t launch_mx_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
                                  cudaStream_t stream) {
-  return launch<Epi::kPlain, Caps::kBoth, false, Major::kKMajor, true>(s, SituParams{}, status,
-                                                                     num_sms, stream);
+  if (s.b_fp4)
+    return launch<Epi::kPlain, Caps::kBoth, false, Major::kKMajor, 2>(s, SituParams{}, status,
+                                                                    num_sms, stream);
+  return launch<Epi::kPlain, Caps::kBoth, false, Major::kKMajor, 1>(s, SituParams{}, status,
+                                                                  num_sms, stream);
 }
 
 }  // namespace situ

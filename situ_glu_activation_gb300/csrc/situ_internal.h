@@ -87,6 +87,8 @@ struct GemmShape {
   const void* sfb;
   void* h_codes;
   void* h_sf;
+  // MXFP4 B: E2M1 codes packed two a byte ([b_rows, K / 2] bytes).
+  bool b_fp4;
   // SiTU epilogue: optional bf16 store of the pre-activation (g, u), [rows, 2*split].
   void* gu_store;
   // Backward epilogue: saved (g, u) in, d(g, u) out, both [rows, 2*split] bf16.
@@ -132,9 +134,10 @@ cudaError_t launch_mx_quantize_act(const void* src, const int32_t* row_index, in
 // MXFP8 quantization of G stacked weight matrices [rows_per_group, K] into codes and
 // B-layout scale tiles: split > 0 pairs gate row j < split with up row split + j in
 // tiles of 96 + 96 rows (the SiTU GEMM's B); split == 0 cuts plain 192-row tiles.
+// fp4: E2M1 codes, two a byte ([rows, K / 2] bytes), scale 2^(floor(log2 amax) - 2).
 cudaError_t launch_mx_quantize_weights(const void* w, void* codes, void* scales, int32_t G,
                                        int64_t rows_per_group, int64_t K, int64_t split,
-                                       cudaStream_t stream);
+                                       bool fp4, cudaStream_t stream);
 // Scale bytes of those layouts.
 size_t mx_act_scale_bytes(int64_t R, int64_t K);
 size_t mx_weight_scale_bytes(int32_t G, int64_t rows_per_group, int64_t K, int64_t split);

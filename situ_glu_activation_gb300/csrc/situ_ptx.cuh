@@ -313,12 +313,13 @@ __device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
-// Instruction descriptor of tcgen05.mma kind::mxf8f6f4 block-scaled: E4M3 A and B
-// (both K-major), E8M0 scales, tile M x N; the scale byte k (0..3) of A and B is
-// selected by sf_a_id / sf_b_id (idesc_mxf8_ids).
-__host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t m, uint32_t n) {
-  return (0u << 7)            // A format: E4M3
-         | (0u << 10)         // B format: E4M3
+// Instruction descriptor of tcgen05.mma kind::mxf8f6f4 block-scaled: E4M3 A, B of
+// format b_fmt (kMxE4M3 or kMxE2M1), both K-major, E8M0 scales, tile M x N; the scale
+// byte k (0..3) of A and B is selected by sf_a_id / sf_b_id (idesc_mxf8_ids).
+constexpr uint32_t kMxE4M3 = 0, kMxE2M1 = 5;
+__host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t m, uint32_t n, uint32_t b_fmt) {
+  return (kMxE4M3 << 7)       // A format: E4M3
+         | (b_fmt << 10)      // B format
          | ((n >> 3) << 17)   // N / 8
          | (1u << 23)         // scale format: E8M0
          | ((m >> 4) << 24);  // M / 16
@@ -332,6 +333,21 @@ __host__ __device__ constexpr uint32_t idesc_mxf8_ids(uint32_t sf_a_id, uint32_t
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Eight floats -> eight E2M1 codes packed in a word (element 2j in the low nibble of
+// byte j), round to nearest even, magnitudes past 6 clamped to 6 (satfinite).
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&v)[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
   return r;
 }
 

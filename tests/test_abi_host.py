@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(situ_lib):
 
 
 def test_version_and_status_strings(situ_lib):
-    assert situ_lib.situ_abi_version() == 1
+    assert situ_lib.situ_abi_version() == 2
     for code, name in _native.STATUS_NAMES.items():
         assert situ_lib.situ_status_string(code).decode() == name
     assert situ_lib.situ_status_string(99).decode() == "SITU_ERR_UNKNOWN"

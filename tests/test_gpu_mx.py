@@ -110,19 +110,52 @@ def test_quantize_every_bf16_value(oracle, cuda_dev, order):
     assert bad.size == 0, f"{bad.size} codes differ, first at {bad[:4]}"
 
 
+FMTS = [situ.MX_E4M3, situ.MX_E2M1]
+FMT_IDS = ["mxfp8_w", "mxfp4_w"]
+
+
+def _oracle_wq(oracle, t, fmt):
+    """The oracle's quantization of weight rows in format fmt."""
+    bits = _bf16_bits(t.reshape(-1, t.shape[-1]))
+    return oracle.mxfp4_quantize(bits) if fmt == situ.MX_E2M1 else oracle.mx_quantize(bits)
+
+
+def _wdeq(oracle, q, fmt):
+    return oracle.mxfp4_dequantize(*q) if fmt == situ.MX_E2M1 else oracle.mx_dequantize(*q)
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=FMT_IDS)
 @pytest.mark.parametrize("kind", [situ.MX_GATE_UP, situ.MX_DOWN], ids=["gate_up", "down"])
-def test_quantize_weights_bit_exact(oracle, cuda_dev, kind):
+def test_quantize_weights_bit_exact(oracle, cuda_dev, kind, fmt):
     E, M, I = 2, 256, 384
     wgu, wd = wl.expert_weights(E, M, I, seed=11)
     W = wgu if kind == situ.MX_GATE_UP else wd
-    codes, sf = situ.mx_quantize_weights(W.to(cuda_dev), kind)
+    codes, sf, _ = situ.mx_quantize_weights(W.to(cuda_dev), kind, fmt)
     torch.cuda.synchronize()
     rows, K = W.shape[1], W.shape[2]
     split = I if kind == situ.MX_GATE_UP else 0
     got_s = untile_weight_scales(sf.cpu().numpy(), E, rows, K, split)
-    rc, rs = oracle.mx_quantize(_bf16_bits(W.reshape(E * rows, K)))
-    assert np.array_equal(codes.cpu().numpy().reshape(E * rows, K), rc)
+    rc, rs = _oracle_wq(oracle, W, fmt)
+    assert np.array_equal(codes.cpu().numpy().reshape(rc.shape), rc)
     assert np.array_equal(got_s.reshape(E * rows, K // 32), rs)
+
+
+def test_quantize_fp4_every_bf16_value(oracle, cuda_dev):
+    """Every finite bf16 value through the MXFP4 weight quantizer (seeded-shuffled
+    into 32-blocks of mixed magnitudes), codes and scales bit-exact."""
+    bits = np.arange(65536, dtype=np.uint32)
+    finite = np.random.default_rng(8).permutation(bits[(bits & 0x7F80) != 0x7F80].astype(np.uint16))
+    M, I = 256, 256
+    v = np.zeros(M * I, dtype=np.uint16)
+    v[: finite.size] = finite
+    W = torch.from_numpy(v.view(np.int16).reshape(1, M, I).copy()).view(torch.bfloat16)
+    codes, sf, _ = situ.mx_quantize_weights(W.to(cuda_dev), situ.MX_DOWN, situ.MX_E2M1)
+    torch.cuda.synchronize()
+    rc, rs = oracle.mxfp4_quantize(v.reshape(M, I))
+    got_s = untile_weight_scales(sf.cpu().numpy(), 1, M, I, 0).reshape(M, I // 32)
+    assert np.array_equal(got_s, rs)
+    bad = np.flatnonzero(codes.cpu().numpy().reshape(M, I // 2) != rc)
+    assert bad.size == 0, f"{bad.size} code bytes differ, first at {bad[:4]}"
 
 
 def _mx_inputs(R, M, I, seed):
@@ -143,28 +176,30 @@ def _gemm_close(got, ref, abs_terms, K, what):
     assert_ffn_close(g, ref, what)
 
 
+@pytest.mark.parametrize("fmt", FMTS, ids=FMT_IDS)
 @pytest.mark.parametrize("R,M,I", [(300, 256, 384), (1, 128, 128), (513, 512, 1152)])
-def test_gate_up_mxfp8(oracle, cuda_dev, R, M, I):
+def test_gate_up_mxfp8(oracle, cuda_dev, R, M, I, fmt):
     """h of the block-scaled gate_up GEMM against the oracle's FFN on the decoded MX
     operands (activation at the FP64 gu; FFN tolerance)."""
     x, wgu, wd = _mx_inputs(R, M, I, seed=R + I)
     xq = situ.mx_quantize_act(x.to(cuda_dev))
-    wq = situ.mx_quantize_weights(wgu.to(cuda_dev), situ.MX_GATE_UP)
+    wq = situ.mx_quantize_weights(wgu.to(cuda_dev), situ.MX_GATE_UP, fmt)
     h = situ.situ_ffn_gate_up_mxfp8(xq, wq)
     torch.cuda.synchronize()
     assert situ.device_status(clear=True) == 0
     xd = oracle.mx_dequantize(*_oracle_q(oracle, x))
-    wgud = oracle.mx_dequantize(*_oracle_q(oracle, wgu))
+    wgud = _wdeq(oracle, _oracle_wq(oracle, wgu, fmt), fmt)
     _, h_ref = oracle.ffn_forward(xd, wgud, to_f64(wd), want_h=True)
     assert_ffn_close(to_f64(h), h_ref, f"MX h {R}x{M}x{I}")
 
 
+@pytest.mark.parametrize("fmt", FMTS, ids=FMT_IDS)
 @pytest.mark.parametrize("R,M,I", [(300, 256, 384), (129, 128, 256), (513, 512, 1152)])
-def test_ffn_forward_mxfp8(oracle, cuda_dev, R, M, I):
+def test_ffn_forward_mxfp8(oracle, cuda_dev, R, M, I, fmt):
     x, wgu, wd = _mx_inputs(R, M, I, seed=3 * R + I)
     xd_, wgud_, wdd_ = x.to(cuda_dev), wgu.to(cuda_dev), wd.to(cuda_dev)
-    wguq = situ.mx_quantize_weights(wgud_, situ.MX_GATE_UP)
-    wdq = situ.mx_quantize_weights(wdd_, situ.MX_DOWN)
+    wguq = situ.mx_quantize_weights(wgud_, situ.MX_GATE_UP, fmt)
+    wdq = situ.mx_quantize_weights(wdd_, situ.MX_DOWN, fmt)
     ws = torch.empty(situ.ffn_mxfp8_workspace_bytes(R, M, I), dtype=torch.uint8, device=cuda_dev)
     y = situ.situ_ffn_forward_mxfp8(xd_, wguq, wdq, workspace=ws)
     h_bf16 = situ.situ_ffn_gate_up_mxfp8(situ.mx_quantize_act(xd_), wguq)
@@ -182,12 +217,13 @@ def test_ffn_forward_mxfp8(oracle, cuda_dev, R, M, I):
     assert np.array_equal(hs, rs)
     assert np.array_equal(hc, rc)
     # 2. The down GEMM against the FP64 product of the decoded operands.
-    wdd = oracle.mx_dequantize(*_oracle_q(oracle, wd))
+    wdd = _wdeq(oracle, _oracle_wq(oracle, wd, fmt), fmt)
     hdec = oracle.mx_dequantize(hc, hs)
     _gemm_close(y, hdec @ wdd.T, np.abs(hdec) @ np.abs(wdd).T, I, f"MX down {R}x{M}x{I}")
     # 3. End to end against the oracle's MX FFN, allowing the codes that differ.
-    y_ref, _, (hc_r, hs_r) = oracle.mx_ffn_forward(_oracle_q(oracle, x), _oracle_q(oracle, wgu),
-                                                   _oracle_q(oracle, wd))
+    y_ref, _, (hc_r, hs_r) = oracle.mx_ffn_forward(
+        _oracle_q(oracle, x), _oracle_wq(oracle, wgu, fmt), _oracle_wq(oracle, wd, fmt),
+        weights_fp4=fmt == situ.MX_E2M1)
     diff = np.abs(hdec - oracle.mx_dequantize(hc_r, hs_r))
     assert (hc != hc_r).mean() < 0.02, "more than 2% of the h codes differ"
     err = np.abs(to_f64(y) - y_ref)
@@ -211,23 +247,24 @@ def test_ffn_mxfp8_variants(oracle, cuda_dev):
         assert_ffn_close(to_f64(h), h_ref, f"MX h caps {caps}")
 
 
-def _grouped_case(T, k, E, M, I, seed, dev):
+def _grouped_case(T, k, E, M, I, seed, dev, fmt=situ.MX_E4M3):
     g = torch.Generator().manual_seed(seed)
     ids = torch.stack([torch.randperm(E - 1, generator=g)[:k] for _ in range(T)]).to(torch.int32)
     x = wl.normal((T, M), 1.0, seed=seed)
     wgu, wd = wl.expert_weights(E, M, I, seed=seed + 1)
     off, tix = situ.situ_moe_build_index(ids.to(dev), E)
-    wguq = situ.mx_quantize_weights(wgu.to(dev), situ.MX_GATE_UP)
-    wdq = situ.mx_quantize_weights(wd.to(dev), situ.MX_DOWN)
+    wguq = situ.mx_quantize_weights(wgu.to(dev), situ.MX_GATE_UP, fmt)
+    wdq = situ.mx_quantize_weights(wd.to(dev), situ.MX_DOWN, fmt)
     return ids, x, wgu, wd, off, tix, wguq, wdq
 
 
+@pytest.mark.parametrize("fmt", FMTS, ids=FMT_IDS)
 @pytest.mark.parametrize("T,k,E,M,I", [(50, 3, 6, 256, 384), (300, 2, 3, 128, 256)])
-def test_grouped_mxfp8_equals_dense_per_expert(cuda_dev, T, k, E, M, I):
+def test_grouped_mxfp8_equals_dense_per_expert(cuda_dev, T, k, E, M, I, fmt):
     """Each (token, slot) row of the grouped MX forward equals the dense MX FFN of its
     expert on the token, bit for bit: rows are quantized and multiplied
     independently of the other rows of their tile."""
-    ids, x, wgu, wd, off, tix, wguq, wdq = _grouped_case(T, k, E, M, I, T + E, cuda_dev)
+    ids, x, wgu, wd, off, tix, wguq, wdq = _grouped_case(T, k, E, M, I, T + E, cuda_dev, fmt)
     y = situ.situ_moe_grouped_forward_mxfp8(x.to(cuda_dev), off, tix, wguq, wdq, k)
     torch.cuda.synchronize()
     assert situ.device_status(clear=True) == 0
@@ -236,15 +273,16 @@ def test_grouped_mxfp8_equals_dense_per_expert(cuda_dev, T, k, E, M, I):
         t_idx, s_idx = (ids == e).nonzero(as_tuple=True)
         if len(t_idx) == 0:
             continue
-        we = (wguq[0][e].contiguous(), wguq[1].view(E, -1)[e].contiguous())
-        wde = (wdq[0][e].contiguous(), wdq[1].view(E, -1)[e].contiguous())
+        we = situ.MxWeights(wguq[0][e].contiguous(), wguq[1].view(E, -1)[e].contiguous(), fmt)
+        wde = situ.MxWeights(wdq[0][e].contiguous(), wdq[1].view(E, -1)[e].contiguous(), fmt)
         ye = situ.situ_ffn_forward_mxfp8(x.to(cuda_dev), we, wde).cpu()
         assert torch.equal(y[t_idx, s_idx].view(torch.int16), ye[t_idx].view(torch.int16)), e
 
 
-def test_grouped_mxfp8_against_oracle(oracle, cuda_dev):
+@pytest.mark.parametrize("fmt", FMTS, ids=FMT_IDS)
+def test_grouped_mxfp8_against_oracle(oracle, cuda_dev, fmt):
     T, k, E, M, I = 40, 4, 9, 256, 384
-    ids, x, wgu, wd, off, tix, wguq, wdq = _grouped_case(T, k, E, M, I, 5, cuda_dev)
+    ids, x, wgu, wd, off, tix, wguq, wdq = _grouped_case(T, k, E, M, I, 5, cuda_dev, fmt)
     y = situ.situ_moe_grouped_forward_mxfp8(x.to(cuda_dev), off, tix, wguq, wdq, k)
     torch.cuda.synchronize()
     y = to_f64(y)
@@ -255,7 +293,9 @@ def test_grouped_mxfp8_against_oracle(oracle, cuda_dev):
             continue
         t_np = t_idx.numpy()
         xe = (xq[0][t_np], xq[1][t_np])
-        y_ref, _, _ = oracle.mx_ffn_forward(xe, _oracle_q(oracle, wgu[e]), _oracle_q(oracle, wd[e]))
+        y_ref, _, _ = oracle.mx_ffn_forward(xe, _oracle_wq(oracle, wgu[e], fmt),
+                                            _oracle_wq(oracle, wd[e], fmt),
+                                            weights_fp4=fmt == situ.MX_E2M1)
         assert_ffn_close(y[t_idx, s_idx], y_ref, f"grouped MX expert {e}")
 
 
