@@ -9,7 +9,8 @@ with CUDA events, L2 flushed between steps.  The same JSON line also carries:
   * ``moe``: the routed layer (index build + grouped FFN + combine) on the Zipf
     top-8 64-expert workload and on the Kimi-K3-shaped layer (896 routed + 2
     shared experts) at 512 and 32768 tokens;
-  * ``mxfp8``: the same FFN and routed layers with MXFP8 (block-scaled 8-bit) experts;
+  * ``mxfp8``: the same FFN and routed layers with MX experts (MXFP8 activations,
+    MXFP8 or MXFP4 weights, block-scaled tensor cores);
   * ``train``: a training step of the dense FFN (forward keeping gu and h, backward),
     and (``train.grouped``) of the grouped experts on the Zipf top-8 64-expert workload;
   * ``roofline`` of the dominant kernel (the fused gate_up GEMM);
@@ -395,9 +396,10 @@ def bench_train(args, dev, peaks, world, flush):
 
 
 def bench_mx(args, dev, peaks, world, flush, names=("grouped", "k3_decode", "k3_prefill")):
-    """MXFP8 experts: the dense FFN (quantize x, block-scaled gate_up with the
-    activation and h's MX quantization in its epilogue, block-scaled down) and the
-    routed layers with MXFP8 expert weights (quantized once, outside the timing)."""
+    """MX experts: the dense FFN (quantize x, block-scaled gate_up with the activation
+    and h's MX quantization in its epilogue, block-scaled down) and the routed layers,
+    each with MXFP8 and with MXFP4 expert weights (quantized once, outside the
+    timing); activations are MXFP8 throughout."""
     import torch
 
     import situ_glu_activation_gb300 as situ
@@ -405,45 +407,43 @@ def bench_mx(args, dev, peaks, world, flush, names=("grouped", "k3_decode", "k3_
 
     fp8_peak = 2.0 * peaks["bf16_tflops"]  # nominal dense fp8 / bf16 ratio 4.5 / 2.25
     out = {"peak_fp8_tflops": fp8_peak,
-           "peak_note": "measured bf16 burst x 2 (nominal dense fp8/bf16 ratio)"}
+           "peak_note": "measured bf16 burst x 2 (nominal dense fp8/bf16 ratio); the "
+                        "E4M3 x E2M1 MMA runs at the fp8 rate"}
+    fmts = (("mxfp8", situ.MX_E4M3, 1.0), ("mxfp4", situ.MX_E2M1, 0.5))
     w = wl.WORKLOADS["dense"]
     x, wgu, wd = wl.ffn_inputs(w.M, w.I, w.rows, seed=0, device=dev)
-    wguq = situ.mx_quantize_weights(wgu, situ.MX_GATE_UP)
-    wdq = situ.mx_quantize_weights(wd, situ.MX_DOWN)
-    del wgu, wd
     y = torch.empty_like(x)
     ws = torch.empty(situ.ffn_mxfp8_workspace_bytes(w.rows, w.M, w.I), dtype=torch.uint8,
                      device=dev)
-    per_step, _ = timed_steps(
-        lambda m: situ.situ_ffn_forward_mxfp8(x, wguq, wdq, wl.BETA, wl.LINEAR_BETA, y=y,
-                                              workspace=ws),
-        args.steps, args.warmup, flush, world)
     xq = situ.mx_quantize_act(x)
-    gu_ms, _ = timed_steps(lambda m: situ.situ_ffn_gate_up_mxfp8(xq, wguq, wl.BETA,
-                                                                 wl.LINEAR_BETA),
-                           args.steps, args.warmup, flush, world)
-    ms = mean(per_step)
     flop = FLOP_PER_ROW * w.rows * w.M * w.I
     flop_gu = 4.0 * w.rows * w.M * w.I
-    out["dense"] = {"workload": w.name + ", MXFP8 weights and activations", "ms": ms,
-                    "tokens_per_s": w.rows / (ms * 1e-3), "tflops": flop / (ms * 1e-3) / 1e12,
-                    "tc_frac_fp8": flop / (ms * 1e-3) / 1e12 / fp8_peak,
-                    "gate_up_mx_ms": mean(gu_ms),
-                    "gate_up_mx_tflops": flop_gu / (mean(gu_ms) * 1e-3) / 1e12,
-                    "gate_up_mx_tc_frac_fp8": flop_gu / (mean(gu_ms) * 1e-3) / 1e12 / fp8_peak,
-                    "launches_per_step": 3}
-    del x, y, ws, xq, wguq, wdq
+    for tag, fmt, _ in fmts:
+        wguq = situ.mx_quantize_weights(wgu, situ.MX_GATE_UP, fmt)
+        wdq = situ.mx_quantize_weights(wd, situ.MX_DOWN, fmt)
+        per_step, _ = timed_steps(
+            lambda m: situ.situ_ffn_forward_mxfp8(x, wguq, wdq, wl.BETA, wl.LINEAR_BETA, y=y,
+                                                  workspace=ws),
+            args.steps, args.warmup, flush, world)
+        gu_ms, _ = timed_steps(lambda m: situ.situ_ffn_gate_up_mxfp8(xq, wguq, wl.BETA,
+                                                                     wl.LINEAR_BETA),
+                               args.steps, args.warmup, flush, world)
+        ms = mean(per_step)
+        out["dense_" + tag] = {
+            "workload": w.name + f", MXFP8 activations, {tag.upper()} weights", "ms": ms,
+            "tokens_per_s": w.rows / (ms * 1e-3), "tflops": flop / (ms * 1e-3) / 1e12,
+            "tc_frac_fp8": flop / (ms * 1e-3) / 1e12 / fp8_peak,
+            "gate_up_ms": mean(gu_ms),
+            "gate_up_tflops": flop_gu / (mean(gu_ms) * 1e-3) / 1e12,
+            "gate_up_tc_frac_fp8": flop_gu / (mean(gu_ms) * 1e-3) / 1e12 / fp8_peak,
+            "launches_per_step": 3}
+        del wguq, wdq
+    del x, y, ws, xq, wgu, wd
     torch.cuda.empty_cache()
     for name in names:
         wk = wl.WORKLOADS[name]
         E = wk.num_experts
         R = wk.T * wk.k_eff
-        wgu, wd = wl.expert_weights(E, wk.M, wk.I, seed=0, device=dev)
-        wguq = situ.mx_quantize_weights(wgu, situ.MX_GATE_UP)
-        del wgu
-        wdq = situ.mx_quantize_weights(wd, situ.MX_DOWN)
-        del wd
-        torch.cuda.empty_cache()
         ids_cpu = wl.routes(wk, seed=0)
         ids = ids_cpu.to(dev)
         x = wl.normal((wk.T, wk.M), 1.0, seed=0, device=dev)
@@ -454,28 +454,38 @@ def bench_mx(args, dev, peaks, world, flush, names=("grouped", "k3_decode", "k3_
         layer_out = torch.empty(wk.T, wk.M, dtype=torch.bfloat16, device=dev)
         ws = torch.empty(situ.moe_mxfp8_workspace_bytes(R, E, wk.M, wk.I), dtype=torch.uint8,
                          device=dev)
-
-        def step(marks):
-            situ.situ_moe_build_index(ids, E, expert_offsets=off, token_index=tix)
-            situ.situ_moe_grouped_forward_mxfp8(x, off, tix, wguq, wdq, wk.k_eff, wl.BETA,
-                                                wl.LINEAR_BETA, y=y, workspace=ws)
-            situ.situ_moe_combine(y, cw, out=layer_out)
-
-        per_step, _ = timed_steps(step, args.steps, args.warmup, flush, world)
-        ms = mean(per_step)
         counts = torch.bincount(ids_cpu.view(-1).long(), minlength=E)
         touched = int((counts > 0).sum())
-        # weight bytes streamed: codes (1 byte per element) + scales (1 per 32)
-        wbytes = touched * 3 * wk.M * wk.I * (1 + 1 / 32)
         flop = FLOP_PER_ROW * R * wk.M * wk.I
-        out[name] = {"workload": wk.name + ", MXFP8 expert weights", "ms": ms,
-                     "tokens_per_s": wk.T / (ms * 1e-3),
-                     "tflops": flop / (ms * 1e-3) / 1e12,
-                     "tc_frac_fp8": flop / (ms * 1e-3) / 1e12 / fp8_peak,
-                     "weight_gbs": wbytes / (ms * 1e-3) / 1e9,
-                     "hbm_frac": wbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                     "launches_per_step": 3 + 4 + 1}
-        del wguq, wdq, x, y, ws, off, tix, ids
+        for tag, fmt, code_bytes in fmts:
+            wgu, wd = wl.expert_weights(E, wk.M, wk.I, seed=0, device=dev)
+            wguq = situ.mx_quantize_weights(wgu, situ.MX_GATE_UP, fmt)
+            del wgu
+            wdq = situ.mx_quantize_weights(wd, situ.MX_DOWN, fmt)
+            del wd
+            torch.cuda.empty_cache()
+
+            def step(marks):
+                situ.situ_moe_build_index(ids, E, expert_offsets=off, token_index=tix)
+                situ.situ_moe_grouped_forward_mxfp8(x, off, tix, wguq, wdq, wk.k_eff, wl.BETA,
+                                                    wl.LINEAR_BETA, y=y, workspace=ws)
+                situ.situ_moe_combine(y, cw, out=layer_out)
+
+            per_step, _ = timed_steps(step, args.steps, args.warmup, flush, world)
+            ms = mean(per_step)
+            # weight bytes streamed: codes + scales (1 byte per 32 elements)
+            wbytes = touched * 3 * wk.M * wk.I * (code_bytes + 1 / 32)
+            out[name + "_" + tag] = {
+                "workload": wk.name + f", MXFP8 activations, {tag.upper()} expert weights",
+                "ms": ms, "tokens_per_s": wk.T / (ms * 1e-3),
+                "tflops": flop / (ms * 1e-3) / 1e12,
+                "tc_frac_fp8": flop / (ms * 1e-3) / 1e12 / fp8_peak,
+                "weight_gbs": wbytes / (ms * 1e-3) / 1e9,
+                "hbm_frac": wbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                "launches_per_step": 3 + 4 + 1}
+            del wguq, wdq
+            torch.cuda.empty_cache()
+        del x, y, ws, off, tix, ids
         torch.cuda.empty_cache()
     return out
 
