@@ -672,7 +672,7 @@ def run_situ(args):
     status = situ.device_status(clear=True)
 
     achieved = dense["gate_up_tflops"]
-    digest = source_digest("gemm.cu", "situ_math.cuh", "situ_ptx.cuh")
+    digest = source_digest("gemm_kernel.cuh", "gemm.cu", "situ_math.cuh", "situ_ptx.cuh")
     line = {
         "metric": METRIC,
         "value": value,
