@@ -338,6 +338,17 @@ def bench_moe(args, dev, peaks, world, flush, names):
         per_step, (t_idx, t_ffn, t_comb) = timed_steps(step, args.steps, args.warmup, flush,
                                                        world, inner=2)
         ms = mean(per_step)
+        # The same layer with the combine fused into the down projection (scatter-add).
+        ws_c = torch.empty(situ.moe_combined_workspace_bytes(w.T, w.k_eff, E, w.M, w.I),
+                           dtype=torch.uint8, device=dev)
+
+        def fused_step(marks):
+            situ.situ_moe_build_index(ids, E, expert_offsets=off, token_index=tix)
+            situ.situ_moe_grouped_forward_combined(x, off, tix, wgu, wd, cw, wl.BETA,
+                                                   wl.LINEAR_BETA, out=layer_out, workspace=ws_c)
+
+        fused_ms, _ = timed_steps(fused_step, args.steps, args.warmup, flush, world)
+        del ws_c
         counts = torch.bincount(ids_cpu.view(-1).long(), minlength=E)
         touched = int((counts > 0).sum())
         wbytes = touched * 3 * w.M * w.I * 2
@@ -347,6 +358,7 @@ def bench_moe(args, dev, peaks, world, flush, names):
         results[name] = {
             "workload": w.name, "ms": ms, "index_ms": mean(t_idx), "ffn_ms": mean(t_ffn),
             "combine_ms": mean(t_comb),
+            "fused_combine_layer_ms": mean(fused_ms),
             "tokens": w.T, "routes": R, "experts_touched": touched,
             "tokens_per_s": w.T / (ms * 1e-3), "tflops": tflops,
             "tc_frac": tflops / peaks["bf16_tflops"],

@@ -350,6 +350,38 @@ situ_status situ_moe_grouped_forward(const void* x, const int32_t* expert_offset
                                      float linear_beta, situ_dtype dt, void* stream);
 
 /* -------------------------------------------------------------------------
+ * situ_moe_grouped_forward_combined -- the routed layer output in one pass:
+ *   out[t, :] = dtype( sum over slots s of weights[t, s] * FFN_{e(t,s)}(x[t, :]) )
+ * i.e. situ_moe_grouped_forward followed by situ_moe_combine, with the combine fused
+ * into the down projection's epilogue as a scatter-add: each (token, slot) row is
+ * multiplied by its weight and added into an FP32 [T, M] accumulator with atomic
+ * vector adds, then cast to dtype.  The per-route rows are never written, and they
+ * are added unrounded.  The order of the additions depends on scheduling, so the
+ * result can differ from run to run in the last bits (situ_moe_combine is the
+ * deterministic path).  Each routed and shared expert of Kimi K3 runs on its tokens
+ * ("SiTU-GLU" chapter, "Ou SiTU-GLU est utilise"), and the layer output is their
+ * router-weighted sum.
+ *
+ *   x, expert_offsets, token_index, W_gate_up, W_down, T, k_eff, E, M, I, caps, dt:
+ *               as situ_moe_grouped_forward (bf16 only).
+ *   weights     device, [T, k_eff] float32.
+ *   out         device, [T, M] bf16, written.
+ *   workspace   device, >= situ_moe_combined_workspace_size(T, k_eff, E, M, I, dt)
+ *               bytes, 256-byte aligned.
+ * Errors: those of situ_moe_grouped_forward.
+ * ------------------------------------------------------------------------- */
+size_t situ_moe_combined_workspace_size(int64_t T, int32_t k_eff, int32_t E, int64_t M,
+                                        int64_t I, situ_dtype dt);
+
+situ_status situ_moe_grouped_forward_combined(const void* x, const int32_t* expert_offsets,
+                                              const int32_t* token_index, const void* W_gate_up,
+                                              const void* W_down, const float* weights,
+                                              void* out, void* workspace, size_t workspace_bytes,
+                                              int64_t T, int32_t k_eff, int32_t E, int64_t M,
+                                              int64_t I, float beta, float linear_beta,
+                                              situ_dtype dt, void* stream);
+
+/* -------------------------------------------------------------------------
  * situ_moe_grouped_forward_train / situ_moe_grouped_backward -- training step of
  * the grouped experts.
  *

@@ -56,6 +56,9 @@ SIGNATURES = {
     "situ_moe_grouped_backward": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                    _sz, _i64, _i32, _i32, _i64, _i64, _f32, _f32, _ci, _vp], _ci),
     "situ_moe_combine": ([_vp, _vp, _vp, _i64, _i32, _i64, _ci, _vp], _ci),
+    "situ_moe_combined_workspace_size": ([_i64, _i32, _i32, _i64, _i64, _ci], _sz),
+    "situ_moe_grouped_forward_combined": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64,
+                                           _i32, _i32, _i64, _i64, _f32, _f32, _ci, _vp], _ci),
     "situ_mx_act_scales_size": ([_i64, _i64], _sz),
     "situ_mx_weight_scales_size": ([_i32, _i64, _i64, _ci], _sz),
     "situ_mx_quantize_act": ([_vp, _vp, _vp, _i64, _i64, _vp], _ci),

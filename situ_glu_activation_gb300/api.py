@@ -569,6 +569,42 @@ def situ_moe_grouped_forward_mxfp8(x: torch.Tensor, expert_offsets: torch.Tensor
     return y
 
 
+def situ_moe_grouped_forward_combined(x: torch.Tensor, expert_offsets: torch.Tensor,
+                                      token_index: torch.Tensor, W_gate_up: torch.Tensor,
+                                      W_down: torch.Tensor, weights: torch.Tensor,
+                                      beta: float = 4.0, linear_beta: float = 25.0,
+                                      out: torch.Tensor | None = None,
+                                      workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """Routed layer output with the combine fused into the down projection (FP32
+    scatter-add): out[t] = sum_s weights[t, s] * FFN_{expert of (t, s)}(x[t]), [T, M].
+    Not bitwise reproducible (atomic order); situ_moe_combine is the deterministic path."""
+    T, M, E, I = _moe_shapes(x, expert_offsets, token_index, W_gate_up, W_down,
+                             weights.shape[1] if weights.dim() == 2 else 1)
+    _cuda_contig("weights", weights)
+    k_eff = weights.shape[1]
+    if weights.dtype != torch.float32 or weights.shape != (T, k_eff):
+        raise ValueError("weights must be float32 [T, k_eff]")
+    if out is None:
+        out = torch.empty(T, M, dtype=x.dtype, device=x.device)
+    if T == 0:
+        return out
+    lib = _native.lib()
+    need = int(lib.situ_moe_combined_workspace_size(T, k_eff, E, M, I, _dt(x)))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    check("situ_moe_grouped_forward_combined",
+          lib.situ_moe_grouped_forward_combined(
+              x.data_ptr(), expert_offsets.data_ptr(), token_index.data_ptr(),
+              W_gate_up.data_ptr(), W_down.data_ptr(), weights.data_ptr(), out.data_ptr(),
+              workspace.data_ptr(), workspace.numel() * workspace.element_size(), T, k_eff, E, M,
+              I, *caps(beta, linear_beta), _dt(x), _stream(x.device)))
+    return out
+
+
+def moe_combined_workspace_bytes(T: int, k_eff: int, E: int, M: int, I: int) -> int:
+    return int(_native.lib().situ_moe_combined_workspace_size(T, k_eff, E, M, I, SITU_BF16))
+
+
 def situ_moe_combine(y: torch.Tensor, weights: torch.Tensor,
                      out: torch.Tensor | None = None) -> torch.Tensor:
     """Layer output of a routed batch: out[t] = sum_s weights[t, s] * y[t, s] (FP32,
@@ -608,6 +644,7 @@ __all__ = [
     "device_status", "selftest_bounded_wait", "ffn_host_workspace_bytes", "situ_moe_combine",
     "situ_ffn_forward_train", "situ_ffn_backward", "ffn_backward_workspace_bytes",
     "situ_moe_grouped_forward_train", "situ_moe_grouped_backward", "moe_backward_workspace_bytes",
+    "situ_moe_grouped_forward_combined", "moe_combined_workspace_bytes",
     "MX_GATE_UP", "MX_DOWN", "MX_E4M3", "MX_E2M1", "MxWeights", "mx_act_scales_bytes", "mx_weight_scales_bytes", "mx_quantize_act",
     "mx_quantize_weights", "situ_ffn_gate_up_mxfp8", "situ_ffn_forward_mxfp8",
     "ffn_mxfp8_workspace_bytes", "situ_moe_grouped_forward_mxfp8", "moe_mxfp8_workspace_bytes",

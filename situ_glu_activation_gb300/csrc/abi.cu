@@ -503,12 +503,15 @@ situ_status moe_common_checks(const void* x, const int32_t* expert_offsets,
   return SITU_OK;
 }
 
-// The grouped forward; gu_store (training) additionally keeps the pre-activation.
+// The grouped forward; gu_store (training) additionally keeps the pre-activation;
+// with combine_w the down GEMM adds the weighted rows into combine_acc instead of
+// writing y.
 situ_status moe_forward_impl(const void* x, const int32_t* expert_offsets,
                              const int32_t* token_index, const void* W_gate_up,
                              const void* W_down, void* y, void* h_perm, void* gu_store,
                              void* workspace, int64_t T, int32_t k_eff, int32_t E, int64_t M,
-                             int64_t I, float beta, float linear_beta, cudaStream_t cs) {
+                             int64_t I, float beta, float linear_beta, cudaStream_t cs,
+                             const float* combine_w = nullptr, float* combine_acc = nullptr) {
   const int64_t R = T * k_eff;
   DeviceState* st = nullptr;
   situ_status s = device_state(&st);
@@ -563,6 +566,9 @@ situ_status moe_forward_impl(const void* x, const int32_t* expert_offsets,
   d.ldo = M;
   d.out_rows = R;
   d.out_row_index = token_index;
+  d.combine_w = combine_w;
+  d.combine_out = combine_acc;
+  d.combine_k = k_eff;
   return finish(launch_gemm_plain(d, st->status, st->num_sms, cs));
 }
 
@@ -632,6 +638,56 @@ situ_status situ_moe_grouped_forward_train(const void* x, const int32_t* expert_
   return moe_forward_impl(x, expert_offsets, token_index, W_gate_up, W_down, y, h, gu, workspace,
                           T, k_eff, E, M, I, beta, linear_beta,
                           static_cast<cudaStream_t>(stream));
+}
+
+size_t situ_moe_combined_workspace_size(int64_t T, int32_t k_eff, int32_t E, int64_t M,
+                                        int64_t I, situ_dtype dt) {
+  if (T < 0 || k_eff < 1) return 0;
+  const size_t base = situ_moe_workspace_size(T * k_eff, E, M, I, dt);
+  if (base == 0) return 0;
+  return base + round_up(static_cast<size_t>(T) * M * 4, 256);  // FP32 accumulator [T, M]
+}
+
+situ_status situ_moe_grouped_forward_combined(const void* x, const int32_t* expert_offsets,
+                                              const int32_t* token_index, const void* W_gate_up,
+                                              const void* W_down, const float* weights,
+                                              void* out, void* workspace, size_t workspace_bytes,
+                                              int64_t T, int32_t k_eff, int32_t E, int64_t M,
+                                              int64_t I, float beta, float linear_beta,
+                                              situ_dtype dt, void* stream) {
+  situ_status s = moe_common_checks(x, expert_offsets, token_index, W_gate_up, W_down, T, k_eff,
+                                    E, M, I, beta, linear_beta, dt);
+  const int64_t R = T * k_eff;
+  if (s != SITU_OK || R == 0) return s;
+  if (!weights || !out) return SITU_ERR_ARG;
+  if (!aligned16(out)) return SITU_ERR_ALIGN;
+  const size_t need = situ_moe_combined_workspace_size(T, k_eff, E, M, I, dt);
+  if (!workspace || workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256)
+    return SITU_ERR_WORKSPACE;
+  const size_t x_b = static_cast<size_t>(T) * M * 2, out_b = x_b;
+  const size_t wgu_b = static_cast<size_t>(E) * 2 * I * M * 2, wd_b = static_cast<size_t>(E) * M * I * 2;
+  const size_t off_b = static_cast<size_t>(E + 1) * 4, tix_b = static_cast<size_t>(R) * 4,
+               w_b = static_cast<size_t>(R) * 4;
+  const void* ins[] = {x, W_gate_up, W_down, expert_offsets, token_index, weights};
+  const size_t in_b[] = {x_b, wgu_b, wd_b, off_b, tix_b, w_b};
+  for (int i = 0; i < 6; ++i)
+    if (overlap(out, out_b, ins[i], in_b[i]) || overlap(workspace, need, ins[i], in_b[i]))
+      return SITU_ERR_ALIAS;
+  if (overlap(out, out_b, workspace, need)) return SITU_ERR_ALIAS;
+  DeviceState* st = nullptr;
+  if ((s = device_state(&st)) != SITU_OK) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const size_t base = situ_moe_workspace_size(R, E, M, I, dt);
+  float* acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + base);
+  cudaError_t e = cudaMemsetAsync(acc, 0, static_cast<size_t>(T) * M * 4, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const size_t prefix_bytes = round_up(static_cast<size_t>(E + 1) * 4, 256);
+  void* h_perm = static_cast<uint8_t*>(workspace) + 3 * prefix_bytes +
+                 round_up(static_cast<size_t>(R) * M * 2, 256);
+  s = moe_forward_impl(x, expert_offsets, token_index, W_gate_up, W_down, nullptr, h_perm,
+                       nullptr, workspace, T, k_eff, E, M, I, beta, linear_beta, cs, weights, acc);
+  if (s != SITU_OK) return s;
+  return finish(launch_f32_to_bf16(acc, out, T * M, st->num_sms, cs));
 }
 
 size_t situ_moe_backward_workspace_size(int64_t R, int32_t E, int64_t M, int64_t I,

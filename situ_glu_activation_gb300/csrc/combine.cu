@@ -98,6 +98,22 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// FP32 -> bf16 (round to nearest even), 8 values a thread when aligned.
+__global__ void __launch_bounds__(kThreads)
+    f32_to_bf16_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ out, int64_t n) {
+  const int64_t n8 = n / 8;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(acc) + 2 * i);
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
+    __stcs(reinterpret_cast<uint4*>(out) + i,
+           make_uint4(pack2(a.x, a.y), pack2(a.z, a.w), pack2(b.x, b.y), pack2(b.z, b.w)));
+  }
+  for (int64_t i = n8 * 8 + static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * kThreads)
+    out[i] = __float2bfloat16_rn(acc[i]);
+}
+
 int grid_of(int64_t items, int num_sms) {
   int64_t b = (items + kThreads - 1) / kThreads;
   const int64_t cap = static_cast<int64_t>(num_sms) * 16;
@@ -106,6 +122,14 @@ int grid_of(int64_t items, int num_sms) {
 }
 
 }  // namespace
+
+cudaError_t launch_f32_to_bf16(const float* acc, void* out, int64_t n, int num_sms,
+                               cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  f32_to_bf16_kernel<<<grid_of((n + 7) / 8, num_sms), kThreads, 0, stream>>>(
+      acc, static_cast<__nv_bfloat16*>(out), n);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const void* y, const float* w, void* out, int64_t T, int32_t k_eff,
                            int64_t M, situ_dtype dt, int num_sms, cudaStream_t stream) {

@@ -139,6 +139,12 @@ struct Args {
   const uint8_t* sfb;
   uint8_t* h_codes;
   uint8_t* h_sf;
+  // kPlain with a fused combine: instead of storing output row r (a route, flat
+  // token * k_eff + slot), add combine_w[r] * row into combine_out[r / combine_k]
+  // (FP32 [tokens, n_out]) with vector atomics.
+  const float* combine_w;
+  float* combine_out;
+  int32_t combine_k;
 };
 
 struct SharedCtl {
@@ -821,7 +827,23 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
                         : pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
           }
           const int64_t col0 = static_cast<int64_t>(tc.n_tile) * G::BN + c * 32;
-          if (valid) store_row_chunk(dst_row + col0, w, col0, args.n_out);
+          if (kEpi == Epi::kPlain && args.combine_w) {
+            // Fused combine: FP32 atomic adds of the weighted row (order-dependent
+            // rounding).
+            if (valid) {
+              const float wr = __ldg(args.combine_w + out_row);
+              float* dst = args.combine_out + (out_row / args.combine_k) * args.n_out + col0;
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                if (col0 + 4 * v + 4 <= args.n_out)
+                  red_add_v4_f32(dst + 4 * v, wr * __uint_as_float(a[4 * v]),
+                                 wr * __uint_as_float(a[4 * v + 1]), wr * __uint_as_float(a[4 * v + 2]),
+                                 wr * __uint_as_float(a[4 * v + 3]));
+              }
+            }
+          } else if (valid) {
+            store_row_chunk(dst_row + col0, w, col0, args.n_out);
+          }
         }
       }
       tc_fence_before_sync();
@@ -982,6 +1004,9 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
   a.sfb = static_cast<const uint8_t*>(s.sfb);
   a.h_codes = static_cast<uint8_t*>(s.h_codes);
   a.h_sf = static_cast<uint8_t*>(s.h_sf);
+  a.combine_w = s.combine_w;
+  a.combine_out = static_cast<float*>(s.combine_out);
+  a.combine_k = s.combine_k > 0 ? s.combine_k : 1;
   const int64_t m_tiles = (s.a_rows + kBM - 1) / kBM;
   // The shared-memory opt-in is a per-device property of each kernel: set once.
   static bool smem_set[64] = {};

@@ -89,6 +89,13 @@ struct GemmShape {
   void* h_sf;
   // MXFP4 B: E2M1 codes packed two a byte ([b_rows, K / 2] bytes).
   bool b_fp4;
+  // Plain epilogue with a fused combine (routed down projection): output row r (flat
+  // route token * combine_k + slot, from out_row_index) is added, times combine_w[r],
+  // into combine_out[r / combine_k] (FP32 [tokens, n_out], 16-byte aligned rows) by
+  // atomic adds instead of being stored.
+  const float* combine_w;
+  void* combine_out;
+  int32_t combine_k;
   // SiTU epilogue: optional bf16 store of the pre-activation (g, u), [rows, 2*split].
   void* gu_store;
   // Backward epilogue: saved (g, u) in, d(g, u) out, both [rows, 2*split] bf16.
@@ -161,6 +168,9 @@ cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, uint32_t* status,
                                          cudaStream_t stream);
 
 // ----- routed-layer combine (combine.cu) --------------------------------------
+// out[i] = bf16(acc[i]) for n FP32 values (the fused combine's cast).
+cudaError_t launch_f32_to_bf16(const float* acc, void* out, int64_t n, int num_sms,
+                               cudaStream_t stream);
 // out[t, :] = sum_s w[t, s] * y[t, s, :] in FP32, slot order (w == NULL: all 1).
 cudaError_t launch_combine(const void* y, const float* w, void* out, int64_t T, int32_t k_eff,
                            int64_t M, situ_dtype dt, int num_sms, cudaStream_t stream);

@@ -351,6 +351,14 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&v)[8]) {
   return r;
 }
 
+// Four FP32 atomic adds to 16 consecutive bytes of global memory (one vector
+// reduction, no return value); p 16-byte aligned.
+__device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
 // 16 zero bytes into this CTA's shared memory (generic proxy).
 __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");

@@ -187,3 +187,72 @@ def test_moe_layer_output(oracle, cuda_dev):
                                       oracle_input(wd))
     ref = oracle.moe_combine(yref, w.numpy())
     assert_ffn_close(to_f64(out), ref, "moe layer output")
+
+
+# ---------------------------------------------------------------------------
+# Combine fused into the down projection (FP32 scatter-add)
+# ---------------------------------------------------------------------------
+def _layer_case(T, k, E, M, I, seed, dev):
+    g = torch.Generator().manual_seed(seed)
+    ids = torch.stack([torch.randperm(E - 1, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    ids = torch.cat([ids, torch.full((T, 1), E - 1, dtype=torch.int32)], dim=1)  # a shared expert
+    x = wl.normal((T, M), 1.0, seed=seed + 1)
+    wgu, wd = wl.expert_weights(E, M, I, seed=seed + 2)
+    w = wl.combine_weights(T, k, 1, seed=seed + 3)
+    off, tix = situ.situ_moe_build_index(ids.to(dev), E)
+    return ids, x, wgu, wd, w, off, tix
+
+
+@pytest.mark.parametrize("T,k,E,M,I", [(40, 3, 6, 256, 384), (300, 2, 4, 136, 200)])
+def test_fused_combine_against_oracle(oracle, cuda_dev, T, k, E, M, I):
+    ids, x, wgu, wd, w, off, tix = _layer_case(T, k, E, M, I, T + E, cuda_dev)
+    out = situ.situ_moe_grouped_forward_combined(x.to(cuda_dev), off, tix, wgu.to(cuda_dev),
+                                                 wd.to(cuda_dev), w.to(cuda_dev))
+    torch.cuda.synchronize()
+    assert situ.device_status(clear=True) == 0
+    yref = oracle.moe_grouped_forward(oracle_input(x), ids.numpy(), oracle_input(wgu),
+                                      oracle_input(wd))
+    assert_ffn_close(to_f64(out), oracle.moe_combine(yref, w.numpy()), "fused combine")
+
+
+def test_fused_combine_matches_unfused(cuda_dev):
+    """The fused and the separate combine add the same weighted rows; they differ by
+    the bf16 rounding of each route's row in the separate path (2^-9 |w y| a route),
+    the order of the FP32 additions (2^-22 sum |w y|) and the output rounding (one
+    bf16 ulp of either result): |fused - unfused| <= 2^-8 sum_s |w_s y_s| + 2^-7 |out|."""
+    T, k, E, M, I = 256, 4, 8, 512, 384
+    ids, x, wgu, wd, w, off, tix = _layer_case(T, k, E, M, I, 77, cuda_dev)
+    xd, wgud, wdd, wdv = x.to(cuda_dev), wgu.to(cuda_dev), wd.to(cuda_dev), w.to(cuda_dev)
+    fused = situ.situ_moe_grouped_forward_combined(xd, off, tix, wgud, wdd, wdv)
+    y = situ.situ_moe_grouped_forward(xd, off, tix, wgud, wdd, k + 1)
+    sep = situ.situ_moe_combine(y, wdv)
+    torch.cuda.synchronize()
+    absum = np.einsum("tk,tkm->tm", np.abs(w.numpy().astype(np.float64)), np.abs(to_f64(y)))
+    f, u = to_f64(fused), to_f64(sep)
+    tol = 2.0 ** -8 * absum + 2.0 ** -7 * np.maximum(np.abs(f), np.abs(u))
+    assert (np.abs(f - u) <= tol).all(), float((np.abs(f - u) / tol).max())
+
+
+def test_fused_combine_full_size(oracle, cuda_dev):
+    """The 64-expert Zipf workload (16384 tokens, top-8, M=2048, I=3072) at full size
+    through the fused combine, 16 sampled tokens against the oracle's layer output."""
+    wk = wl.WORKLOADS["grouped"]
+    E = wk.num_experts
+    ids = wl.routes(wk, seed=0)
+    x = wl.normal((wk.T, wk.M), 1.0, seed=0, device=cuda_dev)
+    wgu, wd = wl.expert_weights(E, wk.M, wk.I, seed=0, device=cuda_dev)
+    w = wl.combine_weights(wk.T, wk.k, 0, seed=0)
+    off, tix = situ.situ_moe_build_index(ids.to(cuda_dev), E)
+    out = situ.situ_moe_grouped_forward_combined(x, off, tix, wgu, wd, w.to(cuda_dev))
+    torch.cuda.synchronize()
+    assert situ.device_status(clear=True) == 0
+    g = torch.Generator().manual_seed(6)
+    toks = [0, wk.T - 1] + torch.randint(1, wk.T - 1, (14,), generator=g).tolist()
+    for t in toks:
+        ref = np.zeros(wk.M)
+        for s in range(wk.k):
+            e = int(ids[t, s])
+            ref += float(w[t, s]) * oracle.ffn_forward(oracle_input(x[t:t + 1].cpu()),
+                                                        oracle_input(wgu[e].cpu()),
+                                                        oracle_input(wd[e].cpu()))[0]
+        assert_ffn_close(to_f64(out[t]), ref, f"fused combine token {t}")
