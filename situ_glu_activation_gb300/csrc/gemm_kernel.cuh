@@ -779,37 +779,65 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
       } else if (kEpi == Epi::kSituBwd) {
         const __nv_bfloat16* gu_row = args.gu_in + static_cast<int64_t>(row) * 2 * args.split;
         __nv_bfloat16* dgu_row = args.dgu_out + static_cast<int64_t>(row) * 2 * args.split;
+        // The saved (g, u) of a 32-column chunk are loaded one chunk ahead, through the
+        // read-only path: loaded in the loop, each 16-byte load would wait behind the
+        // previous stores (whose asm carries a memory clobber) and the tile's epilogue
+        // would serialise 32 global-load latencies.
+        uint4 gq[4], uq[4];
+        auto load_gu = [&](int c, uint4 (&gd)[4], uint4 (&ud)[4]) {
+          const int64_t col0 = static_cast<int64_t>(tc.n_tile) * G::BN + c * 32;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int64_t cv = col0 + 8 * v;
+            if (valid && cv + 8 <= args.n_out) {
+              gd[v] = __ldg(reinterpret_cast<const uint4*>(gu_row + cv));
+              ud[v] = __ldg(reinterpret_cast<const uint4*>(gu_row + args.split + cv));
+            } else {
+              gd[v] = make_uint4(0, 0, 0, 0);
+              ud[v] = make_uint4(0, 0, 0, 0);
+            }
+          }
+        };
+        load_gu(0, gq, uq);
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
+          uint4 gn[4], un[4];
+          if (c + 1 < 8) load_gu(c + 1, gn, un);
           __syncwarp();
           uint32_t a[32];
           tmem_ld32(t_acc + c * 32, a);
           tmem_ld_wait(a);
           const int64_t col0 = static_cast<int64_t>(tc.n_tile) * G::BN + c * 32;
-          if (!valid) continue;
+          if (valid) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int64_t cv = col0 + 8 * v;
-            if (cv + 8 > args.n_out) continue;
-            const uint4 gv = *reinterpret_cast<const uint4*>(gu_row + cv);
-            const uint4 uv = *reinterpret_cast<const uint4*>(gu_row + args.split + cv);
-            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-            const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
-            uint32_t og[4], ou[4];
+            for (int v = 0; v < 4; ++v) {
+              const int64_t cv = col0 + 8 * v;
+              if (cv + 8 > args.n_out) continue;
+              const uint32_t gw[4] = {gq[v].x, gq[v].y, gq[v].z, gq[v].w};
+              const uint32_t uw[4] = {uq[v].x, uq[v].y, uq[v].z, uq[v].w};
+              uint32_t og[4], ou[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              float pg0, pu0, pg1, pu1;
-              situ_act_grad<kC>(__uint_as_float(gw[i] << 16), __uint_as_float(uw[i] << 16),
-                                args.sp, pg0, pu0);
-              situ_act_grad<kC>(__uint_as_float(gw[i] & 0xFFFF0000u),
-                                __uint_as_float(uw[i] & 0xFFFF0000u), args.sp, pg1, pu1);
-              const float dh0 = __uint_as_float(a[8 * v + 2 * i]);
-              const float dh1 = __uint_as_float(a[8 * v + 2 * i + 1]);
-              og[i] = pack_bf16x2(dh0 * pg0, dh1 * pg1);
-              ou[i] = pack_bf16x2(dh0 * pu0, dh1 * pu1);
+              for (int i = 0; i < 4; ++i) {
+                float pg0, pu0, pg1, pu1;
+                situ_act_grad<kC>(__uint_as_float(gw[i] << 16), __uint_as_float(uw[i] << 16),
+                                  args.sp, pg0, pu0);
+                situ_act_grad<kC>(__uint_as_float(gw[i] & 0xFFFF0000u),
+                                  __uint_as_float(uw[i] & 0xFFFF0000u), args.sp, pg1, pu1);
+                const float dh0 = __uint_as_float(a[8 * v + 2 * i]);
+                const float dh1 = __uint_as_float(a[8 * v + 2 * i + 1]);
+                og[i] = pack_bf16x2(dh0 * pg0, dh1 * pg1);
+                ou[i] = pack_bf16x2(dh0 * pu0, dh1 * pu1);
+              }
+              st_global_v4(dgu_row + cv, og[0], og[1], og[2], og[3]);
+              st_global_v4(dgu_row + args.split + cv, ou[0], ou[1], ou[2], ou[3]);
             }
-            st_global_v4(dgu_row + cv, og[0], og[1], og[2], og[3]);
-            st_global_v4(dgu_row + args.split + cv, ou[0], ou[1], ou[2], ou[3]);
+          }
+          if (c + 1 < 8) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              gq[v] = gn[v];
+              uq[v] = un[v];
+            }
           }
         }
       } else {
