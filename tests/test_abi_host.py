@@ -102,6 +102,45 @@ def test_argument_checks(situ_lib):
     assert b(1 << 20, 2 << 20, 3 << 20, 0, 0, 10, 4, None) == WS
 
 
+def test_training_and_mx_argument_checks(situ_lib):
+    UNSUP = 6
+    # grouped training: fp32 unsupported, no routes -> no-op / zeroing path needs weights
+    f = situ_lib.situ_moe_grouped_forward_train
+    assert f(0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 4, 2, 3, 8, 8, 4.0, 25.0, 1, None) == UNSUP
+    assert f(0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 2, 3, 8, 8, 4.0, 25.0, 0, None) == 0
+    b = situ_lib.situ_moe_grouped_backward
+    assert b(0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 4, 2, 3, 8, 8, 0.0, 25.0, 0, None) == BAD
+    assert b(0, 0, 0, 0, 0, 0, 0, 0, 0, None, None, 0, 0, 0, 2, 3, 8, 8, 4.0, 25.0, 0, None) == BAD
+    # MX quantizers: K must be a multiple of 128; bad kind / format rejected
+    q = situ_lib.situ_mx_quantize_act
+    assert q(1 << 20, 2 << 20, 3 << 20, 4, 136, None) == UNSUP
+    assert q(None, None, None, 0, 128, None) == 0
+    assert q(None, 2 << 20, 3 << 20, 4, 128, None) == BAD
+    w = situ_lib.situ_mx_quantize_weights
+    assert w(1 << 20, 2 << 20, 3 << 20, 1, 256, 384, 2, 0, None) == BAD      # bad kind
+    assert w(1 << 20, 2 << 20, 3 << 20, 1, 256, 384, 0, 7, None) == BAD      # bad format
+    assert w(1 << 20, 2 << 20, 3 << 20, 1, 200, 384, 0, 0, None) == UNSUP   # M % 128
+    assert situ_lib.situ_mx_act_scales_size(300, 256) == 3 * 2 * 512
+    assert situ_lib.situ_mx_weight_scales_size(1, 2048, 3072, 0) == 32 * 16 * 1024
+    assert situ_lib.situ_mx_weight_scales_size(2, 2048, 3072, 1) == 2 * 11 * 24 * 1024
+    assert situ_lib.situ_mx_weight_scales_size(1, 200, 3072, 0) == 0
+    ffn = situ_lib.situ_ffn_forward_mxfp8
+    args = [1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20, 0, 6 << 20, 7 << 20, 16, 4, 256, 384,
+            4.0, 25.0, None]
+    assert ffn(*args) == WS                                  # workspace too small
+    bad_fmt = list(args)
+    bad_fmt[5] = 3
+    assert ffn(*bad_fmt) == BAD
+    assert situ_lib.situ_ffn_mxfp8_workspace_size(4, 256, 384) > 0
+    assert situ_lib.situ_ffn_mxfp8_workspace_size(4, 250, 384) == 0
+    # fused combine: needs weights and an output
+    c = situ_lib.situ_moe_grouped_forward_combined
+    assert c(1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20, None, 6 << 20, 7 << 20, 16, 4, 2, 3,
+             256, 384, 4.0, 25.0, 0, None) == BAD
+    assert situ_lib.situ_moe_combined_workspace_size(4, 2, 3, 256, 384, 0) == \
+        situ_lib.situ_moe_workspace_size(8, 3, 256, 384, 0) + 4 * 256 * 4
+
+
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not found"):
         _native.lib(str(tmp_path / "libsitu.so"))
