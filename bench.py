@@ -581,6 +581,48 @@ def cpu_baseline(seconds: float, rows_hint: int = 0):
                       f"(FP64 gate_up, SiTU-GLU, down), {dt:.1f} s"}
 
 
+def cpu_baseline_moe(seconds: float):
+    """The FP64 oracle's grouped experts (as it stands) on a bounded sample of the
+    64-expert workload: the routes of the first tokens (top-8 Zipf), timed on the host
+    cores.  The oracle's work per route (6 M I multiply-adds) does not depend on which
+    expert a route uses, so the sample's experts are mapped onto 8 seeded expert weight
+    sets; routes/s and tokens/s (routes / 8) are extrapolated from the sample."""
+    import numpy as np
+    import torch
+
+    from oracle import Oracle
+    from situ_glu_activation_gb300 import workloads as wl
+
+    o = Oracle()
+    w = wl.WORKLOADS["grouped"]
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    ids = wl.routes(w, seed=0)
+    E_s = 8
+    wgu, wd = wl.expert_weights(E_s, w.M, w.I, seed=0)
+    wgb, wdb = bits(wgu), bits(wd)
+    threads = o.num_threads()
+    n_tok = max(1, threads // 4)
+    x = wl.normal((w.T, w.M), 1.0, seed=0)
+    xb = bits(x)
+
+    def run(nt):
+        sub = (ids[:nt].numpy() % E_s).astype(np.int32)
+        t0 = time.perf_counter()
+        o.moe_grouped_forward(xb[:nt], sub, wgb, wdb)
+        return time.perf_counter() - t0
+
+    dt = run(n_tok)
+    if dt < seconds:
+        n_tok = min(w.T, max(n_tok, int(n_tok * seconds / max(dt, 1e-3))))
+        dt = run(n_tok)
+    routes = n_tok * w.k_eff
+    return {"value": n_tok / dt, "unit": "tokens/s", "routes_per_s": routes / dt,
+            "cores": threads, "kind": "oracle",
+            "sample": f"{routes} routes of the first {n_tok} tokens of the 64-expert Zipf top-8 "
+                      f"workload (FP64 grouped experts, per-route loop), {dt:.1f} s; "
+                      "extrapolated to the workload"}
+
+
 # ---------------------------------------------------------------------------
 # arms
 # ---------------------------------------------------------------------------
@@ -741,6 +783,8 @@ def run_situ(args):
         line["train"] = train
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        if moe:
+            line["moe"]["grouped"]["cpu_baseline"] = cpu_baseline_moe(args.cpu_seconds / 2)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
