@@ -321,3 +321,38 @@ def test_mxfp8_bad_shapes(cuda_dev):
     x = torch.zeros(4, 136, dtype=torch.bfloat16, device=cuda_dev)
     with pytest.raises(situ.SituError, match="UNSUPPORTED"):
         situ.mx_quantize_act(x)
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=FMT_IDS)
+def test_k3_decode_mx_full_size_sampled(oracle, cuda_dev, fmt):
+    """The Kimi-K3-shaped layer (896 routed + 2 shared experts, 512 tokens, M=2048,
+    I=3072) through the grouped MX path at full size; 16 sampled routes (first and
+    last rows of expert groups, random rows) against the oracle's MX FFN of their
+    expert on their token."""
+    w = wl.WORKLOADS["k3_decode"]
+    E = w.num_experts
+    ids = wl.routes(w, seed=0)
+    x = wl.normal((w.T, w.M), 1.0, seed=0, device=cuda_dev)
+    wgu, wd = wl.expert_weights(E, w.M, w.I, seed=0, device=cuda_dev)
+    wguq = situ.mx_quantize_weights(wgu, situ.MX_GATE_UP, fmt)
+    wdq = situ.mx_quantize_weights(wd, situ.MX_DOWN, fmt)
+    off, tix = situ.situ_moe_build_index(ids.to(cuda_dev), E)
+    y = situ.situ_moe_grouped_forward_mxfp8(x, off, tix, wguq, wdq, w.k_eff)
+    torch.cuda.synchronize()
+    assert situ.device_status(clear=True) == 0
+    off_c, tix_c = off.cpu().numpy(), tix.cpu().numpy()
+    nonempty = np.flatnonzero(np.diff(off_c) > 0)
+    g = torch.Generator().manual_seed(12)
+    pick = [int(off_c[nonempty[0]]), int(off_c[nonempty[-1] + 1] - 1)]
+    pick += torch.randint(0, w.T * w.k_eff, (14,), generator=g).tolist()
+    for r in pick:
+        flat = int(tix_c[r])
+        t, s = divmod(flat, w.k_eff)
+        e = int(ids[t, s])
+        y_ref, _, _ = oracle.mx_ffn_forward(_oracle_q(oracle, x[t:t + 1].cpu()),
+                                            _oracle_wq(oracle, wgu[e].cpu(), fmt),
+                                            _oracle_wq(oracle, wd[e].cpu(), fmt),
+                                            weights_fp4=fmt == situ.MX_E2M1)
+        assert_ffn_close(to_f64(y[t, s:s + 1]), y_ref, f"K3 MX route {r} (t={t}, s={s}, e={e})")
+    del wgu, wd, wguq, wdq
+    torch.cuda.empty_cache()
