@@ -1,37 +1,18 @@
-// gemm.cu -- persistent, warp-specialised tcgen05 GEMMs for the SiTU-GLU
-// feed-forward on sm_103a, dense or grouped over experts.
-//
+// gemm.cu -- the bf16 tcgen05 GEMMs of the SiTU-GLU feed-forward on sm_103a
+// (the kernel itself is in gemm_kernel.cuh): dispatch of the forward GEMMs
 //   gate_up + SiTU-GLU:  h[r, j] = SiTU-GLU(x[r] . Wgu[j], x[r] . Wgu[I + j])
 //   down:                y[r, m] = h[r] . Wd[m]
 // ("DenseFFN and SituGLU - Docs - Kimi K3 from Scratch", "Two linear maps and a
-// guarded compiled branch": packed gate_up_proj M -> 2I, down_proj I -> M; the
-// activation of "SiTU-GLU: one split, two softly bounded branches" applied to the
-// FP32 accumulators so the [R, 2I] product never reaches memory.)
-//
-// Design (one CTA per SM, 192 threads):
-//   warp 0      TMA producer: per k-block, one 128x64 A box and two 128x64 B
-//               boxes (gate rows and the matching up rows for the SiTU GEMM; two
-//               adjacent 128-row halves for the plain GEMM) into a 4-stage ring of
-//               128-byte-swizzled shared-memory buffers.
-//   warp 1      MMA issuer: tcgen05.mma kind::f16, M=128 N=256 K=16, accumulating
-//               in tensor memory; tcgen05.commit frees each stage and publishes each
-//               finished accumulator.  Two 256-column accumulators (all 512 TMEM
-//               columns) let the epilogue of tile i overlap the MMAs of tile i+1.
-//   warps 2..5  epilogue: tcgen05.ld of the FP32 accumulator (thread = tile row),
-//               SiTU-GLU on (gate column j, up column 128 + j) or plain conversion,
-//               bf16 round-to-nearest-even, 16-byte stores of each row's segment.
-// Tiles are walked in (m-tile, n-tile) order with a grid-wide stride, so the
-// n-tiles of one m-tile run side by side and share the A rows in L2.
-// Every wait is bounded (mbar_wait); on a timeout the CTA records
-// SITU_ERR_TIMEOUT, drains its in-flight copies and MMAs with bounded waits,
-// frees its tensor memory and exits.
+// guarded compiled branch"), dense or grouped over experts, and of the backward
+// GEMMs (the activation's derivative in the dh epilogue; MN-major operands; the
+// K-grouped per-expert weight gradients); plus the small kernels of the grouped
+// path (per-group tile and unit prefixes, row gather) and the bounded-wait self test.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
-
 
 #include "gemm_kernel.cuh"
 

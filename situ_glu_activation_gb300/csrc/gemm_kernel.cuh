@@ -2,6 +2,30 @@
 // by the bf16 GEMMs (gemm.cu) and the MXFP8 block-scaled GEMMs (mx_gemm.cu), with
 // its host-side launch.  Included by exactly those translation units; everything
 // is in an anonymous namespace, so each unit instantiates what it launches.
+//
+// One CTA per SM (persistent), 192 threads (224 for MXFP8):
+//   warp 0      TMA producer: per k-block, the A box(es) and two B halves into a ring
+//               of 128-byte-swizzled shared-memory stages (bf16: 4 stages of
+//               A 128x64 + B 256x64; MXFP8: 5 stages of A 128x128 + B 192x128 codes
+//               and the stage's scale tiles).
+//   warp 1      MMA issuer: tcgen05.mma (kind::f16 M=128 N=256 K=16, or M=64 for tiles
+//               with at most 64 rows; kind::mxf8f6f4 block-scaled M=128 N=192 K=32),
+//               accumulating in tensor memory; tcgen05.commit frees each stage and
+//               publishes each finished accumulator.  Two accumulators let the
+//               epilogue of tile i overlap the MMAs of tile i+1.
+//   warps 2..5  epilogue: tcgen05.ld (thread = tile row); SiTU-GLU on (gate column j,
+//               up column BN/2 + j) with bf16 or MXFP8 output, plain conversion, the
+//               activation's derivative (backward), or a fused weighted scatter-add.
+//   warp 6      (MXFP8) copies each stage's scale tiles into TMEM as it lands.
+// Work is scheduled in units of two tiles for the two CTAs of a cluster: adjacent
+// m-tiles of one n-tile sharing the B tile, or -- for a group's odd last m-tile --
+// adjacent n-tiles sharing the A tile; each CTA fetches half of the shared tile and
+// multicasts it.  Units run in (group, m-pair, n-tile) order, so the n-tiles of one
+// m-tile run side by side and share A in L2.  Operands are K-major, or MN-major
+// ({64, 64} boxes) for the backward, which also has a K-grouped schedule (each group
+// contracts over its own row range).  Every wait is bounded (ctl_wait / mbar_wait);
+// on a timeout the CTA records SITU_ERR_TIMEOUT, drains its in-flight copies and
+// MMAs with bounded waits, frees its tensor memory and exits.
 #pragma once
 
 #include <cuda.h>
