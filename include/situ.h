@@ -83,6 +83,15 @@ const char* situ_status_string(situ_status s);
  * ("" if none).  Static storage per thread; valid until the next call. */
 const char* situ_last_cuda_error(void);
 
+/* Which path this host thread's last successful bf16 situ_ffn_forward took:
+ * SITU_FFN_PATH_FUSED (one persistent launch for both projections),
+ * SITU_FFN_PATH_TWO_LAUNCHES (the device refused that grid as co-resident, so the
+ * projections ran as two launches), or 0 before the first such call.  Both paths
+ * produce the same bits. */
+#define SITU_FFN_PATH_FUSED 1
+#define SITU_FFN_PATH_TWO_LAUNCHES 2
+int situ_ffn_last_path(void);
+
 /* Device-side status of the current device: SITU_OK, or the first failure a
  * kernel recorded since the last clear (SITU_ERR_TIMEOUT, SITU_ERR_INDEX).
  * Synchronous: call it after synchronising the streams the kernels ran on.
@@ -123,8 +132,10 @@ situ_status situ_glu_act(const void* gate_up, void* out, int64_t rows, int64_t I
  *   y  = dtype(h W_down^T)        (FP32 accumulation)
  * For bf16 the gate_up product and the activation run in one tcgen05 GEMM whose
  * epilogue applies SiTU-GLU to the FP32 accumulators, so the [R, 2I] tensor never
- * reaches memory; h ([R, I], bf16) is written to the workspace and read back by a
- * second tcgen05 GEMM.
+ * reaches memory; h ([R, I], bf16) is written to the workspace and read back by the
+ * down GEMM.  Both GEMMs run in one persistent launch: a down tile starts once every
+ * gate_up tile of its 128 rows has stored its h (two launches when the grid cannot be
+ * made co-resident).
  *
  *   x          device, [R, M] of `dt`.
  *   W_gate_up  device, [2I, M] of `dt`.
@@ -132,7 +143,8 @@ situ_status situ_glu_act(const void* gate_up, void* out, int64_t rows, int64_t I
  *   y          device, [R, M] of `dt`, written; must not overlap any input or the
  *              workspace.
  *   workspace  device, >= situ_ffn_workspace_size(R, M, I, dt) bytes, 256-byte
- *              aligned; its contents are overwritten (h lives there).
+ *              aligned; its contents are overwritten: h [R, I] first (rounded up to
+ *              256 bytes) then, for bf16, one int32 per 128-row tile of h-ready counts.
  *   R >= 0, M >= 1, I >= 1.  bf16 requires M % 8 == 0, I % 8 == 0 and 16-byte
  *   aligned x, W_gate_up, W_down and y (tensor-memory-access rules); otherwise
  *   SITU_ERR_UNSUPPORTED / SITU_ERR_ALIGN.  f32 accepts any shape.

@@ -624,6 +624,15 @@ def situ_moe_combine(y: torch.Tensor, weights: torch.Tensor,
     return out
 
 
+FFN_PATH_FUSED, FFN_PATH_TWO_LAUNCHES = 1, 2
+
+
+def ffn_last_path() -> int:
+    """The path of this thread's last bf16 situ_ffn_forward: FFN_PATH_FUSED (one
+    persistent launch), FFN_PATH_TWO_LAUNCHES, or 0 before the first call."""
+    return int(_native.lib().situ_ffn_last_path())
+
+
 def device_status(clear: bool = True) -> int:
     """First device-side failure recorded since the last clear (0 = SITU_OK)."""
     return int(_native.lib().situ_device_status(1 if clear else 0))
@@ -642,6 +651,7 @@ __all__ = [
     "situ_moe_build_index",
     "situ_moe_grouped_forward", "ffn_workspace_bytes", "moe_workspace_bytes",
     "device_status", "selftest_bounded_wait", "ffn_host_workspace_bytes", "situ_moe_combine",
+    "ffn_last_path", "FFN_PATH_FUSED", "FFN_PATH_TWO_LAUNCHES",
     "situ_ffn_forward_train", "situ_ffn_backward", "ffn_backward_workspace_bytes",
     "situ_moe_grouped_forward_train", "situ_moe_grouped_backward", "moe_backward_workspace_bytes",
     "situ_moe_grouped_forward_combined", "moe_combined_workspace_bytes",

@@ -30,6 +30,7 @@ struct DeviceState {
 DeviceState g_devices[kMaxDevices];
 std::mutex g_mutex;
 thread_local char t_last_cuda_error[256] = "";
+thread_local int t_ffn_path = 0;  // the path of this thread's last bf16 dense forward
 
 situ_status cuda_fail(cudaError_t e) {
   std::snprintf(t_last_cuda_error, sizeof t_last_cuda_error, "%s: %s", cudaGetErrorName(e),
@@ -106,6 +107,8 @@ const char* situ_status_string(situ_status s) {
 
 const char* situ_last_cuda_error(void) { return t_last_cuda_error; }
 
+int situ_ffn_last_path(void) { return t_ffn_path; }
+
 situ_status situ_device_status(int clear) {
   DeviceState* st = nullptr;
   situ_status s = device_state(&st);
@@ -143,7 +146,10 @@ situ_status situ_glu_act(const void* gate_up, void* out, int64_t rows, int64_t I
 size_t situ_ffn_workspace_size(int64_t R, int64_t M, int64_t I, situ_dtype dt) {
   (void)M;
   if (R <= 0 || I <= 0 || !dtype_ok(dt)) return 0;
-  return round_up(static_cast<size_t>(R) * I * dtype_size(dt), 256);
+  const size_t h = round_up(static_cast<size_t>(R) * I * dtype_size(dt), 256);
+  if (dt == SITU_F32) return h;
+  // bf16: h, then one int32 per 128-row m-tile (the fused launch's h-ready counts).
+  return h + round_up(static_cast<size_t>((R + 127) / 128) * 4, 256);
 }
 
 namespace {
@@ -239,7 +245,46 @@ situ_status situ_ffn_forward(const void* x, const void* W_gate_up, const void* W
   }
   if ((s = bf16_gemm_checks(x, W_gate_up, W_down, M, I)) != SITU_OK) return s;
   if (!aligned16(y)) return SITU_ERR_ALIGN;
-  cudaError_t e = run_gate_up(st, x, W_gate_up, workspace, R, M, I, beta, linear_beta, cs);
+  // One persistent launch for both GEMMs (down tiles start as the gate_up tiles of
+  // their rows complete); two launches when that grid cannot be co-resident.
+  GemmShape g{};
+  g.a = x;
+  g.a_rows = R;
+  g.b = W_gate_up;
+  g.b_rows = 2 * I;
+  g.K = M;
+  g.num_groups = 1;
+  g.b_group_rows = 2 * I;
+  g.b_up_offset = I;
+  g.n_out = I;
+  g.out = workspace;
+  g.ldo = I;
+  g.out_rows = R;
+  GemmShape d{};
+  d.a = workspace;
+  d.a_rows = R;
+  d.b = W_down;
+  d.b_rows = M;
+  d.K = I;
+  d.num_groups = 1;
+  d.b_group_rows = M;
+  d.n_out = M;
+  d.out = y;
+  d.ldo = M;
+  d.out_rows = R;
+  int32_t* h_ready = reinterpret_cast<int32_t*>(
+      static_cast<uint8_t*>(workspace) + round_up(static_cast<size_t>(R) * I * 2, 256));
+  cudaError_t e = launch_ffn_fused(g, d, p, caps_of(beta, linear_beta), h_ready, st->status,
+                                   st->num_sms, cs);
+  if (e == cudaSuccess) {
+    t_ffn_path = SITU_FFN_PATH_FUSED;
+    return SITU_OK;
+  }
+  // A refused launch configuration is not sticky: clear it and take the two launches
+  // (a sticky error fails them as well and is reported from there).
+  (void)cudaGetLastError();
+  t_ffn_path = SITU_FFN_PATH_TWO_LAUNCHES;
+  e = run_gate_up(st, x, W_gate_up, workspace, R, M, I, beta, linear_beta, cs);
   if (e != cudaSuccess) return cuda_fail(e);
   return finish(run_down(st, workspace, W_down, y, R, M, I, cs));
 }

@@ -186,6 +186,23 @@ cudaError_t launch_gemm_situ_bwd(const GemmShape& s, const SituParams& p, Caps c
   return cudaErrorInvalidValue;
 }
 
+cudaError_t launch_ffn_fused(const GemmShape& s_gu, const GemmShape& s_dn, const SituParams& p,
+                             Caps caps, int32_t* h_ready, uint32_t* status, int num_sms,
+                             cudaStream_t stream) {
+  switch (caps) {
+    case Caps::kBoth:
+      return launch_ffn_fused_impl<Caps::kBoth>(s_gu, s_dn, p, h_ready, status, num_sms, stream);
+    case Caps::kGateOnly:
+      return launch_ffn_fused_impl<Caps::kGateOnly>(s_gu, s_dn, p, h_ready, status, num_sms,
+                                                    stream);
+    case Caps::kUpOnly:
+      return launch_ffn_fused_impl<Caps::kUpOnly>(s_gu, s_dn, p, h_ready, status, num_sms, stream);
+    case Caps::kNone:
+      return launch_ffn_fused_impl<Caps::kNone>(s_gu, s_dn, p, h_ready, status, num_sms, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,
                                int32_t n_tiles_1, int32_t n_tiles_2, int32_t* tile_offsets,
                                int32_t* units_1, int32_t* units_2, uint32_t* status,

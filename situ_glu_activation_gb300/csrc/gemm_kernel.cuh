@@ -122,8 +122,11 @@ constexpr uint32_t kSfTmemCols = 12;  // per stage: A 4 columns, B 8 columns
 // dh accumulators into d(gate, up) through the activation's derivative, reading
 // the saved pre-activation pair.
 // kSituMx (MXFP8 only) applies SiTU-GLU, rounds h to bf16 and stores it as MXFP8
-// codes and scales, the input format of the next block-scaled GEMM.
-enum class Epi { kSitu, kPlain, kSituBwd, kSituMx };
+// codes and scales, the input format of the next block-scaled GEMM.  kFfn is the
+// whole dense FFN in one persistent launch: units [0, fused_units1) are gate_up
+// tiles with the SiTU epilogue (h), the rest are down tiles with the plain epilogue
+// (y); a down tile starts once every gate_up tile of its rows has stored its h.
+enum class Epi { kSitu, kPlain, kSituBwd, kSituMx, kFfn };
 
 struct Args {
   int32_t num_groups;
@@ -169,6 +172,14 @@ struct Args {
   const float* combine_w;
   float* combine_out;
   int32_t combine_k;
+  // kFfn: the down GEMM's geometry and output, and the per-m-tile count of gate_up
+  // tiles whose h rows are stored (zeroed before the launch; ready at h_ready_target).
+  int32_t fused_units1, fused_units2;
+  int32_t n_tiles2, k_blocks2;
+  int64_t n_out2, ldo2;
+  __nv_bfloat16* out2;
+  int32_t* h_ready;
+  int32_t h_ready_target;
 };
 
 struct SharedCtl {
@@ -192,6 +203,7 @@ struct TileCoord {
   int32_t k0;       // first K row of the contraction (K-grouped; 0 otherwise)
   int32_t k_end;    // one past its last K row (K-grouped)
   int32_t k_blocks; // k-blocks of this tile
+  int32_t phase2;   // kFfn: a down tile
 };
 
 __device__ __forceinline__ int32_t total_tiles(const Args& a) {
@@ -226,11 +238,11 @@ __device__ __forceinline__ TileCoord decode_tile(const Args& a, int32_t t) {
 }
 
 // Tile `local` of one group's rows row0 .. row_end-1 (unpaired: m-tile-major).
-__device__ __forceinline__ TileCoord in_group_tile(const Args& a, int32_t local, int32_t row0,
+__device__ __forceinline__ TileCoord in_group_tile(int32_t n_tiles, int32_t local, int32_t row0,
                                                    int32_t row_end) {
   TileCoord c;
-  const int32_t mt = local / a.n_tiles;
-  c.n_tile = local - mt * a.n_tiles;
+  const int32_t mt = local / n_tiles;
+  c.n_tile = local - mt * n_tiles;
   c.a_row0 = row0 + mt * kBM;
   c.row_end = row_end;
   c.group = 0;
@@ -248,21 +260,21 @@ __device__ __forceinline__ TileCoord in_group_tile(const Args& a, int32_t local,
 //     the A tile, each fetching 64 of its 128 rows and multicasting them.
 // Dense calls are one group of all rows; grouped calls read the per-group unit
 // prefix from unit_offsets.
-__device__ __forceinline__ int32_t units_of(int32_t m, int32_t n_tiles) {
+__host__ __device__ __forceinline__ int32_t units_of(int32_t m, int32_t n_tiles) {
   return (m >> 1) * n_tiles + (m & 1) * ((n_tiles + 1) >> 1);
 }
 
 // Paired unit `local` of one group's rows row0 .. row_end-1 (see above).
-__device__ __forceinline__ TileCoord in_group_unit(const Args& a, int32_t local, uint32_t rank,
+__device__ __forceinline__ TileCoord in_group_unit(int32_t n_tiles, int32_t local, uint32_t rank,
                                                    int32_t row0, int32_t row_end) {
   const int32_t m = (row_end - row0 + kBM - 1) / kBM;
-  const int32_t shared_b_units = (m >> 1) * a.n_tiles;
+  const int32_t shared_b_units = (m >> 1) * n_tiles;
   TileCoord c;
   c.group = 0;
   c.row_end = row_end;
   if (local < shared_b_units) {
-    const int32_t p = local / a.n_tiles;
-    c.n_tile = local - p * a.n_tiles;
+    const int32_t p = local / n_tiles;
+    c.n_tile = local - p * n_tiles;
     c.a_row0 = row0 + (2 * p + static_cast<int32_t>(rank)) * kBM;
     c.share_a = 0;
   } else {
@@ -274,8 +286,9 @@ __device__ __forceinline__ TileCoord in_group_unit(const Args& a, int32_t local,
   return c;
 }
 
-template <bool kPair, bool kKG>
+template <bool kPair, bool kKG, bool kFfn = false>
 __device__ __forceinline__ int32_t num_units(const Args& a) {
+  if (kFfn) return a.fused_units1 + a.fused_units2;
   if (kKG) {
     if (a.tile_offsets && __ldg(a.tile_offsets + a.num_groups) == 0) return 0;
     return a.num_groups * a.units_per_group;
@@ -285,15 +298,31 @@ __device__ __forceinline__ int32_t num_units(const Args& a) {
   return units_of((a.dense_rows + kBM - 1) / kBM, a.n_tiles);
 }
 
-template <bool kPair, bool kKG>
+template <bool kPair, bool kKG, bool kFfn = false>
 __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_t rank) {
   TileCoord c;
+  if (kFfn) {
+    // The gate_up units, then the down units, both over the dense rows.
+    const bool p2 = u >= a.fused_units1;
+    const int32_t local = p2 ? u - a.fused_units1 : u;
+    const int32_t nt = p2 ? a.n_tiles2 : a.n_tiles;
+    c = kPair ? in_group_unit(nt, local, rank, 0, a.dense_rows)
+              : in_group_tile(nt, local, 0, a.dense_rows);
+    c.group = 0;
+    c.k0 = 0;
+    c.k_end = 0;
+    c.k_blocks = p2 ? a.k_blocks2 : a.k_blocks;
+    c.phase2 = p2 ? 1 : 0;
+    return c;
+  }
+  c.phase2 = 0;
   if (kKG) {
     // Every group has the same output tiles; its K range is its row range.
     const int32_t g = u / a.units_per_group;
     const int32_t local = u - g * a.units_per_group;
-    c = kPair ? in_group_unit(a, local, rank, 0, a.dense_rows)
-              : in_group_tile(a, local, 0, a.dense_rows);
+    c = kPair ? in_group_unit(a.n_tiles, local, rank, 0, a.dense_rows)
+              : in_group_tile(a.n_tiles, local, 0, a.dense_rows);
+    c.phase2 = 0;
     c.group = g;
     c.k0 = __ldg(a.k_group_offsets + g);
     c.k_end = __ldg(a.k_group_offsets + g + 1);
@@ -315,9 +344,10 @@ __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_
       row_end = __ldg(a.group_offsets + g + 1);
       local = u - __ldg(a.unit_offsets + g);
     }
-    c = in_group_unit(a, local, rank, row0, row_end);
+    c = in_group_unit(a.n_tiles, local, rank, row0, row_end);
     c.group = g;
   }
+  c.phase2 = 0;
   c.k0 = 0;
   c.k_end = 0;
   c.k_blocks = a.k_blocks;
@@ -354,6 +384,26 @@ __device__ __forceinline__ void zero_k_tail(uint32_t sa, uint32_t sb, int32_t kv
   for (int at = 0; at < 6; ++at) {
     const uint32_t base = (at < 2 ? sa + at * kMnAtomBytes : sb + (at - 2) * kMnAtomBytes) + first;
     for (uint32_t i = lane; i < n; i += 32) st_shared_zero16(base + 16u * i);
+  }
+}
+
+// Bounded wait (as ctl_wait) until the int32 at p reaches target (acquire).
+__device__ __forceinline__ bool wait_count(SharedCtl* ctl, const int32_t* p, int32_t target,
+                                           uint32_t* status) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t polls = 0;
+  while (true) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if ((++polls & 15u) == 0u) {
+      if (ctl->abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        record_status(status, SITU_ERR_TIMEOUT);
+        ctl->abort = 1;
+        return false;
+      }
+    }
   }
 }
 
@@ -412,7 +462,10 @@ template <Epi kEpi, Caps kC, bool kPair, bool kStoreGu, Major kMajor, int kMx = 
 __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_a64,
-                    const __grid_constant__ CUtensorMap map_b, const Args args) {
+                    const __grid_constant__ CUtensorMap map_b,
+                    const __grid_constant__ CUtensorMap map_a2,
+                    const __grid_constant__ CUtensorMap map_a2_64,
+                    const __grid_constant__ CUtensorMap map_b2, const Args args) {
   using G = Geo<kMx>;
   static_assert(!kMx || kMajor == Major::kKMajor, "MXFP8 operands are K-major");
   static_assert(kMx || kEpi != Epi::kSituMx, "the MXFP8 epilogue needs MXFP8 GEMMs");
@@ -422,6 +475,8 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
                                              ~static_cast<uintptr_t>(1023));
   SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + G::Stages * G::StageBytes);
   constexpr bool kSituEpi = kEpi == Epi::kSitu || kEpi == Epi::kSituMx;
+  constexpr bool kFfn = kEpi == Epi::kFfn;
+  static_assert(!kFfn || (kMajor == Major::kKMajor && !kMx), "the fused FFN is bf16 K-major");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -450,6 +505,11 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
     tma_prefetch_map(&map_a);
     if (kPair) tma_prefetch_map(&map_a64);
     tma_prefetch_map(&map_b);
+    if (kFfn) {
+      tma_prefetch_map(&map_a2);
+      if (kPair) tma_prefetch_map(&map_a2_64);
+      tma_prefetch_map(&map_b2);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
@@ -460,7 +520,7 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
   if (kPair) cluster_sync();  // the peer's barriers exist before any multicast
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
-  const int32_t n_total = num_units<kPair, kKG>(args);
+  const int32_t n_total = num_units<kPair, kKG, kFfn>(args);
   const int32_t u0 = kPair ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x);
   const int32_t ustride = kPair ? static_cast<int32_t>(gridDim.x >> 1) : static_cast<int32_t>(gridDim.x);
 
@@ -471,14 +531,20 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
       uint32_t issued = 0;
       bool ok = true;
       for (int32_t t = u0; t < n_total && ok; t += ustride) {
-        const TileCoord tc = unit_tile<kPair, kKG>(args, t, rank);
+        const TileCoord tc = unit_tile<kPair, kKG, kFfn>(args, t, rank);
         const int64_t gbase = static_cast<int64_t>(tc.group) * args.b_group_rows;
+        // kFfn: gate_up tiles read x and W_gate_up, down tiles read h and W_down.
+        const bool p2 = kFfn && tc.phase2;
+        const CUtensorMap* pm_a = p2 ? &map_a2 : &map_a;
+        const CUtensorMap* pm_a64 = p2 ? &map_a2_64 : &map_a64;
+        const CUtensorMap* pm_b = p2 ? &map_b2 : &map_b;
+        const bool situ_tile = kSituEpi || (kFfn && !p2);
         constexpr bool kBMNp = kMajor != Major::kKMajor;
         // K-major B: a group's weights are b_group_rows further down the N rows.
         // MN-major B: they are b_group_rows further down the K rows (grouped by
         // rows), or the contraction itself starts at k0 (K-grouped).
         int32_t b_row0, b_row1, kb_off = 0;
-        if (kSituEpi) {
+        if (situ_tile) {
           b_row0 = static_cast<int32_t>(gbase + static_cast<int64_t>(tc.n_tile) * (G::BN / 2));
           b_row1 = static_cast<int32_t>(gbase + args.b_up_offset +
                                         static_cast<int64_t>(tc.n_tile) * (G::BN / 2));
@@ -502,6 +568,16 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
           sfb_unit = args.sfb + (static_cast<int64_t>(tc.group) * args.n_tiles + tc.n_tile) *
                                     args.k_blocks * kSfbStageBytes;
         }
+        if (p2) {
+          // The h rows of this tile's m-tile must be stored by every gate_up tile:
+          // acquire the count, then order the TMA reads of h after it.
+          const int32_t mt = tc.a_row0 / kBM;
+          if (!wait_count(ctl, args.h_ready + mt, args.h_ready_target, args.status)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_all();
+        }
         for (int32_t kb = 0; kb < tc.k_blocks; ++kb) {
           if (!ctl_wait(ctl, &ctl->empty[stage], phase ^ 1u, args.status)) {
             ok = false;
@@ -520,14 +596,14 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
             for (int j = 0; j < rows64; ++j) {
               const uint32_t d = dst + j * (kAMN ? kMnAtomBytes : 0u);
               if (kAMN) {
-                if (mcast) tma_load_2d_multicast(d, &map_a, row + 64 * j, kx, full, 0x3);
-                else tma_load_2d(d, &map_a, row + 64 * j, kx, full);
+                if (mcast) tma_load_2d_multicast(d, pm_a, row + 64 * j, kx, full, 0x3);
+                else tma_load_2d(d, pm_a, row + 64 * j, kx, full);
               } else if (rows64 == 2) {
-                tma_load_2d(d, &map_a, kx, row, full);
+                tma_load_2d(d, pm_a, kx, row, full);
                 break;
               } else {
-                if (mcast) tma_load_2d_multicast(d, &map_a64, kx, row, full, 0x3);
-                else tma_load_2d(d, &map_a64, kx, row, full);
+                if (mcast) tma_load_2d_multicast(d, pm_a64, kx, row, full, 0x3);
+                else tma_load_2d(d, pm_a64, kx, row, full);
               }
             }
           };
@@ -535,12 +611,12 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
           auto load_b = [&](uint32_t dst, int32_t row, bool mcast) {
             if (kBMN) {
               for (int j = 0; j < 2; ++j) {
-                if (mcast) tma_load_2d_multicast(dst + j * kMnAtomBytes, &map_b, row + 64 * j, kxb, full, 0x3);
-                else tma_load_2d(dst + j * kMnAtomBytes, &map_b, row + 64 * j, kxb, full);
+                if (mcast) tma_load_2d_multicast(dst + j * kMnAtomBytes, pm_b, row + 64 * j, kxb, full, 0x3);
+                else tma_load_2d(dst + j * kMnAtomBytes, pm_b, row + 64 * j, kxb, full);
               }
             } else {
-              if (mcast) tma_load_2d_multicast(dst, &map_b, kxb, row, full, 0x3);
-              else tma_load_2d(dst, &map_b, kxb, row, full);
+              if (mcast) tma_load_2d_multicast(dst, pm_b, kxb, row, full, 0x3);
+              else tma_load_2d(dst, pm_b, kxb, row, full);
             }
           };
           constexpr uint32_t kBHalf = G::BHalfRows * 128;  // bytes of one B half
@@ -607,7 +683,7 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * G::BN;
-        const TileCoord tcm = unit_tile<kPair, kKG>(args, t, rank);
+        const TileCoord tcm = unit_tile<kPair, kKG, kFfn>(args, t, rank);
         const uint32_t idesc = kMx ? idesc_mxf8(kBM, G::BN, kMx == 2 ? kMxE2M1 : kMxE4M3)
                                    : (tcm.row_end - tcm.a_row0 <= 64 ? kIdescHalf : kIdesc) |
                                          (a_mn_major(kMajor) ? kAMnBit : 0u) |
@@ -687,7 +763,7 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int32_t t = u0; t < n_total && ok; t += ustride) {
-        const TileCoord tcs = unit_tile<kPair, kKG>(args, t, rank);
+        const TileCoord tcs = unit_tile<kPair, kKG, kFfn>(args, t, rank);
         for (int32_t kb = 0; kb < tcs.k_blocks; ++kb) {
           if (!ctl_wait(ctl, &ctl->full[stage], phase, args.status)) {
             ok = false;
@@ -726,7 +802,8 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after_sync();
-      const TileCoord tc = unit_tile<kPair, kKG>(args, t, rank);
+      const TileCoord tc = unit_tile<kPair, kKG, kFfn>(args, t, rank);
+      const bool p2 = kFfn && tc.phase2;
       // M=64 tiles (bf16 only): only the first 16 lanes of each quarter hold rows
       // (16q + lane).
       const bool half = !kMx && tc.row_end - tc.a_row0 <= 64;
@@ -745,7 +822,7 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
         valid = out_row >= 0 && out_row < args.out_rows;
       }
       const uint32_t t_acc = tmem_base + lane_addr + acc * G::BN;
-      if (kSituEpi) {
+      if (kSituEpi || (kFfn && !p2)) {
         // Gate column j of the tile pairs with up column BN/2 + j.
         constexpr int kHalfN = G::BN / 2;
         __nv_bfloat16* dst_row = args.out + out_row * args.ldo;
@@ -799,6 +876,16 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
             store_row_chunk(gu_row + col0, wg, col0, args.n_out);
             store_row_chunk(gu_row + args.split + col0, wu, col0, args.n_out);
           }
+        }
+        if (kFfn) {
+          // Publish this tile's h rows: each epilogue thread orders its stores, the
+          // epilogue warps meet, and one release add counts the tile for its m-tile
+          // (a shared-A unit's tile past the last n-tile stores nothing and does not
+          // count).
+          __threadfence();
+          named_barrier_sync(1, kEpiThreads);
+          if (threadIdx.x == 64 && tc.n_tile < args.n_tiles)
+            red_release_add_gpu(args.h_ready + tc.a_row0 / kBM, 1);
         }
       } else if (kEpi == Epi::kSituBwd) {
         const __nv_bfloat16* gu_row = args.gu_in + static_cast<int64_t>(row) * 2 * args.split;
@@ -865,7 +952,8 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
           }
         }
       } else {
-        __nv_bfloat16* dst_row = args.out + out_row * args.ldo;
+        const int64_t n_out = p2 ? args.n_out2 : args.n_out;
+        __nv_bfloat16* dst_row = p2 ? args.out2 + out_row * args.ldo2 : args.out + out_row * args.ldo;
 #pragma unroll 1
         for (int c = 0; c < G::BN / 32; ++c) {
           __syncwarp();
@@ -884,17 +972,17 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
             // rounding).
             if (valid) {
               const float wr = __ldg(args.combine_w + out_row);
-              float* dst = args.combine_out + (out_row / args.combine_k) * args.n_out + col0;
+              float* dst = args.combine_out + (out_row / args.combine_k) * n_out + col0;
 #pragma unroll
               for (int v = 0; v < 8; ++v) {
-                if (col0 + 4 * v + 4 <= args.n_out)
+                if (col0 + 4 * v + 4 <= n_out)
                   red_add_v4_f32(dst + 4 * v, wr * __uint_as_float(a[4 * v]),
                                  wr * __uint_as_float(a[4 * v + 1]), wr * __uint_as_float(a[4 * v + 2]),
                                  wr * __uint_as_float(a[4 * v + 3]));
               }
             }
           } else if (valid) {
-            store_row_chunk(dst_row + col0, w, col0, args.n_out);
+            store_row_chunk(dst_row + col0, w, col0, n_out);
           }
         }
       }
@@ -1098,7 +1186,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx>, ma,
-                              ma64, mb, a);
+                              ma64, mb, ma, ma64, mb, a);
   }
   int grid = num_sms;
   if (s.k_group_offsets) {
@@ -1110,8 +1198,92 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     if (tiles < grid) grid = static_cast<int>(tiles);
   }
   ffn_gemm_kernel<kEpi, kC, false, kStoreGu, kMajor, kMx>
-      <<<grid, G::Threads, kSmem, stream>>>(ma, ma64, mb, a);
+      <<<grid, G::Threads, kSmem, stream>>>(ma, ma64, mb, ma, ma64, mb, a);
   return cudaGetLastError();
+}
+
+// The dense FFN in one persistent launch (Epi::kFfn): s_gu describes the gate_up
+// GEMM (A = x, B = W_gate_up, out = h), s_dn the down GEMM (A = h, B = W_down, out = y);
+// h_ready: one int32 per 128-row m-tile, zeroed here.  Every CTA must be resident at
+// once (down tiles wait for gate_up tiles of other CTAs), so the launch is cooperative:
+// a grid that cannot be co-resident fails to launch instead of waiting.
+template <Caps kC>
+cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
+                                  const SituParams& p, int32_t* h_ready, uint32_t* status,
+                                  int num_sms, cudaStream_t stream) {
+  constexpr size_t kSmem = smem_bytes<0>();
+  if (s_gu.a_rows == 0) return cudaSuccess;
+  CUtensorMap ma, ma64, mb, ma2, ma2_64, mb2;
+  if (!make_map(&ma, s_gu.a, s_gu.a_rows, s_gu.K, 128) ||
+      !make_map(&ma64, s_gu.a, s_gu.a_rows, s_gu.K, 64) ||
+      !make_map(&mb, s_gu.b, s_gu.b_rows, s_gu.K, 128) ||
+      !make_map(&ma2, s_dn.a, s_dn.a_rows, s_dn.K, 128) ||
+      !make_map(&ma2_64, s_dn.a, s_dn.a_rows, s_dn.K, 64) ||
+      !make_map(&mb2, s_dn.b, s_dn.b_rows, s_dn.K, 128))
+    return cudaErrorInvalidValue;
+  const int64_t m_tiles = (s_gu.a_rows + kBM - 1) / kBM;
+  cudaError_t e = cudaMemsetAsync(h_ready, 0, static_cast<size_t>(m_tiles) * 4, stream);
+  if (e != cudaSuccess) return e;
+  Args a{};
+  a.num_groups = 1;
+  a.dense_rows = static_cast<int32_t>(s_gu.a_rows);
+  a.n_tiles = static_cast<int32_t>((s_gu.n_out + 127) / 128);
+  a.k_blocks = static_cast<int32_t>((s_gu.K + kBK - 1) / kBK);
+  a.b_group_rows = s_gu.b_group_rows;
+  a.b_up_offset = s_gu.b_up_offset;
+  a.n_out = s_gu.n_out;
+  a.out = static_cast<__nv_bfloat16*>(s_gu.out);
+  a.ldo = s_gu.ldo;
+  a.out_rows = s_gu.a_rows;
+  a.sp = p;
+  a.status = status;
+  a.combine_k = 1;
+  a.n_tiles2 = static_cast<int32_t>((s_dn.n_out + kBN - 1) / kBN);
+  a.k_blocks2 = static_cast<int32_t>((s_dn.K + kBK - 1) / kBK);
+  a.n_out2 = s_dn.n_out;
+  a.out2 = static_cast<__nv_bfloat16*>(s_dn.out);
+  a.ldo2 = s_dn.ldo;
+  a.h_ready = h_ready;
+  a.h_ready_target = a.n_tiles;
+  static bool smem_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!smem_set[dev]) {
+    for (auto fn : {ffn_gemm_kernel<Epi::kFfn, kC, false, false, Major::kKMajor, 0>,
+                    ffn_gemm_kernel<Epi::kFfn, kC, true, false, Major::kKMajor, 0>}) {
+      if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(kSmem))) != cudaSuccess)
+        return e;
+    }
+    smem_set[dev] = true;
+  }
+  const int clusters = max_pair_clusters<Epi::kFfn, kC, false, Major::kKMajor, 0>(kSmem);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeCooperative;
+  attrs[0].val.cooperative = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = stream;
+  cfg.attrs = attrs;
+  if (clusters > 0) {
+    a.fused_units1 = units_of(static_cast<int32_t>(m_tiles), a.n_tiles);
+    a.fused_units2 = units_of(static_cast<int32_t>(m_tiles), a.n_tiles2);
+    attrs[1].id = cudaLaunchAttributeClusterDimension;
+    attrs[1].val.clusterDim.x = 2;
+    attrs[1].val.clusterDim.y = 1;
+    attrs[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<Epi::kFfn, kC, true, false, Major::kKMajor, 0>,
+                              ma, ma64, mb, ma2, ma2_64, mb2, a);
+  }
+  a.fused_units1 = static_cast<int32_t>(m_tiles) * a.n_tiles;
+  a.fused_units2 = static_cast<int32_t>(m_tiles) * a.n_tiles2;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(num_sms, 1, 1);
+  return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<Epi::kFfn, kC, false, false, Major::kKMajor, 0>,
+                            ma, ma64, mb, ma2, ma2_64, mb2, a);
 }
 
 }  // namespace

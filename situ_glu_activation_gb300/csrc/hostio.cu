@@ -61,8 +61,8 @@ extern "C" size_t situ_ffn_host_workspace_size(int64_t R, int64_t M, int64_t I, 
   const int64_t rows = c < R ? c : R;
   const size_t esz = dtype_size(dt);
   const size_t xb = round256(static_cast<size_t>(rows) * M * esz);
-  const size_t hb = round256(static_cast<size_t>(rows) * I * esz);
-  return 4 * xb + hb;  // x[2], y[2], h
+  const size_t hb = situ_ffn_workspace_size(rows, M, I, dt);
+  return 4 * xb + hb;  // x[2], y[2], the FFN's workspace (h)
 }
 
 extern "C" situ_status situ_ffn_forward_host(const void* x_host, const void* W_gate_up,

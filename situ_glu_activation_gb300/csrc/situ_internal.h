@@ -111,6 +111,13 @@ cudaError_t launch_gemm_situ(const GemmShape& s, const SituParams& p, Caps caps,
 // C = A B^T, bf16 output.
 cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
                               cudaStream_t stream);
+// The dense bf16 FFN in one persistent cooperative launch: s_gu is the gate_up GEMM
+// (SiTU epilogue into h), s_dn the down GEMM (A = h, out = y); h_ready holds one int32
+// per 128-row m-tile of scratch.  Returns an error (and launches nothing) when the
+// grid cannot be co-resident.
+cudaError_t launch_ffn_fused(const GemmShape& s_gu, const GemmShape& s_dn, const SituParams& p,
+                             Caps caps, int32_t* h_ready, uint32_t* status, int num_sms,
+                             cudaStream_t stream);
 // dh = A B^T (B 256-wide tiles like the plain GEMM), epilogue: d(g, u) = dh * the
 // activation's partial derivatives at the saved (g, u).
 cudaError_t launch_gemm_situ_bwd(const GemmShape& s, const SituParams& p, Caps caps,

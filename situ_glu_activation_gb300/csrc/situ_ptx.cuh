@@ -359,6 +359,27 @@ __device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float
                : "memory");
 }
 
+// Acquire load / release add of a global int32 at GPU scope (cross-CTA signals).
+__device__ __forceinline__ int32_t ld_acquire_gpu(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add_gpu(int32_t* p, int32_t v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Orders this thread's earlier memory accesses (all state spaces, generic proxy)
+// against its later async-proxy accesses (TMA loads of data other CTAs stored).
+__device__ __forceinline__ void fence_proxy_async_all() {
+  asm volatile("fence.proxy.async;" ::: "memory");
+}
+
+// Barrier among `count` threads of the CTA on hardware barrier `id` (1..15).
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // 16 zero bytes into this CTA's shared memory (generic proxy).
 __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");

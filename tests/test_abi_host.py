@@ -42,7 +42,9 @@ def test_version_and_status_strings(situ_lib):
 
 
 def test_workspace_sizes(situ_lib):
-    assert situ_lib.situ_ffn_workspace_size(16384, 2048, 3072, 0) == 16384 * 3072 * 2
+    # bf16: h, then one int32 h-ready count per 128-row tile (rounded to 256 B)
+    assert situ_lib.situ_ffn_workspace_size(16384, 2048, 3072, 0) == 16384 * 3072 * 2 + 512
+    assert situ_lib.situ_ffn_workspace_size(300, 8, 8, 0) == 4864 + 256
     assert situ_lib.situ_ffn_workspace_size(3, 8, 5, 1) == 256  # fp32 h, rounded to 256 B
     assert situ_lib.situ_ffn_workspace_size(0, 8, 8, 0) == 0
     R, E, M, I = 1000, 7, 64, 96

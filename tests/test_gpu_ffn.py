@@ -48,6 +48,34 @@ def test_dense_variants(oracle, cuda_dev, caps):
     assert_ffn_close(to_f64(y), ref, f"ffn caps {caps}")
 
 
+@pytest.mark.parametrize("R,M,I,caps", [
+    (300, 512, 384, (4.0, 25.0)),     # 3 row tiles (ragged), pairs and a lone tile
+    (1, 128, 256, (4.0, 25.0)),       # a single row: 64-row MMAs on both projections
+    (77, 136, 200, (4.0, INF)),       # ragged K and N
+    (129, 256, 128, (INF, 25.0)),     # a full tile then a 1-row tile
+    (640, 1024, 1536, (INF, INF)),    # 5 row tiles (odd count)
+    (2000, 512, 64, (1.0, 1.0)),      # one narrow activation tile per row tile
+    (4096, 2048, 3072, (4.0, 25.0)),  # more units than CTAs on both projections
+])
+def test_dense_single_launch_matches_two_launches(cuda_dev, R, M, I, caps):
+    """The one-launch forward (down tiles wait on per-row-tile h-ready counts) gives
+    the bits of the gate_up launch followed by the down launch: the same tiles, the
+    same k order, the same epilogues.  Repeated calls reset the counts."""
+    x, wgu, wd = wl.ffn_inputs(M, I, R, seed=R + I, device=cuda_dev)
+    kw = dict(beta=caps[0], linear_beta=caps[1])
+    h2 = situ.situ_ffn_gate_up(x, wgu, **kw)
+    y2 = situ.situ_ffn_down(h2, wd)
+    ws = torch.empty(situ.ffn_workspace_bytes(R, M, I), dtype=torch.uint8, device=cuda_dev)
+    for _ in range(3):
+        y = situ.situ_ffn_forward(x, wgu, wd, workspace=ws, **kw)
+        assert situ.ffn_last_path() == situ.FFN_PATH_FUSED
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    h = ws[: R * I * 2].view(torch.bfloat16).view(R, I)
+    assert torch.equal(h.view(torch.int16), h2.view(torch.int16))
+    assert situ.device_status() == 0
+
+
 def test_dense_h_in_workspace(oracle, cuda_dev):
     """The fused epilogue's output h (kept in the workspace) matches the oracle's h."""
     R, M, I = 200, 256, 384
