@@ -237,8 +237,9 @@ def bench_dense(args, dev, peaks, world, flush):
 
     per_step, _ = timed_steps(step, args.steps, args.warmup, flush, world)
     ms = mean(per_step)
-    if situ.ffn_last_path() != situ.FFN_PATH_FUSED:
-        raise RuntimeError("the dense forward did not run as one launch")
+    path = situ.ffn_last_path()
+    if path != (situ.FFN_PATH_TWO_LAUNCHES if args.ffn_two_launches else situ.FFN_PATH_FUSED):
+        raise RuntimeError(f"the dense forward took path {path}")
 
     # The same projections as two launches, timed apart: the per-GEMM figures.
     def step2(marks):
@@ -256,7 +257,8 @@ def bench_dense(args, dev, peaks, world, flush):
     flop_gu = 2.0 * w.rows * w.M * 2 * w.I
     flop_down = 2.0 * w.rows * w.I * w.M
     out = {
-        "ms": ms, "tokens": w.rows, "launches_per_step": 1,
+        "ms": ms, "tokens": w.rows, "launches_per_step": 2 if args.ffn_two_launches else 1,
+        "path": "two launches" if args.ffn_two_launches else "one persistent launch",
         "two_launch_ms": mean(per_step2),
         "gate_up_ms": mean(t_gu), "down_ms": mean(t_down),
         "tflops": (flop_gu + flop_down) / (ms * 1e-3) / 1e12,
@@ -697,6 +699,8 @@ def run_situ(args):
     from situ_glu_activation_gb300.build import build
 
     build()
+    if args.ffn_two_launches:
+        situ.ffn_set_single_launch(False)
     peaks, peak_src = load_peaks()
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush = lambda: flush_buf.fill_(1)
@@ -760,14 +764,23 @@ def run_situ(args):
         "tc_frac": dense["tflops"] / peaks["bf16_tflops"],
         "kernels": {"ffn_fused": {"ms": dense["ms"], "tflops": dense["tflops"]},
                     "two_launches": {"ms": dense["two_launch_ms"],
-                                     "ffn_gate_up_situ": {"ms": dense["gate_up_ms"],
-                                                          "tflops": dense["gate_up_tflops"],
-                                                          "frac": dense["gate_up_tflops"] /
-                                                          peaks["bf16_tflops"]},
-                                     "ffn_down": {"ms": dense["down_ms"],
-                                                  "tflops": dense["down_tflops"]}}},
-        "roofline": {"bound": "tensor", "kernel": "ffn_fused (gate_up GEMM + SiTU-GLU epilogue "
-                     "+ down GEMM, one persistent launch)", "achieved": achieved,
+                                     "ffn_gate_up_situ": {
+                                         "ms": dense["gate_up_ms"],
+                                         "tflops": dense["gate_up_tflops"],
+                                         "frac": dense["gate_up_tflops"] / peaks["bf16_tflops"],
+                                         "traffic": profiled_traffic("ffn_gate_up_situ", digest,
+                                                                     w.rows)},
+                                     "ffn_down": {
+                                         "ms": dense["down_ms"],
+                                         "tflops": dense["down_tflops"],
+                                         "frac": dense["down_tflops"] / peaks["bf16_tflops"],
+                                         "traffic": profiled_traffic("ffn_down", digest,
+                                                                     w.rows)}}},
+        "roofline": {"bound": "tensor",
+                     "kernel": ("ffn_gate_up_situ + ffn_down (two launches)"
+                                if args.ffn_two_launches else
+                                "ffn_fused (gate_up GEMM + SiTU-GLU epilogue + down GEMM, one "
+                                "persistent launch)"), "achieved": achieved,
                      "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                      "peak_source": f"{peak_src} (bf16 dense, burst)",
@@ -827,6 +840,9 @@ def main(argv=None):
                          "only; any other name: that workload alone (for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ffn-two-launches", action="store_true",
+                    help="run the bf16 dense forward as two launches (for kernel profilers, "
+                         "which do not replay its cooperative cluster launch)")
     ap.add_argument("--ref-rows", type=int, default=0, help="oracle rows per reference step")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -92,6 +92,13 @@ const char* situ_last_cuda_error(void);
 #define SITU_FFN_PATH_TWO_LAUNCHES 2
 int situ_ffn_last_path(void);
 
+/* Process-wide switch for that single launch (on by default); returns the previous
+ * setting.  With it off, bf16 situ_ffn_forward always runs the two launches.  The
+ * single launch is a cooperative launch of thread-block clusters, which tools that
+ * intercept and replay launches (kernel profilers) may not reproduce faithfully:
+ * turn it off under such a tool. */
+int situ_ffn_set_single_launch(int enable);
+
 /* Device-side status of the current device: SITU_OK, or the first failure a
  * kernel recorded since the last clear (SITU_ERR_TIMEOUT, SITU_ERR_INDEX).
  * Synchronous: call it after synchronising the streams the kernels ran on.

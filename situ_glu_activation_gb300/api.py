@@ -633,6 +633,13 @@ def ffn_last_path() -> int:
     return int(_native.lib().situ_ffn_last_path())
 
 
+def ffn_set_single_launch(enable: bool) -> bool:
+    """Turn the one-launch bf16 dense forward on or off for the process (on by
+    default; off runs the two launches, e.g. under a kernel profiler that cannot
+    replay a cooperative cluster launch).  Returns the previous setting."""
+    return bool(_native.lib().situ_ffn_set_single_launch(1 if enable else 0))
+
+
 def device_status(clear: bool = True) -> int:
     """First device-side failure recorded since the last clear (0 = SITU_OK)."""
     return int(_native.lib().situ_device_status(1 if clear else 0))
@@ -651,7 +658,7 @@ __all__ = [
     "situ_moe_build_index",
     "situ_moe_grouped_forward", "ffn_workspace_bytes", "moe_workspace_bytes",
     "device_status", "selftest_bounded_wait", "ffn_host_workspace_bytes", "situ_moe_combine",
-    "ffn_last_path", "FFN_PATH_FUSED", "FFN_PATH_TWO_LAUNCHES",
+    "ffn_last_path", "FFN_PATH_FUSED", "FFN_PATH_TWO_LAUNCHES", "ffn_set_single_launch",
     "situ_ffn_forward_train", "situ_ffn_backward", "ffn_backward_workspace_bytes",
     "situ_moe_grouped_forward_train", "situ_moe_grouped_backward", "moe_backward_workspace_bytes",
     "situ_moe_grouped_forward_combined", "moe_combined_workspace_bytes",

@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "situ.h"
@@ -31,6 +32,7 @@ DeviceState g_devices[kMaxDevices];
 std::mutex g_mutex;
 thread_local char t_last_cuda_error[256] = "";
 thread_local int t_ffn_path = 0;  // the path of this thread's last bf16 dense forward
+std::atomic<int> g_ffn_single_launch{1};
 
 situ_status cuda_fail(cudaError_t e) {
   std::snprintf(t_last_cuda_error, sizeof t_last_cuda_error, "%s: %s", cudaGetErrorName(e),
@@ -108,6 +110,10 @@ const char* situ_status_string(situ_status s) {
 const char* situ_last_cuda_error(void) { return t_last_cuda_error; }
 
 int situ_ffn_last_path(void) { return t_ffn_path; }
+
+int situ_ffn_set_single_launch(int enable) {
+  return g_ffn_single_launch.exchange(enable ? 1 : 0);
+}
 
 situ_status situ_device_status(int clear) {
   DeviceState* st = nullptr;
@@ -274,15 +280,18 @@ situ_status situ_ffn_forward(const void* x, const void* W_gate_up, const void* W
   d.out_rows = R;
   int32_t* h_ready = reinterpret_cast<int32_t*>(
       static_cast<uint8_t*>(workspace) + round_up(static_cast<size_t>(R) * I * 2, 256));
-  cudaError_t e = launch_ffn_fused(g, d, p, caps_of(beta, linear_beta), h_ready, st->status,
-                                   st->num_sms, cs);
-  if (e == cudaSuccess) {
-    t_ffn_path = SITU_FFN_PATH_FUSED;
-    return SITU_OK;
+  cudaError_t e = cudaSuccess;
+  if (g_ffn_single_launch.load(std::memory_order_relaxed)) {
+    e = launch_ffn_fused(g, d, p, caps_of(beta, linear_beta), h_ready, st->status, st->num_sms,
+                         cs);
+    if (e == cudaSuccess) {
+      t_ffn_path = SITU_FFN_PATH_FUSED;
+      return SITU_OK;
+    }
+    // A refused launch configuration is not sticky: clear it and take the two launches
+    // (a sticky error fails them as well and is reported from there).
+    (void)cudaGetLastError();
   }
-  // A refused launch configuration is not sticky: clear it and take the two launches
-  // (a sticky error fails them as well and is reported from there).
-  (void)cudaGetLastError();
   t_ffn_path = SITU_FFN_PATH_TWO_LAUNCHES;
   e = run_gate_up(st, x, W_gate_up, workspace, R, M, I, beta, linear_beta, cs);
   if (e != cudaSuccess) return cuda_fail(e);

@@ -146,3 +146,12 @@ def test_training_and_mx_argument_checks(situ_lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not found"):
         _native.lib(str(tmp_path / "libsitu.so"))
+
+
+def test_ffn_single_launch_switch(situ_lib):
+    """The process-wide switch for the one-launch dense forward: on by default,
+    returns the previous setting; no dense call has run on this thread yet."""
+    assert situ_lib.situ_ffn_last_path() == 0
+    assert situ_lib.situ_ffn_set_single_launch(0) == 1
+    assert situ_lib.situ_ffn_set_single_launch(7) == 0
+    assert situ_lib.situ_ffn_set_single_launch(1) == 1

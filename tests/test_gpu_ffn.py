@@ -76,6 +76,23 @@ def test_dense_single_launch_matches_two_launches(cuda_dev, R, M, I, caps):
     assert situ.device_status() == 0
 
 
+def test_dense_single_launch_switch(cuda_dev):
+    """With the single launch switched off the dense forward runs the two launches,
+    with the same bits."""
+    R, M, I = 300, 512, 384
+    x, wgu, wd = wl.ffn_inputs(M, I, R, seed=5, device=cuda_dev)
+    y1 = situ.situ_ffn_forward(x, wgu, wd)
+    assert situ.ffn_last_path() == situ.FFN_PATH_FUSED
+    assert situ.ffn_set_single_launch(False) is True
+    try:
+        y2 = situ.situ_ffn_forward(x, wgu, wd)
+        assert situ.ffn_last_path() == situ.FFN_PATH_TWO_LAUNCHES
+    finally:
+        situ.ffn_set_single_launch(True)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
 def test_dense_h_in_workspace(oracle, cuda_dev):
     """The fused epilogue's output h (kept in the workspace) matches the oracle's h."""
     R, M, I = 200, 256, 384
