@@ -835,7 +835,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["situ", "reference"], default="situ")
     ap.add_argument("--suite", default="full",
                     choices=["full", "dense", "act", "grouped", "k3_decode", "k3_prefill",
-                             "k3_prefill_slice", "train", "grouped_train", "mx", "mx_dense"],
+                             "k3_prefill_slice", "k3_decode_slice", "train", "grouped_train",
+                             "mx", "mx_dense"],
                     help="full: the headline line with every sub-result; dense: the headline "
                          "only; any other name: that workload alone (for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)

@@ -85,6 +85,11 @@ WORKLOADS = {
     "k3_prefill_slice": Workload("64 routed experts, 2344 tokens top-8 uniform (about 293 rows "
                                  "per expert, the K3 prefill shape)", "moe", T=2344, E=64, k=8,
                                  routing="uniform"),
+    # A 64-expert slice with the decode's rows per expert (about 6): the same
+    # weight-streaming GEMM shapes with 2.4 GB of weights, for profiling.
+    "k3_decode_slice": Workload("64 routed experts, 48 tokens top-8 uniform (about 6 rows per "
+                                "expert, the K3 decode shape)", "moe", T=48, E=64, k=8,
+                                routing="uniform"),
 }
 
 
