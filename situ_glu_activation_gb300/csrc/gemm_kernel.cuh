@@ -48,7 +48,6 @@ constexpr int kBK = 64;   // K per stage: one 128-byte swizzle row of bf16
 constexpr int kUK = 16;   // K per tcgen05.mma for 16-bit inputs
 constexpr int kAccBufs = 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint64_t kWaitLimitNs = 10ull * 1000 * 1000 * 1000;  // 10 s
 constexpr uint64_t kDrainLimitNs = 100ull * 1000 * 1000;       // 100 ms
@@ -82,7 +81,6 @@ constexpr uint32_t kMnAtomBytes = 64 * 64 * 2;
 // operands, so the stage keeps the MXFP8 geometry and only half the B bytes travel).
 template <int kMx>
 struct Geo {
-  static constexpr int Threads = kThreads;
   static constexpr int BN = 256, BK = 64, UK = 16, Stages = 4, BHalfRows = 128;
   static constexpr uint32_t ABytes = 16384, BBytes = 32768, SfBytes = 0;
   static constexpr uint32_t TxBytes = ABytes + BBytes;  // bytes the copies of a stage bring
@@ -94,7 +92,6 @@ struct Geo<1> {
   // lands, so the MMA warp never issues a tcgen05.cp in front of its own MMAs (a
   // copy issued right before the MMAs that read it held the tensor pipe ~20 % idle,
   // measured on GB300).
-  static constexpr int Threads = kThreads + 32;
   static constexpr int BN = 192, BK = 128, UK = 32, Stages = 5, BHalfRows = 96;
   static constexpr uint32_t ABytes = 16384, BBytes = 24576, SfBytes = 512 + 1024;
   static constexpr uint32_t TxBytes = ABytes + BBytes + SfBytes;
@@ -127,6 +124,22 @@ constexpr uint32_t kSfTmemCols = 12;  // per stage: A 4 columns, B 8 columns
 // tiles with the SiTU epilogue (h), the rest are down tiles with the plain epilogue
 // (y); a down tile starts once every gate_up tile of its rows has stored its h.
 enum class Epi { kSitu, kPlain, kSituBwd, kSituMx, kFfn };
+
+// Epilogue warps: 4 (one per TMEM lane quarter), or 8 for the activation-derivative
+// epilogue, whose per-element work (six SFU ops, ~40 FP32 ops, the saved (g, u) loads
+// and the d(g, u) stores) matches the tile's MMAs: with one warp per SM sub-partition
+// its latency was exposed (the dh GEMM ran at 40 % of the dx GEMM's rate, measured on
+// GB300).  With 8, warps e and e + 4 share a lane quarter and split the columns.
+template <Epi kEpi>
+__host__ __device__ constexpr int epi_warps() {
+  return kEpi == Epi::kSituBwd ? 8 : 4;
+}
+// Threads per CTA: producer and MMA warps, the epilogue warps, and (MXFP8) the scale
+// copier.
+template <Epi kEpi, int kMx>
+__host__ __device__ constexpr int block_threads() {
+  return 32 * (2 + epi_warps<kEpi>() + (kMx ? 1 : 0));
+}
 
 struct Args {
   int32_t num_groups;
@@ -459,7 +472,7 @@ __host__ __device__ __forceinline__ int64_t sf_tile_offset(int64_t m_tile, int64
 }
 
 template <Epi kEpi, Caps kC, bool kPair, bool kStoreGu, Major kMajor, int kMx = 0>
-__global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
+__global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_a64,
                     const __grid_constant__ CUtensorMap map_b,
@@ -493,7 +506,7 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
     }
     for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(smem_u32(&ctl->acc_full[b]), 1);
-      mbar_init(smem_u32(&ctl->acc_empty[b]), kEpiThreads);
+      mbar_init(smem_u32(&ctl->acc_empty[b]), 32 * epi_warps<kEpi>());
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     if (kMx) {
@@ -754,7 +767,7 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
         mbar_wait(smem_u32(&ctl->drain), 0, nullptr, kDrainLimitNs);
       }
     }
-  } else if (kMx && warp == 6) {
+  } else if (kMx && warp == 2 + epi_warps<kEpi>()) {
     // ---------------- scale copier (MXFP8) ----------------
     // Per stage, once its copies landed: the A and B scale tiles into the stage's
     // TMEM slot, then a commit that tells the MMA warp.  A slot is rewritten only
@@ -788,9 +801,12 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
         mbar_wait(smem_u32(&ctl->sf_drain), 0, nullptr, kDrainLimitNs);
       }
     }
-  } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+  } else if (warp >= 2 && warp < 2 + epi_warps<kEpi>()) {
+    // ---------------- epilogue (warps 2 .. 2 + epi_warps - 1) ----------------
     const int quarter = warp & 3;  // TMEM lanes this warp may access
+    // With 8 epilogue warps, warps 2..5 take the first half of the tile's 32-column
+    // chunks and warps 6..9 the second half.
+    const int col_group = (warp - 2) >> 2;
     const int row_in_tile = quarter * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t local = 0;
@@ -909,11 +925,13 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
             }
           }
         };
-        load_gu(0, gq, uq);
+        constexpr int kChunks = 8 / (epi_warps<kEpi>() / 4);  // chunks per warp
+        const int c_begin = col_group * kChunks, c_end = c_begin + kChunks;
+        load_gu(c_begin, gq, uq);
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = c_begin; c < c_end; ++c) {
           uint4 gn[4], un[4];
-          if (c + 1 < 8) load_gu(c + 1, gn, un);
+          if (c + 1 < c_end) load_gu(c + 1, gn, un);
           __syncwarp();
           uint32_t a[32];
           tmem_ld32(t_acc + c * 32, a);
@@ -943,7 +961,7 @@ __global__ void __launch_bounds__(Geo<kMx>::Threads, 1)
               st_global_v4(dgu_row + args.split + cv, ou[0], ou[1], ou[2], ou[3]);
             }
           }
-          if (c + 1 < 8) {
+          if (c + 1 < c_end) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               gq[v] = gn[v];
@@ -1064,7 +1082,7 @@ int max_pair_clusters(size_t smem) {
     done[dev] = true;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(Geo<kMx>::Threads, 1, 1);
+    cfg.blockDim = dim3(block_threads<kEpi, kMx>(), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -1175,7 +1193,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(G::Threads, 1, 1);
+    cfg.blockDim = dim3(block_threads<kEpi, kMx>(), 1, 1);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr;
@@ -1198,7 +1216,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     if (tiles < grid) grid = static_cast<int>(tiles);
   }
   ffn_gemm_kernel<kEpi, kC, false, kStoreGu, kMajor, kMx>
-      <<<grid, G::Threads, kSmem, stream>>>(ma, ma64, mb, ma, ma64, mb, a);
+      <<<grid, block_threads<kEpi, kMx>(), kSmem, stream>>>(ma, ma64, mb, ma, ma64, mb, a);
   return cudaGetLastError();
 }
 
@@ -1262,7 +1280,7 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeCooperative;
   attrs[0].val.cooperative = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(block_threads<Epi::kFfn, 0>(), 1, 1);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
   cfg.attrs = attrs;
