@@ -462,7 +462,9 @@ situ_status situ_ffn_backward(const void* x, const void* W_gate_up, const void* 
     if ((e = launch_gemm_plain(g, st->status, st->num_sms, cs)) != cudaSuccess)
       return cuda_fail(e);
   }
-  // dW_down = dy^T h: both operands read MN-major, contracting over the R rows.
+  // The weight gradients, both operands read MN-major, contracting over the R rows,
+  // in one launch (their tiles together fill the last wave better than either alone):
+  // dW_down = dy^T h and dW_gate_up = dgu^T x.
   {
     GemmShape g{};
     g.a = dy;
@@ -477,25 +479,20 @@ situ_status situ_ffn_backward(const void* x, const void* W_gate_up, const void* 
     g.out = dW_down;
     g.ldo = I;
     g.out_rows = M;
-    if ((e = launch_gemm_plain(g, st->status, st->num_sms, cs)) != cudaSuccess)
-      return cuda_fail(e);
-  }
-  // dW_gate_up = dgu^T x.
-  {
-    GemmShape g{};
-    g.a = dgu;
-    g.a_rows = 2 * I;
-    g.a_mn_major = true;
-    g.b = x;
-    g.b_rows = M;
-    g.b_mn_major = true;
-    g.K = R;
-    g.num_groups = 1;
-    g.n_out = M;
-    g.out = dW_gate_up;
-    g.ldo = M;
-    g.out_rows = 2 * I;
-    if ((e = launch_gemm_plain(g, st->status, st->num_sms, cs)) != cudaSuccess)
+    GemmShape g2{};
+    g2.a = dgu;
+    g2.a_rows = 2 * I;
+    g2.a_mn_major = true;
+    g2.b = x;
+    g2.b_rows = M;
+    g2.b_mn_major = true;
+    g2.K = R;
+    g2.num_groups = 1;
+    g2.n_out = M;
+    g2.out = dW_gate_up;
+    g2.ldo = M;
+    g2.out_rows = 2 * I;
+    if ((e = launch_gemm_plain2(g, g2, st->status, st->num_sms, cs)) != cudaSuccess)
       return cuda_fail(e);
   }
   return SITU_OK;

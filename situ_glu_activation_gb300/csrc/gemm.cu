@@ -203,6 +203,20 @@ cudaError_t launch_ffn_fused(const GemmShape& s_gu, const GemmShape& s_dn, const
   return cudaErrorInvalidValue;
 }
 
+cudaError_t launch_gemm_plain2(const GemmShape& s1, const GemmShape& s2, uint32_t* status,
+                               int num_sms, cudaStream_t stream) {
+  if (s1.a_mn_major != s2.a_mn_major || s1.b_mn_major != s2.b_mn_major || s1.group_offsets ||
+      s2.group_offsets || s1.k_group_offsets || s2.k_group_offsets)
+    return cudaErrorInvalidValue;
+  if (s1.a_mn_major && s1.b_mn_major)
+    return launch_plain2_impl<Major::kABMN>(s1, s2, status, num_sms, stream);
+  if (!s1.a_mn_major && s1.b_mn_major)
+    return launch_plain2_impl<Major::kBMN>(s1, s2, status, num_sms, stream);
+  if (!s1.a_mn_major && !s1.b_mn_major)
+    return launch_plain2_impl<Major::kKMajor>(s1, s2, status, num_sms, stream);
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,
                                int32_t n_tiles_1, int32_t n_tiles_2, int32_t* tile_offsets,
                                int32_t* units_1, int32_t* units_2, uint32_t* status,

@@ -123,7 +123,10 @@ constexpr uint32_t kSfTmemCols = 12;  // per stage: A 4 columns, B 8 columns
 // whole dense FFN in one persistent launch: units [0, fused_units1) are gate_up
 // tiles with the SiTU epilogue (h), the rest are down tiles with the plain epilogue
 // (y); a down tile starts once every gate_up tile of its rows has stored its h.
-enum class Epi { kSitu, kPlain, kSituBwd, kSituMx, kFfn };
+// kPlain2 runs two independent plain GEMMs of the same operand layout in one
+// persistent launch (units of the first, then of the second): the weight gradients of
+// the dense backward, whose own tile counts (192 and 384) leave partial last waves.
+enum class Epi { kSitu, kPlain, kSituBwd, kSituMx, kFfn, kPlain2 };
 
 // Epilogue warps: 4 (one per TMEM lane quarter), or 8 for the activation-derivative
 // epilogue, whose per-element work (six SFU ops, ~40 FP32 ops, the saved (g, u) loads
@@ -187,7 +190,9 @@ struct Args {
   int32_t combine_k;
   // kFfn: the down GEMM's geometry and output, and the per-m-tile count of gate_up
   // tiles whose h rows are stored (zeroed before the launch; ready at h_ready_target).
+  // kPlain2: the second GEMM's geometry and output (its A rows: dense_rows2).
   int32_t fused_units1, fused_units2;
+  int32_t dense_rows2;
   int32_t n_tiles2, k_blocks2;
   int64_t n_out2, ldo2;
   __nv_bfloat16* out2;
@@ -216,7 +221,7 @@ struct TileCoord {
   int32_t k0;       // first K row of the contraction (K-grouped; 0 otherwise)
   int32_t k_end;    // one past its last K row (K-grouped)
   int32_t k_blocks; // k-blocks of this tile
-  int32_t phase2;   // kFfn: a down tile
+  int32_t phase2;   // kFfn: a down tile; kPlain2: a tile of the second GEMM
 };
 
 __device__ __forceinline__ int32_t total_tiles(const Args& a) {
@@ -299,9 +304,9 @@ __device__ __forceinline__ TileCoord in_group_unit(int32_t n_tiles, int32_t loca
   return c;
 }
 
-template <bool kPair, bool kKG, bool kFfn = false>
+template <bool kPair, bool kKG, bool kTwo = false>
 __device__ __forceinline__ int32_t num_units(const Args& a) {
-  if (kFfn) return a.fused_units1 + a.fused_units2;
+  if (kTwo) return a.fused_units1 + a.fused_units2;
   if (kKG) {
     if (a.tile_offsets && __ldg(a.tile_offsets + a.num_groups) == 0) return 0;
     return a.num_groups * a.units_per_group;
@@ -311,16 +316,16 @@ __device__ __forceinline__ int32_t num_units(const Args& a) {
   return units_of((a.dense_rows + kBM - 1) / kBM, a.n_tiles);
 }
 
-template <bool kPair, bool kKG, bool kFfn = false>
+template <bool kPair, bool kKG, bool kTwo = false>
 __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_t rank) {
   TileCoord c;
-  if (kFfn) {
-    // The gate_up units, then the down units, both over the dense rows.
+  if (kTwo) {
+    // The first GEMM's units (gate_up), then the second's (down).
     const bool p2 = u >= a.fused_units1;
     const int32_t local = p2 ? u - a.fused_units1 : u;
     const int32_t nt = p2 ? a.n_tiles2 : a.n_tiles;
-    c = kPair ? in_group_unit(nt, local, rank, 0, a.dense_rows)
-              : in_group_tile(nt, local, 0, a.dense_rows);
+    const int32_t rows = p2 ? a.dense_rows2 : a.dense_rows;
+    c = kPair ? in_group_unit(nt, local, rank, 0, rows) : in_group_tile(nt, local, 0, rows);
     c.group = 0;
     c.k0 = 0;
     c.k_end = 0;
@@ -490,6 +495,10 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
   constexpr bool kSituEpi = kEpi == Epi::kSitu || kEpi == Epi::kSituMx;
   constexpr bool kFfn = kEpi == Epi::kFfn;
   static_assert(!kFfn || (kMajor == Major::kKMajor && !kMx), "the fused FFN is bf16 K-major");
+  // Two GEMMs in one launch: the one-launch FFN, or two independent plain GEMMs.
+  constexpr bool kTwo = kFfn || kEpi == Epi::kPlain2;
+  static_assert(kEpi != Epi::kPlain2 || (!kMx && kMajor != Major::kABMNGrouped),
+                "two plain GEMMs: bf16, not K-grouped");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -518,7 +527,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
     tma_prefetch_map(&map_a);
     if (kPair) tma_prefetch_map(&map_a64);
     tma_prefetch_map(&map_b);
-    if (kFfn) {
+    if (kTwo) {
       tma_prefetch_map(&map_a2);
       if (kPair) tma_prefetch_map(&map_a2_64);
       tma_prefetch_map(&map_b2);
@@ -533,7 +542,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
   if (kPair) cluster_sync();  // the peer's barriers exist before any multicast
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
-  const int32_t n_total = num_units<kPair, kKG, kFfn>(args);
+  const int32_t n_total = num_units<kPair, kKG, kTwo>(args);
   const int32_t u0 = kPair ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x);
   const int32_t ustride = kPair ? static_cast<int32_t>(gridDim.x >> 1) : static_cast<int32_t>(gridDim.x);
 
@@ -544,10 +553,10 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       uint32_t issued = 0;
       bool ok = true;
       for (int32_t t = u0; t < n_total && ok; t += ustride) {
-        const TileCoord tc = unit_tile<kPair, kKG, kFfn>(args, t, rank);
+        const TileCoord tc = unit_tile<kPair, kKG, kTwo>(args, t, rank);
         const int64_t gbase = static_cast<int64_t>(tc.group) * args.b_group_rows;
-        // kFfn: gate_up tiles read x and W_gate_up, down tiles read h and W_down.
-        const bool p2 = kFfn && tc.phase2;
+        // Second-GEMM tiles read the second pair of operands (kFfn: h and W_down).
+        const bool p2 = kTwo && tc.phase2;
         const CUtensorMap* pm_a = p2 ? &map_a2 : &map_a;
         const CUtensorMap* pm_a64 = p2 ? &map_a2_64 : &map_a64;
         const CUtensorMap* pm_b = p2 ? &map_b2 : &map_b;
@@ -581,7 +590,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
           sfb_unit = args.sfb + (static_cast<int64_t>(tc.group) * args.n_tiles + tc.n_tile) *
                                     args.k_blocks * kSfbStageBytes;
         }
-        if (p2) {
+        if (kFfn && p2) {
           // The h rows of this tile's m-tile must be stored by every gate_up tile:
           // acquire the count, then order the TMA reads of h after it.
           const int32_t mt = tc.a_row0 / kBM;
@@ -696,7 +705,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * G::BN;
-        const TileCoord tcm = unit_tile<kPair, kKG, kFfn>(args, t, rank);
+        const TileCoord tcm = unit_tile<kPair, kKG, kTwo>(args, t, rank);
         const uint32_t idesc = kMx ? idesc_mxf8(kBM, G::BN, kMx == 2 ? kMxE2M1 : kMxE4M3)
                                    : (tcm.row_end - tcm.a_row0 <= 64 ? kIdescHalf : kIdesc) |
                                          (a_mn_major(kMajor) ? kAMnBit : 0u) |
@@ -776,7 +785,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int32_t t = u0; t < n_total && ok; t += ustride) {
-        const TileCoord tcs = unit_tile<kPair, kKG, kFfn>(args, t, rank);
+        const TileCoord tcs = unit_tile<kPair, kKG, kTwo>(args, t, rank);
         for (int32_t kb = 0; kb < tcs.k_blocks; ++kb) {
           if (!ctl_wait(ctl, &ctl->full[stage], phase, args.status)) {
             ok = false;
@@ -818,8 +827,8 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after_sync();
-      const TileCoord tc = unit_tile<kPair, kKG, kFfn>(args, t, rank);
-      const bool p2 = kFfn && tc.phase2;
+      const TileCoord tc = unit_tile<kPair, kKG, kTwo>(args, t, rank);
+      const bool p2 = kTwo && tc.phase2;
       // M=64 tiles (bf16 only): only the first 16 lanes of each quarter hold rows
       // (16q + lane).
       const bool half = !kMx && tc.row_end - tc.a_row0 <= 64;
@@ -1263,6 +1272,7 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
   a.ldo2 = s_dn.ldo;
   a.h_ready = h_ready;
   a.h_ready_target = a.n_tiles;
+  a.dense_rows2 = a.dense_rows;
   static bool smem_set[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -1302,6 +1312,91 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
   cfg.gridDim = dim3(num_sms, 1, 1);
   return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<Epi::kFfn, kC, false, false, Major::kKMajor, 0>,
                             ma, ma64, mb, ma2, ma2_64, mb2, a);
+}
+
+// Two independent plain GEMMs of one operand layout in one persistent launch
+// (Epi::kPlain2): the units of s1, then those of s2.  No CTA waits on another.
+template <Major kMajor>
+cudaError_t launch_plain2_impl(const GemmShape& s1, const GemmShape& s2, uint32_t* status,
+                               int num_sms, cudaStream_t stream) {
+  constexpr size_t kSmem = smem_bytes<0>();
+  static_assert(kMajor != Major::kABMNGrouped, "not K-grouped");
+  if (s1.a_rows == 0 || s2.a_rows == 0) return cudaErrorInvalidValue;
+  CUtensorMap ma, ma64, mb, ma2, ma2_64, mb2;
+  auto maps = [&](const GemmShape& s, CUtensorMap* a, CUtensorMap* a64, CUtensorMap* b) {
+    bool ok;
+    if (a_mn_major(kMajor)) {
+      ok = make_map(a, s.a, s.K, s.a_rows, 64, s.a_ld);
+      *a64 = *a;
+    } else {
+      ok = make_map(a, s.a, s.a_rows, s.K, 128, s.a_ld) &&
+           make_map(a64, s.a, s.a_rows, s.K, 64, s.a_ld);
+    }
+    if (kMajor != Major::kKMajor) return ok && make_map(b, s.b, s.K, s.b_rows, 64, s.b_ld);
+    return ok && make_map(b, s.b, s.b_rows, s.K, 128, s.b_ld);
+  };
+  if (!maps(s1, &ma, &ma64, &mb) || !maps(s2, &ma2, &ma2_64, &mb2)) return cudaErrorInvalidValue;
+  Args a{};
+  a.num_groups = 1;
+  a.dense_rows = static_cast<int32_t>(s1.a_rows);
+  a.dense_rows2 = static_cast<int32_t>(s2.a_rows);
+  a.n_tiles = static_cast<int32_t>((s1.n_out + kBN - 1) / kBN);
+  a.k_blocks = static_cast<int32_t>((s1.K + kBK - 1) / kBK);
+  a.n_out = s1.n_out;
+  a.out = static_cast<__nv_bfloat16*>(s1.out);
+  a.ldo = s1.ldo;
+  a.out_rows = s1.a_rows;
+  a.status = status;
+  a.combine_k = 1;
+  a.n_tiles2 = static_cast<int32_t>((s2.n_out + kBN - 1) / kBN);
+  a.k_blocks2 = static_cast<int32_t>((s2.K + kBK - 1) / kBK);
+  a.n_out2 = s2.n_out;
+  a.out2 = static_cast<__nv_bfloat16*>(s2.out);
+  a.ldo2 = s2.ldo;
+  const int32_t m1 = static_cast<int32_t>((s1.a_rows + kBM - 1) / kBM);
+  const int32_t m2 = static_cast<int32_t>((s2.a_rows + kBM - 1) / kBM);
+  static bool smem_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaError_t e;
+  if (!smem_set[dev]) {
+    for (auto fn : {ffn_gemm_kernel<Epi::kPlain2, Caps::kBoth, false, false, kMajor, 0>,
+                    ffn_gemm_kernel<Epi::kPlain2, Caps::kBoth, true, false, kMajor, 0>}) {
+      if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(kSmem))) != cudaSuccess)
+        return e;
+    }
+    smem_set[dev] = true;
+  }
+  int clusters = max_pair_clusters<Epi::kPlain2, Caps::kBoth, false, kMajor, 0>(kSmem);
+  if (clusters > 0) {
+    a.fused_units1 = units_of(m1, a.n_tiles);
+    a.fused_units2 = units_of(m2, a.n_tiles2);
+    const int32_t units = a.fused_units1 + a.fused_units2;
+    if (units < clusters) clusters = units;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(block_threads<Epi::kPlain2, 0>(), 1, 1);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<Epi::kPlain2, Caps::kBoth, true, false, kMajor, 0>,
+                              ma, ma64, mb, ma2, ma2_64, mb2, a);
+  }
+  a.fused_units1 = m1 * a.n_tiles;
+  a.fused_units2 = m2 * a.n_tiles2;
+  int grid = num_sms;
+  if (a.fused_units1 + a.fused_units2 < grid) grid = a.fused_units1 + a.fused_units2;
+  ffn_gemm_kernel<Epi::kPlain2, Caps::kBoth, false, false, kMajor, 0>
+      <<<grid, block_threads<Epi::kPlain2, 0>(), kSmem, stream>>>(ma, ma64, mb, ma2, ma2_64, mb2,
+                                                                   a);
+  return cudaGetLastError();
 }
 
 }  // namespace

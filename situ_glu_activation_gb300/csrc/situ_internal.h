@@ -111,6 +111,10 @@ cudaError_t launch_gemm_situ(const GemmShape& s, const SituParams& p, Caps caps,
 // C = A B^T, bf16 output.
 cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
                               cudaStream_t stream);
+// Two independent plain GEMMs (same operand layouts, dense) in one persistent launch:
+// the tiles of s1, then those of s2.
+cudaError_t launch_gemm_plain2(const GemmShape& s1, const GemmShape& s2, uint32_t* status,
+                               int num_sms, cudaStream_t stream);
 // The dense bf16 FFN in one persistent cooperative launch: s_gu is the gate_up GEMM
 // (SiTU epilogue into h), s_dn the down GEMM (A = h, out = y); h_ready holds one int32
 // per 128-row m-tile of scratch.  Returns an error (and launches nothing) when the
