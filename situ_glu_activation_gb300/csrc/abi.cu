@@ -744,10 +744,10 @@ situ_status situ_moe_grouped_forward_combined(const void* x, const int32_t* expe
 size_t situ_moe_backward_workspace_size(int64_t R, int32_t E, int64_t M, int64_t I,
                                         situ_dtype dt) {
   if (R < 0 || E < 1 || M < 1 || I < 1 || dt != SITU_BF16) return 0;
-  // m-tile prefix + paired-unit prefixes of the dh and dx GEMMs, one [R, M] buffer
-  // (dy in expert order, then the per-route dx, then x in expert order) and
-  // d(g, u) [R, 2I] in expert order.
-  const size_t tiles = 3 * round_up(static_cast<size_t>(E + 1) * 4, 256);
+  // m-tile prefix + paired-unit prefixes of the dh and dx GEMMs + the experts by
+  // descending rows, one [R, M] buffer (dy in expert order, then the per-route dx,
+  // then x in expert order) and d(g, u) [R, 2I] in expert order.
+  const size_t tiles = 4 * round_up(static_cast<size_t>(E + 1) * 4, 256);
   const size_t rows_m = round_up(static_cast<size_t>(R) * M * 2, 256);
   const size_t dgu = round_up(static_cast<size_t>(R) * 2 * I * 2, 256);
   return tiles + rows_m + dgu;
@@ -803,13 +803,16 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
   int32_t* tile_offsets = reinterpret_cast<int32_t*>(ws);
   int32_t* units_dh = reinterpret_cast<int32_t*>(ws + prefix_bytes);
   int32_t* units_dx = reinterpret_cast<int32_t*>(ws + 2 * prefix_bytes);
-  void* rows_m = ws + 3 * prefix_bytes;  // [R, M]: dy, then per-route dx, then x
+  int32_t* expert_order = reinterpret_cast<int32_t*>(ws + 3 * prefix_bytes);
+  void* rows_m = ws + 4 * prefix_bytes;  // [R, M]: dy, then per-route dx, then x
   void* dgu = static_cast<uint8_t*>(rows_m) + round_up(static_cast<size_t>(R) * M * 2, 256);
   const SituParams p = make_situ_params(beta, linear_beta);
   cudaError_t e = launch_group_tiles(expert_offsets, E, R, gemm_n_tiles_wide(I),
                                      gemm_n_tiles_wide(M), tile_offsets, units_dh, units_dx,
                                      st->status, cs);
   if (e != cudaSuccess) return cuda_fail(e);
+  if ((e = launch_group_order(expert_offsets, E, expert_order, cs)) != cudaSuccess)
+    return cuda_fail(e);
   // dy in expert order: dy_perm[r] = dy[token_index[r]] (one row per route).
   e = launch_gather_rows(dy, token_index, rows_m, R, 1, M, st->status, cs);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -851,6 +854,7 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
     g.num_groups = E;
     g.tile_offsets = tile_offsets;
     g.k_group_offsets = expert_offsets;
+    g.group_order = expert_order;
     g.out_group_rows = M;
     g.n_out = I;
     g.out = dW_down;
@@ -902,6 +906,7 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
     g.num_groups = E;
     g.tile_offsets = tile_offsets;
     g.k_group_offsets = expert_offsets;
+    g.group_order = expert_order;
     g.out_group_rows = 2 * I;
     g.n_out = M;
     g.out = dW_gate_up;

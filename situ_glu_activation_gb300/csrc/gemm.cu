@@ -29,6 +29,22 @@ namespace {
 //   units_dn[g] = sum over g' < g of units(m_g', n_dn) (paired units, down GEMM)
 // Invalid offsets (not starting at 0, decreasing, not ending at R) zero all three
 // so the GEMMs do nothing, and record SITU_ERR_INDEX.  One block of 1024 threads.
+// Rank of each group by (row count descending, index ascending) -- a strict total order,
+// so order[] is a permutation of 0..G-1 for any offsets (invalid offsets are caught by
+// group_tiles_kernel, which then stops the GEMMs).
+__global__ void group_order_kernel(const int32_t* __restrict__ off, int32_t G,
+                                   int32_t* __restrict__ order) {
+  for (int32_t g = threadIdx.x; g < G; g += blockDim.x) {
+    const int32_t rows = __ldg(off + g + 1) - __ldg(off + g);
+    int32_t rank = 0;
+    for (int32_t h = 0; h < G; ++h) {
+      const int32_t rh = __ldg(off + h + 1) - __ldg(off + h);
+      rank += (rh > rows || (rh == rows && h < g)) ? 1 : 0;
+    }
+    order[rank] = g;
+  }
+}
+
 __global__ void group_tiles_kernel(const int32_t* __restrict__ off, int32_t G, int64_t R,
                                    int32_t n_gu, int32_t n_dn, int32_t* __restrict__ tiles,
                                    int32_t* __restrict__ units_gu,
@@ -215,6 +231,13 @@ cudaError_t launch_gemm_plain2(const GemmShape& s1, const GemmShape& s2, uint32_
   if (!s1.a_mn_major && !s1.b_mn_major)
     return launch_plain2_impl<Major::kKMajor>(s1, s2, status, num_sms, stream);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_group_order(const int32_t* group_offsets, int32_t G, int32_t* order,
+                               cudaStream_t stream) {
+  if (G <= 0) return cudaSuccess;
+  group_order_kernel<<<1, 1024, 0, stream>>>(group_offsets, G, order);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,

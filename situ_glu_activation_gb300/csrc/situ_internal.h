@@ -77,6 +77,9 @@ struct GemmShape {
   // tile_offsets given, a zero tile_offsets[num_groups] (offsets that failed
   // validation) makes the GEMM do nothing.
   const int32_t* k_group_offsets;
+  // K-grouped: an optional permutation of the groups (device, [num_groups]), the
+  // order their units run in (largest row count first balances the CTAs).
+  const int32_t* group_order;
   int64_t out_group_rows;
   // MXFP8 operands (launch_mx_gemm_*): A and B are E4M3 codes (row-major, K
   // contiguous, K a multiple of 128); sfa / sfb their E8M0 scale tiles (A: 512 bytes
@@ -162,6 +165,10 @@ size_t mx_weight_scale_bytes(int32_t G, int64_t rows_per_group, int64_t K, int64
 
 // Per-group prefixes of m-tiles and of the paired units of two grouped GEMMs with
 // n_tiles_1 and n_tiles_2 output tiles per m-tile, plus validation of the offsets.
+// order[rank] = group, ranking groups by descending row count (ties by index): the
+// K-grouped weight-gradient GEMMs run the largest contractions first.
+cudaError_t launch_group_order(const int32_t* group_offsets, int32_t G, int32_t* order,
+                               cudaStream_t stream);
 cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,
                                int32_t n_tiles_1, int32_t n_tiles_2, int32_t* tile_offsets,
                                int32_t* units_1, int32_t* units_2, uint32_t* status,
