@@ -83,7 +83,8 @@ const char* situ_status_string(situ_status s);
  * ("" if none).  Static storage per thread; valid until the next call. */
 const char* situ_last_cuda_error(void);
 
-/* Which path this host thread's last successful bf16 situ_ffn_forward took:
+/* Which path this host thread's last successful bf16 situ_ffn_forward or
+ * situ_ffn_forward_mxfp8 took:
  * SITU_FFN_PATH_FUSED (one persistent launch for both projections),
  * SITU_FFN_PATH_TWO_LAUNCHES (the device refused that grid as co-resident, so the
  * projections ran as two launches), or 0 before the first such call.  Both paths
@@ -93,7 +94,8 @@ const char* situ_last_cuda_error(void);
 int situ_ffn_last_path(void);
 
 /* Process-wide switch for that single launch (on by default); returns the previous
- * setting.  With it off, bf16 situ_ffn_forward always runs the two launches.  The
+ * setting.  With it off, bf16 situ_ffn_forward and situ_ffn_forward_mxfp8 always run
+ * the two launches.  The
  * single launch is a cooperative launch of thread-block clusters, which tools that
  * intercept and replay launches (kernel profilers) may not reproduce faithfully:
  * turn it off under such a tool. */
@@ -524,13 +526,15 @@ situ_status situ_ffn_gate_up_mxfp8(const void* x_codes, const void* x_scales,
 /* The dense FFN with MXFP8 experts: x [R, M] bf16 is quantized to MXFP8; the gate_up
  * GEMM (block-scaled, FP32 accumulation) applies SiTU-GLU, rounds h to bf16 (the
  * pages' cast back to the input dtype) and writes it as MXFP8 in its epilogue; the
- * down GEMM (block-scaled) writes y [R, M] bf16.
+ * down GEMM (block-scaled) writes y [R, M] bf16.  Both GEMMs run in one persistent
+ * launch as in situ_ffn_forward (two launches when that grid cannot be co-resident).
  *   wgu_*, wd_*   device, one expert's weights as situ_mx_quantize_weights wrote them,
  *                 in format weight_fmt.
  *   workspace     device, >= situ_ffn_mxfp8_workspace_size(R, M, I) bytes, 256-byte
  *                 aligned; regions (each starting 256-byte aligned, in order): x codes
- *                 [R, M], x scales, h codes [R, I], h scales -- after the call they
- *                 hold the quantized x and h.
+ *                 [R, M], x scales, h codes [R, I], h scales, one int32 per 128-row
+ *                 tile of h-ready counts -- after the call the first four hold the
+ *                 quantized x and h.
  * Errors: those of situ_ffn_gate_up_mxfp8, SITU_ERR_WORKSPACE. */
 size_t situ_ffn_mxfp8_workspace_size(int64_t R, int64_t M, int64_t I);
 situ_status situ_ffn_forward_mxfp8(const void* x, const void* wgu_codes, const void* wgu_scales,

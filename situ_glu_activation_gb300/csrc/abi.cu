@@ -1049,9 +1049,10 @@ cudaError_t run_mx_down(const DeviceState* st, const void* h_codes, const void* 
   return launch_mx_gemm_plain(d, st->status, st->num_sms, cs);
 }
 
-// Carving of the dense MXFP8 FFN workspace: x codes, x scales, h codes, h scales.
+// Carving of the dense MXFP8 FFN workspace: x codes, x scales, h codes, h scales, and
+// one int32 per 128-row m-tile (the one-launch FFN's h-ready counts).
 struct MxFfnWs {
-  size_t x_codes, x_sf, h_codes, h_sf, total;
+  size_t x_codes, x_sf, h_codes, h_sf, h_ready, total;
 };
 MxFfnWs mx_ffn_ws(int64_t R, int64_t M, int64_t I) {
   MxFfnWs w;
@@ -1059,7 +1060,8 @@ MxFfnWs mx_ffn_ws(int64_t R, int64_t M, int64_t I) {
   w.x_sf = round_up(static_cast<size_t>(R) * M, 256);
   w.h_codes = w.x_sf + round_up(mx_act_scale_bytes(R, M), 256);
   w.h_sf = w.h_codes + round_up(static_cast<size_t>(R) * I, 256);
-  w.total = w.h_sf + round_up(mx_act_scale_bytes(R, I), 256);
+  w.h_ready = w.h_sf + round_up(mx_act_scale_bytes(R, I), 256);
+  w.total = w.h_ready + round_up(static_cast<size_t>((R + 127) / 128) * 4, 256);
   return w;
 }
 
@@ -1134,6 +1136,50 @@ situ_status situ_ffn_forward_mxfp8(const void* x, const void* wgu_codes, const v
                                          cs);
   if (e != cudaSuccess) return cuda_fail(e);
   const bool fp4 = weight_fmt == SITU_MX_E2M1;
+  if (g_ffn_single_launch.load(std::memory_order_relaxed)) {
+    // Both projections in one persistent launch, as the bf16 forward.
+    GemmShape g{};
+    g.b_fp4 = fp4;
+    g.a = ws + w.x_codes;
+    g.a_rows = R;
+    g.b = wgu_codes;
+    g.b_rows = 2 * I;
+    g.K = M;
+    g.num_groups = 1;
+    g.b_group_rows = 2 * I;
+    g.b_up_offset = I;
+    g.n_out = I;
+    g.ldo = I;
+    g.out_rows = R;
+    g.sfa = ws + w.x_sf;
+    g.sfb = wgu_scales;
+    g.h_codes = ws + w.h_codes;
+    g.h_sf = ws + w.h_sf;
+    GemmShape d{};
+    d.b_fp4 = fp4;
+    d.a = ws + w.h_codes;
+    d.a_rows = R;
+    d.b = wd_codes;
+    d.b_rows = M;
+    d.K = I;
+    d.num_groups = 1;
+    d.b_group_rows = M;
+    d.n_out = M;
+    d.out = y;
+    d.ldo = M;
+    d.out_rows = R;
+    d.sfa = ws + w.h_sf;
+    d.sfb = wd_scales;
+    e = launch_mx_ffn_fused(g, d, make_situ_params(beta, linear_beta), caps_of(beta, linear_beta),
+                            reinterpret_cast<int32_t*>(ws + w.h_ready), st->status, st->num_sms,
+                            cs);
+    if (e == cudaSuccess) {
+      t_ffn_path = SITU_FFN_PATH_FUSED;
+      return SITU_OK;
+    }
+    (void)cudaGetLastError();  // a refused launch configuration: take the two launches
+  }
+  t_ffn_path = SITU_FFN_PATH_TWO_LAUNCHES;
   e = run_mx_gate_up(st, ws + w.x_codes, ws + w.x_sf, wgu_codes, wgu_scales, nullptr,
                      ws + w.h_codes, ws + w.h_sf, R, M, I, beta, linear_beta, 1, nullptr, nullptr,
                      nullptr, fp4, cs);

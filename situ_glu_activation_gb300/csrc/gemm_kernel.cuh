@@ -181,6 +181,8 @@ struct Args {
   // [rows, ldo] and h scale tiles (A layout, n_out / 128 k-blocks per m-tile).
   const uint8_t* sfa;
   const uint8_t* sfb;
+  const uint8_t* sfa2;  // kFfn with MXFP8: the down GEMM's scale tiles (h, W_down)
+  const uint8_t* sfb2;
   uint8_t* h_codes;
   uint8_t* h_sf;
   // kPlain with a fused combine: instead of storing output row r (a route, flat
@@ -507,7 +509,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
   SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + G::Stages * G::StageBytes);
   constexpr bool kSituEpi = kEpi == Epi::kSitu || kEpi == Epi::kSituMx;
   constexpr bool kFfn = kEpi == Epi::kFfn;
-  static_assert(!kFfn || (kMajor == Major::kKMajor && !kMx), "the fused FFN is bf16 K-major");
+  static_assert(!kFfn || kMajor == Major::kKMajor, "the one-launch FFN is K-major");
   // Two GEMMs in one launch: the one-launch FFN, or two independent plain GEMMs.
   constexpr bool kTwo = kFfn || kEpi == Epi::kPlain2;
   static_assert(kEpi != Epi::kPlain2 || (!kMx && kMajor != Major::kABMNGrouped),
@@ -601,9 +603,12 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
               args.tile_offsets ? __ldg(args.tile_offsets + tc.group) +
                                       (tc.a_row0 - __ldg(args.group_offsets + tc.group)) / kBM
                                 : tc.a_row0 / kBM;
-          sfa_unit = args.sfa + static_cast<int64_t>(a_tile) * args.k_blocks * kSfTileBytes;
-          sfb_unit = args.sfb + (static_cast<int64_t>(tc.group) * args.n_tiles + tc.n_tile) *
-                                    args.k_blocks * kSfbStageBytes;
+          const uint8_t* sfa = p2 ? args.sfa2 : args.sfa;
+          const uint8_t* sfb = p2 ? args.sfb2 : args.sfb;
+          const int32_t nt = p2 ? args.n_tiles2 : args.n_tiles;
+          sfa_unit = sfa + static_cast<int64_t>(a_tile) * tc.k_blocks * kSfTileBytes;
+          sfb_unit = sfb + (static_cast<int64_t>(tc.group) * nt + tc.n_tile) * tc.k_blocks *
+                               kSfbStageBytes;
         }
         if (kFfn && p2) {
           // The h rows of this tile's m-tile must be stored by every gate_up tile:
@@ -877,7 +882,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         constexpr int kHalfN = G::BN / 2;
         __nv_bfloat16* dst_row = args.out + out_row * args.ldo;
         int64_t h_tile = 0;
-        if constexpr (kEpi == Epi::kSituMx) {
+        if constexpr (kEpi == Epi::kSituMx || (kFfn && kMx != 0)) {
           h_tile = args.tile_offsets
                        ? __ldg(args.tile_offsets + tc.group) +
                              (tc.a_row0 - __ldg(args.group_offsets + tc.group)) / kBM
@@ -899,7 +904,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
                              args.sp));
           }
           const int64_t col0 = static_cast<int64_t>(tc.n_tile) * kHalfN + c * 32;
-          if constexpr (kEpi == Epi::kSituMx) {
+          if constexpr (kEpi == Epi::kSituMx || (kFfn && kMx != 0)) {
             // h rounded to bf16 (w), then one 32-wide MXFP8 block: 32 codes and the
             // block's scale in the A-operand scale tiles of the next GEMM.
             if (valid && col0 < args.n_out) {
@@ -1260,19 +1265,25 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
 // h_ready: one int32 per 128-row m-tile, zeroed here.  Every CTA must be resident at
 // once (down tiles wait for gate_up tiles of other CTAs), so the launch is cooperative:
 // a grid that cannot be co-resident fails to launch instead of waiting.
-template <Caps kC>
+template <Caps kC, int kMx = 0>
 cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
                                   const SituParams& p, int32_t* h_ready, uint32_t* status,
                                   int num_sms, cudaStream_t stream) {
-  constexpr size_t kSmem = smem_bytes<0>();
+  using G = Geo<kMx>;
+  constexpr size_t kSmem = smem_bytes<kMx>();
   if (s_gu.a_rows == 0) return cudaSuccess;
+  if (kMx && (!s_gu.sfa || !s_gu.sfb || !s_gu.h_codes || !s_gu.h_sf || !s_dn.sfa || !s_dn.sfb ||
+              s_gu.K % G::BK != 0 || s_dn.K % G::BK != 0))
+    return cudaErrorInvalidValue;
+  // bf16: 64-element boxes; MXFP8: 128-byte boxes of codes (B: packed 4-bit for MXFP4).
+  const int ea = kMx ? 1 : 0, eb = kMx == 2 ? 2 : ea;
   CUtensorMap ma, ma64, mb, ma2, ma2_64, mb2;
-  if (!make_map(&ma, s_gu.a, s_gu.a_rows, s_gu.K, 128) ||
-      !make_map(&ma64, s_gu.a, s_gu.a_rows, s_gu.K, 64) ||
-      !make_map(&mb, s_gu.b, s_gu.b_rows, s_gu.K, 128) ||
-      !make_map(&ma2, s_dn.a, s_dn.a_rows, s_dn.K, 128) ||
-      !make_map(&ma2_64, s_dn.a, s_dn.a_rows, s_dn.K, 64) ||
-      !make_map(&mb2, s_dn.b, s_dn.b_rows, s_dn.K, 128))
+  if (!make_map(&ma, s_gu.a, s_gu.a_rows, s_gu.K, 128, 0, ea) ||
+      !make_map(&ma64, s_gu.a, s_gu.a_rows, s_gu.K, 64, 0, ea) ||
+      !make_map(&mb, s_gu.b, s_gu.b_rows, s_gu.K, G::BHalfRows, 0, eb) ||
+      !make_map(&ma2, s_dn.a, s_dn.a_rows, s_dn.K, 128, 0, ea) ||
+      !make_map(&ma2_64, s_dn.a, s_dn.a_rows, s_dn.K, 64, 0, ea) ||
+      !make_map(&mb2, s_dn.b, s_dn.b_rows, s_dn.K, G::BHalfRows, 0, eb))
     return cudaErrorInvalidValue;
   const int64_t m_tiles = (s_gu.a_rows + kBM - 1) / kBM;
   cudaError_t e = cudaMemsetAsync(h_ready, 0, static_cast<size_t>(m_tiles) * 4, stream);
@@ -1280,8 +1291,8 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
   Args a{};
   a.num_groups = 1;
   a.dense_rows = static_cast<int32_t>(s_gu.a_rows);
-  a.n_tiles = static_cast<int32_t>((s_gu.n_out + 127) / 128);
-  a.k_blocks = static_cast<int32_t>((s_gu.K + kBK - 1) / kBK);
+  a.n_tiles = static_cast<int32_t>((s_gu.n_out + G::BN / 2 - 1) / (G::BN / 2));
+  a.k_blocks = static_cast<int32_t>((s_gu.K + G::BK - 1) / G::BK);
   a.b_group_rows = s_gu.b_group_rows;
   a.b_up_offset = s_gu.b_up_offset;
   a.n_out = s_gu.n_out;
@@ -1291,8 +1302,14 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
   a.sp = p;
   a.status = status;
   a.combine_k = 1;
-  a.n_tiles2 = static_cast<int32_t>((s_dn.n_out + kBN - 1) / kBN);
-  a.k_blocks2 = static_cast<int32_t>((s_dn.K + kBK - 1) / kBK);
+  a.sfa = static_cast<const uint8_t*>(s_gu.sfa);
+  a.sfb = static_cast<const uint8_t*>(s_gu.sfb);
+  a.h_codes = static_cast<uint8_t*>(s_gu.h_codes);
+  a.h_sf = static_cast<uint8_t*>(s_gu.h_sf);
+  a.sfa2 = static_cast<const uint8_t*>(s_dn.sfa);
+  a.sfb2 = static_cast<const uint8_t*>(s_dn.sfb);
+  a.n_tiles2 = static_cast<int32_t>((s_dn.n_out + G::BN - 1) / G::BN);
+  a.k_blocks2 = static_cast<int32_t>((s_dn.K + G::BK - 1) / G::BK);
   a.n_out2 = s_dn.n_out;
   a.out2 = static_cast<__nv_bfloat16*>(s_dn.out);
   a.ldo2 = s_dn.ldo;
@@ -1303,20 +1320,20 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!smem_set[dev]) {
-    for (auto fn : {ffn_gemm_kernel<Epi::kFfn, kC, false, false, Major::kKMajor, 0>,
-                    ffn_gemm_kernel<Epi::kFfn, kC, true, false, Major::kKMajor, 0>}) {
+    for (auto fn : {ffn_gemm_kernel<Epi::kFfn, kC, false, false, Major::kKMajor, kMx>,
+                    ffn_gemm_kernel<Epi::kFfn, kC, true, false, Major::kKMajor, kMx>}) {
       if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kSmem))) != cudaSuccess)
         return e;
     }
     smem_set[dev] = true;
   }
-  const int clusters = max_pair_clusters<Epi::kFfn, kC, false, Major::kKMajor, 0>(kSmem);
+  const int clusters = max_pair_clusters<Epi::kFfn, kC, false, Major::kKMajor, kMx>(kSmem);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeCooperative;
   attrs[0].val.cooperative = 1;
-  cfg.blockDim = dim3(block_threads<Epi::kFfn, 0>(), 1, 1);
+  cfg.blockDim = dim3(block_threads<Epi::kFfn, kMx>(), 1, 1);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
   cfg.attrs = attrs;
@@ -1329,14 +1346,15 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
     attrs[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
     cfg.gridDim = dim3(2 * clusters, 1, 1);
-    return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<Epi::kFfn, kC, true, false, Major::kKMajor, 0>,
+    return cudaLaunchKernelEx(&cfg,
+                              ffn_gemm_kernel<Epi::kFfn, kC, true, false, Major::kKMajor, kMx>,
                               ma, ma64, mb, ma2, ma2_64, mb2, a);
   }
   a.fused_units1 = static_cast<int32_t>(m_tiles) * a.n_tiles;
   a.fused_units2 = static_cast<int32_t>(m_tiles) * a.n_tiles2;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(num_sms, 1, 1);
-  return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<Epi::kFfn, kC, false, false, Major::kKMajor, 0>,
+  return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<Epi::kFfn, kC, false, false, Major::kKMajor, kMx>,
                             ma, ma64, mb, ma2, ma2_64, mb2, a);
 }
 

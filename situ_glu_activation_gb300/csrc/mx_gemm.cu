@@ -265,6 +265,34 @@ cudaError_t launch_mx_gemm_situ(const GemmShape& s, const SituParams& p, Caps ca
                  : mx_situ<1>(s, p, caps, status, num_sms, stream);
 }
 
+template <int kMx>
+cudaError_t mx_ffn_fused(const GemmShape& s_gu, const GemmShape& s_dn, const SituParams& p,
+                         Caps caps, int32_t* h_ready, uint32_t* status, int num_sms,
+                         cudaStream_t stream) {
+  switch (caps) {
+    case Caps::kBoth:
+      return launch_ffn_fused_impl<Caps::kBoth, kMx>(s_gu, s_dn, p, h_ready, status, num_sms,
+                                                     stream);
+    case Caps::kGateOnly:
+      return launch_ffn_fused_impl<Caps::kGateOnly, kMx>(s_gu, s_dn, p, h_ready, status, num_sms,
+                                                         stream);
+    case Caps::kUpOnly:
+      return launch_ffn_fused_impl<Caps::kUpOnly, kMx>(s_gu, s_dn, p, h_ready, status, num_sms,
+                                                       stream);
+    case Caps::kNone:
+      return launch_ffn_fused_impl<Caps::kNone, kMx>(s_gu, s_dn, p, h_ready, status, num_sms,
+                                                     stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_mx_ffn_fused(const GemmShape& s_gu, const GemmShape& s_dn, const SituParams& p,
+                                Caps caps, int32_t* h_ready, uint32_t* status, int num_sms,
+                                cudaStream_t stream) {
+  return s_gu.b_fp4 ? mx_ffn_fused<2>(s_gu, s_dn, p, caps, h_ready, status, num_sms, stream)
+                    : mx_ffn_fused<1>(s_gu, s_dn, p, caps, h_ready, status, num_sms, stream);
+}
+
 cudaError_t launch_mx_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
                                  cudaStream_t stream) {
   if (s.b_fp4)

@@ -142,6 +142,13 @@ cudaError_t launch_mx_gemm_situ(const GemmShape& s, const SituParams& p, Caps ca
 // C = A B^T (MXFP8), bf16 output.
 cudaError_t launch_mx_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
                                  cudaStream_t stream);
+// The dense MXFP8 FFN in one persistent cooperative launch: s_gu the gate_up GEMM (h as
+// MXFP8 into h_codes / h_sf), s_dn the down GEMM (A = h codes, sfa = h scales); h_ready
+// holds one int32 per 128-row m-tile.  Launches nothing and returns an error when the
+// grid cannot be co-resident.
+cudaError_t launch_mx_ffn_fused(const GemmShape& s_gu, const GemmShape& s_dn, const SituParams& p,
+                                Caps caps, int32_t* h_ready, uint32_t* status, int num_sms,
+                                cudaStream_t stream);
 // MXFP8 quantization of bf16 rows [R, K] (K % 128 == 0) into codes [R, K] and A-layout
 // scale tiles.  Row r is read from src row (row_index ? row_index[r] / k_eff : r);
 // with group offsets (and their m-tile prefix) the tiles follow the groups' m-tiles.

@@ -22,6 +22,7 @@ from situ_glu_activation_gb300 import workloads as wl
 from numerics import assert_ffn_close, oracle_input, to_f64
 
 pytestmark = pytest.mark.gpu
+INF = float("inf")
 
 
 # ----- scale-tile layouts (as include/situ.h documents them), read on the host -----
@@ -229,6 +230,33 @@ def test_ffn_forward_mxfp8(oracle, cuda_dev, R, M, I, fmt):
     err = np.abs(to_f64(y) - y_ref)
     tol = 2e-2 * (1 + np.abs(y_ref)) + diff @ np.abs(wdd).T
     assert (err <= tol).all(), f"MX FFN end to end: worst err/tol {float((err / tol).max()):.3g}"
+
+
+@pytest.mark.parametrize("fmt", FMTS, ids=FMT_IDS)
+@pytest.mark.parametrize("R,M,I,caps", [(300, 256, 384, (4.0, 25.0)), (129, 128, 256, (INF, INF)),
+                                        (513, 512, 1152, (4.0, INF)),
+                                        (4096, 2048, 3072, (4.0, 25.0))])
+def test_ffn_mxfp8_single_launch_matches_two_launches(cuda_dev, R, M, I, caps, fmt):
+    """The one-launch MX FFN (down tiles wait on per-row-tile h-ready counts) gives the
+    bits of the gate_up launch followed by the down launch; repeated calls reset the
+    counts."""
+    x, wgu, wd = _mx_inputs(R, M, I, seed=R + I)
+    xd_ = x.to(cuda_dev)
+    wguq = situ.mx_quantize_weights(wgu.to(cuda_dev), situ.MX_GATE_UP, fmt)
+    wdq = situ.mx_quantize_weights(wd.to(cuda_dev), situ.MX_DOWN, fmt)
+    ws = torch.empty(situ.ffn_mxfp8_workspace_bytes(R, M, I), dtype=torch.uint8, device=cuda_dev)
+    assert situ.ffn_set_single_launch(False) is True
+    try:
+        y2 = situ.situ_ffn_forward_mxfp8(xd_, wguq, wdq, *caps, workspace=ws)
+        assert situ.ffn_last_path() == situ.FFN_PATH_TWO_LAUNCHES
+    finally:
+        situ.ffn_set_single_launch(True)
+    for _ in range(3):
+        y = situ.situ_ffn_forward_mxfp8(xd_, wguq, wdq, *caps, workspace=ws)
+        assert situ.ffn_last_path() == situ.FFN_PATH_FUSED
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    assert situ.device_status() == 0
 
 
 def test_ffn_mxfp8_variants(oracle, cuda_dev):
