@@ -104,11 +104,32 @@ def test_grouped_equals_dense_per_expert(cuda_dev):
         assert torch.equal(y[t_idx, s_idx].view(torch.int16), ye[t_idx].view(torch.int16))
 
 
+_WEIGHTS = {}
+
+
+def _expert_weights(E, M, I, seed, dev):
+    """Seeded expert weights, generated once per shape for this module (the
+    898-expert set is 34 GB; the decode and prefill checks share it)."""
+    key = (E, M, I, seed)
+    if key not in _WEIGHTS:
+        _WEIGHTS.clear()
+        torch.cuda.empty_cache()
+        _WEIGHTS[key] = wl.expert_weights(E, M, I, seed=seed, device=dev)
+    return _WEIGHTS[key]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _free_weights():
+    yield
+    _WEIGHTS.clear()
+    torch.cuda.empty_cache()
+
+
 def _sample_check(oracle, w, dev, n_sample, seed=0):
     ids = wl.routes(w, seed=seed)
     E = w.num_experts
     x = wl.normal((w.T, w.M), 1.0, seed=seed, device=dev)
-    wgu, wd = wl.expert_weights(E, w.M, w.I, seed=seed, device=dev)
+    wgu, wd = _expert_weights(E, w.M, w.I, seed, dev)
     off, tix = situ.situ_moe_build_index(ids.to(dev), E)
     y = situ.situ_moe_grouped_forward(x, off, tix, wgu, wd, w.k_eff)
     torch.cuda.synchronize()
@@ -134,6 +155,13 @@ def test_grouped_zipf_full_size_sampled(oracle, cuda_dev):
 
 def test_k3_decode_full_size_sampled(oracle, cuda_dev):
     _sample_check(oracle, wl.WORKLOADS["k3_decode"], cuda_dev, 40)
+
+
+def test_k3_prefill_full_size_sampled(oracle, cuda_dev):
+    """The 32768-token K3-shaped layer (898 experts, 327680 routes) as the benchmark
+    launches it; the oracle checks 40 routes (first and last rows of several experts,
+    the shared experts' included, and random routes)."""
+    _sample_check(oracle, wl.WORKLOADS["k3_prefill"], cuda_dev, 40)
 
 
 def test_bad_offsets_write_nothing(cuda_dev):
