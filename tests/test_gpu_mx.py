@@ -351,13 +351,15 @@ def test_mxfp8_bad_shapes(cuda_dev):
         situ.mx_quantize_act(x)
 
 
+@pytest.mark.parametrize("name", ["k3_decode", "k3_prefill", "grouped"])
 @pytest.mark.parametrize("fmt", FMTS, ids=FMT_IDS)
-def test_k3_decode_mx_full_size_sampled(oracle, cuda_dev, fmt):
-    """The Kimi-K3-shaped layer (896 routed + 2 shared experts, 512 tokens, M=2048,
-    I=3072) through the grouped MX path at full size; 16 sampled routes (first and
-    last rows of expert groups, random rows) against the oracle's MX FFN of their
-    expert on their token."""
-    w = wl.WORKLOADS["k3_decode"]
+def test_moe_mx_full_size_sampled(oracle, cuda_dev, fmt, name):
+    """The routed-expert workloads the benchmark times through the grouped MX path at
+    full size -- the Kimi-K3-shaped layer (896 routed + 2 shared experts, M=2048,
+    I=3072) at 512 and 32768 tokens, and the 64-expert Zipf workload; 16 sampled routes
+    (first and last rows of expert groups, random rows) against the oracle's MX FFN of
+    their expert on their token."""
+    w = wl.WORKLOADS[name]
     E = w.num_experts
     ids = wl.routes(w, seed=0)
     x = wl.normal((w.T, w.M), 1.0, seed=0, device=cuda_dev)
