@@ -138,22 +138,22 @@ cudaError_t launch_gemm_situ(const GemmShape& s, const SituParams& p, Caps caps,
   if (s.gu_store) {
     switch (caps) {
       case Caps::kBoth:
-        return launch<Epi::kSitu, Caps::kBoth, true>(s, p, status, num_sms, stream);
+        return launch<Epi::kSitu, Caps::kBoth, true, Major::kKMajor, 0, true>(s, p, status, num_sms, stream);
       case Caps::kGateOnly:
-        return launch<Epi::kSitu, Caps::kGateOnly, true>(s, p, status, num_sms, stream);
+        return launch<Epi::kSitu, Caps::kGateOnly, true, Major::kKMajor, 0, true>(s, p, status, num_sms, stream);
       case Caps::kUpOnly:
-        return launch<Epi::kSitu, Caps::kUpOnly, true>(s, p, status, num_sms, stream);
+        return launch<Epi::kSitu, Caps::kUpOnly, true, Major::kKMajor, 0, true>(s, p, status, num_sms, stream);
       case Caps::kNone:
-        return launch<Epi::kSitu, Caps::kNone, true>(s, p, status, num_sms, stream);
+        return launch<Epi::kSitu, Caps::kNone, true, Major::kKMajor, 0, true>(s, p, status, num_sms, stream);
     }
     return cudaErrorInvalidValue;
   }
   switch (caps) {
-    case Caps::kBoth: return launch<Epi::kSitu, Caps::kBoth>(s, p, status, num_sms, stream);
+    case Caps::kBoth: return launch<Epi::kSitu, Caps::kBoth, false, Major::kKMajor, 0, true>(s, p, status, num_sms, stream);
     case Caps::kGateOnly:
-      return launch<Epi::kSitu, Caps::kGateOnly>(s, p, status, num_sms, stream);
-    case Caps::kUpOnly: return launch<Epi::kSitu, Caps::kUpOnly>(s, p, status, num_sms, stream);
-    case Caps::kNone: return launch<Epi::kSitu, Caps::kNone>(s, p, status, num_sms, stream);
+      return launch<Epi::kSitu, Caps::kGateOnly, false, Major::kKMajor, 0, true>(s, p, status, num_sms, stream);
+    case Caps::kUpOnly: return launch<Epi::kSitu, Caps::kUpOnly, false, Major::kKMajor, 0, true>(s, p, status, num_sms, stream);
+    case Caps::kNone: return launch<Epi::kSitu, Caps::kNone, false, Major::kKMajor, 0, true>(s, p, status, num_sms, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -170,7 +170,8 @@ cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
     return launch<Epi::kPlain, Caps::kBoth, false, Major::kBMN>(s, SituParams{}, status, num_sms,
                                                                stream);
   if (s.a_mn_major) return cudaErrorInvalidValue;
-  return launch<Epi::kPlain, Caps::kBoth>(s, SituParams{}, status, num_sms, stream);
+  return launch<Epi::kPlain, Caps::kBoth, false, Major::kKMajor, 0, true>(s, SituParams{}, status,
+                                                                        num_sms, stream);
 }
 
 cudaError_t launch_gemm_situ_bwd(const GemmShape& s, const SituParams& p, Caps caps,

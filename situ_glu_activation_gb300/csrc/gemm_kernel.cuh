@@ -34,6 +34,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "situ_internal.h"
 #include "situ_math.cuh"
@@ -101,7 +102,16 @@ template <>
 struct Geo<2> : Geo<1> {
   static constexpr uint32_t TxBytes = ABytes + BBytes / 2 + SfBytes;  // B arrives packed
 };
-constexpr int kMaxStages = 5;
+// Two-CTA MMA (dense bf16): each CTA of the pair stages its own A tile and its half of
+// B (32 KB), so six stages fit where four shared-B stages did; the even CTA's barrier
+// counts both CTAs' bytes.
+struct GeoPair {
+  static constexpr int BN = 256, BK = 64, UK = 16, Stages = 6, BHalfRows = 128;
+  static constexpr uint32_t ABytes = 16384, BBytes = 16384, SfBytes = 0;
+  static constexpr uint32_t TxBytes = 2 * (ABytes + BBytes);  // both CTAs' copies
+  static constexpr uint32_t StageBytes = ABytes + BBytes;
+};
+constexpr int kMaxStages = 6;
 // MXFP8 scale tiles.  The block-scaled MMA reads the E8M0 scale of A row m for its
 // k-th 32-wide K block (k = 0..3 within a 128-K stage) from TMEM lane m, column
 // base + m / 32, byte k; that of B row n from column base + n / 32, byte k, in the
@@ -307,9 +317,10 @@ __device__ __forceinline__ TileCoord in_group_unit(int32_t n_tiles, int32_t loca
   return c;
 }
 
-template <bool kPair, bool kKG, bool kTwo = false>
+template <bool kPair, bool kKG, bool kTwo = false, bool k2Cta = false>
 __device__ __forceinline__ int32_t num_units(const Args& a) {
   if (kTwo) return a.fused_units1 + a.fused_units2;
+  if (k2Cta) return ((a.dense_rows + 2 * kBM - 1) / (2 * kBM)) * a.n_tiles;
   if (kKG) {
     if (a.tile_offsets && __ldg(a.tile_offsets + a.num_groups) == 0) return 0;
     return a.num_groups * a.units_per_group;
@@ -330,7 +341,21 @@ __device__ __forceinline__ int32_t round_unit(int32_t i, int32_t u0, int32_t str
   return i * stride + ((kSerpentine && (i & 1)) ? stride - 1 - u0 : u0);
 }
 
-template <bool kPair, bool kKG, bool kTwo = false>
+// Two-CTA unit `local` of a dense GEMM: CTA r of the pair takes m-tile 2p + r of n-tile n
+// (a last pair past the rows computes fill that is not stored).
+__device__ __forceinline__ TileCoord pair_unit(int32_t n_tiles, int32_t local, uint32_t rank,
+                                               int32_t row_end) {
+  TileCoord c;
+  const int32_t p = local / n_tiles;
+  c.n_tile = local - p * n_tiles;
+  c.a_row0 = (2 * p + static_cast<int32_t>(rank)) * kBM;
+  c.row_end = row_end;
+  c.group = 0;
+  c.share_a = 0;
+  return c;
+}
+
+template <bool kPair, bool kKG, bool kTwo = false, bool k2Cta = false>
 __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_t rank) {
   TileCoord c;
   if (kTwo) {
@@ -339,7 +364,9 @@ __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_
     const int32_t local = p2 ? u - a.fused_units1 : u;
     const int32_t nt = p2 ? a.n_tiles2 : a.n_tiles;
     const int32_t rows = p2 ? a.dense_rows2 : a.dense_rows;
-    c = kPair ? in_group_unit(nt, local, rank, 0, rows) : in_group_tile(nt, local, 0, rows);
+    c = k2Cta  ? pair_unit(nt, local, rank, rows)
+        : kPair ? in_group_unit(nt, local, rank, 0, rows)
+                : in_group_tile(nt, local, 0, rows);
     c.group = 0;
     c.k0 = 0;
     c.k_end = 0;
@@ -348,6 +375,14 @@ __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_
     return c;
   }
   c.phase2 = 0;
+  if (k2Cta) {
+    c = pair_unit(a.n_tiles, u, rank, a.dense_rows);
+    c.phase2 = 0;
+    c.k0 = 0;
+    c.k_end = 0;
+    c.k_blocks = a.k_blocks;
+    return c;
+  }
   if (kKG) {
     // Every group has the same output tiles; its K range is its row range.
     const int32_t gi = u / a.units_per_group;
@@ -491,7 +526,8 @@ __host__ __device__ __forceinline__ int64_t sf_tile_offset(int64_t m_tile, int64
          (r_in_tile / 32) * 4 + (b % 4);
 }
 
-template <Epi kEpi, Caps kC, bool kPair, bool kStoreGu, Major kMajor, int kMx = 0>
+template <Epi kEpi, Caps kC, bool kPair, bool kStoreGu, Major kMajor, int kMx = 0,
+          bool k2Cta = false>
 __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_a64,
@@ -499,7 +535,11 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
                     const __grid_constant__ CUtensorMap map_a2,
                     const __grid_constant__ CUtensorMap map_a2_64,
                     const __grid_constant__ CUtensorMap map_b2, const Args args) {
-  using G = Geo<kMx>;
+  // k2Cta: the pair's MMAs are tcgen05 cta_group::2 (M = 256 over the two CTAs).
+  using G = std::conditional_t<k2Cta, GeoPair, Geo<kMx>>;
+  static_assert(!k2Cta || (kPair && !kMx && kMajor == Major::kKMajor &&
+                           (kEpi == Epi::kSitu || kEpi == Epi::kPlain || kEpi == Epi::kFfn)),
+                "two-CTA MMA: dense bf16 K-major forward GEMMs");
   static_assert(!kMx || kMajor == Major::kKMajor, "MXFP8 operands are K-major");
   static_assert(kMx || kEpi != Epi::kSituMx, "the MXFP8 epilogue needs MXFP8 GEMMs");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -526,11 +566,13 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       mbar_init(smem_u32(&ctl->full[s]), 1);
       // Paired: a stage is free once the MMAs of both CTAs have read it (the
       // peer's multicast writes into this CTA's copy of the stage).
-      mbar_init(smem_u32(&ctl->empty[s]), kPair ? 2 : 1);
+      // Two-CTA: one commit of the even CTA frees the stage in both.
+      mbar_init(smem_u32(&ctl->empty[s]), (kPair && !k2Cta) ? 2 : 1);
     }
     for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(smem_u32(&ctl->acc_full[b]), 1);
-      mbar_init(smem_u32(&ctl->acc_empty[b]), 32 * epi_warps<kEpi>());
+      // Two-CTA: the even CTA's MMAs wait for both CTAs' epilogues.
+      mbar_init(smem_u32(&ctl->acc_empty[b]), (k2Cta ? 2 : 1) * 32 * epi_warps<kEpi>());
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     if (kMx) {
@@ -549,15 +591,20 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
-    tmem_relinquish();
+    if constexpr (k2Cta) {
+      tmem_alloc_pair(smem_u32(&ctl->tmem_base), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+      tmem_relinquish();
+    }
     tc_fence_before_sync();
   }
   __syncthreads();
   if (kPair) cluster_sync();  // the peer's barriers exist before any multicast
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
-  const int32_t n_total = num_units<kPair, kKG, kTwo>(args);
+  const int32_t n_total = num_units<kPair, kKG, kTwo, k2Cta>(args);
   const int32_t u0 = kPair ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x);
   const int32_t ustride = kPair ? static_cast<int32_t>(gridDim.x >> 1) : static_cast<int32_t>(gridDim.x);
 
@@ -570,7 +617,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       for (int32_t i = 0; i * ustride < n_total && ok; ++i) {
         const int32_t t = round_unit<kKG>(i, u0, ustride);
         if (t >= n_total) continue;
-        const TileCoord tc = unit_tile<kPair, kKG, kTwo>(args, t, rank);
+        const TileCoord tc = unit_tile<kPair, kKG, kTwo, k2Cta>(args, t, rank);
         const int64_t gbase = static_cast<int64_t>(tc.group) * args.b_group_rows;
         // Second-GEMM tiles read the second pair of operands (kFfn: h and W_down).
         const bool p2 = kTwo && tc.phase2;
@@ -610,9 +657,10 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
           sfb_unit = sfb + (static_cast<int64_t>(tc.group) * nt + tc.n_tile) * tc.k_blocks *
                                kSfbStageBytes;
         }
-        if (kFfn && p2) {
+        if (kFfn && p2 && tc.a_row0 < tc.row_end) {
           // The h rows of this tile's m-tile must be stored by every gate_up tile:
-          // acquire the count, then order the TMA reads of h after it.
+          // acquire the count, then order the TMA reads of h after it.  (A two-CTA
+          // pair's m-tile past the rows has no count and loads only fill.)
           const int32_t mt = tc.a_row0 / kBM;
           if (!wait_count(ctl, args.h_ready + mt, args.h_ready_target, args.status)) {
             ok = false;
@@ -628,6 +676,20 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
           const uint32_t full = smem_u32(&ctl->full[stage]);
           const uint32_t sa = smem_u32(smem + stage * G::StageBytes);
           const uint32_t sb = sa + G::ABytes;
+          if constexpr (k2Cta) {
+            // This CTA's A rows and its half of B; both CTAs' copies count on the even
+            // CTA's barrier, which expects them all.
+            const uint32_t full0 = map_to_rank(full, 0);
+            if (rank == 0) mbar_arrive_expect_tx(full, G::TxBytes);
+            tma_load_2d_pair(sa, pm_a, kb * G::BK, tc.a_row0, full0);
+            tma_load_2d_pair(sb, pm_b, kb * G::BK, rank == 0 ? b_row0 : b_row1, full0);
+            ++issued;
+            if (++stage == G::Stages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           mbar_arrive_expect_tx(full, G::TxBytes);
           constexpr bool kAMN = a_mn_major(kMajor);
           constexpr bool kBMN = kMajor != Major::kKMajor;
@@ -691,8 +753,10 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
           }
         }
       }
-      if (!ok) {
-        // Drain: wait (bounded) for the copies of the last stages issued.
+      if (!ok && !(k2Cta && rank != 0)) {
+        // Drain: wait (bounded) for the copies of the last stages issued.  (Two-CTA: the
+        // odd CTA's copies count on the even CTA's barriers, drained there, and the odd
+        // CTA leaves only after the even one at the final cluster barrier.)
         const uint32_t n = issued < G::Stages ? issued : G::Stages;
         for (uint32_t i = 0; i < n; ++i) {
           stage = (stage + G::Stages - 1) % G::Stages;
@@ -706,7 +770,8 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
     // Lane 0 waits and issues.  K-grouped contractions run the whole warp: the
     // last k-block of a group holds the next group's first rows (or fill) past
     // k_end, and the warp zeroes those K rows of both operands before the MMAs.
-    if (kKG || lane == 0) {
+    // Two-CTA: the even CTA's thread issues the pair's MMAs; the odd CTA's MMA warp idles.
+    if ((kKG || lane == 0) && (!k2Cta || rank == 0)) {
       uint32_t stage = 0, phase = 0;
       uint32_t local = 0;
       bool ok = true;
@@ -727,9 +792,10 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * G::BN;
-        const TileCoord tcm = unit_tile<kPair, kKG, kTwo>(args, t, rank);
-        const uint32_t idesc = kMx ? idesc_mxf8(kBM, G::BN, kMx == 2 ? kMxE2M1 : kMxE4M3)
-                                   : (tcm.row_end - tcm.a_row0 <= 64 ? kIdescHalf : kIdesc) |
+        const TileCoord tcm = unit_tile<kPair, kKG, kTwo, k2Cta>(args, t, rank);
+        const uint32_t idesc = kMx      ? idesc_mxf8(kBM, G::BN, kMx == 2 ? kMxE2M1 : kMxE4M3)
+                               : k2Cta ? idesc_bf16_f32(2 * kBM, G::BN)
+                                       : (tcm.row_end - tcm.a_row0 <= 64 ? kIdescHalf : kIdesc) |
                                          (a_mn_major(kMajor) ? kAMnBit : 0u) |
                                          (kMajor != Major::kKMajor ? kBMnBit : 0u);
         for (int32_t kb = 0; kb < tcm.k_blocks; ++kb) {
@@ -774,9 +840,12 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
               const uint64_t bd = kMajor != Major::kKMajor
                                       ? sw128_mnmajor_desc(sb + k * 2048, kMnAtomBytes)
                                       : sw128_kmajor_desc(sb + k * kUK * 2);
-              umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              if constexpr (k2Cta) umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              else umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
             }
-            if (kPair) {
+            if constexpr (k2Cta) {
+              umma_commit_pair(smem_u32(&ctl->empty[stage]), 0x3);
+            } else if (kPair) {
               umma_commit_multicast(smem_u32(&ctl->empty[stage]), 0x3);
             } else {
               umma_commit(smem_u32(&ctl->empty[stage]));
@@ -790,12 +859,16 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         if (!ok) break;
         // A group without rows issues no MMA: the commit arrives at once and the
         // epilogue writes zeros.
-        if (lane == 0) umma_commit(smem_u32(&ctl->acc_full[acc]));
+        if (lane == 0) {
+          if constexpr (k2Cta) umma_commit_pair(smem_u32(&ctl->acc_full[acc]), 0x3);
+          else umma_commit(smem_u32(&ctl->acc_full[acc]));
+        }
         ++local;
       }
       if (!ok && lane == 0) {
         // Drain the MMAs already issued before the tensor memory is freed.
-        umma_commit(smem_u32(&ctl->drain));
+        if constexpr (k2Cta) umma_commit_pair(smem_u32(&ctl->drain), 0x1);
+        else umma_commit(smem_u32(&ctl->drain));
         mbar_wait(smem_u32(&ctl->drain), 0, nullptr, kDrainLimitNs);
       }
     }
@@ -810,7 +883,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       for (int32_t i = 0; i * ustride < n_total && ok; ++i) {
         const int32_t t = round_unit<kKG>(i, u0, ustride);
         if (t >= n_total) continue;
-        const TileCoord tcs = unit_tile<kPair, kKG, kTwo>(args, t, rank);
+        const TileCoord tcs = unit_tile<kPair, kKG, kTwo, k2Cta>(args, t, rank);
         for (int32_t kb = 0; kb < tcs.k_blocks; ++kb) {
           if (!ctl_wait(ctl, &ctl->full[stage], phase, args.status)) {
             ok = false;
@@ -857,11 +930,11 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after_sync();
-      const TileCoord tc = unit_tile<kPair, kKG, kTwo>(args, t, rank);
+      const TileCoord tc = unit_tile<kPair, kKG, kTwo, k2Cta>(args, t, rank);
       const bool p2 = kTwo && tc.phase2;
       // M=64 tiles (bf16 only): only the first 16 lanes of each quarter hold rows
       // (16q + lane).
-      const bool half = !kMx && tc.row_end - tc.a_row0 <= 64;
+      const bool half = !kMx && !k2Cta && tc.row_end - tc.a_row0 <= 64;
       const int32_t row = tc.a_row0 + (half ? quarter * 16 + lane : row_in_tile);
       bool valid = row < tc.row_end && (!half || lane < 16);
       int64_t out_row = row;
@@ -939,7 +1012,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
           // count).
           __threadfence();
           named_barrier_sync(1, kEpiThreads);
-          if (threadIdx.x == 64 && tc.n_tile < args.n_tiles)
+          if (threadIdx.x == 64 && tc.n_tile < args.n_tiles && tc.a_row0 < tc.row_end)
             red_release_add_gpu(args.h_ready + tc.a_row0 / kBM, 1);
         }
       } else if (kEpi == Epi::kSituBwd) {
@@ -1044,7 +1117,12 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         }
       }
       tc_fence_before_sync();
-      mbar_arrive(smem_u32(&ctl->acc_empty[acc]));
+      // Two-CTA: the accumulator is free once both CTAs' epilogues have read it; they
+      // arrive on the even CTA's barrier, where its MMA thread waits.
+      if (k2Cta && rank != 0)
+        mbar_arrive_remote(map_to_rank(smem_u32(&ctl->acc_empty[acc]), 0));
+      else
+        mbar_arrive(smem_u32(&ctl->acc_empty[acc]));
     }
   }
 
@@ -1054,7 +1132,8 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (k2Cta) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -1105,13 +1184,17 @@ template <int kMx>
 constexpr size_t smem_bytes() {
   return Geo<kMx>::Stages * Geo<kMx>::StageBytes + sizeof(SharedCtl) + 1024;
 }
+// Shared memory of the two-CTA kernels (the pair geometry).
+constexpr size_t smem_bytes_pair() {
+  return GeoPair::Stages * GeoPair::StageBytes + sizeof(SharedCtl) + 1024;
+}
 static_assert(smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448 &&
-                  smem_bytes<0>() <= 232448,
+                  smem_bytes<0>() <= 232448 && smem_bytes_pair() <= 232448,
               "shared memory per CTA");
 
 // Most 2-CTA clusters of ffn_gemm_kernel<kEpi, kC, true, ...> resident at once,
 // per device (0 if the query fails: the unpaired kernel is used then).
-template <Epi kEpi, Caps kC, bool kStoreGu, Major kMajor, int kMx>
+template <Epi kEpi, Caps kC, bool kStoreGu, Major kMajor, int kMx, bool k2Cta = false>
 int max_pair_clusters(size_t smem) {
   static int cached[64] = {};
   static bool done[64] = {};
@@ -1131,8 +1214,9 @@ int max_pair_clusters(size_t smem) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx>,
-                                       &cfg) == cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(
+            &n, ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx, k2Cta>, &cfg) ==
+        cudaSuccess)
       cached[dev] = n;
     else
       (void)cudaGetLastError();
@@ -1140,8 +1224,9 @@ int max_pair_clusters(size_t smem) {
   return cached[dev];
 }
 
+// k2Cta: a dense (ungrouped) call runs the two-CTA MMA kernel when 2-CTA clusters fit.
 template <Epi kEpi, Caps kC, bool kStoreGu = false, Major kMajor = Major::kKMajor,
-          int kMx = 0>
+          int kMx = 0, bool k2Cta = false>
 cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, int num_sms,
                    cudaStream_t stream) {
   using G = Geo<kMx>;
@@ -1217,7 +1302,38 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
                                            static_cast<int>(kSmem));
       if (e != cudaSuccess) return e;
     }
+    if constexpr (k2Cta) {
+      cudaError_t e = cudaFuncSetAttribute(
+          ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx, true>,
+          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes_pair()));
+      if (e != cudaSuccess) return e;
+    }
     smem_set[dev] = true;
+  }
+  if constexpr (k2Cta) {
+    const bool dense = !s.group_offsets && !s.tile_offsets && !s.k_group_offsets &&
+                       !s.out_row_index && !s.combine_w;
+    int clusters2 =
+        dense ? max_pair_clusters<kEpi, kC, kStoreGu, kMajor, kMx, true>(smem_bytes_pair()) : 0;
+    if (clusters2 > 0) {
+      // Two-CTA MMA: unit (p, n) gives CTA r m-tile 2p + r of n-tile n.
+      const int64_t units = ((m_tiles + 1) / 2) * a.n_tiles;
+      if (units < clusters2) clusters2 = static_cast<int>(units);
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * clusters2, 1, 1);
+      cfg.blockDim = dim3(block_threads<kEpi, kMx>(), 1, 1);
+      cfg.dynamicSmemBytes = smem_bytes_pair();
+      cfg.stream = stream;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = 2;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx, true>,
+                                ma, ma64, mb, ma, ma64, mb, a);
+    }
   }
   int clusters = max_pair_clusters<kEpi, kC, kStoreGu, kMajor, kMx>(kSmem);
   const int64_t pair_units = (m_tiles / 2) * a.n_tiles + (m_tiles % 2) * ((a.n_tiles + 1) / 2);
@@ -1270,7 +1386,9 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
                                   const SituParams& p, int32_t* h_ready, uint32_t* status,
                                   int num_sms, cudaStream_t stream) {
   using G = Geo<kMx>;
-  constexpr size_t kSmem = smem_bytes<kMx>();
+  // bf16: the paired kernel is the two-CTA MMA one.
+  constexpr bool k2 = kMx == 0;
+  constexpr size_t kSmem = k2 ? smem_bytes_pair() : smem_bytes<kMx>();
   if (s_gu.a_rows == 0) return cudaSuccess;
   if (kMx && (!s_gu.sfa || !s_gu.sfb || !s_gu.h_codes || !s_gu.h_sf || !s_dn.sfa || !s_dn.sfb ||
               s_gu.K % G::BK != 0 || s_dn.K % G::BK != 0))
@@ -1321,14 +1439,14 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!smem_set[dev]) {
     for (auto fn : {ffn_gemm_kernel<Epi::kFfn, kC, false, false, Major::kKMajor, kMx>,
-                    ffn_gemm_kernel<Epi::kFfn, kC, true, false, Major::kKMajor, kMx>}) {
+                    ffn_gemm_kernel<Epi::kFfn, kC, true, false, Major::kKMajor, kMx, k2>}) {
       if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kSmem))) != cudaSuccess)
         return e;
     }
     smem_set[dev] = true;
   }
-  const int clusters = max_pair_clusters<Epi::kFfn, kC, false, Major::kKMajor, kMx>(kSmem);
+  const int clusters = max_pair_clusters<Epi::kFfn, kC, false, Major::kKMajor, kMx, k2>(kSmem);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeCooperative;
@@ -1338,8 +1456,9 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
   cfg.stream = stream;
   cfg.attrs = attrs;
   if (clusters > 0) {
-    a.fused_units1 = units_of(static_cast<int32_t>(m_tiles), a.n_tiles);
-    a.fused_units2 = units_of(static_cast<int32_t>(m_tiles), a.n_tiles2);
+    const int32_t mt = static_cast<int32_t>(m_tiles);
+    a.fused_units1 = k2 ? ((mt + 1) / 2) * a.n_tiles : units_of(mt, a.n_tiles);
+    a.fused_units2 = k2 ? ((mt + 1) / 2) * a.n_tiles2 : units_of(mt, a.n_tiles2);
     attrs[1].id = cudaLaunchAttributeClusterDimension;
     attrs[1].val.clusterDim.x = 2;
     attrs[1].val.clusterDim.y = 1;
@@ -1347,7 +1466,7 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
     cfg.numAttrs = 2;
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     return cudaLaunchKernelEx(&cfg,
-                              ffn_gemm_kernel<Epi::kFfn, kC, true, false, Major::kKMajor, kMx>,
+                              ffn_gemm_kernel<Epi::kFfn, kC, true, false, Major::kKMajor, kMx, k2>,
                               ma, ma64, mb, ma2, ma2_64, mb2, a);
   }
   a.fused_units1 = static_cast<int32_t>(m_tiles) * a.n_tiles;
