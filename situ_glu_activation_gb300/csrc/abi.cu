@@ -574,9 +574,13 @@ situ_status moe_forward_impl(const void* x, const int32_t* expert_offsets,
   int32_t* units_dn = reinterpret_cast<int32_t*>(ws + 2 * prefix_bytes);
   void* x_perm = ws + 3 * prefix_bytes;
 
+  // Experts with many rows on average run as two-CTA MMAs (M = 256 over a CTA pair);
+  // with few rows (an expert's tail tile of at most 64 rows would cost a whole pair
+  // MMA) the multicast-paired kernel with its 64-row MMAs is faster.
+  const bool two_cta = R >= 512 * static_cast<int64_t>(E) && gemm_two_cta_available();
   cudaError_t e = launch_group_tiles(expert_offsets, E, R, gemm_n_tiles_situ(I),
                                      gemm_n_tiles_wide(M), tile_offsets, units_gu, units_dn,
-                                     st->status, cs);
+                                     st->status, cs, two_cta);
   if (e != cudaSuccess) return cuda_fail(e);
   e = launch_gather_rows(x, token_index, x_perm, R, k_eff, M, st->status, cs);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -591,6 +595,7 @@ situ_status moe_forward_impl(const void* x, const int32_t* expert_offsets,
   g.group_offsets = expert_offsets;
   g.tile_offsets = tile_offsets;
   g.unit_offsets = units_gu;
+  g.pair_units = two_cta;
   g.b_group_rows = 2 * I;
   g.b_up_offset = I;
   g.n_out = I;
@@ -611,6 +616,7 @@ situ_status moe_forward_impl(const void* x, const int32_t* expert_offsets,
   d.group_offsets = expert_offsets;
   d.tile_offsets = tile_offsets;
   d.unit_offsets = units_dn;
+  d.pair_units = two_cta;
   d.b_group_rows = M;
   d.n_out = M;
   d.out = y;

@@ -48,7 +48,10 @@ __global__ void group_order_kernel(const int32_t* __restrict__ off, int32_t G,
 __global__ void group_tiles_kernel(const int32_t* __restrict__ off, int32_t G, int64_t R,
                                    int32_t n_gu, int32_t n_dn, int32_t* __restrict__ tiles,
                                    int32_t* __restrict__ units_gu,
-                                   int32_t* __restrict__ units_dn, uint32_t* status) {
+                                   int32_t* __restrict__ units_dn, uint32_t* status,
+                                   int two_cta) {
+  // Units of a group with m m-tiles: two-CTA pairs, or multicast-paired units.
+  auto units = [two_cta](int32_t m, int32_t n) { return two_cta ? ((m + 1) >> 1) * n : units_of(m, n); };
   __shared__ int32_t partial[3][1024];
   __shared__ int bad;
   if (threadIdx.x == 0) bad = 0;
@@ -61,8 +64,8 @@ __global__ void group_tiles_kernel(const int32_t* __restrict__ off, int32_t G, i
     if (b < a) bad = 1;
     const int32_t m = (b - a + kBM - 1) / kBM;
     sum[0] += m;
-    sum[1] += units_of(m, n_gu);
-    sum[2] += units_of(m, n_dn);
+    sum[1] += units(m, n_gu);
+    sum[2] += units(m, n_dn);
   }
   if (threadIdx.x == 0 && (off[0] != 0 || static_cast<int64_t>(off[G]) != R)) bad = 1;
   for (int k = 0; k < 3; ++k) partial[k][threadIdx.x] = sum[k];
@@ -89,8 +92,8 @@ __global__ void group_tiles_kernel(const int32_t* __restrict__ off, int32_t G, i
     units_dn[g] = run[2];
     const int32_t m = (off[g + 1] - off[g] + kBM - 1) / kBM;
     run[0] += m;
-    run[1] += units_of(m, n_gu);
-    run[2] += units_of(m, n_dn);
+    run[1] += units(m, n_gu);
+    run[2] += units(m, n_dn);
   }
   if (threadIdx.x == blockDim.x - 1) {
     tiles[G] = partial[0][threadIdx.x];
@@ -244,10 +247,16 @@ cudaError_t launch_group_order(const int32_t* group_offsets, int32_t G, int32_t*
 cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,
                                int32_t n_tiles_1, int32_t n_tiles_2, int32_t* tile_offsets,
                                int32_t* units_1, int32_t* units_2, uint32_t* status,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, bool two_cta) {
   group_tiles_kernel<<<1, 1024, 0, stream>>>(group_offsets, G, R, n_tiles_1, n_tiles_2,
-                                             tile_offsets, units_1, units_2, status);
+                                             tile_offsets, units_1, units_2, status,
+                                             two_cta ? 1 : 0);
   return cudaGetLastError();
+}
+
+bool gemm_two_cta_available() {
+  return max_pair_clusters<Epi::kPlain, Caps::kBoth, false, Major::kKMajor, 0, true>(
+             smem_bytes_pair()) > 0;
 }
 
 int32_t gemm_n_tiles_situ(int64_t n_out) { return static_cast<int32_t>((n_out + 127) / 128); }

@@ -320,7 +320,10 @@ __device__ __forceinline__ TileCoord in_group_unit(int32_t n_tiles, int32_t loca
 template <bool kPair, bool kKG, bool kTwo = false, bool k2Cta = false>
 __device__ __forceinline__ int32_t num_units(const Args& a) {
   if (kTwo) return a.fused_units1 + a.fused_units2;
-  if (k2Cta) return ((a.dense_rows + 2 * kBM - 1) / (2 * kBM)) * a.n_tiles;
+  if (k2Cta) {
+    if (a.unit_offsets) return __ldg(a.unit_offsets + a.num_groups);
+    return ((a.dense_rows + 2 * kBM - 1) / (2 * kBM)) * a.n_tiles;
+  }
   if (kKG) {
     if (a.tile_offsets && __ldg(a.tile_offsets + a.num_groups) == 0) return 0;
     return a.num_groups * a.units_per_group;
@@ -376,7 +379,22 @@ __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_
   }
   c.phase2 = 0;
   if (k2Cta) {
-    c = pair_unit(a.n_tiles, u, rank, a.dense_rows);
+    // Dense, or grouped with a per-group prefix of two-CTA units.
+    int32_t g = 0, row0 = 0, row_end = a.dense_rows, local = u;
+    if (a.unit_offsets) {
+      int32_t lo = 0, hi = a.num_groups - 1;
+      while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (__ldg(a.unit_offsets + mid) <= u) lo = mid; else hi = mid - 1;
+      }
+      g = lo;
+      row0 = __ldg(a.group_offsets + g);
+      row_end = __ldg(a.group_offsets + g + 1);
+      local = u - __ldg(a.unit_offsets + g);
+    }
+    c = pair_unit(a.n_tiles, local, rank, row_end);
+    c.a_row0 += row0;
+    c.group = g;
     c.phase2 = 0;
     c.k0 = 0;
     c.k_end = 0;
@@ -1214,9 +1232,12 @@ int max_pair_clusters(size_t smem) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(
-            &n, ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx, k2Cta>, &cfg) ==
-        cudaSuccess)
+    // The query counts the dynamic shared memory against the kernel's opt-in limit:
+    // raise it first (it may not have been launched yet).
+    auto fn = ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx, k2Cta>;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) == cudaSuccess &&
+        cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess)
       cached[dev] = n;
     else
       (void)cudaGetLastError();
@@ -1311,14 +1332,21 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     smem_set[dev] = true;
   }
   if constexpr (k2Cta) {
+    // Two-CTA MMA for a dense call, or a grouped call whose unit prefix counts two-CTA
+    // units (pair_units).
     const bool dense = !s.group_offsets && !s.tile_offsets && !s.k_group_offsets &&
                        !s.out_row_index && !s.combine_w;
+    const bool use2 = dense || (s.pair_units && s.unit_offsets && !s.k_group_offsets);
     int clusters2 =
-        dense ? max_pair_clusters<kEpi, kC, kStoreGu, kMajor, kMx, true>(smem_bytes_pair()) : 0;
+        use2 ? max_pair_clusters<kEpi, kC, kStoreGu, kMajor, kMx, true>(smem_bytes_pair()) : 0;
+    if (s.pair_units && clusters2 == 0) return cudaErrorNotSupported;
     if (clusters2 > 0) {
-      // Two-CTA MMA: unit (p, n) gives CTA r m-tile 2p + r of n-tile n.
-      const int64_t units = ((m_tiles + 1) / 2) * a.n_tiles;
-      if (units < clusters2) clusters2 = static_cast<int>(units);
+      // Unit (p, n) gives CTA r m-tile 2p + r of n-tile n (of its group).
+      a.unit_offsets = s.pair_units ? s.unit_offsets : nullptr;
+      if (dense) {
+        const int64_t units = ((m_tiles + 1) / 2) * a.n_tiles;
+        if (units < clusters2) clusters2 = static_cast<int>(units);
+      }
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * clusters2, 1, 1);
       cfg.blockDim = dim3(block_threads<kEpi, kMx>(), 1, 1);

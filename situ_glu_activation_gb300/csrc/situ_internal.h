@@ -53,6 +53,9 @@ struct GemmShape {
   const int32_t* tile_offsets;
   // Paired-unit prefix per group for this GEMM (from launch_group_tiles), or NULL.
   const int32_t* unit_offsets;
+  // unit_offsets count two-CTA units (ceil(m-tiles / 2) per output tile; the group's
+  // pairs run as cta_group::2 MMAs) instead of multicast-paired units.
+  bool pair_units;
   int64_t b_group_rows;  // B rows per group
   int64_t b_up_offset;   // SiTU epilogue: row offset of the up half inside a group
   int64_t n_out;         // valid output columns
@@ -176,10 +179,13 @@ size_t mx_weight_scale_bytes(int32_t G, int64_t rows_per_group, int64_t K, int64
 // K-grouped weight-gradient GEMMs run the largest contractions first.
 cudaError_t launch_group_order(const int32_t* group_offsets, int32_t G, int32_t* order,
                                cudaStream_t stream);
+// two_cta: the unit prefixes count two-CTA units (ceil(m/2) per output tile).
 cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,
                                int32_t n_tiles_1, int32_t n_tiles_2, int32_t* tile_offsets,
                                int32_t* units_1, int32_t* units_2, uint32_t* status,
-                               cudaStream_t stream);
+                               cudaStream_t stream, bool two_cta = false);
+// Whether the two-CTA MMA kernels can run on this device (2-CTA clusters fit).
+bool gemm_two_cta_available();
 // Output tiles per m-tile: of the SiTU GEMM (128 activation columns per tile) and
 // of the plain / backward GEMMs (256 columns per tile), for n_out output columns.
 int32_t gemm_n_tiles_situ(int64_t n_out);

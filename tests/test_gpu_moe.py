@@ -89,12 +89,22 @@ def test_grouped_swiglu_variant(oracle, cuda_dev):
     assert_ffn_close(to_f64(y), ref, "grouped swiglu")
 
 
-def test_grouped_equals_dense_per_expert(cuda_dev):
+@pytest.mark.parametrize("T,k,E,M,I,skew", [
+    (64, 2, 4, 256, 256, False),    # few rows per expert: multicast-paired kernel
+    # >= 512 rows per expert on average: two-CTA MMAs; skewed sizes give experts with
+    # odd m-tile counts, a partial last pair, one expert with no rows
+    (1024, 2, 4, 512, 384, True),
+])
+def test_grouped_equals_dense_per_expert(cuda_dev, T, k, E, M, I, skew):
     """Grouped vs naive on the GPU: each (token, slot) row equals the dense FFN of
-    that expert applied to the token (same kernels, same rounding of h)."""
-    T, k, E, M, I = 64, 2, 4, 256, 256
+    that expert applied to the token (same tiles, same rounding of h)."""
     g = torch.Generator().manual_seed(1)
-    ids = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    if skew:
+        # slot 0: expert 0 (~70 %) or 1; slot 1: expert 2; expert 3 gets no rows
+        first = torch.where(torch.rand(T, generator=g) < 0.7, 0, 1)
+        ids = torch.stack([first, torch.full_like(first, 2)], 1).to(torch.int32)
+    else:
+        ids = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
     x = wl.normal((T, M), 1.0, seed=2)
     wgu, wd = wl.expert_weights(E, M, I, seed=3)
     y = _grouped(x, ids, wgu, wd, cuda_dev).cpu()
