@@ -167,11 +167,11 @@ cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
     return launch<Epi::kPlain, Caps::kBoth, false, Major::kABMNGrouped>(s, SituParams{}, status,
                                                                        num_sms, stream);
   if (s.a_mn_major && s.b_mn_major)
-    return launch<Epi::kPlain, Caps::kBoth, false, Major::kABMN>(s, SituParams{}, status, num_sms,
-                                                                stream);
+    return launch<Epi::kPlain, Caps::kBoth, false, Major::kABMN, 0, true>(s, SituParams{}, status,
+                                                                         num_sms, stream);
   if (s.b_mn_major)
-    return launch<Epi::kPlain, Caps::kBoth, false, Major::kBMN>(s, SituParams{}, status, num_sms,
-                                                               stream);
+    return launch<Epi::kPlain, Caps::kBoth, false, Major::kBMN, 0, true>(s, SituParams{}, status,
+                                                                        num_sms, stream);
   if (s.a_mn_major) return cudaErrorInvalidValue;
   return launch<Epi::kPlain, Caps::kBoth, false, Major::kKMajor, 0, true>(s, SituParams{}, status,
                                                                         num_sms, stream);
@@ -183,25 +183,25 @@ cudaError_t launch_gemm_situ_bwd(const GemmShape& s, const SituParams& p, Caps c
   if (s.b_mn_major) {
     switch (caps) {
       case Caps::kBoth:
-        return launch<Epi::kSituBwd, Caps::kBoth, false, Major::kBMN>(s, p, status, num_sms, stream);
+        return launch<Epi::kSituBwd, Caps::kBoth, false, Major::kBMN, 0, true>(s, p, status, num_sms, stream);
       case Caps::kGateOnly:
-        return launch<Epi::kSituBwd, Caps::kGateOnly, false, Major::kBMN>(s, p, status, num_sms,
+        return launch<Epi::kSituBwd, Caps::kGateOnly, false, Major::kBMN, 0, true>(s, p, status, num_sms,
                                                                          stream);
       case Caps::kUpOnly:
-        return launch<Epi::kSituBwd, Caps::kUpOnly, false, Major::kBMN>(s, p, status, num_sms,
+        return launch<Epi::kSituBwd, Caps::kUpOnly, false, Major::kBMN, 0, true>(s, p, status, num_sms,
                                                                        stream);
       case Caps::kNone:
-        return launch<Epi::kSituBwd, Caps::kNone, false, Major::kBMN>(s, p, status, num_sms, stream);
+        return launch<Epi::kSituBwd, Caps::kNone, false, Major::kBMN, 0, true>(s, p, status, num_sms, stream);
     }
     return cudaErrorInvalidValue;
   }
   switch (caps) {
-    case Caps::kBoth: return launch<Epi::kSituBwd, Caps::kBoth>(s, p, status, num_sms, stream);
+    case Caps::kBoth: return launch<Epi::kSituBwd, Caps::kBoth, false, Major::kKMajor, 0, true>(s, p, status, num_sms, stream);
     case Caps::kGateOnly:
-      return launch<Epi::kSituBwd, Caps::kGateOnly>(s, p, status, num_sms, stream);
+      return launch<Epi::kSituBwd, Caps::kGateOnly, false, Major::kKMajor, 0, true>(s, p, status, num_sms, stream);
     case Caps::kUpOnly:
-      return launch<Epi::kSituBwd, Caps::kUpOnly>(s, p, status, num_sms, stream);
-    case Caps::kNone: return launch<Epi::kSituBwd, Caps::kNone>(s, p, status, num_sms, stream);
+      return launch<Epi::kSituBwd, Caps::kUpOnly, false, Major::kKMajor, 0, true>(s, p, status, num_sms, stream);
+    case Caps::kNone: return launch<Epi::kSituBwd, Caps::kNone, false, Major::kKMajor, 0, true>(s, p, status, num_sms, stream);
   }
   return cudaErrorInvalidValue;
 }

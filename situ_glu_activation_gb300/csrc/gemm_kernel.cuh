@@ -555,9 +555,9 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
                     const __grid_constant__ CUtensorMap map_b2, const Args args) {
   // k2Cta: the pair's MMAs are tcgen05 cta_group::2 (M = 256 over the two CTAs).
   using G = std::conditional_t<k2Cta, GeoPair, Geo<kMx>>;
-  static_assert(!k2Cta || (kPair && !kMx && kMajor == Major::kKMajor &&
-                           (kEpi == Epi::kSitu || kEpi == Epi::kPlain || kEpi == Epi::kFfn)),
-                "two-CTA MMA: dense bf16 K-major forward GEMMs");
+  static_assert(!k2Cta || (kPair && !kMx && kMajor != Major::kABMNGrouped &&
+                           kEpi != Epi::kSituMx),
+                "two-CTA MMA: bf16 GEMMs without a K-grouped contraction");
   static_assert(!kMx || kMajor == Major::kKMajor, "MXFP8 operands are K-major");
   static_assert(kMx || kEpi != Epi::kSituMx, "the MXFP8 epilogue needs MXFP8 GEMMs");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -695,12 +695,25 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
           const uint32_t sa = smem_u32(smem + stage * G::StageBytes);
           const uint32_t sb = sa + G::ABytes;
           if constexpr (k2Cta) {
-            // This CTA's A rows and its half of B; both CTAs' copies count on the even
-            // CTA's barrier, which expects them all.
+            // This CTA's A rows and its half of B (K-major: one 128-row box; MN-major:
+            // two {64, 64} atoms); both CTAs' copies count on the even CTA's barrier,
+            // which expects them all.
             const uint32_t full0 = map_to_rank(full, 0);
             if (rank == 0) mbar_arrive_expect_tx(full, G::TxBytes);
-            tma_load_2d_pair(sa, pm_a, kb * G::BK, tc.a_row0, full0);
-            tma_load_2d_pair(sb, pm_b, kb * G::BK, rank == 0 ? b_row0 : b_row1, full0);
+            const int32_t kxa = kb * G::BK + tc.k0, kxb2 = kb * G::BK + kb_off;
+            const int32_t brow = rank == 0 ? b_row0 : b_row1;
+            if constexpr (a_mn_major(kMajor)) {
+              for (int j = 0; j < 2; ++j)
+                tma_load_2d_pair(sa + j * kMnAtomBytes, pm_a, tc.a_row0 + 64 * j, kxa, full0);
+            } else {
+              tma_load_2d_pair(sa, pm_a, kxa, tc.a_row0, full0);
+            }
+            if constexpr (kMajor != Major::kKMajor) {
+              for (int j = 0; j < 2; ++j)
+                tma_load_2d_pair(sb + j * kMnAtomBytes, pm_b, brow + 64 * j, kxb2, full0);
+            } else {
+              tma_load_2d_pair(sb, pm_b, kxb2, brow, full0);
+            }
             ++issued;
             if (++stage == G::Stages) {
               stage = 0;
@@ -812,8 +825,8 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         const uint32_t d_tmem = tmem_base + acc * G::BN;
         const TileCoord tcm = unit_tile<kPair, kKG, kTwo, k2Cta>(args, t, rank);
         const uint32_t idesc = kMx      ? idesc_mxf8(kBM, G::BN, kMx == 2 ? kMxE2M1 : kMxE4M3)
-                               : k2Cta ? idesc_bf16_f32(2 * kBM, G::BN)
-                                       : (tcm.row_end - tcm.a_row0 <= 64 ? kIdescHalf : kIdesc) |
+                               : (k2Cta ? idesc_bf16_f32(2 * kBM, G::BN)
+                                        : (tcm.row_end - tcm.a_row0 <= 64 ? kIdescHalf : kIdesc)) |
                                          (a_mn_major(kMajor) ? kAMnBit : 0u) |
                                          (kMajor != Major::kKMajor ? kBMnBit : 0u);
         for (int32_t kb = 0; kb < tcm.k_blocks; ++kb) {
@@ -1511,6 +1524,7 @@ template <Major kMajor>
 cudaError_t launch_plain2_impl(const GemmShape& s1, const GemmShape& s2, uint32_t* status,
                                int num_sms, cudaStream_t stream) {
   constexpr size_t kSmem = smem_bytes<0>();
+  static_assert(smem_bytes<0>() == smem_bytes_pair(), "one opt-in size for both kernels");
   static_assert(kMajor != Major::kABMNGrouped, "not K-grouped");
   if (s1.a_rows == 0 || s2.a_rows == 0) return cudaErrorInvalidValue;
   CUtensorMap ma, ma64, mb, ma2, ma2_64, mb2;
@@ -1552,17 +1566,18 @@ cudaError_t launch_plain2_impl(const GemmShape& s1, const GemmShape& s2, uint32_
   cudaError_t e;
   if (!smem_set[dev]) {
     for (auto fn : {ffn_gemm_kernel<Epi::kPlain2, Caps::kBoth, false, false, kMajor, 0>,
-                    ffn_gemm_kernel<Epi::kPlain2, Caps::kBoth, true, false, kMajor, 0>}) {
+                    ffn_gemm_kernel<Epi::kPlain2, Caps::kBoth, true, false, kMajor, 0, true>}) {
       if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kSmem))) != cudaSuccess)
         return e;
     }
     smem_set[dev] = true;
   }
-  int clusters = max_pair_clusters<Epi::kPlain2, Caps::kBoth, false, kMajor, 0>(kSmem);
+  // Pairs of CTAs run two-CTA MMAs (unit (p, n): CTA r takes m-tile 2p + r).
+  int clusters = max_pair_clusters<Epi::kPlain2, Caps::kBoth, false, kMajor, 0, true>(kSmem);
   if (clusters > 0) {
-    a.fused_units1 = units_of(m1, a.n_tiles);
-    a.fused_units2 = units_of(m2, a.n_tiles2);
+    a.fused_units1 = ((m1 + 1) / 2) * a.n_tiles;
+    a.fused_units2 = ((m2 + 1) / 2) * a.n_tiles2;
     const int32_t units = a.fused_units1 + a.fused_units2;
     if (units < clusters) clusters = units;
     cudaLaunchConfig_t cfg = {};
@@ -1577,7 +1592,8 @@ cudaError_t launch_plain2_impl(const GemmShape& s1, const GemmShape& s2, uint32_
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<Epi::kPlain2, Caps::kBoth, true, false, kMajor, 0>,
+    return cudaLaunchKernelEx(&cfg,
+                              ffn_gemm_kernel<Epi::kPlain2, Caps::kBoth, true, false, kMajor, 0, true>,
                               ma, ma64, mb, ma2, ma2_64, mb2, a);
   }
   a.fused_units1 = m1 * a.n_tiles;
