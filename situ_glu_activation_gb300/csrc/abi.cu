@@ -813,9 +813,12 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
   void* rows_m = ws + 4 * prefix_bytes;  // [R, M]: dy, then per-route dx, then x
   void* dgu = static_cast<uint8_t*>(rows_m) + round_up(static_cast<size_t>(R) * M * 2, 256);
   const SituParams p = make_situ_params(beta, linear_beta);
+  // The dh and dx GEMMs run as two-CTA MMAs when experts average >= 512 rows (as the
+  // forward); the K-grouped weight gradients keep one CTA per tile.
+  const bool two_cta = R >= 512 * static_cast<int64_t>(E) && gemm_two_cta_available();
   cudaError_t e = launch_group_tiles(expert_offsets, E, R, gemm_n_tiles_wide(I),
                                      gemm_n_tiles_wide(M), tile_offsets, units_dh, units_dx,
-                                     st->status, cs);
+                                     st->status, cs, two_cta);
   if (e != cudaSuccess) return cuda_fail(e);
   if ((e = launch_group_order(expert_offsets, E, expert_order, cs)) != cudaSuccess)
     return cuda_fail(e);
@@ -836,6 +839,7 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
     g.group_offsets = expert_offsets;
     g.tile_offsets = tile_offsets;
     g.unit_offsets = units_dh;
+    g.pair_units = two_cta;
     g.b_group_rows = M;
     g.n_out = I;
     g.out = dgu;
@@ -883,6 +887,7 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
     g.group_offsets = expert_offsets;
     g.tile_offsets = tile_offsets;
     g.unit_offsets = units_dx;
+    g.pair_units = two_cta;
     g.b_group_rows = 2 * I;
     g.n_out = M;
     g.out = rows_m;

@@ -140,10 +140,12 @@ def test_forward_train_matches_forward(oracle, cuda_dev):
         _close(h_c[rows], rh, 0.0, f"h of expert {e}")
 
 
-def test_grouped_backward_equals_dense_single_expert(cuda_dev):
+@pytest.mark.parametrize("T", [333, 1200])
+def test_grouped_backward_equals_dense_single_expert(cuda_dev, T):
     """One expert, one slot: the grouped backward runs the same tiles in the same
-    order as the dense backward, so every output is bit-identical."""
-    T, M, I = 333, 256, 384
+    order as the dense backward, so every output is bit-identical (333 rows: the
+    multicast-paired grouped kernels; 1200: two-CTA grouped dh and dx GEMMs)."""
+    M, I = 256, 384
     ids = torch.zeros(T, 1, dtype=torch.int32)
     x = wl.normal((T, M), 1.0, seed=31)
     wgu, wd = wl.expert_weights(1, M, I, seed=32)
