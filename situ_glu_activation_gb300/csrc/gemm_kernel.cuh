@@ -3,29 +3,37 @@
 // its host-side launch.  Included by exactly those translation units; everything
 // is in an anonymous namespace, so each unit instantiates what it launches.
 //
-// One CTA per SM (persistent), 192 threads (224 for MXFP8):
-//   warp 0      TMA producer: per k-block, the A box(es) and two B halves into a ring
-//               of 128-byte-swizzled shared-memory stages (bf16: 4 stages of
-//               A 128x64 + B 256x64; MXFP8: 5 stages of A 128x128 + B 192x128 codes
-//               and the stage's scale tiles).
-//   warp 1      MMA issuer: tcgen05.mma (kind::f16 M=128 N=256 K=16, or M=64 for tiles
-//               with at most 64 rows; kind::mxf8f6f4 block-scaled M=128 N=192 K=32),
-//               accumulating in tensor memory; tcgen05.commit frees each stage and
-//               publishes each finished accumulator.  Two accumulators let the
-//               epilogue of tile i overlap the MMAs of tile i+1.
-//   warps 2..5  epilogue: tcgen05.ld (thread = tile row); SiTU-GLU on (gate column j,
-//               up column BN/2 + j) with bf16 or MXFP8 output, plain conversion, the
-//               activation's derivative (backward), or a fused weighted scatter-add.
-//   warp 6      (MXFP8) copies each stage's scale tiles into TMEM as it lands.
+// One CTA per SM (persistent); 192 threads (224 for MXFP8, 320 for the activation-
+// derivative epilogue):
+//   warp 0      TMA producer: per k-block, the A box(es) and B rows into a ring of
+//               128-byte-swizzled shared-memory stages (bf16: 4 stages of A 128x64 +
+//               B 256x64, or 6 stages of A 128x64 + half of B with two-CTA MMAs;
+//               MXFP8: 5 stages of A 128x128 + B 192x128 codes and the scale tiles).
+//   warp 1      MMA issuer: tcgen05.mma (kind::f16 M=128 N=256 K=16, M=64 for tiles with
+//               at most 64 rows, or cta_group::2 M=256 over a CTA pair; kind::mxf8f6f4
+//               block-scaled M=128 N=192 K=32), accumulating in tensor memory;
+//               tcgen05.commit frees each stage and publishes each finished accumulator.
+//               Two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+//   warps 2..   epilogue (4 warps, 8 for the derivative): tcgen05.ld (thread = tile row);
+//               SiTU-GLU on (gate column j, up column BN/2 + j) with bf16 or MXFP8 output,
+//               plain conversion, the activation's derivative (backward), or a fused
+//               weighted scatter-add.
+//   last warp   (MXFP8) copies each stage's scale tiles into TMEM as it lands.
 // Work is scheduled in units of two tiles for the two CTAs of a cluster: adjacent
 // m-tiles of one n-tile sharing the B tile, or -- for a group's odd last m-tile --
 // adjacent n-tiles sharing the A tile; each CTA fetches half of the shared tile and
-// multicasts it.  Units run in (group, m-pair, n-tile) order, so the n-tiles of one
+// multicasts it.  With two-CTA MMAs (dense GEMMs, large-expert grouped GEMMs) the pair's
+// m-tiles 2p and 2p+1 form one M=256 MMA instead: each CTA stages its own A rows and its
+// half of B, both CTAs' copies count on the even CTA's barrier, and its MMA thread
+// issues for both.  Units run in (group, m-pair, n-tile) order, so the n-tiles of one
 // m-tile run side by side and share A in L2.  Operands are K-major, or MN-major
 // ({64, 64} boxes) for the backward, which also has a K-grouped schedule (each group
-// contracts over its own row range).  Every wait is bounded (ctl_wait / mbar_wait);
-// on a timeout the CTA records SITU_ERR_TIMEOUT, drains its in-flight copies and
-// MMAs with bounded waits, frees its tensor memory and exits.
+// contracts over its own row range; groups largest first, rounds in serpentine order).
+// Two GEMMs can share one launch: the whole FFN (down tiles wait, across CTAs, for the
+// h rows of their m-tile; a cooperative launch) or two independent plain GEMMs.  Every
+// wait is bounded (ctl_wait / mbar_wait / wait_count); on a timeout the CTA records
+// SITU_ERR_TIMEOUT, drains its in-flight copies and MMAs with bounded waits, frees its
+// tensor memory and exits.
 #pragma once
 
 #include <cuda.h>
