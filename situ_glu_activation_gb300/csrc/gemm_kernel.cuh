@@ -729,7 +729,12 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
             }
             continue;
           }
-          mbar_arrive_expect_tx(full, G::TxBytes);
+          // A shared-A unit whose tile has at most 64 valid rows needs only A rows 0..63
+          // (the 64-row MMA reads no more; with MXFP8, rows 64..127 only feed output rows
+          // that are not stored): the odd CTA fetches no A half and the stage expects
+          // that many bytes less.
+          const bool a_half_only = kPair && tc.share_a && tc.row_end - tc.a_row0 <= 64;
+          mbar_arrive_expect_tx(full, a_half_only ? G::TxBytes - G::ABytes / 2 : G::TxBytes);
           constexpr bool kAMN = a_mn_major(kMajor);
           constexpr bool kBMN = kMajor != Major::kKMajor;
           const int32_t kx = kb * G::BK + tc.k0;     // A's K coordinate
@@ -773,8 +778,9 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
             load_b(sb + rank * kBHalf, rank == 0 ? b_row0 : b_row1, true);
           } else {
             // Shared A: this CTA fetches 64 of the 128 A rows for both CTAs.
-            load_a(sa + rank * (G::ABytes / 2), tc.a_row0 + static_cast<int32_t>(rank) * 64, 1,
-                   true);
+            if (!a_half_only || rank == 0)
+              load_a(sa + rank * (G::ABytes / 2), tc.a_row0 + static_cast<int32_t>(rank) * 64, 1,
+                     true);
             load_b(sb, b_row0, false);
             load_b(sb + kBHalf, b_row1, false);
           }
