@@ -8,25 +8,29 @@
 //   warp 0      TMA producer: per k-block, the A box(es) and B rows into a ring of
 //               128-byte-swizzled shared-memory stages (bf16: 4 stages of A 128x64 +
 //               B 256x64, or 6 stages of A 128x64 + half of B with two-CTA MMAs;
-//               MXFP8: 5 stages of A 128x128 + B 192x128 codes and the scale tiles).
+//               MXFP8: 5 stages of A 128x128 + B 192x128 codes and the scale tiles,
+//               or 7 stages of A 128x128 + half of B and the scale tiles with two-CTA
+//               MMAs).
 //   warp 1      MMA issuer: tcgen05.mma (kind::f16 M=128 N=256 K=16, M=64 for tiles with
 //               at most 64 rows, or cta_group::2 M=256 over a CTA pair; kind::mxf8f6f4
-//               block-scaled M=128 N=192 K=32), accumulating in tensor memory;
+//               block-scaled M=128 or M=256 N=192 K=32), accumulating in tensor memory;
 //               tcgen05.commit frees each stage and publishes each finished accumulator.
 //               Two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
 //   warps 2..   epilogue (4 warps, 8 for the derivative): tcgen05.ld (thread = tile row);
 //               SiTU-GLU on (gate column j, up column BN/2 + j) with bf16 or MXFP8 output,
 //               plain conversion, the activation's derivative (backward), or a fused
 //               weighted scatter-add.
-//   last warp   (MXFP8) copies each stage's scale tiles into TMEM as it lands.
+//   last warp   (MXFP8) copies each stage's scale tiles into TMEM as it lands (with
+//               two-CTA MMAs: the even CTA's warp copies both CTAs' tiles, the odd
+//               CTA's relays the landing of its own to the even CTA's barrier).
 // Work is scheduled in units of two tiles for the two CTAs of a cluster: adjacent
 // m-tiles of one n-tile sharing the B tile, or -- for a group's odd last m-tile --
 // adjacent n-tiles sharing the A tile; each CTA fetches half of the shared tile and
-// multicasts it.  With two-CTA MMAs (dense GEMMs, large-expert grouped GEMMs) the pair's
-// m-tiles 2p and 2p+1 form one M=256 MMA instead: each CTA stages its own A rows and its
-// half of B, both CTAs' copies count on the even CTA's barrier, and its MMA thread
-// issues for both.  Units run in (group, m-pair, n-tile) order, so the n-tiles of one
-// m-tile run side by side and share A in L2.  Operands are K-major, or MN-major
+// multicasts it.  With two-CTA MMAs (dense GEMMs, large-expert grouped GEMMs, the dense
+// MXFP8 GEMMs) the pair's m-tiles 2p and 2p+1 form one M=256 MMA instead: each CTA
+// stages its own A rows and its half of B, both CTAs' copies count on the even CTA's
+// barrier, and its MMA thread issues for both.  Units run in (group, m-pair, n-tile)
+// order, so the n-tiles of one m-tile run side by side and share A in L2.  Operands are K-major, or MN-major
 // ({64, 64} boxes) for the backward, which also has a K-grouped schedule (each group
 // contracts over its own row range; groups largest first, rounds in serpentine order).
 // Two GEMMs can share one launch: the whole FFN (down tiles wait, across CTAs, for the
@@ -119,7 +123,25 @@ struct GeoPair {
   static constexpr uint32_t TxBytes = 2 * (ABytes + BBytes);  // both CTAs' copies
   static constexpr uint32_t StageBytes = ABytes + BBytes;
 };
-constexpr int kMaxStages = 6;
+// Two-CTA MMA (MXFP8 / MXFP4 B): M = 256, N = 192; each CTA stages its own A codes, its
+// 96-row half of B and its own A and B scale tiles (the pair MMA reads both from each
+// CTA's own tensor memory), 30 KB a stage, seven stages.  The even CTA's barrier counts
+// both CTAs' codes and its own scales; the odd CTA's scales land on a barrier of its own
+// and are relayed (see the scale copier).
+template <int kMx>
+struct GeoPairT : GeoPair {};
+template <>
+struct GeoPairT<1> {
+  static constexpr int BN = 192, BK = 128, UK = 32, Stages = 7, BHalfRows = 96;
+  static constexpr uint32_t ABytes = 16384, BBytes = 12288, SfBytes = 512 + 1024;
+  static constexpr uint32_t TxBytes = 2 * (ABytes + BBytes) + SfBytes;
+  static constexpr uint32_t StageBytes = 30720;  // A + B + scales rounded up to 1 KB
+};
+template <>
+struct GeoPairT<2> : GeoPairT<1> {
+  static constexpr uint32_t TxBytes = 2 * (ABytes + BBytes / 2) + SfBytes;  // B arrives packed
+};
+constexpr int kMaxStages = 7;
 // MXFP8 scale tiles.  The block-scaled MMA reads the E8M0 scale of A row m for its
 // k-th 32-wide K block (k = 0..3 within a 128-K stage) from TMEM lane m, column
 // base + m / 32, byte k; that of B row n from column base + n / 32, byte k, in the
@@ -448,14 +470,19 @@ __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_
   return c;
 }
 
+// kCluster: acquire at cluster scope (a barrier the peer CTA arrives on).
+template <bool kCluster = false>
 __device__ __forceinline__ bool ctl_wait(SharedCtl* ctl, uint64_t* bar, uint32_t parity,
                                          uint32_t* status) {
   const uint32_t b = smem_u32(bar);
-  if (mbar_try_wait(b, parity)) return true;
+  auto try_wait = [&]() {
+    return kCluster ? mbar_try_wait_cluster(b, parity) : mbar_try_wait(b, parity);
+  };
+  if (try_wait()) return true;
   const uint64_t t0 = global_timer_ns();
   uint32_t polls = 0;
   while (true) {
-    if (mbar_try_wait(b, parity)) return true;
+    if (try_wait()) return true;
     if ((++polls & 63u) == 0u) {
       if (ctl->abort) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -562,10 +589,13 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
                     const __grid_constant__ CUtensorMap map_a2_64,
                     const __grid_constant__ CUtensorMap map_b2, const Args args) {
   // k2Cta: the pair's MMAs are tcgen05 cta_group::2 (M = 256 over the two CTAs).
-  using G = std::conditional_t<k2Cta, GeoPair, Geo<kMx>>;
-  static_assert(!k2Cta || (kPair && !kMx && kMajor != Major::kABMNGrouped &&
-                           kEpi != Epi::kSituMx),
-                "two-CTA MMA: bf16 GEMMs without a K-grouped contraction");
+  using G = std::conditional_t<k2Cta, GeoPairT<kMx>, Geo<kMx>>;
+  static_assert(!k2Cta || (kPair && kMajor != Major::kABMNGrouped),
+                "two-CTA MMA: GEMMs without a K-grouped contraction");
+  static_assert(G::Stages * G::StageBytes + sizeof(SharedCtl) + 1024 <= 232448,
+                "shared memory per CTA");
+  static_assert(!kMx || 2 * G::BN + kSfTmemCols * G::Stages <= kTmemCols,
+                "accumulators and scale slots fit in tensor memory");
   static_assert(!kMx || kMajor == Major::kKMajor, "MXFP8 operands are K-major");
   static_assert(kMx || kEpi != Epi::kSituMx, "the MXFP8 epilogue needs MXFP8 GEMMs");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -589,7 +619,8 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < G::Stages; ++s) {
-      mbar_init(smem_u32(&ctl->full[s]), 1);
+      // Two-CTA MXFP8: the even CTA's own arrival and the odd CTA's relayed one.
+      mbar_init(smem_u32(&ctl->full[s]), (k2Cta && kMx) ? 2 : 1);
       // Paired: a stage is free once the MMAs of both CTAs have read it (the
       // peer's multicast writes into this CTA's copy of the stage).
       // Two-CTA: one commit of the even CTA frees the stage in both.
@@ -672,10 +703,14 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         const uint8_t* sfa_unit = nullptr;
         const uint8_t* sfb_unit = nullptr;
         if constexpr (kMx) {
+          // A two-CTA pair's m-tile past the rows has no scale tile: it reads its
+          // partner's (its products are not stored).
+          const int32_t a_row_sf =
+              (k2Cta && tc.a_row0 >= tc.row_end) ? tc.a_row0 - kBM : tc.a_row0;
           const int32_t a_tile =
               args.tile_offsets ? __ldg(args.tile_offsets + tc.group) +
-                                      (tc.a_row0 - __ldg(args.group_offsets + tc.group)) / kBM
-                                : tc.a_row0 / kBM;
+                                      (a_row_sf - __ldg(args.group_offsets + tc.group)) / kBM
+                                : a_row_sf / kBM;
           const uint8_t* sfa = p2 ? args.sfa2 : args.sfa;
           const uint8_t* sfb = p2 ? args.sfb2 : args.sfb;
           const int32_t nt = p2 ? args.n_tiles2 : args.n_tiles;
@@ -721,6 +756,20 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
                 tma_load_2d_pair(sb + j * kMnAtomBytes, pm_b, brow + 64 * j, kxb2, full0);
             } else {
               tma_load_2d_pair(sb, pm_b, kxb2, brow, full0);
+            }
+            if constexpr (kMx) {
+              // This CTA's own scale tiles: the even CTA's land on its full barrier,
+              // the odd CTA's on its sf_ready barrier, from where they are relayed.
+              const uint32_t ssf = sb + G::BBytes;
+              uint32_t sf_bar = full;
+              if (rank != 0) {
+                sf_bar = smem_u32(&ctl->sf_ready[stage]);
+                mbar_arrive_expect_tx(sf_bar, G::SfBytes);
+              }
+              bulk_load(ssf, sfa_unit + static_cast<int64_t>(kb) * kSfTileBytes, kSfTileBytes,
+                        sf_bar);
+              bulk_load(ssf + kSfTileBytes, sfb_unit + static_cast<int64_t>(kb) * kSfbStageBytes,
+                        kSfbStageBytes, sf_bar);
             }
             ++issued;
             if (++stage == G::Stages) {
@@ -798,15 +847,18 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
           }
         }
       }
-      if (!ok && !(k2Cta && rank != 0)) {
-        // Drain: wait (bounded) for the copies of the last stages issued.  (Two-CTA: the
-        // odd CTA's copies count on the even CTA's barriers, drained there, and the odd
-        // CTA leaves only after the even one at the final cluster barrier.)
+      // Two-CTA: the odd CTA's operand copies count on the even CTA's barriers, drained
+      // there (the odd CTA leaves only after the even one, at the final cluster
+      // barrier); its own MXFP8 scale copies land on its sf_ready barriers.
+      const bool drain_sf = k2Cta && kMx && rank != 0;
+      if (!ok && (!(k2Cta && rank != 0) || drain_sf)) {
+        // Drain: wait (bounded) for the copies of the last stages issued.
         const uint32_t n = issued < G::Stages ? issued : G::Stages;
         for (uint32_t i = 0; i < n; ++i) {
           stage = (stage + G::Stages - 1) % G::Stages;
           if (stage == G::Stages - 1) phase ^= 1u;
-          mbar_wait(smem_u32(&ctl->full[stage]), phase, nullptr, kDrainLimitNs);
+          mbar_wait(smem_u32(drain_sf ? &ctl->sf_ready[stage] : &ctl->full[stage]), phase,
+                    nullptr, kDrainLimitNs);
         }
       }
     }
@@ -838,7 +890,8 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * G::BN;
         const TileCoord tcm = unit_tile<kPair, kKG, kTwo, k2Cta>(args, t, rank);
-        const uint32_t idesc = kMx      ? idesc_mxf8(kBM, G::BN, kMx == 2 ? kMxE2M1 : kMxE4M3)
+        const uint32_t idesc = kMx      ? idesc_mxf8(k2Cta ? 2 * kBM : kBM, G::BN,
+                                                kMx == 2 ? kMxE2M1 : kMxE4M3)
                                : (k2Cta ? idesc_bf16_f32(2 * kBM, G::BN)
                                         : (tcm.row_end - tcm.a_row0 <= 64 ? kIdescHalf : kIdesc)) |
                                          (a_mn_major(kMajor) ? kAMnBit : 0u) |
@@ -866,10 +919,18 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
             const uint32_t sf_t = tmem_base + 2 * G::BN + kSfTmemCols * stage;
 #pragma unroll
             for (int k = 0; k < G::BK / G::UK; ++k) {
-              umma_mxf8(d_tmem, sw128_kmajor_desc(sa + k * 32), sw128_kmajor_desc(sb + k * 32),
-                        idesc | idesc_mxf8_ids(k, k), sf_t, sf_t + 4, (kb | k) != 0 ? 1u : 0u);
+              if constexpr (k2Cta) {
+                umma_mxf8_pair(d_tmem, sw128_kmajor_desc(sa + k * 32),
+                               sw128_kmajor_desc(sb + k * 32), idesc | idesc_mxf8_ids(k, k), sf_t,
+                               sf_t + 4, (kb | k) != 0 ? 1u : 0u);
+              } else {
+                umma_mxf8(d_tmem, sw128_kmajor_desc(sa + k * 32), sw128_kmajor_desc(sb + k * 32),
+                          idesc | idesc_mxf8_ids(k, k), sf_t, sf_t + 4, (kb | k) != 0 ? 1u : 0u);
+              }
             }
-            if (kPair) {
+            if constexpr (k2Cta) {
+              umma_commit_pair(smem_u32(&ctl->empty[stage]), 0x3);
+            } else if (kPair) {
               umma_commit_multicast(smem_u32(&ctl->empty[stage]), 0x3);
             } else {
               umma_commit(smem_u32(&ctl->empty[stage]));
@@ -922,34 +983,53 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
     // Per stage, once its copies landed: the A and B scale tiles into the stage's
     // TMEM slot, then a commit that tells the MMA warp.  A slot is rewritten only
     // after its stage was refilled, i.e. after the MMAs that read it completed.
+    // Two-CTA: the even CTA's copies move both CTAs' scale tiles, each into its own
+    // CTA's tensor memory, once the even CTA's full barrier has seen both CTAs' codes,
+    // its own scales and the odd CTA's relay; the odd CTA's warp is that relay: once its
+    // own scale tiles of a stage have landed it arrives on the even CTA's full barrier.
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
+      const bool relay = k2Cta && rank != 0;
       for (int32_t i = 0; i * ustride < n_total && ok; ++i) {
         const int32_t t = round_unit<kKG>(i, u0, ustride);
         if (t >= n_total) continue;
         const TileCoord tcs = unit_tile<kPair, kKG, kTwo, k2Cta>(args, t, rank);
         for (int32_t kb = 0; kb < tcs.k_blocks; ++kb) {
-          if (!ctl_wait(ctl, &ctl->full[stage], phase, args.status)) {
+          const bool landed = relay ? ctl_wait(ctl, &ctl->sf_ready[stage], phase, args.status)
+                                    : ctl_wait<k2Cta>(ctl, &ctl->full[stage], phase, args.status);
+          if (!landed) {
             ok = false;
             break;
           }
-          tc_fence_after_sync();
-          const uint32_t ssf = smem_u32(smem + stage * G::StageBytes) + G::ABytes + G::BBytes;
-          const uint32_t sf_t = tmem_base + 2 * G::BN + kSfTmemCols * stage;
-          tmem_cp_32x128b_x4(sf_t, ssf);
-          tmem_cp_32x128b_x4(sf_t + 4, ssf + kSfTileBytes);
-          tmem_cp_32x128b_x4(sf_t + 8, ssf + 2 * kSfTileBytes);
-          umma_commit(smem_u32(&ctl->sf_ready[stage]));
+          if (relay) {
+            mbar_arrive_remote(map_to_rank(smem_u32(&ctl->full[stage]), 0));
+          } else {
+            tc_fence_after_sync();
+            const uint32_t ssf = smem_u32(smem + stage * G::StageBytes) + G::ABytes + G::BBytes;
+            const uint32_t sf_t = tmem_base + 2 * G::BN + kSfTmemCols * stage;
+            if constexpr (k2Cta) {
+              tmem_cp_32x128b_x4_pair(sf_t, ssf);
+              tmem_cp_32x128b_x4_pair(sf_t + 4, ssf + kSfTileBytes);
+              tmem_cp_32x128b_x4_pair(sf_t + 8, ssf + 2 * kSfTileBytes);
+              umma_commit_pair(smem_u32(&ctl->sf_ready[stage]), 0x1);
+            } else {
+              tmem_cp_32x128b_x4(sf_t, ssf);
+              tmem_cp_32x128b_x4(sf_t + 4, ssf + kSfTileBytes);
+              tmem_cp_32x128b_x4(sf_t + 8, ssf + 2 * kSfTileBytes);
+              umma_commit(smem_u32(&ctl->sf_ready[stage]));
+            }
+          }
           if (++stage == G::Stages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok) {
+      if (!ok && !relay) {
         // Drain the copies already issued before the tensor memory is freed.
-        umma_commit(smem_u32(&ctl->sf_drain));
+        if constexpr (k2Cta) umma_commit_pair(smem_u32(&ctl->sf_drain), 0x1);
+        else umma_commit(smem_u32(&ctl->sf_drain));
         mbar_wait(smem_u32(&ctl->sf_drain), 0, nullptr, kDrainLimitNs);
       }
     }
@@ -1230,11 +1310,13 @@ constexpr size_t smem_bytes() {
   return Geo<kMx>::Stages * Geo<kMx>::StageBytes + sizeof(SharedCtl) + 1024;
 }
 // Shared memory of the two-CTA kernels (the pair geometry).
+template <int kMx = 0>
 constexpr size_t smem_bytes_pair() {
-  return GeoPair::Stages * GeoPair::StageBytes + sizeof(SharedCtl) + 1024;
+  return GeoPairT<kMx>::Stages * GeoPairT<kMx>::StageBytes + sizeof(SharedCtl) + 1024;
 }
 static_assert(smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448 &&
-                  smem_bytes<0>() <= 232448 && smem_bytes_pair() <= 232448,
+                  smem_bytes<0>() <= 232448 && smem_bytes_pair<0>() <= 232448 &&
+                  smem_bytes_pair<1>() <= 232448 && smem_bytes_pair<2>() <= 232448,
               "shared memory per CTA");
 
 // Most 2-CTA clusters of ffn_gemm_kernel<kEpi, kC, true, ...> resident at once,
@@ -1353,7 +1435,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     if constexpr (k2Cta) {
       cudaError_t e = cudaFuncSetAttribute(
           ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx, true>,
-          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes_pair()));
+          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes_pair<kMx>()));
       if (e != cudaSuccess) return e;
     }
     smem_set[dev] = true;
@@ -1365,7 +1447,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
                        !s.out_row_index && !s.combine_w;
     const bool use2 = dense || (s.pair_units && s.unit_offsets && !s.k_group_offsets);
     int clusters2 =
-        use2 ? max_pair_clusters<kEpi, kC, kStoreGu, kMajor, kMx, true>(smem_bytes_pair()) : 0;
+        use2 ? max_pair_clusters<kEpi, kC, kStoreGu, kMajor, kMx, true>(smem_bytes_pair<kMx>()) : 0;
     if (s.pair_units && clusters2 == 0) return cudaErrorNotSupported;
     if (clusters2 > 0) {
       // Unit (p, n) gives CTA r m-tile 2p + r of n-tile n (of its group).
@@ -1377,7 +1459,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * clusters2, 1, 1);
       cfg.blockDim = dim3(block_threads<kEpi, kMx>(), 1, 1);
-      cfg.dynamicSmemBytes = smem_bytes_pair();
+      cfg.dynamicSmemBytes = smem_bytes_pair<kMx>();
       cfg.stream = stream;
       cudaLaunchAttribute attr;
       attr.id = cudaLaunchAttributeClusterDimension;
@@ -1441,9 +1523,14 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
                                   const SituParams& p, int32_t* h_ready, uint32_t* status,
                                   int num_sms, cudaStream_t stream) {
   using G = Geo<kMx>;
-  // bf16: the paired kernel is the two-CTA MMA one.
-  constexpr bool k2 = kMx == 0;
-  constexpr size_t kSmem = k2 ? smem_bytes_pair() : smem_bytes<kMx>();
+  // The paired kernel is the two-CTA MMA one (its N, BK and B half match Geo<kMx>).
+  constexpr bool k2 = true;
+  static_assert(GeoPairT<kMx>::BN == G::BN && GeoPairT<kMx>::BK == G::BK &&
+                    GeoPairT<kMx>::BHalfRows == G::BHalfRows,
+                "tile geometry of the two-CTA kernel");
+  // One opt-in size serves the paired kernel and the unpaired fallback.
+  constexpr size_t kSmem = smem_bytes_pair<kMx>() > smem_bytes<kMx>() ? smem_bytes_pair<kMx>()
+                                                                       : smem_bytes<kMx>();
   if (s_gu.a_rows == 0) return cudaSuccess;
   if (kMx && (!s_gu.sfa || !s_gu.sfb || !s_gu.h_codes || !s_gu.h_sf || !s_dn.sfa || !s_dn.sfb ||
               s_gu.K % G::BK != 0 || s_dn.K % G::BK != 0))
@@ -1538,7 +1625,7 @@ template <Major kMajor>
 cudaError_t launch_plain2_impl(const GemmShape& s1, const GemmShape& s2, uint32_t* status,
                                int num_sms, cudaStream_t stream) {
   constexpr size_t kSmem = smem_bytes<0>();
-  static_assert(smem_bytes<0>() == smem_bytes_pair(), "one opt-in size for both kernels");
+  static_assert(smem_bytes<0>() == smem_bytes_pair<0>(), "one opt-in size for both kernels");
   static_assert(kMajor != Major::kABMNGrouped, "not K-grouped");
   if (s1.a_rows == 0 || s2.a_rows == 0) return cudaErrorInvalidValue;
   CUtensorMap ma, ma64, mb, ma2, ma2_64, mb2;

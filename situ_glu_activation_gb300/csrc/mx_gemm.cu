@@ -234,25 +234,25 @@ cudaError_t mx_situ(const GemmShape& s, const SituParams& p, Caps caps, uint32_t
   if (s.h_codes) {
     switch (caps) {
       case Caps::kBoth:
-        return launch<Epi::kSituMx, Caps::kBoth, false, K, kMx>(s, p, status, num_sms, stream);
+        return launch<Epi::kSituMx, Caps::kBoth, false, K, kMx, true>(s, p, status, num_sms, stream);
       case Caps::kGateOnly:
-        return launch<Epi::kSituMx, Caps::kGateOnly, false, K, kMx>(s, p, status, num_sms, stream);
+        return launch<Epi::kSituMx, Caps::kGateOnly, false, K, kMx, true>(s, p, status, num_sms, stream);
       case Caps::kUpOnly:
-        return launch<Epi::kSituMx, Caps::kUpOnly, false, K, kMx>(s, p, status, num_sms, stream);
+        return launch<Epi::kSituMx, Caps::kUpOnly, false, K, kMx, true>(s, p, status, num_sms, stream);
       case Caps::kNone:
-        return launch<Epi::kSituMx, Caps::kNone, false, K, kMx>(s, p, status, num_sms, stream);
+        return launch<Epi::kSituMx, Caps::kNone, false, K, kMx, true>(s, p, status, num_sms, stream);
     }
     return cudaErrorInvalidValue;
   }
   switch (caps) {
     case Caps::kBoth:
-      return launch<Epi::kSitu, Caps::kBoth, false, K, kMx>(s, p, status, num_sms, stream);
+      return launch<Epi::kSitu, Caps::kBoth, false, K, kMx, true>(s, p, status, num_sms, stream);
     case Caps::kGateOnly:
-      return launch<Epi::kSitu, Caps::kGateOnly, false, K, kMx>(s, p, status, num_sms, stream);
+      return launch<Epi::kSitu, Caps::kGateOnly, false, K, kMx, true>(s, p, status, num_sms, stream);
     case Caps::kUpOnly:
-      return launch<Epi::kSitu, Caps::kUpOnly, false, K, kMx>(s, p, status, num_sms, stream);
+      return launch<Epi::kSitu, Caps::kUpOnly, false, K, kMx, true>(s, p, status, num_sms, stream);
     case Caps::kNone:
-      return launch<Epi::kSitu, Caps::kNone, false, K, kMx>(s, p, status, num_sms, stream);
+      return launch<Epi::kSitu, Caps::kNone, false, K, kMx, true>(s, p, status, num_sms, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -296,9 +296,9 @@ cudaError_t launch_mx_ffn_fused(const GemmShape& s_gu, const GemmShape& s_dn, co
 cudaError_t launch_mx_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
                                  cudaStream_t stream) {
   if (s.b_fp4)
-    return launch<Epi::kPlain, Caps::kBoth, false, Major::kKMajor, 2>(s, SituParams{}, status,
+    return launch<Epi::kPlain, Caps::kBoth, false, Major::kKMajor, 2, true>(s, SituParams{}, status,
                                                                     num_sms, stream);
-  return launch<Epi::kPlain, Caps::kBoth, false, Major::kKMajor, 1>(s, SituParams{}, status,
+  return launch<Epi::kPlain, Caps::kBoth, false, Major::kKMajor, 1, true>(s, SituParams{}, status,
                                                                   num_sms, stream);
 }
 

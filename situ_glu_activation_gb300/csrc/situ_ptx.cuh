@@ -56,6 +56,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Same at cluster scope: for a barrier that a peer CTA arrives on with a release at
+// cluster scope, so the waiter acquires what the peer released.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Wait until the phase with the given parity has completed.  The wait is
 // bounded: after limit_ns of wall time (the GPU's global nanosecond timer) it
 // records SITU_ERR_TIMEOUT in *status and returns false, so a lost arrival can
@@ -260,10 +274,14 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* map, 
       : "memory");
 }
 
-// Arrive (release, cluster scope) on an mbarrier in another CTA of the cluster.
+// Arrive on an mbarrier in another CTA of the cluster, with the instruction's default
+// semantics (release at CTA scope).  What the arrival orders is either tensor-memory
+// reads (closed by tcgen05.fence::before_thread_sync) or async-proxy writes this
+// thread saw complete on its own barrier.  The release at cluster scope costs far
+// more: on the relay of the two-CTA MXFP8 kernel (one arrival per stage) it halved
+// the GEMM's throughput (measured on GB300).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B (both K-major),
@@ -377,6 +395,30 @@ __device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Two-CTA forms (issued by the even CTA of a pair; every tcgen05 op of a kernel uses
+// one .cta_group).  The copy moves each CTA's own shared-memory bytes, at saddr, into
+// its own tensor memory at taddr; the pair MMA (M = 256) takes each CTA's A scales and
+// the scales of all N columns of B from that CTA's own tensor memory (measured on
+// GB300 with an in-bounds probe).
+__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint32_t saddr) {
+  const uint64_t desc = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4)
+                        | (static_cast<uint64_t>(128 >> 4) << 16)
+                        | (static_cast<uint64_t>(128 >> 4) << 32)
+                        | (static_cast<uint64_t>(1) << 46);
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
+               : "memory");
+}
+__device__ __forceinline__ void umma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t sfa_tmem,
+                                               uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
