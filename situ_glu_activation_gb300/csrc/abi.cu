@@ -1007,9 +1007,10 @@ cudaError_t run_mx_gate_up(const DeviceState* st, const void* x_codes, const voi
                            void* h_sf, int64_t R, int64_t M, int64_t I, float beta,
                            float linear_beta, int32_t E, const int32_t* offsets,
                            const int32_t* tiles, const int32_t* units, bool fp4,
-                           cudaStream_t cs) {
+                           cudaStream_t cs, bool pair_units = false) {
   GemmShape g{};
   g.b_fp4 = fp4;
+  g.pair_units = pair_units;
   g.a = x_codes;
   g.a_rows = R;
   g.b = wgu_codes;
@@ -1037,9 +1038,10 @@ cudaError_t run_mx_down(const DeviceState* st, const void* h_codes, const void* 
                         const void* wd_codes, const void* wd_scales, void* y, int64_t R,
                         int64_t M, int64_t I, int32_t E, const int32_t* offsets,
                         const int32_t* tiles, const int32_t* units, const int32_t* row_index,
-                        bool fp4, cudaStream_t cs) {
+                        bool fp4, cudaStream_t cs, bool pair_units = false) {
   GemmShape d{};
   d.b_fp4 = fp4;
+  d.pair_units = pair_units;
   d.a = h_codes;
   d.a_rows = R;
   d.b = wd_codes;
@@ -1272,10 +1274,12 @@ situ_status situ_moe_grouped_forward_mxfp8(const void* x, const int32_t* expert_
   int32_t* tiles = reinterpret_cast<int32_t*>(ws + w.tiles);
   int32_t* units_gu = reinterpret_cast<int32_t*>(ws + w.units_gu);
   int32_t* units_dn = reinterpret_cast<int32_t*>(ws + w.units_dn);
+  // Two-CTA MMAs when the experts average at least 512 rows (as for bf16).
+  const bool two_cta = R >= 512 * static_cast<int64_t>(E) && gemm_two_cta_available();
   cudaError_t e = launch_group_tiles(expert_offsets, E, R,
                                      static_cast<int32_t>((I + kMxSituCols - 1) / kMxSituCols),
                                      static_cast<int32_t>((M + kMxPlainCols - 1) / kMxPlainCols),
-                                     tiles, units_gu, units_dn, st->status, cs);
+                                     tiles, units_gu, units_dn, st->status, cs, two_cta);
   if (e != cudaSuccess) return cuda_fail(e);
   // Gather x into expert order and quantize it, scales tiled by the experts' m-tiles.
   e = launch_mx_quantize_act(x, token_index, k_eff, T, ws + w.x_codes, ws + w.x_sf,
@@ -1284,10 +1288,10 @@ situ_status situ_moe_grouped_forward_mxfp8(const void* x, const int32_t* expert_
   const bool fp4 = weight_fmt == SITU_MX_E2M1;
   e = run_mx_gate_up(st, ws + w.x_codes, ws + w.x_sf, wgu_codes, wgu_scales, nullptr,
                      ws + w.h_codes, ws + w.h_sf, R, M, I, beta, linear_beta, E, expert_offsets,
-                     tiles, units_gu, fp4, cs);
+                     tiles, units_gu, fp4, cs, two_cta);
   if (e != cudaSuccess) return cuda_fail(e);
   return finish(run_mx_down(st, ws + w.h_codes, ws + w.h_sf, wd_codes, wd_scales, y, R, M, I, E,
-                            expert_offsets, tiles, units_dn, token_index, fp4, cs));
+                            expert_offsets, tiles, units_dn, token_index, fp4, cs, two_cta));
 }
 
 situ_status situ_moe_combine(const void* y, const float* weights, void* out, int64_t T,

@@ -287,7 +287,14 @@ def _grouped_case(T, k, E, M, I, seed, dev, fmt=situ.MX_E4M3):
 
 
 @pytest.mark.parametrize("fmt", FMTS, ids=FMT_IDS)
-@pytest.mark.parametrize("T,k,E,M,I", [(50, 3, 6, 256, 384), (300, 2, 3, 128, 256)])
+@pytest.mark.parametrize("T,k,E,M,I", [
+    (50, 3, 6, 256, 384),
+    (300, 2, 3, 128, 256),
+    # 1600 routes over 3 experts (at least 512 rows per expert on average): two-CTA
+    # MMAs; experts 0 and 1 hold 800 rows (7 m-tiles, so each has a pair whose second
+    # m-tile is past its rows), expert 2 none.
+    (800, 2, 3, 128, 256),
+])
 def test_grouped_mxfp8_equals_dense_per_expert(cuda_dev, T, k, E, M, I, fmt):
     """Each (token, slot) row of the grouped MX forward equals the dense MX FFN of its
     expert on the token, bit for bit: rows are quantized and multiplied
