@@ -257,7 +257,8 @@ def bench_dense(args, dev, peaks, world, flush):
     flop_gu = 2.0 * w.rows * w.M * 2 * w.I
     flop_down = 2.0 * w.rows * w.I * w.M
     out = {
-        "ms": ms, "tokens": w.rows, "launches_per_step": 2 if args.ffn_two_launches else 1,
+        "ms": ms, "ms_median": statistics.median(per_step), "tokens": w.rows,
+        "launches_per_step": 2 if args.ffn_two_launches else 1,
         "path": "two launches" if args.ffn_two_launches else "one persistent launch",
         "two_launch_ms": mean(per_step2),
         "gate_up_ms": mean(t_gu), "down_ms": mean(t_down),
@@ -751,6 +752,7 @@ def run_situ(args):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": ms_max,
+        "ms_per_step_median": dense["ms_median"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
