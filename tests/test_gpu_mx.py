@@ -292,8 +292,9 @@ def _grouped_case(T, k, E, M, I, seed, dev, fmt=situ.MX_E4M3):
     (300, 2, 3, 128, 256),
     # 1600 routes over 3 experts (at least 512 rows per expert on average): two-CTA
     # MMAs; experts 0 and 1 hold 800 rows (7 m-tiles, so each has a pair whose second
-    # m-tile is past its rows), expert 2 none.
-    (800, 2, 3, 128, 256),
+    # m-tile is past its rows), expert 2 none; K of 2 and of 3 128-wide k-blocks.
+    (800, 2, 3, 256, 256),
+    (800, 2, 3, 384, 256),
 ])
 def test_grouped_mxfp8_equals_dense_per_expert(cuda_dev, T, k, E, M, I, fmt):
     """Each (token, slot) row of the grouped MX forward equals the dense MX FFN of its
