@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <type_traits>
 
@@ -1266,18 +1267,16 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
 // Host side
 // ---------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  // Resolved once; the static's initialisation is thread-safe.
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() {
     cudaDriverEntryPointQueryResult q;
     void* p = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess) {
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-  }
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -1320,15 +1319,16 @@ static_assert(smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448 &&
               "shared memory per CTA");
 
 // Most 2-CTA clusters of ffn_gemm_kernel<kEpi, kC, true, ...> resident at once,
-// per device (0 if the query fails: the unpaired kernel is used then).
+// per device (0 if the query fails: the unpaired kernel is used then).  Cached per
+// device as the count + 1 (0: not queried yet); threads that race on the first call
+// each query and store the same value.
 template <Epi kEpi, Caps kC, bool kStoreGu, Major kMajor, int kMx, bool k2Cta = false>
 int max_pair_clusters(size_t smem) {
-  static int cached[64] = {};
-  static bool done[64] = {};
+  static std::atomic<int> cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (!done[dev]) {
-    done[dev] = true;
+  int c = cached[dev].load(std::memory_order_acquire);
+  if (c == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(block_threads<kEpi, kMx>(), 1, 1);
@@ -1344,14 +1344,16 @@ int max_pair_clusters(size_t smem) {
     // The query counts the dynamic shared memory against the kernel's opt-in limit:
     // raise it first (it may not have been launched yet).
     auto fn = ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx, k2Cta>;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) == cudaSuccess &&
-        cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess)
-      cached[dev] = n;
-    else
+    if (!(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem)) == cudaSuccess &&
+          cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess)) {
       (void)cudaGetLastError();
+      n = 0;
+    }
+    c = n + 1;
+    cached[dev].store(c, std::memory_order_release);
   }
-  return cached[dev];
+  return c - 1;
 }
 
 // k2Cta: a dense (ungrouped) call runs the two-CTA MMA kernel when 2-CTA clusters fit.
@@ -1421,11 +1423,12 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
   a.combine_out = static_cast<float*>(s.combine_out);
   a.combine_k = s.combine_k > 0 ? s.combine_k : 1;
   const int64_t m_tiles = (s.a_rows + kBM - 1) / kBM;
-  // The shared-memory opt-in is a per-device property of each kernel: set once.
-  static bool smem_set[64] = {};
+  // The shared-memory opt-in is a per-device property of each kernel: set once (threads
+  // racing on the first call each set it; the flag is published after the settings).
+  static std::atomic<bool> smem_set[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!smem_set[dev]) {
+  if (!smem_set[dev].load(std::memory_order_acquire)) {
     for (auto fn : {ffn_gemm_kernel<kEpi, kC, false, kStoreGu, kMajor, kMx>,
                     ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx>}) {
       cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1438,7 +1441,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes_pair<kMx>()));
       if (e != cudaSuccess) return e;
     }
-    smem_set[dev] = true;
+    smem_set[dev].store(true, std::memory_order_release);
   }
   if constexpr (k2Cta) {
     // Two-CTA MMA for a dense call, or a grouped call whose unit prefix counts two-CTA
@@ -1576,17 +1579,17 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
   a.h_ready = h_ready;
   a.h_ready_target = a.n_tiles;
   a.dense_rows2 = a.dense_rows;
-  static bool smem_set[64] = {};
+  static std::atomic<bool> smem_set[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!smem_set[dev]) {
+  if (!smem_set[dev].load(std::memory_order_acquire)) {
     for (auto fn : {ffn_gemm_kernel<Epi::kFfn, kC, false, false, Major::kKMajor, kMx>,
                     ffn_gemm_kernel<Epi::kFfn, kC, true, false, Major::kKMajor, kMx, k2>}) {
       if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kSmem))) != cudaSuccess)
         return e;
     }
-    smem_set[dev] = true;
+    smem_set[dev].store(true, std::memory_order_release);
   }
   const int clusters = max_pair_clusters<Epi::kFfn, kC, false, Major::kKMajor, kMx, k2>(kSmem);
   cudaLaunchConfig_t cfg = {};
@@ -1661,18 +1664,18 @@ cudaError_t launch_plain2_impl(const GemmShape& s1, const GemmShape& s2, uint32_
   a.ldo2 = s2.ldo;
   const int32_t m1 = static_cast<int32_t>((s1.a_rows + kBM - 1) / kBM);
   const int32_t m2 = static_cast<int32_t>((s2.a_rows + kBM - 1) / kBM);
-  static bool smem_set[64] = {};
+  static std::atomic<bool> smem_set[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   cudaError_t e;
-  if (!smem_set[dev]) {
+  if (!smem_set[dev].load(std::memory_order_acquire)) {
     for (auto fn : {ffn_gemm_kernel<Epi::kPlain2, Caps::kBoth, false, false, kMajor, 0>,
                     ffn_gemm_kernel<Epi::kPlain2, Caps::kBoth, true, false, kMajor, 0, true>}) {
       if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kSmem))) != cudaSuccess)
         return e;
     }
-    smem_set[dev] = true;
+    smem_set[dev].store(true, std::memory_order_release);
   }
   // Pairs of CTAs run two-CTA MMAs (unit (p, n): CTA r takes m-tile 2p + r).
   int clusters = max_pair_clusters<Epi::kPlain2, Caps::kBoth, false, kMajor, 0, true>(kSmem);
