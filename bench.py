@@ -732,14 +732,21 @@ def run_situ(args):
     value = tokens_all / (ms_max * 1e-3)
     e2e_ms, _ = aggregate(dense["e2e_ms"], 0.0, world)
 
-    act = bench_act(args, dev, peaks, world, flush) if args.suite == "full" else None
-    moe = (bench_moe(args, dev, peaks, world, flush, ["grouped", "k3_decode", "k3_prefill"])
-           if args.suite == "full" else None)
-    mx = bench_mx(args, dev, peaks, world, flush) if args.suite == "full" else None
-    train = None
+    def with_clocks(fn):
+        """A sub-suite's result with the clock record taken while it ran."""
+        with ClockSampler(dev.index or 0) as suite_clk:
+            res = fn()
+        res["clocks"] = suite_clk.summary()
+        return res
+
+    act = moe = mx = train = None
     if args.suite == "full":
-        train = bench_train(args, dev, peaks, world, flush)
-        train["grouped"] = bench_moe_train(args, dev, peaks, world, flush)
+        act = with_clocks(lambda: bench_act(args, dev, peaks, world, flush))
+        moe = with_clocks(lambda: bench_moe(args, dev, peaks, world, flush,
+                                            ["grouped", "k3_decode", "k3_prefill"]))
+        mx = with_clocks(lambda: bench_mx(args, dev, peaks, world, flush))
+        train = with_clocks(lambda: bench_train(args, dev, peaks, world, flush))
+        train["grouped"] = with_clocks(lambda: bench_moe_train(args, dev, peaks, world, flush))
     status = situ.device_status(clear=True)
 
     achieved = dense["tflops"]
