@@ -106,3 +106,62 @@ def test_grouped_mx_random_shape(cuda_dev, T, k, E, M, I, fmt):
         wde = situ.MxWeights(wdq[0][e].contiguous(), wdq[1].view(E, -1)[e].contiguous(), fmt)
         ye = situ.situ_ffn_forward_mxfp8(x, we, wde).cpu()
         assert torch.equal(y[t_idx, s_idx].view(torch.int16), ye[t_idx].view(torch.int16)), e
+
+
+# ---------------------------------------------------------------------------
+# Training paths and the dense MX FFN at random shapes, with the checks (and the
+# tolerances derived there) of their own test modules.
+# ---------------------------------------------------------------------------
+from test_gpu_backward import _check_backward, _inputs as _bwd_inputs  # noqa: E402
+from test_gpu_moe_backward import _check as _grouped_bwd_check  # noqa: E402
+from test_gpu_moe_backward import _routes as _bwd_routes  # noqa: E402
+from test_gpu_moe_backward import _train_step  # noqa: E402
+from test_gpu_mx import test_ffn_forward_mxfp8 as _mx_ffn_check  # noqa: E402
+
+
+@pytest.mark.parametrize("R,M,I", _dense_shapes(n=6, seed=404))
+def test_dense_backward_random_shape(oracle, cuda_dev, R, M, I):
+    R = max(1, R // 2)  # the oracle's FP64 backward is the slow side
+    x, wgu, wd, dy, (xd, wgud, wdd, dyd) = _bwd_inputs(R, M, I, R + 3 * M, cuda_dev)
+    _, gu, h = situ.situ_ffn_forward_train(xd, wgud, wdd)
+    dx, dwg, dwd = situ.situ_ffn_backward(xd, wgud, wdd, gu, h, dyd)
+    torch.cuda.synchronize()
+    _check_backward(oracle, x, wgu, wd, dy, dx, dwg, dwd, what=f"{R}x{M}x{I}")
+
+
+def _grouped_bwd_shapes(n=5, seed=505):
+    """(T, k, E, M, I); the last expert has no routes.  The first two route 1600 or more
+    rows to 2 experts (two-CTA dh and dx GEMMs)."""
+    g = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        if i < 2:
+            E, k, T = 3, 2, int(g.integers(800, 1000))
+        else:
+            E = int(g.integers(3, 10))
+            k = int(g.integers(1, min(3, E - 1) + 1))
+            T = int(g.integers(1, 200))
+        out.append((T, k, E, 8 * int(g.integers(8, 41)), 8 * int(g.integers(8, 41))))
+    return out
+
+
+@pytest.mark.parametrize("T,k,E,M,I", _grouped_bwd_shapes())
+def test_grouped_backward_random_shape(oracle, cuda_dev, T, k, E, M, I):
+    ids = _bwd_routes(T, k, E, seed=T + k + E)
+    x = wl.normal((T, M), 1.0, seed=T + 1)
+    wgu, wd = wl.expert_weights(E, M, I, seed=E + 2)
+    dy = wl.normal((T, k, M), 1.0, seed=T + 3)
+    _, got = _train_step(x, ids, wgu, wd, dy, cuda_dev)
+    _grouped_bwd_check(oracle, x, ids, wgu, wd, dy, got, what=f"T={T} k={k} E={E} M={M} I={I}")
+
+
+def _mx_dense_shapes(n=4, seed=606):
+    g = np.random.default_rng(seed)
+    return [(int(g.integers(1, 700)), 128 * int(g.integers(1, 7)), 128 * int(g.integers(1, 7)))
+            for _ in range(n)]
+
+
+@pytest.mark.parametrize("fmt", [situ.MX_E4M3, situ.MX_E2M1], ids=["mxfp8", "mxfp4"])
+@pytest.mark.parametrize("R,M,I", _mx_dense_shapes())
+def test_dense_mx_random_shape(oracle, cuda_dev, R, M, I, fmt):
+    _mx_ffn_check(oracle, cuda_dev, R, M, I, fmt)
