@@ -155,3 +155,22 @@ def test_ffn_single_launch_switch(situ_lib):
     assert situ_lib.situ_ffn_set_single_launch(0) == 1
     assert situ_lib.situ_ffn_set_single_launch(7) == 0
     assert situ_lib.situ_ffn_set_single_launch(1) == 1
+
+
+def test_size_limits(situ_lib):
+    """The largest sizes: row counts and weight-row counts index the tensor maps and the
+    kernels' tile arithmetic as int32, so the calls refuse 2^31 and more before touching
+    any pointer (no GPU needed), and take 2^31 - 1 past that check."""
+    UNSUP = 6
+    g = situ_lib.situ_ffn_forward
+    p = [1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20, 64]
+    assert g(*p, 1 << 31, 8, 8, 4.0, 25.0, 0, None) == UNSUP          # R
+    assert g(*p, 8, 8, 1 << 30, 4.0, 25.0, 0, None) == UNSUP          # 2I
+    assert g(*p, 8, 1 << 31, 8, 4.0, 25.0, 0, None) == UNSUP          # M
+    assert g(*p, (1 << 31) - 1, 8, 8, 4.0, 25.0, 0, None) == WS       # past the limit check
+    m = situ_lib.situ_moe_grouped_forward
+    q = [1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20, 6 << 20, 7 << 20, 64]
+    assert m(*q, 1 << 28, 8, 4, 8, 8, 4.0, 25.0, 0, None) == UNSUP     # T * k_eff = 2^31
+    assert m(*q, 4, 2, 65536, 8, 16384, 4.0, 25.0, 0, None) == UNSUP  # E * 2I = 2^31
+    assert m(*q, 4, 2, 65536, 32768, 8, 4.0, 25.0, 0, None) == UNSUP  # E * M = 2^31
+    assert m(*q, 4, 2, 65537, 8, 8, 4.0, 25.0, 0, None) == BAD        # more than 65536 experts
