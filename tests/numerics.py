@@ -1,6 +1,6 @@
 """Comparison helpers for the GPU parity tests (test code, not the oracle).
 
-Tolerances (the stated targets of this build):
+Tolerances (the stated targets):
   * standalone activation: |gpu - ref| <= 1 bf16 ulp of the FP64 oracle value ref,
     ulp(ref) = 2^(floor(log2|ref|) - 7) for |ref| >= 2^-126, else 2^-133 (the bf16
     subnormal spacing; gradual underflow assumed), sign of zero ignored; and
