@@ -528,7 +528,7 @@ situ_status situ_moe_build_index(const int32_t* expert_ids, int32_t* expert_offs
 
 size_t situ_moe_workspace_size(int64_t R, int32_t E, int64_t M, int64_t I, situ_dtype dt) {
   if (R < 0 || E < 1 || M < 1 || I < 1 || dt != SITU_BF16) return 0;
-  // m-tile prefix + paired-unit prefixes of the two GEMMs
+  // m-tile prefix + work-unit prefixes of the two GEMMs
   const size_t tiles = 3 * round_up(static_cast<size_t>(E + 1) * 4, 256);
   const size_t xperm = round_up(static_cast<size_t>(R) * M * 2, 256);
   const size_t h = round_up(static_cast<size_t>(R) * I * 2, 256);
@@ -576,7 +576,7 @@ situ_status moe_forward_impl(const void* x, const int32_t* expert_offsets,
 
   // Experts with many rows on average run as two-CTA MMAs (M = 256 over a CTA pair);
   // with few rows (an expert's tail tile of at most 64 rows would cost a whole pair
-  // MMA) the multicast-paired kernel with its 64-row MMAs is faster.
+  // MMA) the one-CTA kernel with its 64-row MMAs is faster.
   const bool two_cta = R >= 512 * static_cast<int64_t>(E) && gemm_two_cta_available();
   cudaError_t e = launch_group_tiles(expert_offsets, E, R, gemm_n_tiles_situ(I),
                                      gemm_n_tiles_wide(M), tile_offsets, units_gu, units_dn,
@@ -750,7 +750,7 @@ situ_status situ_moe_grouped_forward_combined(const void* x, const int32_t* expe
 size_t situ_moe_backward_workspace_size(int64_t R, int32_t E, int64_t M, int64_t I,
                                         situ_dtype dt) {
   if (R < 0 || E < 1 || M < 1 || I < 1 || dt != SITU_BF16) return 0;
-  // m-tile prefix + paired-unit prefixes of the dh and dx GEMMs + the experts by
+  // m-tile prefix + work-unit prefixes of the dh and dx GEMMs + the experts by
   // descending rows, one [R, M] buffer (dy in expert order, then the per-route dx,
   // then x in expert order) and d(g, u) [R, 2I] in expert order.
   const size_t tiles = 4 * round_up(static_cast<size_t>(E + 1) * 4, 256);

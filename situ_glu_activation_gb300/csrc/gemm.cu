@@ -25,8 +25,8 @@ namespace {
 
 // Per-group work prefixes of the grouped GEMMs, and validation of the offsets:
 //   tiles[g]    = sum over g' < g of m_g'            (m_g = ceil(rows_g / 128))
-//   units_gu[g] = sum over g' < g of units(m_g', n_gu) (paired units, gate_up GEMM)
-//   units_dn[g] = sum over g' < g of units(m_g', n_dn) (paired units, down GEMM)
+//   units_gu[g] = sum over g' < g of units(m_g', n_gu) (work units, gate_up GEMM)
+//   units_dn[g] = sum over g' < g of units(m_g', n_dn) (work units, down GEMM)
 // Invalid offsets (not starting at 0, decreasing, not ending at R) zero all three
 // so the GEMMs do nothing, and record SITU_ERR_INDEX.  One block of 1024 threads.
 // Rank of each group by (row count descending, index ascending) -- a strict total order,
@@ -50,8 +50,8 @@ __global__ void group_tiles_kernel(const int32_t* __restrict__ off, int32_t G, i
                                    int32_t* __restrict__ units_gu,
                                    int32_t* __restrict__ units_dn, uint32_t* status,
                                    int two_cta) {
-  // Units of a group with m m-tiles: two-CTA pairs, or multicast-paired units.
-  auto units = [two_cta](int32_t m, int32_t n) { return two_cta ? ((m + 1) >> 1) * n : units_of(m, n); };
+  // Units of a group with m m-tiles: two-CTA pairs (ceil(m / 2) per n-tile), or tiles.
+  auto units = [two_cta](int32_t m, int32_t n) { return two_cta ? ((m + 1) >> 1) * n : m * n; };
   __shared__ int32_t partial[3][1024];
   __shared__ int bad;
   if (threadIdx.x == 0) bad = 0;
@@ -255,7 +255,7 @@ cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t 
 }
 
 bool gemm_two_cta_available() {
-  return max_pair_clusters<Epi::kPlain, Caps::kBoth, false, Major::kKMajor, 0, true>(
+  return max_pair_clusters<Epi::kPlain, Caps::kBoth, false, Major::kKMajor, 0>(
              smem_bytes_pair()) > 0;
 }
 

@@ -23,14 +23,15 @@
 //   last warp   (MXFP8) copies each stage's scale tiles into TMEM as it lands (with
 //               two-CTA MMAs: the even CTA's warp copies both CTAs' tiles, the odd
 //               CTA's relays the landing of its own to the even CTA's barrier).
-// Work is scheduled in units of two tiles for the two CTAs of a cluster: adjacent
-// m-tiles of one n-tile sharing the B tile, or -- for a group's odd last m-tile --
-// adjacent n-tiles sharing the A tile; each CTA fetches half of the shared tile and
-// multicasts it.  With two-CTA MMAs (dense GEMMs, large-expert grouped GEMMs, the dense
-// MXFP8 GEMMs) the pair's m-tiles 2p and 2p+1 form one M=256 MMA instead: each CTA
-// stages its own A rows and its half of B, both CTAs' copies count on the even CTA's
-// barrier, and its MMA thread issues for both.  Units run in (group, m-pair, n-tile)
-// order, so the n-tiles of one m-tile run side by side and share A in L2.  Operands are K-major, or MN-major
+// Every CTA loads its own operands with plain TMA tile copies into its own shared
+// memory (no copy is multicast).  One-CTA kernels take one tile per work unit, in
+// (group, m-tile, n-tile) order, so the n-tiles of one m-tile run side by side and
+// share A in L2, and the m-tiles of one group follow each other and share B there; a
+// tile with at most 64 valid rows fetches only those 64 A rows.  With two-CTA MMAs
+// (dense GEMMs, large-expert grouped GEMMs, the dense MXFP8 GEMMs) a cluster of two
+// CTAs takes m-tiles 2p and 2p+1 of one n-tile as one M=256 MMA: each CTA stages its
+// own A rows and its half of B, both CTAs' copies count on the even CTA's barrier, and
+// its MMA thread issues for both.  Operands are K-major, or MN-major
 // ({64, 64} boxes) for the backward, which also has a K-grouped schedule (each group
 // contracts over its own row range; groups largest first, rounds in serpentine order).
 // Two GEMMs can share one launch: the whole FFN (down tiles wait, across CTAs, for the
@@ -189,7 +190,7 @@ struct Args {
   int32_t num_groups;
   const int32_t* group_offsets;  // [G+1] device or null (dense)
   const int32_t* tile_offsets;   // [G+1] device or null (dense): m-tile prefix
-  const int32_t* unit_offsets;   // [G+1] device or null (dense): paired-unit prefix
+  const int32_t* unit_offsets;   // [G+1] device or null (dense): two-CTA unit prefix
   int32_t dense_rows;
   int32_t n_tiles;
   int32_t k_blocks;
@@ -261,7 +262,6 @@ struct TileCoord {
   int32_t row_end;  // one past the last valid A row (group end)
   int32_t group;
   int32_t n_tile;
-  int32_t share_a;  // paired unit of one m-tile and two n-tiles (A multicast)
   int32_t k0;       // first K row of the contraction (K-grouped; 0 otherwise)
   int32_t k_end;    // one past its last K row (K-grouped)
   int32_t k_blocks; // k-blocks of this tile
@@ -282,7 +282,6 @@ __device__ __forceinline__ TileCoord decode_tile(const Args& a, int32_t t) {
     c.group = 0;
     c.a_row0 = mt * kBM;
     c.row_end = a.dense_rows;
-    c.share_a = 0;
     return c;
   }
   // Largest g with tile_offsets[g] <= mt (empty groups repeat an offset; the
@@ -295,11 +294,10 @@ __device__ __forceinline__ TileCoord decode_tile(const Args& a, int32_t t) {
   c.group = lo;
   c.a_row0 = __ldg(a.group_offsets + lo) + (mt - __ldg(a.tile_offsets + lo)) * kBM;
   c.row_end = __ldg(a.group_offsets + lo + 1);
-  c.share_a = 0;
   return c;
 }
 
-// Tile `local` of one group's rows row0 .. row_end-1 (unpaired: m-tile-major).
+// Tile `local` of one group's rows row0 .. row_end-1 (m-tile-major).
 __device__ __forceinline__ TileCoord in_group_tile(int32_t n_tiles, int32_t local, int32_t row0,
                                                    int32_t row_end) {
   TileCoord c;
@@ -308,50 +306,18 @@ __device__ __forceinline__ TileCoord in_group_tile(int32_t n_tiles, int32_t loca
   c.a_row0 = row0 + mt * kBM;
   c.row_end = row_end;
   c.group = 0;
-  c.share_a = 0;
   return c;
 }
 
-// Work units.  Unpaired: one unit = one tile, from decode_tile.  Paired
-// (clusters of two CTAs, CTA rank r):
-//   * a group (expert) with m m-tiles has floor(m/2) * n_tiles "shared-B" units:
-//     unit (p, n) gives rank r the tile (m-tile 2p + r, n-tile n); the two CTAs
-//     share the B tile of n-tile n, each fetching one half and multicasting it;
-//   * when m is odd, its last m-tile forms ceil(n_tiles/2) "shared-A" units:
-//     unit q gives rank r the tile (m-tile m-1, n-tile 2q + r); the two CTAs share
-//     the A tile, each fetching 64 of its 128 rows and multicasting them.
-// Dense calls are one group of all rows; grouped calls read the per-group unit
-// prefix from unit_offsets.
-__host__ __device__ __forceinline__ int32_t units_of(int32_t m, int32_t n_tiles) {
-  return (m >> 1) * n_tiles + (m & 1) * ((n_tiles + 1) >> 1);
-}
-
-// Paired unit `local` of one group's rows row0 .. row_end-1 (see above).
-__device__ __forceinline__ TileCoord in_group_unit(int32_t n_tiles, int32_t local, uint32_t rank,
-                                                   int32_t row0, int32_t row_end) {
-  const int32_t m = (row_end - row0 + kBM - 1) / kBM;
-  const int32_t shared_b_units = (m >> 1) * n_tiles;
-  TileCoord c;
-  c.group = 0;
-  c.row_end = row_end;
-  if (local < shared_b_units) {
-    const int32_t p = local / n_tiles;
-    c.n_tile = local - p * n_tiles;
-    c.a_row0 = row0 + (2 * p + static_cast<int32_t>(rank)) * kBM;
-    c.share_a = 0;
-  } else {
-    const int32_t q = local - shared_b_units;
-    c.n_tile = 2 * q + static_cast<int32_t>(rank);
-    c.a_row0 = row0 + (m - 1) * kBM;
-    c.share_a = 1;
-  }
-  return c;
-}
-
-template <bool kPair, bool kKG, bool kTwo = false, bool k2Cta = false>
+// Work units.  One-CTA kernels: one unit = one tile (decode_tile; K-grouped:
+// in_group_tile within each group).  Two-CTA kernels (clusters of two CTAs, CTA rank
+// r): unit (p, n) of a group gives rank r m-tile 2p + r of n-tile n (pair_unit); dense
+// calls are one group of all rows, grouped calls read the per-group unit prefix from
+// unit_offsets.
+template <bool kPair, bool kKG, bool kTwo = false>
 __device__ __forceinline__ int32_t num_units(const Args& a) {
   if (kTwo) return a.fused_units1 + a.fused_units2;
-  if (k2Cta) {
+  if (kPair) {
     if (a.unit_offsets) return __ldg(a.unit_offsets + a.num_groups);
     return ((a.dense_rows + 2 * kBM - 1) / (2 * kBM)) * a.n_tiles;
   }
@@ -359,9 +325,7 @@ __device__ __forceinline__ int32_t num_units(const Args& a) {
     if (a.tile_offsets && __ldg(a.tile_offsets + a.num_groups) == 0) return 0;
     return a.num_groups * a.units_per_group;
   }
-  if (!kPair) return total_tiles(a);
-  if (a.unit_offsets) return __ldg(a.unit_offsets + a.num_groups);
-  return units_of((a.dense_rows + kBM - 1) / kBM, a.n_tiles);
+  return total_tiles(a);
 }
 
 // The unit of a CTA's i-th round: round i covers units [i * stride, (i + 1) * stride),
@@ -385,11 +349,10 @@ __device__ __forceinline__ TileCoord pair_unit(int32_t n_tiles, int32_t local, u
   c.a_row0 = (2 * p + static_cast<int32_t>(rank)) * kBM;
   c.row_end = row_end;
   c.group = 0;
-  c.share_a = 0;
   return c;
 }
 
-template <bool kPair, bool kKG, bool kTwo = false, bool k2Cta = false>
+template <bool kPair, bool kKG, bool kTwo = false>
 __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_t rank) {
   TileCoord c;
   if (kTwo) {
@@ -398,9 +361,7 @@ __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_
     const int32_t local = p2 ? u - a.fused_units1 : u;
     const int32_t nt = p2 ? a.n_tiles2 : a.n_tiles;
     const int32_t rows = p2 ? a.dense_rows2 : a.dense_rows;
-    c = k2Cta  ? pair_unit(nt, local, rank, rows)
-        : kPair ? in_group_unit(nt, local, rank, 0, rows)
-                : in_group_tile(nt, local, 0, rows);
+    c = kPair ? pair_unit(nt, local, rank, rows) : in_group_tile(nt, local, 0, rows);
     c.group = 0;
     c.k0 = 0;
     c.k_end = 0;
@@ -409,7 +370,7 @@ __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_
     return c;
   }
   c.phase2 = 0;
-  if (k2Cta) {
+  if (kPair) {
     // Dense, or grouped with a per-group prefix of two-CTA units.
     int32_t g = 0, row0 = 0, row_end = a.dense_rows, local = u;
     if (a.unit_offsets) {
@@ -437,8 +398,7 @@ __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_
     const int32_t gi = u / a.units_per_group;
     const int32_t local = u - gi * a.units_per_group;
     const int32_t g = a.group_order ? __ldg(a.group_order + gi) : gi;
-    c = kPair ? in_group_unit(a.n_tiles, local, rank, 0, a.dense_rows)
-              : in_group_tile(a.n_tiles, local, 0, a.dense_rows);
+    c = in_group_tile(a.n_tiles, local, 0, a.dense_rows);
     c.phase2 = 0;
     c.group = g;
     c.k0 = __ldg(a.k_group_offsets + g);
@@ -446,24 +406,7 @@ __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_
     c.k_blocks = c.k_end > c.k0 ? (c.k_end - c.k0 + kBK - 1) / kBK : 0;
     return c;
   }
-  if (!kPair) {
-    c = decode_tile(a, u);
-  } else {
-    int32_t g = 0, row0 = 0, row_end = a.dense_rows, local = u;
-    if (a.unit_offsets) {
-      int32_t lo = 0, hi = a.num_groups - 1;
-      while (lo < hi) {
-        const int32_t mid = (lo + hi + 1) >> 1;
-        if (__ldg(a.unit_offsets + mid) <= u) lo = mid; else hi = mid - 1;
-      }
-      g = lo;
-      row0 = __ldg(a.group_offsets + g);
-      row_end = __ldg(a.group_offsets + g + 1);
-      local = u - __ldg(a.unit_offsets + g);
-    }
-    c = in_group_unit(a.n_tiles, local, rank, row0, row_end);
-    c.group = g;
-  }
+  c = decode_tile(a, u);
   c.phase2 = 0;
   c.k0 = 0;
   c.k_end = 0;
@@ -580,8 +523,9 @@ __host__ __device__ __forceinline__ int64_t sf_tile_offset(int64_t m_tile, int64
          (r_in_tile / 32) * 4 + (b % 4);
 }
 
-template <Epi kEpi, Caps kC, bool kPair, bool kStoreGu, Major kMajor, int kMx = 0,
-          bool k2Cta = false>
+// kPair: clusters of two CTAs whose MMAs are tcgen05 cta_group::2 (M = 256 over the
+// pair); otherwise one CTA per tile with cta_group::1 MMAs.
+template <Epi kEpi, Caps kC, bool kPair, bool kStoreGu, Major kMajor, int kMx = 0>
 __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_a64,
@@ -589,9 +533,9 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
                     const __grid_constant__ CUtensorMap map_a2,
                     const __grid_constant__ CUtensorMap map_a2_64,
                     const __grid_constant__ CUtensorMap map_b2, const Args args) {
-  // k2Cta: the pair's MMAs are tcgen05 cta_group::2 (M = 256 over the two CTAs).
+  constexpr bool k2Cta = kPair;
   using G = std::conditional_t<k2Cta, GeoPairT<kMx>, Geo<kMx>>;
-  static_assert(!k2Cta || (kPair && kMajor != Major::kABMNGrouped),
+  static_assert(!k2Cta || kMajor != Major::kABMNGrouped,
                 "two-CTA MMA: GEMMs without a K-grouped contraction");
   static_assert(G::Stages * G::StageBytes + sizeof(SharedCtl) + 1024 <= 232448,
                 "shared memory per CTA");
@@ -622,10 +566,8 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
     for (int s = 0; s < G::Stages; ++s) {
       // Two-CTA MXFP8: the even CTA's own arrival and the odd CTA's relayed one.
       mbar_init(smem_u32(&ctl->full[s]), (k2Cta && kMx) ? 2 : 1);
-      // Paired: a stage is free once the MMAs of both CTAs have read it (the
-      // peer's multicast writes into this CTA's copy of the stage).
       // Two-CTA: one commit of the even CTA frees the stage in both.
-      mbar_init(smem_u32(&ctl->empty[s]), (kPair && !k2Cta) ? 2 : 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
     for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(smem_u32(&ctl->acc_full[b]), 1);
@@ -640,11 +582,11 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
     ctl->abort = 0;
     fence_mbar_init();
     tma_prefetch_map(&map_a);
-    if (kPair) tma_prefetch_map(&map_a64);
+    if (!kPair) tma_prefetch_map(&map_a64);
     tma_prefetch_map(&map_b);
     if (kTwo) {
       tma_prefetch_map(&map_a2);
-      if (kPair) tma_prefetch_map(&map_a2_64);
+      if (!kPair) tma_prefetch_map(&map_a2_64);
       tma_prefetch_map(&map_b2);
     }
   }
@@ -659,10 +601,10 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
     tc_fence_before_sync();
   }
   __syncthreads();
-  if (kPair) cluster_sync();  // the peer's barriers exist before any multicast
+  if (kPair) cluster_sync();  // the peer's barriers exist before any copy or MMA names them
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
-  const int32_t n_total = num_units<kPair, kKG, kTwo, k2Cta>(args);
+  const int32_t n_total = num_units<kPair, kKG, kTwo>(args);
   const int32_t u0 = kPair ? static_cast<int32_t>(blockIdx.x >> 1) : static_cast<int32_t>(blockIdx.x);
   const int32_t ustride = kPair ? static_cast<int32_t>(gridDim.x >> 1) : static_cast<int32_t>(gridDim.x);
 
@@ -675,7 +617,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       for (int32_t i = 0; i * ustride < n_total && ok; ++i) {
         const int32_t t = round_unit<kKG>(i, u0, ustride);
         if (t >= n_total) continue;
-        const TileCoord tc = unit_tile<kPair, kKG, kTwo, k2Cta>(args, t, rank);
+        const TileCoord tc = unit_tile<kPair, kKG, kTwo>(args, t, rank);
         const int64_t gbase = static_cast<int64_t>(tc.group) * args.b_group_rows;
         // Second-GEMM tiles read the second pair of operands (kFfn: h and W_down).
         const bool p2 = kTwo && tc.phase2;
@@ -779,63 +721,39 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
             }
             continue;
           }
-          // A shared-A unit whose tile has at most 64 valid rows needs only A rows 0..63
-          // (the 64-row MMA reads no more; with MXFP8, rows 64..127 only feed output rows
-          // that are not stored): the odd CTA fetches no A half and the stage expects
-          // that many bytes less.
-          const bool a_half_only = kPair && tc.share_a && tc.row_end - tc.a_row0 <= 64;
-          mbar_arrive_expect_tx(full, a_half_only ? G::TxBytes - G::ABytes / 2 : G::TxBytes);
+          // A tile with at most 64 valid rows needs only A rows 0..63 (the 64-row MMA reads
+          // no more; with MXFP8, rows 64..127 only feed output rows that are not stored):
+          // one 64-row box, and the stage expects that many bytes less.
+          const bool a_half = tc.row_end - tc.a_row0 <= 64;
+          mbar_arrive_expect_tx(full, a_half ? G::TxBytes - G::ABytes / 2 : G::TxBytes);
           constexpr bool kAMN = a_mn_major(kMajor);
           constexpr bool kBMN = kMajor != Major::kKMajor;
           const int32_t kx = kb * G::BK + tc.k0;     // A's K coordinate
           const int32_t kxb = kb * G::BK + kb_off;   // B's K coordinate
-          // A (128 rows of the tile); `half` picks one 64-row half for a shared-A unit.
-          auto load_a = [&](uint32_t dst, int32_t row, int rows64, bool mcast) {
-            for (int j = 0; j < rows64; ++j) {
-              const uint32_t d = dst + j * (kAMN ? kMnAtomBytes : 0u);
-              if (kAMN) {
-                if (mcast) tma_load_2d_multicast(d, pm_a, row + 64 * j, kx, full, 0x3);
-                else tma_load_2d(d, pm_a, row + 64 * j, kx, full);
-              } else if (rows64 == 2) {
-                tma_load_2d(d, pm_a, kx, row, full);
-                break;
-              } else {
-                if (mcast) tma_load_2d_multicast(d, pm_a64, kx, row, full, 0x3);
-                else tma_load_2d(d, pm_a64, kx, row, full);
-              }
-            }
-          };
-          // B (128 rows = one half of the 256-row tile).
-          auto load_b = [&](uint32_t dst, int32_t row, bool mcast) {
-            if (kBMN) {
-              for (int j = 0; j < 2; ++j) {
-                if (mcast) tma_load_2d_multicast(dst + j * kMnAtomBytes, pm_b, row + 64 * j, kxb, full, 0x3);
-                else tma_load_2d(dst + j * kMnAtomBytes, pm_b, row + 64 * j, kxb, full);
-              }
-            } else {
-              if (mcast) tma_load_2d_multicast(dst, pm_b, kxb, row, full, 0x3);
-              else tma_load_2d(dst, pm_b, kxb, row, full);
-            }
-          };
-          constexpr uint32_t kBHalf = G::BHalfRows * 128;  // bytes of one B half
-          if (!kPair) {
-            load_a(sa, tc.a_row0, 2, false);
-            load_b(sb, b_row0, false);
-            load_b(sb + kBHalf, b_row1, false);
-          } else if (!tc.share_a) {
-            // Shared B: this CTA fetches one half of the B tile for both CTAs.
-            load_a(sa, tc.a_row0, 2, false);
-            load_b(sb + rank * kBHalf, rank == 0 ? b_row0 : b_row1, true);
+          // A: rows a_row0 .. +127, or the first 64 of them (MN-major: one {64, 64} atom
+          // per 64 rows; K-major: one 128-row box, or one 64-row box).
+          if (kAMN) {
+            for (int j = 0; j < (a_half ? 1 : 2); ++j)
+              tma_load_2d(sa + j * kMnAtomBytes, pm_a, tc.a_row0 + 64 * j, kx, full);
+          } else if (a_half) {
+            tma_load_2d(sa, pm_a64, kx, tc.a_row0, full);
           } else {
-            // Shared A: this CTA fetches 64 of the 128 A rows for both CTAs.
-            if (!a_half_only || rank == 0)
-              load_a(sa + rank * (G::ABytes / 2), tc.a_row0 + static_cast<int32_t>(rank) * 64, 1,
-                     true);
-            load_b(sb, b_row0, false);
-            load_b(sb + kBHalf, b_row1, false);
+            tma_load_2d(sa, pm_a, kx, tc.a_row0, full);
+          }
+          // B: two halves of BHalfRows rows (MN-major: two {64, 64} atoms each).
+          constexpr uint32_t kBHalf = G::BHalfRows * 128;  // bytes of one B half
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t dst = sb + h * kBHalf;
+            const int32_t row = h == 0 ? b_row0 : b_row1;
+            if (kBMN) {
+              for (int j = 0; j < 2; ++j)
+                tma_load_2d(dst + j * kMnAtomBytes, pm_b, row + 64 * j, kxb, full);
+            } else {
+              tma_load_2d(dst, pm_b, kxb, row, full);
+            }
           }
           if constexpr (kMx) {
-            // This CTA's own scale tiles of the stage (not multicast).
+            // The stage's A and B scale tiles.
             const uint32_t ssf = sb + G::BBytes;
             bulk_load(ssf, sfa_unit + static_cast<int64_t>(kb) * kSfTileBytes, kSfTileBytes, full);
             bulk_load(ssf + kSfTileBytes, sfb_unit + static_cast<int64_t>(kb) * kSfbStageBytes,
@@ -890,7 +808,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * G::BN;
-        const TileCoord tcm = unit_tile<kPair, kKG, kTwo, k2Cta>(args, t, rank);
+        const TileCoord tcm = unit_tile<kPair, kKG, kTwo>(args, t, rank);
         const uint32_t idesc = kMx      ? idesc_mxf8(k2Cta ? 2 * kBM : kBM, G::BN,
                                                 kMx == 2 ? kMxE2M1 : kMxE4M3)
                                : (k2Cta ? idesc_bf16_f32(2 * kBM, G::BN)
@@ -931,8 +849,6 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
             }
             if constexpr (k2Cta) {
               umma_commit_pair(smem_u32(&ctl->empty[stage]), 0x3);
-            } else if (kPair) {
-              umma_commit_multicast(smem_u32(&ctl->empty[stage]), 0x3);
             } else {
               umma_commit(smem_u32(&ctl->empty[stage]));
             }
@@ -952,8 +868,6 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
             }
             if constexpr (k2Cta) {
               umma_commit_pair(smem_u32(&ctl->empty[stage]), 0x3);
-            } else if (kPair) {
-              umma_commit_multicast(smem_u32(&ctl->empty[stage]), 0x3);
             } else {
               umma_commit(smem_u32(&ctl->empty[stage]));
             }
@@ -995,7 +909,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       for (int32_t i = 0; i * ustride < n_total && ok; ++i) {
         const int32_t t = round_unit<kKG>(i, u0, ustride);
         if (t >= n_total) continue;
-        const TileCoord tcs = unit_tile<kPair, kKG, kTwo, k2Cta>(args, t, rank);
+        const TileCoord tcs = unit_tile<kPair, kKG, kTwo>(args, t, rank);
         for (int32_t kb = 0; kb < tcs.k_blocks; ++kb) {
           const bool landed = relay ? ctl_wait(ctl, &ctl->sf_ready[stage], phase, args.status)
                                     : ctl_wait<k2Cta>(ctl, &ctl->full[stage], phase, args.status);
@@ -1056,7 +970,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after_sync();
-      const TileCoord tc = unit_tile<kPair, kKG, kTwo, k2Cta>(args, t, rank);
+      const TileCoord tc = unit_tile<kPair, kKG, kTwo>(args, t, rank);
       const bool p2 = kTwo && tc.phase2;
       // M=64 tiles (bf16 only): only the first 16 lanes of each quarter hold rows
       // (16q + lane).
@@ -1133,9 +1047,8 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         }
         if (kFfn) {
           // Publish this tile's h rows: each epilogue thread orders its stores, the
-          // epilogue warps meet, and one release add counts the tile for its m-tile
-          // (a shared-A unit's tile past the last n-tile stores nothing and does not
-          // count).
+          // epilogue warps meet, and one release add counts the tile for its m-tile (a
+          // two-CTA pair's m-tile past the rows stores nothing and does not count).
           __threadfence();
           named_barrier_sync(1, kEpiThreads);
           if (threadIdx.x == 64 && tc.n_tile < args.n_tiles && tc.a_row0 < tc.row_end)
@@ -1318,11 +1231,11 @@ static_assert(smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448 &&
                   smem_bytes_pair<1>() <= 232448 && smem_bytes_pair<2>() <= 232448,
               "shared memory per CTA");
 
-// Most 2-CTA clusters of ffn_gemm_kernel<kEpi, kC, true, ...> resident at once,
-// per device (0 if the query fails: the unpaired kernel is used then).  Cached per
-// device as the count + 1 (0: not queried yet); threads that race on the first call
-// each query and store the same value.
-template <Epi kEpi, Caps kC, bool kStoreGu, Major kMajor, int kMx, bool k2Cta = false>
+// Most 2-CTA clusters of the two-CTA kernel ffn_gemm_kernel<kEpi, kC, true, ...>
+// resident at once, per device (0 if the query fails: the one-CTA kernel is used
+// then).  Cached per device as the count + 1 (0: not queried yet); threads that race
+// on the first call each query and store the same value.
+template <Epi kEpi, Caps kC, bool kStoreGu, Major kMajor, int kMx>
 int max_pair_clusters(size_t smem) {
   static std::atomic<int> cached[64] = {};
   int dev = 0;
@@ -1343,7 +1256,7 @@ int max_pair_clusters(size_t smem) {
     int n = 0;
     // The query counts the dynamic shared memory against the kernel's opt-in limit:
     // raise it first (it may not have been launched yet).
-    auto fn = ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx, k2Cta>;
+    auto fn = ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx>;
     if (!(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem)) == cudaSuccess &&
           cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess)) {
@@ -1429,16 +1342,14 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!smem_set[dev].load(std::memory_order_acquire)) {
-    for (auto fn : {ffn_gemm_kernel<kEpi, kC, false, kStoreGu, kMajor, kMx>,
-                    ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx>}) {
-      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(kSmem));
-      if (e != cudaSuccess) return e;
-    }
+    cudaError_t e = cudaFuncSetAttribute(ffn_gemm_kernel<kEpi, kC, false, kStoreGu, kMajor, kMx>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmem));
+    if (e != cudaSuccess) return e;
     if constexpr (k2Cta) {
-      cudaError_t e = cudaFuncSetAttribute(
-          ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx, true>,
-          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_bytes_pair<kMx>()));
+      e = cudaFuncSetAttribute(ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem_bytes_pair<kMx>()));
       if (e != cudaSuccess) return e;
     }
     smem_set[dev].store(true, std::memory_order_release);
@@ -1450,7 +1361,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
                        !s.out_row_index && !s.combine_w;
     const bool use2 = dense || (s.pair_units && s.unit_offsets && !s.k_group_offsets);
     int clusters2 =
-        use2 ? max_pair_clusters<kEpi, kC, kStoreGu, kMajor, kMx, true>(smem_bytes_pair<kMx>()) : 0;
+        use2 ? max_pair_clusters<kEpi, kC, kStoreGu, kMajor, kMx>(smem_bytes_pair<kMx>()) : 0;
     if (s.pair_units && clusters2 == 0) return cudaErrorNotSupported;
     if (clusters2 > 0) {
       // Unit (p, n) gives CTA r m-tile 2p + r of n-tile n (of its group).
@@ -1471,37 +1382,12 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
       attr.val.clusterDim.z = 1;
       cfg.attrs = &attr;
       cfg.numAttrs = 1;
-      return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx, true>,
+      return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx>,
                                 ma, ma64, mb, ma, ma64, mb, a);
     }
   }
-  int clusters = max_pair_clusters<kEpi, kC, kStoreGu, kMajor, kMx>(kSmem);
-  const int64_t pair_units = (m_tiles / 2) * a.n_tiles + (m_tiles % 2) * ((a.n_tiles + 1) / 2);
-  if (clusters > 0 && (!s.tile_offsets || s.unit_offsets || s.k_group_offsets)) {
-    // Clusters of two CTAs sharing a B or an A tile by multicast.
-    a.unit_offsets = s.unit_offsets;
-    if (s.k_group_offsets) {
-      a.units_per_group = static_cast<int32_t>(pair_units);
-      const int64_t units = pair_units * s.num_groups;
-      if (units < clusters) clusters = static_cast<int>(units < 1 ? 1 : units);
-    } else if (!s.tile_offsets) {
-      if (pair_units < clusters) clusters = static_cast<int>(pair_units);
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(block_threads<kEpi, kMx>(), 1, 1);
-    cfg.dynamicSmemBytes = kSmem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx>, ma,
-                              ma64, mb, ma, ma64, mb, a);
-  }
+  // One CTA per tile, persistent: tiles in (group, m-tile, n-tile) order (K-grouped:
+  // every group has the same m_tiles x n_tiles output tiles).
   int grid = num_sms;
   if (s.k_group_offsets) {
     a.units_per_group = static_cast<int32_t>(m_tiles * a.n_tiles);
@@ -1526,12 +1412,11 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
                                   const SituParams& p, int32_t* h_ready, uint32_t* status,
                                   int num_sms, cudaStream_t stream) {
   using G = Geo<kMx>;
-  // The paired kernel is the two-CTA MMA one (its N, BK and B half match Geo<kMx>).
-  constexpr bool k2 = true;
+  // The cluster kernel is the two-CTA MMA one (its N, BK and B half match Geo<kMx>).
   static_assert(GeoPairT<kMx>::BN == G::BN && GeoPairT<kMx>::BK == G::BK &&
                     GeoPairT<kMx>::BHalfRows == G::BHalfRows,
                 "tile geometry of the two-CTA kernel");
-  // One opt-in size serves the paired kernel and the unpaired fallback.
+  // One opt-in size serves the two-CTA kernel and the one-CTA fallback.
   constexpr size_t kSmem = smem_bytes_pair<kMx>() > smem_bytes<kMx>() ? smem_bytes_pair<kMx>()
                                                                        : smem_bytes<kMx>();
   if (s_gu.a_rows == 0) return cudaSuccess;
@@ -1584,14 +1469,14 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!smem_set[dev].load(std::memory_order_acquire)) {
     for (auto fn : {ffn_gemm_kernel<Epi::kFfn, kC, false, false, Major::kKMajor, kMx>,
-                    ffn_gemm_kernel<Epi::kFfn, kC, true, false, Major::kKMajor, kMx, k2>}) {
+                    ffn_gemm_kernel<Epi::kFfn, kC, true, false, Major::kKMajor, kMx>}) {
       if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kSmem))) != cudaSuccess)
         return e;
     }
     smem_set[dev].store(true, std::memory_order_release);
   }
-  const int clusters = max_pair_clusters<Epi::kFfn, kC, false, Major::kKMajor, kMx, k2>(kSmem);
+  const int clusters = max_pair_clusters<Epi::kFfn, kC, false, Major::kKMajor, kMx>(kSmem);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeCooperative;
@@ -1602,8 +1487,8 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
   cfg.attrs = attrs;
   if (clusters > 0) {
     const int32_t mt = static_cast<int32_t>(m_tiles);
-    a.fused_units1 = k2 ? ((mt + 1) / 2) * a.n_tiles : units_of(mt, a.n_tiles);
-    a.fused_units2 = k2 ? ((mt + 1) / 2) * a.n_tiles2 : units_of(mt, a.n_tiles2);
+    a.fused_units1 = ((mt + 1) / 2) * a.n_tiles;
+    a.fused_units2 = ((mt + 1) / 2) * a.n_tiles2;
     attrs[1].id = cudaLaunchAttributeClusterDimension;
     attrs[1].val.clusterDim.x = 2;
     attrs[1].val.clusterDim.y = 1;
@@ -1611,7 +1496,7 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
     cfg.numAttrs = 2;
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     return cudaLaunchKernelEx(&cfg,
-                              ffn_gemm_kernel<Epi::kFfn, kC, true, false, Major::kKMajor, kMx, k2>,
+                              ffn_gemm_kernel<Epi::kFfn, kC, true, false, Major::kKMajor, kMx>,
                               ma, ma64, mb, ma2, ma2_64, mb2, a);
   }
   a.fused_units1 = static_cast<int32_t>(m_tiles) * a.n_tiles;
@@ -1670,7 +1555,7 @@ cudaError_t launch_plain2_impl(const GemmShape& s1, const GemmShape& s2, uint32_
   cudaError_t e;
   if (!smem_set[dev].load(std::memory_order_acquire)) {
     for (auto fn : {ffn_gemm_kernel<Epi::kPlain2, Caps::kBoth, false, false, kMajor, 0>,
-                    ffn_gemm_kernel<Epi::kPlain2, Caps::kBoth, true, false, kMajor, 0, true>}) {
+                    ffn_gemm_kernel<Epi::kPlain2, Caps::kBoth, true, false, kMajor, 0>}) {
       if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kSmem))) != cudaSuccess)
         return e;
@@ -1678,7 +1563,7 @@ cudaError_t launch_plain2_impl(const GemmShape& s1, const GemmShape& s2, uint32_
     smem_set[dev].store(true, std::memory_order_release);
   }
   // Pairs of CTAs run two-CTA MMAs (unit (p, n): CTA r takes m-tile 2p + r).
-  int clusters = max_pair_clusters<Epi::kPlain2, Caps::kBoth, false, kMajor, 0, true>(kSmem);
+  int clusters = max_pair_clusters<Epi::kPlain2, Caps::kBoth, false, kMajor, 0>(kSmem);
   if (clusters > 0) {
     a.fused_units1 = ((m1 + 1) / 2) * a.n_tiles;
     a.fused_units2 = ((m2 + 1) / 2) * a.n_tiles2;
@@ -1697,7 +1582,7 @@ cudaError_t launch_plain2_impl(const GemmShape& s1, const GemmShape& s2, uint32_
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg,
-                              ffn_gemm_kernel<Epi::kPlain2, Caps::kBoth, true, false, kMajor, 0, true>,
+                              ffn_gemm_kernel<Epi::kPlain2, Caps::kBoth, true, false, kMajor, 0>,
                               ma, ma64, mb, ma2, ma2_64, mb2, a);
   }
   a.fused_units1 = m1 * a.n_tiles;

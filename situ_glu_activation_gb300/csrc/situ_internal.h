@@ -51,10 +51,11 @@ struct GemmShape {
   int32_t num_groups;
   const int32_t* group_offsets;
   const int32_t* tile_offsets;
-  // Paired-unit prefix per group for this GEMM (from launch_group_tiles), or NULL.
+  // Work-unit prefix per group for this GEMM (from launch_group_tiles), or NULL.
   const int32_t* unit_offsets;
   // unit_offsets count two-CTA units (ceil(m-tiles / 2) per output tile; the group's
-  // pairs run as cta_group::2 MMAs) instead of multicast-paired units.
+  // pairs run as cta_group::2 MMAs); otherwise the grouped GEMM runs one CTA per tile
+  // over tile_offsets.
   bool pair_units;
   int64_t b_group_rows;  // B rows per group
   int64_t b_up_offset;   // SiTU epilogue: row offset of the up half inside a group
@@ -173,13 +174,14 @@ cudaError_t launch_mx_quantize_weights(const void* w, void* codes, void* scales,
 size_t mx_act_scale_bytes(int64_t R, int64_t K);
 size_t mx_weight_scale_bytes(int32_t G, int64_t rows_per_group, int64_t K, int64_t split);
 
-// Per-group prefixes of m-tiles and of the paired units of two grouped GEMMs with
+// Per-group prefixes of m-tiles and of the work units of two grouped GEMMs with
 // n_tiles_1 and n_tiles_2 output tiles per m-tile, plus validation of the offsets.
 // order[rank] = group, ranking groups by descending row count (ties by index): the
 // K-grouped weight-gradient GEMMs run the largest contractions first.
 cudaError_t launch_group_order(const int32_t* group_offsets, int32_t G, int32_t* order,
                                cudaStream_t stream);
-// two_cta: the unit prefixes count two-CTA units (ceil(m/2) per output tile).
+// two_cta: the unit prefixes count two-CTA units (ceil(m/2) per output tile); otherwise
+// tiles (m per output tile).
 cudaError_t launch_group_tiles(const int32_t* group_offsets, int32_t G, int64_t R,
                                int32_t n_tiles_1, int32_t n_tiles_2, int32_t* tile_offsets,
                                int32_t* units_1, int32_t* units_2, uint32_t* status,

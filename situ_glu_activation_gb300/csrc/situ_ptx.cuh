@@ -116,19 +116,6 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* map, 
       : "memory");
 }
 
-// Same tile load, multicast: the box lands at the same shared-memory offset in
-// every CTA of the cluster named in cta_mask and completes tx on each CTA's
-// mbarrier at the same offset.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const void* map, int32_t x,
-                                                      int32_t y, uint32_t bar,
-                                                      uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // Thread-block clusters
 // ---------------------------------------------------------------------------
@@ -200,15 +187,6 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// Same, arriving once on the mbarrier at this offset in every CTA of cta_mask.
-__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
       : "memory");
 }
 

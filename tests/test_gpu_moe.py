@@ -90,7 +90,7 @@ def test_grouped_swiglu_variant(oracle, cuda_dev):
 
 
 @pytest.mark.parametrize("T,k,E,M,I,skew", [
-    (64, 2, 4, 256, 256, False),    # few rows per expert: multicast-paired kernel
+    (64, 2, 4, 256, 256, False),    # few rows per expert: one-CTA kernel
     # >= 512 rows per expert on average: two-CTA MMAs; skewed sizes give experts with
     # odd m-tile counts, a partial last pair, one expert with no rows
     (1024, 2, 4, 512, 384, True),

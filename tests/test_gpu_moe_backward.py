@@ -144,7 +144,7 @@ def test_forward_train_matches_forward(oracle, cuda_dev):
 def test_grouped_backward_equals_dense_single_expert(cuda_dev, T):
     """One expert, one slot: the grouped backward runs the same tiles in the same
     order as the dense backward, so every output is bit-identical (333 rows: the
-    multicast-paired grouped kernels; 1200: two-CTA grouped dh and dx GEMMs)."""
+    one-CTA grouped kernels; 1200: two-CTA grouped dh and dx GEMMs)."""
     M, I = 256, 384
     ids = torch.zeros(T, 1, dtype=torch.int32)
     x = wl.normal((T, M), 1.0, seed=31)
