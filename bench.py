@@ -857,6 +857,12 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    world = dist_env()[0]
+    if args.gpus != world:
+        # One process per GPU: N GPUs are N ranks (torchrun --nproc-per-node N).
+        ap.error(f"--gpus {args.gpus} with {world} rank(s): run one rank per GPU, e.g. "
+                 f"python -m torch.distributed.run --nproc-per-node {args.gpus} bench.py "
+                 f"--gpus {args.gpus}")
     if args.impl == "reference":
         return run_reference(args)
     return run_situ(args)

@@ -18,6 +18,8 @@ namespace {
 using namespace situ;
 
 constexpr int kMaxDevices = 64;
+// Grouped bf16 GEMMs run two-CTA MMAs when the experts average at least this many rows.
+constexpr int64_t kTwoCtaMinRows = 128;
 
 // Per-device status word: the first device-side failure since the last clear.
 __device__ uint32_t g_device_status;
@@ -574,10 +576,10 @@ situ_status moe_forward_impl(const void* x, const int32_t* expert_offsets,
   int32_t* units_dn = reinterpret_cast<int32_t*>(ws + 2 * prefix_bytes);
   void* x_perm = ws + 3 * prefix_bytes;
 
-  // Experts with many rows on average run as two-CTA MMAs (M = 256 over a CTA pair);
-  // with few rows (an expert's tail tile of at most 64 rows would cost a whole pair
-  // MMA) the one-CTA kernel with its 64-row MMAs is faster.
-  const bool two_cta = R >= 512 * static_cast<int64_t>(E) && gemm_two_cta_available();
+  // Experts averaging at least 128 rows run as two-CTA MMAs (M = 256 over a CTA pair; an
+  // expert's odd last m-tile as an M = 128 pair, 64 rows per CTA); experts of a few
+  // rows (decode) stream their weights through the one-CTA kernel's 64-row MMAs.
+  const bool two_cta = R >= kTwoCtaMinRows * static_cast<int64_t>(E) && gemm_two_cta_available();
   cudaError_t e = launch_group_tiles(expert_offsets, E, R, gemm_n_tiles_situ(I),
                                      gemm_n_tiles_wide(M), tile_offsets, units_gu, units_dn,
                                      st->status, cs, two_cta);
@@ -813,9 +815,9 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
   void* rows_m = ws + 4 * prefix_bytes;  // [R, M]: dy, then per-route dx, then x
   void* dgu = static_cast<uint8_t*>(rows_m) + round_up(static_cast<size_t>(R) * M * 2, 256);
   const SituParams p = make_situ_params(beta, linear_beta);
-  // The dh and dx GEMMs run as two-CTA MMAs when experts average >= 512 rows (as the
+  // The dh and dx GEMMs run as two-CTA MMAs when experts average >= 128 rows (as the
   // forward); the K-grouped weight gradients keep one CTA per tile.
-  const bool two_cta = R >= 512 * static_cast<int64_t>(E) && gemm_two_cta_available();
+  const bool two_cta = R >= kTwoCtaMinRows * static_cast<int64_t>(E) && gemm_two_cta_available();
   cudaError_t e = launch_group_tiles(expert_offsets, E, R, gemm_n_tiles_wide(I),
                                      gemm_n_tiles_wide(M), tile_offsets, units_dh, units_dx,
                                      st->status, cs, two_cta);

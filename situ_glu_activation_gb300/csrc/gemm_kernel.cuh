@@ -243,6 +243,9 @@ struct Args {
   __nv_bfloat16* out2;
   int32_t* h_ready;
   int32_t h_ready_target;
+  // Two-CTA grouped bf16 GEMMs: a group's odd last m-tile runs as an M = 128 pair
+  // (64 rows per CTA) instead of an M = 256 pair with a phantom half.
+  int32_t pair_tails;
 };
 
 struct SharedCtl {
@@ -262,6 +265,7 @@ struct TileCoord {
   int32_t row_end;  // one past the last valid A row (group end)
   int32_t group;
   int32_t n_tile;
+  int32_t half_pair;  // two-CTA M = 128 pair: this CTA holds 64 rows from a_row0
   int32_t k0;       // first K row of the contraction (K-grouped; 0 otherwise)
   int32_t k_end;    // one past its last K row (K-grouped)
   int32_t k_blocks; // k-blocks of this tile
@@ -282,6 +286,7 @@ __device__ __forceinline__ TileCoord decode_tile(const Args& a, int32_t t) {
     c.group = 0;
     c.a_row0 = mt * kBM;
     c.row_end = a.dense_rows;
+    c.half_pair = 0;
     return c;
   }
   // Largest g with tile_offsets[g] <= mt (empty groups repeat an offset; the
@@ -294,6 +299,7 @@ __device__ __forceinline__ TileCoord decode_tile(const Args& a, int32_t t) {
   c.group = lo;
   c.a_row0 = __ldg(a.group_offsets + lo) + (mt - __ldg(a.tile_offsets + lo)) * kBM;
   c.row_end = __ldg(a.group_offsets + lo + 1);
+  c.half_pair = 0;
   return c;
 }
 
@@ -306,6 +312,7 @@ __device__ __forceinline__ TileCoord in_group_tile(int32_t n_tiles, int32_t loca
   c.a_row0 = row0 + mt * kBM;
   c.row_end = row_end;
   c.group = 0;
+  c.half_pair = 0;
   return c;
 }
 
@@ -339,14 +346,18 @@ __device__ __forceinline__ int32_t round_unit(int32_t i, int32_t u0, int32_t str
   return i * stride + ((kSerpentine && (i & 1)) ? stride - 1 - u0 : u0);
 }
 
-// Two-CTA unit `local` of a dense GEMM: CTA r of the pair takes m-tile 2p + r of n-tile n
-// (a last pair past the rows computes fill that is not stored).
+// Two-CTA unit `local` of a group's rows row0 .. row_end-1: CTA r of the pair takes
+// m-tile 2p + r of n-tile n (a last pair past the rows computes fill that is not
+// stored).  With half-pair tails, a group's odd last m-tile (at most 128 rows) is an
+// M = 128 pair instead: CTA r takes its rows 64r .. 64r+63 (half_pair).
 __device__ __forceinline__ TileCoord pair_unit(int32_t n_tiles, int32_t local, uint32_t rank,
-                                               int32_t row_end) {
+                                               int32_t row0, int32_t row_end, bool tails) {
   TileCoord c;
   const int32_t p = local / n_tiles;
   c.n_tile = local - p * n_tiles;
-  c.a_row0 = (2 * p + static_cast<int32_t>(rank)) * kBM;
+  const int32_t m = (row_end - row0 + kBM - 1) / kBM;
+  c.half_pair = (tails && (m & 1) && 2 * p == m - 1) ? 1 : 0;
+  c.a_row0 = row0 + 2 * p * kBM + static_cast<int32_t>(rank) * (c.half_pair ? 64 : kBM);
   c.row_end = row_end;
   c.group = 0;
   return c;
@@ -361,7 +372,7 @@ __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_
     const int32_t local = p2 ? u - a.fused_units1 : u;
     const int32_t nt = p2 ? a.n_tiles2 : a.n_tiles;
     const int32_t rows = p2 ? a.dense_rows2 : a.dense_rows;
-    c = kPair ? pair_unit(nt, local, rank, rows) : in_group_tile(nt, local, 0, rows);
+    c = kPair ? pair_unit(nt, local, rank, 0, rows, false) : in_group_tile(nt, local, 0, rows);
     c.group = 0;
     c.k0 = 0;
     c.k_end = 0;
@@ -384,8 +395,7 @@ __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_
       row_end = __ldg(a.group_offsets + g + 1);
       local = u - __ldg(a.unit_offsets + g);
     }
-    c = pair_unit(a.n_tiles, local, rank, row_end);
-    c.a_row0 += row0;
+    c = pair_unit(a.n_tiles, local, rank, row0, row_end, a.pair_tails != 0);
     c.group = g;
     c.phase2 = 0;
     c.k0 = 0;
@@ -524,7 +534,8 @@ __host__ __device__ __forceinline__ int64_t sf_tile_offset(int64_t m_tile, int64
 }
 
 // kPair: clusters of two CTAs whose MMAs are tcgen05 cta_group::2 (M = 256 over the
-// pair); otherwise one CTA per tile with cta_group::1 MMAs.
+// pair, or M = 128 for a grouped GEMM's half-pair tail); otherwise one CTA per tile
+// with cta_group::1 MMAs.
 template <Epi kEpi, Caps kC, bool kPair, bool kStoreGu, Major kMajor, int kMx = 0>
 __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
@@ -561,6 +572,12 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
   // Contractions over rows (both operands MN-major) may be K-grouped.
   constexpr bool kKG = kMajor == Major::kABMNGrouped;
+  // A two-CTA M = 128 pair tile: a grouped bf16 GEMM's half-pair tail (K-major A; the
+  // launch passes the 64-row B box map in map_b2, which only two-GEMM launches use
+  // otherwise, and those have no half pairs).
+  auto pair_half_tile = [](const TileCoord& c) {
+    return k2Cta && kMx == 0 && !a_mn_major(kMajor) && c.half_pair != 0;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < G::Stages; ++s) {
@@ -683,20 +700,27 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
           if constexpr (k2Cta) {
             // This CTA's A rows and its half of B (K-major: one 128-row box; MN-major:
             // two {64, 64} atoms); both CTAs' copies count on the even CTA's barrier,
-            // which expects them all.
+            // which expects them all.  An M = 128 pair (half_pair) stages 64 A rows per
+            // CTA, and its SiTU tile's B half in CTA r is gate rows n0 + 64r .. +63 then
+            // the matching up rows, so each accumulator lane pairs gate and up columns.
+            const bool hp = pair_half_tile(tc);
             const uint32_t full0 = map_to_rank(full, 0);
-            if (rank == 0) mbar_arrive_expect_tx(full, G::TxBytes);
+            if (rank == 0) mbar_arrive_expect_tx(full, hp ? G::TxBytes - G::ABytes : G::TxBytes);
             const int32_t kxa = kb * G::BK + tc.k0, kxb2 = kb * G::BK + kb_off;
             const int32_t brow = rank == 0 ? b_row0 : b_row1;
             if constexpr (a_mn_major(kMajor)) {
               for (int j = 0; j < 2; ++j)
                 tma_load_2d_pair(sa + j * kMnAtomBytes, pm_a, tc.a_row0 + 64 * j, kxa, full0);
             } else {
-              tma_load_2d_pair(sa, pm_a, kxa, tc.a_row0, full0);
+              tma_load_2d_pair(sa, hp ? pm_a64 : pm_a, kxa, tc.a_row0, full0);
             }
             if constexpr (kMajor != Major::kKMajor) {
               for (int j = 0; j < 2; ++j)
                 tma_load_2d_pair(sb + j * kMnAtomBytes, pm_b, brow + 64 * j, kxb2, full0);
+            } else if (hp && situ_tile) {
+              const int32_t off = 64 * static_cast<int32_t>(rank);
+              tma_load_2d_pair(sb, &map_b2, kxb2, b_row0 + off, full0);
+              tma_load_2d_pair(sb + 64 * 128, &map_b2, kxb2, b_row1 + off, full0);
             } else {
               tma_load_2d_pair(sb, pm_b, kxb2, brow, full0);
             }
@@ -811,7 +835,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         const TileCoord tcm = unit_tile<kPair, kKG, kTwo>(args, t, rank);
         const uint32_t idesc = kMx      ? idesc_mxf8(k2Cta ? 2 * kBM : kBM, G::BN,
                                                 kMx == 2 ? kMxE2M1 : kMxE4M3)
-                               : (k2Cta ? idesc_bf16_f32(2 * kBM, G::BN)
+                               : (k2Cta ? idesc_bf16_f32(pair_half_tile(tcm) ? kBM : 2 * kBM, G::BN)
                                         : (tcm.row_end - tcm.a_row0 <= 64 ? kIdescHalf : kIdesc)) |
                                          (a_mn_major(kMajor) ? kAMnBit : 0u) |
                                          (kMajor != Major::kKMajor ? kBMnBit : 0u);
@@ -975,7 +999,12 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       // M=64 tiles (bf16 only): only the first 16 lanes of each quarter hold rows
       // (16q + lane).
       const bool half = !kMx && !k2Cta && tc.row_end - tc.a_row0 <= 64;
-      const int32_t row = tc.a_row0 + (half ? quarter * 16 + lane : row_in_tile);
+      // Two-CTA M = 128 pair: lane L holds this CTA's row L mod 64, accumulator columns
+      // 0..127 being the tile's columns 128 (L div 64) .. +127 (lh).
+      const bool hp = pair_half_tile(tc);
+      const int lh = hp ? (row_in_tile >> 6) : 0;
+      const int32_t row =
+          tc.a_row0 + (half ? quarter * 16 + lane : hp ? (row_in_tile & 63) : row_in_tile);
       bool valid = row < tc.row_end && (!half || lane < 16);
       int64_t out_row = row;
       // K-grouped: group g's result starts at output row g * out_group_rows; a
@@ -991,8 +1020,11 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       }
       const uint32_t t_acc = tmem_base + lane_addr + acc * G::BN;
       if (kSituEpi || (kFfn && !p2)) {
-        // Gate column j of the tile pairs with up column BN/2 + j.
+        // Gate column j of the tile pairs with up column BN/2 + j (a half pair: the
+        // lane's 64 gate columns, then their 64 up columns, are the activation's
+        // columns 64 lh .. +63 of the tile).
         constexpr int kHalfN = G::BN / 2;
+        const int pair_cols = hp ? 64 : kHalfN;
         __nv_bfloat16* dst_row = args.out + out_row * args.ldo;
         int64_t h_tile = 0;
         if constexpr (kEpi == Epi::kSituMx || (kFfn && kMx != 0)) {
@@ -1002,11 +1034,11 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
                        : tc.a_row0 / kBM;
         }
 #pragma unroll 1
-        for (int c = 0; c < kHalfN / 32; ++c) {
+        for (int c = 0; c < pair_cols / 32; ++c) {
           __syncwarp();  // tcgen05.ld is warp-collective (.sync.aligned)
           uint32_t g[32], u[32];
           tmem_ld32(t_acc + c * 32, g);
-          tmem_ld32(t_acc + kHalfN + c * 32, u);
+          tmem_ld32(t_acc + pair_cols + c * 32, u);
           tmem_ld_wait2(g, u);
           uint32_t w[16];
 #pragma unroll
@@ -1016,7 +1048,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
                 situ_act<kC>(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]),
                              args.sp));
           }
-          const int64_t col0 = static_cast<int64_t>(tc.n_tile) * kHalfN + c * 32;
+          const int64_t col0 = static_cast<int64_t>(tc.n_tile) * kHalfN + lh * 64 + c * 32;
           if constexpr (kEpi == Epi::kSituMx || (kFfn && kMx != 0)) {
             // h rounded to bf16 (w), then one 32-wide MXFP8 block: 32 codes and the
             // block's scale in the A-operand scale tiles of the next GEMM.
@@ -1062,8 +1094,10 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         // previous stores (whose asm carries a memory clobber) and the tile's epilogue
         // would serialise 32 global-load latencies.
         uint4 gq[4], uq[4];
+        // A half pair's lane holds 128 columns (4 chunks) starting at column 128 lh.
+        const int64_t col_base = static_cast<int64_t>(tc.n_tile) * G::BN + lh * 128;
         auto load_gu = [&](int c, uint4 (&gd)[4], uint4 (&ud)[4]) {
-          const int64_t col0 = static_cast<int64_t>(tc.n_tile) * G::BN + c * 32;
+          const int64_t col0 = col_base + c * 32;
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             const int64_t cv = col0 + 8 * v;
@@ -1077,7 +1111,8 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
           }
         };
         constexpr int kChunks = 8 / (epi_warps<kEpi>() / 4);  // chunks per warp
-        const int c_begin = col_group * kChunks, c_end = c_begin + kChunks;
+        const int chunks = hp ? kChunks / 2 : kChunks;
+        const int c_begin = col_group * chunks, c_end = c_begin + chunks;
         load_gu(c_begin, gq, uq);
 #pragma unroll 1
         for (int c = c_begin; c < c_end; ++c) {
@@ -1087,7 +1122,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
           uint32_t a[32];
           tmem_ld32(t_acc + c * 32, a);
           tmem_ld_wait(a);
-          const int64_t col0 = static_cast<int64_t>(tc.n_tile) * G::BN + c * 32;
+          const int64_t col0 = col_base + c * 32;
           if (valid) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -1124,7 +1159,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         const int64_t n_out = p2 ? args.n_out2 : args.n_out;
         __nv_bfloat16* dst_row = p2 ? args.out2 + out_row * args.ldo2 : args.out + out_row * args.ldo;
 #pragma unroll 1
-        for (int c = 0; c < G::BN / 32; ++c) {
+        for (int c = 0; c < (hp ? G::BN / 64 : G::BN / 32); ++c) {
           __syncwarp();
           uint32_t a[32];
           tmem_ld32(t_acc + c * 32, a);
@@ -1135,7 +1170,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
             w[i] = zero ? 0u
                         : pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
           }
-          const int64_t col0 = static_cast<int64_t>(tc.n_tile) * G::BN + c * 32;
+          const int64_t col0 = static_cast<int64_t>(tc.n_tile) * G::BN + lh * 128 + c * 32;
           if (kEpi == Epi::kPlain && args.combine_w) {
             // Fused combine: FP32 atomic adds of the weighted row (order-dependent
             // rounding).
@@ -1301,7 +1336,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     ok = ok && make_map(&mb, s.b, s.b_rows, s.K, G::BHalfRows, s.b_ld, kMx);
   }
   if (!ok) return cudaErrorInvalidValue;
-  Args a;
+  Args a{};
   a.num_groups = s.num_groups;
   a.group_offsets = s.group_offsets;
   a.tile_offsets = s.tile_offsets;
@@ -1364,8 +1399,18 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
         use2 ? max_pair_clusters<kEpi, kC, kStoreGu, kMajor, kMx>(smem_bytes_pair<kMx>()) : 0;
     if (s.pair_units && clusters2 == 0) return cudaErrorNotSupported;
     if (clusters2 > 0) {
-      // Unit (p, n) gives CTA r m-tile 2p + r of n-tile n (of its group).
+      // Unit (p, n) gives CTA r m-tile 2p + r of n-tile n (of its group).  Grouped bf16
+      // GEMMs with K-major A run each group's odd last m-tile as an M = 128 pair (64
+      // rows per CTA); its SiTU B halves are 64-row boxes (the map in the second-GEMM
+      // slot, unused by one-GEMM launches).
       a.unit_offsets = s.pair_units ? s.unit_offsets : nullptr;
+      CUtensorMap mb64 = mb;
+      if (kMx == 0 && !a_mn_major(kMajor) && s.pair_units) {
+        a.pair_tails = 1;
+        if (kMajor == Major::kKMajor &&
+            !make_map(&mb64, s.b, s.b_rows, s.K, 64, s.b_ld, 0))
+          return cudaErrorInvalidValue;
+      }
       if (dense) {
         const int64_t units = ((m_tiles + 1) / 2) * a.n_tiles;
         if (units < clusters2) clusters2 = static_cast<int>(units);
@@ -1383,7 +1428,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
       cfg.attrs = &attr;
       cfg.numAttrs = 1;
       return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx>,
-                                ma, ma64, mb, ma, ma64, mb, a);
+                                ma, ma64, mb, ma, ma64, mb64, a);
     }
   }
   // One CTA per tile, persistent: tiles in (group, m-tile, n-tile) order (K-grouped:

@@ -62,7 +62,7 @@ def test_reference_arm_json(capsys, monkeypatch):
 def test_reference_arm_other_ranks_do_nothing(capsys, monkeypatch):
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("WORLD_SIZE", "2")
-    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"]) == 0
+    assert bench.main(["--gpus", "2", "--impl", "reference", "--steps", "1", "--warmup", "3"]) == 0
     assert capsys.readouterr().out == ""
 
 
@@ -81,3 +81,15 @@ def test_peaks_and_traffic(tmp_path, monkeypatch):
     (tmp_path / "profiles" / "traffic.txt").write_text("# c\nk abc 2.5 row f.md\n")
     assert bench.profiled_traffic("k", "abc", 4) == 10.0
     assert bench.profiled_traffic("k", "old", 4) is None  # kernel changed since the capture
+
+
+def test_gpus_must_match_the_rank_count(monkeypatch):
+    """--gpus N needs N ranks (one process per GPU); a single process asked for more
+    GPUs refuses instead of quietly measuring one."""
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    with pytest.raises(SystemExit) as e:
+        bench.main(["--gpus", "2", "--impl", "reference", "--steps", "1", "--warmup", "3"])
+    assert e.value.code == 2
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    with pytest.raises(SystemExit):
+        bench.main(["--gpus", "1", "--impl", "reference", "--steps", "1", "--warmup", "3"])

@@ -91,8 +91,8 @@ def test_grouped_swiglu_variant(oracle, cuda_dev):
 
 @pytest.mark.parametrize("T,k,E,M,I,skew", [
     (64, 2, 4, 256, 256, False),    # few rows per expert: one-CTA kernel
-    # >= 512 rows per expert on average: two-CTA MMAs; skewed sizes give experts with
-    # odd m-tile counts, a partial last pair, one expert with no rows
+    # >= 128 rows per expert on average: two-CTA MMAs; skewed sizes give experts with
+    # odd m-tile counts (an M = 128 pair tail), one expert with no rows
     (1024, 2, 4, 512, 384, True),
 ])
 def test_grouped_equals_dense_per_expert(cuda_dev, T, k, E, M, I, skew):
@@ -112,6 +112,36 @@ def test_grouped_equals_dense_per_expert(cuda_dev, T, k, E, M, I, skew):
         ye = situ.situ_ffn_forward(x.to(cuda_dev), wgu[e].to(cuda_dev), wd[e].to(cuda_dev)).cpu()
         t_idx, s_idx = (ids == e).nonzero(as_tuple=True)
         assert torch.equal(y[t_idx, s_idx].view(torch.int16), ye[t_idx].view(torch.int16))
+
+
+@pytest.mark.parametrize("sizes", [
+    (228, 356, 300, 0, 77),   # odd m-tile counts with tails of 100, 44 and 77 rows
+    (129, 192, 64, 385, 1),   # tails of 1 and 64 rows, a 64-row expert, one row
+])
+def test_grouped_half_pair_tails(oracle, cuda_dev, sizes):
+    """Experts averaging >= 128 rows run two-CTA MMAs; an expert's odd last m-tile is an
+    M = 128 pair (64 rows per CTA, the second CTA's rows possibly all past the expert's
+    end).  Every row equals the dense FFN of its expert bit for bit, and sampled rows
+    match the oracle."""
+    E, M, I = len(sizes), 256, 384
+    ids = torch.cat([torch.full((n,), e, dtype=torch.int32) for e, n in enumerate(sizes)])
+    ids = ids[torch.randperm(ids.numel(), generator=torch.Generator().manual_seed(9))][:, None]
+    T = ids.shape[0]
+    assert T >= 128 * E  # the two-CTA schedule
+    x = wl.normal((T, M), 1.0, seed=10)
+    wgu, wd = wl.expert_weights(E, M, I, seed=11)
+    y = _grouped(x, ids, wgu, wd, cuda_dev).cpu()
+    for e in range(E):
+        if sizes[e] == 0:
+            continue
+        ye = situ.situ_ffn_forward(x.to(cuda_dev), wgu[e].to(cuda_dev), wd[e].to(cuda_dev)).cpu()
+        t_idx = (ids[:, 0] == e).nonzero(as_tuple=True)[0]
+        assert torch.equal(y[t_idx, 0].view(torch.int16), ye[t_idx].view(torch.int16)), e
+    rows = torch.arange(0, T, 7)
+    ref = oracle.moe_grouped_forward(oracle_input(x[rows]), ids[rows].numpy(), oracle_input(wgu),
+                                     oracle_input(wd))
+    assert_ffn_close(to_f64(y[rows]), ref, "grouped half-pair tails")
+    assert situ.device_status(clear=True) == 0
 
 
 _WEIGHTS = {}

@@ -143,8 +143,9 @@ def test_forward_train_matches_forward(oracle, cuda_dev):
 @pytest.mark.parametrize("T", [333, 1200])
 def test_grouped_backward_equals_dense_single_expert(cuda_dev, T):
     """One expert, one slot: the grouped backward runs the same tiles in the same
-    order as the dense backward, so every output is bit-identical (333 rows: the
-    one-CTA grouped kernels; 1200: two-CTA grouped dh and dx GEMMs)."""
+    order as the dense backward, so every output is bit-identical (333 rows: two-CTA
+    grouped dh and dx GEMMs whose third m-tile is an M = 128 pair, against the dense
+    kernels' M = 256 pair with a phantom half; 1200: whole pairs)."""
     M, I = 256, 384
     ids = torch.zeros(T, 1, dtype=torch.int32)
     x = wl.normal((T, M), 1.0, seed=31)
