@@ -588,6 +588,20 @@ situ_status situ_moe_combine(const void* y, const float* weights, void* out, int
  * ------------------------------------------------------------------------- */
 situ_status situ_selftest_bounded_wait(uint32_t limit_us, void* stream);
 
+/* -------------------------------------------------------------------------
+ * situ_set_wait_limit_ns -- bound of the GEMM kernels' waits (failure detection;
+ * no counterpart on the pages).  Every wait of the pipelined GEMM kernels (a stage's
+ * copies, an accumulator, the one-launch FFN's wait for another CTA's h rows) gives
+ * up after `ns` nanoseconds of wall time: the kernel then records SITU_ERR_TIMEOUT in
+ * the device status, drains its own copies and MMAs with bounded waits, frees its
+ * tensor memory and returns; the results of that call are undefined, the context
+ * stays usable.  Process-wide, read by each launch when it is enqueued; ns = 0
+ * restores the default of 10 s (far above any legitimate wait).  A bound shorter
+ * than the kernels' normal waits (a few microseconds) makes them time out: that is
+ * how the failure path is exercised.  Returns the previous bound.
+ * ------------------------------------------------------------------------- */
+uint64_t situ_set_wait_limit_ns(uint64_t ns);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,6 +24,7 @@ STATUS_NAMES = {
 _vp, _i64, _i32, _u32, _f32, _ci, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
                                           ctypes.c_uint32, ctypes.c_float, ctypes.c_int,
                                           ctypes.c_size_t)
+_u64 = ctypes.c_uint64
 SIGNATURES = {
     "situ_abi_version": ([], _ci),
     "situ_status_string": ([_ci], ctypes.c_char_p),
@@ -74,6 +75,7 @@ SIGNATURES = {
     "situ_moe_grouped_forward_mxfp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _vp, _vp, _sz,
                                         _i64, _i32, _i32, _i64, _i64, _f32, _f32, _vp], _ci),
     "situ_selftest_bounded_wait": ([_u32, _vp], _ci),
+    "situ_set_wait_limit_ns": ([_u64], _u64),
 }
 
 _lock = threading.Lock()

@@ -645,6 +645,12 @@ def device_status(clear: bool = True) -> int:
     return int(_native.lib().situ_device_status(1 if clear else 0))
 
 
+def set_wait_limit_ns(ns: int) -> int:
+    """Bound (ns of wall time) of every pipeline wait in the GEMM kernels launched from
+    now on; 0 restores the default of 10 s.  Returns the previous bound."""
+    return int(_native.lib().situ_set_wait_limit_ns(int(ns)))
+
+
 def selftest_bounded_wait(limit_us: int = 2000) -> None:
     """Launch the bounded-wait self test on the current stream."""
     check("situ_selftest_bounded_wait",
@@ -657,7 +663,7 @@ __all__ = [
     "situ_ffn_down",
     "situ_moe_build_index",
     "situ_moe_grouped_forward", "ffn_workspace_bytes", "moe_workspace_bytes",
-    "device_status", "selftest_bounded_wait", "ffn_host_workspace_bytes", "situ_moe_combine",
+    "device_status", "selftest_bounded_wait", "set_wait_limit_ns", "ffn_host_workspace_bytes", "situ_moe_combine",
     "ffn_last_path", "FFN_PATH_FUSED", "FFN_PATH_TWO_LAUNCHES", "ffn_set_single_launch",
     "situ_ffn_forward_train", "situ_ffn_backward", "ffn_backward_workspace_bytes",
     "situ_moe_grouped_forward_train", "situ_moe_grouped_backward", "moe_backward_workspace_bytes",

@@ -21,6 +21,10 @@ constexpr int kMaxDevices = 64;
 // Grouped bf16 GEMMs run two-CTA MMAs when the experts average at least this many rows.
 constexpr int64_t kTwoCtaMinRows = 128;
 
+// Bound of every pipeline wait in the GEMM kernels (situ_set_wait_limit_ns).
+constexpr uint64_t kDefaultWaitLimitNs = 10ull * 1000 * 1000 * 1000;  // 10 s
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+
 // Per-device status word: the first device-side failure since the last clear.
 __device__ uint32_t g_device_status;
 
@@ -1316,6 +1320,10 @@ situ_status situ_moe_combine(const void* y, const float* weights, void* out, int
                                static_cast<cudaStream_t>(stream)));
 }
 
+uint64_t situ_set_wait_limit_ns(uint64_t ns) {
+  return g_wait_limit_ns.exchange(ns == 0 ? kDefaultWaitLimitNs : ns);
+}
+
 situ_status situ_selftest_bounded_wait(uint32_t limit_us, void* stream) {
   if (limit_us < 1 || limit_us > 1000000) return SITU_ERR_ARG;
   DeviceState* st = nullptr;
@@ -1342,5 +1350,7 @@ situ_status current_device_context(int* num_sms, uint32_t** status) {
 }
 
 situ_status report_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 }  // namespace situ

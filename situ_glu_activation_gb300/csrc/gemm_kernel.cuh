@@ -64,8 +64,13 @@ constexpr int kUK = 16;   // K per tcgen05.mma for 16-bit inputs
 constexpr int kAccBufs = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kEpiThreads = 128;
-constexpr uint64_t kWaitLimitNs = 10ull * 1000 * 1000 * 1000;  // 10 s
-constexpr uint64_t kDrainLimitNs = 100ull * 1000 * 1000;       // 100 ms
+// Every wait of the pipeline is bounded by the launch's wait limit (wait_limit_ns(),
+// default 10 s); the drains after an abort by 100 ms.  After an abort, a CTA of a
+// two-CTA pair stays resident kAbortLingerNs before the final cluster barrier: its
+// operand copies complete on the even CTA's barriers, which it cannot wait on, and
+// the linger lets every copy it issued land while both CTAs' shared memory is live.
+constexpr uint64_t kDrainLimitNs = 100ull * 1000 * 1000;  // 100 ms
+constexpr uint64_t kAbortLingerNs = 1000ull * 1000;       // 1 ms
 constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
 // Tiles with at most 64 valid rows (an expert's tail, a small group) issue M=64
 // MMAs: half the tensor work.  Their accumulator rows 16q..16q+15 sit in TMEM lanes
@@ -246,6 +251,7 @@ struct Args {
   // Two-CTA grouped bf16 GEMMs: a group's odd last m-tile runs as an M = 128 pair
   // (64 rows per CTA) instead of an M = 256 pair with a phantom half.
   int32_t pair_tails;
+  uint64_t wait_limit_ns;  // bound of every pipeline wait (wall time)
 };
 
 struct SharedCtl {
@@ -256,6 +262,7 @@ struct SharedCtl {
   uint64_t drain;
   uint64_t sf_ready[kMaxStages];  // MXFP8: the stage's scales are in TMEM
   uint64_t sf_drain;
+  uint64_t wait_limit_ns;
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -437,9 +444,10 @@ __device__ __forceinline__ bool ctl_wait(SharedCtl* ctl, uint64_t* bar, uint32_t
   uint32_t polls = 0;
   while (true) {
     if (try_wait()) return true;
-    if ((++polls & 63u) == 0u) {
+    // Each try_wait may suspend the thread for a while: check the clock every few.
+    if ((++polls & 7u) == 0u) {
       if (ctl->abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > ctl->wait_limit_ns) {
         record_status(status, SITU_ERR_TIMEOUT);
         ctl->abort = 1;
         return false;
@@ -473,7 +481,7 @@ __device__ __forceinline__ bool wait_count(SharedCtl* ctl, const int32_t* p, int
     if (ld_acquire_gpu(p) >= target) return true;
     if ((++polls & 15u) == 0u) {
       if (ctl->abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > ctl->wait_limit_ns) {
         record_status(status, SITU_ERR_TIMEOUT);
         ctl->abort = 1;
         return false;
@@ -597,6 +605,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       mbar_init(smem_u32(&ctl->sf_drain), 1);
     }
     ctl->abort = 0;
+    ctl->wait_limit_ns = args.wait_limit_ns;
     fence_mbar_init();
     tma_prefetch_map(&map_a);
     if (!kPair) tma_prefetch_map(&map_a64);
@@ -1201,6 +1210,11 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
   }
 
   __syncthreads();
+  if (k2Cta && ctl->abort) {
+    // Aborted: let this CTA's copies that complete on the peer's barriers land.
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < kAbortLingerNs) __nanosleep(1000);
+  }
   // Paired: neither CTA leaves while the peer may still write into it.
   if (kPair) cluster_sync();
   if (warp == 1) {
@@ -1355,6 +1369,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
   a.out_row_index = s.out_row_index;
   a.sp = p;
   a.status = status;
+  a.wait_limit_ns = wait_limit_ns();
   a.gu_store = static_cast<__nv_bfloat16*>(s.gu_store);
   a.gu_in = static_cast<const __nv_bfloat16*>(s.gu_in);
   a.dgu_out = static_cast<__nv_bfloat16*>(s.dgu_out);
@@ -1494,6 +1509,7 @@ cudaError_t launch_ffn_fused_impl(const GemmShape& s_gu, const GemmShape& s_dn,
   a.out_rows = s_gu.a_rows;
   a.sp = p;
   a.status = status;
+  a.wait_limit_ns = wait_limit_ns();
   a.combine_k = 1;
   a.sfa = static_cast<const uint8_t*>(s_gu.sfa);
   a.sfb = static_cast<const uint8_t*>(s_gu.sfb);
@@ -1586,6 +1602,7 @@ cudaError_t launch_plain2_impl(const GemmShape& s1, const GemmShape& s2, uint32_
   a.ldo = s1.ldo;
   a.out_rows = s1.a_rows;
   a.status = status;
+  a.wait_limit_ns = wait_limit_ns();
   a.combine_k = 1;
   a.n_tiles2 = static_cast<int32_t>((s2.n_out + kBN - 1) / kBN);
   a.k_blocks2 = static_cast<int32_t>((s2.K + kBK - 1) / kBK);

@@ -219,6 +219,9 @@ cudaError_t launch_build_index(const int32_t* expert_ids, int32_t* offsets,
 namespace situ {
 
 // ----- shared with abi.cu ------------------------------------------------------
+// Wall-time bound of every pipeline wait in the GEMM kernels, read at each launch
+// (situ_set_wait_limit_ns; default 10 s).
+uint64_t wait_limit_ns();
 // SM count and device address of the status word of the current device (the
 // library's one-time per-device set-up runs on first use; it allocates nothing).
 situ_status current_device_context(int* num_sms, uint32_t** status);
