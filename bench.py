@@ -312,7 +312,9 @@ def bench_act(args, dev, peaks, world, flush):
                          "traffic": profiled_traffic("situ_act", digest, w.rows * w.I)}}
 
 
-def bench_moe(args, dev, peaks, world, flush, names):
+def bench_moe(args, dev, peaks, world, flush, names, cpu=False):
+    """Grouped workloads; cpu: also time the FP64 oracle on a sample of each one's
+    routes (host copies of the expert weights, made once per weight set)."""
     import torch
 
     import situ_glu_activation_gb300 as situ
@@ -320,12 +322,14 @@ def bench_moe(args, dev, peaks, world, flush, names):
 
     results = {}
     weights = {}
+    host_weights = {}
     for name in names:
         w = wl.WORKLOADS[name]
         E = w.num_experts
         key = (E, w.M, w.I)
         if key not in weights:
             weights.clear()
+            host_weights.clear()
             torch.cuda.empty_cache()
             weights[key] = wl.expert_weights(E, w.M, w.I, seed=0, device=dev)
         wgu, wd = weights[key]
@@ -381,8 +385,20 @@ def bench_moe(args, dev, peaks, world, flush, names):
             "launches_per_step": 3 + 4 + 1,
             "step": "expert index, grouped SiTU-GLU experts, router-weighted combine",
         }
+        if cpu:
+            wbytes_all = (wgu.numel() + wd.numel()) * 2
+            if key not in host_weights and host_bytes_available() > 2 * wbytes_all:
+                host_weights[key] = (wgu.cpu(), wd.cpu())
+            if key in host_weights:
+                results[name]["cpu_baseline"] = cpu_baseline_routes(w, x, ids_cpu,
+                                                                    *host_weights[key])
+            else:
+                results[name]["cpu_baseline"] = {
+                    "unavailable": f"host memory below twice the {wbytes_all / 1e9:.1f} GB of "
+                                   "expert weights the oracle needs"}
         del x, y, ws, off, tix, ids
     weights.clear()
+    host_weights.clear()
     torch.cuda.empty_cache()
     return results
 
@@ -596,45 +612,56 @@ def cpu_baseline(seconds: float, rows_hint: int = 0):
                       f"(FP64 gate_up, SiTU-GLU, down), {dt:.1f} s"}
 
 
-def cpu_baseline_moe(seconds: float):
-    """The FP64 oracle's grouped experts (as it stands) on a bounded sample of the
-    64-expert workload: the routes of the first tokens (top-8 Zipf), timed on the host
-    cores.  The oracle's work per route (6 M I multiply-adds) does not depend on which
-    expert a route uses, so the sample's experts are mapped onto 8 seeded expert weight
-    sets; routes/s and tokens/s (routes / 8) are extrapolated from the sample."""
+def route_sample(ids_cpu, n: int, seed: int = 0):
+    """A seeded sample of n flat routes (token * k_eff + slot) of ids [T, k_eff] that
+    covers every expert with at least one route: one route of each non-empty expert
+    (the first in a seeded permutation), then the permutation's next routes."""
+    import numpy as np
+
+    flat = ids_cpu.contiguous().view(-1).numpy()
+    order = np.random.default_rng(seed).permutation(flat.size)
+    _, first = np.unique(flat[order], return_index=True)
+    chosen = order[first]
+    rest = order[~np.isin(order, chosen)][: max(0, n - chosen.size)]
+    return np.sort(np.concatenate([chosen, rest]))
+
+
+def host_bytes_available() -> int:
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def cpu_baseline_routes(w, x, ids_cpu, wgu_host, wd_host, n_routes: int = 4096):
+    """The FP64 oracle's grouped experts (as it stands) on a seeded sample of n_routes
+    routes of a grouped workload covering every non-empty expert, each route with its
+    own expert's weights: the sampled routes run as a grouped call of one slot per
+    sampled route.  routes/s is measured; tokens/s = routes/s / k_eff is extrapolated."""
     import numpy as np
     import torch
 
     from oracle import Oracle
-    from situ_glu_activation_gb300 import workloads as wl
 
     o = Oracle()
-    w = wl.WORKLOADS["grouped"]
     bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
-    ids = wl.routes(w, seed=0)
-    E_s = 8
-    wgu, wd = wl.expert_weights(E_s, w.M, w.I, seed=0)
-    wgb, wdb = bits(wgu), bits(wd)
-    threads = o.num_threads()
-    n_tok = max(1, threads // 4)
-    x = wl.normal((w.T, w.M), 1.0, seed=0)
-    xb = bits(x)
-
-    def run(nt):
-        sub = (ids[:nt].numpy() % E_s).astype(np.int32)
-        t0 = time.perf_counter()
-        o.moe_grouped_forward(xb[:nt], sub, wgb, wdb)
-        return time.perf_counter() - t0
-
-    dt = run(n_tok)
-    if dt < seconds:
-        n_tok = min(w.T, max(n_tok, int(n_tok * seconds / max(dt, 1e-3))))
-        dt = run(n_tok)
-    routes = n_tok * w.k_eff
-    return {"value": n_tok / dt, "unit": "tokens/s", "routes_per_s": routes / dt,
-            "cores": threads, "kind": "oracle",
-            "sample": f"{routes} routes of the first {n_tok} tokens of the 64-expert Zipf top-8 "
-                      f"workload (FP64 grouped experts, per-route loop), {dt:.1f} s; "
+    sample = route_sample(ids_cpu, n_routes, seed=0)
+    tokens = torch.from_numpy(sample // w.k_eff)
+    ids_s = ids_cpu.contiguous().view(-1)[torch.from_numpy(sample)].view(-1, 1).numpy()
+    xs = bits(x.index_select(0, tokens.to(x.device)).cpu())
+    t0 = time.perf_counter()
+    o.moe_grouped_forward(xs, ids_s, bits(wgu_host), bits(wd_host))
+    dt = time.perf_counter() - t0
+    experts = int(np.unique(ids_s).size)
+    return {"value": sample.size / dt / w.k_eff, "unit": "tokens/s",
+            "routes_per_s": sample.size / dt, "cores": o.num_threads(), "kind": "oracle",
+            "sample": f"{sample.size} seeded routes of the workload covering all {experts} "
+                      f"non-empty experts, each with its own weights (FP64 grouped experts, "
+                      f"per-route loop), {dt:.1f} s; tokens/s = routes/s / {w.k_eff}, "
                       "extrapolated to the workload"}
 
 
@@ -718,7 +745,8 @@ def run_situ(args):
         elif args.suite == "mx_dense":
             res = bench_mx(args, dev, peaks, world, flush, names=())
         else:
-            res = bench_moe(args, dev, peaks, world, flush, [args.suite])[args.suite]
+            res = bench_moe(args, dev, peaks, world, flush, [args.suite],
+                            cpu=rank == 0 and world == 1 and not args.no_cpu_baseline)[args.suite]
         if rank == 0:
             print(json.dumps({"suite": args.suite, "steps": args.steps, "warmup": args.warmup,
                               "result": res, "device_status": situ.device_status(clear=True)}),
@@ -742,8 +770,10 @@ def run_situ(args):
     act = moe = mx = train = None
     if args.suite == "full":
         act = with_clocks(lambda: bench_act(args, dev, peaks, world, flush))
+        # The oracle's CPU baseline of the grouped workloads: rank 0 of a 1-GPU run.
+        cpu_moe = rank == 0 and world == 1 and not args.no_cpu_baseline
         moe = with_clocks(lambda: bench_moe(args, dev, peaks, world, flush,
-                                            ["grouped", "k3_decode", "k3_prefill"]))
+                                            ["grouped", "k3_decode", "k3_prefill"], cpu=cpu_moe))
         mx = with_clocks(lambda: bench_mx(args, dev, peaks, world, flush))
         train = with_clocks(lambda: bench_train(args, dev, peaks, world, flush))
         train["grouped"] = with_clocks(lambda: bench_moe_train(args, dev, peaks, world, flush))
@@ -824,8 +854,6 @@ def run_situ(args):
         line["train"] = train
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
-        if moe:
-            line["moe"]["grouped"]["cpu_baseline"] = cpu_baseline_moe(args.cpu_seconds / 2)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -1353,4 +1353,14 @@ situ_status report_cuda_error(cudaError_t e) { return cuda_fail(e); }
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
+situ_status ffn_arg_checks(situ_dtype dt, int64_t R, int64_t M, int64_t I, float beta,
+                           float linear_beta) {
+  return ffn_common_checks(dt, R, M, I, beta, linear_beta);
+}
+
+situ_status ffn_bf16_operand_checks(const void* x, const void* W_gate_up, const void* W_down,
+                                    int64_t M, int64_t I) {
+  return bf16_gemm_checks(x, W_gate_up, W_down, M, I);
+}
+
 }  // namespace situ

@@ -59,10 +59,9 @@ extern "C" situ_status situ_ffn_forward_noalloc(const void* x, const void* W_gat
                                                 int64_t M, int64_t I, float beta,
                                                 float linear_beta, situ_dtype dt,
                                                 void* stream) {
-  if ((dt != SITU_BF16 && dt != SITU_F32) || R < 0 || M < 1 || I < 1) return SITU_ERR_ARG;
-  auto cap_ok = [](float b) { return b == INFINITY || (b > 0.0f && b <= kMaxFiniteCap); };
-  if (!cap_ok(beta) || !cap_ok(linear_beta)) return SITU_ERR_ARG;
-  if (R == 0) return SITU_OK;
+  // The same checks as situ_ffn_forward, then the scratch limit.
+  situ_status s = ffn_arg_checks(dt, R, M, I, beta, linear_beta);
+  if (s != SITU_OK || R == 0) return s;
   if (!x || !W_gate_up || !W_down || !y) return SITU_ERR_ARG;
   const size_t esz = dtype_size(dt);
   // The limit of the built-in scratch: h is R x I elements.
@@ -74,7 +73,7 @@ extern "C" situ_status situ_ffn_forward_noalloc(const void* x, const void* W_gat
       ranges_overlap(y, y_bytes, W_down, static_cast<size_t>(M) * I * esz))
     return SITU_ERR_ALIAS;
   void* scratch = nullptr;
-  situ_status s = scratch_address(&scratch);
+  s = scratch_address(&scratch);
   if (s != SITU_OK) return s;
   int num_sms = 0;
   uint32_t* status = nullptr;
@@ -91,10 +90,8 @@ extern "C" situ_status situ_ffn_forward_noalloc(const void* x, const void* W_gat
                        static_cast<float*>(y), R, M, I, p, caps_of(beta, linear_beta), cs);
     return e == cudaSuccess ? SITU_OK : report_cuda_error(e);
   }
-  if (M % 8 || I % 8) return SITU_ERR_UNSUPPORTED;
-  if (!is_aligned(x, 16) || !is_aligned(W_gate_up, 16) || !is_aligned(W_down, 16) ||
-      !is_aligned(y, 16))
-    return SITU_ERR_ALIGN;
+  if ((s = ffn_bf16_operand_checks(x, W_gate_up, W_down, M, I)) != SITU_OK) return s;
+  if (!is_aligned(y, 16)) return SITU_ERR_ALIGN;
   GemmShape g{};
   g.a = x;
   g.a_rows = R;

@@ -222,6 +222,13 @@ namespace situ {
 // Wall-time bound of every pipeline wait in the GEMM kernels, read at each launch
 // (situ_set_wait_limit_ns; default 10 s).
 uint64_t wait_limit_ns();
+// The argument checks situ_ffn_forward applies: dtype, sizes, caps (SITU_ERR_ARG) and the
+// kernels' size limits (SITU_ERR_UNSUPPORTED); for bf16, M and I multiples of 8
+// (SITU_ERR_UNSUPPORTED) and 16-byte aligned x and weights (SITU_ERR_ALIGN).
+situ_status ffn_arg_checks(situ_dtype dt, int64_t R, int64_t M, int64_t I, float beta,
+                           float linear_beta);
+situ_status ffn_bf16_operand_checks(const void* x, const void* W_gate_up, const void* W_down,
+                                    int64_t M, int64_t I);
 // SM count and device address of the status word of the current device (the
 // library's one-time per-device set-up runs on first use; it allocates nothing).
 situ_status current_device_context(int* num_sms, uint32_t** status);

@@ -93,3 +93,20 @@ def test_gpus_must_match_the_rank_count(monkeypatch):
     monkeypatch.setenv("WORLD_SIZE", "2")
     with pytest.raises(SystemExit):
         bench.main(["--gpus", "1", "--impl", "reference", "--steps", "1", "--warmup", "3"])
+
+
+def test_route_sample_covers_every_expert():
+    """The grouped CPU baseline's sample: n distinct routes, seeded, with at least one
+    route of every expert that has routes."""
+    import numpy as np
+    import torch
+
+    g = torch.Generator().manual_seed(3)
+    ids = torch.randint(0, 50, (300, 4), generator=g, dtype=torch.int32)
+    ids[ids == 7] = 8  # expert 7 without routes
+    s = bench.route_sample(ids, 64, seed=0)
+    flat = ids.view(-1).numpy()
+    assert s.size == 64 and np.unique(s).size == 64 and (np.diff(s) > 0).all()
+    assert set(np.unique(flat[s])) == set(np.unique(flat))
+    assert np.array_equal(s, bench.route_sample(ids, 64, seed=0))
+    assert bench.route_sample(ids, 10, seed=0).size == np.unique(flat).size  # all experts kept
