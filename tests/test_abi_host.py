@@ -174,3 +174,16 @@ def test_size_limits(situ_lib):
     assert m(*q, 4, 2, 65536, 8, 16384, 4.0, 25.0, 0, None) == UNSUP  # E * 2I = 2^31
     assert m(*q, 4, 2, 65536, 32768, 8, 4.0, 25.0, 0, None) == UNSUP  # E * M = 2^31
     assert m(*q, 4, 2, 65537, 8, 8, 4.0, 25.0, 0, None) == BAD        # more than 65536 experts
+
+
+def test_wait_limit_setting(situ_lib):
+    """The GEMMs' wait bound is a process-wide setting: 10 s by default, 0 restores it,
+    and each call returns the previous bound."""
+    default = 10 * 1000 * 1000 * 1000
+    first = situ_lib.situ_set_wait_limit_ns(5000)
+    try:
+        assert first == default
+        assert situ_lib.situ_set_wait_limit_ns(0) == 5000
+        assert situ_lib.situ_set_wait_limit_ns(0) == default
+    finally:
+        situ_lib.situ_set_wait_limit_ns(first)
