@@ -148,6 +148,18 @@ template <>
 struct GeoPairT<2> : GeoPairT<1> {
   static constexpr uint32_t TxBytes = 2 * (ABytes + BBytes / 2) + SfBytes;  // B arrives packed
 };
+// The two-CTA activation-derivative GEMM (dh): five operand stages, and kGuSlots
+// 16 KB slots in which a loader warp stages the saved (g, u) of the epilogue's
+// 32-column chunks ahead of the accumulator.  A slot holds the chunk's g columns for
+// the CTA's 128 rows (64 bytes a row), then its u columns, each with the 64-byte
+// swizzle: 16-byte piece v of slot row r sits at piece v ^ ((r >> 1) & 3) of the row,
+// so that eight threads reading piece v of eight consecutive rows hit distinct banks.
+struct GeoPairBwd : GeoPair {
+  static constexpr int Stages = 5;
+};
+constexpr int kGuSlots = 4;
+constexpr uint32_t kGuSlotBytes = 16384;
+constexpr uint32_t kGuHalfBytes = kGuSlotBytes / 2;  // the g (or u) part of a slot
 constexpr int kMaxStages = 7;
 // MXFP8 scale tiles.  The block-scaled MMA reads the E8M0 scale of A row m for its
 // k-th 32-wide K block (k = 0..3 within a 128-K stage) from TMEM lane m, column
@@ -176,19 +188,20 @@ constexpr uint32_t kSfTmemCols = 12;  // per stage: A 4 columns, B 8 columns
 enum class Epi { kSitu, kPlain, kSituBwd, kSituMx, kFfn, kPlain2 };
 
 // Epilogue warps: 4 (one per TMEM lane quarter), or 8 for the activation-derivative
-// epilogue, whose per-element work (six SFU ops, ~40 FP32 ops, the saved (g, u) loads
-// and the d(g, u) stores) matches the tile's MMAs: with one warp per SM sub-partition
-// its latency was exposed (the dh GEMM ran at 40 % of the dx GEMM's rate, measured on
-// GB300).  With 8, warps e and e + 4 share a lane quarter and split the columns.
+// epilogue, whose per-element work (eight SFU ops, about 30 FP32 ops, the saved (g, u)
+// reads and the d(g, u) stores) is of the order of the tile's MMAs: with one warp per SM
+// sub-partition its latency was exposed (the dh GEMM ran at 40 % of the dx GEMM's rate,
+// measured on GB300).  With 8, warps e and e + 4 share a lane quarter and split the
+// columns.
 template <Epi kEpi>
 __host__ __device__ constexpr int epi_warps() {
   return kEpi == Epi::kSituBwd ? 8 : 4;
 }
 // Threads per CTA: producer and MMA warps, the epilogue warps, and (MXFP8) the scale
-// copier.
+// copier or (activation derivative) the loader of the saved (g, u).
 template <Epi kEpi, int kMx>
 __host__ __device__ constexpr int block_threads() {
-  return 32 * (2 + epi_warps<kEpi>() + (kMx ? 1 : 0));
+  return 32 * (2 + epi_warps<kEpi>() + ((kMx || kEpi == Epi::kSituBwd) ? 1 : 0));
 }
 
 struct Args {
@@ -262,6 +275,8 @@ struct SharedCtl {
   uint64_t drain;
   uint64_t sf_ready[kMaxStages];  // MXFP8: the stage's scales are in TMEM
   uint64_t sf_drain;
+  uint64_t gu_full[kGuSlots];   // dh GEMM: a slot's saved (g, u) have landed
+  uint64_t gu_empty[kGuSlots];  // dh GEMM: the epilogue warps have read the slot
   uint64_t wait_limit_ns;
   uint32_t tmem_base;
   volatile int abort;
@@ -553,10 +568,15 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
                     const __grid_constant__ CUtensorMap map_a2_64,
                     const __grid_constant__ CUtensorMap map_b2, const Args args) {
   constexpr bool k2Cta = kPair;
-  using G = std::conditional_t<k2Cta, GeoPairT<kMx>, Geo<kMx>>;
+  // The two-CTA dh GEMM stages the saved (g, u) through shared memory (a loader warp);
+  // its one-CTA form reads them from global memory in the epilogue.
+  constexpr bool kGuStage = k2Cta && kEpi == Epi::kSituBwd;
+  using G = std::conditional_t<k2Cta,
+                               std::conditional_t<kGuStage, GeoPairBwd, GeoPairT<kMx>>, Geo<kMx>>;
+  constexpr uint32_t kGuBytes = kGuStage ? kGuSlots * kGuSlotBytes : 0u;
   static_assert(!k2Cta || kMajor != Major::kABMNGrouped,
                 "two-CTA MMA: GEMMs without a K-grouped contraction");
-  static_assert(G::Stages * G::StageBytes + sizeof(SharedCtl) + 1024 <= 232448,
+  static_assert(G::Stages * G::StageBytes + kGuBytes + sizeof(SharedCtl) + 1024 <= 232448,
                 "shared memory per CTA");
   static_assert(!kMx || 2 * G::BN + kSfTmemCols * G::Stages <= kTmemCols,
                 "accumulators and scale slots fit in tensor memory");
@@ -566,7 +586,9 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
   // 1024-byte alignment for the swizzled operand buffers.
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + G::Stages * G::StageBytes);
+  // Operand stages, then (dh GEMM) the (g, u) slots, then the control block.
+  uint8_t* gu_smem = smem + G::Stages * G::StageBytes;
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(gu_smem + kGuBytes);
   constexpr bool kSituEpi = kEpi == Epi::kSitu || kEpi == Epi::kSituMx;
   constexpr bool kFfn = kEpi == Epi::kFfn;
   static_assert(!kFfn || kMajor == Major::kKMajor, "the one-launch FFN is K-major");
@@ -604,6 +626,13 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       for (int s = 0; s < G::Stages; ++s) mbar_init(smem_u32(&ctl->sf_ready[s]), 1);
       mbar_init(smem_u32(&ctl->sf_drain), 1);
     }
+    if (kGuStage) {
+      for (int s = 0; s < kGuSlots; ++s) {
+        mbar_init(smem_u32(&ctl->gu_full[s]), 1);
+        // Every thread of the column group that reads the slot (half the epilogue).
+        mbar_init(smem_u32(&ctl->gu_empty[s]), 16 * epi_warps<kEpi>());
+      }
+    }
     ctl->abort = 0;
     ctl->wait_limit_ns = args.wait_limit_ns;
     fence_mbar_init();
@@ -614,6 +643,11 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       tma_prefetch_map(&map_a2);
       if (!kPair) tma_prefetch_map(&map_a2_64);
       tma_prefetch_map(&map_b2);
+    }
+    if (kGuStage) {
+      // The dh GEMM's saved-(g, u) maps ride in the second-GEMM slots.
+      tma_prefetch_map(&map_a2);
+      tma_prefetch_map(&map_a2_64);
     }
   }
   if (warp == 1) {
@@ -981,6 +1015,69 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         mbar_wait(smem_u32(&ctl->sf_drain), 0, nullptr, kDrainLimitNs);
       }
     }
+  } else if (kGuStage && warp == 2 + epi_warps<kEpi>()) {
+    // ---------------- saved (g, u) loader (two-CTA dh GEMM) ----------------
+    // For each unit, the epilogue's 32-column chunks in the order in which the two
+    // column groups of epilogue warps take them (group 0's first chunk, group 1's
+    // first, group 0's second, ...), each into the next slot once the threads that
+    // read its previous contents have arrived.  A slot takes this CTA's rows of the
+    // chunk (an M = 128 pair: slot rows 0..63 are the CTA's 64 rows at the tile's
+    // column offset 0, rows 64..127 the same rows at offset 128, the columns of the
+    // accumulator lanes 64..127).  A CTA whose rows all lie past its group's end
+    // (the idle half of a group's last pair) loads nothing and only arrives.
+    if (lane == 0) {
+      uint32_t seq = 0;  // chunks issued
+      bool ok = true;
+      const int32_t split = static_cast<int32_t>(args.split);
+      for (int32_t i = 0; i * ustride < n_total && ok; ++i) {
+        const int32_t t = round_unit<kKG>(i, u0, ustride);
+        if (t >= n_total) continue;
+        const TileCoord tc = unit_tile<kPair, kKG, kTwo>(args, t, rank);
+        const bool hp = pair_half_tile(tc);
+        const bool rows = tc.a_row0 < tc.row_end;
+        const int per_group = hp ? 2 : 4;
+        const int32_t col_base = tc.n_tile * G::BN;
+        for (int j = 0; j < per_group && ok; ++j) {
+          for (int cg = 0; cg < 2; ++cg, ++seq) {
+            const uint32_t slot = seq % kGuSlots;
+            if (!ctl_wait(ctl, &ctl->gu_empty[slot], ((seq / kGuSlots) & 1u) ^ 1u,
+                          args.status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t full = smem_u32(&ctl->gu_full[slot]);
+            if (!rows) {
+              mbar_arrive(full);
+              continue;
+            }
+            mbar_arrive_expect_tx(full, kGuSlotBytes);
+            const uint32_t dst = smem_u32(gu_smem + slot * kGuSlotBytes);
+            const int32_t x = col_base + (cg * per_group + j) * 32;
+            if (hp) {
+              for (int h = 0; h < 2; ++h) {
+                tma_load_2d(dst + h * (kGuHalfBytes / 2), &map_a2_64, x + 128 * h, tc.a_row0,
+                            full);
+                tma_load_2d(dst + kGuHalfBytes + h * (kGuHalfBytes / 2), &map_a2_64,
+                            split + x + 128 * h, tc.a_row0, full);
+              }
+            } else {
+              tma_load_2d(dst, &map_a2, x, tc.a_row0, full);
+              tma_load_2d(dst + kGuHalfBytes, &map_a2, split + x, tc.a_row0, full);
+            }
+          }
+        }
+      }
+      if (!ok || ctl->abort) {
+        // Aborted: wait (bounded) for the copies of the last slots issued, which land in
+        // this CTA's shared memory, before the CTA may leave.
+        const uint32_t n = seq < static_cast<uint32_t>(kGuSlots) ? seq : kGuSlots;
+        for (uint32_t k = 1; k <= n; ++k) {
+          const uint32_t sq = seq - k;
+          mbar_wait(smem_u32(&ctl->gu_full[sq % kGuSlots]), (sq / kGuSlots) & 1u, nullptr,
+                    kDrainLimitNs);
+        }
+      }
+    }
   } else if (warp >= 2 && warp < 2 + epi_warps<kEpi>()) {
     // ---------------- epilogue (warps 2 .. 2 + epi_warps - 1) ----------------
     const int quarter = warp & 3;  // TMEM lanes this warp may access
@@ -990,6 +1087,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
     const int row_in_tile = quarter * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     uint32_t local = 0;
+    uint32_t gseq = 0;  // dh GEMM: (g, u) chunks of the units before this one
     for (int32_t i = 0; i * ustride < n_total; ++i, ++local) {
       const int32_t t = round_unit<kKG>(i, u0, ustride);
       if (t >= n_total) {
@@ -1095,6 +1193,71 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
           if (threadIdx.x == 64 && tc.n_tile < args.n_tiles && tc.a_row0 < tc.row_end)
             red_release_add_gpu(args.h_ready + tc.a_row0 / kBM, 1);
         }
+      } else if (kGuStage) {
+        // The saved (g, u) of each chunk come from the slot the loader filled: this
+        // thread's slot row is its accumulator lane.  It reads its 64 bytes of g and of
+        // u, releases the slot, then forms and stores d(g, u).
+        __nv_bfloat16* dgu_row = args.dgu_out + static_cast<int64_t>(row) * 2 * args.split;
+        const int64_t col_base = static_cast<int64_t>(tc.n_tile) * G::BN + lh * 128;
+        const int chunks = hp ? 2 : 4;
+        const uint32_t srow = static_cast<uint32_t>(row_in_tile) * 64u;
+        const uint32_t swz = static_cast<uint32_t>((row_in_tile >> 1) & 3);
+        bool gu_ok = true;
+#pragma unroll 1
+        for (int j = 0; j < chunks; ++j) {
+          const uint32_t seq = gseq + 2 * j + col_group;
+          const uint32_t slot = seq % kGuSlots, par = (seq / kGuSlots) & 1u;
+          int w = 1;
+          if (lane == 0) w = ctl_wait(ctl, &ctl->gu_full[slot], par, args.status) ? 1 : 0;
+          w = __shfl_sync(0xFFFFFFFFu, w, 0);
+          if (!w) {
+            gu_ok = false;
+            break;
+          }
+          // Each lane's own acquire of the landed bytes (the phase is complete: one try).
+          (void)mbar_try_wait(smem_u32(&ctl->gu_full[slot]), par);
+          const int c = col_group * chunks + j;
+          __syncwarp();  // tcgen05.ld is warp-collective
+          uint32_t a[32];
+          tmem_ld32(t_acc + c * 32, a);
+          const uint32_t sg = smem_u32(gu_smem + slot * kGuSlotBytes) + srow;
+          uint4 gq[4], uq[4];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint32_t piece = 16u * (static_cast<uint32_t>(v) ^ swz);
+            gq[v] = ld_shared_v4(sg + piece);
+            uq[v] = ld_shared_v4(sg + kGuHalfBytes + piece);
+          }
+          mbar_arrive(smem_u32(&ctl->gu_empty[slot]));
+          tmem_ld_wait(a);
+          const int64_t col0 = col_base + c * 32;
+          if (valid) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int64_t cv = col0 + 8 * v;
+              if (cv + 8 > args.n_out) continue;
+              const uint32_t gw[4] = {gq[v].x, gq[v].y, gq[v].z, gq[v].w};
+              const uint32_t uw[4] = {uq[v].x, uq[v].y, uq[v].z, uq[v].w};
+              uint32_t og[4], ou[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float pg0, pu0, pg1, pu1;
+                situ_act_grad<kC>(__uint_as_float(gw[e] << 16), __uint_as_float(uw[e] << 16),
+                                  args.sp, pg0, pu0);
+                situ_act_grad<kC>(__uint_as_float(gw[e] & 0xFFFF0000u),
+                                  __uint_as_float(uw[e] & 0xFFFF0000u), args.sp, pg1, pu1);
+                const float dh0 = __uint_as_float(a[8 * v + 2 * e]);
+                const float dh1 = __uint_as_float(a[8 * v + 2 * e + 1]);
+                og[e] = pack_bf16x2(dh0 * pg0, dh1 * pg1);
+                ou[e] = pack_bf16x2(dh0 * pu0, dh1 * pu1);
+              }
+              st_global_v4(dgu_row + cv, og[0], og[1], og[2], og[3]);
+              st_global_v4(dgu_row + args.split + cv, ou[0], ou[1], ou[2], ou[3]);
+            }
+          }
+        }
+        gseq += 2u * static_cast<uint32_t>(chunks);
+        if (!gu_ok) break;
       } else if (kEpi == Epi::kSituBwd) {
         const __nv_bfloat16* gu_row = args.gu_in + static_cast<int64_t>(row) * 2 * args.split;
         __nv_bfloat16* dgu_row = args.dgu_out + static_cast<int64_t>(row) * 2 * args.split;
@@ -1266,6 +1429,24 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over the saved pre-activation pair, bf16 [rows, cols] row-major (cols = 2 *
+// split: g columns, then u columns): {32 columns, box_rows} boxes, 64 bytes a box row
+// in shared memory with the 64-byte swizzle (16-byte piece v of box row r lands at
+// piece v ^ ((r >> 1) & 3)), zero fill out of bounds.
+bool make_map_gu(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
+                 uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int kMx>
 constexpr size_t smem_bytes() {
   return Geo<kMx>::Stages * Geo<kMx>::StageBytes + sizeof(SharedCtl) + 1024;
@@ -1275,6 +1456,15 @@ template <int kMx = 0>
 constexpr size_t smem_bytes_pair() {
   return GeoPairT<kMx>::Stages * GeoPairT<kMx>::StageBytes + sizeof(SharedCtl) + 1024;
 }
+// Shared memory of a two-CTA kernel of epilogue kEpi: the dh GEMM's five stages and
+// (g, u) slots, or the pair geometry's stages.
+template <Epi kEpi, int kMx = 0>
+constexpr size_t smem_bytes_pair_epi() {
+  return kEpi == Epi::kSituBwd ? GeoPairBwd::Stages * GeoPairBwd::StageBytes +
+                                     kGuSlots * kGuSlotBytes + sizeof(SharedCtl) + 1024
+                               : smem_bytes_pair<kMx>();
+}
+static_assert(smem_bytes_pair_epi<Epi::kSituBwd>() <= 232448, "shared memory per CTA");
 static_assert(smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448 &&
                   smem_bytes<0>() <= 232448 && smem_bytes_pair<0>() <= 232448 &&
                   smem_bytes_pair<1>() <= 232448 && smem_bytes_pair<2>() <= 232448,
@@ -1399,7 +1589,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     if constexpr (k2Cta) {
       e = cudaFuncSetAttribute(ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem_bytes_pair<kMx>()));
+                               static_cast<int>(smem_bytes_pair_epi<kEpi, kMx>()));
       if (e != cudaSuccess) return e;
     }
     smem_set[dev].store(true, std::memory_order_release);
@@ -1411,7 +1601,9 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
                        !s.out_row_index && !s.combine_w;
     const bool use2 = dense || (s.pair_units && s.unit_offsets && !s.k_group_offsets);
     int clusters2 =
-        use2 ? max_pair_clusters<kEpi, kC, kStoreGu, kMajor, kMx>(smem_bytes_pair<kMx>()) : 0;
+        use2 ? max_pair_clusters<kEpi, kC, kStoreGu, kMajor, kMx>(
+                   smem_bytes_pair_epi<kEpi, kMx>())
+             : 0;
     if (s.pair_units && clusters2 == 0) return cudaErrorNotSupported;
     if (clusters2 > 0) {
       // Unit (p, n) gives CTA r m-tile 2p + r of n-tile n (of its group).  Grouped bf16
@@ -1426,6 +1618,13 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
             !make_map(&mb64, s.b, s.b_rows, s.K, 64, s.b_ld, 0))
           return cudaErrorInvalidValue;
       }
+      // The dh GEMM: maps over the saved (g, u) for its loader warp (128- and 64-row
+      // boxes), in the second-GEMM slots.
+      CUtensorMap mg = ma, mg64 = ma64;
+      if (kEpi == Epi::kSituBwd &&
+          !(make_map_gu(&mg, s.gu_in, s.a_rows, 2 * s.split, 128) &&
+            make_map_gu(&mg64, s.gu_in, s.a_rows, 2 * s.split, 64)))
+        return cudaErrorInvalidValue;
       if (dense) {
         const int64_t units = ((m_tiles + 1) / 2) * a.n_tiles;
         if (units < clusters2) clusters2 = static_cast<int>(units);
@@ -1433,7 +1632,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * clusters2, 1, 1);
       cfg.blockDim = dim3(block_threads<kEpi, kMx>(), 1, 1);
-      cfg.dynamicSmemBytes = smem_bytes_pair<kMx>();
+      cfg.dynamicSmemBytes = smem_bytes_pair_epi<kEpi, kMx>();
       cfg.stream = stream;
       cudaLaunchAttribute attr;
       attr.id = cudaLaunchAttributeClusterDimension;
@@ -1443,7 +1642,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
       cfg.attrs = &attr;
       cfg.numAttrs = 1;
       return cudaLaunchKernelEx(&cfg, ffn_gemm_kernel<kEpi, kC, true, kStoreGu, kMajor, kMx>,
-                                ma, ma64, mb, ma, ma64, mb64, a);
+                                ma, ma64, mb, mg, mg64, mb64, a);
     }
   }
   // One CTA per tile, persistent: tiles in (group, m-tile, n-tile) order (K-grouped:

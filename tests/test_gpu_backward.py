@@ -81,6 +81,55 @@ def test_backward_variants(oracle, cuda_dev, caps):
     _check_backward(oracle, x, wgu, wd, dy, dx, dwg, dwd, caps=oc, what=str(caps))
 
 
+@pytest.mark.parametrize("R,M,I,caps", [(300, 512, 384, (4.0, 25.0)),
+                                         (77, 136, 200, (4.0, 25.0)),
+                                         (130, 256, 256, (INF, INF)),
+                                         (130, 256, 256, (4.0, INF)),
+                                         (130, 256, 256, (INF, 25.0))],
+                         ids=["situ", "situ_ragged", "swiglu", "up_uncapped", "gate_uncapped"])
+def test_dgu_elementwise(oracle, cuda_dev, R, M, I, caps):
+    """The dh GEMM's activation-derivative epilogue, element by element: d(g, u) (left in
+    the workspace) against dh = dy W_down (library matmul of the exact bf16 values) times
+    the oracle's partial derivatives at the saved bf16 (g, u).
+
+    Bound: the bf16 rounding of the result and the relative error of the FP32 partials
+    (2^-8 |ref| covers both); for dg, the error of a'(g)'s two terms, each with a relative
+    error of about 2^-11 from the hardware tanh, taken against their absolute sizes
+    sigmoid(g) + |a(g)| sigmoid(-g) (2^-9 |dh| |b(u)| times that, where a'(g) cancels);
+    and the FP32 accumulation of dh (2^-12 of its sum of absolute terms)."""
+    x, wgu, wd, dy, (xd, wgud, wdd, dyd) = _inputs(R, M, I, 3 * R + I, cuda_dev)
+    _, gu, h = situ.situ_ffn_forward_train(xd, wgud, wdd, *caps)
+    ws = torch.empty(situ.ffn_backward_workspace_bytes(R, M, I), dtype=torch.uint8,
+                     device=cuda_dev)
+    situ.situ_ffn_backward(xd, wgud, wdd, gu, h, dyd, *caps, workspace=ws)
+    torch.cuda.synchronize()
+    assert situ.device_status(clear=True) == 0
+    dgu = to_f64(ws[: R * 2 * I * 2].view(torch.bfloat16).view(R, 2 * I).cpu())
+    assert np.isfinite(dgu).all()
+    b1, b2 = (0.0 if c == INF else c for c in caps)
+    guf = to_f64(gu.cpu())
+    dh = to_f64(dy) @ to_f64(wd)
+    dh_abs = np.abs(to_f64(dy)) @ np.abs(to_f64(wd))
+    pg = np.empty((R, I))
+    pu = np.empty((R, I))
+    gate_terms = np.empty((R, I))
+    up_abs = np.empty((R, I))
+    for r in range(R):
+        for j in range(I):
+            g, u = guf[r, j], guf[r, I + j]
+            pg[r, j], pu[r, j] = oracle.pair_grad(g, u, b1, b2)
+            gate_terms[r, j] = oracle.sigmoid(g) + abs(oracle.gate(g, b1)) * oracle.sigmoid(-g)
+            up_abs[r, j] = abs(oracle.up(u, b2))
+    for got, part, extra, what in ((dgu[:, :I], pg, 2.0 ** -9 * np.abs(dh) * up_abs * gate_terms,
+                                    "dg"),
+                                   (dgu[:, I:], pu, 0.0, "du")):
+        ref = dh * part
+        tol = 2.0 ** -8 * np.abs(ref) + extra + 2.0 ** -12 * dh_abs * np.abs(part)
+        err = np.abs(got - ref)
+        assert (err <= tol).all(), f"{what} {R}x{M}x{I} {caps}: worst err/tol " \
+                                   f"{float((err / np.maximum(tol, 1e-300)).max()):.3g}"
+
+
 def test_backward_full_size_sparse_dy(oracle, cuda_dev):
     """The 16384-token workload (M=2048, I=3072) at full size, with dy nonzero on 16
     seeded rows only: every other row contributes exactly zero, so the oracle's

@@ -160,6 +160,26 @@ def test_grouped_backward_equals_dense_single_expert(cuda_dev, T):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+@pytest.mark.parametrize("M,I", [(256, 384), (136, 200)])
+def test_grouped_backward_two_cta_tails(oracle, cuda_dev, M, I):
+    """Experts averaging >= 128 routes run the two-CTA dh and dx GEMMs: whole pairs, an
+    expert's odd last m-tile as an M = 128 pair (333 routes: its second CTA holds 13
+    rows; 129: one row; 64: no rows), an empty expert, and (I = 200) a ragged last
+    32-column chunk of the saved (g, u).  Every gradient against the oracle."""
+    sizes = [333, 129, 0, 200, 64]
+    E = len(sizes)
+    ids = torch.cat([torch.full((n,), e, dtype=torch.int32) for e, n in enumerate(sizes)])
+    ids = ids[torch.randperm(ids.numel(), generator=torch.Generator().manual_seed(41))][:, None]
+    T = ids.shape[0]
+    assert T >= 128 * E
+    x = wl.normal((T, M), 1.0, seed=42)
+    wgu, wd = wl.expert_weights(E, M, I, seed=43)
+    dy = wl.normal((T, 1, M), 1.0, seed=44)
+    _, got = _train_step(x, ids, wgu, wd, dy, cuda_dev)
+    assert not got[1][2].any() and not got[2][2].any()  # the empty expert
+    _check(oracle, x, ids, wgu, wd, dy, got, what=f"two-CTA tails M={M} I={I}")
+
+
 def test_grouped_backward_no_routes(cuda_dev):
     E, M, I = 3, 64, 64
     x = torch.empty(0, M, dtype=torch.bfloat16, device=cuda_dev)
