@@ -276,7 +276,7 @@ struct SharedCtl {
   uint64_t sf_ready[kMaxStages];  // MXFP8: the stage's scales are in TMEM
   uint64_t sf_drain;
   uint64_t gu_full[kGuSlots];   // dh GEMM: a slot's saved (g, u) have landed
-  uint64_t gu_empty[kGuSlots];  // dh GEMM: the epilogue warps have read the slot
+  uint64_t gu_done[kGuSlots];   // dh GEMM: the epilogue warps are done with the slot
   uint64_t wait_limit_ns;
   uint32_t tmem_base;
   volatile int abort;
@@ -444,6 +444,14 @@ __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_
   c.k_end = 0;
   c.k_blocks = a.k_blocks;
   return c;
+}
+
+// dh GEMM: whether the d(g, u) of a unit's chunks may leave as one TMA box store of the
+// CTA's 128 rows: all of them inside the unit's group, or running past the tensor's last
+// row (the store does not write those).  Half-pair tiles and CTAs without rows store
+// from registers.
+__device__ __forceinline__ bool gu_tma_out_rows(const TileCoord& c, bool hp, int32_t total_rows) {
+  return !hp && c.a_row0 < c.row_end && (c.a_row0 + kBM <= c.row_end || c.row_end == total_rows);
 }
 
 // kCluster: acquire at cluster scope (a barrier the peer CTA arrives on).
@@ -630,7 +638,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       for (int s = 0; s < kGuSlots; ++s) {
         mbar_init(smem_u32(&ctl->gu_full[s]), 1);
         // Every thread of the column group that reads the slot (half the epilogue).
-        mbar_init(smem_u32(&ctl->gu_empty[s]), 16 * epi_warps<kEpi>());
+        mbar_init(smem_u32(&ctl->gu_done[s]), 16 * epi_warps<kEpi>());
       }
     }
     ctl->abort = 0;
@@ -645,9 +653,11 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       tma_prefetch_map(&map_b2);
     }
     if (kGuStage) {
-      // The dh GEMM's saved-(g, u) maps ride in the second-GEMM slots.
+      // The dh GEMM's saved-(g, u) maps ride in the second-GEMM A slots, its d(g, u) map
+      // in the 64-row B slot.
       tma_prefetch_map(&map_a2);
       tma_prefetch_map(&map_a2_64);
+      tma_prefetch_map(&map_b2);
     }
   }
   if (warp == 1) {
@@ -1016,35 +1026,58 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       }
     }
   } else if (kGuStage && warp == 2 + epi_warps<kEpi>()) {
-    // ---------------- saved (g, u) loader (two-CTA dh GEMM) ----------------
+    // ---------------- saved (g, u) loader and d(g, u) storer (two-CTA dh GEMM) ----------
     // For each unit, the epilogue's 32-column chunks in the order in which the two
     // column groups of epilogue warps take them (group 0's first chunk, group 1's
-    // first, group 0's second, ...), each into the next slot once the threads that
-    // read its previous contents have arrived.  A slot takes this CTA's rows of the
-    // chunk (an M = 128 pair: slot rows 0..63 are the CTA's 64 rows at the tile's
-    // column offset 0, rows 64..127 the same rows at offset 128, the columns of the
-    // accumulator lanes 64..127).  A CTA whose rows all lie past its group's end
+    // first, group 0's second, ...), each copied into the next slot.  A slot takes this
+    // CTA's rows of the chunk (an M = 128 pair: slot rows 0..63 are the CTA's 64 rows at
+    // the tile's column offset 0, rows 64..127 the same rows at offset 128, the columns
+    // of the accumulator lanes 64..127).  A CTA whose rows all lie past its group's end
     // (the idle half of a group's last pair) loads nothing and only arrives.
+    // The epilogue writes a chunk's d(g, u) over its (g, u) in the slot when the chunk's
+    // box may be stored whole (gu_tma_out); this warp then stores the slot to dgu with
+    // TMA before it copies the slot's next chunk in.  Other chunks' d(g, u) the epilogue
+    // stores itself, releasing the slot as soon as it has read it.
     if (lane == 0) {
       uint32_t seq = 0;  // chunks issued
       bool ok = true;
       const int32_t split = static_cast<int32_t>(args.split);
+      int32_t out_x[kGuSlots], out_y[kGuSlots];  // pending TMA store of a slot (y < 0: none)
+      for (int q = 0; q < kGuSlots; ++q) {
+        out_x[q] = 0;
+        out_y[q] = -1;
+      }
+      // Waits until the epilogue is done with chunk sq, then stores its d(g, u) if the
+      // epilogue left them in the slot; the slot is free once the store has read it.
+      auto retire = [&](uint32_t sq) {
+        const uint32_t slot = sq % kGuSlots;
+        if (!ctl_wait(ctl, &ctl->gu_done[slot], (sq / kGuSlots) & 1u, args.status)) return false;
+        if (out_y[slot] >= 0) {
+          const uint32_t src = smem_u32(gu_smem + slot * kGuSlotBytes);
+          tma_store_2d(&map_b2, src, out_x[slot], out_y[slot]);
+          tma_store_2d(&map_b2, src + kGuHalfBytes, split + out_x[slot], out_y[slot]);
+          bulk_commit_group();
+          bulk_wait_group_read<0>();
+          out_y[slot] = -1;
+        }
+        return true;
+      };
       for (int32_t i = 0; i * ustride < n_total && ok; ++i) {
         const int32_t t = round_unit<kKG>(i, u0, ustride);
         if (t >= n_total) continue;
         const TileCoord tc = unit_tile<kPair, kKG, kTwo>(args, t, rank);
         const bool hp = pair_half_tile(tc);
         const bool rows = tc.a_row0 < tc.row_end;
+        const bool out_rows = gu_tma_out_rows(tc, hp, args.dense_rows);
         const int per_group = hp ? 2 : 4;
         const int32_t col_base = tc.n_tile * G::BN;
         for (int j = 0; j < per_group && ok; ++j) {
           for (int cg = 0; cg < 2; ++cg, ++seq) {
-            const uint32_t slot = seq % kGuSlots;
-            if (!ctl_wait(ctl, &ctl->gu_empty[slot], ((seq / kGuSlots) & 1u) ^ 1u,
-                          args.status)) {
+            if (seq >= static_cast<uint32_t>(kGuSlots) && !retire(seq - kGuSlots)) {
               ok = false;
               break;
             }
+            const uint32_t slot = seq % kGuSlots;
             const uint32_t full = smem_u32(&ctl->gu_full[slot]);
             if (!rows) {
               mbar_arrive(full);
@@ -1064,9 +1097,17 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
               tma_load_2d(dst, &map_a2, x, tc.a_row0, full);
               tma_load_2d(dst + kGuHalfBytes, &map_a2, split + x, tc.a_row0, full);
             }
+            if (out_rows && x + 32 <= args.n_out) {
+              out_x[slot] = x;
+              out_y[slot] = tc.a_row0;
+            }
           }
         }
       }
+      // The last chunks' stores.
+      for (uint32_t sq = seq > static_cast<uint32_t>(kGuSlots) ? seq - kGuSlots : 0u;
+           ok && sq < seq; ++sq)
+        ok = retire(sq);
       if (!ok || ctl->abort) {
         // Aborted: wait (bounded) for the copies of the last slots issued, which land in
         // this CTA's shared memory, before the CTA may leave.
@@ -1077,6 +1118,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
                     kDrainLimitNs);
         }
       }
+      bulk_wait_group<0>();  // the stores' writes are performed
     }
   } else if (warp >= 2 && warp < 2 + epi_warps<kEpi>()) {
     // ---------------- epilogue (warps 2 .. 2 + epi_warps - 1) ----------------
@@ -1196,10 +1238,13 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
       } else if (kGuStage) {
         // The saved (g, u) of each chunk come from the slot the loader filled: this
         // thread's slot row is its accumulator lane.  It reads its 64 bytes of g and of
-        // u, releases the slot, then forms and stores d(g, u).
+        // u and forms d(g, u).  A chunk whose box leaves by TMA store (the loader's) gets
+        // d(g, u) written over (g, u) in the slot before the slot is released; otherwise
+        // the slot is released as soon as it is read and d(g, u) is stored from registers.
         __nv_bfloat16* dgu_row = args.dgu_out + static_cast<int64_t>(row) * 2 * args.split;
         const int64_t col_base = static_cast<int64_t>(tc.n_tile) * G::BN + lh * 128;
         const int chunks = hp ? 2 : 4;
+        const bool out_rows = gu_tma_out_rows(tc, hp, args.dense_rows);
         const uint32_t srow = static_cast<uint32_t>(row_in_tile) * 64u;
         const uint32_t swz = static_cast<uint32_t>((row_in_tile >> 1) & 3);
         bool gu_ok = true;
@@ -1228,14 +1273,18 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
             gq[v] = ld_shared_v4(sg + piece);
             uq[v] = ld_shared_v4(sg + kGuHalfBytes + piece);
           }
-          mbar_arrive(smem_u32(&ctl->gu_empty[slot]));
-          tmem_ld_wait(a);
           const int64_t col0 = col_base + c * 32;
+          const bool tma_out = out_rows && col0 + 32 <= args.n_out;
+          const uint32_t done = smem_u32(&ctl->gu_done[slot]);
+          if (!tma_out) mbar_arrive(done);
+          tmem_ld_wait(a);
+          // Rows past the tensor's end (a dense GEMM's last tile) compute nothing; the
+          // TMA store does not write them.
           if (valid) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               const int64_t cv = col0 + 8 * v;
-              if (cv + 8 > args.n_out) continue;
+              if (!tma_out && cv + 8 > args.n_out) continue;
               const uint32_t gw[4] = {gq[v].x, gq[v].y, gq[v].z, gq[v].w};
               const uint32_t uw[4] = {uq[v].x, uq[v].y, uq[v].z, uq[v].w};
               uint32_t og[4], ou[4];
@@ -1251,9 +1300,21 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
                 og[e] = pack_bf16x2(dh0 * pg0, dh1 * pg1);
                 ou[e] = pack_bf16x2(dh0 * pu0, dh1 * pu1);
               }
-              st_global_v4(dgu_row + cv, og[0], og[1], og[2], og[3]);
-              st_global_v4(dgu_row + args.split + cv, ou[0], ou[1], ou[2], ou[3]);
+              if (tma_out) {
+                const uint32_t piece = 16u * (static_cast<uint32_t>(v) ^ swz);
+                st_shared_v4(sg + piece, og[0], og[1], og[2], og[3]);
+                st_shared_v4(sg + kGuHalfBytes + piece, ou[0], ou[1], ou[2], ou[3]);
+              } else {
+                st_global_v4(dgu_row + cv, og[0], og[1], og[2], og[3]);
+                st_global_v4(dgu_row + args.split + cv, ou[0], ou[1], ou[2], ou[3]);
+              }
             }
+          }
+          if (tma_out) {
+            // The slot's d(g, u) are visible to the loader's TMA store once it has seen
+            // every thread's arrival.
+            fence_proxy_async_smem();
+            mbar_arrive(done);
           }
         }
         gseq += 2u * static_cast<uint32_t>(chunks);
@@ -1619,11 +1680,13 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
           return cudaErrorInvalidValue;
       }
       // The dh GEMM: maps over the saved (g, u) for its loader warp (128- and 64-row
-      // boxes), in the second-GEMM slots.
+      // boxes) in the second-GEMM slots, and over d(g, u) for its TMA stores in the
+      // 64-row B slot (its B is never a SiTU tile's).
       CUtensorMap mg = ma, mg64 = ma64;
       if (kEpi == Epi::kSituBwd &&
           !(make_map_gu(&mg, s.gu_in, s.a_rows, 2 * s.split, 128) &&
-            make_map_gu(&mg64, s.gu_in, s.a_rows, 2 * s.split, 64)))
+            make_map_gu(&mg64, s.gu_in, s.a_rows, 2 * s.split, 64) &&
+            make_map_gu(&mb64, s.dgu_out, s.a_rows, 2 * s.split, 128)))
         return cudaErrorInvalidValue;
       if (dense) {
         const int64_t units = ((m_tiles + 1) / 2) * a.n_tiles;
