@@ -197,6 +197,12 @@ template <Epi kEpi>
 __host__ __device__ constexpr int epi_warps() {
   return kEpi == Epi::kSituBwd ? 8 : 4;
 }
+// Column groups of epilogue warps: warps e, e + 4, ... share a TMEM lane quarter and
+// split a tile's columns.
+template <Epi kEpi>
+__host__ __device__ constexpr int epi_col_groups() {
+  return epi_warps<kEpi>() / 4;
+}
 // Threads per CTA: producer and MMA warps, the epilogue warps, and (MXFP8) the scale
 // copier or (activation derivative) the loader of the saved (g, u).
 template <Epi kEpi, int kMx>
@@ -637,8 +643,8 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
     if (kGuStage) {
       for (int s = 0; s < kGuSlots; ++s) {
         mbar_init(smem_u32(&ctl->gu_full[s]), 1);
-        // Every thread of the column group that reads the slot (half the epilogue).
-        mbar_init(smem_u32(&ctl->gu_done[s]), 16 * epi_warps<kEpi>());
+        // Every thread of the column group that reads the slot.
+        mbar_init(smem_u32(&ctl->gu_done[s]), 128);
       }
     }
     ctl->abort = 0;
@@ -1069,10 +1075,11 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         const bool hp = pair_half_tile(tc);
         const bool rows = tc.a_row0 < tc.row_end;
         const bool out_rows = gu_tma_out_rows(tc, hp, args.dense_rows);
-        const int per_group = hp ? 2 : 4;
+        constexpr int kGroups = epi_col_groups<kEpi>();
+        const int per_group = (hp ? 4 : 8) / kGroups;
         const int32_t col_base = tc.n_tile * G::BN;
         for (int j = 0; j < per_group && ok; ++j) {
-          for (int cg = 0; cg < 2; ++cg, ++seq) {
+          for (int cg = 0; cg < kGroups; ++cg, ++seq) {
             if (seq >= static_cast<uint32_t>(kGuSlots) && !retire(seq - kGuSlots)) {
               ok = false;
               break;
@@ -1243,14 +1250,14 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         // the slot is released as soon as it is read and d(g, u) is stored from registers.
         __nv_bfloat16* dgu_row = args.dgu_out + static_cast<int64_t>(row) * 2 * args.split;
         const int64_t col_base = static_cast<int64_t>(tc.n_tile) * G::BN + lh * 128;
-        const int chunks = hp ? 2 : 4;
+        const int chunks = (hp ? 4 : 8) / epi_col_groups<kEpi>();  // this warp's chunks
         const bool out_rows = gu_tma_out_rows(tc, hp, args.dense_rows);
         const uint32_t srow = static_cast<uint32_t>(row_in_tile) * 64u;
         const uint32_t swz = static_cast<uint32_t>((row_in_tile >> 1) & 3);
         bool gu_ok = true;
 #pragma unroll 1
         for (int j = 0; j < chunks; ++j) {
-          const uint32_t seq = gseq + 2 * j + col_group;
+          const uint32_t seq = gseq + epi_col_groups<kEpi>() * j + col_group;
           const uint32_t slot = seq % kGuSlots, par = (seq / kGuSlots) & 1u;
           int w = 1;
           if (lane == 0) w = ctl_wait(ctl, &ctl->gu_full[slot], par, args.status) ? 1 : 0;
@@ -1317,7 +1324,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
             mbar_arrive(done);
           }
         }
-        gseq += 2u * static_cast<uint32_t>(chunks);
+        gseq += static_cast<uint32_t>(epi_col_groups<kEpi>() * chunks);
         if (!gu_ok) break;
       } else if (kEpi == Epi::kSituBwd) {
         const __nv_bfloat16* gu_row = args.gu_in + static_cast<int64_t>(row) * 2 * args.split;
