@@ -52,6 +52,34 @@ def _grouped_backward(dev):
     return lambda: situ.situ_moe_grouped_backward(x, off, tix, wgu, wd, gu, h, dy)
 
 
+def _dense_backward(dev):
+    """The dense training step's backward: the two-CTA dh GEMM whose loader warp stages
+    the saved (g, u) and stores d(g, u) with TMA."""
+    x, wgu, wd = wl.ffn_inputs(4096, 512, 512, seed=10)
+    x, wgu, wd = x.to(dev), wgu.to(dev), wd.to(dev)
+    dy = wl.normal((512, 4096), 1.0, seed=11).to(dev)
+    _, gu, h = situ.situ_ffn_forward_train(x, wgu, wd)
+    torch.cuda.synchronize()
+    return lambda: situ.situ_ffn_backward(x, wgu, wd, gu, h, dy)
+
+
+def _grouped_backward_two_cta(dev):
+    """A grouped backward whose experts average >= 128 routes: two-CTA dh (staged) and dx
+    GEMMs, half-pair tails."""
+    sizes, M, I = (300, 290, 140), 4096, 384
+    E = len(sizes)
+    ids = torch.cat([torch.full((n,), e, dtype=torch.int32) for e, n in enumerate(sizes)])
+    ids = ids[torch.randperm(ids.numel(), generator=torch.Generator().manual_seed(12))][:, None]
+    T = ids.shape[0]
+    x = wl.normal((T, M), 1.0, seed=13).to(dev)
+    dy = wl.normal((T, 1, M), 1.0, seed=14).to(dev)
+    wgu, wd = (w.to(dev) for w in wl.expert_weights(E, M, I, seed=15))
+    off, tix = situ.situ_moe_build_index(ids.to(dev), E)
+    _, gu, h = situ.situ_moe_grouped_forward_train(x, off, tix, wgu, wd, 1)
+    torch.cuda.synchronize()
+    return lambda: situ.situ_moe_grouped_backward(x, off, tix, wgu, wd, gu, h, dy)
+
+
 def _mx_dense(dev):
     x, wgu, wd = wl.ffn_inputs(4096, 1536, 2048, seed=9)
     wq = situ.mx_quantize_weights(wgu.to(dev), situ.MX_GATE_UP, situ.MX_E2M1)
@@ -61,7 +89,8 @@ def _mx_dense(dev):
 
 
 @pytest.mark.parametrize("case", ["dense_one_launch", "grouped_two_cta", "grouped_one_cta",
-                                  "grouped_backward", "mx_dense"])
+                                  "grouped_backward", "dense_backward",
+                                  "grouped_backward_two_cta", "mx_dense"])
 def test_gemm_waits_time_out_and_recover(cuda_dev, case):
     """With a 1 us bound every pipelined GEMM's waits run out (a tile's MMAs alone take
     several microseconds): the call records SITU_ERR_TIMEOUT, drains, frees its tensor
@@ -72,6 +101,8 @@ def test_gemm_waits_time_out_and_recover(cuda_dev, case):
            "grouped_two_cta": lambda: _grouped(cuda_dev, (300, 290, 140)),
            "grouped_one_cta": lambda: _grouped(cuda_dev, (20, 7, 33, 1, 12)),
            "grouped_backward": lambda: _grouped_backward(cuda_dev),
+           "dense_backward": lambda: _dense_backward(cuda_dev),
+           "grouped_backward_two_cta": lambda: _grouped_backward_two_cta(cuda_dev),
            "mx_dense": lambda: _mx_dense(cuda_dev)}[case]()
     flat = lambda out: [t.contiguous().view(torch.uint8).clone()
                         for t in (out if isinstance(out, tuple) else (out,))]
