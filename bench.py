@@ -614,14 +614,17 @@ def cpu_baseline(seconds: float, rows_hint: int = 0):
 
 def route_sample(ids_cpu, n: int, seed: int = 0):
     """A seeded sample of n flat routes (token * k_eff + slot) of ids [T, k_eff] that
-    covers every expert with at least one route: one route of each non-empty expert
-    (the first in a seeded permutation), then the permutation's next routes."""
+    covers every non-empty expert with the first and the last row of its group (in
+    expert order, ties by flat index: the expert's smallest and largest flat route),
+    then takes a seeded permutation's next routes up to n."""
     import numpy as np
 
     flat = ids_cpu.contiguous().view(-1).numpy()
+    experts, first = np.unique(flat, return_index=True)
+    _, last_rev = np.unique(flat[::-1], return_index=True)
+    last = flat.size - 1 - last_rev
+    chosen = np.unique(np.concatenate([first, last]))
     order = np.random.default_rng(seed).permutation(flat.size)
-    _, first = np.unique(flat[order], return_index=True)
-    chosen = order[first]
     rest = order[~np.isin(order, chosen)][: max(0, n - chosen.size)]
     return np.sort(np.concatenate([chosen, rest]))
 
@@ -639,8 +642,8 @@ def host_bytes_available() -> int:
 
 def cpu_baseline_routes(w, x, ids_cpu, wgu_host, wd_host, n_routes: int = 4096):
     """The FP64 oracle's grouped experts (as it stands) on a seeded sample of n_routes
-    routes of a grouped workload covering every non-empty expert, each route with its
-    own expert's weights: the sampled routes run as a grouped call of one slot per
+    routes of a grouped workload holding the first and last row of every non-empty
+    expert's group, each route with its own expert's weights: the sampled routes run as a grouped call of one slot per
     sampled route.  routes/s is measured; tokens/s = routes/s / k_eff is extrapolated."""
     import numpy as np
     import torch
@@ -659,8 +662,9 @@ def cpu_baseline_routes(w, x, ids_cpu, wgu_host, wd_host, n_routes: int = 4096):
     experts = int(np.unique(ids_s).size)
     return {"value": sample.size / dt / w.k_eff, "unit": "tokens/s",
             "routes_per_s": sample.size / dt, "cores": o.num_threads(), "kind": "oracle",
-            "sample": f"{sample.size} seeded routes of the workload covering all {experts} "
-                      f"non-empty experts, each with its own weights (FP64 grouped experts, "
+            "sample": f"{sample.size} seeded routes of the workload holding the first and last "
+                      f"row of all {experts} non-empty experts' groups, each route with its "
+                      f"expert's own weights (FP64 grouped experts, "
                       f"per-route loop), {dt:.1f} s; tokens/s = routes/s / {w.k_eff}, "
                       "extrapolated to the workload"}
 

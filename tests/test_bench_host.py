@@ -96,17 +96,22 @@ def test_gpus_must_match_the_rank_count(monkeypatch):
 
 
 def test_route_sample_covers_every_expert():
-    """The grouped CPU baseline's sample: n distinct routes, seeded, with at least one
-    route of every expert that has routes."""
+    """The grouped CPU baseline's sample: n distinct routes, seeded, holding the first and
+    the last row of every non-empty expert's group (expert order, ties by flat index)."""
     import numpy as np
     import torch
 
     g = torch.Generator().manual_seed(3)
     ids = torch.randint(0, 50, (300, 4), generator=g, dtype=torch.int32)
     ids[ids == 7] = 8  # expert 7 without routes
-    s = bench.route_sample(ids, 64, seed=0)
+    s = bench.route_sample(ids, 160, seed=0)
     flat = ids.view(-1).numpy()
-    assert s.size == 64 and np.unique(s).size == 64 and (np.diff(s) > 0).all()
+    assert s.size == 160 and np.unique(s).size == 160 and (np.diff(s) > 0).all()
     assert set(np.unique(flat[s])) == set(np.unique(flat))
-    assert np.array_equal(s, bench.route_sample(ids, 64, seed=0))
-    assert bench.route_sample(ids, 10, seed=0).size == np.unique(flat).size  # all experts kept
+    assert np.array_equal(s, bench.route_sample(ids, 160, seed=0))
+    for e in np.unique(flat):
+        where = np.nonzero(flat == e)[0]
+        assert where[0] in s and where[-1] in s
+    # Fewer routes asked than the group ends: every group's first and last row is kept.
+    ends = {int(i) for e in np.unique(flat) for i in np.nonzero(flat == e)[0][[0, -1]]}
+    assert set(bench.route_sample(ids, 10, seed=0).tolist()) == ends
