@@ -1297,15 +1297,19 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
               uint32_t og[4], ou[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                float pg0, pu0, pg1, pu1;
-                situ_act_grad<kC>(__uint_as_float(gw[e] << 16), __uint_as_float(uw[e] << 16),
-                                  args.sp, pg0, pu0);
-                situ_act_grad<kC>(__uint_as_float(gw[e] & 0xFFFF0000u),
-                                  __uint_as_float(uw[e] & 0xFFFF0000u), args.sp, pg1, pu1);
-                const float dh0 = __uint_as_float(a[8 * v + 2 * e]);
-                const float dh1 = __uint_as_float(a[8 * v + 2 * e + 1]);
-                og[e] = pack_bf16x2(dh0 * pg0, dh1 * pg1);
-                ou[e] = pack_bf16x2(dh0 * pu0, dh1 * pu1);
+                uint64_t dg2, du2;
+                situ_act_grad_x2<kC>(__uint_as_float(gw[e] << 16),
+                                     __uint_as_float(gw[e] & 0xFFFF0000u),
+                                     __uint_as_float(uw[e] << 16),
+                                     __uint_as_float(uw[e] & 0xFFFF0000u),
+                                     f2_pack(__uint_as_float(a[8 * v + 2 * e]),
+                                             __uint_as_float(a[8 * v + 2 * e + 1])),
+                                     args.sp, dg2, du2);
+                float lo, hi;
+                f2_unpack(dg2, lo, hi);
+                og[e] = pack_bf16x2(lo, hi);
+                f2_unpack(du2, lo, hi);
+                ou[e] = pack_bf16x2(lo, hi);
               }
               if (tma_out) {
                 const uint32_t piece = 16u * (static_cast<uint32_t>(v) ^ swz);
@@ -1373,15 +1377,19 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
               uint32_t og[4], ou[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                float pg0, pu0, pg1, pu1;
-                situ_act_grad<kC>(__uint_as_float(gw[i] << 16), __uint_as_float(uw[i] << 16),
-                                  args.sp, pg0, pu0);
-                situ_act_grad<kC>(__uint_as_float(gw[i] & 0xFFFF0000u),
-                                  __uint_as_float(uw[i] & 0xFFFF0000u), args.sp, pg1, pu1);
-                const float dh0 = __uint_as_float(a[8 * v + 2 * i]);
-                const float dh1 = __uint_as_float(a[8 * v + 2 * i + 1]);
-                og[i] = pack_bf16x2(dh0 * pg0, dh1 * pg1);
-                ou[i] = pack_bf16x2(dh0 * pu0, dh1 * pu1);
+                uint64_t dg2, du2;
+                situ_act_grad_x2<kC>(__uint_as_float(gw[i] << 16),
+                                     __uint_as_float(gw[i] & 0xFFFF0000u),
+                                     __uint_as_float(uw[i] << 16),
+                                     __uint_as_float(uw[i] & 0xFFFF0000u),
+                                     f2_pack(__uint_as_float(a[8 * v + 2 * i]),
+                                             __uint_as_float(a[8 * v + 2 * i + 1])),
+                                     args.sp, dg2, du2);
+                float lo, hi;
+                f2_unpack(dg2, lo, hi);
+                og[i] = pack_bf16x2(lo, hi);
+                f2_unpack(du2, lo, hi);
+                ou[i] = pack_bf16x2(lo, hi);
               }
               st_global_v4(dgu_row + cv, og[0], og[1], og[2], og[3]);
               st_global_v4(dgu_row + args.split + cv, ou[0], ou[1], ou[2], ou[3]);

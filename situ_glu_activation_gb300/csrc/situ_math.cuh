@@ -228,6 +228,86 @@ __device__ __forceinline__ void situ_act_grad(float g, float u, const SituParams
   pu = a * db;
 }
 
+// Two FP32 lanes in one 64-bit register pair, for the paired FP32 instructions
+// (add/mul/fma .rn.f32x2): one issue slot for two elements.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// tanh and sech^2 of two arguments (as tanh_sech2, the FP32 arithmetic paired).
+__device__ __forceinline__ void tanh_sech2_x2(uint64_t x, uint64_t& t, uint64_t& sech2) {
+  float x0, x1;
+  f2_unpack(x, x0, x1);
+  t = f2_pack(tanh_approx(x0), tanh_approx(x1));
+  const uint64_t e4 = f2_pack(ex2_approx(fmaf(fabsf(x0), -2.0f * kLog2e, 2.0f)),
+                              ex2_approx(fmaf(fabsf(x1), -2.0f * kLog2e, 2.0f)));
+  float d0, d1;
+  f2_unpack(f2_fma(f2_pack(0.25f, 0.25f), e4, f2_pack(1.0f, 1.0f)), d0, d1);
+  const uint64_t r = f2_pack(rcp_approx(d0), rcp_approx(d1));
+  sech2 = f2_mul(f2_mul(e4, r), r);
+}
+
+// d(g, u) of two adjacent outputs: dh * (dh/dg, dh/du) at (g0, u0) and (g1, u1), the
+// partial derivatives as in situ_act_grad, with the FP32 products and sums on pairs.
+// dh holds the two dh values; returns dg (lo, hi) in og and du in ou.
+template <Caps kC>
+__device__ __forceinline__ void situ_act_grad_x2(float g0, float g1, float u0, float u1,
+                                                 uint64_t dh, const SituParams& p, uint64_t& og,
+                                                 uint64_t& ou) {
+  const uint64_t one = f2_pack(1.0f, 1.0f);
+  const uint64_t e0 = f2_pack(ex2_approx(-fabsf(g0) * kLog2e), ex2_approx(-fabsf(g1) * kLog2e));
+  float den0, den1;
+  f2_unpack(f2_add(e0, one), den0, den1);
+  const float r00 = rcp_approx(den0), r01 = rcp_approx(den1);
+  float lo0, lo1;
+  f2_unpack(f2_mul(e0, f2_pack(r00, r01)), lo0, lo1);  // sigmoid(-|g|)
+  const uint64_t sg = f2_pack(g0 >= 0.0f ? r00 : lo0, g1 >= 0.0f ? r01 : lo1);   // sigmoid(g)
+  const uint64_t sgm = f2_pack(g0 >= 0.0f ? lo0 : r00, g1 >= 0.0f ? lo1 : r01);  // sigmoid(-g)
+  const uint64_t g = f2_pack(g0, g1), u = f2_pack(u0, u1);
+  uint64_t a, da;
+  if constexpr (kC == Caps::kBoth || kC == Caps::kGateOnly) {
+    uint64_t t, sech2;
+    tanh_sech2_x2(f2_mul(g, f2_pack(p.inv_b1, p.inv_b1)), t, sech2);
+    a = f2_mul(f2_mul(f2_pack(p.b1, p.b1), t), sg);
+    da = f2_fma(a, sgm, f2_mul(sech2, sg));
+  } else {
+    a = f2_mul(g, sg);
+    da = f2_fma(a, sgm, sg);
+  }
+  uint64_t pg, pu;
+  if constexpr (kC == Caps::kBoth || kC == Caps::kUpOnly) {
+    uint64_t t, sech2;
+    tanh_sech2_x2(f2_mul(u, f2_pack(p.inv_b2, p.inv_b2)), t, sech2);
+    pg = f2_mul(f2_mul(f2_pack(p.b2, p.b2), t), da);
+    pu = f2_mul(a, sech2);
+  } else {
+    pg = f2_mul(u, da);
+    pu = a;
+  }
+  og = f2_mul(dh, pg);
+  ou = f2_mul(dh, pu);
+}
+
 // SiTU-GLU with both caps (the hot path).
 __device__ __forceinline__ float situ_glu_f32(float g, float u, const SituParams& p) {
   return situ_act<Caps::kBoth>(g, u, p);
