@@ -130,6 +130,60 @@ def test_dgu_elementwise(oracle, cuda_dev, R, M, I, caps):
                                    f"{float((err / np.maximum(tol, 1e-300)).max()):.3g}"
 
 
+def test_dgu_special_values(oracle, cuda_dev):
+    """The derivative epilogue on a saved pre-activation pair built to hit the method's
+    edges: zeros and tiny values, the caps' saturation (|g| or |u| up to 1e4), the gate's
+    negative tail down to -100 (where sigmoid(g) and a(g) leave the FP32 normal range),
+    large positive gates, mixed with N(0, 1).  d(g, u) against dh times the oracle's
+    partial derivatives, with the bound of test_dgu_elementwise plus an absolute
+    2^-120 * |dh| * (1 + |a(g)| + |b(u)|): the kernel's FP32 special-function ops flush
+    results below 2^-126 to zero, where the exact partials are smaller still."""
+    R, M, I = 160, 256, 256
+    g = torch.Generator().manual_seed(77)
+    special = torch.tensor([0.0, -0.0, 1e-20, -1e-20, 1e-3, -1e-3, 2.0, -2.0, 20.0, -20.0, 44.0,
+                            -44.0, 87.0, -87.0, -88.0, -90.0, -100.0, 100.0, 1e3, -1e3, 1e4,
+                            -1e4, 30.0, -30.0])
+    pick = torch.randint(0, special.numel(), (R, 2 * I), generator=g)
+    gu = torch.where(torch.rand(R, 2 * I, generator=g) < 0.5, special[pick],
+                     torch.randn(R, 2 * I, generator=g)).to(torch.bfloat16)
+    x, wgu, wd = wl.ffn_inputs(M, I, R, seed=78)
+    dy = wl.normal((R, M), 1.0, seed=79)
+    h = wl.normal((R, I), 1.0, seed=80)  # only dW_down reads h; d(g, u) is checked
+    dev = cuda_dev
+    ws = torch.empty(situ.ffn_backward_workspace_bytes(R, M, I), dtype=torch.uint8, device=dev)
+    situ.situ_ffn_backward(x.to(dev), wgu.to(dev), wd.to(dev), gu.to(dev), h.to(dev), dy.to(dev),
+                           workspace=ws)
+    torch.cuda.synchronize()
+    assert situ.device_status(clear=True) == 0
+    dgu = to_f64(ws[: R * 2 * I * 2].view(torch.bfloat16).view(R, 2 * I).cpu())
+    assert np.isfinite(dgu).all()
+    guf = to_f64(gu)
+    dh = to_f64(dy) @ to_f64(wd)
+    dh_abs = np.abs(to_f64(dy)) @ np.abs(to_f64(wd))
+    pg = np.empty((R, I))
+    pu = np.empty((R, I))
+    gate_terms = np.empty((R, I))
+    a_abs = np.empty((R, I))
+    b_abs = np.empty((R, I))
+    for r in range(R):
+        for j in range(I):
+            gv, uv = guf[r, j], guf[r, I + j]
+            pg[r, j], pu[r, j] = oracle.pair_grad(gv, uv, 4.0, 25.0)
+            a_abs[r, j] = abs(oracle.gate(gv, 4.0))
+            b_abs[r, j] = abs(oracle.up(uv, 25.0))
+            gate_terms[r, j] = oracle.sigmoid(gv) + a_abs[r, j] * oracle.sigmoid(-gv)
+    flush = 2.0 ** -120 * np.abs(dh) * (1.0 + a_abs + b_abs)
+    for got, part, extra, what in ((dgu[:, :I], pg, 2.0 ** -9 * np.abs(dh) * b_abs * gate_terms,
+                                    "dg"),
+                                   (dgu[:, I:], pu, 0.0, "du")):
+        ref = dh * part
+        tol = 2.0 ** -8 * np.abs(ref) + extra + 2.0 ** -12 * dh_abs * np.abs(part) + flush
+        err = np.abs(got - ref)
+        bad = err > tol
+        assert not bad.any(), f"{what}: {int(bad.sum())} outside the bound, e.g. gu = " \
+                              f"{guf[np.nonzero(bad)[0][0]]}"
+
+
 def test_backward_full_size_sparse_dy(oracle, cuda_dev):
     """The 16384-token workload (M=2048, I=3072) at full size, with dy nonzero on 16
     seeded rows only: every other row contributes exactly zero, so the oracle's
