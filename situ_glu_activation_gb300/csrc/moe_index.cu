@@ -5,9 +5,11 @@
 //
 // Three passes over chunks of 1024 routes:
 //   1. per-chunk histograms (shared-memory atomics) -> counts[chunk][e];
-//   2. one block turns counts into absolute bases: for each expert an exclusive
-//      scan over chunks, plus the exclusive scan over experts (the offsets);
-//   3. per chunk, the 32 warps take turns in route order; inside a warp the lanes
+//   2. per expert (a block each) an exclusive scan of its counts over the chunks (the
+//      chunk's base within the expert's rows) and its total; then one block scans the
+//      totals into the offsets;
+//   3. per chunk (each expert's cursor starting at its offset plus the chunk's base),
+//      the 32 warps take turns in route order; inside a warp the lanes
 //      that share an expert rank themselves by __match_any_sync and a popcount
 //      of the lower lanes, which keeps equal keys in route order (stable).
 // The result is the same permutation on every run (no atomics decide order).
@@ -42,22 +44,44 @@ __global__ void index_count_kernel(const int32_t* __restrict__ ids, int64_t n, i
   for (int e = threadIdx.x; e < E; e += blockDim.x) row[e] = hist[e];
 }
 
-// counts[c][e] <- offsets[e] + sum_{c' < c} counts[c'][e]; offsets[e] = exclusive
-// scan of the per-expert totals.  One block of 1024 threads.
-__global__ void index_scan_kernel(int32_t* __restrict__ counts, int32_t nchunks, int32_t E,
-                                  int32_t* __restrict__ offsets) {
+// Per expert (one block each): counts[c][e] <- sum_{c' < c} counts[c'][e], the chunk's base
+// within its expert's rows, and offsets[e] <- the expert's total.  Each thread scans a run
+// of consecutive chunks; a block-wide scan of the runs' sums joins them.
+constexpr int kScanThreads = 256;
+__global__ void __launch_bounds__(kScanThreads)
+    index_scan_chunks_kernel(int32_t* __restrict__ counts, int32_t nchunks, int32_t E,
+                             int32_t* __restrict__ offsets) {
+  __shared__ int32_t part[kScanThreads];
+  const int e = blockIdx.x;
+  const int per = (nchunks + kScanThreads - 1) / kScanThreads;
+  const int c0 = threadIdx.x * per;
+  const int c1 = min(c0 + per, nchunks);
+  int32_t sum = 0;
+  for (int c = c0; c < c1; ++c) sum += counts[static_cast<int64_t>(c) * E + e];
+  part[threadIdx.x] = sum;
+  __syncthreads();
+  for (int d = 1; d < kScanThreads; d <<= 1) {
+    const int32_t v = threadIdx.x >= static_cast<unsigned>(d) ? part[threadIdx.x - d] : 0;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int32_t run = part[threadIdx.x] - sum;  // exclusive prefix of this thread's run
+  for (int c = c0; c < c1; ++c) {
+    int32_t* p = counts + static_cast<int64_t>(c) * E + e;
+    const int32_t v = *p;
+    *p = run;
+    run += v;
+  }
+  if (threadIdx.x == kScanThreads - 1) offsets[e] = part[threadIdx.x];
+}
+
+// offsets[0..E-1] (the experts' totals) <- their exclusive scan; offsets[E] <- the sum.
+// One block of 1024 threads.
+__global__ void index_scan_experts_kernel(int32_t E, int32_t* __restrict__ offsets) {
   extern __shared__ int32_t tot[];  // [E] totals, then [blockDim] partial sums
   int32_t* partial = tot + E;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int32_t run = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      int32_t* p = counts + static_cast<int64_t>(c) * E + e;
-      const int32_t v = *p;
-      *p = run;
-      run += v;
-    }
-    tot[e] = run;
-  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) tot[e] = offsets[e];
   __syncthreads();
   const int per = (E + blockDim.x - 1) / blockDim.x;
   const int e0 = threadIdx.x * per;
@@ -77,19 +101,15 @@ __global__ void index_scan_kernel(int32_t* __restrict__ counts, int32_t nchunks,
     run += tot[e];
   }
   if (threadIdx.x == blockDim.x - 1) offsets[E] = partial[threadIdx.x];
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int32_t o = offsets[e];
-    for (int c = 0; c < nchunks; ++c) counts[static_cast<int64_t>(c) * E + e] += o;
-  }
 }
 
 __global__ void __launch_bounds__(kChunk)
     index_place_kernel(const int32_t* __restrict__ ids, int64_t n, int32_t E,
-                       const int32_t* __restrict__ bases, int32_t* __restrict__ token_index) {
+                       const int32_t* __restrict__ bases, const int32_t* __restrict__ offsets,
+                       int32_t* __restrict__ token_index) {
   extern __shared__ int32_t cursor[];
   const int32_t* row = bases + static_cast<int64_t>(blockIdx.x) * E;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cursor[e] = row[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cursor[e] = offsets[e] + row[e];
   __syncthreads();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -135,16 +155,20 @@ cudaError_t launch_build_index(const int32_t* expert_ids, int32_t* offsets,
     index_count_kernel<<<nchunks, 256, hist_bytes, stream>>>(expert_ids, n, E, counts, status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  // Per expert, the chunks' bases within its rows and its total (in offsets); then the
+  // offsets; the placement adds an expert's offset to its chunk bases.
+  index_scan_chunks_kernel<<<E, kScanThreads, 0, stream>>>(counts, nchunks, E, offsets);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t scan_bytes = hist_bytes + 1024 * 4;
-  e = cudaFuncSetAttribute(reinterpret_cast<const void*>(index_scan_kernel),
+  e = cudaFuncSetAttribute(reinterpret_cast<const void*>(index_scan_experts_kernel),
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(scan_bytes));
   if (e != cudaSuccess) return e;
-  index_scan_kernel<<<1, 1024, scan_bytes, stream>>>(counts, nchunks, E, offsets);
+  index_scan_experts_kernel<<<1, 1024, scan_bytes, stream>>>(E, offsets);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (nchunks > 0) {
     index_place_kernel<<<nchunks, kChunk, hist_bytes, stream>>>(expert_ids, n, E, counts,
-                                                                token_index);
+                                                                offsets, token_index);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
