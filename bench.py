@@ -382,7 +382,7 @@ def bench_moe(args, dev, peaks, world, flush, names, cpu=False):
             "tokens_per_s": w.T / (ms * 1e-3), "tflops": tflops,
             "tc_frac": tflops / peaks["bf16_tflops"],
             "weight_gbs": weight_gbs, "hbm_frac": weight_gbs / peaks["hbm_gbs"],
-            "launches_per_step": 3 + 4 + 1,
+            "launches_per_step": 4 + 4 + 1,
             "step": "expert index, grouped SiTU-GLU experts, router-weighted combine",
         }
         if cpu:
@@ -525,7 +525,7 @@ def bench_mx(args, dev, peaks, world, flush, names=("grouped", "k3_decode", "k3_
                 "tc_frac_fp8": flop / (ms * 1e-3) / 1e12 / fp8_peak,
                 "weight_gbs": wbytes / (ms * 1e-3) / 1e9,
                 "hbm_frac": wbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                "launches_per_step": 3 + 4 + 1}
+                "launches_per_step": 4 + 4 + 1}
             del wguq, wdq
             torch.cuda.empty_cache()
         del x, y, ws, off, tix, ids
@@ -576,7 +576,7 @@ def bench_moe_train(args, dev, peaks, world, flush):
            "tflops": (flop_f + flop_b) / (ms * 1e-3) / 1e12,
            "backward_tflops": flop_b / (mean(t_bwd) * 1e-3) / 1e12,
            "tc_frac": (flop_f + flop_b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
-           "launches_per_step": 3 + 4 + 8}
+           "launches_per_step": 4 + 4 + 8}
     del wgu, wd, ws_f, ws_b, dy, x
     torch.cuda.empty_cache()
     return out
