@@ -102,7 +102,8 @@ __global__ void group_tiles_kernel(const int32_t* __restrict__ off, int32_t G, i
   }
 }
 
-// One warp per gathered row: x_perm[r] = x[token_index[r] / k_eff] (16-byte copies).
+// One warp per gathered row: x_perm[r] = x[token_index[r] / k_eff] (16-byte copies, eight
+// loads in flight per lane before their stores).
 __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ tix,
                                    uint4* __restrict__ xp, int64_t R, int32_t k_eff,
                                    int64_t vec_per_row, int64_t T, uint32_t* status) {
@@ -118,7 +119,15 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* _
       continue;
     }
     const uint4* src = x + t * vec_per_row;
-    for (int64_t v = threadIdx.x & 31; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+    int64_t v = threadIdx.x & 31;
+    for (; v + 7 * 32 < vec_per_row; v += 8 * 32) {
+      uint4 q[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) q[j] = __ldg(src + v + 32 * j);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) dst[v + 32 * j] = q[j];
+    }
+    for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
   }
 }
 
