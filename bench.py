@@ -282,12 +282,18 @@ def bench_dense(args, dev, peaks, world, flush):
 
     e2e_ms, _ = timed_steps(e2e_step, args.steps, args.warmup, flush, world)
     out["e2e_ms"] = mean(e2e_ms)
+    # The timed step's inputs and output, for the oracle's baseline and accuracy check.
+    out["inputs"] = (x.cpu(), wgu.cpu(), wd.cpu())
+    out["y"] = y.cpu()
     out["h2d_bytes"] = x.numel() * x.element_size()
     out["d2h_bytes"] = y.numel() * y.element_size()
     return out, w
 
 
-def bench_act(args, dev, peaks, world, flush):
+def bench_act(args, dev, peaks, world, flush, check_rows: int = 0):
+    """check_rows > 0: the first check_rows output rows against the FP64 oracle, in bf16
+    ulps (the oracle on the host cores)."""
+    import numpy as np
     import torch
 
     import situ_glu_activation_gb300 as situ
@@ -299,17 +305,27 @@ def bench_act(args, dev, peaks, world, flush):
     per_step, _ = timed_steps(lambda m: situ.situ_glu_act(g, wl.BETA, wl.LINEAR_BETA, out=o),
                               args.steps, args.warmup, flush, world)
     ms = mean(per_step)
+    accuracy = None
+    if check_rows > 0:
+        from oracle import Oracle
+
+        gin = g[:check_rows].contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+        ref = Oracle().situ_glu_act(gin, wl.BETA, wl.LINEAR_BETA)
+        accuracy = ulp_stats(o[:check_rows].cpu(), ref)
     inf = float("inf")
     sw_ms, _ = timed_steps(lambda m: situ.situ_glu_act(g, inf, inf, out=o), args.steps,
                            args.warmup, flush, world)
     nbytes = 3 * w.rows * w.I * 2  # read 2I, write I per row, bf16
     gbs = nbytes / (ms * 1e-3) / 1e9
     digest = source_digest("act.cu", "situ_math.cuh")
-    return {"workload": w.name, "ms": ms, "bytes": nbytes, "gbs": gbs, "swiglu_ms": mean(sw_ms),
-            "roofline": {"bound": "hbm", "kernel": "act_bf16_vec_kernel", "achieved": gbs,
-                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / peaks["hbm_gbs"],
-                         "traffic": profiled_traffic("situ_act", digest, w.rows * w.I)}}
+    res = {"workload": w.name, "ms": ms, "bytes": nbytes, "gbs": gbs, "swiglu_ms": mean(sw_ms),
+           "roofline": {"bound": "hbm", "kernel": "act_bf16_vec_kernel", "achieved": gbs,
+                        "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / peaks["hbm_gbs"],
+                        "traffic": profiled_traffic("situ_act", digest, w.rows * w.I)}}
+    if accuracy is not None:
+        res["accuracy"] = accuracy
+    return res
 
 
 def bench_moe(args, dev, peaks, world, flush, names, cpu=False):
@@ -390,8 +406,11 @@ def bench_moe(args, dev, peaks, world, flush, names, cpu=False):
             if key not in host_weights and host_bytes_available() > 2 * wbytes_all:
                 host_weights[key] = (wgu.cpu(), wd.cpu())
             if key in host_weights:
-                results[name]["cpu_baseline"] = cpu_baseline_routes(w, x, ids_cpu,
-                                                                    *host_weights[key])
+                base, sample, ref = cpu_baseline_routes(w, x, ids_cpu, *host_weights[key])
+                results[name]["cpu_baseline"] = base
+                # The GPU's outputs of the sampled routes against the oracle's.
+                got = y.view(-1, w.M).index_select(0, torch.from_numpy(sample).to(dev)).cpu()
+                results[name]["accuracy"] = accuracy_stats(got, ref.reshape(-1, w.M))
             else:
                 results[name]["cpu_baseline"] = {
                     "unavailable": f"host memory below twice the {wbytes_all / 1e9:.1f} GB of "
@@ -582,9 +601,39 @@ def bench_moe_train(args, dev, peaks, world, flush):
     return out
 
 
-def cpu_baseline(seconds: float, rows_hint: int = 0):
+def accuracy_stats(got, ref):
+    """Error of GPU outputs `got` (a bf16 or float tensor) against the FP64 oracle's `ref`
+    (same shape): the largest error over the FFN bound 2e-2 (1 + |ref|) the parity tests
+    use, the largest absolute error and the relative RMS error."""
+    import numpy as np
+
+    g = got.float().numpy().astype(np.float64).reshape(ref.shape)
+    err = np.abs(g - ref)
+    return {"reference": "FP64 oracle", "values": int(ref.size),
+            "max_err_over_bound": float((err / (2e-2 * (1.0 + np.abs(ref)))).max()),
+            "bound": "2e-2 (1 + |ref|)", "max_abs_err": float(err.max()),
+            "rms_rel_err": float(np.sqrt((err ** 2).sum() / max(float((ref ** 2).sum()), 1e-300)))}
+
+
+def ulp_stats(got, ref):
+    """Error of bf16 outputs against the FP64 oracle in bf16 ulps of the oracle's value:
+    2^(floor(log2 |ref|) - 7) for |ref| >= 2^-126, else 2^-133 (zero included)."""
+    import numpy as np
+
+    g = got.float().numpy().astype(np.float64).reshape(ref.shape)
+    a = np.abs(ref)
+    ulp = np.where(a >= 2.0 ** -126, np.exp2(np.floor(np.log2(np.maximum(a, 2.0 ** -126))) - 7),
+                   2.0 ** -133)
+    e = np.abs(g - ref) / ulp
+    return {"reference": "FP64 oracle", "values": int(ref.size), "max_ulp_err": float(e.max()),
+            "frac_within_half_ulp": float((e <= 0.5).mean()), "bound": "1 bf16 ulp"}
+
+
+def cpu_baseline(seconds: float, rows_hint: int = 0, inputs=None):
     """The FP64 oracle (as it stands) on a bounded sample of the dense workload's
-    rows: rows/s = tokens/s on the host cores."""
+    rows: rows/s = tokens/s on the host cores.  inputs: the GPU run's (x, W_gate_up,
+    W_down) on the host (generated on the CPU otherwise; the device generator's values
+    differ).  Returns the baseline and the oracle's outputs of the sampled rows."""
     import numpy as np
     import torch
 
@@ -593,23 +642,23 @@ def cpu_baseline(seconds: float, rows_hint: int = 0):
 
     o = Oracle()
     w = wl.WORKLOADS["dense"]
-    x, wgu, wd = wl.ffn_inputs(w.M, w.I, w.rows, seed=0)
+    x, wgu, wd = inputs if inputs is not None else wl.ffn_inputs(w.M, w.I, w.rows, seed=0)
     bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
     xb, wgb, wdb = bits(x), bits(wgu), bits(wd)
     threads = o.num_threads()
     n = rows_hint or max(threads, 8)
     t0 = time.perf_counter()
-    o.ffn_forward(xb[:n], wgb, wdb)
+    ref = o.ffn_forward(xb[:n], wgb, wdb)
     dt = time.perf_counter() - t0
     if not rows_hint and dt < seconds:
         n2 = min(w.rows, max(n, int(n * seconds / max(dt, 1e-3))))
         t0 = time.perf_counter()
-        o.ffn_forward(xb[:n2], wgb, wdb)
+        ref = o.ffn_forward(xb[:n2], wgb, wdb)
         dt = time.perf_counter() - t0
         n = n2
     return {"value": n / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"first {n} of the 16384 token rows of the dense workload "
-                      f"(FP64 gate_up, SiTU-GLU, down), {dt:.1f} s"}
+                      f"(FP64 gate_up, SiTU-GLU, down), {dt:.1f} s"}, ref
 
 
 def route_sample(ids_cpu, n: int, seed: int = 0):
@@ -657,7 +706,7 @@ def cpu_baseline_routes(w, x, ids_cpu, wgu_host, wd_host, n_routes: int = 4096):
     ids_s = ids_cpu.contiguous().view(-1)[torch.from_numpy(sample)].view(-1, 1).numpy()
     xs = bits(x.index_select(0, tokens.to(x.device)).cpu())
     t0 = time.perf_counter()
-    o.moe_grouped_forward(xs, ids_s, bits(wgu_host), bits(wd_host))
+    ref = o.moe_grouped_forward(xs, ids_s, bits(wgu_host), bits(wd_host))
     dt = time.perf_counter() - t0
     experts = int(np.unique(ids_s).size)
     return {"value": sample.size / dt / w.k_eff, "unit": "tokens/s",
@@ -666,7 +715,7 @@ def cpu_baseline_routes(w, x, ids_cpu, wgu_host, wd_host, n_routes: int = 4096):
                       f"row of all {experts} non-empty experts' groups, each route with its "
                       f"expert's own weights (FP64 grouped experts, "
                       f"per-route loop), {dt:.1f} s; tokens/s = routes/s / {w.k_eff}, "
-                      "extrapolated to the workload"}
+                      "extrapolated to the workload"}, sample, ref
 
 
 # ---------------------------------------------------------------------------
@@ -773,7 +822,8 @@ def run_situ(args):
 
     act = moe = mx = train = None
     if args.suite == "full":
-        act = with_clocks(lambda: bench_act(args, dev, peaks, world, flush))
+        check = 64 if rank == 0 and not args.no_cpu_baseline else 0
+        act = with_clocks(lambda: bench_act(args, dev, peaks, world, flush, check_rows=check))
         # The oracle's CPU baseline of the grouped workloads: rank 0 of a 1-GPU run.
         cpu_moe = rank == 0 and world == 1 and not args.no_cpu_baseline
         moe = with_clocks(lambda: bench_moe(args, dev, peaks, world, flush,
@@ -857,7 +907,9 @@ def run_situ(args):
     if train:
         line["train"] = train
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        line["cpu_baseline"], ref = cpu_baseline(args.cpu_seconds, inputs=dense["inputs"])
+        # The timed dense call's outputs of the oracle's rows against the oracle's.
+        line["accuracy"] = accuracy_stats(dense["y"][: ref.shape[0]], ref)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -115,3 +115,24 @@ def test_route_sample_covers_every_expert():
     # Fewer routes asked than the group ends: every group's first and last row is kept.
     ends = {int(i) for e in np.unique(flat) for i in np.nonzero(flat == e)[0][[0, -1]]}
     assert set(bench.route_sample(ids, 10, seed=0).tolist()) == ends
+
+
+def test_accuracy_and_ulp_stats():
+    """The bench's accuracy figures: error over the FFN bound 2e-2 (1 + |ref|), and bf16
+    ulps of the FP64 value (2^(floor(log2 |ref|) - 7), 2^-133 below 2^-126)."""
+    import math
+
+    import numpy as np
+    import torch
+
+    ref = np.array([1.0, 2.0])
+    a = bench.accuracy_stats(torch.tensor([1.0, 2.0625]), ref)
+    assert math.isclose(a["max_abs_err"], 0.0625)
+    assert math.isclose(a["max_err_over_bound"], 0.0625 / 0.06)
+    assert math.isclose(a["rms_rel_err"], math.sqrt(0.0625 ** 2 / 5.0))
+    u = bench.ulp_stats(torch.tensor([1.0 + 2.0 ** -7, 3.0, 0.0, 2.0 ** -130]),
+                        np.array([1.0, 3.0, 0.0, 0.0]))
+    assert math.isclose(u["max_ulp_err"], 2.0 ** 3)  # 2^-130 off a zero: 2^-130 / 2^-133
+    assert math.isclose(u["frac_within_half_ulp"], 0.5)  # 3.0 and 0.0 exact
+    u2 = bench.ulp_stats(torch.tensor([1.0 + 2.0 ** -7]), np.array([1.0]))
+    assert math.isclose(u2["max_ulp_err"], 1.0)
