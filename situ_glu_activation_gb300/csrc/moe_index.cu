@@ -15,6 +15,7 @@
 // The result is the same permutation on every run (no atomics decide order).
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "situ_internal.h"
@@ -24,6 +25,7 @@ namespace situ {
 namespace {
 
 constexpr int kChunk = 1024;
+constexpr int32_t kMaxExperts = 16384;  // the ABI's bound on E
 
 __global__ void index_count_kernel(const int32_t* __restrict__ ids, int64_t n, int32_t E,
                                    int32_t* __restrict__ counts, uint32_t* status) {
@@ -144,14 +146,27 @@ cudaError_t launch_build_index(const int32_t* expert_ids, int32_t* offsets,
   const int32_t nchunks = static_cast<int32_t>((n + kChunk - 1) / kChunk);
   int32_t* counts = static_cast<int32_t*>(workspace);
   const size_t hist_bytes = static_cast<size_t>(E) * 4;
+  const size_t scan_bytes = hist_bytes + 1024 * 4;
   cudaError_t e;
-  if (nchunks > 0) {
+  // The shared-memory opt-ins, set once per device for the largest expert count (a
+  // per-device property of each kernel; threads racing on the first call each set it).
+  static std::atomic<bool> smem_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!smem_set[dev].load(std::memory_order_acquire)) {
+    const int max_hist = static_cast<int>(kMaxExperts) * 4;
     for (auto fn : {reinterpret_cast<const void*>(index_count_kernel),
                     reinterpret_cast<const void*>(index_place_kernel)}) {
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(hist_bytes));
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_hist);
       if (e != cudaSuccess) return e;
     }
+    e = cudaFuncSetAttribute(reinterpret_cast<const void*>(index_scan_experts_kernel),
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, max_hist + 1024 * 4);
+    if (e != cudaSuccess) return e;
+    smem_set[dev].store(true, std::memory_order_release);
+  }
+  if (E > kMaxExperts) return cudaErrorInvalidValue;
+  if (nchunks > 0) {
     index_count_kernel<<<nchunks, 256, hist_bytes, stream>>>(expert_ids, n, E, counts, status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -159,11 +174,6 @@ cudaError_t launch_build_index(const int32_t* expert_ids, int32_t* offsets,
   // offsets; the placement adds an expert's offset to its chunk bases.
   index_scan_chunks_kernel<<<E, kScanThreads, 0, stream>>>(counts, nchunks, E, offsets);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const size_t scan_bytes = hist_bytes + 1024 * 4;
-  e = cudaFuncSetAttribute(reinterpret_cast<const void*>(index_scan_experts_kernel),
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(scan_bytes));
-  if (e != cudaSuccess) return e;
   index_scan_experts_kernel<<<1, 1024, scan_bytes, stream>>>(E, offsets);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (nchunks > 0) {
