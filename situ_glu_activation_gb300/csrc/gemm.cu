@@ -173,8 +173,8 @@ cudaError_t launch_gemm_situ(const GemmShape& s, const SituParams& p, Caps caps,
 cudaError_t launch_gemm_plain(const GemmShape& s, uint32_t* status, int num_sms,
                               cudaStream_t stream) {
   if (s.a_mn_major && s.b_mn_major && s.k_group_offsets)
-    return launch<Epi::kPlain, Caps::kBoth, false, Major::kABMNGrouped>(s, SituParams{}, status,
-                                                                       num_sms, stream);
+    return launch<Epi::kPlain, Caps::kBoth, false, Major::kABMNGrouped, 0, true>(
+        s, SituParams{}, status, num_sms, stream);
   if (s.a_mn_major && s.b_mn_major)
     return launch<Epi::kPlain, Caps::kBoth, false, Major::kABMN, 0, true>(s, SituParams{}, status,
                                                                          num_sms, stream);

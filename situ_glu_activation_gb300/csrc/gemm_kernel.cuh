@@ -204,10 +204,12 @@ __host__ __device__ constexpr int epi_col_groups() {
   return epi_warps<kEpi>() / 4;
 }
 // Threads per CTA: producer and MMA warps, the epilogue warps, and (MXFP8) the scale
-// copier or (activation derivative) the loader of the saved (g, u).
-template <Epi kEpi, int kMx>
+// copier, (activation derivative) the loader of the saved (g, u), or (K-grouped
+// contraction) the warp that zeroes the K rows past a group's end.
+template <Epi kEpi, int kMx, Major kMajor = Major::kKMajor>
 __host__ __device__ constexpr int block_threads() {
-  return 32 * (2 + epi_warps<kEpi>() + ((kMx || kEpi == Epi::kSituBwd) ? 1 : 0));
+  return 32 * (2 + epi_warps<kEpi>() +
+               ((kMx || kEpi == Epi::kSituBwd || kMajor == Major::kABMNGrouped) ? 1 : 0));
 }
 
 struct Args {
@@ -283,6 +285,7 @@ struct SharedCtl {
   uint64_t sf_drain;
   uint64_t gu_full[kGuSlots];   // dh GEMM: a slot's saved (g, u) have landed
   uint64_t gu_done[kGuSlots];   // dh GEMM: the epilogue warps are done with the slot
+  uint64_t tail_full[kMaxStages];  // two-CTA K-grouped: a group's last k-block has landed
   uint64_t wait_limit_ns;
   uint32_t tmem_base;
   volatile int abort;
@@ -352,13 +355,13 @@ __device__ __forceinline__ TileCoord in_group_tile(int32_t n_tiles, int32_t loca
 template <bool kPair, bool kKG, bool kTwo = false>
 __device__ __forceinline__ int32_t num_units(const Args& a) {
   if (kTwo) return a.fused_units1 + a.fused_units2;
-  if (kPair) {
-    if (a.unit_offsets) return __ldg(a.unit_offsets + a.num_groups);
-    return ((a.dense_rows + 2 * kBM - 1) / (2 * kBM)) * a.n_tiles;
-  }
   if (kKG) {
     if (a.tile_offsets && __ldg(a.tile_offsets + a.num_groups) == 0) return 0;
     return a.num_groups * a.units_per_group;
+  }
+  if (kPair) {
+    if (a.unit_offsets) return __ldg(a.unit_offsets + a.num_groups);
+    return ((a.dense_rows + 2 * kBM - 1) / (2 * kBM)) * a.n_tiles;
   }
   return total_tiles(a);
 }
@@ -409,6 +412,21 @@ __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_
     return c;
   }
   c.phase2 = 0;
+  if (kKG) {
+    // Every group has the same output tiles (one-CTA tiles, or two-CTA units of m-tile
+    // pairs); its K range is its row range.
+    const int32_t gi = u / a.units_per_group;
+    const int32_t local = u - gi * a.units_per_group;
+    const int32_t g = a.group_order ? __ldg(a.group_order + gi) : gi;
+    c = kPair ? pair_unit(a.n_tiles, local, rank, 0, a.dense_rows, false)
+              : in_group_tile(a.n_tiles, local, 0, a.dense_rows);
+    c.phase2 = 0;
+    c.group = g;
+    c.k0 = __ldg(a.k_group_offsets + g);
+    c.k_end = __ldg(a.k_group_offsets + g + 1);
+    c.k_blocks = c.k_end > c.k0 ? (c.k_end - c.k0 + kBK - 1) / kBK : 0;
+    return c;
+  }
   if (kPair) {
     // Dense, or grouped with a per-group prefix of two-CTA units.
     int32_t g = 0, row0 = 0, row_end = a.dense_rows, local = u;
@@ -429,19 +447,6 @@ __device__ __forceinline__ TileCoord unit_tile(const Args& a, int32_t u, uint32_
     c.k0 = 0;
     c.k_end = 0;
     c.k_blocks = a.k_blocks;
-    return c;
-  }
-  if (kKG) {
-    // Every group has the same output tiles; its K range is its row range.
-    const int32_t gi = u / a.units_per_group;
-    const int32_t local = u - gi * a.units_per_group;
-    const int32_t g = a.group_order ? __ldg(a.group_order + gi) : gi;
-    c = in_group_tile(a.n_tiles, local, 0, a.dense_rows);
-    c.phase2 = 0;
-    c.group = g;
-    c.k0 = __ldg(a.k_group_offsets + g);
-    c.k_end = __ldg(a.k_group_offsets + g + 1);
-    c.k_blocks = c.k_end > c.k0 ? (c.k_end - c.k0 + kBK - 1) / kBK : 0;
     return c;
   }
   c = decode_tile(a, u);
@@ -485,17 +490,22 @@ __device__ __forceinline__ bool ctl_wait(SharedCtl* ctl, uint64_t* bar, uint32_t
   }
 }
 
-// Zero K rows kv..63 of a stage's MN-major operand tiles (2 A atoms, 4 B
-// atoms): row k of a {64 MN, 64 K} 128-byte-swizzled atom is the 128 bytes at
-// k * 128 (the swizzle permutes 16-byte pieces within a row), so the tail is one
-// contiguous range per atom.  Warp-collective.
+// Zero K rows kv..63 of a stage's MN-major operand tiles (2 A atoms, and kBAtoms B
+// atoms: 4 for a one-CTA tile, 2 for a CTA's half of a two-CTA one): row k of a
+// {64 MN, 64 K} 128-byte-swizzled atom is the 128 bytes at k * 128 (the swizzle
+// permutes 16-byte pieces within a row), so the tail is one contiguous range per atom.
+// kPeer: sa and sb are the other CTA's (shared::cluster addresses).  Warp-collective.
+template <int kBAtoms, bool kPeer = false>
 __device__ __forceinline__ void zero_k_tail(uint32_t sa, uint32_t sb, int32_t kv, int lane) {
   const uint32_t first = static_cast<uint32_t>(kv) * 128u;
   const uint32_t n = (kMnAtomBytes - first) / 16u;
 #pragma unroll 1
-  for (int at = 0; at < 6; ++at) {
+  for (int at = 0; at < 2 + kBAtoms; ++at) {
     const uint32_t base = (at < 2 ? sa + at * kMnAtomBytes : sb + (at - 2) * kMnAtomBytes) + first;
-    for (uint32_t i = lane; i < n; i += 32) st_shared_zero16(base + 16u * i);
+    for (uint32_t i = lane; i < n; i += 32) {
+      if constexpr (kPeer) st_cluster_zero16(base + 16u * i);
+      else st_shared_zero16(base + 16u * i);
+    }
   }
 }
 
@@ -574,7 +584,7 @@ __host__ __device__ __forceinline__ int64_t sf_tile_offset(int64_t m_tile, int64
 // pair, or M = 128 for a grouped GEMM's half-pair tail); otherwise one CTA per tile
 // with cta_group::1 MMAs.
 template <Epi kEpi, Caps kC, bool kPair, bool kStoreGu, Major kMajor, int kMx = 0>
-__global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
+__global__ void __launch_bounds__(block_threads<kEpi, kMx, kMajor>(), 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_a64,
                     const __grid_constant__ CUtensorMap map_b,
@@ -588,8 +598,6 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
   using G = std::conditional_t<k2Cta,
                                std::conditional_t<kGuStage, GeoPairBwd, GeoPairT<kMx>>, Geo<kMx>>;
   constexpr uint32_t kGuBytes = kGuStage ? kGuSlots * kGuSlotBytes : 0u;
-  static_assert(!k2Cta || kMajor != Major::kABMNGrouped,
-                "two-CTA MMA: GEMMs without a K-grouped contraction");
   static_assert(G::Stages * G::StageBytes + kGuBytes + sizeof(SharedCtl) + 1024 <= 232448,
                 "shared memory per CTA");
   static_assert(!kMx || 2 * G::BN + kSfTmemCols * G::Stages <= kTmemCols,
@@ -639,6 +647,9 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
     if (kMx) {
       for (int s = 0; s < G::Stages; ++s) mbar_init(smem_u32(&ctl->sf_ready[s]), 1);
       mbar_init(smem_u32(&ctl->sf_drain), 1);
+    }
+    if (kKG && k2Cta) {
+      for (int s = 0; s < G::Stages; ++s) mbar_init(smem_u32(&ctl->tail_full[s]), 1);
     }
     if (kGuStage) {
       for (int s = 0; s < kGuSlots; ++s) {
@@ -763,8 +774,14 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
             // CTA, and its SiTU tile's B half in CTA r is gate rows n0 + 64r .. +63 then
             // the matching up rows, so each accumulator lane pairs gate and up columns.
             const bool hp = pair_half_tile(tc);
-            const uint32_t full0 = map_to_rank(full, 0);
-            if (rank == 0) mbar_arrive_expect_tx(full, hp ? G::TxBytes - G::ABytes : G::TxBytes);
+            // K-grouped: a group's last k-block holds K rows past its end; its copies count
+            // on the even CTA's tail barrier, and the zeroing warp clears those rows in both
+            // CTAs' tiles before it completes the stage's full barrier.
+            const uint32_t fbar = (kKG && tc.k_end - (tc.k0 + kb * G::BK) < G::BK)
+                                      ? smem_u32(&ctl->tail_full[stage])
+                                      : full;
+            const uint32_t full0 = map_to_rank(fbar, 0);
+            if (rank == 0) mbar_arrive_expect_tx(fbar, hp ? G::TxBytes - G::ABytes : G::TxBytes);
             const int32_t kxa = kb * G::BK + tc.k0, kxb2 = kb * G::BK + kb_off;
             const int32_t brow = rank == 0 ? b_row0 : b_row1;
             if constexpr (a_mn_major(kMajor)) {
@@ -866,18 +883,20 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    // Lane 0 waits and issues.  K-grouped contractions run the whole warp: the
+    // Lane 0 waits and issues.  One-CTA K-grouped contractions run the whole warp: the
     // last k-block of a group holds the next group's first rows (or fill) past
-    // k_end, and the warp zeroes those K rows of both operands before the MMAs.
+    // k_end, and the warp zeroes those K rows of both operands before the MMAs (two-CTA:
+    // the zeroing warp does, before the stage's full barrier completes).
     // Two-CTA: the even CTA's thread issues the pair's MMAs; the odd CTA's MMA warp idles.
-    if ((kKG || lane == 0) && (!k2Cta || rank == 0)) {
+    constexpr bool kWarpZero = kKG && !k2Cta;
+    if ((kWarpZero || lane == 0) && (!k2Cta || rank == 0)) {
       uint32_t stage = 0, phase = 0;
       uint32_t local = 0;
       bool ok = true;
       auto wait = [&](uint64_t* bar, uint32_t par) {
         int w = 1;
         if (lane == 0) w = ctl_wait(ctl, bar, par, args.status) ? 1 : 0;
-        if (kKG) w = __shfl_sync(0xFFFFFFFFu, w, 0);
+        if (kWarpZero) w = __shfl_sync(0xFFFFFFFFu, w, 0);
         return w != 0;
       };
       for (int32_t i = 0; i * ustride < n_total && ok; ++i) {
@@ -907,10 +926,10 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
           tc_fence_after_sync();
           const uint32_t sa = smem_u32(smem + stage * G::StageBytes);
           const uint32_t sb = sa + G::ABytes;
-          if (kKG) {
+          if (kWarpZero) {
             const int32_t kv = tcm.k_end - (tcm.k0 + kb * G::BK);
             if (kv < G::BK) {
-              zero_k_tail(sa, sb, kv, lane);
+              zero_k_tail<4>(sa, sb, kv, lane);
               fence_proxy_async_smem();
             }
             __syncwarp();
@@ -1029,6 +1048,42 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
         if constexpr (k2Cta) umma_commit_pair(smem_u32(&ctl->sf_drain), 0x1);
         else umma_commit(smem_u32(&ctl->sf_drain));
         mbar_wait(smem_u32(&ctl->sf_drain), 0, nullptr, kDrainLimitNs);
+      }
+    }
+  } else if (kKG && k2Cta && warp == 2 + epi_warps<kEpi>()) {
+    // ---------------- K-tail zeroing (two-CTA K-grouped contractions) ----------------
+    // Only a unit's last k-block can run past its group's end.  The even CTA's warp waits
+    // for that stage's copies of both CTAs on the tail barrier, zeroes the K rows past the
+    // end in its own A and B atoms and, through distributed shared memory, in the odd
+    // CTA's, makes the writes visible to the async proxy and completes the stage's full
+    // barrier, on which the MMA thread waits as for any stage.  A stage's tail barrier
+    // completes once per K-tail use: one parity bit per stage.
+    if (rank == 0) {
+      uint32_t stage = 0, tail_parity = 0;
+      for (int32_t i = 0; i * ustride < n_total; ++i) {
+        const int32_t t = round_unit<kKG>(i, u0, ustride);
+        if (t >= n_total) continue;
+        const TileCoord tcz = unit_tile<kPair, kKG, kTwo>(args, t, rank);
+        const int32_t kb_last = tcz.k_blocks - 1;
+        const int32_t kv = tcz.k_end - (tcz.k0 + kb_last * G::BK);
+        if (tcz.k_blocks > 0 && kv < G::BK) {
+          const uint32_t ts = (stage + static_cast<uint32_t>(kb_last)) % G::Stages;
+          int w = 1;
+          if (lane == 0)
+            w = ctl_wait<true>(ctl, &ctl->tail_full[ts], (tail_parity >> ts) & 1u, args.status)
+                    ? 1 : 0;
+          w = __shfl_sync(0xFFFFFFFFu, w, 0);
+          if (!w) break;
+          tail_parity ^= 1u << ts;
+          const uint32_t sa = smem_u32(smem + ts * G::StageBytes);
+          const uint32_t sb = sa + G::ABytes;
+          zero_k_tail<2>(sa, sb, kv, lane);
+          zero_k_tail<2, true>(map_to_rank(sa, 1), map_to_rank(sb, 1), kv, lane);
+          fence_proxy_async_cluster_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&ctl->full[ts]));
+        }
+        stage = (stage + static_cast<uint32_t>(tcz.k_blocks)) % G::Stages;
       }
     }
   } else if (kGuStage && warp == 2 + epi_warps<kEpi>()) {
@@ -1559,7 +1614,7 @@ int max_pair_clusters(size_t smem) {
   if (c == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(block_threads<kEpi, kMx>(), 1, 1);
+    cfg.blockDim = dim3(block_threads<kEpi, kMx, kMajor>(), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -1671,11 +1726,12 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     smem_set[dev].store(true, std::memory_order_release);
   }
   if constexpr (k2Cta) {
-    // Two-CTA MMA for a dense call, or a grouped call whose unit prefix counts two-CTA
-    // units (pair_units).
+    // Two-CTA MMA for a dense call, a grouped call whose unit prefix counts two-CTA
+    // units (pair_units), or a K-grouped contraction.
     const bool dense = !s.group_offsets && !s.tile_offsets && !s.k_group_offsets &&
                        !s.out_row_index && !s.combine_w;
-    const bool use2 = dense || (s.pair_units && s.unit_offsets && !s.k_group_offsets);
+    const bool kgrouped = kMajor == Major::kABMNGrouped && s.k_group_offsets;
+    const bool use2 = dense || kgrouped || (s.pair_units && s.unit_offsets && !s.k_group_offsets);
     int clusters2 =
         use2 ? max_pair_clusters<kEpi, kC, kStoreGu, kMajor, kMx>(
                    smem_bytes_pair_epi<kEpi, kMx>())
@@ -1706,10 +1762,15 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
       if (dense) {
         const int64_t units = ((m_tiles + 1) / 2) * a.n_tiles;
         if (units < clusters2) clusters2 = static_cast<int>(units);
+      } else if (kgrouped) {
+        // Every group: units (p, n) over the output's m-tile pairs and n-tiles.
+        a.units_per_group = static_cast<int32_t>(((m_tiles + 1) / 2) * a.n_tiles);
+        const int64_t units = static_cast<int64_t>(a.units_per_group) * s.num_groups;
+        if (units < clusters2) clusters2 = static_cast<int>(units < 1 ? 1 : units);
       }
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * clusters2, 1, 1);
-      cfg.blockDim = dim3(block_threads<kEpi, kMx>(), 1, 1);
+      cfg.blockDim = dim3(block_threads<kEpi, kMx, kMajor>(), 1, 1);
       cfg.dynamicSmemBytes = smem_bytes_pair_epi<kEpi, kMx>();
       cfg.stream = stream;
       cudaLaunchAttribute attr;
@@ -1735,7 +1796,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     if (tiles < grid) grid = static_cast<int>(tiles);
   }
   ffn_gemm_kernel<kEpi, kC, false, kStoreGu, kMajor, kMx>
-      <<<grid, block_threads<kEpi, kMx>(), kSmem, stream>>>(ma, ma64, mb, ma, ma64, mb, a);
+      <<<grid, block_threads<kEpi, kMx, kMajor>(), kSmem, stream>>>(ma, ma64, mb, ma, ma64, mb, a);
   return cudaGetLastError();
 }
 

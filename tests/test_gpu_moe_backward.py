@@ -180,6 +180,26 @@ def test_grouped_backward_two_cta_tails(oracle, cuda_dev, M, I):
     _check(oracle, x, ids, wgu, wd, dy, got, what=f"two-CTA tails M={M} I={I}")
 
 
+def test_grouped_backward_weight_gradient_k_tails(oracle, cuda_dev):
+    """The weight gradients contract each expert over its own routes in 64-route
+    k-blocks on two-CTA MMAs: experts of 1, 63, 64, 65, 130 and 191 routes (a last
+    k-block of 1..64 valid routes, followed by the next expert's rows or, for the last
+    expert, the end of the buffer), an empty expert, and output row counts (M = 128
+    for dW_down, 2I = 384 for dW_gate_up) with an odd number of 128-row m-tiles, whose
+    last pair has a second half past the rows."""
+    sizes = [1, 63, 64, 65, 0, 130, 191]
+    E, M, I = len(sizes), 128, 192
+    ids = torch.cat([torch.full((n,), e, dtype=torch.int32) for e, n in enumerate(sizes)])
+    ids = ids[torch.randperm(ids.numel(), generator=torch.Generator().manual_seed(51))][:, None]
+    T = ids.shape[0]
+    x = wl.normal((T, M), 1.0, seed=52)
+    wgu, wd = wl.expert_weights(E, M, I, seed=53)
+    dy = wl.normal((T, 1, M), 1.0, seed=54)
+    _, got = _train_step(x, ids, wgu, wd, dy, cuda_dev)
+    assert not got[1][4].any() and not got[2][4].any()  # the empty expert
+    _check(oracle, x, ids, wgu, wd, dy, got, what="weight-gradient K tails")
+
+
 def test_grouped_backward_no_routes(cuda_dev):
     E, M, I = 3, 64, 64
     x = torch.empty(0, M, dtype=torch.bfloat16, device=cuda_dev)
