@@ -578,6 +578,26 @@ situ_status situ_moe_combine(const void* y, const float* weights, void* out, int
                              int32_t k_eff, int64_t M, situ_dtype dt, void* stream);
 
 /* -------------------------------------------------------------------------
+ * situ_selftest_group_maps -- self test of the per-group tensor maps of the
+ * K-grouped weight-gradient GEMMs (no counterpart on the pages).  Encodes two tensor
+ * maps over MN-major operands of `rows` x `cols` (and 2 * cols) bf16 elements on the
+ * host, lets a kernel write one copy of each per group with its row extent set to the
+ * group's end k_offsets[g + 1], copies them back and compares each byte for byte with
+ * the driver's own encoding of that base and extent (a group ending before row 32 gets
+ * 32 rows from a base moved that many rows earlier; a group without rows keeps the
+ * template).  No copy reads through the maps.
+ *   k_offsets   host, [groups + 1] int32, non-decreasing, k_offsets[0] >= 0,
+ *               k_offsets[groups] <= rows.
+ *   groups      1 .. 65536;  rows 1 .. 2^31 - 1;  cols a multiple of 8.
+ *   mismatches  host, out, [2 * groups] int32: entry 2g (A) and 2g + 1 (B) are 1 where
+ *               group g's map differs from the driver's encoding, else 0.
+ * Synchronises `stream`; allocates and frees a little device memory.
+ * Errors: SITU_ERR_ARG, SITU_ERR_CUDA.
+ * ------------------------------------------------------------------------- */
+situ_status situ_selftest_group_maps(const int32_t* k_offsets, int32_t groups, int64_t rows,
+                                     int64_t cols, int32_t* mismatches, void* stream);
+
+/* -------------------------------------------------------------------------
  * situ_selftest_bounded_wait -- failure-detection self test (no counterpart on
  * the pages).  Launches one block that waits on a shared-memory barrier nothing
  * ever completes, with a wait limit of `limit_us` microseconds (1..1000000).

@@ -24,7 +24,7 @@ from .api import (MX_DOWN, MX_E2M1, MX_E4M3, MX_GATE_UP, MxWeights, SituError,
                   situ_ffn_gate_up_mxfp8, situ_moe_grouped_forward_mxfp8, device_status, ffn_backward_workspace_bytes,
                   ffn_last_path, FFN_PATH_FUSED, FFN_PATH_TWO_LAUNCHES, ffn_set_single_launch,
                   ffn_host_workspace_bytes, ffn_workspace_bytes, moe_backward_workspace_bytes,
-                  moe_workspace_bytes, selftest_bounded_wait, set_wait_limit_ns,
+                  moe_workspace_bytes, selftest_bounded_wait, selftest_group_maps, set_wait_limit_ns,
                   situ_ffn_backward, situ_ffn_down,
                   situ_ffn_forward, situ_ffn_forward_host, situ_ffn_forward_train,
                   situ_ffn_gate_up, situ_glu_act, situ_moe_build_index, situ_moe_combine,
@@ -36,7 +36,7 @@ __all__ = [
     "situ_ffn_down",
     "situ_moe_build_index",
     "situ_moe_grouped_forward", "ffn_workspace_bytes", "moe_workspace_bytes",
-    "device_status", "selftest_bounded_wait", "set_wait_limit_ns", "ffn_host_workspace_bytes",
+    "device_status", "selftest_bounded_wait", "selftest_group_maps", "set_wait_limit_ns", "ffn_host_workspace_bytes",
     "situ_moe_combine",
     "ffn_last_path", "FFN_PATH_FUSED", "FFN_PATH_TWO_LAUNCHES", "ffn_set_single_launch",
     "situ_ffn_forward_train", "situ_ffn_backward", "ffn_backward_workspace_bytes",

@@ -75,6 +75,7 @@ SIGNATURES = {
     "situ_moe_grouped_forward_mxfp8": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _vp, _vp, _sz,
                                         _i64, _i32, _i32, _i64, _i64, _f32, _f32, _vp], _ci),
     "situ_selftest_bounded_wait": ([_u32, _vp], _ci),
+    "situ_selftest_group_maps": ([_vp, _i32, _i64, _i64, _vp, _vp], _ci),
     "situ_set_wait_limit_ns": ([_u64], _u64),
 }
 

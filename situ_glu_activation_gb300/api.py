@@ -8,6 +8,7 @@ CPU or PyTorch fallback, and a missing library raises.
 """
 from __future__ import annotations
 
+import numpy as np
 import torch
 
 from . import _native
@@ -651,6 +652,19 @@ def set_wait_limit_ns(ns: int) -> int:
     return int(_native.lib().situ_set_wait_limit_ns(int(ns)))
 
 
+def selftest_group_maps(k_offsets, rows: int, cols: int) -> int:
+    """Per-group tensor maps written on the device against the driver's encoding:
+    returns [groups, 2] int32 flags, 1 where group g's A or B map differs (see
+    situ_selftest_group_maps)."""
+    off = np.ascontiguousarray(np.asarray(k_offsets, dtype=np.int32))
+    out = np.zeros(2 * (len(off) - 1), dtype=np.int32)
+    check("situ_selftest_group_maps",
+          _native.lib().situ_selftest_group_maps(off.ctypes.data, len(off) - 1, int(rows),
+                                                 int(cols), out.ctypes.data,
+                                                 _stream(torch.device("cuda"))))
+    return out.reshape(-1, 2)
+
+
 def selftest_bounded_wait(limit_us: int = 2000) -> None:
     """Launch the bounded-wait self test on the current stream."""
     check("situ_selftest_bounded_wait",
@@ -663,7 +677,7 @@ __all__ = [
     "situ_ffn_down",
     "situ_moe_build_index",
     "situ_moe_grouped_forward", "ffn_workspace_bytes", "moe_workspace_bytes",
-    "device_status", "selftest_bounded_wait", "set_wait_limit_ns", "ffn_host_workspace_bytes", "situ_moe_combine",
+    "device_status", "selftest_bounded_wait", "selftest_group_maps", "set_wait_limit_ns", "ffn_host_workspace_bytes", "situ_moe_combine",
     "ffn_last_path", "FFN_PATH_FUSED", "FFN_PATH_TWO_LAUNCHES", "ffn_set_single_launch",
     "situ_ffn_forward_train", "situ_ffn_backward", "ffn_backward_workspace_bytes",
     "situ_moe_grouped_forward_train", "situ_moe_grouped_backward", "moe_backward_workspace_bytes",

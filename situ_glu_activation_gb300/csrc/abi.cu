@@ -753,16 +753,29 @@ situ_status situ_moe_grouped_forward_combined(const void* x, const int32_t* expe
   return finish(launch_f32_to_bf16(acc, out, T * M, st->num_sms, cs));
 }
 
+}  // extern "C"
+
+namespace {
+// Bytes of one GEMM's per-expert tensor maps (two 128-byte maps per expert).
+size_t moe_group_maps_bytes(int32_t E) {
+  return round_up(static_cast<size_t>(E) * 2 * 128, 256);
+}
+}  // namespace
+
+extern "C" {
+
 size_t situ_moe_backward_workspace_size(int64_t R, int32_t E, int64_t M, int64_t I,
                                         situ_dtype dt) {
   if (R < 0 || E < 1 || M < 1 || I < 1 || dt != SITU_BF16) return 0;
   // m-tile prefix + work-unit prefixes of the dh and dx GEMMs + the experts by
-  // descending rows, one [R, M] buffer (dy in expert order, then the per-route dx,
-  // then x in expert order) and d(g, u) [R, 2I] in expert order.
+  // descending rows, the per-expert tensor maps of the two weight-gradient GEMMs, one
+  // [R, M] buffer (dy in expert order, then the per-route dx, then x in expert order)
+  // and d(g, u) [R, 2I] in expert order.
   const size_t tiles = 4 * round_up(static_cast<size_t>(E + 1) * 4, 256);
+  const size_t maps = 2 * moe_group_maps_bytes(E);
   const size_t rows_m = round_up(static_cast<size_t>(R) * M * 2, 256);
   const size_t dgu = round_up(static_cast<size_t>(R) * 2 * I * 2, 256);
-  return tiles + rows_m + dgu;
+  return tiles + maps + rows_m + dgu;
 }
 
 situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offsets,
@@ -816,11 +829,14 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
   int32_t* units_dh = reinterpret_cast<int32_t*>(ws + prefix_bytes);
   int32_t* units_dx = reinterpret_cast<int32_t*>(ws + 2 * prefix_bytes);
   int32_t* expert_order = reinterpret_cast<int32_t*>(ws + 3 * prefix_bytes);
-  void* rows_m = ws + 4 * prefix_bytes;  // [R, M]: dy, then per-route dx, then x
+  void* maps_dwd = ws + 4 * prefix_bytes;  // per-expert tensor maps of dW_down
+  void* maps_dwg = static_cast<uint8_t*>(maps_dwd) + moe_group_maps_bytes(E);  // of dW_gate_up
+  void* rows_m = static_cast<uint8_t*>(maps_dwg) + moe_group_maps_bytes(E);  // [R, M]
   void* dgu = static_cast<uint8_t*>(rows_m) + round_up(static_cast<size_t>(R) * M * 2, 256);
   const SituParams p = make_situ_params(beta, linear_beta);
   // The dh and dx GEMMs run as two-CTA MMAs when experts average >= 128 rows (as the
-  // forward); the K-grouped weight gradients keep one CTA per tile.
+  // forward); the K-grouped weight gradients always do (one CTA per tile only where
+  // two-CTA clusters cannot be launched).
   const bool two_cta = R >= kTwoCtaMinRows * static_cast<int64_t>(E) && gemm_two_cta_available();
   cudaError_t e = launch_group_tiles(expert_offsets, E, R, gemm_n_tiles_wide(I),
                                      gemm_n_tiles_wide(M), tile_offsets, units_dh, units_dx,
@@ -871,6 +887,7 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
     g.tile_offsets = tile_offsets;
     g.k_group_offsets = expert_offsets;
     g.group_order = expert_order;
+    g.group_maps = maps_dwd;
     g.out_group_rows = M;
     g.n_out = I;
     g.out = dW_down;
@@ -924,6 +941,7 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
     g.tile_offsets = tile_offsets;
     g.k_group_offsets = expert_offsets;
     g.group_order = expert_order;
+    g.group_maps = maps_dwg;
     g.out_group_rows = 2 * I;
     g.n_out = M;
     g.out = dW_gate_up;
@@ -1322,6 +1340,22 @@ situ_status situ_moe_combine(const void* y, const float* weights, void* out, int
 
 uint64_t situ_set_wait_limit_ns(uint64_t ns) {
   return g_wait_limit_ns.exchange(ns == 0 ? kDefaultWaitLimitNs : ns);
+}
+
+situ_status situ_selftest_group_maps(const int32_t* k_offsets, int32_t groups, int64_t rows,
+                                     int64_t cols, int32_t* mismatches, void* stream) {
+  if (!k_offsets || !mismatches || groups < 1 || groups > (1 << 16) || rows < 1 ||
+      rows >= (int64_t(1) << 31) || cols < 8 || cols % 8 || cols >= (int64_t(1) << 30))
+    return SITU_ERR_ARG;
+  for (int32_t g = 0; g < groups; ++g)
+    if (k_offsets[g] < 0 || k_offsets[g + 1] < k_offsets[g] || k_offsets[g + 1] > rows)
+      return SITU_ERR_ARG;
+  DeviceState* st = nullptr;
+  situ_status s = device_state(&st);
+  if (s != SITU_OK) return s;
+  const cudaError_t e = group_maps_selftest(k_offsets, groups, rows, cols, mismatches,
+                                            static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SITU_OK : report_cuda_error(e);
 }
 
 situ_status situ_selftest_bounded_wait(uint32_t limit_us, void* stream) {

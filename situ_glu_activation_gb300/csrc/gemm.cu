@@ -14,6 +14,9 @@
 
 #include <cstdint>
 
+#include <cstring>
+#include <vector>
+
 #include "gemm_kernel.cuh"
 
 namespace situ {
@@ -283,6 +286,59 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* token_index, void* 
       static_cast<const uint4*>(x), token_index, static_cast<uint4*>(x_perm), R, k_eff, M / 8,
       T, status);
   return cudaGetLastError();
+}
+
+// Writes per-group row extents into device copies of two host-encoded maps and compares
+// each with the driver's own encoding of that base and extent (no copy uses the maps):
+// mismatches[2g], [2g + 1] = 1 where group g's A or B map differs.
+cudaError_t group_maps_selftest(const int32_t* k_offsets, int32_t groups, int64_t rows,
+                                int64_t cols, int32_t* mismatches, cudaStream_t stream) {
+  for (int32_t i = 0; i < 2 * groups; ++i) mismatches[i] = -1;
+  void* alloc = nullptr;
+  int32_t* d_off = nullptr;
+  CUtensorMap* d_maps = nullptr;
+  cudaError_t e = cudaMalloc(&alloc, 2048);
+  if (e == cudaSuccess) e = cudaMalloc(&d_off, sizeof(int32_t) * (groups + 1));
+  if (e == cudaSuccess) e = cudaMalloc(&d_maps, sizeof(CUtensorMap) * 2 * groups);
+  std::vector<CUtensorMap> got(2 * static_cast<size_t>(groups));
+  // Operand A [rows, cols] at base_a, B [rows, 2 cols] at base_b (only encoded).
+  uint8_t* base_a = static_cast<uint8_t*>(alloc) + 1024;
+  uint8_t* base_b = base_a + 512;
+  const int64_t ld_a = cols * 2, ld_b = 4 * cols;
+  CUtensorMap ta, tb;
+  if (e == cudaSuccess && !(make_map(&ta, base_a, rows, cols, 64, cols) &&
+                            make_map(&tb, base_b, rows, 2 * cols, 64, 2 * cols)))
+    e = cudaErrorInvalidValue;
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(d_off, k_offsets, sizeof(int32_t) * (groups + 1), cudaMemcpyHostToDevice,
+                        stream);
+  if (e == cudaSuccess) {
+    group_maps_kernel<<<(groups + 127) / 128, 128, 0, stream>>>(ta, tb, base_a, base_b, ld_a,
+                                                                 ld_b, d_off, groups, d_maps);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(got.data(), d_maps, sizeof(CUtensorMap) * 2 * groups,
+                        cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  for (int32_t g = 0; e == cudaSuccess && g < groups; ++g) {
+    const int32_t k0 = k_offsets[g], k_end = k_offsets[g + 1];
+    CUtensorMap ea = ta, eb = tb;
+    if (k_end > k0 && k0 >= 0) {
+      const int32_t shift = group_map_shift(k_end);
+      if (!(make_map(&ea, base_a - shift * ld_a, k_end + shift, cols, 64, cols) &&
+            make_map(&eb, base_b - shift * ld_b, k_end + shift, 2 * cols, 64, 2 * cols))) {
+        e = cudaErrorInvalidValue;
+        break;
+      }
+    }
+    mismatches[2 * g] = std::memcmp(&got[2 * g], &ea, sizeof(CUtensorMap)) != 0;
+    mismatches[2 * g + 1] = std::memcmp(&got[2 * g + 1], &eb, sizeof(CUtensorMap)) != 0;
+  }
+  cudaFree(d_maps);
+  cudaFree(d_off);
+  cudaFree(alloc);
+  return e;
 }
 
 cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, uint32_t* status,

@@ -87,6 +87,13 @@ enum class Major { kKMajor = 0, kBMN = 1, kABMN = 2, kABMNGrouped = 3 };
 __host__ __device__ constexpr bool a_mn_major(Major m) { return m == Major::kABMN || m == Major::kABMNGrouped; }
 constexpr uint32_t kAMnBit = 1u << 15, kBMnBit = 1u << 16;
 constexpr uint32_t kMnAtomBytes = 64 * 64 * 2;
+// Two-CTA K-grouped contractions read each group through tensor maps whose rows end at
+// the group's end (group_maps_kernel); such a map spans at least kMinGroupMapRows rows, a
+// group ending before that row is read through a map based group_map_shift rows earlier.
+constexpr int32_t kMinGroupMapRows = 32;
+__host__ __device__ __forceinline__ int32_t group_map_shift(int32_t k_end) {
+  return k_end < kMinGroupMapRows ? kMinGroupMapRows - k_end : 0;
+}
 
 // Tile geometry per operand type.  Both stage 128-byte rows of K (one 128-byte
 // swizzle row): 64 bf16 or 128 MXFP8 codes.
@@ -204,12 +211,10 @@ __host__ __device__ constexpr int epi_col_groups() {
   return epi_warps<kEpi>() / 4;
 }
 // Threads per CTA: producer and MMA warps, the epilogue warps, and (MXFP8) the scale
-// copier, (activation derivative) the loader of the saved (g, u), or (K-grouped
-// contraction) the warp that zeroes the K rows past a group's end.
-template <Epi kEpi, int kMx, Major kMajor = Major::kKMajor>
+// copier or (activation derivative) the loader of the saved (g, u).
+template <Epi kEpi, int kMx>
 __host__ __device__ constexpr int block_threads() {
-  return 32 * (2 + epi_warps<kEpi>() +
-               ((kMx || kEpi == Epi::kSituBwd || kMajor == Major::kABMNGrouped) ? 1 : 0));
+  return 32 * (2 + epi_warps<kEpi>() + ((kMx || kEpi == Epi::kSituBwd) ? 1 : 0));
 }
 
 struct Args {
@@ -242,6 +247,9 @@ struct Args {
   // offsets as validated (zero: nothing runs).
   const int32_t* k_group_offsets;
   const int32_t* group_order;  // K-grouped: the groups in this order (null: index order)
+  // Two-CTA K-grouped: per group, the A and B maps whose row extent ends at the group's
+  // end (2g, 2g + 1; see group_maps_kernel).
+  const CUtensorMap* group_maps;
   int32_t units_per_group;
   int64_t out_group_rows;
   // MXFP8: the scale tiles of A (per global m-tile and k-block, 512 bytes) and of
@@ -285,7 +293,6 @@ struct SharedCtl {
   uint64_t sf_drain;
   uint64_t gu_full[kGuSlots];   // dh GEMM: a slot's saved (g, u) have landed
   uint64_t gu_done[kGuSlots];   // dh GEMM: the epilogue warps are done with the slot
-  uint64_t tail_full[kMaxStages];  // two-CTA K-grouped: a group's last k-block has landed
   uint64_t wait_limit_ns;
   uint32_t tmem_base;
   volatile int abort;
@@ -584,7 +591,7 @@ __host__ __device__ __forceinline__ int64_t sf_tile_offset(int64_t m_tile, int64
 // pair, or M = 128 for a grouped GEMM's half-pair tail); otherwise one CTA per tile
 // with cta_group::1 MMAs.
 template <Epi kEpi, Caps kC, bool kPair, bool kStoreGu, Major kMajor, int kMx = 0>
-__global__ void __launch_bounds__(block_threads<kEpi, kMx, kMajor>(), 1)
+__global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
     ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_a64,
                     const __grid_constant__ CUtensorMap map_b,
@@ -648,9 +655,6 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx, kMajor>(), 1)
       for (int s = 0; s < G::Stages; ++s) mbar_init(smem_u32(&ctl->sf_ready[s]), 1);
       mbar_init(smem_u32(&ctl->sf_drain), 1);
     }
-    if (kKG && k2Cta) {
-      for (int s = 0; s < G::Stages; ++s) mbar_init(smem_u32(&ctl->tail_full[s]), 1);
-    }
     if (kGuStage) {
       for (int s = 0; s < kGuSlots; ++s) {
         mbar_init(smem_u32(&ctl->gu_full[s]), 1);
@@ -701,6 +705,8 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx, kMajor>(), 1)
       uint32_t stage = 0, phase = 0;
       uint32_t issued = 0;
       bool ok = true;
+      int32_t last_group = -1;  // two-CTA K-grouped: the group whose maps were acquired
+      (void)last_group;
       for (int32_t i = 0; i * ustride < n_total && ok; ++i) {
         const int32_t t = round_unit<kKG>(i, u0, ustride);
         if (t >= n_total) continue;
@@ -711,6 +717,22 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx, kMajor>(), 1)
         const CUtensorMap* pm_a = p2 ? &map_a2 : &map_a;
         const CUtensorMap* pm_a64 = p2 ? &map_a2_64 : &map_a64;
         const CUtensorMap* pm_b = p2 ? &map_b2 : &map_b;
+        // Two-CTA K-grouped: the group's own maps, whose rows end at the group's end, so
+        // that its last k-block reads zeros past it (a group ending before row
+        // kMinGroupMapRows: maps based that many rows earlier, coordinates shifted).
+        int32_t k_shift = 0;
+        if constexpr (kKG && k2Cta) {
+          if (tc.k_blocks > 0) {
+            pm_a = args.group_maps + 2 * tc.group;
+            pm_b = pm_a + 1;
+            k_shift = group_map_shift(tc.k_end);
+            if (tc.group != last_group) {
+              fence_tensormap_acquire(pm_a);
+              fence_tensormap_acquire(pm_b);
+              last_group = tc.group;
+            }
+          }
+        }
         const bool situ_tile = kSituEpi || (kFfn && !p2);
         constexpr bool kBMNp = kMajor != Major::kKMajor;
         // K-major B: a group's weights are b_group_rows further down the N rows.
@@ -774,15 +796,9 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx, kMajor>(), 1)
             // CTA, and its SiTU tile's B half in CTA r is gate rows n0 + 64r .. +63 then
             // the matching up rows, so each accumulator lane pairs gate and up columns.
             const bool hp = pair_half_tile(tc);
-            // K-grouped: a group's last k-block holds K rows past its end; its copies count
-            // on the even CTA's tail barrier, and the zeroing warp clears those rows in both
-            // CTAs' tiles before it completes the stage's full barrier.
-            const uint32_t fbar = (kKG && tc.k_end - (tc.k0 + kb * G::BK) < G::BK)
-                                      ? smem_u32(&ctl->tail_full[stage])
-                                      : full;
-            const uint32_t full0 = map_to_rank(fbar, 0);
-            if (rank == 0) mbar_arrive_expect_tx(fbar, hp ? G::TxBytes - G::ABytes : G::TxBytes);
-            const int32_t kxa = kb * G::BK + tc.k0, kxb2 = kb * G::BK + kb_off;
+            const uint32_t full0 = map_to_rank(full, 0);
+            if (rank == 0) mbar_arrive_expect_tx(full, hp ? G::TxBytes - G::ABytes : G::TxBytes);
+            const int32_t kxa = kb * G::BK + tc.k0 + k_shift, kxb2 = kb * G::BK + kb_off + k_shift;
             const int32_t brow = rank == 0 ? b_row0 : b_row1;
             if constexpr (a_mn_major(kMajor)) {
               for (int j = 0; j < 2; ++j)
@@ -886,7 +902,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx, kMajor>(), 1)
     // Lane 0 waits and issues.  One-CTA K-grouped contractions run the whole warp: the
     // last k-block of a group holds the next group's first rows (or fill) past
     // k_end, and the warp zeroes those K rows of both operands before the MMAs (two-CTA:
-    // the zeroing warp does, before the stage's full barrier completes).
+    // the group's tensor maps end at k_end, so those rows arrive as zeros).
     // Two-CTA: the even CTA's thread issues the pair's MMAs; the odd CTA's MMA warp idles.
     constexpr bool kWarpZero = kKG && !k2Cta;
     if ((kWarpZero || lane == 0) && (!k2Cta || rank == 0)) {
@@ -1048,42 +1064,6 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx, kMajor>(), 1)
         if constexpr (k2Cta) umma_commit_pair(smem_u32(&ctl->sf_drain), 0x1);
         else umma_commit(smem_u32(&ctl->sf_drain));
         mbar_wait(smem_u32(&ctl->sf_drain), 0, nullptr, kDrainLimitNs);
-      }
-    }
-  } else if (kKG && k2Cta && warp == 2 + epi_warps<kEpi>()) {
-    // ---------------- K-tail zeroing (two-CTA K-grouped contractions) ----------------
-    // Only a unit's last k-block can run past its group's end.  The even CTA's warp waits
-    // for that stage's copies of both CTAs on the tail barrier, zeroes the K rows past the
-    // end in its own A and B atoms and, through distributed shared memory, in the odd
-    // CTA's, makes the writes visible to the async proxy and completes the stage's full
-    // barrier, on which the MMA thread waits as for any stage.  A stage's tail barrier
-    // completes once per K-tail use: one parity bit per stage.
-    if (rank == 0) {
-      uint32_t stage = 0, tail_parity = 0;
-      for (int32_t i = 0; i * ustride < n_total; ++i) {
-        const int32_t t = round_unit<kKG>(i, u0, ustride);
-        if (t >= n_total) continue;
-        const TileCoord tcz = unit_tile<kPair, kKG, kTwo>(args, t, rank);
-        const int32_t kb_last = tcz.k_blocks - 1;
-        const int32_t kv = tcz.k_end - (tcz.k0 + kb_last * G::BK);
-        if (tcz.k_blocks > 0 && kv < G::BK) {
-          const uint32_t ts = (stage + static_cast<uint32_t>(kb_last)) % G::Stages;
-          int w = 1;
-          if (lane == 0)
-            w = ctl_wait<true>(ctl, &ctl->tail_full[ts], (tail_parity >> ts) & 1u, args.status)
-                    ? 1 : 0;
-          w = __shfl_sync(0xFFFFFFFFu, w, 0);
-          if (!w) break;
-          tail_parity ^= 1u << ts;
-          const uint32_t sa = smem_u32(smem + ts * G::StageBytes);
-          const uint32_t sb = sa + G::ABytes;
-          zero_k_tail<2>(sa, sb, kv, lane);
-          zero_k_tail<2, true>(map_to_rank(sa, 1), map_to_rank(sb, 1), kv, lane);
-          fence_proxy_async_cluster_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&ctl->full[ts]));
-        }
-        stage = (stage + static_cast<uint32_t>(tcz.k_blocks)) % G::Stages;
       }
     }
   } else if (kGuStage && warp == 2 + epi_warps<kEpi>()) {
@@ -1578,6 +1558,38 @@ bool make_map_gu(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
   return r == CUDA_SUCCESS;
 }
 
+// Per-group copies of two tensor maps over row-major [K rows, cols] operands (the
+// MN-major operands of a K-grouped contraction, at base_a and base_b with row pitches
+// ld_a and ld_b bytes) whose rows end at the group's end, k_offsets[g + 1]: a copy of
+// the group's last k-block then reads zeros past the group's end instead of the next
+// group's rows.  Thread g writes out[2g] (from ta) and out[2g + 1] (from tb).  The
+// device-written extent is at least kMinGroupMapRows rows (the driver encodes smaller
+// extents differently from what the replacement writes): a group ending before that
+// row gets a map of kMinGroupMapRows rows whose base lies kMinGroupMapRows - end rows
+// before the operand's, and its loads add that many rows to their row coordinate
+// (group_map_shift); they never reach below the group's first row.  A group without
+// rows keeps the templates.
+__global__ void group_maps_kernel(const __grid_constant__ CUtensorMap ta,
+                                  const __grid_constant__ CUtensorMap tb, const uint8_t* base_a,
+                                  const uint8_t* base_b, int64_t ld_a, int64_t ld_b,
+                                  const int32_t* k_offsets, int32_t groups, CUtensorMap* out) {
+  const int32_t g = static_cast<int32_t>(blockIdx.x * blockDim.x + threadIdx.x);
+  if (g >= groups) return;
+  const int32_t k0 = __ldg(k_offsets + g), k_end = __ldg(k_offsets + g + 1);
+  out[2 * g] = ta;
+  out[2 * g + 1] = tb;
+  if (k_end > k0 && k0 >= 0) {
+    const int32_t shift = group_map_shift(k_end);
+    if (shift > 0) {
+      tensormap_set_base(out + 2 * g, base_a - shift * ld_a);
+      tensormap_set_base(out + 2 * g + 1, base_b - shift * ld_b);
+    }
+    tensormap_set_rows(out + 2 * g, k_end + shift);
+    tensormap_set_rows(out + 2 * g + 1, k_end + shift);
+  }
+  fence_tensormap_release();
+}
+
 template <int kMx>
 constexpr size_t smem_bytes() {
   return Geo<kMx>::Stages * Geo<kMx>::StageBytes + sizeof(SharedCtl) + 1024;
@@ -1614,7 +1626,7 @@ int max_pair_clusters(size_t smem) {
   if (c == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(block_threads<kEpi, kMx, kMajor>(), 1, 1);
+    cfg.blockDim = dim3(block_threads<kEpi, kMx>(), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -1730,7 +1742,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     // units (pair_units), or a K-grouped contraction.
     const bool dense = !s.group_offsets && !s.tile_offsets && !s.k_group_offsets &&
                        !s.out_row_index && !s.combine_w;
-    const bool kgrouped = kMajor == Major::kABMNGrouped && s.k_group_offsets;
+    const bool kgrouped = kMajor == Major::kABMNGrouped && s.k_group_offsets && s.group_maps;
     const bool use2 = dense || kgrouped || (s.pair_units && s.unit_offsets && !s.k_group_offsets);
     int clusters2 =
         use2 ? max_pair_clusters<kEpi, kC, kStoreGu, kMajor, kMx>(
@@ -1763,14 +1775,22 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
         const int64_t units = ((m_tiles + 1) / 2) * a.n_tiles;
         if (units < clusters2) clusters2 = static_cast<int>(units);
       } else if (kgrouped) {
-        // Every group: units (p, n) over the output's m-tile pairs and n-tiles.
+        // Every group: units (p, n) over the output's m-tile pairs and n-tiles; its own
+        // A and B maps end at the group's last row.
         a.units_per_group = static_cast<int32_t>(((m_tiles + 1) / 2) * a.n_tiles);
         const int64_t units = static_cast<int64_t>(a.units_per_group) * s.num_groups;
         if (units < clusters2) clusters2 = static_cast<int>(units < 1 ? 1 : units);
+        a.group_maps = static_cast<const CUtensorMap*>(s.group_maps);
+        group_maps_kernel<<<(s.num_groups + 127) / 128, 128, 0, stream>>>(
+            ma, mb, static_cast<const uint8_t*>(s.a), static_cast<const uint8_t*>(s.b),
+            (s.a_ld > 0 ? s.a_ld : s.a_rows) * 2, (s.b_ld > 0 ? s.b_ld : s.b_rows) * 2,
+            s.k_group_offsets, s.num_groups, static_cast<CUtensorMap*>(s.group_maps));
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
       }
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * clusters2, 1, 1);
-      cfg.blockDim = dim3(block_threads<kEpi, kMx, kMajor>(), 1, 1);
+      cfg.blockDim = dim3(block_threads<kEpi, kMx>(), 1, 1);
       cfg.dynamicSmemBytes = smem_bytes_pair_epi<kEpi, kMx>();
       cfg.stream = stream;
       cudaLaunchAttribute attr;
@@ -1796,7 +1816,7 @@ cudaError_t launch(const GemmShape& s, const SituParams& p, uint32_t* status, in
     if (tiles < grid) grid = static_cast<int>(tiles);
   }
   ffn_gemm_kernel<kEpi, kC, false, kStoreGu, kMajor, kMx>
-      <<<grid, block_threads<kEpi, kMx, kMajor>(), kSmem, stream>>>(ma, ma64, mb, ma, ma64, mb, a);
+      <<<grid, block_threads<kEpi, kMx>(), kSmem, stream>>>(ma, ma64, mb, ma, ma64, mb, a);
   return cudaGetLastError();
 }
 

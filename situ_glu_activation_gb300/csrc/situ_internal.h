@@ -85,6 +85,10 @@ struct GemmShape {
   // order their units run in (largest row count first balances the CTAs).
   const int32_t* group_order;
   int64_t out_group_rows;
+  // K-grouped: device scratch for two tensor maps per group ([2 * num_groups]
+  // CUtensorMap, 128-byte aligned), written by the launch; with it the contraction runs
+  // as two-CTA MMAs (without it, one CTA per tile).
+  void* group_maps;
   // MXFP8 operands (launch_mx_gemm_*): A and B are E4M3 codes (row-major, K
   // contiguous, K a multiple of 128); sfa / sfb their E8M0 scale tiles (A: 512 bytes
   // per 128-row m-tile and 128-wide K stage; B: 1024 bytes per (group, n-tile) and K
@@ -196,6 +200,10 @@ int32_t gemm_n_tiles_wide(int64_t n_out);
 cudaError_t launch_gather_rows(const void* x, const int32_t* token_index, void* x_perm,
                                int64_t R, int32_t k_eff, int64_t M, uint32_t* status,
                                cudaStream_t stream);
+// Per-group tensor-map extents written on the device against the driver's encoding
+// (host k_offsets [groups + 1]); mismatches [2 * groups]: 1 where a map differs.
+cudaError_t group_maps_selftest(const int32_t* k_offsets, int32_t groups, int64_t rows,
+                                int64_t cols, int32_t* mismatches, cudaStream_t stream);
 // One block waiting on a barrier nothing completes, bounded by limit_ns.
 cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, uint32_t* status,
                                          cudaStream_t stream);

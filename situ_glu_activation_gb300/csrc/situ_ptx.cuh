@@ -468,6 +468,31 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) 
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Tensor maps in global memory.  Sets the extent of dimension 1 (the rows of a 2-D
+// map) of the 128-byte map at `map` (generic proxy); a TMA copy may use the map once the
+// writer has released and the user acquired it through the tensor-map proxy fences.
+__device__ __forceinline__ void tensormap_set_rows(void* map, int32_t rows) {
+  asm volatile(
+      "{\n\t.reg .u64 g;\n\tcvta.to.global.u64 g, %0;\n\t"
+      "tensormap.replace.tile.global_dim.global.b1024.b32 [g], 1, %1;\n\t}" ::"l"(map),
+      "r"(rows)
+      : "memory");
+}
+// Sets the global base address of the map at `map` (16-byte aligned; generic proxy).
+__device__ __forceinline__ void tensormap_set_base(void* map, const void* base) {
+  asm volatile(
+      "{\n\t.reg .u64 g, b;\n\tcvta.to.global.u64 g, %0;\n\tcvta.to.global.u64 b, %1;\n\t"
+      "tensormap.replace.tile.global_address.global.b1024.b64 [g], b;\n\t}" ::"l"(map),
+      "l"(base)
+      : "memory");
+}
+__device__ __forceinline__ void fence_tensormap_release() {
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+__device__ __forceinline__ void fence_tensormap_acquire(const void* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
+}
+
 // 16 zero bytes into this CTA's shared memory (generic proxy).
 __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
