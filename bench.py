@@ -552,16 +552,17 @@ def bench_mx(args, dev, peaks, world, flush, names=("grouped", "k3_decode", "k3_
     return out
 
 
-def bench_moe_train(args, dev, peaks, world, flush):
-    """Training step of the grouped experts (E=64, 16384 tokens top-8 Zipf): expert
-    index, forward that keeps gu and h in expert order, backward for a seeded
-    upstream gradient of the per-route outputs (dx, per-expert dW)."""
+def bench_moe_train(args, dev, peaks, world, flush, name="grouped"):
+    """Training step of the grouped experts (E=64, 16384 tokens top-8 Zipf; or the
+    16-expert slice for profiling): expert index, forward that keeps gu and h in
+    expert order, backward for a seeded upstream gradient of the per-route outputs
+    (dx, per-expert dW)."""
     import torch
 
     import situ_glu_activation_gb300 as situ
     from situ_glu_activation_gb300 import workloads as wl
 
-    w = wl.WORKLOADS["grouped"]
+    w = wl.WORKLOADS[name]
     E = w.num_experts
     R = w.T * w.k_eff
     wgu, wd = wl.expert_weights(E, w.M, w.I, seed=0, device=dev)
@@ -595,7 +596,7 @@ def bench_moe_train(args, dev, peaks, world, flush):
            "tflops": (flop_f + flop_b) / (ms * 1e-3) / 1e12,
            "backward_tflops": flop_b / (mean(t_bwd) * 1e-3) / 1e12,
            "tc_frac": (flop_f + flop_b) / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
-           "launches_per_step": 4 + 4 + 8}
+           "launches_per_step": 4 + 4 + 10}
     del wgu, wd, ws_f, ws_b, dy, x
     torch.cuda.empty_cache()
     return out
@@ -793,6 +794,8 @@ def run_situ(args):
             res = bench_train(args, dev, peaks, world, flush)
         elif args.suite == "grouped_train":
             res = bench_moe_train(args, dev, peaks, world, flush)
+        elif args.suite == "grouped_train_slice":
+            res = bench_moe_train(args, dev, peaks, world, flush, "grouped_slice")
         elif args.suite == "mx":
             res = bench_mx(args, dev, peaks, world, flush)
         elif args.suite == "mx_dense":
@@ -929,6 +932,7 @@ def main(argv=None):
     ap.add_argument("--suite", default="full",
                     choices=["full", "dense", "act", "grouped", "k3_decode", "k3_prefill",
                              "k3_prefill_slice", "k3_decode_slice", "train", "grouped_train",
+                             "grouped_train_slice",
                              "mx", "mx_dense"],
                     help="full: the headline line with every sub-result; dense: the headline "
                          "only; any other name: that workload alone (for profiling)")

@@ -74,6 +74,11 @@ WORKLOADS = {
     # Grouped routed experts: E=64, top-8 Zipf(1.1) with 4 empty experts.
     "grouped": Workload("grouped SiTU-GLU experts, bf16, E=64, 16384 tokens top-8 Zipf(1.1)",
                         "moe", T=16384, E=64, k=8, routing="zipf", n_empty=4),
+    # The grouped shapes at a quarter of the tokens (16 experts, one of them empty): the
+    # same per-expert GEMM shapes with about 2 GB on the device, for profiling.
+    "grouped_slice": Workload("16 routed experts, 4096 tokens top-8 Zipf(1.1) with 1 empty "
+                              "expert (the grouped shapes, for profiling)", "moe", T=4096, E=16,
+                              k=8, routing="zipf", n_empty=1),
     # Kimi-K3-shaped layer: 896 routed + 2 shared experts.
     "k3_decode": Workload("Kimi-K3-shaped MoE layer, 896 routed + 2 shared experts, 512 tokens",
                           "moe", T=512, E=896, k=8, shared=(896, 897), routing="uniform"),
