@@ -101,6 +101,13 @@ int situ_ffn_last_path(void);
  * turn it off under such a tool. */
 int situ_ffn_set_single_launch(int enable);
 
+/* Process-wide switch (on by default; returns the previous setting) for the form of
+ * situ_moe_grouped_backward's per-expert weight gradients: on, two-CTA MMAs reading each
+ * expert through tensor maps that end at its last row; off, one CTA per tile with the
+ * rows past an expert's end zeroed in shared memory (the form used where two-CTA
+ * clusters cannot be launched).  Both produce the same bits. */
+int situ_moe_set_kgrouped_two_cta(int enable);
+
 /* Device-side status of the current device: SITU_OK, or the first failure a
  * kernel recorded since the last clear (SITU_ERR_TIMEOUT, SITU_ERR_INDEX).
  * Synchronous: call it after synchronising the streams the kernels ran on.

@@ -23,6 +23,7 @@ from .api import (MX_DOWN, MX_E2M1, MX_E4M3, MX_GATE_UP, MxWeights, SituError,
                   mx_quantize_weights, mx_weight_scales_bytes, situ_ffn_forward_mxfp8,
                   situ_ffn_gate_up_mxfp8, situ_moe_grouped_forward_mxfp8, device_status, ffn_backward_workspace_bytes,
                   ffn_last_path, FFN_PATH_FUSED, FFN_PATH_TWO_LAUNCHES, ffn_set_single_launch,
+                  moe_set_kgrouped_two_cta,
                   ffn_host_workspace_bytes, ffn_workspace_bytes, moe_backward_workspace_bytes,
                   moe_workspace_bytes, selftest_bounded_wait, selftest_group_maps, set_wait_limit_ns,
                   situ_ffn_backward, situ_ffn_down,
@@ -39,6 +40,7 @@ __all__ = [
     "device_status", "selftest_bounded_wait", "selftest_group_maps", "set_wait_limit_ns", "ffn_host_workspace_bytes",
     "situ_moe_combine",
     "ffn_last_path", "FFN_PATH_FUSED", "FFN_PATH_TWO_LAUNCHES", "ffn_set_single_launch",
+    "moe_set_kgrouped_two_cta",
     "situ_ffn_forward_train", "situ_ffn_backward", "ffn_backward_workspace_bytes",
     "situ_moe_grouped_forward_train", "situ_moe_grouped_backward", "moe_backward_workspace_bytes",
     "situ_moe_grouped_forward_combined", "moe_combined_workspace_bytes",

@@ -31,6 +31,7 @@ SIGNATURES = {
     "situ_last_cuda_error": ([], ctypes.c_char_p),
     "situ_ffn_last_path": ([], _ci),
     "situ_ffn_set_single_launch": ([_ci], _ci),
+    "situ_moe_set_kgrouped_two_cta": ([_ci], _ci),
     "situ_device_status": ([_ci], _ci),
     "situ_glu_act": ([_vp, _vp, _i64, _i64, _f32, _f32, _ci, _vp], _ci),
     "situ_ffn_workspace_size": ([_i64, _i64, _i64, _ci], _sz),

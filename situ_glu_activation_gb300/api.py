@@ -641,6 +641,13 @@ def ffn_set_single_launch(enable: bool) -> bool:
     return bool(_native.lib().situ_ffn_set_single_launch(1 if enable else 0))
 
 
+def moe_set_kgrouped_two_cta(enable: bool) -> bool:
+    """Two-CTA form (per-expert tensor maps) of the grouped backward's weight gradients on
+    or off for the process (on by default; off: one CTA per tile, the form used where
+    two-CTA clusters cannot launch; same bits).  Returns the previous setting."""
+    return bool(_native.lib().situ_moe_set_kgrouped_two_cta(1 if enable else 0))
+
+
 def device_status(clear: bool = True) -> int:
     """First device-side failure recorded since the last clear (0 = SITU_OK)."""
     return int(_native.lib().situ_device_status(1 if clear else 0))
@@ -679,6 +686,7 @@ __all__ = [
     "situ_moe_grouped_forward", "ffn_workspace_bytes", "moe_workspace_bytes",
     "device_status", "selftest_bounded_wait", "selftest_group_maps", "set_wait_limit_ns", "ffn_host_workspace_bytes", "situ_moe_combine",
     "ffn_last_path", "FFN_PATH_FUSED", "FFN_PATH_TWO_LAUNCHES", "ffn_set_single_launch",
+    "moe_set_kgrouped_two_cta",
     "situ_ffn_forward_train", "situ_ffn_backward", "ffn_backward_workspace_bytes",
     "situ_moe_grouped_forward_train", "situ_moe_grouped_backward", "moe_backward_workspace_bytes",
     "situ_moe_grouped_forward_combined", "moe_combined_workspace_bytes",

@@ -39,6 +39,9 @@ std::mutex g_mutex;
 thread_local char t_last_cuda_error[256] = "";
 thread_local int t_ffn_path = 0;  // the path of this thread's last bf16 dense forward
 std::atomic<int> g_ffn_single_launch{1};
+// The grouped backward's K-grouped weight gradients on two-CTA MMAs (per-expert tensor
+// maps); off: one CTA per tile (the path taken where two-CTA clusters cannot launch).
+std::atomic<int> g_kgrouped_two_cta{1};
 
 situ_status cuda_fail(cudaError_t e) {
   std::snprintf(t_last_cuda_error, sizeof t_last_cuda_error, "%s: %s", cudaGetErrorName(e),
@@ -119,6 +122,10 @@ int situ_ffn_last_path(void) { return t_ffn_path; }
 
 int situ_ffn_set_single_launch(int enable) {
   return g_ffn_single_launch.exchange(enable ? 1 : 0);
+}
+
+int situ_moe_set_kgrouped_two_cta(int enable) {
+  return g_kgrouped_two_cta.exchange(enable ? 1 : 0);
 }
 
 situ_status situ_device_status(int clear) {
@@ -836,7 +843,8 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
   const SituParams p = make_situ_params(beta, linear_beta);
   // The dh and dx GEMMs run as two-CTA MMAs when experts average >= 128 rows (as the
   // forward); the K-grouped weight gradients always do (one CTA per tile only where
-  // two-CTA clusters cannot be launched).
+  // two-CTA clusters cannot be launched, or with situ_moe_set_kgrouped_two_cta(0)).
+  const bool kg_two_cta = g_kgrouped_two_cta.load() != 0;
   const bool two_cta = R >= kTwoCtaMinRows * static_cast<int64_t>(E) && gemm_two_cta_available();
   cudaError_t e = launch_group_tiles(expert_offsets, E, R, gemm_n_tiles_wide(I),
                                      gemm_n_tiles_wide(M), tile_offsets, units_dh, units_dx,
@@ -887,7 +895,7 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
     g.tile_offsets = tile_offsets;
     g.k_group_offsets = expert_offsets;
     g.group_order = expert_order;
-    g.group_maps = maps_dwd;
+    g.group_maps = kg_two_cta ? maps_dwd : nullptr;
     g.out_group_rows = M;
     g.n_out = I;
     g.out = dW_down;
@@ -941,7 +949,7 @@ situ_status situ_moe_grouped_backward(const void* x, const int32_t* expert_offse
     g.tile_offsets = tile_offsets;
     g.k_group_offsets = expert_offsets;
     g.group_order = expert_order;
-    g.group_maps = maps_dwg;
+    g.group_maps = kg_two_cta ? maps_dwg : nullptr;
     g.out_group_rows = 2 * I;
     g.n_out = M;
     g.out = dW_gate_up;

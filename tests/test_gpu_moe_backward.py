@@ -200,6 +200,31 @@ def test_grouped_backward_weight_gradient_k_tails(oracle, cuda_dev):
     _check(oracle, x, ids, wgu, wd, dy, got, what="weight-gradient K tails")
 
 
+@pytest.mark.parametrize("sizes,M,I", [
+    ([1, 63, 64, 65, 0, 130, 191], 128, 192),   # K tails of every kind, odd m-tile counts
+    ([5, 14, 0, 40, 700, 333], 256, 384),       # experts ending before row 32, a long one
+])
+def test_grouped_backward_weight_gradient_forms_agree(cuda_dev, sizes, M, I):
+    """The two forms of the per-expert weight gradients, two-CTA MMAs through per-expert
+    tensor maps that end at each expert's last row and one CTA per tile with the rows
+    past the end zeroed in shared memory, produce the same bits."""
+    E = len(sizes)
+    ids = torch.cat([torch.full((n,), e, dtype=torch.int32) for e, n in enumerate(sizes)])
+    ids = ids[torch.randperm(ids.numel(), generator=torch.Generator().manual_seed(61))][:, None]
+    T = ids.shape[0]
+    x = wl.normal((T, M), 1.0, seed=62)
+    wgu, wd = wl.expert_weights(E, M, I, seed=63)
+    dy = wl.normal((T, 1, M), 1.0, seed=64)
+    _, two = _train_step(x, ids, wgu, wd, dy, cuda_dev)
+    prev = situ.moe_set_kgrouped_two_cta(False)
+    try:
+        _, one = _train_step(x, ids, wgu, wd, dy, cuda_dev)
+    finally:
+        situ.moe_set_kgrouped_two_cta(prev)
+    for a, b, what in zip(two, one, ("dx", "dW_gate_up", "dW_down")):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), what
+
+
 def test_grouped_backward_no_routes(cuda_dev):
     E, M, I = 3, 64, 64
     x = torch.empty(0, M, dtype=torch.bfloat16, device=cuda_dev)
