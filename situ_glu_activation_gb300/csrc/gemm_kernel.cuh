@@ -28,12 +28,13 @@
 // (group, m-tile, n-tile) order, so the n-tiles of one m-tile run side by side and
 // share A in L2, and the m-tiles of one group follow each other and share B there; a
 // tile with at most 64 valid rows fetches only those 64 A rows.  With two-CTA MMAs
-// (dense GEMMs, large-expert grouped GEMMs, the dense MXFP8 GEMMs) a cluster of two
-// CTAs takes m-tiles 2p and 2p+1 of one n-tile as one M=256 MMA: each CTA stages its
-// own A rows and its half of B, both CTAs' copies count on the even CTA's barrier, and
-// its MMA thread issues for both.  Operands are K-major, or MN-major
-// ({64, 64} boxes) for the backward, which also has a K-grouped schedule (each group
-// contracts over its own row range; groups largest first, rounds in serpentine order).
+// (dense GEMMs, large-expert grouped GEMMs, the K-grouped weight gradients, the dense
+// MXFP8 GEMMs) a cluster of two CTAs takes m-tiles 2p and 2p+1 of one n-tile as one
+// M=256 MMA: each CTA stages its own A rows and its half of B, both CTAs' copies count
+// on the even CTA's barrier, and its MMA thread issues for both.  Operands are K-major,
+// or MN-major ({64, 64} boxes) for the backward, which also has a K-grouped schedule
+// (each group contracts over its own row range, read through tensor maps that end at
+// the group's end; groups largest first, rounds in serpentine order).
 // Two GEMMs can share one launch: the whole FFN (down tiles wait, across CTAs, for the
 // h rows of their m-tile; a cooperative launch) or two independent plain GEMMs.  Every
 // wait is bounded (ctl_wait / mbar_wait / wait_count); on a timeout the CTA records
