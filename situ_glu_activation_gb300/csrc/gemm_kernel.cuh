@@ -498,22 +498,17 @@ __device__ __forceinline__ bool ctl_wait(SharedCtl* ctl, uint64_t* bar, uint32_t
   }
 }
 
-// Zero K rows kv..63 of a stage's MN-major operand tiles (2 A atoms, and kBAtoms B
-// atoms: 4 for a one-CTA tile, 2 for a CTA's half of a two-CTA one): row k of a
-// {64 MN, 64 K} 128-byte-swizzled atom is the 128 bytes at k * 128 (the swizzle
-// permutes 16-byte pieces within a row), so the tail is one contiguous range per atom.
-// kPeer: sa and sb are the other CTA's (shared::cluster addresses).  Warp-collective.
-template <int kBAtoms, bool kPeer = false>
+// Zero K rows kv..63 of a stage's MN-major operand tiles (2 A atoms, 4 B
+// atoms): row k of a {64 MN, 64 K} 128-byte-swizzled atom is the 128 bytes at
+// k * 128 (the swizzle permutes 16-byte pieces within a row), so the tail is one
+// contiguous range per atom.  Warp-collective.
 __device__ __forceinline__ void zero_k_tail(uint32_t sa, uint32_t sb, int32_t kv, int lane) {
   const uint32_t first = static_cast<uint32_t>(kv) * 128u;
   const uint32_t n = (kMnAtomBytes - first) / 16u;
 #pragma unroll 1
-  for (int at = 0; at < 2 + kBAtoms; ++at) {
+  for (int at = 0; at < 6; ++at) {
     const uint32_t base = (at < 2 ? sa + at * kMnAtomBytes : sb + (at - 2) * kMnAtomBytes) + first;
-    for (uint32_t i = lane; i < n; i += 32) {
-      if constexpr (kPeer) st_cluster_zero16(base + 16u * i);
-      else st_shared_zero16(base + 16u * i);
-    }
+    for (uint32_t i = lane; i < n; i += 32) st_shared_zero16(base + 16u * i);
   }
 }
 
@@ -946,7 +941,7 @@ __global__ void __launch_bounds__(block_threads<kEpi, kMx>(), 1)
           if (kWarpZero) {
             const int32_t kv = tcm.k_end - (tcm.k0 + kb * G::BK);
             if (kv < G::BK) {
-              zero_k_tail<4>(sa, sb, kv, lane);
+              zero_k_tail(sa, sb, kv, lane);
               fence_proxy_async_smem();
             }
             __syncwarp();

@@ -498,22 +498,10 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
 }
 
-// The same store into another CTA's shared memory (addr: a shared::cluster address).
-__device__ __forceinline__ void st_cluster_zero16(uint32_t addr) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u)
-               : "memory");
-}
-
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy accesses (tcgen05.mma operand reads, TMA writes).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// As fence_proxy_async_smem, for this thread's writes to the shared memory of any CTA of
-// the cluster (a pair MMA then reads both CTAs' operand tiles).
-__device__ __forceinline__ void fence_proxy_async_cluster_smem() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 
 // 16 bytes from this CTA's shared memory.  Volatile, so that it stays after the
