@@ -157,6 +157,43 @@ def test_ffn_single_launch_switch(situ_lib):
     assert situ_lib.situ_ffn_set_single_launch(1) == 1
 
 
+def test_kgrouped_two_cta_switch(situ_lib):
+    """The process-wide switch for the two-CTA weight gradients of the grouped backward:
+    on by default, returns the previous setting."""
+    assert situ_lib.situ_moe_set_kgrouped_two_cta(0) == 1
+    assert situ_lib.situ_moe_set_kgrouped_two_cta(3) == 0
+    assert situ_lib.situ_moe_set_kgrouped_two_cta(1) == 1
+
+
+def test_moe_backward_workspace_holds_the_expert_maps(situ_lib):
+    """The grouped backward's workspace: four per-expert prefix arrays, two 128-byte
+    tensor maps per expert for each of the two weight-gradient GEMMs, the [R, M] rows
+    buffer and d(g, u) [R, 2I], each rounded up to 256 bytes."""
+    up = lambda n: (n + 255) // 256 * 256
+    for R, E, M, I in [(1000, 7, 64, 96), (131072, 64, 2048, 3072), (5, 898, 8, 8)]:
+        expect = 4 * up((E + 1) * 4) + 2 * up(E * 256) + up(R * M * 2) + up(R * 2 * I * 2)
+        assert situ_lib.situ_moe_backward_workspace_size(R, E, M, I, 0) == expect
+    assert situ_lib.situ_moe_backward_workspace_size(10, 0, 8, 8, 0) == 0
+
+
+def test_group_maps_selftest_argument_checks(situ_lib):
+    """situ_selftest_group_maps refuses offsets that are not non-decreasing within
+    [0, rows], bad group counts and widths, before any device work."""
+    def call(offsets, rows=64, cols=64, groups=None):
+        off = (ctypes.c_int32 * len(offsets))(*offsets)
+        g = len(offsets) - 1 if groups is None else groups
+        flags = (ctypes.c_int32 * max(2 * g, 2))()
+        return situ_lib.situ_selftest_group_maps(off, g, rows, cols, flags, None)
+    assert call([0, 5, 3]) == BAD            # decreasing
+    assert call([-1, 5]) == BAD              # negative start
+    assert call([0, 65], rows=64) == BAD     # past the rows
+    assert call([0, 5], cols=60) == BAD      # width not a multiple of 8
+    assert call([0, 5], cols=0) == BAD
+    assert call([0, 5], rows=0) == BAD
+    assert call([0, 5], groups=0) == BAD
+    assert situ_lib.situ_selftest_group_maps(None, 1, 64, 64, None, None) == BAD
+
+
 def test_size_limits(situ_lib):
     """The largest sizes: row counts and weight-row counts index the tensor maps and the
     kernels' tile arithmetic as int32, so the calls refuse 2^31 and more before touching
